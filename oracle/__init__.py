@@ -1,0 +1,308 @@
+"""CPU oracle for the batched speculative-decoding verifier (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+import this package.  The GPU library never imports, links or calls it, and the two share
+no code: the arithmetic lives in ``sv_oracle.c`` (plain C, fp64), written from the pages'
+definitions and cited there function by function.  This module only builds that file with
+gcc and marshals numpy arrays into it.
+
+Dtype codes: 0 = bf16 (passed as uint16 bit patterns), 1 = fp32, 2 = fp64.
+Status codes per request: 0 ok, 1 draft/node token outside [-1, V), 2 a row holding NaN,
++inf or no finite logit, 3 malformed tree, 4 duplicate sibling tokens (target-only trees).
+When a request has several faults the largest code is reported.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sv_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libsvoracle.so")
+_lib = None
+_lock = threading.Lock()
+
+DT_BF16, DT_FP32, DT_FP64 = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile sv_oracle.c into libsvoracle.so beside it (gcc, -O2, no fast-math)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P, I32P, F64P = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_double)
+        i32, i64, u64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_double
+        lib.svo_philox4x32_10.argtypes = [P, P, P]
+        lib.svo_philox4x32_10.restype = None
+        lib.svo_u01.argtypes = [ctypes.c_uint32]
+        lib.svo_u01.restype = f64
+        lib.svo_uniform_pair.argtypes = [u64, u64, ctypes.c_uint32, ctypes.c_uint32, F64P, F64P]
+        lib.svo_uniform_pair.restype = None
+        lib.svo_softmax_row.argtypes = [P, i32, i64, i64, f64, P]
+        lib.svo_softmax_row.restype = i32
+        lib.svo_argmax_row.argtypes = [P, i32, i64, i64, I32P]
+        lib.svo_argmax_row.restype = i32
+        lib.svo_chain_core.argtypes = [P, P, P, i32, i64, P, P, P, I32P, I32P, P, P]
+        lib.svo_chain_core.restype = i32
+        lib.svo_tree_check.argtypes = [P, P, i32, i64, i32]
+        lib.svo_tree_check.restype = i32
+        lib.svo_tree_core.argtypes = [P, P, P, P, i32, i64, i32, P, P, P, P, I32P, I32P, P]
+        lib.svo_tree_core.restype = i32
+        lib.svo_verify_greedy.argtypes = [P, i32, P, i32, i32, i64, P, i32, P, P, P]
+        lib.svo_verify_greedy.restype = i32
+        lib.svo_verify_rejection.argtypes = [P, i32, P, P, i32, i32, i64, f64, u64, u64, P, i32,
+                                             P, P, P, P, P]
+        lib.svo_verify_rejection.restype = i32
+        lib.svo_verify_tree.argtypes = [P, i32, P, P, i32, i32, i64, i32, f64, u64, u64, P, i32,
+                                        P, P, P, P, P]
+        lib.svo_verify_tree.restype = i32
+        lib.svo_grid_chain_first_token.argtypes = [P, P, P, i64, i32, P, F64P]
+        lib.svo_grid_chain_first_token.restype = i32
+        lib.svo_grid_tree_first_token.argtypes = [P, P, i32, i64, i32, P, F64P]
+        lib.svo_grid_tree_first_token.restype = i32
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _logits(logits):
+    """Accept a numpy array (uint16 = bf16 bits, float32, float64) and return (array, code)."""
+    a = np.ascontiguousarray(logits)
+    if a.dtype == np.uint16:
+        return a, DT_BF16
+    if a.dtype == np.float32:
+        return a, DT_FP32
+    if a.dtype == np.float64:
+        return a, DT_FP64
+    raise TypeError(f"unsupported logits dtype {a.dtype}")
+
+
+def _req_ids(req_ids, B):
+    if req_ids is None:
+        return np.arange(B, dtype=np.int32)
+    return _c(req_ids, np.int32)
+
+
+def _check(rc):
+    if rc != 0:
+        raise RuntimeError(f"oracle returned {rc}")
+
+
+# ---------------------------------------------------------------------------------------
+# RNG
+# ---------------------------------------------------------------------------------------
+def philox4x32_10(ctr, key):
+    """Philox4x32-10 of one 4-word counter and 2-word key -> 4 uint32 words."""
+    lib = _load()
+    c = _c(ctr, np.uint32)
+    k = _c(key, np.uint32)
+    out = np.zeros(4, np.uint32)
+    lib.svo_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def u01(x: int) -> float:
+    return _load().svo_u01(int(x))
+
+
+def uniform_pair(seed: int, offset: int, slot: int, request: int):
+    lib = _load()
+    u, v = ctypes.c_double(), ctypes.c_double()
+    lib.svo_uniform_pair(seed, offset, slot, request, ctypes.byref(u), ctypes.byref(v))
+    return u.value, v.value
+
+
+# ---------------------------------------------------------------------------------------
+# Rows
+# ---------------------------------------------------------------------------------------
+def softmax_rows(logits, T: float):
+    """p = softmax(l / T) for every row of a [rows, V] array (fp64 out); raises on bad rows."""
+    lib = _load()
+    a, dt = _logits(logits)
+    a2 = a.reshape(-1, a.shape[-1])
+    rows, V = a2.shape
+    p = np.zeros((rows, V), np.float64)
+    for r in range(rows):
+        st = lib.svo_softmax_row(_ptr(a2), dt, r, V, float(T), _ptr(p[r]))
+        if st != 0:
+            raise ValueError(f"row {r} invalid (status {st})")
+    return p.reshape(a.shape)
+
+
+def argmax_rows(logits):
+    lib = _load()
+    a, dt = _logits(logits)
+    a2 = a.reshape(-1, a.shape[-1])
+    rows, V = a2.shape
+    out = np.zeros(rows, np.int32)
+    for r in range(rows):
+        idx = ctypes.c_int32()
+        st = lib.svo_argmax_row(_ptr(a2), dt, r, V, ctypes.byref(idx))
+        if st != 0:
+            raise ValueError(f"row {r} invalid (status {st})")
+        out[r] = idx.value
+    return out.reshape(a.shape[:-1])
+
+
+# ---------------------------------------------------------------------------------------
+# Cores with explicit uniforms (used by the self-tests)
+# ---------------------------------------------------------------------------------------
+def chain_core(p, q, drafts, u, v):
+    """One request: p [(k+1), V] fp64, q [k, V] fp64 or None, drafts [k], u/v [k+1]."""
+    lib = _load()
+    p = _c(p, np.float64)
+    k1, V = p.shape
+    k = k1 - 1
+    q = None if q is None else _c(q, np.float64)
+    d = _c(drafts, np.int32)
+    u = _c(u, np.float64)
+    v = _c(v, np.float64)
+    tokens = np.zeros(k + 1, np.int32)
+    probs = np.zeros((k + 1, 3), np.float64)
+    work = np.zeros(V, np.float64)
+    alen, bnd = ctypes.c_int32(), ctypes.c_int32(0)
+    st = lib.svo_chain_core(_ptr(p), _ptr(q), _ptr(d), k, V, _ptr(u), _ptr(v), _ptr(tokens),
+                            ctypes.byref(alen), ctypes.byref(bnd), _ptr(probs), _ptr(work))
+    return dict(status=st, tokens=tokens, accept_len=alen.value, boundary=bnd.value, probs=probs)
+
+
+def tree_core(p, amax, tokens, parents, mode, coin, v, V=None):
+    lib = _load()
+    tokens = _c(tokens, np.int32)
+    parents = _c(parents, np.int32)
+    N = tokens.shape[0]
+    if p is not None:
+        p = _c(p, np.float64)
+        V = p.shape[1]
+    amax = None if amax is None else _c(amax, np.int32)
+    coin = None if coin is None else _c(coin, np.float64)
+    v = None if v is None else _c(v, np.float64)
+    ot = np.zeros(N, np.int32)
+    ai = np.zeros(N, np.int32)
+    work = np.zeros(V, np.float64)
+    alen, bnd = ctypes.c_int32(), ctypes.c_int32(0)
+    st = lib.svo_tree_core(_ptr(p), _ptr(amax), _ptr(tokens), _ptr(parents), N, V, mode,
+                           _ptr(coin), _ptr(v), _ptr(ot), _ptr(ai), ctypes.byref(alen),
+                           ctypes.byref(bnd), _ptr(work))
+    return dict(status=st, out_tokens=ot, accept_index=ai, accept_len=alen.value,
+                boundary=bnd.value)
+
+
+def tree_check(tokens, parents, V, mode):
+    lib = _load()
+    t = _c(tokens, np.int32)
+    pa = _c(parents, np.int32)
+    return lib.svo_tree_check(_ptr(t), _ptr(pa), t.shape[0], V, mode)
+
+
+def grid_chain_first_token(p0, q0, w, G: int):
+    """Integrate one chain position over a G x G (u, v) grid, drafts weighted by w."""
+    lib = _load()
+    p0 = _c(p0, np.float64)
+    V = p0.shape[0]
+    q0 = None if q0 is None else _c(q0, np.float64)
+    w = _c(w, np.float64)
+    dist = np.zeros(V, np.float64)
+    acc = ctypes.c_double()
+    _check(lib.svo_grid_chain_first_token(_ptr(p0), _ptr(q0), _ptr(w), V, G, _ptr(dist),
+                                          ctypes.byref(acc)))
+    return dist, acc.value
+
+
+def grid_tree_first_token(p0, child_tokens, G: int):
+    lib = _load()
+    p0 = _c(p0, np.float64)
+    V = p0.shape[0]
+    ct = _c(child_tokens, np.int32)
+    dist = np.zeros(V, np.float64)
+    acc = ctypes.c_double()
+    _check(lib.svo_grid_tree_first_token(_ptr(p0), _ptr(ct), ct.shape[0], V, G, _ptr(dist),
+                                         ctypes.byref(acc)))
+    return dist, acc.value
+
+
+# ---------------------------------------------------------------------------------------
+# Batched entry points (same semantics as the GPU library's C ABI)
+# ---------------------------------------------------------------------------------------
+def verify_greedy(logits, drafts, req_ids=None):
+    """logits [B, k+1, V]; drafts [B, k] int32."""
+    lib = _load()
+    a, dt = _logits(logits)
+    B, k1, V = a.shape
+    k = k1 - 1
+    d = _c(drafts, np.int32).reshape(B, k)
+    ids = _req_ids(req_ids, B)
+    n = ids.shape[0]
+    out = np.zeros((n, k + 1), np.int32)
+    alen = np.zeros(n, np.int32)
+    status = np.zeros(n, np.int32)
+    _check(lib.svo_verify_greedy(_ptr(a), dt, _ptr(d), B, k, V, _ptr(ids), n, _ptr(out),
+                                 _ptr(alen), _ptr(status)))
+    return dict(out_tokens=out, accept_len=alen, status=status)
+
+
+def verify_rejection(logits, drafts, q, T: float, seed: int, offset: int, req_ids=None):
+    """logits [B, k+1, V]; drafts [B, k]; q [B, k, V] float32 or None (one-hot drafts)."""
+    lib = _load()
+    a, dt = _logits(logits)
+    B, k1, V = a.shape
+    k = k1 - 1
+    d = _c(drafts, np.int32).reshape(B, k)
+    qq = None if q is None else _c(q, np.float32).reshape(B, k, V)
+    ids = _req_ids(req_ids, B)
+    n = ids.shape[0]
+    out = np.zeros((n, k + 1), np.int32)
+    alen = np.zeros(n, np.int32)
+    probs = np.zeros((n, k + 1, 3), np.float64)
+    bnd = np.zeros(n, np.int32)
+    status = np.zeros(n, np.int32)
+    _check(lib.svo_verify_rejection(_ptr(a), dt, _ptr(d), _ptr(qq), B, k, V, float(T), seed,
+                                    offset, _ptr(ids), n, _ptr(out), _ptr(alen), _ptr(probs),
+                                    _ptr(bnd), _ptr(status)))
+    return dict(out_tokens=out, accept_len=alen, out_probs=probs, boundary=bnd, status=status)
+
+
+def verify_tree(logits, tokens, parents, mode: int, T: float, seed: int, offset: int,
+                req_ids=None):
+    """logits [B, N, V]; tokens, parents [B, N] int32; mode 0 greedy, 1 target-only."""
+    lib = _load()
+    a, dt = _logits(logits)
+    B, N, V = a.shape
+    t = _c(tokens, np.int32).reshape(B, N)
+    pa = _c(parents, np.int32).reshape(B, N)
+    ids = _req_ids(req_ids, B)
+    n = ids.shape[0]
+    ot = np.zeros((n, N), np.int32)
+    ai = np.zeros((n, N), np.int32)
+    alen = np.zeros(n, np.int32)
+    bnd = np.zeros(n, np.int32)
+    status = np.zeros(n, np.int32)
+    _check(lib.svo_verify_tree(_ptr(a), dt, _ptr(t), _ptr(pa), B, N, V, mode, float(T), seed,
+                               offset, _ptr(ids), n, _ptr(ot), _ptr(ai), _ptr(alen), _ptr(bnd),
+                               _ptr(status)))
+    return dict(out_tokens=ot, accept_index=ai, accept_len=alen, boundary=bnd, status=status)
