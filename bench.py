@@ -1,0 +1,497 @@
+#!/usr/bin/env python
+"""Benchmark of the batched speculative-decoding verifier on GB300.
+
+One step = one verification call over one batch: the headline workload is the target-only
+(one-hot draft) chain with B=64 requests, k=7 drafts, V=128256, bf16 logits (T = 1), i.e.
+512 verified positions per step.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank verifies its own batch (weak scaling, no
+data-path collective); the host-side barrier and the max of the ranks' times are the only
+communication.  --impl reference times the CPU oracle on the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified positions/sec and HBM GB/s (fraction of GB300 peak) for verify"
+UNIT = "positions/s"
+WORKLOAD = ("b64k7 target-only chain: B=64 requests, k=7 drafts, V=128256, bf16 logits "
+            "~N(0,3^2) with one +8 peak per row, one-hot drafts (target argmax w.p. 0.7), T=1.0")
+B, K_DRAFTS, V = 64, 7, 128256
+N_SETS = 3  # rotating input sets: 3 x 131 MB > L2 (129 MB)
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "stream_kernel_b64k7_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_verify_gb300", "csrc", f)
+                  for f in ("spec_verify.cu", "sv_device.cuh", "sv_draw.cuh")]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work spent timing the oracle baseline")
+    ap.add_argument("--no-modes", action="store_true", help="skip the other verify modes")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------------------------
+# Distributed plumbing (host-side only)
+# --------------------------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend, rank=self.rank, world_size=self.world)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float, device) -> float:
+        if not self.pg:
+            return x
+        import torch
+
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def rank_offset(rank: int) -> int:
+    """Each rank draws from its own Philox counter range (offset high word = rank)."""
+    return rank << 32
+
+
+# --------------------------------------------------------------------------------------------
+# Bytes
+# --------------------------------------------------------------------------------------------
+def chain_bytes(B, k, V, esize, with_q=False):
+    logits = B * (k + 1) * V * esize
+    q = B * k * V * 4 if with_q else 0
+    return logits + q + B * k * 4 + B * (k + 1) * 4 + B * 4
+
+
+def tree_bytes(B, N, V, esize):
+    return B * N * V * esize + 2 * B * N * 4 + 2 * B * N * 4 + B * 4
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return {}
+
+
+# --------------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+# --------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            if t0 - 0.05 <= ts <= t1 + 0.05:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[4:8]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+
+
+def gpu_selector(torch, dev) -> str:
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        return uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+    except Exception:
+        return str(dev.index or 0)
+
+
+# --------------------------------------------------------------------------------------------
+# Our arm
+# --------------------------------------------------------------------------------------------
+def run_ours(args, D: Dist):
+    import numpy as np
+    import torch
+
+    import speculative_decoding_verification_verify_gb300 as sv
+    from speculative_decoding_verification_verify_gb300 import binding
+    from speculative_decoding_verification_verify_gb300 import workloads as wl
+
+    dev = torch.device("cuda", D.local_rank)
+    torch.cuda.set_device(dev)
+    D.init("nccl")
+    lib = sv.load_library()
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    off0 = rank_offset(D.rank)
+
+    # Inputs: N_SETS independent batches, resident in HBM.
+    sets = []
+    ws_bytes = sv.spec_verify_workspace_bytes(sv.MODE_REJECTION, B, K_DRAFTS, V)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for i in range(N_SETS):
+        inp = wl.chain_b64k7(dev, seed=1236 + 101 * i + 7919 * D.rank)
+        out = torch.empty((B, K_DRAFTS + 1), dtype=torch.int32, device=dev)
+        alen = torch.empty(B, dtype=torch.int32, device=dev)
+        sets.append((inp, out, alen))
+    torch.cuda.synchronize()
+
+    def call(i, offset):
+        inp, out, alen = sets[i % N_SETS]
+        return lib.spec_verify_rejection(
+            ctypes.c_void_p(inp.logits.data_ptr()), sv.BF16, ctypes.c_void_p(inp.drafts.data_ptr()),
+            None, B, K_DRAFTS, V, 1.0, inp.seed, offset, ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(alen.data_ptr()), None, ctypes.c_void_p(ws.data_ptr()), ws_bytes,
+            ctypes.c_void_p(status.data_ptr()), sh)
+
+    for w in range(args.warmup):
+        assert call(w, off0 + w) == 0
+    torch.cuda.synchronize()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(gpu_selector(torch, dev))
+    time.sleep(0.1)
+    D.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for s in range(K):
+        starts[s].record(stream)
+        rc = call(s, off0 + args.warmup + s)
+        ends[s].record(stream)
+        if rc != 0:
+            raise RuntimeError(f"spec_verify_rejection returned {rc}")
+    torch.cuda.synchronize()
+    t1 = time.time()
+    D.barrier()
+    clocks.stop()
+    total_ms = starts[0].elapsed_time(ends[-1])
+    per_launch = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    launch_ms = statistics.mean(per_launch)
+    max_total_ms = D.max(total_ms, dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during the benchmark")
+
+    positions = B * (K_DRAFTS + 1)
+    value = D.world * positions * K / (max_total_ms * 1e-3)
+    alg = chain_bytes(B, K_DRAFTS, V, 2)
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_kind = "measured" if peak else "fallback"
+    if not peak:
+        peak = 6800.0
+    achieved = alg / (launch_ms * 1e-3) / 1e9
+    traffic = None
+    try:
+        tr = json.load(open(PROFILE_TRAFFIC))
+        if tr.get("kernel_source_hash") == kernel_source_hash():
+            traffic = tr.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": D.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": max_total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "k": K_DRAFTS, "V": V, "logits": "bf16",
+                   "mode": "target-only (one-hot q)", "positions_per_step": positions,
+                   "l2": f"{N_SETS} rotating input sets of {alg / 1e6:.1f} MB each (> L2)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": alg, "kernel": "sv_stream_kernel<bf16, sample>",
+                     "launch_ms": launch_ms,
+                     "launch_ms_p10_p90": [float(np.percentile(per_launch, 10)),
+                                           float(np.percentile(per_launch, 90))]},
+        "gpu_launches": K,
+        "clocks": clocks.summary(t0, t1),
+    }
+
+    # End to end through the same C ABI with host buffers: H2D of the step's inputs from pinned
+    # memory, the call, D2H of its outputs, every step.
+    line["e2e"] = run_e2e(args, D, torch, sv, lib, sets, ws, ws_bytes, status, stream, sh, off0)
+
+    if D.rank == 0 and D.world == 1:
+        line["cpu_baseline"] = cpu_baseline(sets[0][0], args.cpu_seconds)
+    if not args.no_modes:
+        line["modes"] = other_modes(args, D, torch, sv, wl, dev, stream, peak)
+    D.close()
+    if D.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, D, torch, sv, lib, sets, ws, ws_bytes, status, stream, sh, off0):
+    steps = min(args.steps, 200)
+    host = []
+    for inp, out, alen in sets[:2]:
+        hl = torch.empty(inp.logits.shape, dtype=inp.logits.dtype, pin_memory=True)
+        hl.copy_(inp.logits)
+        hd = torch.empty(inp.drafts.shape, dtype=torch.int32, pin_memory=True)
+        hd.copy_(inp.drafts)
+        ho = torch.empty(out.shape, dtype=torch.int32, pin_memory=True)
+        ha = torch.empty(alen.shape, dtype=torch.int32, pin_memory=True)
+        host.append((hl, hd, ho, ha, inp.seed))
+    dl = torch.empty_like(sets[0][0].logits)
+    dd = torch.empty_like(sets[0][0].drafts)
+    out, alen = sets[0][1], sets[0][2]
+    h2d = dl.numel() * dl.element_size() + dd.numel() * 4
+    d2h = out.numel() * 4 + alen.numel() * 4
+
+    def step(s, offset):
+        hl, hd, ho, ha, seed = host[s % len(host)]
+        dl.copy_(hl, non_blocking=True)
+        dd.copy_(hd, non_blocking=True)
+        rc = lib.spec_verify_rejection(
+            ctypes.c_void_p(dl.data_ptr()), sv.BF16, ctypes.c_void_p(dd.data_ptr()), None, B,
+            K_DRAFTS, V, 1.0, seed, offset, ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(alen.data_ptr()), None, ctypes.c_void_p(ws.data_ptr()), ws_bytes,
+            ctypes.c_void_p(status.data_ptr()), sh)
+        ho.copy_(out, non_blocking=True)
+        ha.copy_(alen, non_blocking=True)
+        return rc
+
+    for w in range(3):
+        step(w, off0 + 10**6 + w)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    D.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for s in range(steps):
+        assert step(s, off0 + 2 * 10**6 + s) == 0
+    e1.record(stream)
+    torch.cuda.synchronize()
+    D.barrier()
+    ms = D.max(e0.elapsed_time(e1), torch.device("cuda", D.local_rank))
+    return {"value": D.world * B * (K_DRAFTS + 1) * steps / (ms * 1e-3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": ms / steps, "gpu_launches": steps,
+            "path": "pinned host -> device copy, spec_verify_rejection, device -> pinned host"}
+
+
+def cpu_baseline(inp, seconds):
+    import numpy as np
+
+    import oracle
+    from speculative_decoding_verification_verify_gb300 import workloads as wl
+
+    lg = wl.to_numpy_logits(inp.logits)
+    d = inp.drafts.cpu().numpy()
+    oracle.build()
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        b = done % B
+        oracle.verify_rejection(lg, d, None, 1.0, inp.seed, 0, req_ids=np.array([b], np.int32))
+        done += 1
+        if time.perf_counter() - t0 >= seconds and done >= 2:
+            break
+    el = time.perf_counter() - t0
+    return {"value": done * (K_DRAFTS + 1) / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} requests (8 positions each) of the b64k7 workload, one thread, "
+                      f"{el:.1f} s"}
+
+
+# --------------------------------------------------------------------------------------------
+# The other modes, timed briefly (per-launch CUDA events, L2 handled per workload)
+# --------------------------------------------------------------------------------------------
+def _time_launches(torch, stream, fn, n, flush=None):
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    for i in range(n):
+        if flush is not None:
+            flush()
+        starts[i].record(stream)
+        fn(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return statistics.median([a.elapsed_time(b) for a, b in zip(starts, ends)])
+
+
+def other_modes(args, D, torch, sv, wl, dev, stream, peak):
+    res = {}
+    n = 200
+    # Greedy on the headline workload (3 rotating sets > L2).
+    sets = [wl.chain_b64k7(dev, seed=5000 + i) for i in range(N_SETS)]
+    ms = _time_launches(torch, stream, lambda i: sv.spec_verify_greedy(
+        sets[i % N_SETS].logits, sets[i % N_SETS].drafts), n)
+    alg = chain_bytes(B, K_DRAFTS, V, 2)
+    res["greedy_b64k7"] = _mode_entry(ms, B * (K_DRAFTS + 1), alg, peak, 1)
+    del sets
+    # Tree, both modes (3 x 117 MB).
+    trees = [wl.tree_b48(dev, seed=6000 + i) for i in range(N_SETS)]
+    Bt, Nt, Vt = trees[0].shape
+    talg = tree_bytes(Bt, Nt, Vt, 2)
+    for mode, name in ((0, "tree_b48_greedy"), (1, "tree_b48_target_only")):
+        ms = _time_launches(torch, stream, lambda i: sv.spec_verify_tree(
+            trees[i % N_SETS].logits, trees[i % N_SETS].node_tokens, trees[i % N_SETS].parents,
+            mode=mode, temperature=1.0, seed=1, offset=i), n)
+        res[name] = _mode_entry(ms, Bt * Nt, talg, peak, 1)
+    del trees
+    # Standard rejection, B=1 k=3 (2.6 MB: L2 flushed before each launch).
+    inp = wl.chain_b1k3(dev)
+    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    ms = _time_launches(torch, stream, lambda i: sv.spec_verify_rejection(
+        inp.logits, inp.drafts, inp.q, temperature=inp.temperature, seed=inp.seed, offset=i),
+        n, flush=lambda: flush_buf.zero_())
+    Bq, kq, Vq = inp.shape
+    res["standard_b1k3"] = _mode_entry(ms, Bq * (kq + 1), chain_bytes(Bq, kq, Vq, 2, with_q=True),
+                                       peak, 2, note="latency-bound; L2 flushed before each launch; "
+                                       "algorithmic bytes count all of q")
+    return res
+
+
+def _mode_entry(ms, positions, alg, peak, launches, note=None):
+    gbs = alg / (ms * 1e-3) / 1e9
+    e = {"ms_per_launch_median": ms, "positions_per_s": positions / (ms * 1e-3),
+         "algorithmic_bytes": alg, "gbs": gbs, "frac_of_peak": gbs / peak,
+         "launches_per_call": launches}
+    if note:
+        e["note"] = note
+    return e
+
+
+# --------------------------------------------------------------------------------------------
+# Reference arm: the CPU oracle on the same workload
+# --------------------------------------------------------------------------------------------
+def run_reference(args, D: Dist):
+    if D.rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    from speculative_decoding_verification_verify_gb300 import workloads as wl
+
+    oracle.build()
+    inp = wl.chain_b64k7("cpu", seed=1236)
+    lg = wl.to_numpy_logits(inp.logits)
+    d = inp.drafts.numpy()
+
+    def step(s):
+        oracle.verify_rejection(lg, d, None, 1.0, inp.seed, s,
+                                req_ids=np.array([s % B], np.int32))
+
+    for w in range(args.warmup):
+        step(w)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(args.warmup + s)
+    el = time.perf_counter() - t0
+    value = (K_DRAFTS + 1) * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": D.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "k": K_DRAFTS, "V": V, "logits": "bf16",
+                   "mode": "target-only (one-hot q)",
+                   "step": "one request (8 positions) of the workload per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} requests of the b64k7 workload, one per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    del torch
+
+
+def main():
+    args = parse_args()
+    D = Dist()
+    if args.impl == "reference":
+        run_reference(args, D)
+    else:
+        run_ours(args, D)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify.so, the batched speculative-decoding verifier for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (pages: "投机解码" [Speculative decoding], rustineverything, sections
+ * 目标模型怎么一次验证 [how the target verifies in one pass] and 接受规则为什么不改变分布 [why
+ * the acceptance rule keeps the distribution]; "The speculative decoding zoo",
+ * mlinterviewnotes 06-06, DFlash section and verification-method section):
+ * the target model has produced, for each of B requests, logits for k+1 positions, where
+ * position i conditions on the prefix and the first i drafts.  With p = softmax(logits / T),
+ * drafts are accepted left to right with probability min(1, p(x) / q(x)); the first rejected
+ * position is replaced by a draw from max(0, p - q) / Z; when all k are accepted one bonus
+ * token is drawn from position k+1.  Each request therefore emits 1 to k+1 tokens, and
+ * accept_len (the accepted draft count) tells the caller how many KV entries to keep.
+ *
+ * Conventions shared by every entry point
+ *   - All array pointers are DEVICE pointers owned by the caller, contiguous, row-major.
+ *     Logits must be aligned to their element size; any further alignment is optional
+ *     (16-byte aligned rows take the vectorised path everywhere).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue
+ *     work on it; none synchronises the host, and none allocates memory.
+ *   - The return value is a host status, known when the call returns:
+ *       SPEC_VERIFY_OK, SPEC_VERIFY_EINVAL (bad argument), SPEC_VERIFY_EWORKSPACE
+ *       (workspace too small or misaligned), SPEC_VERIFY_ECUDA (a launch failed).
+ *     On a non-OK return nothing was enqueued (ECUDA: possibly part of it).
+ *   - `dev_status` (optional, may be NULL) is a device int32.  The kernels raise it with an
+ *     atomic maximum when they detect a fault in the data; they never clear it.  The caller
+ *     zeroes it and reads it after the stream completes.  Codes: SPEC_VERIFY_DEV_*.
+ *     A faulted request gets out_tokens = -1, accept_len = -1 (and accept_index = -1).
+ *   - `workspace` is device scratch of at least spec_verify_workspace_bytes(...) bytes,
+ *     256-byte aligned, ZERO-FILLED before its first use.  Every call leaves the part that
+ *     must start at zero (per-request arrival counters, kept in a fixed region at the start of
+ *     the workspace whatever the call's shape) zero again when it completes, so a workspace is
+ *     zeroed once and reused by calls of any mode and shape.  Two calls in flight at the same
+ *     time (different streams) must not share a workspace.
+ *   - Random numbers: Philox4x32-10 (Salmon et al., SC'11) with key = (seed low word, seed
+ *     high word) and counter = (slot, request, offset low word, offset high word).  Output
+ *     word 0 gives u (the accept test, or the tree coin), word 1 gives v (the draw at the stop
+ *     slot); a word x maps to (x >> 8) * 2^-24.  slot = draft position (chain) or depth (tree).
+ *     A call uses only counters whose last two words equal `offset`: advance offset by one
+ *     per call to get fresh randomness; the same (seed, offset) replays bit-exactly.
+ *   - Draws use the inverse CDF in ascending token order: the smallest y whose running sum
+ *     of the (unnormalised) weights exceeds v * Z.
+ *   - Limits: 1 <= B <= 65536, 0 <= k <= 63 (chain), 1 <= N <= 64 (tree), 1 <= V < 2^31,
+ *     and |logit| / T must stay below 2^127 (the scaled logit is formed in fp32).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Logit element types. */
+#define SPEC_VERIFY_BF16 0
+#define SPEC_VERIFY_FP32 1
+
+/* Host return codes. */
+#define SPEC_VERIFY_OK 0
+#define SPEC_VERIFY_EINVAL (-1)
+#define SPEC_VERIFY_EWORKSPACE (-2)
+#define SPEC_VERIFY_ECUDA (-3)
+
+/* Device status codes (largest wins). */
+#define SPEC_VERIFY_DEV_OK 0
+#define SPEC_VERIFY_DEV_BAD_TOKEN 1   /* a draft / node token outside [-1, V) */
+#define SPEC_VERIFY_DEV_BAD_ROW 2     /* a logit row holding NaN or +inf, or no finite value */
+#define SPEC_VERIFY_DEV_BAD_TREE 3    /* parents[0] != -1, or parents[j] outside [0, j) */
+#define SPEC_VERIFY_DEV_DUP_SIBLING 4 /* two children of one node share a token (target-only) */
+
+/* Modes for spec_verify_workspace_bytes. */
+#define SPEC_VERIFY_MODE_GREEDY 0
+#define SPEC_VERIFY_MODE_REJECTION 1
+#define SPEC_VERIFY_MODE_TREE 2
+
+/*
+ * Greedy chain verification ("The speculative decoding zoo", DFlash section: matches =
+ * draft == argmax of the previous position, correct_len = cumprod(matches).sum, bonus =
+ * argmax[correct_len]; "投机解码", subsection 贪心 [greedy]: a draft is accepted iff it equals
+ * the target argmax, and on rejection the argmax is emitted without resampling).
+ *   logits     [B][k+1][V], dtype SPEC_VERIFY_BF16 or SPEC_VERIFY_FP32
+ *   draft_ids  [B][k] int32 in [-1, V); -1 means "no draft here" and ends the chain
+ *   out_tokens [B][k+1] int32: accepted drafts, then the argmax at the stop position, then -1
+ *   accept_len [B] int32: accepted drafts (0..k); emitted tokens = accept_len + 1
+ * Argmax ties go to the lowest token index.  No temperature and no random numbers.
+ */
+int spec_verify_greedy(const void *logits, int dtype, const int32_t *draft_ids, int B, int k,
+                       int V, int32_t *out_tokens, int32_t *accept_len, void *workspace,
+                       size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Sampled chain verification: standard rejection sampling when draft_probs is given, the
+ * one-hot ("target-only") rule when it is NULL ("投机解码", subsections 采样：标准拒绝采样
+ * [standard rejection] and 默认路径：草稿当 one-hot [default: one-hot draft]; "The speculative
+ * decoding zoo", verification-method section: with a one-hot q, min(1, p/q) = p(x)).
+ *   logits      [B][k+1][V] bf16 / fp32; p = softmax(logits / temperature)
+ *   draft_ids   [B][k] int32 in [-1, V)
+ *   draft_probs [B][k][V] fp32 draft distributions q, or NULL (q = one-hot at the draft)
+ *   temperature > 0 and finite (use spec_verify_greedy for T = 0)
+ *   out_tokens  [B][k+1] int32, accept_len [B] int32 (as for greedy)
+ *   out_probs   optional [B][k+1][3] fp32 parity aid: for each position i < k with a draft,
+ *               p_i(x_i) and q_i(x_i) (1 for one-hot); at the stop position j = accept_len,
+ *               column 2 holds the normaliser Z of the distribution drawn from (the residual
+ *               mass sum max(0, p - q), or 1 for a bonus or absent-draft draw); zeros elsewhere.
+ * Accept test: u * q(x) < p(x) (so q(x) = 0 accepts iff p(x) > 0; p(x) = 0 never accepts).
+ * If the residual mass underflows to zero the draw falls back to p.
+ */
+int spec_verify_rejection(const void *logits, int dtype, const int32_t *draft_ids,
+                          const float *draft_probs, int B, int k, int V, float temperature,
+                          uint64_t seed, uint64_t offset, int32_t *out_tokens,
+                          int32_t *accept_len, float *out_probs, void *workspace,
+                          size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Tree verification ("投机解码", subsection SGLang 默认：只看目标概率，可以验证一棵树
+ * [SGLang default: target probabilities only, can verify a tree]: one coin per tree level,
+ * siblings tried in order with a running sum of their target probabilities, residual =
+ * p with the tried siblings zeroed; greedy trees follow the child equal to the argmax).
+ *   logits       [B][N][V] bf16 / fp32: row n is the target distribution for node n's children
+ *   node_tokens  [B][N] int32: token of each node; node 0 is the root (its token is ignored);
+ *                -1 marks an absent node, which is never tried
+ *   parents      [B][N] int32: parents[.][0] = -1 and 0 <= parents[.][j] < j for j >= 1;
+ *                children of a node are tried in ascending node index
+ *   mode         0 = greedy (temperature, seed, offset ignored), 1 = target-only sampling
+ *   out_tokens   [B][N] int32: tokens of the accepted nodes, then the token drawn at the stop
+ *                node (argmax in greedy mode; a bonus draw when the stop node is a leaf)
+ *   accept_index [B][N] int32: node 0, then the accepted nodes in path order, then -1
+ *   accept_len   [B] int32: accepted nodes (the root not counted)
+ * Coin test at node n: the first child c with p_n(tok_c) > 0 and coin < sum of p_n over the
+ * children tried so far (c included) is accepted.  Sibling tokens must be distinct in mode 1.
+ */
+int spec_verify_tree(const void *logits, int dtype, const int32_t *node_tokens,
+                     const int32_t *parents, int B, int N, int V, int mode, float temperature,
+                     uint64_t seed, uint64_t offset, int32_t *out_tokens, int32_t *accept_index,
+                     int32_t *accept_len, void *workspace, size_t ws_bytes, int32_t *dev_status,
+                     void *stream);
+
+/*
+ * Workspace bytes needed by one call of the given mode (SPEC_VERIFY_MODE_*) with B requests,
+ * k drafts (chain) or N nodes (tree) and vocabulary V.  A pure host function; 0 on bad input.
+ * The size does not depend on dtype or on the device.
+ */
+size_t spec_verify_workspace_bytes(int mode, int B, int k_or_N, int V);
+
+/* Static description of a status code (host or device code); never NULL. */
+const char *spec_verify_strerror(int code);
+
+/*
+ * The library's Philox4x32-10 stream, exposed so that callers and tests can reproduce the
+ * uniforms: out[((slot * n_req) + req) * 4 + w] = word w of counter (slot, req, offset_lo,
+ * offset_hi) under key (seed_lo, seed_hi), for slot < n_slot, req < n_req.  `out` is a device
+ * array of n_slot * n_req * 4 uint32.
+ */
+int spec_verify_philox(uint64_t seed, uint64_t offset, int n_slot, int n_req, uint32_t *out,
+                       void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

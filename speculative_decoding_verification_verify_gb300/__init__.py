@@ -1,0 +1,21 @@
+"""Batched speculative-decoding verifier for NVIDIA GB300 (sm_103a).
+
+The compute lives in libspecverify.so (hand-written CUDA, C ABI in include/spec_verify.h);
+`binding` marshals torch tensors into it and `workloads` builds seeded synthetic inputs.
+"""
+from .binding import (  # noqa: F401
+    BF16,
+    FP32,
+    MODE_GREEDY,
+    MODE_REJECTION,
+    MODE_TREE,
+    Result,
+    SpecVerifyError,
+    load_library,
+    spec_verify_greedy,
+    spec_verify_philox,
+    spec_verify_rejection,
+    spec_verify_strerror,
+    spec_verify_tree,
+    spec_verify_workspace_bytes,
+)

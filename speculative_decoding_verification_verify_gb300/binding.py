@@ -1,0 +1,240 @@
+"""ctypes binding of libspecverify.so with the same entry-point names as include/spec_verify.h.
+
+Argument marshalling only: tensors are checked and their device pointers handed to the C ABI
+on the current CUDA stream; every step of verification runs in the library's CUDA kernels.
+PyTorch supplies device memory (outputs, the workspace) and the stream.  There is no CPU
+fallback: if the library is not built or no GPU is present, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import NamedTuple, Optional
+
+import torch
+
+from . import _build
+
+BF16, FP32 = 0, 1
+MODE_GREEDY, MODE_REJECTION, MODE_TREE = 0, 1, 2
+OK, EINVAL, EWORKSPACE, ECUDA = 0, -1, -2, -3
+DEV_OK, DEV_BAD_TOKEN, DEV_BAD_ROW, DEV_BAD_TREE, DEV_DUP_SIBLING = 0, 1, 2, 3, 4
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load libspecverify.so (in-tree).  Raises when it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with __graft_entry__.build() (nvcc, sm_103a)")
+        lib = ctypes.CDLL(path)
+        vp, i32, u64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_float,
+                                 ctypes.c_size_t)
+        lib.spec_verify_greedy.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp, vp, sz, vp, vp]
+        lib.spec_verify_greedy.restype = i32
+        lib.spec_verify_rejection.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, u64, u64, vp,
+                                              vp, vp, vp, sz, vp, vp]
+        lib.spec_verify_rejection.restype = i32
+        lib.spec_verify_tree.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, f32, u64, u64, vp,
+                                         vp, vp, vp, sz, vp, vp]
+        lib.spec_verify_tree.restype = i32
+        lib.spec_verify_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        lib.spec_verify_workspace_bytes.restype = sz
+        lib.spec_verify_strerror.argtypes = [i32]
+        lib.spec_verify_strerror.restype = ctypes.c_char_p
+        lib.spec_verify_philox.argtypes = [u64, u64, i32, i32, vp, vp]
+        lib.spec_verify_philox.restype = i32
+        _lib = lib
+        return lib
+
+
+def spec_verify_strerror(code: int) -> str:
+    return load_library().spec_verify_strerror(int(code)).decode()
+
+
+def spec_verify_workspace_bytes(mode: int, B: int, k_or_N: int, V: int) -> int:
+    return int(load_library().spec_verify_workspace_bytes(mode, B, k_or_N, V))
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code}: {spec_verify_strerror(code)}")
+        self.code = code
+
+
+# --------------------------------------------------------------------------------------------
+# Marshalling helpers
+# --------------------------------------------------------------------------------------------
+_ws_cache: dict = {}
+
+
+def workspace_for(nbytes: int, device: torch.device, stream: torch.cuda.Stream) -> torch.Tensor:
+    """A zero-filled uint8 device buffer of at least nbytes, kept per (device, stream).
+
+    The library leaves a workspace's counters zero after each call, so one zero-fill suffices.
+    """
+    key = (device.index, stream.cuda_stream)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _logits_dtype(logits: torch.Tensor) -> int:
+    if logits.dtype == torch.bfloat16:
+        return BF16
+    if logits.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"logits must be bfloat16 or float32, got {logits.dtype}")
+
+
+def _check_dev(name: str, t: torch.Tensor, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _ws_and_status(nbytes, device, stream, workspace, dev_status):
+    if workspace is None:
+        workspace = workspace_for(nbytes, device, stream)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=device)
+    return workspace, dev_status
+
+
+class Result(NamedTuple):
+    out_tokens: torch.Tensor
+    accept_len: torch.Tensor
+    dev_status: torch.Tensor
+    accept_index: Optional[torch.Tensor] = None
+    out_probs: Optional[torch.Tensor] = None
+
+
+# --------------------------------------------------------------------------------------------
+# Entry points
+# --------------------------------------------------------------------------------------------
+def spec_verify_greedy(logits: torch.Tensor, draft_ids: torch.Tensor, *, out_tokens=None,
+                       accept_len=None, workspace=None, dev_status=None, stream=None) -> Result:
+    """logits [B, k+1, V] (bf16 / fp32), draft_ids [B, k] int32 -> Result."""
+    lib = load_library()
+    _check_dev("logits", logits)
+    B, k1, V = logits.shape
+    k = k1 - 1
+    _check_dev("draft_ids", draft_ids, torch.int32)
+    if tuple(draft_ids.shape) != (B, k):
+        raise ValueError("draft_ids must be [B, k]")
+    dev = logits.device
+    stream = stream or torch.cuda.current_stream(dev)
+    out_tokens = out_tokens if out_tokens is not None else torch.empty((B, k1), dtype=torch.int32, device=dev)
+    accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    nbytes = spec_verify_workspace_bytes(MODE_GREEDY, B, k, V)
+    workspace, dev_status = _ws_and_status(nbytes, dev, stream, workspace, dev_status)
+    rc = lib.spec_verify_greedy(_ptr(logits), _logits_dtype(logits), _ptr(draft_ids), B, k, V,
+                                _ptr(out_tokens), _ptr(accept_len), _ptr(workspace),
+                                workspace.numel(), _ptr(dev_status),
+                                ctypes.c_void_p(stream.cuda_stream))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_greedy", rc)
+    return Result(out_tokens, accept_len, dev_status)
+
+
+def spec_verify_rejection(logits: torch.Tensor, draft_ids: torch.Tensor,
+                          draft_probs: Optional[torch.Tensor] = None, *, temperature: float,
+                          seed: int, offset: int, out_tokens=None, accept_len=None,
+                          out_probs=None, want_probs: bool = False, workspace=None,
+                          dev_status=None, stream=None) -> Result:
+    """Standard rejection (draft_probs [B, k, V] fp32) or one-hot (draft_probs None)."""
+    lib = load_library()
+    _check_dev("logits", logits)
+    B, k1, V = logits.shape
+    k = k1 - 1
+    _check_dev("draft_ids", draft_ids, torch.int32)
+    if tuple(draft_ids.shape) != (B, k):
+        raise ValueError("draft_ids must be [B, k]")
+    if draft_probs is not None:
+        _check_dev("draft_probs", draft_probs, torch.float32)
+        if tuple(draft_probs.shape) != (B, k, V):
+            raise ValueError("draft_probs must be [B, k, V]")
+    dev = logits.device
+    stream = stream or torch.cuda.current_stream(dev)
+    out_tokens = out_tokens if out_tokens is not None else torch.empty((B, k1), dtype=torch.int32, device=dev)
+    accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    if out_probs is None and want_probs:
+        out_probs = torch.empty((B, k1, 3), dtype=torch.float32, device=dev)
+    nbytes = spec_verify_workspace_bytes(MODE_REJECTION, B, k, V)
+    workspace, dev_status = _ws_and_status(nbytes, dev, stream, workspace, dev_status)
+    rc = lib.spec_verify_rejection(_ptr(logits), _logits_dtype(logits), _ptr(draft_ids),
+                                   _ptr(draft_probs), B, k, V, float(temperature),
+                                   int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                   _ptr(out_tokens), _ptr(accept_len), _ptr(out_probs),
+                                   _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                   ctypes.c_void_p(stream.cuda_stream))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_rejection", rc)
+    return Result(out_tokens, accept_len, dev_status, None, out_probs)
+
+
+def spec_verify_tree(logits: torch.Tensor, node_tokens: torch.Tensor, parents: torch.Tensor, *,
+                     mode: int, temperature: float = 1.0, seed: int = 0, offset: int = 0,
+                     out_tokens=None, accept_index=None, accept_len=None, workspace=None,
+                     dev_status=None, stream=None) -> Result:
+    """logits [B, N, V]; node_tokens, parents [B, N] int32; mode 0 greedy, 1 target-only."""
+    lib = load_library()
+    _check_dev("logits", logits)
+    B, N, V = logits.shape
+    _check_dev("node_tokens", node_tokens, torch.int32)
+    _check_dev("parents", parents, torch.int32)
+    if tuple(node_tokens.shape) != (B, N) or tuple(parents.shape) != (B, N):
+        raise ValueError("node_tokens and parents must be [B, N]")
+    dev = logits.device
+    stream = stream or torch.cuda.current_stream(dev)
+    out_tokens = out_tokens if out_tokens is not None else torch.empty((B, N), dtype=torch.int32, device=dev)
+    accept_index = accept_index if accept_index is not None else torch.empty((B, N), dtype=torch.int32, device=dev)
+    accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    nbytes = spec_verify_workspace_bytes(MODE_TREE, B, N, V)
+    workspace, dev_status = _ws_and_status(nbytes, dev, stream, workspace, dev_status)
+    rc = lib.spec_verify_tree(_ptr(logits), _logits_dtype(logits), _ptr(node_tokens),
+                              _ptr(parents), B, N, V, int(mode), float(temperature),
+                              int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                              _ptr(out_tokens), _ptr(accept_index), _ptr(accept_len),
+                              _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                              ctypes.c_void_p(stream.cuda_stream))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_tree", rc)
+    return Result(out_tokens, accept_len, dev_status, accept_index)
+
+
+def spec_verify_philox(seed: int, offset: int, n_slot: int, n_req: int, out=None,
+                       device=None, stream=None) -> torch.Tensor:
+    """Raw Philox4x32-10 words [n_slot, n_req, 4] (as int32 bit patterns) for the library's
+    counter layout (slot, request, offset)."""
+    lib = load_library()
+    device = torch.device(device or "cuda")
+    stream = stream or torch.cuda.current_stream(device)
+    if out is None:
+        out = torch.empty((n_slot, n_req, 4), dtype=torch.int32, device=device)
+    rc = lib.spec_verify_philox(int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), n_slot, n_req,
+                                _ptr(out), ctypes.c_void_p(stream.cuda_stream))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_philox", rc)
+    return out

@@ -1,0 +1,280 @@
+// sv_device.cuh -- device-side building blocks of the verifier kernels (sm_103a).
+//
+// Everything here is written for the GPU path only; the CPU oracle has its own code.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sv {
+
+constexpr int NT = 256;       // threads per CTA
+constexpr int NW = NT / 32;   // warps per CTA; one (max, sum) record per warp per piece
+constexpr int MAX_RPR = 64;   // rows per request: k + 1 <= 64 (chain) or N <= 64 (tree)
+constexpr int G_MAX = 4096;   // upper bound on CTAs of the streaming kernel
+constexpr int B_MAX = 65536;  // most requests per call (size of the fixed counter region)
+constexpr int C2_MAX = 1024;  // upper bound on column chunks of the residual kernel
+constexpr int64_t E_MIN = 8192;  // fewest elements a streaming CTA is given
+constexpr float NEG_INF = -__builtin_huge_valf();
+constexpr float POS_INF = __builtin_huge_valf();
+
+// ---------------------------------------------------------------------------------------------
+// Kernel parameters (one struct, passed by value).
+// ---------------------------------------------------------------------------------------------
+struct Params {
+    const void *logits;          // [B][rpr][V]
+    const int32_t *drafts;       // chain: [B][k]
+    const float *q;              // chain: [B][k][V] draft distributions, or null (one-hot)
+    const int32_t *node_tokens;  // tree: [B][N]
+    const int32_t *parents;      // tree: [B][N]
+    int B, k, rpr, is_tree;
+    int64_t V;
+    float cs;                    // log2(e) / T: p is proportional to 2^(logit * cs)
+    uint32_t key0, key1, off0, off1;
+    int64_t total;               // B * rpr * V
+    int64_t E;                   // elements per streaming CTA
+    int G;                       // streaming CTAs
+    int mis;                     // logits base address mod 16, in elements
+    int32_t *out_tokens;         // chain [B][k+1], tree [B][N]
+    int32_t *accept_len;         // [B]
+    int32_t *accept_index;       // tree [B][N]
+    float *out_probs;            // chain [B][k+1][3] or null
+    int32_t *dev_status;         // or null
+    // workspace
+    unsigned *cnt1;              // [B] arrivals at the streaming kernel's per-request counter
+    unsigned *cnt2;              // [B] arrivals at the residual kernel's counter
+    float2 *recs;                // [(G + R - 1) * NW] per (piece, warp) records
+    float *caps;                 // [B * rpr] logit of node j's token in its parent's row
+    int4 *pend;                  // [B] residual draw pending: {row, mc bits, total bits, flag}
+    float2 *recs2;               // [B * C2 * NW] residual-kernel records
+    int C2;                      // residual-kernel column chunks per request
+    int64_t Ec2;                 // columns per residual chunk
+};
+
+// ---------------------------------------------------------------------------------------------
+// PTX helpers.
+// ---------------------------------------------------------------------------------------------
+// 16-byte streaming load through the non-coherent path, not kept in L1.
+__device__ __forceinline__ uint4 ldg_stream(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// 2^x on the SFU (approximate, flushes subnormal results to zero).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// max that returns NaN when either input is NaN.
+__device__ __forceinline__ float fmax_nan(float a, float b)
+{
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void raise_status(int32_t *st, int code)
+{
+    if (st && code) atomicMax(st, code);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Element access per dtype: VEC elements per 16-byte vector.
+// ---------------------------------------------------------------------------------------------
+template <typename T>
+struct Elt;
+
+template <>
+struct Elt<__nv_bfloat16> {
+    static constexpr int VEC = 8;
+    static __device__ __forceinline__ float load(const void *row, int64_t c)
+    {
+        return __uint_as_float((uint32_t)__ldg((const unsigned short *)row + c) << 16);
+    }
+    static __device__ __forceinline__ void unpack(const uint4 &w, float (&x)[VEC])
+    {
+        x[0] = bf_lo(w.x); x[1] = bf_hi(w.x);
+        x[2] = bf_lo(w.y); x[3] = bf_hi(w.y);
+        x[4] = bf_lo(w.z); x[5] = bf_hi(w.z);
+        x[6] = bf_lo(w.w); x[7] = bf_hi(w.w);
+    }
+    static __device__ __forceinline__ float vmax(const uint4 &w)
+    {
+        uint32_t m = bmax2_nan(bmax2_nan(w.x, w.y), bmax2_nan(w.z, w.w));
+        return fmax_nan(bf_lo(m), bf_hi(m));
+    }
+};
+
+template <>
+struct Elt<float> {
+    static constexpr int VEC = 4;
+    static __device__ __forceinline__ float load(const void *row, int64_t c)
+    {
+        return __ldg((const float *)row + c);
+    }
+    static __device__ __forceinline__ void unpack(const uint4 &w, float (&x)[VEC])
+    {
+        x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+    }
+    static __device__ __forceinline__ float vmax(const uint4 &w)
+    {
+        return fmax_nan(fmax_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
+                        fmax_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
+    }
+};
+
+// ---------------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): counter (slot, request, off0, off1),
+// key (key0, key1).  u = word 0, v = word 1, each mapped to (x >> 8) * 2^-24.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                               uint32_t k0, uint32_t k1)
+{
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi1 ^ c1 ^ k0;
+        const uint32_t n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return make_uint4(c0, c1, c2, c3);
+}
+
+__device__ __forceinline__ float u01(uint32_t x) { return (float)(x >> 8) * 5.9604644775390625e-08f; }
+
+__device__ __forceinline__ float2 uniforms(const Params &P, uint32_t slot, uint32_t req)
+{
+    const uint4 w = philox4x32_10(slot, req, P.off0, P.off1, P.key0, P.key1);
+    return make_float2(u01(w.x), u01(w.y));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Online (max, sum) records: a record (mc, s) stands for s * 2^mc in the scaled domain.  A
+// record that has seen no finite logit has s = 0 (or NaN when it saw a NaN); its reference mc
+// is never used then, so merges test s, not mc.
+// ---------------------------------------------------------------------------------------------
+constexpr float REF_NONE = -3.4028234663852886e38f;  // reference before any finite logit
+
+__device__ __forceinline__ void rec_merge(float &mc, float &s, float omc, float os)
+{
+    const float nm = fmaxf(mc, omc);
+    const float a = (s == 0.f) ? 0.f : s * ex2(mc - nm);
+    const float b = (os == 0.f) ? 0.f : os * ex2(omc - nm);
+    mc = nm;
+    s = a + b;
+}
+
+__device__ __forceinline__ void warp_rec_merge(float &mc, float &s)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float omc = __shfl_xor_sync(0xffffffffu, mc, off);
+        const float os = __shfl_xor_sync(0xffffffffu, s, off);
+        rec_merge(mc, s, omc, os);
+    }
+}
+
+// Argmax records: larger value wins, lower index on ties, NaN is sticky.
+__device__ __forceinline__ void arg_merge(float &v, int &i, float ov, int oi)
+{
+    const bool nan_a = (v != v), nan_b = (ov != ov);
+    if (nan_a || nan_b) {
+        if (!nan_a) {
+            v = ov;
+            i = oi;
+        }
+        return;
+    }
+    if (ov > v || (ov == v && oi < i)) {
+        v = ov;
+        i = oi;
+    }
+}
+
+__device__ __forceinline__ void warp_arg_merge(float &v, int &i)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+        arg_merge(v, i, ov, oi);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Geometry of the flat split.  The [B * rpr * V] logits are cut into G ranges of E elements;
+// a "piece" is the part of one row inside one CTA's range, and each piece is cut into NW
+// contiguous warp segments.  Segment boundaries inside a piece fall on 16-byte boundaries;
+// warp 0 also takes the unaligned head, warp NW-1 the unaligned tail.  Record index of
+// (CTA g, row r, warp w) = (g + r) * NW + w, which is unique and makes the records of one row
+// contiguous in index order.
+// ---------------------------------------------------------------------------------------------
+struct Seg {
+    int64_t c0, c1;  // segment columns [c0, c1)
+    int64_t b0, b1;  // its vector body [b0, b1), 16-byte aligned
+};
+
+template <int VEC>
+__device__ __forceinline__ Seg seg_of(const Params &P, int64_t g, int64_t r, int w)
+{
+    const int64_t rowf = r * P.V;
+    const int64_t f0 = max(g * P.E, rowf);
+    const int64_t f1 = min(min((g + 1) * P.E, rowf + P.V), P.total);
+    const int64_t p0 = f0 - rowf, p1 = f1 - rowf;
+    int64_t a0 = p0 + (VEC - (f0 + P.mis) % VEC) % VEC;
+    if (a0 > p1) a0 = p1;
+    int64_t a1 = p1 - (f1 + P.mis) % VEC;
+    if (a1 < a0) a1 = a0;
+    const int64_t nv = (a1 - a0) / VEC;
+    const int64_t span = (nv + NW - 1) / NW;
+    const int64_t v0 = min((int64_t)w * span, nv), v1 = min((int64_t)(w + 1) * span, nv);
+    Seg s;
+    s.b0 = a0 + v0 * VEC;
+    s.b1 = a0 + v1 * VEC;
+    s.c0 = (w == 0) ? p0 : s.b0;
+    s.c1 = (w == NW - 1) ? p1 : s.b1;
+    return s;
+}
+
+// Node relations: the chain is a path tree (node j >= 1 has parent j - 1 and token
+// drafts[j - 1]); trees read parents / node_tokens.
+__device__ __forceinline__ int node_parent(const Params &P, int b, int n)
+{
+    if (!P.is_tree) return n - 1;
+    return __ldg(P.parents + (int64_t)b * P.rpr + n);
+}
+
+__device__ __forceinline__ int node_token(const Params &P, int b, int n)
+{
+    if (!P.is_tree) return __ldg(P.drafts + (int64_t)b * P.k + (n - 1));
+    return __ldg(P.node_tokens + (int64_t)b * P.rpr + n);
+}
+
+}  // namespace sv

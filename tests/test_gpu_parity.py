@@ -1,0 +1,381 @@
+"""Parity of the CUDA verifier (through its C ABI) with the CPU oracle.
+
+Token ids and accept lengths must match exactly, except for requests the oracle flags as
+boundary draws (a decision within 1e-6 relative of its boundary), which are counted and must
+stay rare; probabilities must agree within 1e-5 relative.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_verify_gb300 as sv
+from speculative_decoding_verification_verify_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+PROB_RTOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from speculative_decoding_verification_verify_gb300 import _build
+
+    _build.build()
+    oracle.build()
+    torch.cuda.set_device(DEV)
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _req_sample(B, n, seed=0):
+    if B <= n:
+        return np.arange(B, dtype=np.int32)
+    rng = np.random.default_rng(seed)
+    idx = np.sort(rng.choice(B, size=n - 2, replace=False))
+    return np.unique(np.concatenate([[0, B - 1], idx])).astype(np.int32)
+
+
+def _compare(gpu_tokens, gpu_len, ref, ids, extra=None):
+    gt, gl = _np(gpu_tokens)[ids], _np(gpu_len)[ids]
+    flagged = ref.get("boundary", np.zeros(len(ids), np.int32)).astype(bool)
+    ok = ~flagged
+    np.testing.assert_array_equal(gl[ok], ref["accept_len"][ok])
+    np.testing.assert_array_equal(gt[ok], ref["out_tokens"][ok])
+    if extra is not None:
+        np.testing.assert_array_equal(_np(extra[0])[ids][ok], ref[extra[1]][ok])
+    assert flagged.sum() <= max(2, len(ids) // 100), f"{flagged.sum()} boundary draws"
+    return int(flagged.sum())
+
+
+def _check_probs(out_probs, ref, ids):
+    gp = _np(out_probs)[ids].astype(np.float64)
+    rp = ref["out_probs"]
+    ok = ~ref["boundary"].astype(bool)
+    for col in (0, 1, 2):
+        g, r = gp[ok][..., col], rp[ok][..., col]
+        big = np.abs(r) > 1e-30
+        rel = np.abs(g[big] - r[big]) / np.abs(r[big])
+        assert rel.size == 0 or rel.max() < PROB_RTOL, (col, rel.max())
+        assert np.all(np.abs(g[~big]) < 1e-29)
+
+
+def run_chain(inp: wl.ChainInputs, mode: str, offset=0, ids=None, want_probs=True):
+    B, k, V = inp.shape
+    ids = np.arange(B, dtype=np.int32) if ids is None else ids
+    lg = wl.to_numpy_logits(inp.logits)
+    d = _np(inp.drafts)
+    if mode == "greedy":
+        r = sv.spec_verify_greedy(inp.logits, inp.drafts)
+        ref = oracle.verify_greedy(lg, d, req_ids=ids)
+        _compare(r.out_tokens, r.accept_len, ref, ids)
+    else:
+        q = inp.q if mode == "standard" else None
+        r = sv.spec_verify_rejection(inp.logits, inp.drafts, q, temperature=inp.temperature,
+                                     seed=inp.seed, offset=offset, want_probs=want_probs)
+        ref = oracle.verify_rejection(lg, d, None if q is None else _np(q), inp.temperature,
+                                      inp.seed, offset, req_ids=ids)
+        _compare(r.out_tokens, r.accept_len, ref, ids)
+        if want_probs:
+            _check_probs(r.out_probs, ref, ids)
+    torch.cuda.synchronize()
+    st = int(_np(r.dev_status)[0])
+    assert st == int(ref["status"].max()) or len(ids) < B
+    return r, ref
+
+
+def run_tree(inp: wl.TreeInputs, mode: int, offset=0, ids=None):
+    B, N, V = inp.shape
+    ids = np.arange(B, dtype=np.int32) if ids is None else ids
+    lg = wl.to_numpy_logits(inp.logits)
+    r = sv.spec_verify_tree(inp.logits, inp.node_tokens, inp.parents, mode=mode,
+                            temperature=inp.temperature, seed=inp.seed, offset=offset)
+    ref = oracle.verify_tree(lg, _np(inp.node_tokens), _np(inp.parents), mode, inp.temperature,
+                             inp.seed, offset, req_ids=ids)
+    _compare(r.out_tokens, r.accept_len, ref, ids, extra=(r.accept_index, "accept_index"))
+    torch.cuda.synchronize()
+    return r, ref
+
+
+# --------------------------------------------------------------------------------------------
+# RNG
+# --------------------------------------------------------------------------------------------
+def test_philox_words_match_oracle():
+    for seed, offset in ((0, 0), (20261031, 5), (2**64 - 1, 2**63 + 3)):
+        words = _np(sv.spec_verify_philox(seed, offset, 9, 301)).view(np.uint32)
+        for slot in (0, 4, 8):
+            for req in (0, 1, 150, 300):
+                ref = oracle.philox4x32_10([slot, req, offset & 0xFFFFFFFF, offset >> 32],
+                                           [seed & 0xFFFFFFFF, seed >> 32])
+                assert list(words[slot, req]) == list(ref)
+
+
+# --------------------------------------------------------------------------------------------
+# Chain: the tiny fp32 workload in every mode, several offsets
+# --------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("mode", ["greedy", "standard", "onehot"])
+def test_tiny(mode):
+    inp = wl.chain_tiny(DEV)
+    for off in range(4):
+        run_chain(inp, mode, offset=off)
+
+
+@pytest.mark.parametrize("V", [20000, 20001, 4099, 131])
+@pytest.mark.parametrize("mode", ["greedy", "onehot", "standard"])
+def test_multi_tile_ragged(mode, V):
+    if mode == "standard":
+        inp = wl.chain_sweep(DEV, B=12, k=5, V=V, alpha=0.6)
+    else:
+        inp = wl.chain_b64k7(DEV, B=16, k=7, V=V, seed=99 + V)
+    for off in range(3):
+        run_chain(inp, mode, offset=off)
+
+
+@pytest.mark.parametrize("T", [0.3, 0.8, 2.5])
+def test_temperatures(T):
+    inp = wl.chain_b64k7(DEV, B=8, k=5, V=9000, seed=5, T=T)
+    run_chain(inp, "onehot")
+    inp = wl.chain_sweep(DEV, B=6, k=3, V=9000, alpha=0.5, T=T)
+    run_chain(inp, "standard")
+
+
+def test_fp32_logits_large_vocab():
+    inp = wl.chain_b64k7(DEV, B=6, k=4, V=50001, seed=8, dtype=torch.float32)
+    for mode in ("greedy", "onehot"):
+        run_chain(inp, mode)
+
+
+@pytest.mark.parametrize("shift", [1, 3, 5, 7])
+def test_unaligned_logits(shift):
+    base = wl.chain_b64k7(DEV, B=5, k=3, V=10007, seed=shift)
+    B, k, V = base.shape
+    buf = torch.empty(B * (k + 1) * V + 8, dtype=torch.bfloat16, device=DEV)
+    view = buf[shift:shift + B * (k + 1) * V].view(B, k + 1, V)
+    view.copy_(base.logits)
+    inp = wl.ChainInputs("unaligned", view, base.drafts, None, 1.0, base.seed)
+    for mode in ("greedy", "onehot"):
+        run_chain(inp, mode)
+
+
+def test_many_requests_small_vocab():
+    inp = wl.chain_b64k7(DEV, B=512, k=7, V=1024, seed=3)
+    for mode in ("greedy", "onehot"):
+        run_chain(inp, mode, offset=1)
+    inp = wl.chain_sweep(DEV, B=300, k=3, V=1000, alpha=0.35)
+    run_chain(inp, "standard")
+
+
+def test_k0_and_single_request():
+    inp = wl.chain_b64k7(DEV, B=3, k=0, V=7777, seed=4)
+    r, _ = run_chain(inp, "onehot")
+    assert (_np(r.accept_len) == 0).all()
+    run_chain(inp, "greedy")
+    inp = wl.chain_b64k7(DEV, B=1, k=2, V=300000, seed=6)
+    run_chain(inp, "onehot")
+
+
+def test_absent_drafts():
+    inp = wl.chain_b64k7(DEV, B=10, k=6, V=3001, seed=12)
+    d = inp.drafts.clone()
+    d[0, 0] = -1
+    d[1, 3:] = -1
+    d[2, 5] = -1
+    inp.drafts = d
+    for mode in ("greedy", "onehot"):
+        r, _ = run_chain(inp, mode)
+        assert _np(r.accept_len)[0] == 0
+    q_inp = wl.chain_sweep(DEV, B=10, k=6, V=3001, alpha=0.7)
+    dq = q_inp.drafts.clone()
+    dq[0, 0] = -1
+    dq[4, 2:] = -1
+    q_inp.drafts = dq
+    run_chain(q_inp, "standard")
+
+
+def test_greedy_ties_lowest_index():
+    B, k, V = 20, 4, 3000
+    g = torch.Generator(device=DEV).manual_seed(1)
+    logits = torch.randint(-3, 4, (B, k + 1, V), generator=g, device=DEV).float().to(torch.bfloat16)
+    am = torch.argmax(logits.float(), -1)
+    drafts = am[:, :k].int().contiguous()
+    inp = wl.ChainInputs("ties", logits.contiguous(), drafts, None, 1.0, 0)
+    r, _ = run_chain(inp, "greedy")
+    assert (_np(r.accept_len) == k).all()
+
+
+# --------------------------------------------------------------------------------------------
+# Full-size configurations (sampled requests for the oracle)
+# --------------------------------------------------------------------------------------------
+def test_full_b64k7_onehot():
+    inp = wl.chain_b64k7(DEV)
+    ids = _req_sample(64, 10)
+    for off in (0, 1):
+        run_chain(inp, "onehot", offset=off, ids=ids)
+    run_chain(inp, "greedy", ids=ids)
+
+
+def test_full_b1k3_standard():
+    inp = wl.chain_b1k3(DEV)
+    for off in range(3):
+        run_chain(inp, "standard", offset=off)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_full_tree(mode):
+    inp = wl.tree_b48(DEV)
+    ids = _req_sample(48, 10)
+    for off in (0, 1):
+        run_tree(inp, mode, offset=off, ids=ids)
+
+
+def test_sweep_cells_sampled():
+    for B, k, alpha in ((8, 3, 0.35), (32, 1, 0.7), (64, 7, 0.7)):
+        inp = wl.chain_sweep(DEV, B=B, k=k, alpha=alpha)
+        run_chain(inp, "standard", ids=_req_sample(B, 4))
+
+
+# --------------------------------------------------------------------------------------------
+# Trees at small sizes
+# --------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("V", [5003, 64, 40000])
+def test_tree_small(V):
+    inp = wl.tree_b48(DEV, B=20, N=8, V=V, seed=V)
+    for mode in (0, 1):
+        for off in range(3):
+            run_tree(inp, mode, offset=off)
+
+
+def test_tree_wide_and_deep():
+    for N, topk, steps in ((16, 15, 8), (32, 4, 31), (64, 8, 14)):
+        inp = wl.tree_b48(DEV, B=6, N=N, V=3001, topk=topk, steps=steps, seed=N)
+        for mode in (0, 1):
+            run_tree(inp, mode)
+
+
+def test_path_tree_equals_chain_on_gpu():
+    inp = wl.chain_b64k7(DEV, B=16, k=6, V=8000, seed=21)
+    B, k, V = inp.shape
+    tokens = torch.cat([torch.zeros((B, 1), dtype=torch.int32, device=DEV), inp.drafts], 1)
+    parents = torch.arange(-1, k, dtype=torch.int32, device=DEV).repeat(B, 1).contiguous()
+    c = sv.spec_verify_rejection(inp.logits, inp.drafts, None, temperature=1.0, seed=3, offset=2)
+    t = sv.spec_verify_tree(inp.logits, tokens.contiguous(), parents, mode=1, temperature=1.0,
+                            seed=3, offset=2)
+    assert torch.equal(c.accept_len, t.accept_len)
+    assert torch.equal(c.out_tokens, t.out_tokens)
+
+
+# --------------------------------------------------------------------------------------------
+# Faults found in the data: status word, -1 outputs, other requests unaffected
+# --------------------------------------------------------------------------------------------
+def test_device_status_codes():
+    inp = wl.chain_b64k7(DEV, B=6, k=3, V=2000, seed=30)
+    d = inp.drafts.clone()
+    d[1, 2] = 2000  # out of range
+    inp.drafts = d
+    r, ref = run_chain(inp, "onehot")
+    assert int(_np(r.dev_status)[0]) == 1 and _np(r.accept_len)[1] == -1
+    lg = inp.logits.clone()
+    lg[3, 1, 17] = float("nan")
+    inp2 = wl.ChainInputs("nan", lg, inp.drafts, None, 1.0, 3)
+    r, ref = run_chain(inp2, "onehot")
+    assert int(_np(r.dev_status)[0]) == 2
+    r, ref = run_chain(inp2, "greedy")
+    assert int(_np(r.dev_status)[0]) == 2
+    lg = inp.logits.clone()
+    lg[4, 0, :] = float("-inf")
+    inp3 = wl.ChainInputs("neginf", lg, inp.drafts, None, 1.0, 3)
+    r, ref = run_chain(inp3, "onehot")
+    assert _np(r.accept_len)[4] == -1
+
+
+def test_tree_status_codes():
+    inp = wl.tree_b48(DEV, B=5, N=6, V=1000, seed=2)
+    pa = inp.parents.clone()
+    pa[1, 3] = 4  # forward parent
+    tk = inp.node_tokens.clone()
+    tk[2, 1] = 5
+    tk[2, 2] = 5
+    pa[2, 1] = 0
+    pa[2, 2] = 0  # duplicate siblings
+    bad = wl.TreeInputs("bad", inp.logits, tk.contiguous(), pa.contiguous(), 1.0, 4)
+    r, ref = run_tree(bad, 1)
+    assert int(_np(r.dev_status)[0]) == 4
+    assert _np(r.accept_len)[1] == -1 and _np(r.accept_len)[2] == -1
+    r, ref = run_tree(bad, 0)
+    assert int(_np(r.dev_status)[0]) == 3  # duplicates are fine when greedy
+
+
+# --------------------------------------------------------------------------------------------
+# Determinism and workspace reuse
+# --------------------------------------------------------------------------------------------
+def test_replay_and_workspace_reuse():
+    a = wl.chain_b64k7(DEV, B=9, k=5, V=20000, seed=40)
+    b = wl.chain_sweep(DEV, B=4, k=2, V=7000, alpha=0.5)
+    r1 = sv.spec_verify_rejection(a.logits, a.drafts, None, temperature=1.0, seed=1, offset=9)
+    t1, l1 = r1.out_tokens.clone(), r1.accept_len.clone()
+    sv.spec_verify_rejection(b.logits, b.drafts, b.q, temperature=1.0, seed=2, offset=0)
+    sv.spec_verify_greedy(b.logits, b.drafts)
+    r2 = sv.spec_verify_rejection(a.logits, a.drafts, None, temperature=1.0, seed=1, offset=9)
+    assert torch.equal(t1, r2.out_tokens) and torch.equal(l1, r2.accept_len)
+
+
+# --------------------------------------------------------------------------------------------
+# The emitted distribution itself (the page's six-token toy, many independent requests)
+# --------------------------------------------------------------------------------------------
+def test_toy_distribution_on_gpu():
+    from scipy import stats
+
+    P = np.array([0.40, 0.25, 0.15, 0.10, 0.07, 0.03])
+    Q = np.array([0.20, 0.35, 0.05, 0.25, 0.10, 0.05])
+    B, V, calls = 50000, 6, 4
+    rng = np.random.default_rng(20261031)
+    lt = torch.from_numpy(np.log(np.stack([P, P]))[None].repeat(B, 0).astype(np.float32)).to(DEV)
+    qt = torch.from_numpy(np.broadcast_to(Q.astype(np.float32), (B, 1, V)).copy()).to(DEV)
+    first, acc = [], []
+    for c in range(calls):
+        dt = torch.from_numpy(rng.choice(V, size=(B, 1), p=Q).astype(np.int32)).to(DEV)
+        r = sv.spec_verify_rejection(lt, dt, qt, temperature=1.0, seed=7, offset=c)
+        first.append(_np(r.out_tokens)[:, 0])
+        acc.append(_np(r.accept_len) == 1)
+    first, acc = np.concatenate(first), np.concatenate(acc)
+    n = first.size
+    assert abs(acc.mean() - 0.70) < 4 * np.sqrt(0.21 / n)
+    assert stats.chisquare(np.bincount(first, minlength=V), P * n).pvalue > 1e-4
+
+
+def test_rows_with_negative_infinity():
+    # -inf logits (masked tokens) are valid as long as a finite logit remains in the row.
+    inp = wl.chain_b64k7(DEV, B=6, k=3, V=3000, seed=60)
+    lg = inp.logits.clone()
+    lg[0, 0, :2000] = float("-inf")
+    lg[1, :, ::2] = float("-inf")
+    lg[2, 1, 8:] = float("-inf")
+    lg[3, 2, :] = float("-inf")
+    lg[3, 2, 2999] = 0.0
+    inp = wl.ChainInputs("masked", lg, inp.drafts, None, 1.0, 5)
+    for mode in ("greedy", "onehot"):
+        r, ref = run_chain(inp, mode)
+        assert int(_np(r.dev_status)[0]) == 0
+
+
+def test_one_workspace_across_shapes():
+    # A caller-owned workspace, zeroed once, shared by calls of different modes and shapes.
+    ws = torch.zeros(sv.spec_verify_workspace_bytes(sv.MODE_REJECTION, 600, 7, 20000),
+                     dtype=torch.uint8, device=DEV)
+    small = wl.chain_b64k7(DEV, B=3, k=2, V=20000, seed=50)
+    big = wl.chain_b64k7(DEV, B=600, k=7, V=517, seed=51)
+    tree = wl.tree_b48(DEV, B=7, N=8, V=9000, seed=52)
+    for inp in (small, big, small, big):
+        r = sv.spec_verify_rejection(inp.logits, inp.drafts, None, temperature=1.0, seed=1,
+                                     offset=0, workspace=ws)
+        ref = oracle.verify_rejection(wl.to_numpy_logits(inp.logits), _np(inp.drafts), None, 1.0,
+                                      1, 0)
+        _compare(r.out_tokens, r.accept_len, ref, np.arange(inp.shape[0], dtype=np.int32))
+        t = sv.spec_verify_tree(tree.logits, tree.node_tokens, tree.parents, mode=1, seed=2,
+                                workspace=ws)
+        tref = oracle.verify_tree(wl.to_numpy_logits(tree.logits), _np(tree.node_tokens),
+                                  _np(tree.parents), 1, 1.0, 2, 0)
+        _compare(t.out_tokens, t.accept_len, tref, np.arange(7, dtype=np.int32))
