@@ -63,6 +63,7 @@ extern "C" {
 #define SPEC_VERIFY_EINVAL (-1)
 #define SPEC_VERIFY_EWORKSPACE (-2)
 #define SPEC_VERIFY_ECUDA (-3)
+#define SPEC_VERIFY_ETOOBIG (-4) /* problem needs more than the built-in no-alloc scratch */
 
 /* Device status codes (largest wins). */
 #define SPEC_VERIFY_DEV_OK 0
@@ -156,6 +157,31 @@ const char *spec_verify_strerror(int code);
  */
 int spec_verify_philox(uint64_t seed, uint64_t offset, int n_slot, int n_req, uint32_t *out,
                        void *stream);
+
+/*
+ * Allocation-free variant of spec_verify_rejection.  The pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory when they verify (a step running
+ * under an allocator that forbids new allocations, an engine whose device memory is owned by
+ * another framework, or a thread that must not take the driver's allocation lock), and so have
+ * no workspace to pass.  It computes exactly what spec_verify_rejection computes, with the same
+ * arguments minus the workspace, using instead a scratch array built into the library: a
+ * file-scope device array of SPEC_VERIFY_NOALLOC_SCRATCH_BYTES that every GPU loading the
+ * library holds until the process exits.
+ *   - Calls whose spec_verify_workspace_bytes(SPEC_VERIFY_MODE_REJECTION, B, k, V) exceeds
+ *     SPEC_VERIFY_NOALLOC_SCRATCH_BYTES return SPEC_VERIFY_ETOOBIG and enqueue nothing.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture on the device.
+ *   - Every call on a device shares the one array and it keeps the last call's contents; each
+ *     call clears the parts that must start at zero (on `stream`, with memsets).  Calls whose
+ *     work overlaps on the GPU (different streams, no ordering between them) race on the array.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+#define SPEC_VERIFY_NOALLOC_SCRATCH_BYTES (4u << 20)
+int spec_verify_rejection_noalloc(const void *logits, int dtype, const int32_t *draft_ids,
+                                  const float *draft_probs, int B, int k, int V,
+                                  float temperature, uint64_t seed, uint64_t offset,
+                                  int32_t *out_tokens, int32_t *accept_len, float *out_probs,
+                                  int32_t *dev_status, void *stream);
 
 #ifdef __cplusplus
 }

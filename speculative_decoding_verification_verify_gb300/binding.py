@@ -18,7 +18,8 @@ from . import _build
 
 BF16, FP32 = 0, 1
 MODE_GREEDY, MODE_REJECTION, MODE_TREE = 0, 1, 2
-OK, EINVAL, EWORKSPACE, ECUDA = 0, -1, -2, -3
+OK, EINVAL, EWORKSPACE, ECUDA, ETOOBIG = 0, -1, -2, -3, -4
+NOALLOC_SCRATCH_BYTES = 4 << 20
 DEV_OK, DEV_BAD_TOKEN, DEV_BAD_ROW, DEV_BAD_TREE, DEV_DUP_SIBLING = 0, 1, 2, 3, 4
 
 _lib = None
@@ -56,6 +57,9 @@ def load_library():
         lib.spec_verify_strerror.restype = ctypes.c_char_p
         lib.spec_verify_philox.argtypes = [u64, u64, i32, i32, vp, vp]
         lib.spec_verify_philox.restype = i32
+        lib.spec_verify_rejection_noalloc.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, u64,
+                                                      u64, vp, vp, vp, vp, vp]
+        lib.spec_verify_rejection_noalloc.restype = i32
         _lib = lib
         return lib
 
@@ -238,3 +242,31 @@ def spec_verify_philox(seed: int, offset: int, n_slot: int, n_req: int, out=None
     if rc != OK:
         raise SpecVerifyError("spec_verify_philox", rc)
     return out
+
+
+def spec_verify_rejection_noalloc(logits: torch.Tensor, draft_ids: torch.Tensor,
+                                  draft_probs: Optional[torch.Tensor] = None, *, temperature: float,
+                                  seed: int, offset: int, out_tokens: torch.Tensor,
+                                  accept_len: torch.Tensor, out_probs=None, dev_status=None,
+                                  stream=None) -> Result:
+    """spec_verify_rejection without a workspace, for callers that cannot allocate device memory
+    while they verify: the library's built-in scratch is used instead.  The caller passes every
+    output buffer (and dev_status, or None), so this wrapper allocates nothing either."""
+    lib = load_library()
+    _check_dev("logits", logits)
+    B, k1, V = logits.shape
+    k = k1 - 1
+    _check_dev("draft_ids", draft_ids, torch.int32)
+    if draft_probs is not None:
+        _check_dev("draft_probs", draft_probs, torch.float32)
+    _check_dev("out_tokens", out_tokens, torch.int32)
+    _check_dev("accept_len", accept_len, torch.int32)
+    stream = stream or torch.cuda.current_stream(logits.device)
+    rc = lib.spec_verify_rejection_noalloc(_ptr(logits), _logits_dtype(logits), _ptr(draft_ids),
+                                           _ptr(draft_probs), B, k, V, float(temperature),
+                                           int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                           _ptr(out_tokens), _ptr(accept_len), _ptr(out_probs),
+                                           _ptr(dev_status), ctypes.c_void_p(stream.cuda_stream))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_rejection_noalloc", rc)
+    return Result(out_tokens, accept_len, dev_status, None, out_probs)

@@ -1117,6 +1117,7 @@ const char *spec_verify_strerror(int code)
     case SPEC_VERIFY_EINVAL: return "invalid argument";
     case SPEC_VERIFY_EWORKSPACE: return "workspace too small or not 256-byte aligned";
     case SPEC_VERIFY_ECUDA: return "CUDA launch or device query failed";
+    case SPEC_VERIFY_ETOOBIG: return "the call needs more scratch than the built-in no-alloc buffer holds";
     case SPEC_VERIFY_DEV_BAD_TOKEN: return "device: a draft or node token outside [-1, V)";
     case SPEC_VERIFY_DEV_BAD_ROW: return "device: a logit row holds NaN or +inf, or no finite value";
     case SPEC_VERIFY_DEV_BAD_TREE: return "device: malformed tree (parents[0] != -1 or parents[j] outside [0, j))";
@@ -1226,3 +1227,67 @@ int spec_verify_philox(uint64_t seed, uint64_t offset, int n_slot, int n_req, ui
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot allocate device memory at the point where they verify: code running
+// inside a memory pool that forbids new allocations, an engine whose allocator is owned by
+// another framework, or a host thread that must not take the driver's allocation lock.  For
+// them, spec_verify_rejection_noalloc uses a scratch buffer that lives in this library's own
+// device image instead of a caller-supplied workspace.  It is a fixed-size file-scope array, so
+// every GPU that loads the library keeps SPEC_VERIFY_NOALLOC_SCRATCH_BYTES of it until the
+// process exits.
+// ---------------------------------------------------------------------------------------------
+namespace sv {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_VERIFY_NOALLOC_SCRATCH_BYTES];
+
+static std::mutex g_noalloc_mu;
+static void *g_noalloc_ptr[64];
+
+// The array's name is only a host-side stand-in; the device address is asked for once per
+// device, with that device current.
+static void *noalloc_scratch_address()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace sv
+
+extern "C" int spec_verify_rejection_noalloc(const void *logits, int dtype,
+                                             const int32_t *draft_ids, const float *draft_probs,
+                                             int B, int k, int V, float temperature,
+                                             uint64_t seed, uint64_t offset, int32_t *out_tokens,
+                                             int32_t *accept_len, float *out_probs,
+                                             int32_t *dev_status, void *stream)
+{
+    if (B < 1 || B > B_MAX || k < 0 || k + 1 > MAX_RPR || V < 1) return SPEC_VERIFY_EINVAL;
+    const size_t need = spec_verify_workspace_bytes(SPEC_VERIFY_MODE_REJECTION, B, k, V);
+    if (need == 0) return SPEC_VERIFY_EINVAL;
+    if (need > SPEC_VERIFY_NOALLOC_SCRATCH_BYTES) return SPEC_VERIFY_ETOOBIG;
+    void *scratch = noalloc_scratch_address();
+    if (!scratch) return SPEC_VERIFY_ECUDA;
+    // The scratch keeps whatever the previous call left; the arrival counters of the requests
+    // this call uses must start at zero, so clear them (a memset, no allocation).
+    const Layout L = layout(B, k + 1, V);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *base = static_cast<char *>(scratch);
+    if (cudaMemsetAsync(base + L.cnt1, 0, sizeof(unsigned) * (size_t)B, s) != cudaSuccess ||
+        cudaMemsetAsync(base + L.cnt2, 0, sizeof(unsigned) * (size_t)B, s) != cudaSuccess)
+        return SPEC_VERIFY_ECUDA;
+    return spec_verify_rejection(logits, dtype, draft_ids, draft_probs, B, k, V, temperature, seed,
+                                 offset, out_tokens, accept_len, out_probs, scratch,
+                                 SPEC_VERIFY_NOALLOC_SCRATCH_BYTES, dev_status, stream);
+}
