@@ -36,7 +36,7 @@ B, K_DRAFTS, V = 64, 7, 128256
 N_SETS = 3  # rotating input sets: 3 x 131 MB > L2 (129 MB)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "stream_kernel_b64k7_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_verify_gb300", "csrc", f)
-                  for f in ("spec_verify.cu", "sv_device.cuh", "sv_draw.cuh")]
+                  for f in ("spec_verify.cu", "sv_device.cuh", "sv_draw.cuh", "sv_stream.cuh", "sv_rescan.cuh")]
 
 
 def kernel_source_hash() -> str:

@@ -5,19 +5,20 @@
 // 接受规则为什么不改变分布; "The speculative decoding zoo", mlinterviewnotes 06-06, DFlash and
 // verification-method sections):
 //
-//   sv_stream_kernel  -- one pass over all B * rows * V logits.  The flat range is split evenly
-//                        over G persistent CTAs.  Each warp keeps a running (max, sum of
-//                        2^(l*cs - max*cs)) over its contiguous segment, skipping the tokens
-//                        that are drafts of the row (they are captured instead), or a running
-//                        argmax (greedy).  Each warp writes one record per piece.  The last CTA
-//                        to finish a request (atomic arrival counter; nothing ever waits) merges
-//                        the request's records, decides acceptance (warp-ballot first-reject
-//                        scan for chains, a walk for trees), and draws the stop token by locating
-//                        the crossing record and rescanning only that segment.
-//   sv_residual_kernel-- standard rejection only: at the rejected row j, the draw comes from
-//                        max(0, p - q); its normaliser needs the row's full softmax sum, so the
-//                        logits and q of row j are read once more, split over CTAs, with the same
-//                        last-arrival finalisation.
+//   sv_stream_kernel   -- one pass over all B * rows * V logits.  The flat range is split evenly
+//                         over G persistent CTAs.  Each warp keeps a running (max, sum of
+//                         2^(l*cs - max*cs)) over its contiguous segment, skipping the tokens
+//                         that are drafts of the row (their logits are captured instead), or a
+//                         running argmax (greedy), and writes one record per piece.
+//   sv_finalize_kernel -- one CTA per request, launched as a programmatic dependent of the
+//                         streaming kernel: it stages the request's inputs, waits for the records,
+//                         merges them per row, decides acceptance (warp-ballot first-reject scan
+//                         for chains, a walk for trees), and draws the stop token by locating the
+//                         record whose running mass crosses v * Z and rescanning only that segment.
+//   sv_residual_kernel -- standard rejection only: at the rejected row j, the draw comes from
+//                         max(0, p - q); its normaliser needs the row's full softmax sum, so the
+//                         logits and q of row j are read once more, split over CTAs; the last CTA
+//                         of a request (atomic arrival counter, nothing waits) draws.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -30,20 +31,18 @@
 #include "spec_verify.h"
 #include "sv_device.cuh"
 #include "sv_draw.cuh"
+#include "sv_stream.cuh"
+#include "sv_rescan.cuh"
 
 namespace sv {
 
-#ifndef SV_UNROLL
-#define SV_UNROLL 4
-#endif
-#ifndef SV_PIPE
-#define SV_PIPE 0
-#endif
 #ifndef SV_MINB
 #define SV_MINB 3
 #endif
-constexpr int UNROLL = SV_UNROLL;  // 16-byte vectors per lane per step
-constexpr bool PIPE = SV_PIPE;     // load step i+1 while step i is processed
+constexpr int NT_FIN = 256;    // threads of a finalising CTA
+#ifndef SV_CTAS_PER_SM
+#define SV_CTAS_PER_SM 0  // streaming CTAs per SM (0: as many as fit)
+#endif
 
 struct StreamSmem {
     int ex_col[MAX_RPR];   // sorted columns of the current row's child tokens
@@ -56,7 +55,7 @@ struct FinSmem {
     int par[MAX_RPR], tok[MAX_RPR];
     int first_child[MAX_RPR], next_sib[MAX_RPR];
     float row_mc[MAX_RPR], row_S[MAX_RPR], row_tot[MAX_RPR];
-    float node_e[MAX_RPR], node_p[MAX_RPR], qx[MAX_RPR];
+    float node_e[MAX_RPR], node_p[MAX_RPR], qx[MAX_RPR], capl[MAX_RPR];
     float u[MAX_RPR], v[MAX_RPR];
     float row_best[MAX_RPR];
     int row_arg[MAX_RPR];
@@ -74,6 +73,7 @@ struct FinSmem {
     int ex_col[MAX_RPR];
     int ex_cnt;
     DrawSmem D;
+    RescanSmem RS;
 };
 
 struct Smem {
@@ -123,170 +123,57 @@ __device__ void build_children(const Params &P, int b, int n, int *ex_col, int *
     __syncwarp();
 }
 
-// ---------------------------------------------------------------------------------------------
-// Streaming accumulators.
-// ---------------------------------------------------------------------------------------------
-struct SampleAcc {
-    float m = NEG_INF;    // running max logit
-    float mc = REF_NONE;  // m * cs once a finite logit was seen: the reference of s
-    float s = 0.f;        // sum of 2^(l*cs - mc) over non-child tokens
-};
-
-struct GreedyAcc {
-    float best = NEG_INF;
-    int idx = INT_MAX;
-};
-
-// Child-token bookkeeping of one lane: the next excluded column at or after its position.
-struct ExCursor {
-    const int *col;
-    const int *node;
-    int cnt, ptr;
-    int64_t next;
-    float *caps;  // capture base of the request
-    __device__ __forceinline__ void init(const int *c, const int *nd, int n, float *cp)
-    {
-        col = c;
-        node = nd;
-        cnt = n;
-        ptr = 0;
-        caps = cp;
-        next = n > 0 ? (int64_t)c[0] : INT64_MAX;
-    }
-    __device__ __forceinline__ void advance()
-    {
-        ++ptr;
-        next = ptr < cnt ? (int64_t)col[ptr] : INT64_MAX;
-    }
-};
-
-template <int N>
-__device__ __forceinline__ void sample_update(SampleAcc &a, float vmax, float cs)
+// The same child list, built by the finalising CTA from the structure it staged in shared memory.
+__device__ void children_from_smem(FinSmem &F, int n, int rpr, int64_t V, int *ex_node, int lane)
 {
-    if (vmax > a.m) {
-        const float mcn = vmax * cs;
-        a.s *= ex2(a.mc - mcn);
-        a.m = vmax;
-        a.mc = mcn;
+    int cnt = 0;
+    for (int base = n + 1; base < rpr; base += 32) {
+        const int ch = base + lane;
+        const bool ok = ch < rpr && F.par[ch] == n && F.tok[ch] >= 0 && (int64_t)F.tok[ch] < V;
+        const unsigned m = __ballot_sync(0xffffffffu, ok);
+        if (ok) {
+            const int pos = cnt + __popc(m & ((1u << lane) - 1u));
+            F.ex_col[pos] = F.tok[ch];
+            ex_node[pos] = ch;
+        }
+        cnt += __popc(m);
     }
-}
-
-template <int N>
-__device__ __forceinline__ void sample_accumulate(SampleAcc &a, const float (&x)[N], int64_t col,
-                                                  float cs, ExCursor &ex)
-{
-    float e[N];
-#pragma unroll
-    for (int j = 0; j < N; ++j) e[j] = ex2(fmaf(x[j], cs, -a.mc));
-    if (ex.next < col + N) {
-        while (ex.next < col + N) {
-            if (ex.next >= col) {
-                float xv = 0.f;
-#pragma unroll
-                for (int j = 0; j < N; ++j) {
-                    if (col + j == ex.next) {
-                        e[j] = 0.f;
-                        xv = x[j];
-                    }
-                }
-                ex.caps[ex.node[ex.ptr]] = xv;
+    __syncwarp();
+    if (lane == 0) {
+        for (int i = 1; i < cnt; ++i) {
+            const int c = F.ex_col[i], nd = ex_node[i];
+            int j = i - 1;
+            while (j >= 0 && F.ex_col[j] > c) {
+                F.ex_col[j + 1] = F.ex_col[j];
+                ex_node[j + 1] = ex_node[j];
+                --j;
             }
-            ex.advance();
+            F.ex_col[j + 1] = c;
+            ex_node[j + 1] = nd;
         }
+        F.ex_cnt = cnt;
     }
-    // Pairwise sum keeps the adds independent.
-#pragma unroll
-    for (int w = 1; w < N; w <<= 1)
-#pragma unroll
-        for (int j = 0; j + w < N; j += 2 * w) e[j] += e[j + w];
-    a.s += e[0];
+    __syncwarp();
 }
 
-template <int N>
-__device__ __forceinline__ void greedy_accumulate(GreedyAcc &a, float vmax, const float (&x)[N],
-                                                  int64_t col)
-{
-    if (vmax > a.best || vmax != vmax) {
-        if (vmax != vmax) {
-            a.best = vmax;
-            a.idx = (int)col;
-        } else if (!(a.best != a.best)) {
-            int jf = N - 1;
-#pragma unroll
-            for (int j = N - 1; j >= 0; --j)
-                if (x[j] == vmax) jf = j;
-            a.best = vmax;
-            a.idx = (int)col + jf;
-        }
-    }
-}
-
-// One warp streams its segment [c0, c1) of a row: unaligned head, 16-byte vector body,
-// unaligned tail, each lane in ascending column order.
+// ---------------------------------------------------------------------------------------------
+// One warp streams its segment [c0, c1) of a row: the unaligned head and tail element by element,
+// the 16-byte aligned body with vector loads.  Each lane visits its columns in ascending order.
+// ---------------------------------------------------------------------------------------------
 template <typename T, bool SAMPLE>
-__device__ __forceinline__ void stream_segment(const void *row, const Seg &sg, int lane, float cs,
+__device__ __forceinline__ void stream_segment(const T *row, const Seg &sg, int lane, float cs,
                                                ExCursor &ex, SampleAcc &sa, GreedyAcc &ga)
 {
-    constexpr int VEC = Elt<T>::VEC;
-    for (int64_t c = sg.c0 + lane; c < sg.b0; c += 32) {
-        float x[1] = {Elt<T>::load(row, c)};
-        if (SAMPLE) {
-            sample_update<1>(sa, x[0], cs);
-            sample_accumulate<1>(sa, x, c, cs, ex);
-        } else {
-            greedy_accumulate<1>(ga, x[0], x, c);
-        }
+    for (int c = (int)sg.c0 + lane; c < (int)sg.b0; c += 32) {
+        const float x = Elt<T>::load(row, c);
+        if (SAMPLE) sample_scalar(sa, x, c, cs, ex);
+        else greedy_scalar(ga, x, c);
     }
-    const uint4 *vp = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(row) + sg.b0);
-    const int64_t nv = (sg.b1 - sg.b0) / VEC;
-    auto process = [&](const uint4 &w, int64_t vi) {
-        float x[VEC];
-        Elt<T>::unpack(w, x);
-        const float vm = Elt<T>::vmax(w);
-        const int64_t col = sg.b0 + vi * VEC;
-        if (SAMPLE) {
-            sample_update<VEC>(sa, vm, cs);
-            sample_accumulate<VEC>(sa, x, col, cs, ex);
-        } else {
-            greedy_accumulate<VEC>(ga, vm, x, col);
-        }
-    };
-    if (PIPE) {
-        uint4 cur[UNROLL], nxt[UNROLL];
-        int64_t i = lane;
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u)
-            if (i + 32 * u < nv) cur[u] = ldg_stream(vp + i + 32 * u);
-        for (; i < nv; i += 32 * UNROLL) {
-            const int64_t in = i + 32 * UNROLL;
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u)
-                if (in + 32 * u < nv) nxt[u] = ldg_stream(vp + in + 32 * u);
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u)
-                if (i + 32 * u < nv) process(cur[u], i + 32 * u);
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u) cur[u] = nxt[u];
-        }
-    } else {
-        int64_t i = lane;
-        for (; i + 32 * (UNROLL - 1) < nv; i += 32 * UNROLL) {
-            uint4 w[UNROLL];
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u) w[u] = ldg_stream(vp + i + 32 * u);
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u) process(w[u], i + 32 * u);
-        }
-        for (; i < nv; i += 32) process(ldg_stream(vp + i), i);
-    }
-    for (int64_t c = sg.b1 + lane; c < sg.c1; c += 32) {
-        float x[1] = {Elt<T>::load(row, c)};
-        if (SAMPLE) {
-            sample_update<1>(sa, x[0], cs);
-            sample_accumulate<1>(sa, x, c, cs, ex);
-        } else {
-            greedy_accumulate<1>(ga, x[0], x, c);
-        }
+    stream_body<T, SAMPLE>(row, (int)sg.b0, (int)sg.b1, lane, cs, ex, sa, ga);
+    for (int c = (int)sg.b1 + lane; c < (int)sg.c1; c += 32) {
+        const float x = Elt<T>::load(row, c);
+        if (SAMPLE) sample_scalar(sa, x, c, cs, ex);
+        else greedy_scalar(ga, x, c);
     }
 }
 
@@ -355,26 +242,57 @@ __device__ __forceinline__ void draw_init(DrawSmem &D, float cum)
 // ---------------------------------------------------------------------------------------------
 // Finalisation of request b by the last CTA to finish it.
 // ---------------------------------------------------------------------------------------------
-template <typename T, bool SAMPLE>
+extern __shared__ __align__(16) unsigned char sv_dyn_smem[];
+
+template <typename T, bool SAMPLE, int NTF>
 __device__ void finalize_request(const Params &P, int b, Smem &sm)
 {
     FinSmem &F = sm.fin;
+    constexpr int NWF = NTF / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rpr = P.rpr;
     const int64_t V = P.V;
     const int64_t rbase = (int64_t)b * rpr;
 
-    // Stage the request's structure: parents and tokens (node 0 has neither).
-    for (int n = tid; n < rpr; n += NT) {
+    // Prologue on inputs only (may overlap the streaming kernel): structure, q(x), uniforms.
+    for (int n = tid; n < rpr; n += NTF) {
         F.par[n] = n == 0 ? (P.is_tree ? __ldg(P.parents + rbase) : -1) : node_parent(P, b, n);
         F.tok[n] = n == 0 ? -1 : node_token(P, b, n);
-        F.qx[n] = 1.f;
+        float qv = 1.f;
+        if (SAMPLE && P.q && n >= 1 && n <= P.k) {
+            const int x = F.tok[n];
+            if (x >= 0 && (int64_t)x < V) qv = __ldg(P.q + ((int64_t)b * P.k + (n - 1)) * V + x);
+        }
+        F.qx[n] = qv;
+        if (SAMPLE) {
+            const float2 uv = uniforms(P, (uint32_t)n, (uint32_t)b);
+            F.u[n] = uv.x;
+            F.v[n] = uv.y;
+        }
     }
     if (tid == 0) F.status = 0;
     __syncthreads();
 
-    // Per-row merge of the warp records: one warp per row.
-    for (int i = warp; i < rpr; i += NW) {
+    // Window of record indices covering all rows of the request (contiguous, possibly with unused
+    // slots); small enough windows are kept in shared memory for the draw's locate step.
+    const int64_t win0 = (rbase * V / P.E + rbase) * NW;
+    const int64_t win1 = (((rbase + rpr) * V - 1) / P.E + rbase + rpr - 1) * NW + NW;
+    float2 *recs_s = reinterpret_cast<float2 *>(sv_dyn_smem);
+    const bool keep = SAMPLE && (win1 - win0) * (int64_t)sizeof(float2) <= (int64_t)RESCAN_SMEM_BYTES;
+
+    // From here on the streaming kernel's records and captures are read.
+    pdl_wait();
+    // Captured logits of each node's token in its parent's row, and the per-row merge of the
+    // warp records (one warp per row); all these loads are in flight together.
+    for (int n = tid; n < rpr; n += NTF) {
+        float l = NEG_INF;
+        if (SAMPLE && n >= 1) {
+            const int pa = F.par[n], tk = F.tok[n];
+            if (pa >= 0 && pa < n && tk >= 0 && (int64_t)tk < V) l = __ldcg(P.caps + rbase + n);
+        }
+        F.capl[n] = l;
+    }
+    for (int i = warp; i < rpr; i += NWF) {
         const int64_t r = rbase + i;
         const int64_t rowf = r * V;
         const int64_t g_lo = rowf / P.E, g_hi = (rowf + V - 1) / P.E;
@@ -384,6 +302,7 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
             float mc = REF_NONE, s = 0.f;
             for (int t = lane; t < L; t += 32) {
                 const float2 rec = __ldcg(P.recs + base + t);
+                if (keep) recs_s[base + t - win0] = rec;
                 rec_merge(mc, s, rec.x, rec.y);
             }
             warp_rec_merge(mc, s);
@@ -405,27 +324,12 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
             }
         }
     }
-    // Draft probabilities at the drafts (standard rejection).
-    if (SAMPLE && P.q) {
-        for (int i = tid; i < P.k; i += NT) {
-            const int x = F.tok[i + 1];
-            if (x >= 0 && (int64_t)x < V) F.qx[i + 1] = __ldg(P.q + ((int64_t)b * P.k + i) * V + x);
-        }
-    }
-    // Uniforms of every slot.
-    if (SAMPLE) {
-        for (int s = tid; s < rpr; s += NT) {
-            const float2 uv = uniforms(P, (uint32_t)s, (uint32_t)b);
-            F.u[s] = uv.x;
-            F.v[s] = uv.y;
-        }
-    }
     __syncthreads();
 
     // Validation; the largest fault code of the request wins.
     {
         int st = 0;
-        for (int n = tid; n < rpr; n += NT) {
+        for (int n = tid; n < rpr; n += NTF) {
             if (n >= 1) {
                 const int tk = F.tok[n];
                 if (tk < -1 || (int64_t)tk >= V) st = max(st, SPEC_VERIFY_DEV_BAD_TOKEN);
@@ -449,7 +353,7 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
         if (st) atomicMax(&F.status, st);
     }
     // Children lists (ascending node index) and, when sampling, each child's probability.
-    for (int n = tid; n < rpr; n += NT) {
+    for (int n = tid; n < rpr; n += NTF) {
         int fc = -1, ns = -1;
         for (int m = n + 1; m < rpr; ++m) {
             if (fc < 0 && F.par[m] == n && F.tok[m] >= 0) fc = m;
@@ -467,23 +371,20 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
         if (SAMPLE && n >= 1) {
             const int pa = F.par[n], tk = F.tok[n];
             float e = 0.f;
-            if (pa >= 0 && pa < n && tk >= 0 && (int64_t)tk < V) {
-                const float l = __ldcg(P.caps + rbase + n);
-                e = ex2(fmaf(l, P.cs, -F.row_mc[pa]));
-            }
+            if (pa >= 0 && pa < n && tk >= 0 && (int64_t)tk < V) e = ex2(fmaf(F.capl[n], P.cs, -F.row_mc[pa]));
             F.node_e[n] = e;
         }
     }
     __syncthreads();
     if (SAMPLE) {
-        for (int n = tid; n < rpr; n += NT) {
+        for (int n = tid; n < rpr; n += NTF) {
             float extra = 0.f;
             for (int m = n + 1; m < rpr; ++m)
                 if (F.par[m] == n && F.tok[m] >= 0 && (int64_t)F.tok[m] < V) extra += F.node_e[m];
             F.row_tot[n] = F.row_S[n] + extra;
         }
         __syncthreads();
-        for (int n = 1 + tid; n < rpr; n += NT) {
+        for (int n = 1 + tid; n < rpr; n += NTF) {
             const int pa = F.par[n];
             F.node_p[n] = (pa >= 0 && pa < n) ? F.node_e[n] / F.row_tot[pa] : 0.f;
         }
@@ -570,7 +471,7 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
         const int64_t r = rbase + n;
         const float mc_r = F.row_mc[n];
         const float vdraw = F.v[P.is_tree ? F.L : n];
-        if (warp == 0) build_children(P, b, n, F.ex_col, sm.st.ex_node, &F.ex_cnt, lane);
+        if (warp == 0) children_from_smem(F, n, rpr, V, sm.st.ex_node, lane);
         __syncthreads();
         if (F.row_S[n] > 0.f) {
             const float t = vdraw * F.row_S[n];
@@ -586,7 +487,7 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
                     const int ti = c + lane;
                     float m = 0.f;
                     if (ti < L) {
-                        const float2 rec = __ldcg(P.recs + base + ti);
+                        const float2 rec = keep ? recs_s[base + ti - win0] : __ldcg(P.recs + base + ti);
                         m = (rec.y == 0.f) ? 0.f : rec.y * ex2(rec.x - mc_r);
                     }
                     const float incl = warp_incl_scan(m, lane);
@@ -626,16 +527,9 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
                 const int w = rec % NW;
                 const Seg sg = seg_of<Elt<T>::VEC>(P, g, r, w);
                 const float tt = F.take_last ? POS_INF : t;
-                const void *row = reinterpret_cast<const T *>(P.logits) + r * V;
-                draw_init(F.D, F.cum_before);
-                ScalarSrc<T> head{row, sg.c0, P.cs, mc_r, F.ex_col, F.ex_cnt};
-                draw_span<1>(head, sg.b0 - sg.c0, tt, F.D);
-                VecSrc<T> body{reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(row) + sg.b0),
-                               sg.b0, P.cs, mc_r, F.ex_col, F.ex_cnt};
-                draw_span<4>(body, (sg.b1 - sg.b0) / Elt<T>::VEC, tt, F.D);
-                ScalarSrc<T> tail{row, sg.b1, P.cs, mc_r, F.ex_col, F.ex_cnt};
-                draw_span<1>(tail, sg.c1 - sg.b1, tt, F.D);
-                drawn = F.D.found >= 0 ? F.D.found : F.D.lastpos;
+                const T *row = reinterpret_cast<const T *>(P.logits) + r * V;
+                drawn = rescan_segment<T, NTF>(row, sg, P.cs, mc_r, tt, F.cum_before, F.ex_col, F.ex_cnt,
+                                               sv_dyn_smem, F.RS);
             }
         } else {
             // Every non-child token underflowed: draw among the children, by p, in column order.
@@ -669,7 +563,7 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
     const int out_w = P.is_tree ? rpr : P.k + 1;
     int32_t *ot = P.out_tokens + (int64_t)b * out_w;
     if (faulted) {
-        for (int i = tid; i < out_w; i += NT) {
+        for (int i = tid; i < out_w; i += NTF) {
             ot[i] = -1;
             if (P.is_tree) P.accept_index[(int64_t)b * rpr + i] = -1;
         }
@@ -678,11 +572,11 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
             raise_status(P.dev_status, F.status);
         }
         if (SAMPLE && P.out_probs && !P.is_tree)
-            for (int i = tid; i < (P.k + 1) * 3; i += NT) P.out_probs[(int64_t)b * (P.k + 1) * 3 + i] = 0.f;
+            for (int i = tid; i < (P.k + 1) * 3; i += NTF) P.out_probs[(int64_t)b * (P.k + 1) * 3 + i] = 0.f;
         if (SAMPLE && P.q && !P.is_tree && tid == 0) P.pend[b] = make_int4(-1, 0, 0, 0);
     } else {
         const int L = F.L;
-        for (int i = tid; i < out_w; i += NT) {
+        for (int i = tid; i < out_w; i += NTF) {
             int v = -1;
             if (i < L) v = F.tok[F.path[i]];
             else if (i == L) v = F.last_tok;
@@ -702,7 +596,7 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
         }
         if (SAMPLE && P.out_probs && !P.is_tree) {
             float *op = P.out_probs + (int64_t)b * (P.k + 1) * 3;
-            for (int i = tid; i <= P.k; i += NT) {
+            for (int i = tid; i <= P.k; i += NTF) {
                 float p0 = 0.f, q0 = 0.f, z = 0.f;
                 if (i < P.k && F.tok[i + 1] >= 0) {
                     p0 = F.node_p[i + 1];
@@ -715,21 +609,21 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
             }
         }
     }
-    if (tid == 0) P.cnt1[b] = 0u;  // ready for the next call
 }
 
 // ---------------------------------------------------------------------------------------------
-// The streaming kernel.
+// The streaming kernel: every CTA folds its share of the flat logits range into per-warp records.
 // ---------------------------------------------------------------------------------------------
 template <typename T, bool SAMPLE>
 __global__ void __launch_bounds__(NT, SV_MINB) sv_stream_kernel(const Params P)
 {
-    __shared__ Smem sm;
+    __shared__ StreamSmem st;
     constexpr int VEC = Elt<T>::VEC;
     const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t V = P.V;
     const int64_t F0 = (int64_t)g * P.E;
     const int64_t F1 = min(F0 + P.E, P.total);
+    pdl_launch_dependents();
     if (F0 >= F1) return;
     const int64_t r_end = (F1 - 1) / V;
     for (int64_t r = F0 / V; r <= r_end; ++r) {
@@ -737,43 +631,38 @@ __global__ void __launch_bounds__(NT, SV_MINB) sv_stream_kernel(const Params P)
         const int n = (int)(r - (int64_t)b * P.rpr);
         if (SAMPLE) {
             __syncthreads();
-            if (warp == 0) build_children(P, b, n, sm.st.ex_col, sm.st.ex_node, &sm.st.ex_cnt, lane);
+            if (warp == 0) build_children(P, b, n, st.ex_col, st.ex_node, &st.ex_cnt, lane);
             __syncthreads();
         }
         const Seg sg = seg_of<VEC>(P, g, r, warp);
-        const void *row = reinterpret_cast<const T *>(P.logits) + r * V;
+        const T *row = reinterpret_cast<const T *>(P.logits) + r * V;
         SampleAcc sa;
         GreedyAcc ga;
         ExCursor ex;
-        ex.init(sm.st.ex_col, sm.st.ex_node, SAMPLE ? sm.st.ex_cnt : 0, P.caps + (int64_t)b * P.rpr);
+        ex.init(st.ex_col, st.ex_node, SAMPLE ? st.ex_cnt : 0, P.caps + (int64_t)b * P.rpr);
         stream_segment<T, SAMPLE>(row, sg, lane, P.cs, ex, sa, ga);
         float2 rec;
         if (SAMPLE) {
-            warp_rec_merge(sa.mc, sa.s);
-            rec = make_float2(sa.mc, sa.s);
+            float mc = sa.mc, sum = sa.total();
+            warp_rec_merge(mc, sum);
+            rec = make_float2(mc, sum);
         } else {
             warp_arg_merge(ga.best, ga.idx);
             rec = make_float2(ga.best, __int_as_float(ga.idx));
         }
         if (lane == 0) P.recs[(g + r) * NW + warp] = rec;
-        // This CTA is done with request b when the request's last row ends inside its range,
-        // or when its range ends.
-        if ((r + 1) % P.rpr == 0 || r == r_end) {
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                const int64_t rf0 = (int64_t)b * P.rpr * V, rf1 = rf0 + (int64_t)P.rpr * V;
-                const unsigned need = (unsigned)((rf1 - 1) / P.E - rf0 / P.E + 1);
-                const unsigned old = atomicAdd(P.cnt1 + b, 1u);
-                sm.st.last = (old == need - 1u);
-            }
-            __syncthreads();
-            if (sm.st.last) {
-                __threadfence();
-                finalize_request<T, SAMPLE>(P, b, sm);
-            }
-        }
     }
+    (void)tid;
+}
+
+// ---------------------------------------------------------------------------------------------
+// The finalising kernel: one CTA per request merges its records, decides and draws.
+// ---------------------------------------------------------------------------------------------
+template <typename T, bool SAMPLE>
+__global__ void __launch_bounds__(NT_FIN) sv_finalize_kernel(const Params P)
+{
+    __shared__ Smem sm;
+    finalize_request<T, SAMPLE, NT_FIN>(P, (int)blockIdx.x, sm);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1015,6 +904,12 @@ static const DevInfo *device_info()
         d.occ[1][0] = o > 0 ? o : 1;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_stream_kernel<float, true>, NT, 0);
         d.occ[1][1] = o > 0 ? o : 1;
+        const void *fin[2] = {(const void *)sv_finalize_kernel<__nv_bfloat16, true>,
+                              (const void *)sv_finalize_kernel<float, true>};
+        for (int i = 0; i < 2; ++i)
+            if (cudaFuncSetAttribute(fin[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)RESCAN_SMEM_BYTES) != cudaSuccess)
+                return nullptr;
         cudaGetLastError();
         d.sms = sms;
     }
@@ -1054,7 +949,8 @@ static int common_setup(Params &P, const void *logits, int dtype, int B, int rpr
     P.rpr = rpr;
     P.V = V;
     P.total = (int64_t)B * rpr * V;
-    plan_split(P.total, d->sms * occ_out, P.E, P.G);
+    const int per_sm = (SV_CTAS_PER_SM > 0 && SV_CTAS_PER_SM < occ_out) ? SV_CTAS_PER_SM : occ_out;
+    plan_split(P.total, d->sms * per_sm, P.E, P.G);
     P.mis = (int)(((uintptr_t)logits % 16) / esize);
     P.cnt1 = reinterpret_cast<unsigned *>(ws + L.cnt1);
     P.cnt2 = reinterpret_cast<unsigned *>(ws + L.cnt2);
@@ -1079,10 +975,29 @@ static void set_rng(Params &P, float temperature, uint64_t seed, uint64_t offset
 template <bool SAMPLE>
 static int launch_stream(const Params &P, int dtype, cudaStream_t s)
 {
-    if (dtype == SPEC_VERIFY_BF16)
+    // The finaliser is launched as a programmatic dependent of the streaming kernel: its CTAs may
+    // start early, stage the request's inputs, and wait (griddepcontrol) for the records.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)P.B);
+    cfg.blockDim = dim3(NT_FIN);
+    cfg.dynamicSmemBytes = SAMPLE ? RESCAN_SMEM_BYTES : 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (dtype == SPEC_VERIFY_BF16) {
         sv_stream_kernel<__nv_bfloat16, SAMPLE><<<P.G, NT, 0, s>>>(P);
-    else
+        if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
+        if (cudaLaunchKernelEx(&cfg, sv_finalize_kernel<__nv_bfloat16, SAMPLE>, P) != cudaSuccess)
+            return SPEC_VERIFY_ECUDA;
+    } else {
         sv_stream_kernel<float, SAMPLE><<<P.G, NT, 0, s>>>(P);
+        if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
+        if (cudaLaunchKernelEx(&cfg, sv_finalize_kernel<float, SAMPLE>, P) != cudaSuccess)
+            return SPEC_VERIFY_ECUDA;
+    }
     return cudaGetLastError() == cudaSuccess ? SPEC_VERIFY_OK : SPEC_VERIFY_ECUDA;
 }
 

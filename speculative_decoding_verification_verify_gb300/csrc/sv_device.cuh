@@ -91,6 +91,15 @@ __device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Programmatic dependent launch: the finalising kernel may start while the streaming kernel
+// runs; it reads only inputs until pdl_wait(), which returns once the streaming grid has
+// completed and its writes are visible.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void raise_status(int32_t *st, int code)
 {
     if (st && code) atomicMax(st, code);

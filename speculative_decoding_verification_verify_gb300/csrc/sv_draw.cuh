@@ -19,8 +19,8 @@ struct DrawSmem {
     int found;          // column found (-1 while searching)
     int lastpos;        // last column with positive weight seen so far
     int first_thread;   // lowest thread whose inclusive sum crosses t
-    float red[NW][4];   // per-warp partial totals of up to 4 rounds
-    float tot[4];       // round totals
+    float red[NW][16];  // per-warp partial totals of up to 16 rounds
+    float tot[16];      // round totals
     float wpre[NW];     // exclusive warp prefixes of the scanned round
 };
 
@@ -51,7 +51,7 @@ __device__ __forceinline__ int warp_max_int(int x)
 // Src provides:  using Raw = ...;  static constexpr int GS;
 //   Raw prefetch(int64_t gi) const;                      // issue the loads of group gi
 //   int weights(const Raw&, int64_t gi, float (&w)[GS]) const;  // weights; returns first column
-// KB rounds per batch (<= 4).  All threads of the CTA must call.
+// KB rounds per batch (<= 16).  All threads of the CTA must call.
 template <int KB, typename Src>
 __device__ void draw_span(const Src &src, int64_t ngroups, float t, DrawSmem &D)
 {
