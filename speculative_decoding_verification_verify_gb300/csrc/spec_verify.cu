@@ -39,46 +39,56 @@ namespace sv {
 #ifndef SV_MINB
 #define SV_MINB 3
 #endif
-constexpr int NT_FIN = 256;    // threads of a finalising CTA
-#ifndef SV_CTAS_PER_SM
-#define SV_CTAS_PER_SM 0  // streaming CTAs per SM (0: as many as fit)
-#endif
+constexpr int NT_FIN_MAX = 256;  // most threads of a finalising CTA: one warp per row, up to 8 rows
+
 
 struct StreamSmem {
-    int ex_col[MAX_RPR];   // sorted columns of the current row's child tokens
-    int ex_node[MAX_RPR];  // the child node of each
-    int ex_cnt;
-    int last;
+    int ex_col[NW][MAX_RPR];   // per warp: sorted columns of its current row's child tokens
+    int ex_node[NW][MAX_RPR];  // the child node of each
+    int ex_cnt[NW];
 };
 
+// Per-request state of the finalising CTA.  Everything above the marked line depends only on the
+// call's inputs and is staged before the streaming kernel's records are read.
 struct FinSmem {
-    int par[MAX_RPR], tok[MAX_RPR];
-    int first_child[MAX_RPR], next_sib[MAX_RPR];
-    float row_mc[MAX_RPR], row_S[MAX_RPR], row_tot[MAX_RPR];
-    float node_e[MAX_RPR], node_p[MAX_RPR], qx[MAX_RPR], capl[MAX_RPR];
-    float u[MAX_RPR], v[MAX_RPR];
+    int par[MAX_RPR], tok[MAX_RPR], dep[MAX_RPR];
+    int first_child[MAX_RPR], next_sib[MAX_RPR];  // children with a usable token, by node index
+    int ex_off[MAX_RPR], ex_n[MAX_RPR];           // each node's children, sorted by token column:
+    int ex_col[MAX_RPR], ex_node[MAX_RPR];        //   ex_col/ex_node[ex_off[n] .. + ex_n[n])
+    float qx[MAX_RPR], u[MAX_RPR], v[MAX_RPR];
+    long long g_lo[MAX_RPR];                      // first streaming CTA of each row
+    long long row_base[MAX_RPR];                  // first record index of each row
+    int row_L[MAX_RPR];                           // records of each row
+    int need_draw[MAX_RPR];                       // the row's speculative draw may be emitted
+    // ---- from the records
+    float row_mc[MAX_RPR], row_S[MAX_RPR];        // non-child mass S * 2^row_mc
+    float row_M[MAX_RPR], row_tot[MAX_RPR];       // reference covering the children too; total in it
+    float row_z[MAX_RPR];                         // non-child share of the row's mass
+    float node_p[MAX_RPR];                        // p of node n's token in its parent's row
     float row_best[MAX_RPR];
     int row_arg[MAX_RPR];
-    int acc[MAX_RPR];
+    int cand[MAX_RPR];                            // the row's draw when it needs no rescan
+    int rs_ok[MAX_RPR];                           // the row's draw rescans columns [rs_c0, rs_c1)
+    int rs_c0[MAX_RPR], rs_c1[MAX_RPR];           //   of its crossing record,
+    float rs_cum[MAX_RPR], rs_t[MAX_RPR];         //   mass before it, threshold (+inf: the last)
+    RescanSmem RS;
     int path[MAX_RPR];
     int status;
     int stop;     // node at which the round stops
     int L;        // accepted drafts
-    int mode;     // 0 emit argmax, 1 draw from the stop row (children zeroed), 2 residual pending
-    int take_last;
-    int rec;
-    float cum_before;
-    float thresh;
+    int mode;     // 0 emit argmax, 1 emit the stop row's draw, 2 residual pending
     int last_tok;
-    int ex_col[MAX_RPR];
-    int ex_cnt;
-    DrawSmem D;
-    RescanSmem RS;
 };
 
-struct Smem {
-    StreamSmem st;
-    FinSmem fin;
+// State of the residual kernel's last CTA.
+struct ResidSmem {
+    int rec;
+    int take_last;
+    int mode;
+    float cum_before;
+    float thresh;
+    float z;
+    DrawSmem D;
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -123,111 +133,38 @@ __device__ void build_children(const Params &P, int b, int n, int *ex_col, int *
     __syncwarp();
 }
 
-// The same child list, built by the finalising CTA from the structure it staged in shared memory.
-__device__ void children_from_smem(FinSmem &F, int n, int rpr, int64_t V, int *ex_node, int lane)
-{
-    int cnt = 0;
-    for (int base = n + 1; base < rpr; base += 32) {
-        const int ch = base + lane;
-        const bool ok = ch < rpr && F.par[ch] == n && F.tok[ch] >= 0 && (int64_t)F.tok[ch] < V;
-        const unsigned m = __ballot_sync(0xffffffffu, ok);
-        if (ok) {
-            const int pos = cnt + __popc(m & ((1u << lane) - 1u));
-            F.ex_col[pos] = F.tok[ch];
-            ex_node[pos] = ch;
-        }
-        cnt += __popc(m);
-    }
-    __syncwarp();
-    if (lane == 0) {
-        for (int i = 1; i < cnt; ++i) {
-            const int c = F.ex_col[i], nd = ex_node[i];
-            int j = i - 1;
-            while (j >= 0 && F.ex_col[j] > c) {
-                F.ex_col[j + 1] = F.ex_col[j];
-                ex_node[j + 1] = ex_node[j];
-                --j;
-            }
-            F.ex_col[j + 1] = c;
-            ex_node[j + 1] = nd;
-        }
-        F.ex_cnt = cnt;
-    }
-    __syncwarp();
-}
-
 // ---------------------------------------------------------------------------------------------
 // One warp streams its segment [c0, c1) of a row: the unaligned head and tail element by element,
 // the 16-byte aligned body with vector loads.  Each lane visits its columns in ascending order.
 // ---------------------------------------------------------------------------------------------
 template <typename T, bool SAMPLE>
 __device__ __forceinline__ void stream_segment(const T *row, const Seg &sg, int lane, float cs,
-                                               ExCursor &ex, SampleAcc &sa, GreedyAcc &ga)
+                                               ExCursor &ex, float4 *recs, int64_t idx0, int nsub)
 {
+    SampleAcc sa;
+    GreedyAcc ga;
     for (int c = (int)sg.c0 + lane; c < (int)sg.b0; c += 32) {
         const float x = Elt<T>::load(row, c);
         if (SAMPLE) sample_scalar(sa, x, c, cs, ex);
         else greedy_scalar(ga, x, c);
     }
-    stream_body<T, SAMPLE>(row, (int)sg.b0, (int)sg.b1, lane, cs, ex, sa, ga);
+    stream_body<T, SAMPLE>(row, (int)sg.c0, (int)sg.b0, (int)sg.b1, lane, cs, ex, sa, ga, recs, idx0);
     for (int c = (int)sg.b1 + lane; c < (int)sg.c1; c += 32) {
         const float x = Elt<T>::load(row, c);
         if (SAMPLE) sample_scalar(sa, x, c, cs, ex);
         else greedy_scalar(ga, x, c);
     }
+    const int nvec = (int)((sg.b1 - sg.b0) / Elt<T>::VEC);
+    const int used = nvec > 0 ? (nvec + SUB_VEC - 1) / SUB_VEC : 1;
+    const int k = used - 1;
+    flush_record<SAMPLE>(recs, idx0 + k, lane, sa, ga,
+                         k == 0 ? (int)sg.c0 : (int)sg.b0 + k * SUB_VEC * Elt<T>::VEC, (int)sg.c1);
+    // Sub-slots this segment does not reach hold empty records.
+    if (lane == 0)
+        for (int k2 = used; k2 < nsub; ++k2)
+            recs[idx0 + k2] = SAMPLE ? make_float4(REF_NONE, 0.f, 0.f, 0.f)
+                                    : make_float4(NEG_INF, __int_as_float(INT_MAX), 0.f, 0.f);
 }
-
-// ---------------------------------------------------------------------------------------------
-// Draw sources for the block rescan.
-// ---------------------------------------------------------------------------------------------
-// Body of a segment: one 16-byte vector per group; weight 2^(l*cs - mc), children zeroed.
-template <typename T>
-struct VecSrc {
-    static constexpr int GS = Elt<T>::VEC;
-    using Raw = uint4;
-    const uint4 *vp;
-    int64_t col0;  // column of group 0
-    float cs, mc;
-    const int *ex;
-    int ex_cnt;
-    __device__ Raw prefetch(int64_t gi) const { return ldg_stream(vp + gi); }
-    __device__ int weights(const Raw &r, int64_t gi, float (&w)[GS]) const
-    {
-        float x[GS];
-        Elt<T>::unpack(r, x);
-        const int c = (int)(col0 + gi * GS);
-#pragma unroll
-        for (int j = 0; j < GS; ++j) w[j] = ex2(fmaf(x[j], cs, -mc));
-        for (int e = 0; e < ex_cnt; ++e) {
-            const int d = ex[e] - c;
-#pragma unroll
-            for (int j = 0; j < GS; ++j)
-                if (d == j) w[j] = 0.f;
-        }
-        return c;
-    }
-};
-
-// Unaligned head or tail: one element per group.
-template <typename T>
-struct ScalarSrc {
-    static constexpr int GS = 1;
-    using Raw = float;
-    const void *row;
-    int64_t col0;
-    float cs, mc;
-    const int *ex;
-    int ex_cnt;
-    __device__ Raw prefetch(int64_t gi) const { return Elt<T>::load(row, col0 + gi); }
-    __device__ int weights(const Raw &x, int64_t gi, float (&w)[1]) const
-    {
-        const int c = (int)(col0 + gi);
-        w[0] = ex2(fmaf(x, cs, -mc));
-        for (int e = 0; e < ex_cnt; ++e)
-            if (ex[e] == c) w[0] = 0.f;
-        return c;
-    }
-};
 
 __device__ __forceinline__ void draw_init(DrawSmem &D, float cum)
 {
@@ -240,22 +177,54 @@ __device__ __forceinline__ void draw_init(DrawSmem &D, float cum)
 }
 
 // ---------------------------------------------------------------------------------------------
-// Finalisation of request b by the last CTA to finish it.
+// Finalisation of request b: one warp per row merges the row's records, weighs the row's
+// children and draws the row's candidate token; then one warp decides.
 // ---------------------------------------------------------------------------------------------
-extern __shared__ __align__(16) unsigned char sv_dyn_smem[];
+constexpr int REC_PER_LANE = 4;  // records a lane keeps in registers for the draw's locate step
 
-template <typename T, bool SAMPLE, int NTF>
-__device__ void finalize_request(const Params &P, int b, Smem &sm)
+// Locate step over one chunk of 32 records with masses m (in the row's reference): finds the
+// first record where the running mass exceeds t, and tracks the last record with positive mass.
+struct Locate {
+    float cum = 0.f, before = 0.f, lp_before = 0.f;
+    int found = -1, lastpos = -1;
+};
+
+__device__ __forceinline__ bool locate_chunk(Locate &Lc, float m, int c0, float t, int lane)
 {
-    FinSmem &F = sm.fin;
-    constexpr int NWF = NTF / 32;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float incl = warp_incl_scan(m, lane);
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.f;
+    const unsigned hit = __ballot_sync(0xffffffffu, Lc.cum + incl > t);
+    const unsigned pos = __ballot_sync(0xffffffffu, m > 0.f);
+    if (pos) {
+        const int lp = 31 - __clz(pos);
+        Lc.lastpos = c0 + lp;
+        Lc.lp_before = Lc.cum + __shfl_sync(0xffffffffu, excl, lp);
+    }
+    if (hit) {
+        const int fl = __ffs(hit) - 1;
+        Lc.found = c0 + fl;
+        Lc.before = Lc.cum + __shfl_sync(0xffffffffu, excl, fl);
+        return true;
+    }
+    Lc.cum += __shfl_sync(0xffffffffu, incl, 31);
+    return false;
+}
+
+__device__ __forceinline__ float rec_mass(const float4 &r, float mc)
+{
+    return (r.y == 0.f) ? 0.f : r.y * ex2(r.x - mc);
+}
+
+// Stage the request's structure, uniforms and record ranges (inputs only).
+template <bool SAMPLE>
+__device__ void stage_request(const Params &P, int b, FinSmem &F)
+{
+    const int tid = threadIdx.x, nt = blockDim.x;
     const int rpr = P.rpr;
     const int64_t V = P.V;
     const int64_t rbase = (int64_t)b * rpr;
-
-    // Prologue on inputs only (may overlap the streaming kernel): structure, q(x), uniforms.
-    for (int n = tid; n < rpr; n += NTF) {
+    for (int n = tid; n < rpr; n += nt) {
         F.par[n] = n == 0 ? (P.is_tree ? __ldg(P.parents + rbase) : -1) : node_parent(P, b, n);
         F.tok[n] = n == 0 ? -1 : node_token(P, b, n);
         float qv = 1.f;
@@ -269,162 +238,316 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
             F.u[n] = uv.x;
             F.v[n] = uv.y;
         }
+        const int64_t rr = rbase + n, rowf = rr * V;
+        const int64_t g_lo = rowf / P.E, g_hi = (rowf + V - 1) / P.E;
+        F.g_lo[n] = g_lo;
+        F.row_base[n] = (g_lo + rr) * NW * P.nsub;
+        F.row_L[n] = (int)((g_hi - g_lo + 1) * NW * P.nsub);
     }
     if (tid == 0) F.status = 0;
     __syncthreads();
-
-    // Window of record indices covering all rows of the request (contiguous, possibly with unused
-    // slots); small enough windows are kept in shared memory for the draw's locate step.
-    const int64_t win0 = (rbase * V / P.E + rbase) * NW;
-    const int64_t win1 = (((rbase + rpr) * V - 1) / P.E + rbase + rpr - 1) * NW + NW;
-    float2 *recs_s = reinterpret_cast<float2 *>(sv_dyn_smem);
-    const bool keep = SAMPLE && (win1 - win0) * (int64_t)sizeof(float2) <= (int64_t)RESCAN_SMEM_BYTES;
-
-    // From here on the streaming kernel's records and captures are read.
-    pdl_wait();
-    // Captured logits of each node's token in its parent's row, and the per-row merge of the
-    // warp records (one warp per row); all these loads are in flight together.
-    for (int n = tid; n < rpr; n += NTF) {
-        float l = NEG_INF;
-        if (SAMPLE && n >= 1) {
-            const int pa = F.par[n], tk = F.tok[n];
-            if (pa >= 0 && pa < n && tk >= 0 && (int64_t)tk < V) l = __ldcg(P.caps + rbase + n);
+    if (!P.is_tree) {
+        // A chain is a path: node n's only child is n + 1 (when its draft is usable).
+        for (int n = tid; n < rpr; n += nt) {
+            const int tk = F.tok[n];
+            if (n >= 1 && (tk < -1 || (int64_t)tk >= V)) atomicMax(&F.status, SPEC_VERIFY_DEV_BAD_TOKEN);
+            const bool has = n + 1 < rpr && F.tok[n + 1] >= 0 && (int64_t)F.tok[n + 1] < V;
+            int off = 0;
+            for (int m = 1; m <= n; ++m) off += (F.tok[m] >= 0 && (int64_t)F.tok[m] < V) ? 1 : 0;
+            F.first_child[n] = has ? n + 1 : -1;
+            F.next_sib[n] = -1;
+            F.ex_n[n] = has ? 1 : 0;
+            F.ex_off[n] = off;
+            if (has) {
+                F.ex_col[off] = F.tok[n + 1];
+                F.ex_node[off] = n + 1;
+            }
+            F.dep[n] = n;
+            // With draft probabilities a rejected draft's row is left to the residual kernel.
+            F.need_draw[n] = SAMPLE && !(P.q && has);
         }
-        F.capl[n] = l;
+        __syncthreads();
+        return;
     }
-    for (int i = warp; i < rpr; i += NWF) {
-        const int64_t r = rbase + i;
-        const int64_t rowf = r * V;
-        const int64_t g_lo = rowf / P.E, g_hi = (rowf + V - 1) / P.E;
-        const int64_t base = (g_lo + r) * NW;
-        const int L = (int)((g_hi - g_lo + 1) * NW);
-        if (SAMPLE) {
-            float mc = REF_NONE, s = 0.f;
-            for (int t = lane; t < L; t += 32) {
-                const float2 rec = __ldcg(P.recs + base + t);
-                if (keep) recs_s[base + t - win0] = rec;
-                rec_merge(mc, s, rec.x, rec.y);
-            }
-            warp_rec_merge(mc, s);
-            if (lane == 0) {
-                F.row_mc[i] = mc;
-                F.row_S[i] = s;
-            }
-        } else {
-            float best = NEG_INF;
-            int idx = INT_MAX;
-            for (int t = lane; t < L; t += 32) {
-                const float2 rec = __ldcg(P.recs + base + t);
-                arg_merge(best, idx, rec.x, __float_as_int(rec.y));
-            }
-            warp_arg_merge(best, idx);
-            if (lane == 0) {
-                F.row_best[i] = best;
-                F.row_arg[i] = idx;
-            }
-        }
-    }
-    __syncthreads();
-
-    // Validation; the largest fault code of the request wins.
-    {
+    // Trees: validation (the largest fault code of the request wins), children and depths.
+    for (int n = tid; n < rpr; n += nt) {
         int st = 0;
-        for (int n = tid; n < rpr; n += NTF) {
-            if (n >= 1) {
-                const int tk = F.tok[n];
-                if (tk < -1 || (int64_t)tk >= V) st = max(st, SPEC_VERIFY_DEV_BAD_TOKEN);
-                if (P.is_tree && (F.par[n] < 0 || F.par[n] >= n)) st = max(st, SPEC_VERIFY_DEV_BAD_TREE);
-                if (P.is_tree && SAMPLE && tk >= 0) {
-                    for (int m = n + 1; m < rpr; ++m)
-                        if (F.par[m] == F.par[n] && F.tok[m] == tk) st = max(st, SPEC_VERIFY_DEV_DUP_SIBLING);
-                }
-            } else if (P.is_tree && F.par[0] != -1) {
-                st = max(st, SPEC_VERIFY_DEV_BAD_TREE);
+        const int tk = F.tok[n];
+        if (n >= 1) {
+            if (tk < -1 || (int64_t)tk >= V) st = SPEC_VERIFY_DEV_BAD_TOKEN;
+            if (F.par[n] < 0 || F.par[n] >= n) st = max(st, SPEC_VERIFY_DEV_BAD_TREE);
+            if (SAMPLE && tk >= 0) {
+                for (int m = n + 1; m < rpr; ++m)
+                    if (F.par[m] == F.par[n] && F.tok[m] == tk) st = max(st, SPEC_VERIFY_DEV_DUP_SIBLING);
             }
-            bool bad;
-            if (SAMPLE) {
-                bad = !(fabsf(F.row_mc[n]) < POS_INF) || !(F.row_S[n] >= 0.f) || !(F.row_S[n] < POS_INF);
-            } else {
-                const float bv = F.row_best[n];
-                bad = !(fabsf(bv) < POS_INF);
-            }
-            if (bad) st = max(st, SPEC_VERIFY_DEV_BAD_ROW);
+        } else if (F.par[0] != -1) {
+            st = SPEC_VERIFY_DEV_BAD_TREE;
         }
         if (st) atomicMax(&F.status, st);
-    }
-    // Children lists (ascending node index) and, when sampling, each child's probability.
-    for (int n = tid; n < rpr; n += NTF) {
-        int fc = -1, ns = -1;
+        int fc = -1, ns = -1, cnt = 0;
         for (int m = n + 1; m < rpr; ++m) {
-            if (fc < 0 && F.par[m] == n && F.tok[m] >= 0) fc = m;
-        }
-        if (n >= 1) {
-            for (int m = n + 1; m < rpr; ++m) {
-                if (F.par[m] == F.par[n] && F.tok[m] >= 0) {
-                    ns = m;
-                    break;
-                }
+            const bool usable = F.tok[m] >= 0 && (int64_t)F.tok[m] < V;
+            if (usable && F.par[m] == n) {
+                if (fc < 0) fc = m;
+                ++cnt;
             }
+            if (n >= 1 && ns < 0 && usable && F.par[m] == F.par[n]) ns = m;
         }
         F.first_child[n] = fc;
         F.next_sib[n] = ns;
-        if (SAMPLE && n >= 1) {
-            const int pa = F.par[n], tk = F.tok[n];
-            float e = 0.f;
-            if (pa >= 0 && pa < n && tk >= 0 && (int64_t)tk < V) e = ex2(fmaf(F.capl[n], P.cs, -F.row_mc[pa]));
-            F.node_e[n] = e;
+        F.ex_n[n] = cnt;
+        int d = 0, m = n;
+        for (int it = 0; it < rpr && m > 0; ++it) {
+            const int pa = F.par[m];
+            if (pa < 0 || pa >= m) break;
+            m = pa;
+            ++d;
         }
+        F.dep[n] = d;
+        F.need_draw[n] = SAMPLE;
     }
     __syncthreads();
-    if (SAMPLE) {
-        for (int n = tid; n < rpr; n += NTF) {
-            float extra = 0.f;
-            for (int m = n + 1; m < rpr; ++m)
-                if (F.par[m] == n && F.tok[m] >= 0 && (int64_t)F.tok[m] < V) extra += F.node_e[m];
-            F.row_tot[n] = F.row_S[n] + extra;
-        }
-        __syncthreads();
-        for (int n = 1 + tid; n < rpr; n += NTF) {
-            const int pa = F.par[n];
-            F.node_p[n] = (pa >= 0 && pa < n) ? F.node_e[n] / F.row_tot[pa] : 0.f;
-        }
-        if (tid < rpr) {
-            const float tot = F.row_tot[tid];
-            if (!(tot > 0.f) || !(tot < POS_INF)) atomicMax(&F.status, SPEC_VERIFY_DEV_BAD_ROW);
-        }
-        __syncthreads();
+    for (int n = tid; n < rpr; n += nt) {
+        int off = 0;
+        for (int m = 0; m < n; ++m) off += F.ex_n[m];
+        F.ex_off[n] = off;
     }
+    __syncthreads();
+    // Each usable child takes its rank among its siblings by (token, node).
+    for (int m = 1 + tid; m < rpr; m += nt) {
+        const int pa = F.par[m], tk = F.tok[m];
+        if (pa < 0 || pa >= m || tk < 0 || (int64_t)tk >= V) continue;
+        int rank = 0;
+        for (int s = pa + 1; s < rpr; ++s) {
+            const int ts = F.tok[s];
+            if (s != m && F.par[s] == pa && ts >= 0 && (int64_t)ts < V && (ts < tk || (ts == tk && s < m)))
+                ++rank;
+        }
+        F.ex_col[F.ex_off[pa] + rank] = tk;
+        F.ex_node[F.ex_off[pa] + rank] = m;
+    }
+    __syncthreads();
+}
+
+// Row n of request b, by one warp, once the records are visible.
+template <typename T, bool SAMPLE>
+__device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane)
+{
+    const int64_t base = F.row_base[n];
+    const int L = F.row_L[n];
+    if (!SAMPLE) {
+        float best = NEG_INF;
+        int idx = INT_MAX;
+        for (int t = lane; t < L; t += 32) {
+            const float4 rec = __ldcg(P.recs + base + t);
+            arg_merge(best, idx, rec.x, __float_as_int(rec.y));
+        }
+        warp_arg_merge(best, idx);
+        if (lane == 0) {
+            F.row_best[n] = best;
+            F.row_arg[n] = idx;
+            if (!(fabsf(best) < POS_INF)) atomicMax(&F.status, SPEC_VERIFY_DEV_BAD_ROW);
+        }
+        return;
+    }
+    // The children's captured logits and the row's records are loaded together.  Each lane takes
+    // a contiguous run of q records; runs of up to REC_PER_LANE stay in registers for the draw's
+    // locate step.
+    const int off = F.ex_off[n], cnt = F.ex_n[n];
+    float cap[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int e = lane + 32 * h;
+        cap[h] = e < cnt ? __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[off + e]) : NEG_INF;
+    }
+    const int q = (L + 31) >> 5;
+    const bool inreg = q <= REC_PER_LANE;
+    float4 rr[REC_PER_LANE];
+    float mc = REF_NONE, s = 0.f;
+    if (inreg) {
+#pragma unroll
+        for (int i = 0; i < REC_PER_LANE; ++i) {
+            const int t = lane * q + i;
+            rr[i] = (i < q && t < L) ? __ldcg(P.recs + base + t) : make_float4(REF_NONE, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < REC_PER_LANE; ++i) rec_merge(mc, s, rr[i].x, rr[i].y);
+    } else {
+        for (int t = lane; t < L; t += 32) {
+            const float4 rec = __ldcg(P.recs + base + t);
+            rec_merge(mc, s, rec.x, rec.y);
+        }
+    }
+    warp_rec_merge(mc, s);
+    // The children: one reference M covers them and the rest, so a child far above every other
+    // token cannot overflow.
+    const float cs = P.cs;
+    float M = mc;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) M = fmaxf(M, cap[h] * cs);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float s_ref = (s == 0.f) ? 0.f : s * ex2(mc - M);
+    float ec[2], esum = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        ec[h] = (lane + 32 * h < cnt) ? ex2(fmaf(cap[h], cs, -M)) : 0.f;
+        esum += ec[h];
+    }
+    esum = warp_sum(esum);
+    const float tot = s_ref + esum;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        if (lane + 32 * h < cnt) F.node_p[F.ex_node[off + lane + 32 * h]] = ec[h] / tot;
+    const bool bad = !(s >= 0.f) || !(s < POS_INF) || !(tot > 0.f) || !(tot < POS_INF);
+    if (lane == 0) {
+        F.row_mc[n] = mc;
+        F.row_S[n] = s;
+        F.row_M[n] = M;
+        F.row_tot[n] = tot;
+        F.row_z[n] = s_ref / tot;
+        F.cand[n] = -1;
+        F.rs_ok[n] = 0;
+        if (bad) atomicMax(&F.status, SPEC_VERIFY_DEV_BAD_ROW);
+    }
+    if (bad || !F.need_draw[n]) return;
+
+    // The row's draw: children excluded, threshold v * Z with Z the non-child mass.  Here only
+    // the record holding the crossing is located; the rescan of its columns waits until the stop
+    // row is known.
+    const float vdraw = F.v[P.is_tree ? F.dep[n] : n];
+    int drawn = -1;
+    if (s > 0.f) {
+        const float t = vdraw * s;
+        int fi = -1;         // crossing record (relative to the row's first), or the last positive
+        float before = 0.f;  // mass of the row's records before it
+        bool take_last = false;
+        float4 frec = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (inreg) {
+            float m[REC_PER_LANE], own = 0.f;
+#pragma unroll
+            for (int i = 0; i < REC_PER_LANE; ++i) {
+                m[i] = rec_mass(rr[i], mc);
+                own += m[i];
+            }
+            const float incl = warp_incl_scan(own, lane);
+            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+            if (lane == 0) excl = 0.f;
+            const unsigned hit = __ballot_sync(0xffffffffu, excl + own > t);
+            const unsigned pos = __ballot_sync(0xffffffffu, own > 0.f);
+            take_last = hit == 0;
+            const int who = take_last ? 31 - __clz(pos) : __ffs(hit) - 1;
+            if (pos && lane == who) {
+                float c = excl, lpc = 0.f;
+                int lpi = -1;
+#pragma unroll
+                for (int i = 0; i < REC_PER_LANE; ++i) {
+                    if (m[i] > 0.f) {
+                        if (fi < 0 && !take_last && c + m[i] > t) {
+                            fi = i;
+                            before = c;
+                        }
+                        if (fi < 0) {
+                            lpi = i;
+                            lpc = c;
+                        }
+                    }
+                    c += m[i];
+                }
+                if (fi < 0) {  // take_last, or rounding: the run crossed, its records did not
+                    fi = lpi;
+                    before = lpc;
+                    take_last = true;
+                }
+#pragma unroll
+                for (int i = 0; i < REC_PER_LANE; ++i)
+                    if (i == fi) frec = rr[i];
+                fi += lane * q;
+            }
+        } else {
+            Locate Lc;
+            for (int c0 = 0; c0 < L; c0 += 32) {
+                const float4 rec = c0 + lane < L ? __ldcg(P.recs + base + c0 + lane)
+                                                 : make_float4(REF_NONE, 0.f, 0.f, 0.f);
+                if (locate_chunk(Lc, rec_mass(rec, mc), c0, t, lane)) break;
+            }
+            if (lane == 0) {
+                fi = Lc.found >= 0 ? Lc.found : Lc.lastpos;
+                before = Lc.found >= 0 ? Lc.before : Lc.lp_before;
+                take_last = Lc.found < 0;
+                if (fi >= 0) frec = __ldcg(P.recs + base + fi);
+            }
+        }
+        if (fi >= 0) {  // exactly one lane holds it
+            F.rs_c0[n] = __float_as_int(frec.z);
+            F.rs_c1[n] = __float_as_int(frec.w);
+            F.rs_cum[n] = before;
+            F.rs_t[n] = take_last ? POS_INF : t;
+            F.rs_ok[n] = 1;
+        }
+    } else if (lane == 0) {
+        // Every non-child token is -inf: draw among the children by p, in column order.
+        const float tc = esum;
+        const float t = vdraw * tc;
+        float c = 0.f;
+        int lastc = -1;
+        for (int e = 0; e < cnt && drawn < 0; ++e) {
+            const float cp = __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[off + e]);
+            const float w = ex2(fmaf(cp, cs, -M));
+            if (w > 0.f) {
+                lastc = F.ex_col[off + e];
+                c += w;
+                if (c > t) drawn = lastc;
+            }
+        }
+        if (drawn < 0) drawn = lastc;
+    }
+    if (lane == 0) F.cand[n] = drawn;
+}
+
+template <typename T, bool SAMPLE>
+__device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stage)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwf = blockDim.x >> 5;
+    const int rpr = P.rpr;
+
+    stage_request<SAMPLE>(P, b, F);
+    // From here on the streaming kernel's records and captures are read.
+    pdl_wait();
+    for (int n = warp; n < rpr; n += nwf) finish_row<T, SAMPLE>(P, b, n, F, lane);
+    __syncthreads();
 
     // Decide the accepted path and the stop node.
-    const bool faulted = F.status != 0;
-    if (!faulted) {
+    if (F.status == 0) {
         if (!P.is_tree) {
-            // Chain: acc[i] for draft slot i; the first non-accepted slot stops the round.
-            const int k = P.k;
-            if (tid < 64) {
-                bool acc = false;
-                if (tid < k) {
-                    const int x = F.tok[tid + 1];
-                    if (x >= 0) {
-                        if (SAMPLE) acc = F.u[tid] * F.qx[tid + 1] < F.node_p[tid + 1];
-                        else acc = (x == F.row_arg[tid]);
+            // Chain: the first draft slot that is not accepted stops the round (warp ballots).
+            if (warp == 0) {
+                const int k = P.k;
+                int j = k;
+                for (int c0 = 0; c0 < k; c0 += 32) {
+                    const int i = c0 + lane;
+                    bool acc = false;
+                    if (i < k) {
+                        const int x = F.tok[i + 1];
+                        if (x >= 0) {
+                            if (SAMPLE) acc = F.u[i] * F.qx[i + 1] < F.node_p[i + 1];
+                            else acc = (x == F.row_arg[i]);
+                        }
+                    }
+                    const unsigned m = __ballot_sync(0xffffffffu, i < k && !acc);
+                    if (m) {
+                        j = c0 + __ffs(m) - 1;
+                        break;
                     }
                 }
-                const unsigned m = __ballot_sync(0xffffffffu, !acc);
-                if (lane == 0) F.acc[warp] = (int)m;  // warps 0 and 1 cover slots 0..63
-            }
-            __syncthreads();
-            if (tid == 0) {
-                const unsigned m0 = (unsigned)F.acc[0];
-                const unsigned m1 = (unsigned)F.acc[1];
-                int j = m0 ? (__ffs(m0) - 1) : (32 + __ffs(m1) - 1);
-                if (j > k) j = k;
-                F.L = j;
-                F.stop = j;
-                for (int i = 0; i < j; ++i) F.path[i] = i + 1;
-                if (!SAMPLE) F.mode = 0;
-                else if (j < k && F.tok[j + 1] >= 0 && P.q) F.mode = 2;
-                else F.mode = 1;
+                for (int i = lane; i < j; i += 32) F.path[i] = i + 1;
+                if (lane == 0) {
+                    F.L = j;
+                    F.stop = j;
+                    if (!SAMPLE) F.mode = 0;
+                    else if (j < k && F.tok[j + 1] >= 0 && P.q) F.mode = 2;
+                    else F.mode = 1;
+                }
             }
         } else if (tid == 0) {
             // Tree walk: one coin per depth, children in ascending node index.
@@ -462,108 +585,13 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
         }
     }
     __syncthreads();
-
-    // Draw the stop token from row `stop`, children zeroed (they were tried), unless the
-    // draw is the standard-rejection residual, which the residual kernel does.
-    int drawn = -1;
-    if (!faulted && F.mode == 1) {
-        const int n = F.stop;
-        const int64_t r = rbase + n;
-        const float mc_r = F.row_mc[n];
-        const float vdraw = F.v[P.is_tree ? F.L : n];
-        if (warp == 0) children_from_smem(F, n, rpr, V, sm.st.ex_node, lane);
-        __syncthreads();
-        if (F.row_S[n] > 0.f) {
-            const float t = vdraw * F.row_S[n];
-            // Locate the record holding the crossing (warp 0).
-            const int64_t rowf = r * V;
-            const int64_t g_lo = rowf / P.E, g_hi = (rowf + V - 1) / P.E;
-            const int64_t base = (g_lo + r) * NW;
-            const int L = (int)((g_hi - g_lo + 1) * NW);
-            if (warp == 0) {
-                float cum = 0.f, before = 0.f, lp_before = 0.f;
-                int found = -1, lastpos = -1;
-                for (int c = 0; c < L; c += 32) {
-                    const int ti = c + lane;
-                    float m = 0.f;
-                    if (ti < L) {
-                        const float2 rec = keep ? recs_s[base + ti - win0] : __ldcg(P.recs + base + ti);
-                        m = (rec.y == 0.f) ? 0.f : rec.y * ex2(rec.x - mc_r);
-                    }
-                    const float incl = warp_incl_scan(m, lane);
-                    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-                    if (lane == 0) excl = 0.f;
-                    const unsigned hit = __ballot_sync(0xffffffffu, cum + incl > t);
-                    const unsigned pos = __ballot_sync(0xffffffffu, m > 0.f);
-                    if (pos) {
-                        const int lp = 31 - __clz(pos);
-                        lastpos = c + lp;
-                        lp_before = cum + __shfl_sync(0xffffffffu, excl, lp);
-                    }
-                    if (hit) {
-                        const int fl = __ffs(hit) - 1;
-                        found = c + fl;
-                        before = cum + __shfl_sync(0xffffffffu, excl, fl);
-                        break;
-                    }
-                    cum += __shfl_sync(0xffffffffu, incl, 31);
-                }
-                if (lane == 0) {
-                    if (found >= 0) {
-                        F.rec = found;
-                        F.cum_before = before;
-                        F.take_last = 0;
-                    } else {
-                        F.rec = lastpos;
-                        F.cum_before = lp_before;
-                        F.take_last = 1;
-                    }
-                }
-            }
-            __syncthreads();
-            const int rec = F.rec;
-            if (rec >= 0) {
-                const int64_t g = g_lo + rec / NW;
-                const int w = rec % NW;
-                const Seg sg = seg_of<Elt<T>::VEC>(P, g, r, w);
-                const float tt = F.take_last ? POS_INF : t;
-                const T *row = reinterpret_cast<const T *>(P.logits) + r * V;
-                drawn = rescan_segment<T, NTF>(row, sg, P.cs, mc_r, tt, F.cum_before, F.ex_col, F.ex_cnt,
-                                               sv_dyn_smem, F.RS);
-            }
-        } else {
-            // Every non-child token underflowed: draw among the children, by p, in column order.
-            if (tid == 0) {
-                float tot = 0.f;
-                for (int e = 0; e < F.ex_cnt; ++e) tot += F.node_e[sm.st.ex_node[e]];
-                const float t = vdraw * tot;
-                float c = 0.f;
-                for (int e = 0; e < F.ex_cnt && drawn < 0; ++e) {
-                    const float w = F.node_e[sm.st.ex_node[e]];
-                    if (w > 0.f) {
-                        c += w;
-                        if (c > t) drawn = F.ex_col[e];
-                    }
-                }
-                if (drawn < 0 && F.ex_cnt > 0) drawn = F.ex_col[F.ex_cnt - 1];
-            }
-        }
-    }
-    if (tid == 0) {
-        int last = -1;
-        if (!faulted) {
-            if (F.mode == 0) last = F.row_arg[F.stop];
-            else if (F.mode == 1) last = drawn >= 0 ? drawn : 0;  // < 0 only through rounding
-        }
-        F.last_tok = last;
-    }
-    __syncthreads();
+    const bool faulted = F.status != 0;
 
     // Outputs.
     const int out_w = P.is_tree ? rpr : P.k + 1;
     int32_t *ot = P.out_tokens + (int64_t)b * out_w;
     if (faulted) {
-        for (int i = tid; i < out_w; i += NTF) {
+        for (int i = tid; i < out_w; i += blockDim.x) {
             ot[i] = -1;
             if (P.is_tree) P.accept_index[(int64_t)b * rpr + i] = -1;
         }
@@ -572,41 +600,53 @@ __device__ void finalize_request(const Params &P, int b, Smem &sm)
             raise_status(P.dev_status, F.status);
         }
         if (SAMPLE && P.out_probs && !P.is_tree)
-            for (int i = tid; i < (P.k + 1) * 3; i += NTF) P.out_probs[(int64_t)b * (P.k + 1) * 3 + i] = 0.f;
+            for (int i = tid; i < (P.k + 1) * 3; i += blockDim.x) P.out_probs[(int64_t)b * (P.k + 1) * 3 + i] = 0.f;
         if (SAMPLE && P.q && !P.is_tree && tid == 0) P.pend[b] = make_int4(-1, 0, 0, 0);
-    } else {
-        const int L = F.L;
-        for (int i = tid; i < out_w; i += NTF) {
-            int v = -1;
-            if (i < L) v = F.tok[F.path[i]];
-            else if (i == L) v = F.last_tok;
-            ot[i] = v;
-            if (P.is_tree) P.accept_index[(int64_t)b * rpr + i] = (i == 0) ? 0 : (i <= L ? F.path[i - 1] : -1);
+        return;
+    }
+    const int L = F.L, stop = F.stop, mode = F.mode;
+    int last = -1;
+    if (mode == 0) {
+        last = F.row_arg[stop];
+    } else if (mode == 1) {
+        int drawn = F.cand[stop];
+        if (F.rs_ok[stop]) {
+            const int64_t r = (int64_t)b * rpr + stop;
+            const T *row = reinterpret_cast<const T *>(P.logits) + r * P.V;
+            drawn = block_rescan<T>(row, r * P.V, P.total, P.mis, F.rs_c0[stop], F.rs_c1[stop], P.cs,
+                                    F.row_mc[stop], F.rs_t[stop], F.rs_cum[stop],
+                                    F.ex_col + F.ex_off[stop], F.ex_n[stop], stage, F.RS);
         }
-        if (tid == 0) {
-            P.accept_len[b] = L;
-            if (SAMPLE && P.q && !P.is_tree) {
-                if (F.mode == 2) {
-                    const int n = F.stop;
-                    P.pend[b] = make_int4(n, __float_as_int(F.row_mc[n]), __float_as_int(F.row_tot[n]), 1);
-                } else {
-                    P.pend[b] = make_int4(-1, 0, 0, 0);
-                }
-            }
+        last = drawn >= 0 ? drawn : 0;  // < 0 only through rounding
+    }
+    for (int i = tid; i < out_w; i += blockDim.x) {
+        int v = -1;
+        if (i < L) v = F.tok[F.path[i]];
+        else if (i == L) v = last;
+        ot[i] = v;
+        if (P.is_tree) P.accept_index[(int64_t)b * rpr + i] = (i == 0) ? 0 : (i <= L ? F.path[i - 1] : -1);
+    }
+    if (tid == 0) {
+        P.accept_len[b] = L;
+        if (SAMPLE && P.q && !P.is_tree) {
+            if (mode == 2)
+                P.pend[b] = make_int4(stop, __float_as_int(F.row_M[stop]), __float_as_int(F.row_tot[stop]), 1);
+            else
+                P.pend[b] = make_int4(-1, 0, 0, 0);
         }
-        if (SAMPLE && P.out_probs && !P.is_tree) {
-            float *op = P.out_probs + (int64_t)b * (P.k + 1) * 3;
-            for (int i = tid; i <= P.k; i += NTF) {
-                float p0 = 0.f, q0 = 0.f, z = 0.f;
-                if (i < P.k && F.tok[i + 1] >= 0) {
-                    p0 = F.node_p[i + 1];
-                    q0 = F.qx[i + 1];
-                }
-                if (i == F.stop && F.mode == 1) z = F.row_S[i] / F.row_tot[i];
-                op[3 * i + 0] = p0;
-                op[3 * i + 1] = q0;
-                op[3 * i + 2] = z;
+    }
+    if (SAMPLE && P.out_probs && !P.is_tree) {
+        float *op = P.out_probs + (int64_t)b * (P.k + 1) * 3;
+        for (int i = tid; i <= P.k; i += blockDim.x) {
+            float p0 = 0.f, q0 = 0.f, z = 0.f;
+            if (i < P.k && F.tok[i + 1] >= 0) {
+                p0 = F.node_p[i + 1];
+                q0 = F.qx[i + 1];
             }
+            if (i == stop && mode == 1) z = F.row_z[i];
+            op[3 * i + 0] = p0;
+            op[3 * i + 1] = q0;
+            op[3 * i + 2] = z;
         }
     }
 }
@@ -629,28 +669,13 @@ __global__ void __launch_bounds__(NT, SV_MINB) sv_stream_kernel(const Params P)
     for (int64_t r = F0 / V; r <= r_end; ++r) {
         const int b = (int)(r / P.rpr);
         const int n = (int)(r - (int64_t)b * P.rpr);
-        if (SAMPLE) {
-            __syncthreads();
-            if (warp == 0) build_children(P, b, n, st.ex_col, st.ex_node, &st.ex_cnt, lane);
-            __syncthreads();
-        }
+        // Each warp keeps its own child list, so no warp waits for another at a row change.
+        if (SAMPLE) build_children(P, b, n, st.ex_col[warp], st.ex_node[warp], &st.ex_cnt[warp], lane);
         const Seg sg = seg_of<VEC>(P, g, r, warp);
         const T *row = reinterpret_cast<const T *>(P.logits) + r * V;
-        SampleAcc sa;
-        GreedyAcc ga;
         ExCursor ex;
-        ex.init(st.ex_col, st.ex_node, SAMPLE ? st.ex_cnt : 0, P.caps + (int64_t)b * P.rpr);
-        stream_segment<T, SAMPLE>(row, sg, lane, P.cs, ex, sa, ga);
-        float2 rec;
-        if (SAMPLE) {
-            float mc = sa.mc, sum = sa.total();
-            warp_rec_merge(mc, sum);
-            rec = make_float2(mc, sum);
-        } else {
-            warp_arg_merge(ga.best, ga.idx);
-            rec = make_float2(ga.best, __int_as_float(ga.idx));
-        }
-        if (lane == 0) P.recs[(g + r) * NW + warp] = rec;
+        ex.init(st.ex_col[warp], st.ex_node[warp], SAMPLE ? st.ex_cnt[warp] : 0, P.caps + (int64_t)b * P.rpr);
+        stream_segment<T, SAMPLE>(row, sg, lane, P.cs, ex, P.recs, ((g + r) * NW + warp) * P.nsub, P.nsub);
     }
     (void)tid;
 }
@@ -659,10 +684,11 @@ __global__ void __launch_bounds__(NT, SV_MINB) sv_stream_kernel(const Params P)
 // The finalising kernel: one CTA per request merges its records, decides and draws.
 // ---------------------------------------------------------------------------------------------
 template <typename T, bool SAMPLE>
-__global__ void __launch_bounds__(NT_FIN) sv_finalize_kernel(const Params P)
+__global__ void __launch_bounds__(NT_FIN_MAX) sv_finalize_kernel(const Params P)
 {
-    __shared__ Smem sm;
-    finalize_request<T, SAMPLE, NT_FIN>(P, (int)blockIdx.x, sm);
+    __shared__ FinSmem F;
+    __shared__ uint4 stage[SAMPLE ? RESCAN_STAGE_VEC : 1];
+    finalize_request<T, SAMPLE>(P, (int)blockIdx.x, F, stage);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -708,7 +734,7 @@ struct ResidSrc {
 template <typename T>
 __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
 {
-    __shared__ FinSmem F;
+    __shared__ ResidSmem F;
     __shared__ int is_last;
     const int c = (int)(blockIdx.x % (unsigned)P.C2), b = (int)(blockIdx.x / (unsigned)P.C2);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -802,7 +828,7 @@ __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
             F.take_last = found < 0;
             F.thresh = t;
             F.mode = use_p;
-            F.row_tot[0] = use_p ? 1.f : zr_t;
+            F.z = use_p ? 1.f : zr_t;
         }
     }
     __syncthreads();
@@ -819,7 +845,7 @@ __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
     }
     if (tid == 0) {
         P.out_tokens[(int64_t)b * (P.k + 1) + j] = drawn >= 0 ? drawn : 0;
-        if (P.out_probs) P.out_probs[((int64_t)b * (P.k + 1) + j) * 3 + 2] = F.row_tot[0];
+        if (P.out_probs) P.out_probs[((int64_t)b * (P.k + 1) + j) * 3 + 2] = F.z;
         P.cnt2[b] = 0u;
     }
 }
@@ -853,6 +879,32 @@ struct Layout {
     size_t cnt1, cnt2, recs, caps, pend, recs2, total;
 };
 
+// Split the flat range: one CTA per resident slot of a GB300 (152 SMs x 3 streaming CTAs), but
+// never fewer than E_MIN elements each; E is a multiple of 64 elements so that CTA boundaries keep
+// 16-byte alignment.  The split depends only on the problem size, so the workspace size does too.
+constexpr int RESIDENT_CTAS = 152 * SV_MINB;
+
+static void plan_split(int64_t total, int64_t &E, int &G)
+{
+    int64_t g = RESIDENT_CTAS;
+    const int64_t by_min = (total + E_MIN - 1) / E_MIN;
+    if (g > by_min) g = by_min;
+    if (g > G_MAX) g = G_MAX;
+    if (g < 1) g = 1;
+    E = (total + g - 1) / g;
+    E = (E + 63) / 64 * 64;
+    G = (int)((total + E - 1) / E);
+}
+
+// Sub-records per warp segment: a warp flushes a record every SUB_VEC vectors of its segment,
+// so the draw rescans at most SUB_VEC vectors.  vec = elements per 16-byte vector.
+static int nsub_of(int64_t E, int vec)
+{
+    const int64_t per_warp = ((E + vec - 1) / vec + 2 + NW - 1) / NW;
+    int64_t n = (per_warp + SUB_VEC - 1) / SUB_VEC;
+    return (int)(n < 1 ? 1 : n);
+}
+
 static Layout layout(int B, int rpr, int64_t V)
 {
     // The arrival counters sit in a fixed region at the start of every layout, so a workspace
@@ -860,6 +912,10 @@ static Layout layout(int B, int rpr, int64_t V)
     // are: every call leaves that region zero, whatever the shape of the next call.
     const int64_t R = (int64_t)B * rpr;
     const int C2 = residual_chunks(B, V);
+    int64_t E;
+    int G;
+    plan_split(R * V, E, G);
+    const int nsub = nsub_of(E, 4);  // fp32 logits need the most sub-records
     Layout L;
     size_t off = 0;
     L.cnt1 = off;
@@ -867,7 +923,7 @@ static Layout layout(int B, int rpr, int64_t V)
     L.cnt2 = off;
     off += sizeof(unsigned) * (size_t)B_MAX;
     L.recs = off;
-    off += align256(sizeof(float2) * (size_t)(G_MAX + R) * NW);
+    off += align256(sizeof(float4) * (size_t)(G + R) * NW * nsub);
     L.caps = off;
     off += align256(sizeof(float) * (size_t)R);
     L.pend = off;
@@ -904,31 +960,12 @@ static const DevInfo *device_info()
         d.occ[1][0] = o > 0 ? o : 1;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_stream_kernel<float, true>, NT, 0);
         d.occ[1][1] = o > 0 ? o : 1;
-        const void *fin[2] = {(const void *)sv_finalize_kernel<__nv_bfloat16, true>,
-                              (const void *)sv_finalize_kernel<float, true>};
-        for (int i = 0; i < 2; ++i)
-            if (cudaFuncSetAttribute(fin[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)RESCAN_SMEM_BYTES) != cudaSuccess)
-                return nullptr;
         cudaGetLastError();
         d.sms = sms;
     }
     return &d;
 }
 
-// Split the flat range: as many CTAs as can be resident at once, but never fewer than E_MIN
-// elements each; E is a multiple of 64 elements so that CTA boundaries stay 16-byte aligned.
-static void plan_split(int64_t total, int resident, int64_t &E, int &G)
-{
-    int64_t g = resident;
-    const int64_t by_min = (total + E_MIN - 1) / E_MIN;
-    if (g > by_min) g = by_min;
-    if (g > G_MAX) g = G_MAX;
-    if (g < 1) g = 1;
-    E = (total + g - 1) / g;
-    E = (E + 63) / 64 * 64;
-    G = (int)((total + E - 1) / E);
-}
 
 static int common_setup(Params &P, const void *logits, int dtype, int B, int rpr, int64_t V,
                         void *workspace, size_t ws_bytes, bool sample, int &occ_out)
@@ -949,12 +986,12 @@ static int common_setup(Params &P, const void *logits, int dtype, int B, int rpr
     P.rpr = rpr;
     P.V = V;
     P.total = (int64_t)B * rpr * V;
-    const int per_sm = (SV_CTAS_PER_SM > 0 && SV_CTAS_PER_SM < occ_out) ? SV_CTAS_PER_SM : occ_out;
-    plan_split(P.total, d->sms * per_sm, P.E, P.G);
+    plan_split(P.total, P.E, P.G);
+    P.nsub = nsub_of(P.E, esize == 2 ? 8 : 4);
     P.mis = (int)(((uintptr_t)logits % 16) / esize);
     P.cnt1 = reinterpret_cast<unsigned *>(ws + L.cnt1);
     P.cnt2 = reinterpret_cast<unsigned *>(ws + L.cnt2);
-    P.recs = reinterpret_cast<float2 *>(ws + L.recs);
+    P.recs = reinterpret_cast<float4 *>(ws + L.recs);
     P.caps = reinterpret_cast<float *>(ws + L.caps);
     P.pend = reinterpret_cast<int4 *>(ws + L.pend);
     P.recs2 = reinterpret_cast<float2 *>(ws + L.recs2);
@@ -979,8 +1016,9 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
     // start early, stage the request's inputs, and wait (griddepcontrol) for the records.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)P.B);
-    cfg.blockDim = dim3(NT_FIN);
-    cfg.dynamicSmemBytes = SAMPLE ? RESCAN_SMEM_BYTES : 0;
+    const int nwf = P.rpr < NT_FIN_MAX / 32 ? P.rpr : NT_FIN_MAX / 32;
+    cfg.blockDim = dim3(32u * (unsigned)nwf);
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -16,6 +16,10 @@ constexpr int G_MAX = 4096;   // upper bound on CTAs of the streaming kernel
 constexpr int B_MAX = 65536;  // most requests per call (size of the fixed counter region)
 constexpr int C2_MAX = 1024;  // upper bound on column chunks of the residual kernel
 constexpr int64_t E_MIN = 8192;  // fewest elements a streaming CTA is given
+#ifndef SV_SUB_VEC
+#define SV_SUB_VEC 512
+#endif
+constexpr int SUB_VEC = SV_SUB_VEC;  // 16-byte vectors per sub-record of a warp segment
 constexpr float NEG_INF = -__builtin_huge_valf();
 constexpr float POS_INF = __builtin_huge_valf();
 
@@ -44,11 +48,12 @@ struct Params {
     // workspace
     unsigned *cnt1;              // [B] arrivals at the streaming kernel's per-request counter
     unsigned *cnt2;              // [B] arrivals at the residual kernel's counter
-    float2 *recs;                // [(G + R - 1) * NW] per (piece, warp) records
+    float4 *recs;                // [(G + R) * NW * nsub] per (piece, warp, sub) records
     float *caps;                 // [B * rpr] logit of node j's token in its parent's row
     int4 *pend;                  // [B] residual draw pending: {row, mc bits, total bits, flag}
     float2 *recs2;               // [B * C2 * NW] residual-kernel records
     int C2;                      // residual-kernel column chunks per request
+    int nsub;                    // sub-records per warp segment
     int64_t Ec2;                 // columns per residual chunk
 };
 

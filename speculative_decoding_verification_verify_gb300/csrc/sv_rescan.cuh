@@ -1,27 +1,25 @@
-// sv_rescan.cuh -- the draw's block-wide rescan of one record segment, kept compact.
+// sv_rescan.cuh -- the finalising CTA draws a token from a short column range of a logit row.
 //
-// The finalising CTA knows which warp segment of the stop row holds the crossing of v * Z.  It
-// copies that segment into shared memory with cp.async (hardware-tracked, nothing spins), then
-// one rolled pass gives each thread the weight of its contiguous share, one block scan orders
-// the shares, and the thread whose share crosses the threshold walks it.  The code is small on
-// purpose: it runs once per request on an SM whose instruction cache has never seen it.
+// The finalising kernel knows which record of the streaming pass holds the crossing of the draw
+// threshold t, and the mass before that record.  The record covers a column range of at most
+// SUB_VEC 16-byte vectors (plus an unaligned head and tail), so the CTA copies that range into
+// shared memory with cp.async (every copy in flight at once, completion tracked by the
+// hardware), each thread weighs a contiguous run of a few vectors as the streaming pass did, a
+// block scan of the thread totals picks the thread that holds the crossing, and that thread walks
+// its run.  Loops stay short: this code runs once per request on an SM whose instruction cache
+// has not seen it.
 #pragma once
 
+#include <climits>
+
 #include "sv_device.cuh"
+#include "sv_draw.cuh"
 
 namespace sv {
 
-constexpr int RESCAN_VEC = 4096;  // 16-byte vectors staged per pass (64 KB)
-constexpr size_t RESCAN_SMEM_BYTES = (size_t)(RESCAN_VEC + 2) * 16;
-
-struct RescanSmem {
-    float wsum[NW];
-    float cum;
-    float total;
-    int found;
-    int lastpos;
-    int first;
-};
+// Shared-memory vectors the CTA stages: the range holds at most SUB_VEC aligned vectors plus a
+// partial one at each end.
+constexpr int RESCAN_STAGE_VEC = SUB_VEC + 2;
 
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc)
 {
@@ -31,129 +29,151 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc)
                  : "memory");
 }
 
-// Weights of one staged 16-byte vector whose first element has stage index i0 and column col0:
-// 2^(x*cs - mc) for stage indices in [lo, hi) that are not excluded columns, else 0.  The
-// cursor ep walks the sorted excluded columns (a thread's vectors come in ascending order).
+// The 16-byte vector of a row starting at column col, with the elements outside [c0, c1) read
+// as -inf, element by element, so that no byte outside [c0, c1) is touched.
 template <typename T>
-__device__ __forceinline__ void staged_weights(const uint4 &w, int i0, int lo, int hi, int col0,
-                                               float cs, float mc, const int *ex, int ex_cnt,
-                                               int &ep, float (&out)[Elt<T>::VEC])
+__device__ __noinline__ uint4 load_partial(const T *row, int64_t col, int64_t c0, int64_t c1)
+{
+    constexpr int VEC = Elt<T>::VEC;
+    uint32_t w[4];
+    if (sizeof(T) == 2) {
+        const unsigned short *r16 = reinterpret_cast<const unsigned short *>(row);
+        for (int i = 0; i < 4; ++i) {
+            const int64_t a = col + 2 * i, b = a + 1;
+            const uint32_t lo = (a >= c0 && a < c1) ? __ldg(r16 + a) : 0xff80u;
+            const uint32_t hi = (b >= c0 && b < c1) ? __ldg(r16 + b) : 0xff80u;
+            w[i] = lo | (hi << 16);
+        }
+    } else {
+        const uint32_t *r32 = reinterpret_cast<const uint32_t *>(row);
+        for (int i = 0; i < VEC; ++i) {
+            const int64_t a = col + i;
+            w[i] = (a >= c0 && a < c1) ? __ldg(r32 + a) : 0xff800000u;
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Weights of one vector at column col with no excluded column in it; elements outside [c0, c1)
+// weigh 0 (only the range's first and last vectors have such elements).
+template <typename T>
+__device__ __forceinline__ void vec_weights_plain(const uint4 &w, int col, int c0, int c1, float cs,
+                                                  float mc, float (&out)[Elt<T>::VEC])
 {
     constexpr int VEC = Elt<T>::VEC;
     float x[VEC];
     Elt<T>::unpack(w, x);
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-        const float e = ex2(fmaf(x[j], cs, -mc));
-        out[j] = (i0 + j >= lo && i0 + j < hi) ? e : 0.f;
-    }
-    while (ep < ex_cnt && ex[ep] < col0) ++ep;
-    for (int e = ep; e < ex_cnt && ex[e] < col0 + VEC; ++e) {
+    for (int j = 0; j < VEC; ++j) out[j] = ex2(fmaf(x[j], cs, -mc));
+    if (col < c0 || col + VEC > c1) {
 #pragma unroll
         for (int j = 0; j < VEC; ++j)
-            if (col0 + j == ex[e]) out[j] = 0.f;
+            if (col + j < c0 || col + j >= c1) out[j] = 0.f;
     }
 }
 
-// First column of [sg.c0, sg.c1) where cum0 + running weight exceeds t; the last column with
-// positive weight if none does (t = +inf asks for that).  All threads of the CTA call it.
-template <typename T, int NTR>
-__device__ int rescan_segment(const T *row, const Seg &sg, float cs, float mc, float t, float cum0,
-                              const int *ex, int ex_cnt, unsigned char *stage_bytes,
-                              RescanSmem &R)
+// The same with the excluded columns ex[e0..e1) (sorted) of this lane's run zeroed as well.
+template <typename T>
+__device__ __forceinline__ void vec_weights_ex(const uint4 &w, int col, int c0, int c1, float cs,
+                                               float mc, const int *ex, int e0, int e1,
+                                               float (&out)[Elt<T>::VEC])
 {
     constexpr int VEC = Elt<T>::VEC;
-    constexpr int NWR = NTR / 32;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    T *stage = reinterpret_cast<T *>(stage_bytes);
-    const int c0 = (int)sg.c0, c1 = (int)sg.c1, b0 = (int)sg.b0, b1 = (int)sg.b1;
-    const int nbody = (b1 - b0) / VEC;
-    const int npass = nbody > 0 ? (nbody + RESCAN_VEC - 1) / RESCAN_VEC : 1;
-    if (tid == 0) {
-        R.cum = cum0;
-        R.found = -1;
-        R.lastpos = -1;
+    vec_weights_plain<T>(w, col, c0, c1, cs, mc, out);
+    for (int e = e0; e < e1; ++e) {
+        const int d = ex[e] - col;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            if (j == d) out[j] = 0.f;
     }
+}
+
+struct RescanSmem {
+    float wsum[32];  // per-warp totals
+    int first;       // lowest thread whose running weight crosses t
+    int last;        // highest thread with positive weight
+    int found;
+};
+
+// First column y of [c0, c1) at which cum0 + (running weight up to and including y) exceeds t;
+// when none does (t = +inf asks for that), the last column with positive weight; -1 if no weight
+// is positive.  Child tokens ex[0..ex_n) (sorted) weigh 0.  row points at column 0 of the row;
+// rowflat is the row's first element in the flat logits array of `total` elements, whose base is
+// mis elements past a 16-byte boundary.  stage holds RESCAN_STAGE_VEC shared vectors.  Every
+// thread of the CTA calls it and gets the result.
+template <typename T>
+__device__ int block_rescan(const T *row, int64_t rowflat, int64_t total, int mis, int c0, int c1,
+                            float cs, float mc, float t, float cum0, const int *ex, int ex_n,
+                            uint4 *stage, RescanSmem &S)
+{
+    constexpr int VEC = Elt<T>::VEC;
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+    const int a0 = c0 - (int)((rowflat + c0 + mis) % VEC);  // aligned-down start column
+    const int nvv = (c1 - a0 + VEC - 1) / VEC;
+    // Whole aligned vectors are copied even where they stick out of [c0, c1) (the weights mask
+    // those elements); only a vector that would reach outside the logits array is read element
+    // by element.
+    for (int i = tid; i < nvv; i += nt) {
+        const int col = a0 + i * VEC;
+        const int64_t f = rowflat + col;
+        if (f >= 0 && f + VEC <= total) cp_async16(stage + i, row + col);
+        else stage[i] = load_partial<T>(row, col, c0, c1);
+    }
+    if (tid == 0) {
+        S.first = INT_MAX;
+        S.last = -1;
+        S.found = -1;
+    }
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-#pragma unroll 1
-    for (int pass = 0; pass < npass; ++pass) {
-        const int v0 = pass * RESCAN_VEC;
-        const int nv = min(RESCAN_VEC, nbody - v0 > 0 ? nbody - v0 : 0);
-        const bool first = pass == 0, last = pass == npass - 1;
-        const int cb0 = b0 + v0 * VEC;          // column at stage index VEC
-        const int nhead = first ? b0 - c0 : 0;  // < VEC
-        const int ntail = last ? c1 - b1 : 0;   // < VEC
-        for (int v = tid; v < nv; v += NTR) cp_async16(stage + VEC + v * VEC, row + cb0 + v * VEC);
-        if (tid < nhead) stage[VEC - nhead + tid] = row[c0 + tid];
-        if (tid < ntail) stage[VEC + nv * VEC + tid] = row[b1 + tid];
-        asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-        __syncthreads();
-        const int lo = VEC - nhead, hi = VEC + nv * VEC + ntail;
-        const int colbase = cb0 - VEC;          // column of stage index 0
-        const uint4 *sv = reinterpret_cast<const uint4 *>(stage_bytes);
-        const int nsv = (hi + VEC - 1) / VEC;   // stage vectors holding [lo, hi)
-        const int per = (nsv + NTR - 1) / NTR;
-        const int v0s = min(tid * per, nsv), v1s = min(v0s + per, nsv);
-        int ep = 0, lastpos = -1;
-        float own = 0.f;
-#pragma unroll 1
-        for (int v = v0s; v < v1s; ++v) {
-            float w[VEC];
-            staged_weights<T>(sv[v], v * VEC, lo, hi, colbase + v * VEC, cs, mc, ex, ex_cnt, ep, w);
+    // Each thread weighs a contiguous run of odd length (conflict-free 16-byte shared reads).
+    const int per = ((nvv + nt - 1) / nt) | 1;
+    const int k0 = min(tid * per, nvv), k1 = min(k0 + per, nvv);
+    const int lc0 = a0 + k0 * VEC, lc1 = a0 + k1 * VEC;
+    int e0 = 0;
+    while (e0 < ex_n && ex[e0] < lc0) ++e0;
+    int e1 = e0;
+    while (e1 < ex_n && ex[e1] < lc1) ++e1;
+    float own = 0.f;
+    for (int k = k0; k < k1; ++k) {
+        float e[VEC];
+        vec_weights_ex<T>(stage[k], a0 + k * VEC, c0, c1, cs, mc, ex, e0, e1, e);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) own += e[j];
+    }
+    // Block scan of the thread totals.
+    const float incl = warp_incl_scan(own, lane);
+    if (lane == 31) S.wsum[warp] = incl;
+    __syncthreads();
+    const float ws = lane < nw ? S.wsum[lane] : 0.f;
+    const float wi = warp_incl_scan(ws, lane);
+    const float cum = cum0 + __shfl_sync(0xffffffffu, wi - ws, warp);
+    if (cum + incl > t) atomicMin(&S.first, tid);
+    if (own > 0.f) atomicMax(&S.last, tid);
+    __syncthreads();
+    const bool take_last = S.first == INT_MAX;
+    const int who = take_last ? S.last : S.first;
+    if (tid == who) {
+        // Walk the run: the first crossing, or (take_last, or rounding) the last positive column.
+        float c = cum + incl - own;
+        int found = -1, lp = -1;
+        for (int k = k0; k < k1 && found < 0; ++k) {
+            const int col = a0 + k * VEC;
+            float e[VEC];
+            vec_weights_ex<T>(stage[k], col, c0, c1, cs, mc, ex, e0, e1, e);
 #pragma unroll
             for (int j = 0; j < VEC; ++j) {
-                if (w[j] > 0.f) lastpos = colbase + v * VEC + j;
-                own += w[j];
-            }
-        }
-        // Block scan of the shares.
-        float incl = own;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
-        }
-        if (lane == 31) R.wsum[warp] = incl;
-        for (int off = 16; off > 0; off >>= 1) lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, off));
-        if (lane == 0 && lastpos >= 0) atomicMax(&R.lastpos, lastpos);
-        if (tid == 0) R.first = NTR;
-        __syncthreads();
-        float wpre = 0.f, tot = 0.f;
-        for (int w = 0; w < NWR; ++w) {
-            if (w < warp) wpre += R.wsum[w];
-            tot += R.wsum[w];
-        }
-        float exw = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane == 0) exw = 0.f;
-        const float cum = R.cum;
-        const float excl = cum + wpre + exw;
-        if (cum + wpre + incl > t) atomicMin(&R.first, tid);
-        __syncthreads();
-        if (tid == R.first) {
-            float c = excl;
-            int found = -1, lp = -1, e2 = 0;
-#pragma unroll 1
-            for (int v = v0s; v < v1s && found < 0; ++v) {
-                float w[VEC];
-                staged_weights<T>(sv[v], v * VEC, lo, hi, colbase + v * VEC, cs, mc, ex, ex_cnt, e2, w);
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    if (found < 0 && w[j] > 0.f) {
-                        lp = colbase + v * VEC + j;
-                        c += w[j];
-                        if (c > t) found = lp;
-                    }
+                if (found < 0 && e[j] > 0.f) {
+                    lp = col + j;
+                    c += e[j];
+                    if (!take_last && c > t) found = lp;
                 }
             }
-            R.found = found >= 0 ? found : lp;
         }
-        if (tid == 0) R.total = cum + tot;
-        __syncthreads();
-        if (R.found >= 0) break;
-        if (tid == 0) R.cum = R.total;
-        __syncthreads();
+        S.found = found >= 0 ? found : lp;
     }
-    return R.found >= 0 ? R.found : R.lastpos;
+    __syncthreads();
+    return S.found;
 }
 
 }  // namespace sv

@@ -10,10 +10,11 @@
 namespace sv {
 
 #ifndef SV_VPL
-#define SV_VPL 4
+#define SV_VPL 8
 #endif
 constexpr int VPL = SV_VPL;            // 16-byte vectors per lane per step
 constexpr int STEP_VEC = 32 * VPL;     // vectors per warp step
+static_assert(SUB_VEC % STEP_VEC == 0, "a sub-record spans whole steps");
 
 // ---------------------------------------------------------------------------------------------
 // Packed fp32 pairs (sm_100+ f32x2 arithmetic): half the FMA-pipe instructions per element.
@@ -115,62 +116,62 @@ __device__ __forceinline__ uint4 neg_inf_vec()
     return make_uint4(n, n, n, n);
 }
 
-// Fold one 16-byte vector at column col into the sums; child tokens are zeroed and captured.
+// Element j of a 16-byte vector, which is then replaced by -inf (so that it adds nothing to the
+// sums and does not raise the running maximum).
 template <typename T>
-__device__ __forceinline__ void sample_vec(SampleAcc &a, const uint4 &w, int col, float cs,
-                                           uint64_t cs2, uint64_t nmc2, ExCursor &ex)
+__device__ __forceinline__ float take_element(uint4 &w, int j)
 {
-    constexpr int VEC = Elt<T>::VEC;
-    constexpr int NP = VEC / 2;
-    uint64_t e[NP];
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-        uint64_t x2;
-        if (VEC == 8) x2 = f2(bf_lo(ww[p]), bf_hi(ww[p]));
-        else x2 = f2(__uint_as_float(ww[2 * p]), __uint_as_float(ww[2 * p + 1]));
-        const float2 z = f2_split(f2_fma(x2, cs2, nmc2));
-        e[p] = f2(ex2(z.x), ex2(z.y));
+    const int wi = sizeof(T) == 2 ? (j >> 1) : j;
+    uint32_t word = wi == 0 ? w.x : wi == 1 ? w.y : wi == 2 ? w.z : w.w;
+    float x;
+    if (sizeof(T) == 2) {
+        const bool hi = (j & 1) != 0;
+        x = hi ? bf_hi(word) : bf_lo(word);
+        word = hi ? ((word & 0x0000ffffu) | 0xff800000u) : ((word & 0xffff0000u) | 0x0000ff80u);
+    } else {
+        x = __uint_as_float(word);
+        word = 0xff800000u;
     }
-    if (col + VEC > ex.next) {
-        // Rare: a child token lies in this vector (or was passed by this lane).
-        float x[VEC], s[VEC];
-        Elt<T>::unpack(w, x);
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) s[j] = ex2(fmaf(x[j], cs, -a.mc));
-        while (ex.next < col + VEC) {
-            if (ex.next >= col) {
-                float xv = 0.f;
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    if (col + j == ex.next) {
-                        s[j] = 0.f;
-                        xv = x[j];
-                    }
-                }
-                ex.caps[ex.node[ex.ptr]] = xv;
-            }
-            ex.advance();
-        }
-#pragma unroll
-        for (int p = 0; p < NP; ++p) e[p] = f2(s[2 * p], s[2 * p + 1]);
-    }
-#pragma unroll
-    for (int p = 0; p < NP; ++p) a.acc[p & 3] = f2_add(a.acc[p & 3], e[p]);
+    if (wi == 0) w.x = word;
+    else if (wi == 1) w.y = word;
+    else if (wi == 2) w.z = word;
+    else w.w = word;
+    return x;
 }
 
+// Rare: a child token lies in this lane's step (or the cursor still points before it).  Capture
+// each child's logit and mask it out of the vectors; filler vectors (step index >= nv) belong to
+// the next segment and are left alone.
+template <typename T>
+__device__ __forceinline__ void exclude_children(uint4 (&w)[VPL], int nv, int col0, int lane, ExCursor &ex)
+{
+    constexpr int VEC = Elt<T>::VEC;
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+        if (lane + 32 * u < nv) {
+            const int col = col0 + u * 32 * VEC;
+            while (ex.next < col + VEC) {
+                if (ex.next >= col) ex.caps[ex.node[ex.ptr]] = take_element<T>(w[u], ex.next - col);
+                ex.advance();
+            }
+        }
+    }
+}
+
+// One element outside the vector body (segment head or tail); a child token is captured instead.
 __device__ __forceinline__ void sample_scalar(SampleAcc &a, float x, int col, float cs, ExCursor &ex)
 {
-    sample_rescale(a, x, cs);
-    float e = ex2(fmaf(x, cs, -a.mc));
+    bool child = false;
     while (ex.next <= col) {
         if (ex.next == col) {
-            e = 0.f;
+            child = true;
             ex.caps[ex.node[ex.ptr]] = x;
         }
         ex.advance();
     }
-    a.acc[0] = f2_add(a.acc[0], f2(e, 0.f));
+    if (child) return;
+    sample_rescale(a, x, cs);
+    a.acc[0] = f2_add(a.acc[0], f2(ex2(fmaf(x, cs, -a.mc)), 0.f));
 }
 
 __device__ __forceinline__ void greedy_scalar(GreedyAcc &a, float x, int col)
@@ -230,54 +231,108 @@ __device__ __forceinline__ void greedy_step(GreedyAcc &a, const uint4 (&w)[VPL],
     a.idx = found;
 }
 
-// Fold one step (VPL vectors per lane at columns col0 + u*32*VEC; those at step index >= nv are
-// fillers holding -inf, whose columns belong to the next warp's segment).
-template <typename T, bool SAMPLE>
-__device__ __forceinline__ void fold_step(const uint4 (&w)[VPL], int nv, int col0, int lane, float cs,
-                                          uint64_t cs2, ExCursor &ex, SampleAcc &sa, GreedyAcc &ga)
+// Fold a lane's step (child tokens already masked to -inf): no per-vector checks; filler and
+// masked elements add 2^-inf = 0 to the sums.
+template <typename T>
+__device__ __forceinline__ void sample_step_fast(SampleAcc &a, const uint4 (&w)[VPL], uint64_t cs2,
+                                                 uint64_t nmc2)
 {
-    constexpr int VEC = Elt<T>::VEC;
-    const float vmax = step_max<T>(w);
-    if (SAMPLE) {
-        sample_rescale(sa, vmax, cs);
-        const float nmc = -sa.mc;
-        const uint64_t nmc2 = f2(nmc, nmc);
+    constexpr int NP = Elt<T>::VEC / 2;
 #pragma unroll
-        for (int u = 0; u < VPL; ++u)
-            if (lane + 32 * u < nv) sample_vec<T>(sa, w[u], col0 + u * 32 * VEC, cs, cs2, nmc2, ex);
-    } else {
-        greedy_step<T>(ga, w, col0, vmax);
+    for (int u = 0; u < VPL; ++u) {
+        const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            uint64_t x2;
+            if (NP == 4) x2 = f2(bf_lo(ww[p]), bf_hi(ww[p]));
+            else x2 = f2(__uint_as_float(ww[2 * p]), __uint_as_float(ww[2 * p + 1]));
+            const float2 z = f2_split(f2_fma(x2, cs2, nmc2));
+            const int j = (u * NP + p) & 3;
+            a.acc[j] = f2_add(a.acc[j], f2(ex2(z.x), ex2(z.y)));
+        }
     }
 }
 
-// Stream the 16-byte aligned body [b0, b1) of a warp segment: two steps per lane in flight.
+// Fold one step (VPL vectors per lane at columns col0 + u*32*VEC; those at step index >= nv are
+// fillers holding -inf, whose columns belong to the next warp's segment).
 template <typename T, bool SAMPLE>
-__device__ __forceinline__ void stream_body(const T *row, int b0, int b1, int lane, float cs,
-                                            ExCursor &ex, SampleAcc &sa, GreedyAcc &ga)
+__device__ __forceinline__ void fold_step(uint4 (&w)[VPL], int nv, int col0, int lane, float cs,
+                                          uint64_t cs2, ExCursor &ex, SampleAcc &sa, GreedyAcc &ga)
+{
+    constexpr int VEC = Elt<T>::VEC;
+    if (SAMPLE) {
+        // Last column this lane's step covers, fillers included.
+        const int last = col0 + ((VPL - 1) * 32 + 1) * VEC - 1;
+        if (ex.next <= last) exclude_children<T>(w, nv, col0, lane, ex);
+        sample_rescale(sa, step_max<T>(w), cs);
+        const float nmc = -sa.mc;
+        sample_step_fast<T>(sa, w, cs2, f2(nmc, nmc));
+    } else {
+        greedy_step<T>(ga, w, col0, step_max<T>(w));
+    }
+}
+
+// Flush the warp's accumulators into record `idx` (lane 0 writes it) and restart the sums; a
+// lane keeps its reference mc, so later records stay in the same scaled domain per lane.  A
+// sampling record also carries the columns [c0, c1) it covers.
+template <bool SAMPLE>
+__device__ __forceinline__ void flush_record(float4 *recs, int64_t idx, int lane, SampleAcc &sa,
+                                             GreedyAcc &ga, int c0, int c1)
+{
+    float4 rec;
+    if (SAMPLE) {
+        float mc = sa.mc, sum = sa.total();
+        warp_rec_merge(mc, sum);
+        rec = make_float4(mc, sum, __int_as_float(c0), __int_as_float(c1));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sa.acc[j] = 0;
+    } else {
+        float v = ga.best;
+        int i = ga.idx;
+        warp_arg_merge(v, i);
+        rec = make_float4(v, __int_as_float(i), 0.f, 0.f);
+        ga.best = NEG_INF;
+        ga.idx = INT_MAX;
+    }
+    if (lane == 0) recs[idx] = rec;
+}
+
+// One lane's loads of a step: vectors p[32*u]; with CHECK, those at 32*u >= lim are -inf fillers.
+template <typename T, bool CHECK>
+__device__ __forceinline__ void load_step(uint4 (&d)[VPL], const uint4 *p, int lim)
+{
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) d[u] = (!CHECK || 32 * u < lim) ? ldg_stream(p + 32 * u) : neg_inf_vec<T>();
+}
+
+// Stream the 16-byte aligned body [b0, b1) of a warp segment that starts at column c0 (its
+// unaligned head, already folded, is [c0, b0)), VPL loads per lane per step.  After every SUB_VEC
+// vectors but the last sub-range, the sub-range's record is flushed to recs[idx0 + k].
+template <typename T, bool SAMPLE>
+__device__ __forceinline__ void stream_body(const T *row, int c0, int b0, int b1, int lane, float cs,
+                                            ExCursor &ex, SampleAcc &sa, GreedyAcc &ga,
+                                            float4 *recs, int64_t idx0)
 {
     constexpr int VEC = Elt<T>::VEC;
     const int nvec = (b1 - b0) / VEC;
     if (nvec <= 0) return;
-    const uint4 *vp = reinterpret_cast<const uint4 *>(row + b0);
+    const uint4 *vp = reinterpret_cast<const uint4 *>(row + b0) + lane;
     const int nst = (nvec + STEP_VEC - 1) / STEP_VEC;
+    const int nfull = nvec / STEP_VEC;  // steps whose vectors are all inside the segment
     const uint64_t cs2 = f2(cs, cs);
-    uint4 cur[VPL], nxt[VPL];
-#pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-        const int v = lane + 32 * u;
-        cur[u] = v < nvec ? ldg_stream(vp + v) : neg_inf_vec<T>();
-    }
+    uint4 cur[VPL];
     for (int s = 0; s < nst; ++s) {
-        const int nb = (s + 1) * STEP_VEC + lane;
-#pragma unroll
-        for (int u = 0; u < VPL; ++u) {
-            const int v = nb + 32 * u;
-            nxt[u] = v < nvec ? ldg_stream(vp + v) : neg_inf_vec<T>();
-        }
+        // All of a step's loads are issued together; the other warps of the SM cover their latency.
+        if (s < nfull) load_step<T, false>(cur, vp + s * STEP_VEC, 0);
+        else load_step<T, true>(cur, vp + s * STEP_VEC, nvec - s * STEP_VEC - lane);
         const int nv = min(STEP_VEC, nvec - s * STEP_VEC);
         fold_step<T, SAMPLE>(cur, nv, b0 + (s * STEP_VEC + lane) * VEC, lane, cs, cs2, ex, sa, ga);
-#pragma unroll
-        for (int u = 0; u < VPL; ++u) cur[u] = nxt[u];
+        constexpr int STEPS_PER_SUB = SUB_VEC / STEP_VEC;
+        if ((s + 1) % STEPS_PER_SUB == 0 && s + 1 < nst) {
+            const int k = (s + 1) / STEPS_PER_SUB - 1;
+            flush_record<SAMPLE>(recs, idx0 + k, lane, sa, ga, k == 0 ? c0 : b0 + k * SUB_VEC * VEC,
+                                 b0 + (k + 1) * SUB_VEC * VEC);
+        }
     }
 }
 
