@@ -876,7 +876,7 @@ static int residual_chunks(int B, int64_t V)
 }
 
 struct Layout {
-    size_t cnt1, cnt2, recs, caps, pend, recs2, total;
+    size_t cnt2, recs, caps, pend, recs2, total;
 };
 
 // Split the flat range: one CTA per resident slot of a GB300 (152 SMs x 3 streaming CTAs), but
@@ -897,10 +897,12 @@ static void plan_split(int64_t total, int64_t &E, int &G)
 }
 
 // Sub-records per warp segment: a warp flushes a record every SUB_VEC vectors of its segment,
-// so the draw rescans at most SUB_VEC vectors.  vec = elements per 16-byte vector.
-static int nsub_of(int64_t E, int vec)
+// so the draw rescans at most SUB_VEC vectors.  A segment lies inside one piece (one row's part
+// of one CTA's range), so it holds at most min(E, V) elements.  vec = elements per 16-byte vector.
+static int nsub_of(int64_t E, int64_t V, int vec)
 {
-    const int64_t per_warp = ((E + vec - 1) / vec + 2 + NW - 1) / NW;
+    const int64_t piece = E < V ? E : V;
+    const int64_t per_warp = ((piece + vec - 1) / vec + 2 + NW - 1) / NW;
     int64_t n = (per_warp + SUB_VEC - 1) / SUB_VEC;
     return (int)(n < 1 ? 1 : n);
 }
@@ -915,11 +917,9 @@ static Layout layout(int B, int rpr, int64_t V)
     int64_t E;
     int G;
     plan_split(R * V, E, G);
-    const int nsub = nsub_of(E, 4);  // fp32 logits need the most sub-records
+    const int nsub = nsub_of(E, V, 4);  // fp32 logits need the most sub-records
     Layout L;
     size_t off = 0;
-    L.cnt1 = off;
-    off += sizeof(unsigned) * (size_t)B_MAX;
     L.cnt2 = off;
     off += sizeof(unsigned) * (size_t)B_MAX;
     L.recs = off;
@@ -987,9 +987,8 @@ static int common_setup(Params &P, const void *logits, int dtype, int B, int rpr
     P.V = V;
     P.total = (int64_t)B * rpr * V;
     plan_split(P.total, P.E, P.G);
-    P.nsub = nsub_of(P.E, esize == 2 ? 8 : 4);
+    P.nsub = nsub_of(P.E, V, esize == 2 ? 8 : 4);
     P.mis = (int)(((uintptr_t)logits % 16) / esize);
-    P.cnt1 = reinterpret_cast<unsigned *>(ws + L.cnt1);
     P.cnt2 = reinterpret_cast<unsigned *>(ws + L.cnt2);
     P.recs = reinterpret_cast<float4 *>(ws + L.recs);
     P.caps = reinterpret_cast<float *>(ws + L.caps);
@@ -1237,8 +1236,7 @@ extern "C" int spec_verify_rejection_noalloc(const void *logits, int dtype,
     const Layout L = layout(B, k + 1, V);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *base = static_cast<char *>(scratch);
-    if (cudaMemsetAsync(base + L.cnt1, 0, sizeof(unsigned) * (size_t)B, s) != cudaSuccess ||
-        cudaMemsetAsync(base + L.cnt2, 0, sizeof(unsigned) * (size_t)B, s) != cudaSuccess)
+    if (cudaMemsetAsync(base + L.cnt2, 0, sizeof(unsigned) * (size_t)B, s) != cudaSuccess)
         return SPEC_VERIFY_ECUDA;
     return spec_verify_rejection(logits, dtype, draft_ids, draft_probs, B, k, V, temperature, seed,
                                  offset, out_tokens, accept_len, out_probs, scratch,

@@ -46,7 +46,6 @@ struct Params {
     float *out_probs;            // chain [B][k+1][3] or null
     int32_t *dev_status;         // or null
     // workspace
-    unsigned *cnt1;              // [B] arrivals at the streaming kernel's per-request counter
     unsigned *cnt2;              // [B] arrivals at the residual kernel's counter
     float4 *recs;                // [(G + R) * NW * nsub] per (piece, warp, sub) records
     float *caps;                 // [B * rpr] logit of node j's token in its parent's row
