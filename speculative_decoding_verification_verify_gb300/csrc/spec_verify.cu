@@ -134,36 +134,47 @@ __device__ void build_children(const Params &P, int b, int n, int *ex_col, int *
 }
 
 // ---------------------------------------------------------------------------------------------
-// One warp streams its segment [c0, c1) of a row: the unaligned head and tail element by element,
-// the 16-byte aligned body with vector loads.  Each lane visits its columns in ascending order.
+// One warp streams its segment [c0, c1) of row r = (request b, node n): the unaligned head and
+// tail (fewer than VEC elements each) element by element, the 16-byte aligned body with vector
+// loads.  The body's first step and the head and tail elements are loaded before anything else,
+// so the child list is built while they are in flight.  Each lane visits its columns in
+// ascending order.
 // ---------------------------------------------------------------------------------------------
 template <typename T, bool SAMPLE>
-__device__ __forceinline__ void stream_segment(const T *row, const Seg &sg, int lane, float cs,
-                                               ExCursor &ex, float4 *recs, int64_t idx0, int nsub)
+__device__ __forceinline__ void stream_segment(const Params &P, const T *row, const Seg &sg, int b, int n,
+                                               int lane, int *ex_col, int *ex_node, int *ex_cnt,
+                                               int64_t idx0)
 {
+    const float cs = P.cs;
+    const int c0 = (int)sg.c0, b0 = (int)sg.b0, b1 = (int)sg.b1, c1 = (int)sg.c1;
+    uint4 cur[VPL];
+    load_first_step<T>(cur, row, b0, b1, lane);
+    const bool has_head = c0 + lane < b0, has_tail = b1 + lane < c1;
+    const float xh = has_head ? Elt<T>::load(row, c0 + lane) : 0.f;
+    const float xt = has_tail ? Elt<T>::load(row, b1 + lane) : 0.f;
+    if (SAMPLE) build_children(P, b, n, ex_col, ex_node, ex_cnt, lane);
+    ExCursor ex;
+    ex.init(ex_col, ex_node, SAMPLE ? *ex_cnt : 0, P.caps + (int64_t)b * P.rpr);
     SampleAcc sa;
     GreedyAcc ga;
-    for (int c = (int)sg.c0 + lane; c < (int)sg.b0; c += 32) {
-        const float x = Elt<T>::load(row, c);
-        if (SAMPLE) sample_scalar(sa, x, c, cs, ex);
-        else greedy_scalar(ga, x, c);
+    if (has_head) {
+        if (SAMPLE) sample_scalar(sa, xh, c0 + lane, cs, ex);
+        else greedy_scalar(ga, xh, c0 + lane);
     }
-    stream_body<T, SAMPLE>(row, (int)sg.c0, (int)sg.b0, (int)sg.b1, lane, cs, ex, sa, ga, recs, idx0);
-    for (int c = (int)sg.b1 + lane; c < (int)sg.c1; c += 32) {
-        const float x = Elt<T>::load(row, c);
-        if (SAMPLE) sample_scalar(sa, x, c, cs, ex);
-        else greedy_scalar(ga, x, c);
+    stream_body<T, SAMPLE>(row, c0, b0, b1, lane, cs, ex, sa, ga, P.recs, idx0, cur);
+    if (has_tail) {
+        if (SAMPLE) sample_scalar(sa, xt, b1 + lane, cs, ex);
+        else greedy_scalar(ga, xt, b1 + lane);
     }
-    const int nvec = (int)((sg.b1 - sg.b0) / Elt<T>::VEC);
+    const int nvec = (b1 - b0) / Elt<T>::VEC;
     const int used = nvec > 0 ? (nvec + SUB_VEC - 1) / SUB_VEC : 1;
     const int k = used - 1;
-    flush_record<SAMPLE>(recs, idx0 + k, lane, sa, ga,
-                         k == 0 ? (int)sg.c0 : (int)sg.b0 + k * SUB_VEC * Elt<T>::VEC, (int)sg.c1);
+    flush_record<SAMPLE>(P.recs, idx0 + k, lane, sa, ga, k == 0 ? c0 : b0 + k * SUB_VEC * Elt<T>::VEC, c1);
     // Sub-slots this segment does not reach hold empty records.
     if (lane == 0)
-        for (int k2 = used; k2 < nsub; ++k2)
-            recs[idx0 + k2] = SAMPLE ? make_float4(REF_NONE, 0.f, 0.f, 0.f)
-                                    : make_float4(NEG_INF, __int_as_float(INT_MAX), 0.f, 0.f);
+        for (int k2 = used; k2 < P.nsub; ++k2)
+            P.recs[idx0 + k2] = SAMPLE ? make_float4(REF_NONE, 0.f, 0.f, 0.f)
+                                       : make_float4(NEG_INF, __int_as_float(INT_MAX), 0.f, 0.f);
 }
 
 __device__ __forceinline__ void draw_init(DrawSmem &D, float cum)
@@ -329,12 +340,25 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
     __syncthreads();
 }
 
-// Row n of request b, by one warp, once the records are visible.
+// What a warp keeps between merging a row's records and locating the draw's crossing in them.
+struct RowState {
+    float4 rr[REC_PER_LANE];  // a lane's contiguous run of q records (when inreg)
+    int64_t base;             // first record index of the row
+    int L, q, off, cnt;       // records, records per lane, the row's children (ex_off, ex_n)
+    bool inreg, bad;
+    float mc, s, M, esum;     // non-child mass s * 2^mc; reference M covering the children too
+};
+
+// Row n of request b, by one warp, once the records are visible: merge the records, weigh the
+// row's children.
 template <typename T, bool SAMPLE>
-__device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane)
+__device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, RowState &rs)
 {
-    const int64_t base = F.row_base[n];
-    const int L = F.row_L[n];
+    rs.base = F.row_base[n];
+    rs.L = F.row_L[n];
+    rs.bad = true;
+    const int64_t base = rs.base;
+    const int L = rs.L;
     if (!SAMPLE) {
         float best = NEG_INF;
         int idx = INT_MAX;
@@ -354,6 +378,8 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane)
     // a contiguous run of q records; runs of up to REC_PER_LANE stay in registers for the draw's
     // locate step.
     const int off = F.ex_off[n], cnt = F.ex_n[n];
+    rs.off = off;
+    rs.cnt = cnt;
     float cap[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -361,17 +387,17 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane)
         cap[h] = e < cnt ? __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[off + e]) : NEG_INF;
     }
     const int q = (L + 31) >> 5;
-    const bool inreg = q <= REC_PER_LANE;
-    float4 rr[REC_PER_LANE];
+    rs.q = q;
+    rs.inreg = q <= REC_PER_LANE;
     float mc = REF_NONE, s = 0.f;
-    if (inreg) {
+    if (rs.inreg) {
 #pragma unroll
         for (int i = 0; i < REC_PER_LANE; ++i) {
             const int t = lane * q + i;
-            rr[i] = (i < q && t < L) ? __ldcg(P.recs + base + t) : make_float4(REF_NONE, 0.f, 0.f, 0.f);
+            rs.rr[i] = (i < q && t < L) ? __ldcg(P.recs + base + t) : make_float4(REF_NONE, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int i = 0; i < REC_PER_LANE; ++i) rec_merge(mc, s, rr[i].x, rr[i].y);
+        for (int i = 0; i < REC_PER_LANE; ++i) rec_merge(mc, s, rs.rr[i].x, rs.rr[i].y);
     } else {
         for (int t = lane; t < L; t += 32) {
             const float4 rec = __ldcg(P.recs + base + t);
@@ -400,6 +426,11 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane)
     for (int h = 0; h < 2; ++h)
         if (lane + 32 * h < cnt) F.node_p[F.ex_node[off + lane + 32 * h]] = ec[h] / tot;
     const bool bad = !(s >= 0.f) || !(s < POS_INF) || !(tot > 0.f) || !(tot < POS_INF);
+    rs.bad = bad;
+    rs.mc = mc;
+    rs.s = s;
+    rs.M = M;
+    rs.esum = esum;
     if (lane == 0) {
         F.row_mc[n] = mc;
         F.row_S[n] = s;
@@ -410,24 +441,27 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane)
         F.rs_ok[n] = 0;
         if (bad) atomicMax(&F.status, SPEC_VERIFY_DEV_BAD_ROW);
     }
-    if (bad || !F.need_draw[n]) return;
+}
 
-    // The row's draw: children excluded, threshold v * Z with Z the non-child mass.  Here only
-    // the record holding the crossing is located; the rescan of its columns waits until the stop
-    // row is known.
+// The row's draw, children excluded, threshold v * Z with Z the non-child mass: locate the
+// record holding the crossing (F.rs_*) for the rescan, or, when every non-child token is -inf,
+// draw among the children directly (F.cand).
+__device__ void row_draw_prep(const Params &P, int b, int n, FinSmem &F, int lane, const RowState &rs)
+{
     const float vdraw = F.v[P.is_tree ? F.dep[n] : n];
-    int drawn = -1;
+    const float s = rs.s, mc = rs.mc;
+    const int L = rs.L, q = rs.q;
     if (s > 0.f) {
         const float t = vdraw * s;
         int fi = -1;         // crossing record (relative to the row's first), or the last positive
         float before = 0.f;  // mass of the row's records before it
         bool take_last = false;
         float4 frec = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (inreg) {
+        if (rs.inreg) {
             float m[REC_PER_LANE], own = 0.f;
 #pragma unroll
             for (int i = 0; i < REC_PER_LANE; ++i) {
-                m[i] = rec_mass(rr[i], mc);
+                m[i] = rec_mass(rs.rr[i], mc);
                 own += m[i];
             }
             const float incl = warp_incl_scan(own, lane);
@@ -461,13 +495,13 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane)
                 }
 #pragma unroll
                 for (int i = 0; i < REC_PER_LANE; ++i)
-                    if (i == fi) frec = rr[i];
+                    if (i == fi) frec = rs.rr[i];
                 fi += lane * q;
             }
         } else {
             Locate Lc;
             for (int c0 = 0; c0 < L; c0 += 32) {
-                const float4 rec = c0 + lane < L ? __ldcg(P.recs + base + c0 + lane)
+                const float4 rec = c0 + lane < L ? __ldcg(P.recs + rs.base + c0 + lane)
                                                  : make_float4(REF_NONE, 0.f, 0.f, 0.f);
                 if (locate_chunk(Lc, rec_mass(rec, mc), c0, t, lane)) break;
             }
@@ -475,7 +509,7 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane)
                 fi = Lc.found >= 0 ? Lc.found : Lc.lastpos;
                 before = Lc.found >= 0 ? Lc.before : Lc.lp_before;
                 take_last = Lc.found < 0;
-                if (fi >= 0) frec = __ldcg(P.recs + base + fi);
+                if (fi >= 0) frec = __ldcg(P.recs + rs.base + fi);
             }
         }
         if (fi >= 0) {  // exactly one lane holds it
@@ -487,41 +521,30 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane)
         }
     } else if (lane == 0) {
         // Every non-child token is -inf: draw among the children by p, in column order.
-        const float tc = esum;
-        const float t = vdraw * tc;
+        const float t = vdraw * rs.esum;
         float c = 0.f;
-        int lastc = -1;
-        for (int e = 0; e < cnt && drawn < 0; ++e) {
-            const float cp = __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[off + e]);
-            const float w = ex2(fmaf(cp, cs, -M));
+        int lastc = -1, drawn = -1;
+        for (int e = 0; e < rs.cnt && drawn < 0; ++e) {
+            const float cp = __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[rs.off + e]);
+            const float w = ex2(fmaf(cp, P.cs, -rs.M));
             if (w > 0.f) {
-                lastc = F.ex_col[off + e];
+                lastc = F.ex_col[rs.off + e];
                 c += w;
                 if (c > t) drawn = lastc;
             }
         }
-        if (drawn < 0) drawn = lastc;
+        F.cand[n] = drawn >= 0 ? drawn : lastc;
     }
-    if (lane == 0) F.cand[n] = drawn;
 }
 
-template <typename T, bool SAMPLE>
-__device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stage)
+// Decide the accepted path and the stop node (warp 0 calls it; the tree walk runs in lane 0).
+template <bool SAMPLE>
+__device__ void decide_request(const Params &P, FinSmem &F, int lane)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwf = blockDim.x >> 5;
-    const int rpr = P.rpr;
-
-    stage_request<SAMPLE>(P, b, F);
-    // From here on the streaming kernel's records and captures are read.
-    pdl_wait();
-    for (int n = warp; n < rpr; n += nwf) finish_row<T, SAMPLE>(P, b, n, F, lane);
-    __syncthreads();
-
-    // Decide the accepted path and the stop node.
     if (F.status == 0) {
         if (!P.is_tree) {
             // Chain: the first draft slot that is not accepted stops the round (warp ballots).
-            if (warp == 0) {
+            {
                 const int k = P.k;
                 int j = k;
                 for (int c0 = 0; c0 < k; c0 += 32) {
@@ -549,7 +572,7 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
                     else F.mode = 1;
                 }
             }
-        } else if (tid == 0) {
+        } else if (lane == 0) {
             // Tree walk: one coin per depth, children in ascending node index.
             int cur = 0, depth = 0, L = 0;
             for (;;) {
@@ -584,7 +607,46 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
             F.mode = SAMPLE ? 1 : 0;
         }
     }
-    __syncthreads();
+}
+
+template <typename T, bool SAMPLE>
+__device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stage)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwf = blockDim.x >> 5;
+    const int rpr = P.rpr;
+
+    stage_request<SAMPLE>(P, b, F);
+    // From here on the streaming kernel's records and captures are read.
+    pdl_wait();
+    // With one row per warp, every warp also prefetches its row's crossing range into its own
+    // stage while warp 0 decides, so the stop row's rescan finds its columns in shared memory.
+    const bool prefetch = SAMPLE && rpr <= nwf;
+    if (rpr <= nwf) {
+        RowState rs;
+        if (warp < rpr) finish_row<T, SAMPLE>(P, b, warp, F, lane, rs);
+        __syncthreads();
+        if (SAMPLE && warp < rpr && !rs.bad && F.need_draw[warp]) {
+            row_draw_prep(P, b, warp, F, lane, rs);
+            __syncwarp();
+            if (F.rs_ok[warp]) {
+                const int64_t r = (int64_t)b * rpr + warp;
+                stage_range<T>(reinterpret_cast<const T *>(P.logits) + r * P.V, r * P.V, P.total, P.mis,
+                               F.rs_c0[warp], F.rs_c1[warp], stage + warp * RESCAN_STAGE_VEC, lane, 32);
+            }
+        }
+        if (warp == 0) decide_request<SAMPLE>(P, F, lane);
+        if (prefetch) cp_async_wait_all();
+        __syncthreads();
+    } else {
+        for (int n = warp; n < rpr; n += nwf) {
+            RowState rs;
+            finish_row<T, SAMPLE>(P, b, n, F, lane, rs);
+            if (SAMPLE && !rs.bad && F.need_draw[n]) row_draw_prep(P, b, n, F, lane, rs);
+        }
+        __syncthreads();
+        if (warp == 0) decide_request<SAMPLE>(P, F, lane);
+        __syncthreads();
+    }
     const bool faulted = F.status != 0;
 
     // Outputs.
@@ -612,10 +674,16 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
         int drawn = F.cand[stop];
         if (F.rs_ok[stop]) {
             const int64_t r = (int64_t)b * rpr + stop;
-            const T *row = reinterpret_cast<const T *>(P.logits) + r * P.V;
-            drawn = block_rescan<T>(row, r * P.V, P.total, P.mis, F.rs_c0[stop], F.rs_c1[stop], P.cs,
-                                    F.row_mc[stop], F.rs_t[stop], F.rs_cum[stop],
-                                    F.ex_col + F.ex_off[stop], F.ex_n[stop], stage, F.RS);
+            const uint4 *staged = stage + (prefetch ? stop : 0) * RESCAN_STAGE_VEC;
+            if (!prefetch) {
+                stage_range<T>(reinterpret_cast<const T *>(P.logits) + r * P.V, r * P.V, P.total, P.mis,
+                               F.rs_c0[stop], F.rs_c1[stop], stage, tid, blockDim.x);
+                cp_async_wait_all();
+                __syncthreads();
+            }
+            drawn = rescan_staged<T>(r * P.V, P.mis, F.rs_c0[stop], F.rs_c1[stop], P.cs, F.row_mc[stop],
+                                     F.rs_t[stop], F.rs_cum[stop], F.ex_col + F.ex_off[stop], F.ex_n[stop],
+                                     staged, F.RS);
         }
         last = drawn >= 0 ? drawn : 0;  // < 0 only through rounding
     }
@@ -665,17 +733,15 @@ __global__ void __launch_bounds__(NT, SV_MINB) sv_stream_kernel(const Params P)
     const int64_t F1 = min(F0 + P.E, P.total);
     pdl_launch_dependents();
     if (F0 >= F1) return;
-    const int64_t r_end = (F1 - 1) / V;
-    for (int64_t r = F0 / V; r <= r_end; ++r) {
-        const int b = (int)(r / P.rpr);
-        const int n = (int)(r - (int64_t)b * P.rpr);
+    const int64_t r_end = div_v(F1 - 1, V, P.v_inv);
+    for (int64_t r = div_v(F0, V, P.v_inv); r <= r_end; ++r) {
+        const int b = (int)r / P.rpr;  // rows < 2^31
+        const int n = (int)r - b * P.rpr;
         // Each warp keeps its own child list, so no warp waits for another at a row change.
-        if (SAMPLE) build_children(P, b, n, st.ex_col[warp], st.ex_node[warp], &st.ex_cnt[warp], lane);
         const Seg sg = seg_of<VEC>(P, g, r, warp);
         const T *row = reinterpret_cast<const T *>(P.logits) + r * V;
-        ExCursor ex;
-        ex.init(st.ex_col[warp], st.ex_node[warp], SAMPLE ? st.ex_cnt[warp] : 0, P.caps + (int64_t)b * P.rpr);
-        stream_segment<T, SAMPLE>(row, sg, lane, P.cs, ex, P.recs, ((g + r) * NW + warp) * P.nsub, P.nsub);
+        stream_segment<T, SAMPLE>(P, row, sg, b, n, lane, st.ex_col[warp], st.ex_node[warp], &st.ex_cnt[warp],
+                                  ((g + r) * NW + warp) * P.nsub);
     }
     (void)tid;
 }
@@ -687,8 +753,8 @@ template <typename T, bool SAMPLE>
 __global__ void __launch_bounds__(NT_FIN_MAX) sv_finalize_kernel(const Params P)
 {
     __shared__ FinSmem F;
-    __shared__ uint4 stage[SAMPLE ? RESCAN_STAGE_VEC : 1];
-    finalize_request<T, SAMPLE>(P, (int)blockIdx.x, F, stage);
+    extern __shared__ uint4 sv_fin_stage[];  // sampling: one rescan stage per warp
+    finalize_request<T, SAMPLE>(P, (int)blockIdx.x, F, sv_fin_stage);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -882,7 +948,10 @@ struct Layout {
 // Split the flat range: one CTA per resident slot of a GB300 (152 SMs x 3 streaming CTAs), but
 // never fewer than E_MIN elements each; E is a multiple of 64 elements so that CTA boundaries keep
 // 16-byte alignment.  The split depends only on the problem size, so the workspace size does too.
-constexpr int RESIDENT_CTAS = 152 * SV_MINB;
+#ifndef SV_WAVES
+#define SV_WAVES 1
+#endif
+constexpr int RESIDENT_CTAS = 152 * SV_MINB * SV_WAVES;
 
 static void plan_split(int64_t total, int64_t &E, int &G)
 {
@@ -960,6 +1029,12 @@ static const DevInfo *device_info()
         d.occ[1][0] = o > 0 ? o : 1;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_stream_kernel<float, true>, NT, 0);
         d.occ[1][1] = o > 0 ? o : 1;
+        const void *fin[2] = {(const void *)sv_finalize_kernel<__nv_bfloat16, true>,
+                              (const void *)sv_finalize_kernel<float, true>};
+        for (int i = 0; i < 2; ++i)
+            if (cudaFuncSetAttribute(fin[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)((NT_FIN_MAX / 32) * RESCAN_STAGE_VEC * sizeof(uint4))) != cudaSuccess)
+                return nullptr;
         cudaGetLastError();
         d.sms = sms;
     }
@@ -985,6 +1060,7 @@ static int common_setup(Params &P, const void *logits, int dtype, int B, int rpr
     P.B = B;
     P.rpr = rpr;
     P.V = V;
+    P.v_inv = 1.0 / (double)V;
     P.total = (int64_t)B * rpr * V;
     plan_split(P.total, P.E, P.G);
     P.nsub = nsub_of(P.E, V, esize == 2 ? 8 : 4);
@@ -1017,7 +1093,7 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
     cfg.gridDim = dim3((unsigned)P.B);
     const int nwf = P.rpr < NT_FIN_MAX / 32 ? P.rpr : NT_FIN_MAX / 32;
     cfg.blockDim = dim3(32u * (unsigned)nwf);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = SAMPLE ? (size_t)nwf * RESCAN_STAGE_VEC * sizeof(uint4) : 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -34,6 +34,7 @@ struct Params {
     const int32_t *parents;      // tree: [B][N]
     int B, k, rpr, is_tree;
     int64_t V;
+    double v_inv;                // 1 / V, for quick exact division by V
     float cs;                    // log2(e) / T: p is proportional to 2^(logit * cs)
     uint32_t key0, key1, off0, off1;
     int64_t total;               // B * rpr * V
@@ -103,6 +104,29 @@ __device__ __forceinline__ void pdl_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+// floor(x / P.V) for 0 <= x < 2^52: a double-precision estimate, then an exact correction.
+__device__ __forceinline__ int64_t div_v(int64_t x, int64_t V, double v_inv)
+{
+    int64_t q = (int64_t)((double)x * v_inv);
+    if (q * V > x) --q;
+    else if ((q + 1) * V <= x) ++q;
+    return q;
+}
+
+// 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned), in the thread's
+// current cp.async group.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gsrc)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 __device__ __forceinline__ void raise_status(int32_t *st, int code)
 {

@@ -21,14 +21,6 @@ namespace sv {
 // partial one at each end.
 constexpr int RESCAN_STAGE_VEC = SUB_VEC + 2;
 
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                     (uint32_t)__cvta_generic_to_shared(smem_dst)),
-                 "l"(gsrc)
-                 : "memory");
-}
-
 // The 16-byte vector of a row starting at column col, with the elements outside [c0, c1) read
 // as -inf, element by element, so that no byte outside [c0, c1) is touched.
 template <typename T>
@@ -90,42 +82,48 @@ __device__ __forceinline__ void vec_weights_ex(const uint4 &w, int col, int c0, 
 
 struct RescanSmem {
     float wsum[32];  // per-warp totals
-    int first;       // lowest thread whose running weight crosses t
-    int last;        // highest thread with positive weight
     int found;
 };
 
-// First column y of [c0, c1) at which cum0 + (running weight up to and including y) exceeds t;
-// when none does (t = +inf asks for that), the last column with positive weight; -1 if no weight
-// is positive.  Child tokens ex[0..ex_n) (sorted) weigh 0.  row points at column 0 of the row;
-// rowflat is the row's first element in the flat logits array of `total` elements, whose base is
-// mis elements past a 16-byte boundary.  stage holds RESCAN_STAGE_VEC shared vectors.  Every
-// thread of the CTA calls it and gets the result.
+// Copy the vectors covering columns [c0, c1) of a row into stage: vector i starts at column
+// a0 + i*VEC, a0 being c0 rounded down to a 16-byte boundary (row points at column 0; rowflat is
+// the row's first element in the flat logits array of `total` elements, whose base is mis
+// elements past a 16-byte boundary).  Whole aligned vectors are copied even where they stick out
+// of [c0, c1) (the weights mask those elements); only a vector that would reach outside the
+// logits array is read element by element.  Threads t = 0..nt-1 share the copies; each thread
+// commits its cp.async group and must wait for it before the stage is read.
 template <typename T>
-__device__ int block_rescan(const T *row, int64_t rowflat, int64_t total, int mis, int c0, int c1,
-                            float cs, float mc, float t, float cum0, const int *ex, int ex_n,
-                            uint4 *stage, RescanSmem &S)
+__device__ __forceinline__ void stage_range(const T *row, int64_t rowflat, int64_t total, int mis, int c0,
+                                            int c1, uint4 *stage, int t, int nt)
 {
     constexpr int VEC = Elt<T>::VEC;
-    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-    const int a0 = c0 - (int)((rowflat + c0 + mis) % VEC);  // aligned-down start column
+    const int a0 = c0 - (int)((rowflat + c0 + mis) % VEC);
     const int nvv = (c1 - a0 + VEC - 1) / VEC;
-    // Whole aligned vectors are copied even where they stick out of [c0, c1) (the weights mask
-    // those elements); only a vector that would reach outside the logits array is read element
-    // by element.
-    for (int i = tid; i < nvv; i += nt) {
+    for (int i = t; i < nvv; i += nt) {
         const int col = a0 + i * VEC;
         const int64_t f = rowflat + col;
         if (f >= 0 && f + VEC <= total) cp_async16(stage + i, row + col);
         else stage[i] = load_partial<T>(row, col, c0, c1);
     }
-    if (tid == 0) {
-        S.first = INT_MAX;
-        S.last = -1;
-        S.found = -1;
-    }
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
+    cp_async_commit();
+}
+
+// First column y of [c0, c1) at which cum0 + (running weight up to and including y) exceeds t;
+// when none does (t = +inf asks for that), the last column with positive weight; -1 if no weight
+// is positive.  Child tokens ex[0..ex_n) (sorted) weigh 0.  stage holds the range as stage_range
+// laid it out, visible to every thread.  Every thread of the CTA calls it and gets the result.
+// Threads take runs of at most RUN_MAX vectors; the warp whose prefix crosses t (or, with none,
+// the last warp with positive weight) finds the thread and the column, so two barriers suffice.
+constexpr int RUN_MAX = 3;  // vectors per thread: (SUB_VEC + 2) / NT_FIN rounded up to odd
+
+template <typename T>
+__device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs, float mc, float t,
+                             float cum0, const int *ex, int ex_n, const uint4 *stage, RescanSmem &S)
+{
+    constexpr int VEC = Elt<T>::VEC;
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+    const int a0 = c0 - (int)((rowflat + c0 + mis) % VEC);
+    const int nvv = (c1 - a0 + VEC - 1) / VEC;
     // Each thread weighs a contiguous run of odd length (conflict-free 16-byte shared reads).
     const int per = ((nvv + nt - 1) / nt) | 1;
     const int k0 = min(tid * per, nvv), k1 = min(k0 + per, nvv);
@@ -134,43 +132,66 @@ __device__ int block_rescan(const T *row, int64_t rowflat, int64_t total, int mi
     while (e0 < ex_n && ex[e0] < lc0) ++e0;
     int e1 = e0;
     while (e1 < ex_n && ex[e1] < lc1) ++e1;
+    float vs[RUN_MAX];
     float own = 0.f;
-    for (int k = k0; k < k1; ++k) {
-        float e[VEC];
-        vec_weights_ex<T>(stage[k], a0 + k * VEC, c0, c1, cs, mc, ex, e0, e1, e);
+    if (per <= RUN_MAX) {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) own += e[j];
+        for (int i = 0; i < RUN_MAX; ++i) {
+            vs[i] = 0.f;
+            if (k0 + i < k1) {
+                float e[VEC];
+                vec_weights_ex<T>(stage[k0 + i], a0 + (k0 + i) * VEC, c0, c1, cs, mc, ex, e0, e1, e);
+                float p0 = (e[0] + e[1]) + (e[2] + e[3]);
+                if (VEC == 8) p0 += (e[VEC - 4] + e[VEC - 3]) + (e[VEC - 2] + e[VEC - 1]);
+                vs[i] = p0;
+            }
+            own += vs[i];
+        }
+    } else {
+        for (int k = k0; k < k1; ++k) {
+            float e[VEC];
+            vec_weights_ex<T>(stage[k], a0 + k * VEC, c0, c1, cs, mc, ex, e0, e1, e);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) own += e[j];
+        }
     }
-    // Block scan of the thread totals.
+    // Warp totals, then every warp knows its prefix.
     const float incl = warp_incl_scan(own, lane);
     if (lane == 31) S.wsum[warp] = incl;
     __syncthreads();
     const float ws = lane < nw ? S.wsum[lane] : 0.f;
     const float wi = warp_incl_scan(ws, lane);
-    const float cum = cum0 + __shfl_sync(0xffffffffu, wi - ws, warp);
-    if (cum + incl > t) atomicMin(&S.first, tid);
-    if (own > 0.f) atomicMax(&S.last, tid);
-    __syncthreads();
-    const bool take_last = S.first == INT_MAX;
-    const int who = take_last ? S.last : S.first;
-    if (tid == who) {
-        // Walk the run: the first crossing, or (take_last, or rounding) the last positive column.
-        float c = cum + incl - own;
-        int found = -1, lp = -1;
-        for (int k = k0; k < k1 && found < 0; ++k) {
-            const int col = a0 + k * VEC;
-            float e[VEC];
-            vec_weights_ex<T>(stage[k], col, c0, c1, cs, mc, ex, e0, e1, e);
+    const unsigned wcross = __ballot_sync(0xffffffffu, lane < nw && cum0 + wi > t);
+    const unsigned wpos = __ballot_sync(0xffffffffu, lane < nw && ws > 0.f);
+    const bool take_last = wcross == 0;
+    const int wsel = take_last ? (wpos ? 31 - __clz(wpos) : -1) : __ffs(wcross) - 1;
+    if (warp == wsel) {
+        const float cum = cum0 + __shfl_sync(0xffffffffu, wi - ws, warp);
+        const unsigned hit = __ballot_sync(0xffffffffu, !take_last && cum + incl > t);
+        const unsigned pos = __ballot_sync(0xffffffffu, own > 0.f);
+        // The crossing thread, or (take_last, or rounding) the warp's last positive thread.
+        const bool last_mode = hit == 0;
+        const int who = last_mode ? 31 - __clz(pos) : __ffs(hit) - 1;
+        if (lane == who) {
+            float c = cum + incl - own;
+            int found = -1, lp = -1;
+            for (int k = k0; k < k1 && found < 0; ++k) {
+                const int col = a0 + k * VEC;
+                float e[VEC];
+                vec_weights_ex<T>(stage[k], col, c0, c1, cs, mc, ex, e0, e1, e);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-                if (found < 0 && e[j] > 0.f) {
-                    lp = col + j;
-                    c += e[j];
-                    if (!take_last && c > t) found = lp;
+                for (int j = 0; j < VEC; ++j) {
+                    if (found < 0 && e[j] > 0.f) {
+                        lp = col + j;
+                        c += e[j];
+                        if (!last_mode && c > t) found = lp;
+                    }
                 }
             }
+            S.found = found >= 0 ? found : lp;
         }
-        S.found = found >= 0 ? found : lp;
+    } else if (wsel < 0 && tid == 0) {
+        S.found = -1;
     }
     __syncthreads();
     return S.found;

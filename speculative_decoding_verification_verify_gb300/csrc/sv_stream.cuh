@@ -306,12 +306,13 @@ __device__ __forceinline__ void load_step(uint4 (&d)[VPL], const uint4 *p, int l
 }
 
 // Stream the 16-byte aligned body [b0, b1) of a warp segment that starts at column c0 (its
-// unaligned head, already folded, is [c0, b0)), VPL loads per lane per step.  After every SUB_VEC
-// vectors but the last sub-range, the sub-range's record is flushed to recs[idx0 + k].
+// unaligned head, already folded, is [c0, b0)), VPL loads per lane per step; cur holds the first
+// step, loaded by the caller.  After every SUB_VEC vectors but the last sub-range, the
+// sub-range's record is flushed to recs[idx0 + k].
 template <typename T, bool SAMPLE>
 __device__ __forceinline__ void stream_body(const T *row, int c0, int b0, int b1, int lane, float cs,
                                             ExCursor &ex, SampleAcc &sa, GreedyAcc &ga,
-                                            float4 *recs, int64_t idx0)
+                                            float4 *recs, int64_t idx0, uint4 (&cur)[VPL])
 {
     constexpr int VEC = Elt<T>::VEC;
     const int nvec = (b1 - b0) / VEC;
@@ -320,11 +321,12 @@ __device__ __forceinline__ void stream_body(const T *row, int c0, int b0, int b1
     const int nst = (nvec + STEP_VEC - 1) / STEP_VEC;
     const int nfull = nvec / STEP_VEC;  // steps whose vectors are all inside the segment
     const uint64_t cs2 = f2(cs, cs);
-    uint4 cur[VPL];
     for (int s = 0; s < nst; ++s) {
         // All of a step's loads are issued together; the other warps of the SM cover their latency.
-        if (s < nfull) load_step<T, false>(cur, vp + s * STEP_VEC, 0);
-        else load_step<T, true>(cur, vp + s * STEP_VEC, nvec - s * STEP_VEC - lane);
+        if (s > 0) {
+            if (s < nfull) load_step<T, false>(cur, vp + s * STEP_VEC, 0);
+            else load_step<T, true>(cur, vp + s * STEP_VEC, nvec - s * STEP_VEC - lane);
+        }
         const int nv = min(STEP_VEC, nvec - s * STEP_VEC);
         fold_step<T, SAMPLE>(cur, nv, b0 + (s * STEP_VEC + lane) * VEC, lane, cs, cs2, ex, sa, ga);
         constexpr int STEPS_PER_SUB = SUB_VEC / STEP_VEC;
@@ -334,6 +336,18 @@ __device__ __forceinline__ void stream_body(const T *row, int c0, int b0, int b1
                                  b0 + (k + 1) * SUB_VEC * VEC);
         }
     }
+}
+
+// The first step of a segment body [b0, b1), issued before anything else of the segment.
+template <typename T>
+__device__ __forceinline__ void load_first_step(uint4 (&cur)[VPL], const T *row, int b0, int b1, int lane)
+{
+    constexpr int VEC = Elt<T>::VEC;
+    const int nvec = (b1 - b0) / VEC;
+    if (nvec <= 0) return;
+    const uint4 *vp = reinterpret_cast<const uint4 *>(row + b0) + lane;
+    if (nvec >= STEP_VEC) load_step<T, false>(cur, vp, 0);
+    else load_step<T, true>(cur, vp, nvec - lane);
 }
 
 }  // namespace sv

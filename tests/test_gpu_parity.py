@@ -4,6 +4,8 @@ Token ids and accept lengths must match exactly, except for requests the oracle 
 boundary draws (a decision within 1e-6 relative of its boundary), which are counted and must
 stay rare; probabilities must agree within 1e-5 relative.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -235,6 +237,96 @@ def test_sweep_cells_sampled():
     for B, k, alpha in ((8, 3, 0.35), (32, 1, 0.7), (64, 7, 0.7)):
         inp = wl.chain_sweep(DEV, B=B, k=k, alpha=alpha)
         run_chain(inp, "standard", ids=_req_sample(B, 4))
+
+
+def test_sweep_largest_cell_sampled():
+    # The sweep's largest cell (B=512, k=7, 1.05 GB of logits and 1.84 GB of q), sampled.
+    inp = wl.chain_sweep(DEV, B=512, k=7, alpha=0.35)
+    run_chain(inp, "standard", ids=_req_sample(512, 6, seed=3))
+
+
+def _dominant_chain(B, k, V, T, seed, hit):
+    """Logits ~N(0,1) with a +25 peak per row; the draft of slot i is row i's peak when hit[b, i]
+    (accepted with p(x) ~ 1), else a random other token (rejected)."""
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    x = torch.randn((B, k + 1, V), generator=g, device=DEV)
+    peak = torch.randint(0, V, (B, k + 1, 1), generator=g, device=DEV)
+    x.scatter_add_(2, peak, torch.full((B, k + 1, 1), 25.0, device=DEV))
+    other = (peak[:, :k, 0] + 1 + torch.randint(0, V - 1, (B, k), generator=g, device=DEV)) % V
+    drafts = torch.where(hit, peak[:, :k, 0], other).to(torch.int32).contiguous()
+    return wl.ChainInputs("dominant", x.to(torch.bfloat16).contiguous(), drafts, None, T, seed)
+
+
+@pytest.mark.parametrize("k", [12, 40, 63])
+def test_long_chains(k):
+    # More rows than the finaliser has warps (its rows loop) and, past 32 drafts, more than one
+    # ballot of draft slots.  Drafts on a +25 peak are accepted, so the runs are long.
+    B, V = 6, 3001
+    hit = torch.ones((B, k), dtype=torch.bool, device=DEV)
+    hit[1, k // 2] = False
+    hit[2, k - 1] = False
+    hit[3, 5] = False
+    inp = _dominant_chain(B, k, V, 1.0, 70 + k, hit)
+    r, ref = run_chain(inp, "onehot")
+    assert int(ref["accept_len"].max()) >= min(k, 32), ref["accept_len"]
+    run_chain(inp, "greedy")
+    q_inp = wl.chain_sweep(DEV, B=5, k=k, V=V, alpha=0.8)
+    run_chain(q_inp, "standard")
+
+
+@pytest.mark.parametrize("T", [1.0, 0.05])
+def test_dominant_child_low_temperature(T):
+    # A draft far above every other token of its row (at T = 0.05 its weight is 2^500 times the
+    # rest in the row's own reference): p(x) ~ 1, no overflow, no fault.
+    B, k, V = 8, 5, 5000
+    g = torch.Generator(device=DEV).manual_seed(9)
+    hit = torch.rand((B, k), generator=g, device=DEV) < 0.8
+    inp = _dominant_chain(B, k, V, T, 80, hit)
+    r, ref = run_chain(inp, "onehot")
+    assert int(ref["status"].max()) == 0
+    assert int(_np(r.dev_status)[0]) == 0
+
+
+def test_graph_captured_calls_match_direct_calls():
+    # Calls captured in a CUDA graph (the two kernels chained by programmatic dependent launch)
+    # give the same tokens as the same calls made directly.
+    from speculative_decoding_verification_verify_gb300 import binding
+
+    lib = binding.load_library()
+    sets = [wl.chain_b64k7(DEV, B=24, k=7, V=20000, seed=900 + i) for i in range(3)]
+    B, k, V = sets[0].shape
+    nb = sv.spec_verify_workspace_bytes(sv.MODE_REJECTION, B, k, V)
+    ws = torch.zeros(nb, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    outs = [(torch.full((B, k + 1), -7, dtype=torch.int32, device=DEV), torch.empty(B, dtype=torch.int32, device=DEV))
+            for _ in range(6)]
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+
+    def call(i):
+        x = sets[i % 3]
+        o, a = outs[i]
+        rc = lib.spec_verify_rejection(P(x.logits), sv.BF16, P(x.drafts), None, B, k, V, 1.0, x.seed, 50 + i,
+                                       P(o), P(a), None, P(ws), nb, P(st),
+                                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0
+
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(3, 6):
+            call(i)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    # The graph's calls used offsets 53..55; compare with direct calls at those offsets.
+    for j, i in enumerate(range(3, 6)):
+        x = sets[i % 3]
+        d = sv.spec_verify_rejection(x.logits, x.drafts, None, temperature=1.0, seed=x.seed, offset=50 + i)
+        np.testing.assert_array_equal(_np(outs[i][0]), _np(d.out_tokens))
+        np.testing.assert_array_equal(_np(outs[i][1]), _np(d.accept_len))
+    assert int(_np(st)[0]) == 0
 
 
 # --------------------------------------------------------------------------------------------
