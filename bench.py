@@ -37,6 +37,7 @@ N_SETS = 3  # rotating input sets: 3 x 131 MB > L2 (129 MB)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_call_b64k7_traffic.json")
 LAUNCHES_PER_CALL = 2  # sv_stream_kernel, then sv_finalize_kernel (programmatic dependent launch)
 GRAPH_CALLS = 30       # verify calls captured in one CUDA graph for the timed region
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_verify_gb300", "csrc", f)
                   for f in ("spec_verify.cu", "sv_device.cuh", "sv_draw.cuh", "sv_stream.cuh", "sv_rescan.cuh")]
 
@@ -289,21 +290,23 @@ def run_ours(args, D: Dist):
     for _ in range(3):
         graph.replay()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(gpu_selector(torch, dev))
     time.sleep(0.1)
     D.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    e0.record()
-    for _ in range(reps):
+    # One event pair per replay (30 calls each) gives the spread; their span gives the total.
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record()
+    for i in range(reps):
         graph.replay()
-    e1.record()
+        ev[i + 1].record()
     torch.cuda.synchronize()
     t1 = time.time()
     D.barrier()
     clocks.stop()
-    total_ms = e0.elapsed_time(e1)
+    total_ms = ev[0].elapsed_time(ev[-1])
+    per_call = [ev[i].elapsed_time(ev[i + 1]) / GRAPH_CALLS for i in range(reps)]
     launch_ms = total_ms / K
     max_total_ms = D.max(total_ms, dev)
     if int(status.item()) != 0:
@@ -343,7 +346,11 @@ def run_ours(args, D: Dist):
                      "algorithmic_bytes_per_launch": alg,
                      "kernel": "verify call: sv_stream_kernel<bf16, sample> + sv_finalize_kernel<bf16, sample>",
                      "launch_ms": launch_ms,
-                     "timing": f"CUDA events around {reps} replays of a graph of {GRAPH_CALLS} calls"},
+                     "launch_ms_median_p10_p90": [statistics.median(per_call),
+                                                  float(np.percentile(per_call, 10)),
+                                                  float(np.percentile(per_call, 90))],
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "timing": f"CUDA events around each of {reps} replays of a graph of {GRAPH_CALLS} calls"},
         "gpu_launches": LAUNCHES_PER_CALL * K,
         "clocks": clocks.summary(t0, t1),
     }
@@ -411,27 +418,49 @@ def run_e2e(args, D, torch, sv, lib, sets, ws, ws_bytes, status, stream, sh, off
             "path": "pinned host -> device copy, spec_verify_rejection, device -> pinned host"}
 
 
-def cpu_baseline(inp, seconds):
+def _oracle_rate(lg, d, seed, seconds, threads):
+    """Requests of the workload verified per second by the oracle on `threads` host threads
+    (each thread verifies whole requests; the oracle's C code runs without the GIL)."""
+    import concurrent.futures as cf
+
     import numpy as np
 
     import oracle
+
+    stop = time.perf_counter() + seconds
+    counter = iter(range(1 << 30))
+
+    def worker():
+        n = 0
+        while time.perf_counter() < stop or n == 0:
+            b = next(counter) % B
+            oracle.verify_rejection(lg, d, None, 1.0, seed, 0, req_ids=np.array([b], np.int32))
+            n += 1
+        return n
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        done = sum(ex.map(lambda _: worker(), range(threads)))
+    el = time.perf_counter() - t0
+    return done, el
+
+
+def cpu_baseline(inp, seconds):
     from speculative_decoding_verification_verify_gb300 import workloads as wl
+
+    import oracle
 
     lg = wl.to_numpy_logits(inp.logits)
     d = inp.drafts.cpu().numpy()
     oracle.build()
-    done = 0
-    t0 = time.perf_counter()
-    while True:
-        b = done % B
-        oracle.verify_rejection(lg, d, None, 1.0, inp.seed, 0, req_ids=np.array([b], np.int32))
-        done += 1
-        if time.perf_counter() - t0 >= seconds and done >= 2:
-            break
-    el = time.perf_counter() - t0
-    return {"value": done * (K_DRAFTS + 1) / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} requests (8 positions each) of the b64k7 workload, one thread, "
-                      f"{el:.1f} s"}
+    threads = os.cpu_count() or 1
+    n1, el1 = _oracle_rate(lg, d, inp.seed, seconds / 2, 1)
+    nt, elt = _oracle_rate(lg, d, inp.seed, seconds / 2, threads)
+    return {"value": nt * (K_DRAFTS + 1) / elt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{nt} requests (8 positions each) of the b64k7 workload on {threads} threads, "
+                      f"{elt:.1f} s",
+            "single_thread": {"value": n1 * (K_DRAFTS + 1) / el1, "cores": 1,
+                              "sample": f"{n1} requests, {el1:.1f} s"}}
 
 
 # --------------------------------------------------------------------------------------------
@@ -532,9 +561,16 @@ def run_reference(args, D: Dist):
     lg = wl.to_numpy_logits(inp.logits)
     d = inp.drafts.numpy()
 
+    import concurrent.futures as cf
+
+    threads = os.cpu_count() or 1
+    pool = cf.ThreadPoolExecutor(max_workers=threads)
+
     def step(s):
-        oracle.verify_rejection(lg, d, None, 1.0, inp.seed, s,
-                                req_ids=np.array([s % B], np.int32))
+        # One step verifies `threads` requests of the workload, one per host thread.
+        ids = [(s * threads + i) % B for i in range(threads)]
+        list(pool.map(lambda b: oracle.verify_rejection(lg, d, None, 1.0, inp.seed, s,
+                                                        req_ids=np.array([b], np.int32)), ids))
 
     for w in range(args.warmup):
         step(w)
@@ -542,7 +578,8 @@ def run_reference(args, D: Dist):
     for s in range(args.steps):
         step(args.warmup + s)
     el = time.perf_counter() - t0
-    value = (K_DRAFTS + 1) * args.steps / el
+    pool.shutdown()
+    value = (K_DRAFTS + 1) * threads * args.steps / el
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": D.world, "steps": args.steps, "warmup": args.warmup,
@@ -550,9 +587,9 @@ def run_reference(args, D: Dist):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B, "k": K_DRAFTS, "V": V, "logits": "bf16",
                    "mode": "target-only (one-hot q)",
-                   "step": "one request (8 positions) of the workload per step"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} requests of the b64k7 workload, one per step"},
+                   "step": f"{threads} requests (8 positions each) of the workload per step, one per host thread"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} steps of {threads} requests of the b64k7 workload"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -618,35 +618,14 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
     stage_request<SAMPLE>(P, b, F);
     // From here on the streaming kernel's records and captures are read.
     pdl_wait();
-    // With one row per warp, every warp also prefetches its row's crossing range into its own
-    // stage while warp 0 decides, so the stop row's rescan finds its columns in shared memory.
-    const bool prefetch = SAMPLE && rpr <= nwf;
-    if (rpr <= nwf) {
+    for (int n = warp; n < rpr; n += nwf) {
         RowState rs;
-        if (warp < rpr) finish_row<T, SAMPLE>(P, b, warp, F, lane, rs);
-        __syncthreads();
-        if (SAMPLE && warp < rpr && !rs.bad && F.need_draw[warp]) {
-            row_draw_prep(P, b, warp, F, lane, rs);
-            __syncwarp();
-            if (F.rs_ok[warp]) {
-                const int64_t r = (int64_t)b * rpr + warp;
-                stage_range<T>(reinterpret_cast<const T *>(P.logits) + r * P.V, r * P.V, P.total, P.mis,
-                               F.rs_c0[warp], F.rs_c1[warp], stage + warp * RESCAN_STAGE_VEC, lane, 32);
-            }
-        }
-        if (warp == 0) decide_request<SAMPLE>(P, F, lane);
-        if (prefetch) cp_async_wait_all();
-        __syncthreads();
-    } else {
-        for (int n = warp; n < rpr; n += nwf) {
-            RowState rs;
-            finish_row<T, SAMPLE>(P, b, n, F, lane, rs);
-            if (SAMPLE && !rs.bad && F.need_draw[n]) row_draw_prep(P, b, n, F, lane, rs);
-        }
-        __syncthreads();
-        if (warp == 0) decide_request<SAMPLE>(P, F, lane);
-        __syncthreads();
+        finish_row<T, SAMPLE>(P, b, n, F, lane, rs);
+        if (SAMPLE && !rs.bad && F.need_draw[n]) row_draw_prep(P, b, n, F, lane, rs);
     }
+    __syncthreads();
+    if (warp == 0) decide_request<SAMPLE>(P, F, lane);
+    __syncthreads();
     const bool faulted = F.status != 0;
 
     // Outputs.
@@ -673,17 +652,15 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
     } else if (mode == 1) {
         int drawn = F.cand[stop];
         if (F.rs_ok[stop]) {
+            // The stop row's crossing record range: copy it to shared memory, then rescan it.
             const int64_t r = (int64_t)b * rpr + stop;
-            const uint4 *staged = stage + (prefetch ? stop : 0) * RESCAN_STAGE_VEC;
-            if (!prefetch) {
-                stage_range<T>(reinterpret_cast<const T *>(P.logits) + r * P.V, r * P.V, P.total, P.mis,
-                               F.rs_c0[stop], F.rs_c1[stop], stage, tid, blockDim.x);
-                cp_async_wait_all();
-                __syncthreads();
-            }
+            stage_range<T>(reinterpret_cast<const T *>(P.logits) + r * P.V, r * P.V, P.total, P.mis,
+                           F.rs_c0[stop], F.rs_c1[stop], stage, tid, blockDim.x);
+            cp_async_wait_all();
+            __syncthreads();
             drawn = rescan_staged<T>(r * P.V, P.mis, F.rs_c0[stop], F.rs_c1[stop], P.cs, F.row_mc[stop],
                                      F.rs_t[stop], F.rs_cum[stop], F.ex_col + F.ex_off[stop], F.ex_n[stop],
-                                     staged, F.RS);
+                                     stage, F.RS);
         }
         last = drawn >= 0 ? drawn : 0;  // < 0 only through rounding
     }
@@ -753,8 +730,8 @@ template <typename T, bool SAMPLE>
 __global__ void __launch_bounds__(NT_FIN_MAX) sv_finalize_kernel(const Params P)
 {
     __shared__ FinSmem F;
-    extern __shared__ uint4 sv_fin_stage[];  // sampling: one rescan stage per warp
-    finalize_request<T, SAMPLE>(P, (int)blockIdx.x, F, sv_fin_stage);
+    __shared__ uint4 stage[SAMPLE ? RESCAN_STAGE_VEC : 1];  // the stop row's rescan range
+    finalize_request<T, SAMPLE>(P, (int)blockIdx.x, F, stage);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1029,12 +1006,6 @@ static const DevInfo *device_info()
         d.occ[1][0] = o > 0 ? o : 1;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_stream_kernel<float, true>, NT, 0);
         d.occ[1][1] = o > 0 ? o : 1;
-        const void *fin[2] = {(const void *)sv_finalize_kernel<__nv_bfloat16, true>,
-                              (const void *)sv_finalize_kernel<float, true>};
-        for (int i = 0; i < 2; ++i)
-            if (cudaFuncSetAttribute(fin[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)((NT_FIN_MAX / 32) * RESCAN_STAGE_VEC * sizeof(uint4))) != cudaSuccess)
-                return nullptr;
         cudaGetLastError();
         d.sms = sms;
     }
@@ -1093,7 +1064,7 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
     cfg.gridDim = dim3((unsigned)P.B);
     const int nwf = P.rpr < NT_FIN_MAX / 32 ? P.rpr : NT_FIN_MAX / 32;
     cfg.blockDim = dim3(32u * (unsigned)nwf);
-    cfg.dynamicSmemBytes = SAMPLE ? (size_t)nwf * RESCAN_STAGE_VEC * sizeof(uint4) : 0;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
