@@ -9,7 +9,8 @@
 //                         over G persistent CTAs.  Each warp keeps a running (max, sum of
 //                         2^(l*cs - max*cs)) over its contiguous segment, skipping the tokens
 //                         that are drafts of the row (their logits are captured instead), or a
-//                         running argmax (greedy), and writes one record per piece.
+//                         running argmax (greedy), and writes one record per SUB_VEC vectors of
+//                         its segment, carrying the columns it covers.
 //   sv_finalize_kernel -- one CTA per request, launched as a programmatic dependent of the
 //                         streaming kernel: it stages the request's inputs, waits for the records,
 //                         merges them per row, decides acceptance (warp-ballot first-reject scan

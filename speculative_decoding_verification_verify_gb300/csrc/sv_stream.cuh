@@ -1,6 +1,6 @@
 // sv_stream.cuh -- the streaming fold: each warp walks its contiguous segment of a logit row with
-// 16-byte non-allocating loads (the next step's loads issued before the current step is folded)
-// and folds every element into a running (max, sum of 2^(l*cs - mc)) or a running argmax.
+// 16-byte non-allocating loads, eight per lane per step, and folds every element into a running
+// (max, sum of 2^(l*cs - mc)) or a running argmax, flushing a record every SUB_VEC vectors.
 #pragma once
 
 #include <climits>
