@@ -74,6 +74,11 @@ def _load():
         lib.svo_verify_tree.argtypes = [P, i32, P, P, i32, i32, i64, i32, f64, u64, u64, P, i32,
                                         P, P, P, P, P]
         lib.svo_verify_tree.restype = i32
+        lib.svo_block_core.argtypes = [P, P, P, i32, i64, P, P, P, I32P, I32P, P]
+        lib.svo_block_core.restype = i32
+        lib.svo_verify_block.argtypes = [P, i32, P, P, i32, i32, i64, f64, u64, u64, P, i32,
+                                         P, P, P, P]
+        lib.svo_verify_block.restype = i32
         lib.svo_grid_chain_first_token.argtypes = [P, P, P, i64, i32, P, F64P]
         lib.svo_grid_chain_first_token.restype = i32
         lib.svo_grid_tree_first_token.argtypes = [P, P, i32, i64, i32, P, F64P]
@@ -285,6 +290,46 @@ def verify_rejection(logits, drafts, q, T: float, seed: int, offset: int, req_id
                                     offset, _ptr(ids), n, _ptr(out), _ptr(alen), _ptr(probs),
                                     _ptr(bnd), _ptr(status)))
     return dict(out_tokens=out, accept_len=alen, out_probs=probs, boundary=bnd, status=status)
+
+
+def block_core(p, q, drafts, u, v):
+    """Block verification of one request from probabilities: p [k+1, V], q [k, V] or None
+    (one-hot drafts), drafts [k], uniforms u, v [k+1].  Returns (tokens, accept_len, boundary)."""
+    lib = _load()
+    pp = _c(p, np.float64)
+    k1, V = pp.shape
+    k = k1 - 1
+    qq = None if q is None else _c(q, np.float64).reshape(k, V)
+    d = _c(drafts, np.int32).reshape(k)
+    uu, vv = _c(u, np.float64), _c(v, np.float64)
+    tok = np.zeros(k + 1, np.int32)
+    alen = ctypes.c_int32(-1)
+    bnd = ctypes.c_int32(0)
+    work = np.zeros(V, np.float64)
+    st = lib.svo_block_core(_ptr(pp), _ptr(qq), _ptr(d), k, V, _ptr(uu), _ptr(vv), _ptr(tok),
+                            ctypes.byref(alen), ctypes.byref(bnd), _ptr(work))
+    if st != 0:
+        raise RuntimeError(f"oracle block core returned {st}")
+    return tok, alen.value, bnd.value
+
+
+def verify_block(logits, drafts, q, T: float, seed: int, offset: int, req_ids=None):
+    """Block verification.  logits [B, k+1, V]; drafts [B, k]; q [B, k, V] or None (one-hot)."""
+    lib = _load()
+    a, dt = _logits(logits)
+    B, k1, V = a.shape
+    k = k1 - 1
+    d = _c(drafts, np.int32).reshape(B, k)
+    qq = None if q is None else _c(q, np.float32).reshape(B, k, V)
+    ids = _req_ids(req_ids, B)
+    n = ids.shape[0]
+    out = np.zeros((n, k + 1), np.int32)
+    alen = np.zeros(n, np.int32)
+    bnd = np.zeros(n, np.int32)
+    status = np.zeros(n, np.int32)
+    _check(lib.svo_verify_block(_ptr(a), dt, _ptr(d), _ptr(qq), B, k, V, float(T), seed, offset,
+                                _ptr(ids), n, _ptr(out), _ptr(alen), _ptr(bnd), _ptr(status)))
+    return dict(out_tokens=out, accept_len=alen, boundary=bnd, status=status)
 
 
 def verify_tree(logits, tokens, parents, mode: int, T: float, seed: int, offset: int,

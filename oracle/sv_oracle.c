@@ -27,6 +27,12 @@
  *   - q(x) = 0 accepts iff p(x) > 0 ("投机解码", section 对照：mistral.rs), which the strict
  *     test u*q < p reproduces.
  *
+ *   - Block verification ("The speculative decoding zoo", mlinterviewnotes 06-06, the block
+ *     branch of the rejection sampler, citing Sun et al. 2024, arXiv:2403.10444): the prefix of
+ *     L drafts is judged by its joint weight w_L and the residual mass r_L at the next position,
+ *     h_L = r_L / (r_L + 1 - w_L) (h = 1 when that denominator is 0), h_k = w_k for the last
+ *     draft; the accepted length is the largest L with a passing test.
+ *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - Uniforms: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
  *     1, 2, 3", SC'11), counter = (slot, request, offset_lo, offset_hi), key = (seed_lo,
@@ -40,6 +46,12 @@
  *   - Tree: node 0 is the root, parents[0] = -1, 0 <= parents[j] < j; children are tried in
  *     ascending node index; a child whose token is -1 is absent (never tried).
  *   - Rows holding NaN or +inf, or no finite logit, are invalid (status 2).
+ *   - Block verification (the pages print only h): w_0 = 1, w_{i+1} = min(1, w_i p_i(x)/q_i(x))
+ *     (a q of 0 gives 1 when w_i p_i(x) > 0), r_L = sum_y max(w_L p_L(y) - q_L(y), 0) with
+ *     q_L the one-hot of the next draft when there are no draft probabilities; candidate
+ *     length L passes iff u_L < h_L, u_L being word 0 of slot L - 1; the token after the
+ *     accepted prefix is drawn from max(w_j p_j - q_j, 0) / Z (from p_j when j reaches the
+ *     last draft or an absent draft), with v of slot j.  These follow Sun et al.'s algorithm.
  *
  * Boundary draws: a decision whose operands lie within 1e-6 (relative) of the decision
  * boundary is flagged, because an fp32 implementation may legitimately decide it the other way.
@@ -55,6 +67,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#define SVO_MAX_ROWS 64 /* rows per request (k + 1) the block verifier accepts */
 #define SVO_DT_BF16 0
 #define SVO_DT_FP32 1
 #define SVO_DT_FP64 2
@@ -472,6 +485,131 @@ done:
     free(work);
     free(u);
     free(v);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Block verification of one request with explicit uniforms.                                   */
+/*   p: (k+1) x V target probabilities; q: k x V draft probabilities, or NULL for one-hot drafts */
+/*   u[L-1] judges candidate length L; v[j] draws the token after the accepted prefix j.         */
+/* ------------------------------------------------------------------------------------------ */
+static double svo_block_q(const double *q, const int32_t *drafts, int row, int64_t V, int64_t y)
+{
+    if (q) return q[(int64_t)row * V + y];
+    return y == drafts[row] ? 1.0 : 0.0;
+}
+
+int svo_block_core(const double *p, const double *q, const int32_t *drafts, int k, int64_t V,
+                   const double *u, const double *v, int32_t *tokens, int32_t *accept_len,
+                   int32_t *boundary, double *work)
+{
+    if (k < 0 || k + 1 > SVO_MAX_ROWS) return SVO_EINVAL;
+    for (int i = 0; i <= k; ++i) tokens[i] = -1;
+    *accept_len = -1;
+    for (int i = 0; i < k; ++i)
+        if (drafts[i] < -1 || drafts[i] >= V) return SVO_BAD_TOKEN;
+    int ke = k; /* drafts actually present: an absent draft ends the block */
+    for (int i = 0; i < k; ++i)
+        if (drafts[i] < 0) {
+            ke = i;
+            break;
+        }
+
+    /* Joint weight of each prefix. */
+    double w[SVO_MAX_ROWS + 1];
+    w[0] = 1.0;
+    for (int i = 0; i < ke; ++i) {
+        double px = p[(int64_t)i * V + drafts[i]];
+        double qx = svo_block_q(q, drafts, i, V, drafts[i]);
+        double next;
+        if (w[i] * px <= 0.0) next = 0.0;
+        else if (qx <= 0.0) next = 1.0;
+        else next = fmin(1.0, w[i] * px / qx);
+        w[i + 1] = next;
+    }
+
+    /* The largest candidate length whose test passes. */
+    int j = 0;
+    for (int L = 1; L <= ke; ++L) {
+        double h;
+        if (L < ke) {
+            const double *pl = p + (int64_t)L * V;
+            double r = 0.0;
+            for (int64_t y = 0; y < V; ++y) r += fmax(0.0, w[L] * pl[y] - svo_block_q(q, drafts, L, V, y));
+            double denom = r + 1.0 - w[L];
+            h = denom > 0.0 ? r / denom : 1.0;
+        } else {
+            h = w[L];
+        }
+        if (fabs(u[L - 1] - h) < SVO_BOUNDARY_REL) *boundary = 1;
+        if (u[L - 1] < h) j = L;
+    }
+
+    /* The token after the accepted prefix. */
+    const double *pj = p + (int64_t)j * V;
+    if (j < ke) {
+        for (int64_t y = 0; y < V; ++y) work[y] = fmax(0.0, w[j] * pj[y] - svo_block_q(q, drafts, j, V, y));
+    } else {
+        for (int64_t y = 0; y < V; ++y) work[y] = pj[y];
+    }
+    double Z;
+    int64_t tok = svo_inverse_cdf(work, V, v[j], boundary, &Z);
+    if (tok < 0) { /* Z <= 0 in floating point: draw from p instead */
+        for (int64_t y = 0; y < V; ++y) work[y] = pj[y];
+        tok = svo_inverse_cdf(work, V, v[j], boundary, &Z);
+    }
+    for (int i = 0; i < j; ++i) tokens[i] = drafts[i];
+    tokens[j] = (int32_t)tok;
+    *accept_len = j;
+    return SVO_OK;
+}
+
+int svo_verify_block(const void *logits, int dtype, const int32_t *drafts, const float *q, int B,
+                     int k, int64_t V, double T, uint64_t seed, uint64_t offset,
+                     const int32_t *req_ids, int n_req, int32_t *out_tokens, int32_t *accept_len,
+                     int32_t *boundary, int32_t *status)
+{
+    if (B < 1 || k < 0 || k + 1 > SVO_MAX_ROWS || V < 1 || n_req < 0 || !(T > 0.0) || !isfinite(T))
+        return SVO_EINVAL;
+    double *p = (double *)malloc(sizeof(double) * (size_t)(k + 1) * (size_t)V);
+    double *qd = q ? (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1) * (size_t)V) : NULL;
+    double *work = (double *)malloc(sizeof(double) * (size_t)V);
+    double u[SVO_MAX_ROWS + 1], v[SVO_MAX_ROWS + 1];
+    int rc = SVO_OK;
+    if (!p || (q && !qd) || !work) {
+        rc = SVO_ENOMEM;
+        goto done;
+    }
+    for (int i = 0; i < n_req; ++i) {
+        int b = req_ids ? req_ids[i] : i;
+        int32_t *tok = out_tokens + (int64_t)i * (k + 1);
+        for (int r = 0; r <= k; ++r) tok[r] = -1;
+        accept_len[i] = -1;
+        boundary[i] = 0;
+        status[i] = SVO_OK;
+        if (b < 0 || b >= B) {
+            rc = SVO_EINVAL;
+            goto done;
+        }
+        const int32_t *d = drafts + (int64_t)b * k;
+        for (int r = 0; r < k; ++r)
+            if (d[r] < -1 || d[r] >= V) status[i] = SVO_BAD_TOKEN;
+        for (int r = 0; r <= k; ++r) {
+            int st = svo_softmax_row(logits, dtype, (int64_t)b * (k + 1) + r, V, T, p + (int64_t)r * V);
+            if (st > status[i]) status[i] = st;
+        }
+        if (status[i] != SVO_OK) continue;
+        if (q) {
+            const float *qb = q + (int64_t)b * k * V;
+            for (int64_t e = 0; e < (int64_t)k * V; ++e) qd[e] = (double)qb[e];
+        }
+        for (int r = 0; r <= k; ++r) svo_uniform_pair(seed, offset, (uint32_t)r, (uint32_t)b, &u[r], &v[r]);
+        status[i] = svo_block_core(p, qd, d, k, V, u, v, tok, &accept_len[i], &boundary[i], work);
+    }
+done:
+    free(p);
+    free(qd);
+    free(work);
     return rc;
 }
 
