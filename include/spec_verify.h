@@ -76,6 +76,7 @@ extern "C" {
 #define SPEC_VERIFY_MODE_GREEDY 0
 #define SPEC_VERIFY_MODE_REJECTION 1
 #define SPEC_VERIFY_MODE_TREE 2
+#define SPEC_VERIFY_MODE_BLOCK 3
 
 /*
  * Greedy chain verification ("The speculative decoding zoo", DFlash section: matches =
@@ -114,6 +115,27 @@ int spec_verify_rejection(const void *logits, int dtype, const int32_t *draft_id
                           uint64_t seed, uint64_t offset, int32_t *out_tokens,
                           int32_t *accept_len, float *out_probs, void *workspace,
                           size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Block verification of a chain ("The speculative decoding zoo", mlinterviewnotes 06-06, the
+ * block branch of the rejection sampler, citing Sun et al. 2024, arXiv:2403.10444): the prefix
+ * of L drafts is judged as a whole.  With w_0 = 1 and w_{i+1} = min(1, w_i p_i(x)/q_i(x)) (q is
+ * one-hot at the draft when draft_probs is NULL), candidate length L passes iff
+ * u_L < h_L = r_L / (r_L + 1 - w_L), r_L = sum_y max(w_L p_L(y) - q_L(y), 0) (h_L = 1 when the
+ * denominator is 0), and h = w at the last present draft; u_L is word 0 of Philox slot L - 1.
+ * The accepted length j is the largest passing L (0 if none); the token after the prefix is
+ * drawn by inverse CDF (v = word 1 of slot j) from max(w_j p_j - q_j, 0), or from p_j at the
+ * last present draft (a bonus when all k are present), falling back to p_j if that mass is 0.
+ *   Arguments, outputs and status codes as for spec_verify_rejection (no out_probs).
+ *   Workspace: spec_verify_workspace_bytes(SPEC_VERIFY_MODE_BLOCK, B, k, V).
+ * With draft_probs the residual masses need every row's softmax, so a third kernel re-reads
+ * the logits and q of rows 0..j_max of each request; with one-hot drafts r_L is w_L times the
+ * row's non-draft mass and no extra pass is made.
+ */
+int spec_verify_block(const void *logits, int dtype, const int32_t *draft_ids,
+                      const float *draft_probs, int B, int k, int V, float temperature,
+                      uint64_t seed, uint64_t offset, int32_t *out_tokens, int32_t *accept_len,
+                      void *workspace, size_t ws_bytes, int32_t *dev_status, void *stream);
 
 /*
  * Tree verification ("投机解码", subsection SGLang 默认：只看目标概率，可以验证一棵树

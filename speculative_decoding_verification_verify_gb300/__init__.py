@@ -9,9 +9,11 @@ from .binding import (  # noqa: F401
     MODE_GREEDY,
     MODE_REJECTION,
     MODE_TREE,
+    MODE_BLOCK,
     Result,
     SpecVerifyError,
     load_library,
+    spec_verify_block,
     spec_verify_greedy,
     spec_verify_philox,
     spec_verify_rejection,

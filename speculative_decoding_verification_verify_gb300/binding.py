@@ -17,7 +17,7 @@ import torch
 from . import _build
 
 BF16, FP32 = 0, 1
-MODE_GREEDY, MODE_REJECTION, MODE_TREE = 0, 1, 2
+MODE_GREEDY, MODE_REJECTION, MODE_TREE, MODE_BLOCK = 0, 1, 2, 3
 OK, EINVAL, EWORKSPACE, ECUDA, ETOOBIG = 0, -1, -2, -3, -4
 NOALLOC_SCRATCH_BYTES = 4 << 20
 DEV_OK, DEV_BAD_TOKEN, DEV_BAD_ROW, DEV_BAD_TREE, DEV_DUP_SIBLING = 0, 1, 2, 3, 4
@@ -48,6 +48,9 @@ def load_library():
         lib.spec_verify_rejection.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, u64, u64, vp,
                                               vp, vp, vp, sz, vp, vp]
         lib.spec_verify_rejection.restype = i32
+        lib.spec_verify_block.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp,
+                                          vp, sz, vp, vp]
+        lib.spec_verify_block.restype = i32
         lib.spec_verify_tree.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, f32, u64, u64, vp,
                                          vp, vp, vp, sz, vp, vp]
         lib.spec_verify_tree.restype = i32
@@ -196,6 +199,38 @@ def spec_verify_rejection(logits: torch.Tensor, draft_ids: torch.Tensor,
     if rc != OK:
         raise SpecVerifyError("spec_verify_rejection", rc)
     return Result(out_tokens, accept_len, dev_status, None, out_probs)
+
+
+def spec_verify_block(logits: torch.Tensor, draft_ids: torch.Tensor,
+                      draft_probs: Optional[torch.Tensor] = None, *, temperature: float,
+                      seed: int, offset: int, out_tokens=None, accept_len=None, workspace=None,
+                      dev_status=None, stream=None) -> Result:
+    """Block verification of a chain: draft_probs [B, k, V] fp32, or None for one-hot drafts."""
+    lib = load_library()
+    _check_dev("logits", logits)
+    B, k1, V = logits.shape
+    k = k1 - 1
+    _check_dev("draft_ids", draft_ids, torch.int32)
+    if tuple(draft_ids.shape) != (B, k):
+        raise ValueError("draft_ids must be [B, k]")
+    if draft_probs is not None:
+        _check_dev("draft_probs", draft_probs, torch.float32)
+        if tuple(draft_probs.shape) != (B, k, V):
+            raise ValueError("draft_probs must be [B, k, V]")
+    dev = logits.device
+    stream = stream or torch.cuda.current_stream(dev)
+    out_tokens = out_tokens if out_tokens is not None else torch.empty((B, k1), dtype=torch.int32, device=dev)
+    accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    nbytes = spec_verify_workspace_bytes(MODE_BLOCK, B, k, V)
+    workspace, dev_status = _ws_and_status(nbytes, dev, stream, workspace, dev_status)
+    rc = lib.spec_verify_block(_ptr(logits), _logits_dtype(logits), _ptr(draft_ids), _ptr(draft_probs),
+                               B, k, V, float(temperature), int(seed) & (2**64 - 1),
+                               int(offset) & (2**64 - 1), _ptr(out_tokens), _ptr(accept_len),
+                               _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                               ctypes.c_void_p(stream.cuda_stream))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_block", rc)
+    return Result(out_tokens, accept_len, dev_status)
 
 
 def spec_verify_tree(logits: torch.Tensor, node_tokens: torch.Tensor, parents: torch.Tensor, *,

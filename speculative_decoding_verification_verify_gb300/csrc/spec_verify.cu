@@ -275,8 +275,9 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
                 F.ex_node[off] = n + 1;
             }
             F.dep[n] = n;
-            // With draft probabilities a rejected draft's row is left to the residual kernel.
-            F.need_draw[n] = SAMPLE && !(P.q && has);
+            // With draft probabilities a rejected draft's row is left to the residual kernel, and
+            // block verification with draft probabilities draws in the block kernel.
+            F.need_draw[n] = SAMPLE && !(P.q && has) && !(P.block && P.q);
         }
         __syncthreads();
         return;
@@ -543,7 +544,53 @@ template <bool SAMPLE>
 __device__ void decide_request(const Params &P, FinSmem &F, int lane)
 {
     if (F.status == 0) {
-        if (!P.is_tree) {
+        if (SAMPLE && !P.is_tree && P.block && !P.q) {
+            // Block verification with one-hot drafts (Sun et al.; "The speculative decoding zoo",
+            // block branch of the rejection sampler): the prefix of L drafts has joint weight
+            // w_L = prod_{i<L} p_i(x_{i+1}); candidate length L passes iff u_{L-1} < h_L, where
+            // h_L = r_L / (r_L + 1 - w_L) with r_L = w_L * (the non-child share of row L) below
+            // the last present draft, and h = w there.  The largest passing L is accepted.
+            const int k = P.k;
+            int ke = k;  // drafts present: an absent draft ends the block
+            for (int c0 = 0; c0 < k; c0 += 32) {
+                const unsigned m = __ballot_sync(0xffffffffu, c0 + lane < k && F.tok[c0 + lane + 1] < 0);
+                if (m) {
+                    ke = c0 + __ffs(m) - 1;
+                    break;
+                }
+            }
+            float wcarry = 1.f;
+            int j = 0;
+            for (int c0 = 0; c0 < ke; c0 += 32) {
+                const int i = c0 + lane, L = i + 1;
+                float w = i < ke ? F.node_p[i + 1] : 1.f;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, w, off);
+                    if (lane >= off) w *= y;
+                }
+                w *= wcarry;  // w_L
+                bool pass = false;
+                if (i < ke) {
+                    float h = w;
+                    if (L < ke) {
+                        const float r = w * F.row_z[L];
+                        const float denom = r + 1.f - w;
+                        h = denom > 0.f ? r / denom : 1.f;
+                    }
+                    pass = F.u[i] < h;
+                }
+                const unsigned m = __ballot_sync(0xffffffffu, pass);
+                if (m) j = c0 + 32 - __clz(m);
+                wcarry = __shfl_sync(0xffffffffu, w, 31);
+            }
+            for (int i = lane; i < j; i += 32) F.path[i] = i + 1;
+            if (lane == 0) {
+                F.L = j;
+                F.stop = j;
+                F.mode = 1;  // the token after the prefix: p with the next draft zeroed, or p
+            }
+        } else if (!P.is_tree) {
             // Chain: the first draft slot that is not accepted stops the round (warp ballots).
             {
                 const int k = P.k;
@@ -625,9 +672,42 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
         if (SAMPLE && !rs.bad && F.need_draw[n]) row_draw_prep(P, b, n, F, lane, rs);
     }
     __syncthreads();
-    if (warp == 0) decide_request<SAMPLE>(P, F, lane);
+    if (warp == 0 && !(P.block && P.q)) decide_request<SAMPLE>(P, F, lane);
     __syncthreads();
     const bool faulted = F.status != 0;
+
+    if (SAMPLE && P.block && P.q) {
+        // Block verification with draft probabilities: the residual masses need every row's
+        // statistics, so the block kernel decides and draws.  Hand it each present row's
+        // reference, total and prefix weight w_L = min(1, w_{L-1} p(x)/q(x)).
+        if (faulted) {
+            for (int i = tid; i <= P.k; i += blockDim.x) P.out_tokens[(int64_t)b * (P.k + 1) + i] = -1;
+            if (tid == 0) {
+                P.accept_len[b] = -1;
+                raise_status(P.dev_status, F.status);
+                P.pend[b] = make_int4(-1, 0, 0, 0);
+            }
+            return;
+        }
+        if (tid == 0) {
+            int ke = P.k;
+            for (int i = 0; i < P.k; ++i)
+                if (F.tok[i + 1] < 0) {
+                    ke = i;
+                    break;
+                }
+            float w = 1.f;
+            for (int L = 0; L <= ke; ++L) {
+                P.bpend[(int64_t)b * rpr + L] = make_float4(F.row_M[L], F.row_tot[L], w, 1.f);
+                if (L < ke) {
+                    const float px = F.node_p[L + 1], qx = F.qx[L + 1];
+                    w = (w * px <= 0.f) ? 0.f : (qx <= 0.f ? 1.f : fminf(1.f, w * px / qx));
+                }
+            }
+            P.pend[b] = make_int4(ke, 0, 0, 1);
+        }
+        return;
+    }
 
     // Outputs.
     const int out_w = P.is_tree ? rpr : P.k + 1;
@@ -751,7 +831,8 @@ struct ResidSrc {
     const float *qrow;
     int64_t col0, col1;  // part [col0, col1)
     float cs, mc, inv;
-    int use_p;           // draw from p instead (residual mass underflowed)
+    int use_p;           // draw from p instead (residual mass underflowed, or no draft here)
+    float w;             // prefix weight of block verification (1 for the standard residual)
     __device__ Raw prefetch(int64_t gi) const
     {
         Raw r;
@@ -760,7 +841,7 @@ struct ResidSrc {
             const int64_t c = col0 + gi * 8 + j;
             const bool in = c < col1;
             r.l[j] = in ? Elt<T>::load(row, c) : NEG_INF;
-            r.q[j] = in ? __ldg(qrow + c) : 0.f;
+            r.q[j] = (in && qrow) ? __ldg(qrow + c) : 0.f;
         }
         return r;
     }
@@ -769,7 +850,7 @@ struct ResidSrc {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float p = ex2(fmaf(r.l[j], cs, -mc)) * inv;
-            w[j] = use_p ? p : fmaxf(0.f, p - r.q[j]);
+            w[j] = use_p ? p : fmaxf(0.f, this->w * p - r.q[j]);
         }
         return (int)(col0 + gi * 8);
     }
@@ -882,7 +963,7 @@ __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
         const int64_t a0 = (int64_t)rc * P.Ec2, a1 = min(a0 + P.Ec2, V);
         const int64_t sp = (a1 - a0 + NW - 1) / NW;
         const int64_t s0 = min(a0 + rw * sp, a1), s1 = min(s0 + sp, a1);
-        ResidSrc<T> src{row, qrow, s0, s1, P.cs, mc, inv, F.mode};
+        ResidSrc<T> src{row, qrow, s0, s1, P.cs, mc, inv, F.mode, 1.f};
         draw_init(F.D, F.cum_before);
         draw_span<2>(src, (s1 - s0 + 7) / 8, F.take_last ? POS_INF : F.thresh, F.D);
         drawn = F.D.found >= 0 ? F.D.found : F.D.lastpos;
@@ -890,6 +971,181 @@ __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
     if (tid == 0) {
         P.out_tokens[(int64_t)b * (P.k + 1) + j] = drawn >= 0 ? drawn : 0;
         if (P.out_probs) P.out_probs[((int64_t)b * (P.k + 1) + j) * 3 + 2] = F.z;
+        P.cnt2[b] = 0u;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Block verification with draft probabilities ("The speculative decoding zoo", block branch of
+// the rejection sampler, after Sun et al.).  Grid (C2 chunks, rows, B): each CTA sums, over its
+// chunk of row L, the residual max(0, w_L p - q) and p per warp.  The last CTA of a request
+// (atomic arrival counter, nothing waits) forms r_L, the tests h_L = r_L / (r_L + 1 - w_L)
+// (h = w at the last present draft), takes the largest passing length j, and draws the next
+// token from max(0, w_j p_j - q_j) (from p_j at the last present draft) by locating the
+// crossing warp record and rescanning that part of the row.
+// ---------------------------------------------------------------------------------------------
+struct BlockSmem {
+    float r[MAX_RPR], z[MAX_RPR];  // per row: residual mass, p mass
+    int j;
+    int use_p;
+    float Z, t;
+    ResidSmem R;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(NT) sv_block_kernel(const Params P)
+{
+    __shared__ BlockSmem S;
+    __shared__ int is_last;
+    const int rpr = P.rpr;
+    const int c = (int)(blockIdx.x % (unsigned)P.C2);
+    const int rest = (int)(blockIdx.x / (unsigned)P.C2);
+    const int L = rest % rpr, b = rest / rpr;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int4 pd = P.pend[b];
+    if (pd.w != 1) return;
+    const int ke = pd.x;
+    if (L > ke) return;
+    const int64_t V = P.V;
+    {
+        const float4 bp = P.bpend[(int64_t)b * rpr + L];
+        const float mc = bp.x, inv = 1.f / bp.y, w = bp.z;
+        const int64_t r = (int64_t)b * rpr + L;
+        const void *row = reinterpret_cast<const T *>(P.logits) + r * V;
+        const float *qrow = L < P.k ? P.q + ((int64_t)b * P.k + L) * V : nullptr;
+        const int64_t cc0 = (int64_t)c * P.Ec2, cc1 = min(cc0 + P.Ec2, V);
+        const int64_t span = (cc1 - cc0 + NW - 1) / NW;
+        const int64_t w0 = min(cc0 + warp * span, cc1), w1 = min(w0 + span, cc1);
+        float zr = 0.f, zp = 0.f;
+        for (int64_t base = w0; base < w1; base += 32 * 8) {
+            float l[8], q[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t col = base + lane + 32 * u;
+                const bool in = col < w1;
+                l[u] = in ? Elt<T>::load(row, col) : NEG_INF;
+                q[u] = (in && qrow) ? __ldg(qrow + col) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float p = ex2(fmaf(l[u], P.cs, -mc)) * inv;
+                zp += p;
+                zr += fmaxf(0.f, w * p - q[u]);
+            }
+        }
+        zr = warp_sum(zr);
+        zp = warp_sum(zp);
+        if (lane == 0) P.recs3[(r * P.C2 + c) * NW + warp] = make_float2(zr, zp);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned old = atomicAdd(P.cnt2 + b, 1u);
+        is_last = (old == (unsigned)((ke + 1) * P.C2) - 1u);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+
+    // Last CTA of request b: row masses, the decision, then the draw.
+    const int per_row = P.C2 * NW;
+    for (int Lr = warp; Lr <= ke; Lr += NW) {
+        const float2 *rb = P.recs3 + ((int64_t)b * rpr + Lr) * per_row;
+        float a = 0.f, z = 0.f;
+        for (int t = lane; t < per_row; t += 32) {
+            const float2 x = __ldcg(rb + t);
+            a += x.x;
+            z += x.y;
+        }
+        a = warp_sum(a);
+        z = warp_sum(z);
+        if (lane == 0) {
+            S.r[Lr] = a;
+            S.z[Lr] = z;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int j = 0;
+        for (int Lc = 1; Lc <= ke; ++Lc) {
+            const float w = __ldcg(&P.bpend[(int64_t)b * rpr + Lc].z);
+            float h = w;
+            if (Lc < ke) {
+                const float denom = S.r[Lc] + 1.f - w;
+                h = denom > 0.f ? S.r[Lc] / denom : 1.f;
+            }
+            if (uniforms(P, (uint32_t)(Lc - 1), (uint32_t)b).x < h) j = Lc;
+        }
+        const int use_p = (j == ke) || !(S.r[j] > 0.f);
+        S.j = j;
+        S.use_p = use_p;
+        S.Z = use_p ? S.z[j] : S.r[j];
+        S.t = uniforms(P, (uint32_t)j, (uint32_t)b).y * S.Z;
+    }
+    __syncthreads();
+    const int j = S.j;
+    const float2 *rb = P.recs3 + ((int64_t)b * rpr + j) * per_row;
+    ResidSmem &F = S.R;
+    if (warp == 0) {
+        float cum = 0.f, before = 0.f, lp_before = 0.f;
+        int found = -1, lastpos = -1;
+        const float t = S.t;
+        for (int c0 = 0; c0 < per_row; c0 += 32) {
+            const int ti = c0 + lane;
+            float m = 0.f;
+            if (ti < per_row) {
+                const float2 x = __ldcg(rb + ti);
+                m = S.use_p ? x.y : x.x;
+            }
+            const float incl = warp_incl_scan(m, lane);
+            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+            if (lane == 0) excl = 0.f;
+            const unsigned hit = __ballot_sync(0xffffffffu, cum + incl > t);
+            const unsigned pos = __ballot_sync(0xffffffffu, m > 0.f);
+            if (pos) {
+                const int lp = 31 - __clz(pos);
+                lastpos = c0 + lp;
+                lp_before = cum + __shfl_sync(0xffffffffu, excl, lp);
+            }
+            if (hit) {
+                const int fl = __ffs(hit) - 1;
+                found = c0 + fl;
+                before = cum + __shfl_sync(0xffffffffu, excl, fl);
+                break;
+            }
+            cum += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            F.rec = found >= 0 ? found : lastpos;
+            F.cum_before = found >= 0 ? before : lp_before;
+            F.take_last = found < 0;
+        }
+    }
+    __syncthreads();
+    int drawn = -1;
+    if (F.rec >= 0) {
+        const int rc = F.rec / NW, rw = F.rec % NW;
+        const int64_t a0 = (int64_t)rc * P.Ec2, a1 = min(a0 + P.Ec2, V);
+        const int64_t sp = (a1 - a0 + NW - 1) / NW;
+        const int64_t s0 = min(a0 + rw * sp, a1), s1 = min(s0 + sp, a1);
+        const float4 bp = P.bpend[(int64_t)b * rpr + j];
+        const int64_t r = (int64_t)b * rpr + j;
+        const void *row = reinterpret_cast<const T *>(P.logits) + r * V;
+        const float *qrow = (j < P.k && !S.use_p) ? P.q + ((int64_t)b * P.k + j) * V : nullptr;
+        ResidSrc<T> src{row, qrow, s0, s1, P.cs, bp.x, 1.f / bp.y, S.use_p, bp.z};
+        draw_init(F.D, F.cum_before);
+        draw_span<2>(src, (s1 - s0 + 7) / 8, F.take_last ? POS_INF : S.t, F.D);
+        drawn = F.D.found >= 0 ? F.D.found : F.D.lastpos;
+    }
+    int32_t *ot = P.out_tokens + (int64_t)b * (P.k + 1);
+    for (int i = tid; i <= P.k; i += NT) {
+        int v = -1;
+        if (i < j) v = __ldg(P.drafts + (int64_t)b * P.k + i);
+        else if (i == j) v = drawn >= 0 ? drawn : 0;
+        ot[i] = v;
+    }
+    if (tid == 0) {
+        P.accept_len[b] = j;
         P.cnt2[b] = 0u;
     }
 }
@@ -920,7 +1176,7 @@ static int residual_chunks(int B, int64_t V)
 }
 
 struct Layout {
-    size_t cnt2, recs, caps, pend, recs2, total;
+    size_t cnt2, recs, caps, pend, recs2, bpend, recs3, total;
 };
 
 // Split the flat range: one CTA per resident slot of a GB300 (152 SMs x 3 streaming CTAs), but
@@ -954,7 +1210,7 @@ static int nsub_of(int64_t E, int64_t V, int vec)
     return (int)(n < 1 ? 1 : n);
 }
 
-static Layout layout(int B, int rpr, int64_t V)
+static Layout layout(int B, int rpr, int64_t V, bool block = false)
 {
     // The arrival counters sit in a fixed region at the start of every layout, so a workspace
     // shared by calls of different shapes never finds another call's records where its counters
@@ -977,13 +1233,19 @@ static Layout layout(int B, int rpr, int64_t V)
     off += align256(sizeof(int4) * (size_t)B);
     L.recs2 = off;
     off += align256(sizeof(float2) * (size_t)B * C2 * NW);
+    L.bpend = off;
+    L.recs3 = off;
+    if (block) {
+        off += align256(sizeof(float4) * (size_t)R);
+        L.recs3 = off;
+        off += align256(sizeof(float2) * (size_t)R * C2 * NW);
+    }
     L.total = off;
     return L;
 }
 
 struct DevInfo {
     int sms = 0;
-    int occ[2][2] = {{0, 0}, {0, 0}};  // [dtype][sample]
 };
 
 static std::mutex g_dev_mu;
@@ -998,15 +1260,6 @@ static const DevInfo *device_info()
     if (d.sms == 0) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
-        int o = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_stream_kernel<__nv_bfloat16, false>, NT, 0);
-        d.occ[0][0] = o > 0 ? o : 1;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_stream_kernel<__nv_bfloat16, true>, NT, 0);
-        d.occ[0][1] = o > 0 ? o : 1;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_stream_kernel<float, false>, NT, 0);
-        d.occ[1][0] = o > 0 ? o : 1;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_stream_kernel<float, true>, NT, 0);
-        d.occ[1][1] = o > 0 ? o : 1;
         cudaGetLastError();
         d.sms = sms;
     }
@@ -1015,18 +1268,17 @@ static const DevInfo *device_info()
 
 
 static int common_setup(Params &P, const void *logits, int dtype, int B, int rpr, int64_t V,
-                        void *workspace, size_t ws_bytes, bool sample, int &occ_out)
+                        void *workspace, size_t ws_bytes, bool block = false)
 {
     if (!logits || !workspace) return SPEC_VERIFY_EINVAL;
     if (dtype != SPEC_VERIFY_BF16 && dtype != SPEC_VERIFY_FP32) return SPEC_VERIFY_EINVAL;
     const int esize = dtype == SPEC_VERIFY_BF16 ? 2 : 4;
     if ((uintptr_t)logits % esize) return SPEC_VERIFY_EINVAL;
     if ((uintptr_t)workspace % 256) return SPEC_VERIFY_EWORKSPACE;
-    const Layout L = layout(B, rpr, V);
+    const Layout L = layout(B, rpr, V, block);
     if (ws_bytes < L.total) return SPEC_VERIFY_EWORKSPACE;
     const DevInfo *d = device_info();
     if (!d) return SPEC_VERIFY_ECUDA;
-    occ_out = d->occ[dtype == SPEC_VERIFY_FP32][sample ? 1 : 0];
     char *ws = static_cast<char *>(workspace);
     P.logits = logits;
     P.B = B;
@@ -1042,6 +1294,8 @@ static int common_setup(Params &P, const void *logits, int dtype, int B, int rpr
     P.caps = reinterpret_cast<float *>(ws + L.caps);
     P.pend = reinterpret_cast<int4 *>(ws + L.pend);
     P.recs2 = reinterpret_cast<float2 *>(ws + L.recs2);
+    P.bpend = reinterpret_cast<float4 *>(ws + L.bpend);
+    P.recs3 = reinterpret_cast<float2 *>(ws + L.recs3);
     P.C2 = residual_chunks(B, V);
     P.Ec2 = (V + P.C2 - 1) / P.C2;
     return SPEC_VERIFY_OK;
@@ -1098,7 +1352,7 @@ size_t spec_verify_workspace_bytes(int mode, int B, int k_or_N, int V)
 {
     if (B < 1 || B > B_MAX || V < 1) return 0;
     int rpr;
-    if (mode == SPEC_VERIFY_MODE_GREEDY || mode == SPEC_VERIFY_MODE_REJECTION) {
+    if (mode == SPEC_VERIFY_MODE_GREEDY || mode == SPEC_VERIFY_MODE_REJECTION || mode == SPEC_VERIFY_MODE_BLOCK) {
         if (k_or_N < 0 || k_or_N + 1 > MAX_RPR) return 0;
         rpr = k_or_N + 1;
     } else if (mode == SPEC_VERIFY_MODE_TREE) {
@@ -1107,7 +1361,7 @@ size_t spec_verify_workspace_bytes(int mode, int B, int k_or_N, int V)
     } else {
         return 0;
     }
-    return layout(B, rpr, V).total;
+    return layout(B, rpr, V, mode == SPEC_VERIFY_MODE_BLOCK).total;
 }
 
 const char *spec_verify_strerror(int code)
@@ -1134,8 +1388,7 @@ int spec_verify_greedy(const void *logits, int dtype, const int32_t *draft_ids, 
     if ((k > 0 && !draft_ids) || !out_tokens || !accept_len) return SPEC_VERIFY_EINVAL;
     Params P;
     memset(&P, 0, sizeof P);
-    int occ = 0;
-    int rc = common_setup(P, logits, dtype, B, k + 1, V, workspace, ws_bytes, false, occ);
+    int rc = common_setup(P, logits, dtype, B, k + 1, V, workspace, ws_bytes);
     if (rc) return rc;
     P.drafts = draft_ids;
     P.k = k;
@@ -1158,8 +1411,7 @@ int spec_verify_rejection(const void *logits, int dtype, const int32_t *draft_id
     if (draft_probs && ((uintptr_t)draft_probs % 4)) return SPEC_VERIFY_EINVAL;
     Params P;
     memset(&P, 0, sizeof P);
-    int occ = 0;
-    int rc = common_setup(P, logits, dtype, B, k + 1, V, workspace, ws_bytes, true, occ);
+    int rc = common_setup(P, logits, dtype, B, k + 1, V, workspace, ws_bytes);
     if (rc) return rc;
     P.drafts = draft_ids;
     P.q = (k > 0) ? draft_probs : nullptr;
@@ -1181,6 +1433,39 @@ int spec_verify_rejection(const void *logits, int dtype, const int32_t *draft_id
     return cudaGetLastError() == cudaSuccess ? SPEC_VERIFY_OK : SPEC_VERIFY_ECUDA;
 }
 
+int spec_verify_block(const void *logits, int dtype, const int32_t *draft_ids, const float *draft_probs,
+                      int B, int k, int V, float temperature, uint64_t seed, uint64_t offset,
+                      int32_t *out_tokens, int32_t *accept_len, void *workspace, size_t ws_bytes,
+                      int32_t *dev_status, void *stream)
+{
+    if (B < 1 || B > B_MAX || k < 0 || k + 1 > MAX_RPR || V < 1) return SPEC_VERIFY_EINVAL;
+    if ((k > 0 && !draft_ids) || !out_tokens || !accept_len) return SPEC_VERIFY_EINVAL;
+    if (!temperature_ok(temperature)) return SPEC_VERIFY_EINVAL;
+    if (draft_probs && ((uintptr_t)draft_probs % 4)) return SPEC_VERIFY_EINVAL;
+    Params P;
+    memset(&P, 0, sizeof P);
+    int rc = common_setup(P, logits, dtype, B, k + 1, V, workspace, ws_bytes, true);
+    if (rc) return rc;
+    P.drafts = draft_ids;
+    P.q = (k > 0) ? draft_probs : nullptr;
+    P.k = k;
+    P.is_tree = 0;
+    P.block = 1;
+    P.out_tokens = out_tokens;
+    P.accept_len = accept_len;
+    P.dev_status = dev_status;
+    set_rng(P, temperature, seed, offset);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = launch_stream<true>(P, dtype, s);
+    if (rc || !P.q) return rc;
+    const unsigned grid = (unsigned)P.C2 * (unsigned)(k + 1) * (unsigned)B;
+    if (dtype == SPEC_VERIFY_BF16)
+        sv_block_kernel<__nv_bfloat16><<<grid, NT, 0, s>>>(P);
+    else
+        sv_block_kernel<float><<<grid, NT, 0, s>>>(P);
+    return cudaGetLastError() == cudaSuccess ? SPEC_VERIFY_OK : SPEC_VERIFY_ECUDA;
+}
+
 int spec_verify_tree(const void *logits, int dtype, const int32_t *node_tokens,
                      const int32_t *parents, int B, int N, int V, int mode, float temperature,
                      uint64_t seed, uint64_t offset, int32_t *out_tokens, int32_t *accept_index,
@@ -1193,8 +1478,7 @@ int spec_verify_tree(const void *logits, int dtype, const int32_t *node_tokens,
     if (mode == 1 && !temperature_ok(temperature)) return SPEC_VERIFY_EINVAL;
     Params P;
     memset(&P, 0, sizeof P);
-    int occ = 0;
-    int rc = common_setup(P, logits, dtype, B, N, V, workspace, ws_bytes, mode == 1, occ);
+    int rc = common_setup(P, logits, dtype, B, N, V, workspace, ws_bytes);
     if (rc) return rc;
     P.node_tokens = node_tokens;
     P.parents = parents;

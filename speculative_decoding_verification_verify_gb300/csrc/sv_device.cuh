@@ -33,6 +33,7 @@ struct Params {
     const int32_t *node_tokens;  // tree: [B][N]
     const int32_t *parents;      // tree: [B][N]
     int B, k, rpr, is_tree;
+    int block;                   // chains: block verification instead of token-by-token
     int64_t V;
     double v_inv;                // 1 / V, for quick exact division by V
     float cs;                    // log2(e) / T: p is proportional to 2^(logit * cs)
@@ -52,6 +53,8 @@ struct Params {
     float *caps;                 // [B * rpr] logit of node j's token in its parent's row
     int4 *pend;                  // [B] residual draw pending: {row, mc bits, total bits, flag}
     float2 *recs2;               // [B * C2 * NW] residual-kernel records
+    float4 *bpend;               // block with q: [B * rpr] per row {max ref, total, prefix weight, 1}
+    float2 *recs3;               // block with q: [B * rpr * C2 * NW] per (row, chunk, warp) sums
     int C2;                      // residual-kernel column chunks per request
     int nsub;                    // sub-records per warp segment
     int64_t Ec2;                 // columns per residual chunk

@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_header_declares_the_abi():
     names = declared_functions()
-    for n in ("spec_verify_greedy", "spec_verify_rejection", "spec_verify_tree",
+    for n in ("spec_verify_greedy", "spec_verify_rejection", "spec_verify_tree", "spec_verify_block",
               "spec_verify_workspace_bytes", "spec_verify_strerror"):
         assert n in names
 
@@ -47,10 +47,13 @@ def test_workspace_bytes(lib):
     assert ws(binding.MODE_REJECTION, 0, 3, 100) == 0
     assert ws(7, 4, 3, 100) == 0
     assert ws(binding.MODE_REJECTION, 4, 3, 100) % 256 == 0
+    # Block verification adds per-row pending state and per-(row, chunk, warp) sums.
+    assert ws(binding.MODE_BLOCK, 64, 7, 128256) > ws(binding.MODE_REJECTION, 64, 7, 128256)
+    assert ws(binding.MODE_BLOCK, 4, 64, 100) == 0
 
 
 def test_strerror(lib):
-    for code in (0, -1, -2, -3, 1, 2, 3, 4, 12345):
+    for code in (0, -1, -2, -3, -4, 1, 2, 3, 4, 12345):
         s = binding.spec_verify_strerror(code)
         assert isinstance(s, str) and s
 
@@ -70,6 +73,14 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
                                      fake, None, fake, n, None, None) == -1
     assert lib.spec_verify_rejection(fake, 0, fake, None, 4, 64, 100, 1.0, 1, 0, fake, fake, None,
                                      fake, n, None, None) == -1
+    assert lib.spec_verify_block(fake, 0, fake, None, 4, 3, 100, 0.0, 1, 0, fake, fake, fake, n,
+                                 None, None) == -1
+    assert lib.spec_verify_block(fake, 0, fake, None, 4, 64, 100, 1.0, 1, 0, fake, fake, fake, n,
+                                 None, None) == -1
+    assert lib.spec_verify_block(fake, 0, fake, P(0x10002), 4, 3, 100, 1.0, 1, 0, fake, fake, fake,
+                                 n, None, None) == -1
+    assert lib.spec_verify_block(fake, 0, fake, None, 4, 3, 100, 1.0, 1, 0, fake, fake, fake,
+                                 ctypes.c_size_t(16), None, None) == -2
     assert lib.spec_verify_tree(fake, 0, fake, fake, 4, 8, 100, 2, 1.0, 1, 0, fake, fake, fake,
                                 fake, n, None, None) == -1
     assert lib.spec_verify_tree(fake, 0, fake, fake, 4, 65, 100, 1, 1.0, 1, 0, fake, fake, fake,
