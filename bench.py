@@ -511,6 +511,38 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
         ms = graph_time_ms(torch, [lambda i=i: tree(i) for i in range(GRAPH_CALLS)], 20)
         res[name] = _mode_entry(ms, Bt * Nt, tree_bytes(Bt, Nt, Vt, 2), peak, 2)
     del trees
+    # Block verification: one-hot on the headline workload, and with draft probabilities on the
+    # sweep's B=64, k=7 cell (logits 131 MB + q 230 MB per call, 3 sets).
+    sets = [wl.chain_b64k7(dev, seed=7000 + i) for i in range(N_SETS)]
+    nb = sv.spec_verify_workspace_bytes(sv.MODE_BLOCK, B, K_DRAFTS, V)
+    bws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+
+    def block(i, x, q):
+        check(lib.spec_verify_block(P(x.logits), sv.BF16, P(x.drafts), P(q), B, K_DRAFTS, V, 1.0, x.seed, i,
+                                    P(out), P(alen), P(bws), nb, P(status), cur()), "spec_verify_block")
+
+    ms = graph_time_ms(torch, [lambda i=i: block(i, sets[i % N_SETS], None) for i in range(GRAPH_CALLS)], 20)
+    res["block_b64k7_one_hot"] = _mode_entry(ms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2), peak, 2)
+    del sets
+    qsets = [wl.chain_sweep(dev, seed=7100 + i, B=B, k=K_DRAFTS, alpha=0.7) for i in range(N_SETS)]
+    ms = graph_time_ms(torch, [lambda i=i: block(i, qsets[i % N_SETS], qsets[i % N_SETS].q) for i in range(12)], 10)
+    nr = sv.spec_verify_workspace_bytes(sv.MODE_REJECTION, B, K_DRAFTS, V)
+    rws = torch.zeros(nr, dtype=torch.uint8, device=dev)
+
+    def standard_q(i, x):
+        check(lib.spec_verify_rejection(P(x.logits), sv.BF16, P(x.drafts), P(x.q), B, K_DRAFTS, V, 1.0, x.seed, i,
+                                        P(out), P(alen), None, P(rws), nr, P(status), cur()), "spec_verify_rejection")
+
+    sms = graph_time_ms(torch, [lambda i=i: standard_q(i, qsets[i % N_SETS]) for i in range(12)], 10)
+    res["standard_sweep_b64k7_with_q"] = _mode_entry(
+        sms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2, with_q=True), peak, 3,
+        note="algorithmic bytes count all of q; the residual kernel reads q only at rejected rows")
+    res["block_sweep_b64k7_with_q"] = _mode_entry(
+        ms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2, with_q=True), peak, 3,
+        note="algorithmic bytes count the logits and q once; the block kernel reads the logits and q "
+             "of the present rows a second time")
+    del qsets
+
     # Standard rejection, B=1 k=3 (2.6 MB: L2 flushed before each call).
     inp = wl.chain_b1k3(dev)
     Bq, kq, Vq = inp.shape
