@@ -351,3 +351,45 @@ def verify_tree(logits, tokens, parents, mode: int, T: float, seed: int, offset:
                                offset, _ptr(ids), n, _ptr(ot), _ptr(ai), _ptr(alen), _ptr(bnd),
                                _ptr(status)))
     return dict(out_tokens=ot, accept_index=ai, accept_len=alen, boundary=bnd, status=status)
+
+
+# ---------------------------------------------------------------------------------------
+# After tree verification: the accepted path's KV rows move to contiguous positions after the
+# committed prefix, and the committed length advances by the accepted nodes plus one ("投机解码",
+# SGLang: committed length plus the accepted count, and with topk > 1 the accepted path, which
+# is not contiguous in the tree, is moved to contiguous positions; the NGRAM walk-through in
+# "The speculative decoding zoo": verification, then move_accept_tokens_to_target_kvcache).
+# ---------------------------------------------------------------------------------------
+KV_OK, KV_BAD_POSITION, KV_BAD_SLOT = 0, 1, 2
+
+
+def kv_compact(pool, slot_table, committed, accept_index, accept_len):
+    """pool [num_slots, row] (any dtype, modified in place); slot_table [B, max_pos] int;
+    committed [B]; accept_index [B, N] (node 0, then the accepted nodes); accept_len [B]
+    (-1: a faulted request, left alone).  Tree node j was written at position committed + j.
+    Returns (new committed [B], status [B]).  The copies run in path order, one row at a time."""
+    pool = np.asarray(pool)
+    B, N = np.asarray(accept_index).shape
+    max_pos = np.asarray(slot_table).shape[1]
+    new = np.array(committed, dtype=np.int64).copy()
+    status = np.zeros(B, np.int32)
+    for b in range(B):
+        L = int(accept_len[b])
+        c = int(committed[b])
+        if L < 0:
+            continue
+        if c < 0 or c + N > max_pos or L >= N:
+            status[b] = KV_BAD_POSITION
+            continue
+        slots = [int(slot_table[b][c + int(accept_index[b][i])]) for i in range(L + 1)]
+        dests = [int(slot_table[b][c + i]) for i in range(L + 1)]
+        if any(s < 0 or s >= pool.shape[0] for s in slots + dests):
+            status[b] = KV_BAD_SLOT
+            continue
+        for i in range(1, L + 1):
+            src = slot_table[b][c + int(accept_index[b][i])]
+            dst = slot_table[b][c + i]
+            if src != dst:
+                pool[dst] = pool[src].copy()
+        new[b] = c + L + 1
+    return new.astype(np.int32), status
