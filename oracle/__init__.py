@@ -356,19 +356,24 @@ def verify_tree(logits, tokens, parents, mode: int, T: float, seed: int, offset:
 # ---------------------------------------------------------------------------------------
 # After tree verification: the accepted path's KV rows move to contiguous positions after the
 # committed prefix, and the committed length advances by the accepted nodes plus one ("投机解码",
-# SGLang: committed length plus the accepted count, and with topk > 1 the accepted path, which
-# is not contiguous in the tree, is moved to contiguous positions; the NGRAM walk-through in
-# "The speculative decoding zoo": verification, then move_accept_tokens_to_target_kvcache).
+# section 与调度、KV 的交互, SGLang part: committed length plus the accepted count, and with
+# topk > 1 the accepted path, which is not contiguous in the tree, is moved to contiguous
+# positions; "Draft sources: draft models, n-gram, suffix decoding", section "SGLang's suffix
+# automaton, in tree", the NGRAM decode-step walk-through: verification, then
+# move_accept_tokens_to_target_kvcache).
 # ---------------------------------------------------------------------------------------
 KV_OK, KV_BAD_POSITION, KV_BAD_SLOT = 0, 1, 2
 
 
 def kv_compact(pool, slot_table, committed, accept_index, accept_len):
-    """pool [num_slots, row] (any dtype, modified in place); slot_table [B, max_pos] int;
-    committed [B]; accept_index [B, N] (node 0, then the accepted nodes); accept_len [B]
-    (-1: a faulted request, left alone).  Tree node j was written at position committed + j.
-    Returns (new committed [B], status [B]).  The copies run in path order, one row at a time."""
+    """pool [num_slots, row] or [planes, num_slots, row] (any dtype, modified in place; a plane is
+    one layer's K or V); slot_table [B, max_pos] int; committed [B]; accept_index [B, N] (node 0,
+    then the accepted nodes); accept_len [B] (-1: a faulted request, left alone).  Tree node j was
+    written at position committed + j.  Returns (new committed [B], status [B]).  The copies run
+    in path order, one row (in every plane) at a time."""
     pool = np.asarray(pool)
+    planes = pool if pool.ndim == 3 else pool[None]
+    num_slots = planes.shape[1]
     B, N = np.asarray(accept_index).shape
     max_pos = np.asarray(slot_table).shape[1]
     new = np.array(committed, dtype=np.int64).copy()
@@ -378,18 +383,18 @@ def kv_compact(pool, slot_table, committed, accept_index, accept_len):
         c = int(committed[b])
         if L < 0:
             continue
-        if c < 0 or c + N > max_pos or L >= N:
+        path = [int(accept_index[b][i]) for i in range(L + 1)] if L < N else []
+        if c < 0 or c + N > max_pos or L >= N or any(a < 0 or a >= N for a in path):
             status[b] = KV_BAD_POSITION
             continue
-        slots = [int(slot_table[b][c + int(accept_index[b][i])]) for i in range(L + 1)]
+        slots = [int(slot_table[b][c + a]) for a in path]
         dests = [int(slot_table[b][c + i]) for i in range(L + 1)]
-        if any(s < 0 or s >= pool.shape[0] for s in slots + dests):
+        if any(s < 0 or s >= num_slots for s in slots + dests):
             status[b] = KV_BAD_SLOT
             continue
         for i in range(1, L + 1):
-            src = slot_table[b][c + int(accept_index[b][i])]
-            dst = slot_table[b][c + i]
+            src, dst = slots[i], dests[i]
             if src != dst:
-                pool[dst] = pool[src].copy()
+                planes[:, dst] = planes[:, src].copy()
         new[b] = c + L + 1
     return new.astype(np.int32), status

@@ -84,3 +84,27 @@ def test_faulted_and_out_of_range_requests_are_left_alone(oracle):
             s = st[b, pos]
             if 0 <= s < pool.shape[0]:
                 np.testing.assert_array_equal(pool[s], before[s])
+
+
+def test_planes_move_together_and_bad_indices_are_rejected(oracle):
+    rng = np.random.default_rng(3)
+    pool, st, c, ai, al = _case(rng)
+    stack = np.stack([pool, pool * 2.0, -pool])  # three planes (layers' K or V)
+    ref = pool.copy()
+    new2, _ = oracle.kv_compact(ref, st, c, ai, al)
+    new3, status = oracle.kv_compact(stack, st, c, ai, al)
+    assert not status.any()
+    np.testing.assert_array_equal(new2, new3)
+    np.testing.assert_array_equal(stack[0], ref)
+    np.testing.assert_array_equal(stack[1], ref * 2.0)
+    np.testing.assert_array_equal(stack[2], -ref)
+    # An accept_index entry outside [0, N) on the accepted path is a position error.
+    b = int(np.argmax(al))
+    assert al[b] >= 1
+    ai2 = ai.copy()
+    ai2[b, al[b]] = ai.shape[1]
+    before = pool.copy()
+    new, status = oracle.kv_compact(pool, st, c, ai2, al)
+    assert status[b] == oracle.KV_BAD_POSITION and new[b] == c[b]
+    for pos in range(st.shape[1]):
+        np.testing.assert_array_equal(pool[st[b, pos]], before[st[b, pos]])
