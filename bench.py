@@ -36,7 +36,8 @@ B, K_DRAFTS, V = 64, 7, 128256
 N_SETS = 3  # rotating input sets: 3 x 131 MB > L2 (129 MB)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_call_b64k7_traffic.json")
 LAUNCHES_PER_CALL = 2  # sv_stream_kernel, then sv_finalize_kernel (programmatic dependent launch)
-GRAPH_CALLS = 30       # verify calls captured in one CUDA graph for the timed region
+GRAPH_CALLS = 30  # verify calls captured in one CUDA graph for the timed region
+KV_SETS = 8       # KV-compaction index sets rotated over one pool
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_verify_gb300", "csrc", f)
                   for f in ("spec_verify.cu", "sv_device.cuh", "sv_draw.cuh", "sv_stream.cuh", "sv_rescan.cuh")]
@@ -58,6 +59,11 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work spent timing the oracle baseline")
     ap.add_argument("--no-modes", action="store_true", help="skip the other verify modes")
+    ap.add_argument("--modes", default="all",
+                    help="comma list of other modes to time: greedy, tree, block, with_q, b1k3, "
+                         "kv_compact (default all)")
+    ap.add_argument("--kv-max-pos", type=int, default=512,
+                    help="positions per request of the KV-compaction cache (512: 3.2 GB)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     return ap.parse_args()
 
@@ -478,10 +484,30 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
             raise RuntimeError(f"{name} returned {rc}")
 
     res = {}
-    # Greedy on the headline workload (3 rotating sets > L2).
-    sets = [wl.chain_b64k7(dev, seed=5000 + i) for i in range(N_SETS)]
+    names = {"greedy", "tree", "block", "with_q", "b1k3", "kv_compact"}
+    want = names if args.modes == "all" else set(args.modes.split(","))
+    if want - names:
+        raise SystemExit(f"unknown modes {sorted(want - names)}; known: {sorted(names)}")
     out = torch.empty((B, K_DRAFTS + 1), dtype=torch.int32, device=dev)
     alen = torch.empty(B, dtype=torch.int32, device=dev)
+    if "greedy" in want:
+        res.update(_greedy_mode(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak))
+    if "tree" in want:
+        res.update(_tree_modes(torch, sv, wl, dev, lib, P, cur, check, status, peak))
+    if want & {"block", "with_q"}:
+        res.update(_block_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak, want))
+    if "b1k3" in want:
+        res.update(_b1k3_mode(torch, sv, wl, dev, lib, P, cur, check, status, peak))
+    if "kv_compact" in want:
+        res.update(_kv_mode(torch, wl, dev, lib, P, cur, check, status, peak, args.kv_max_pos))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the other modes")
+    return res
+
+
+def _greedy_mode(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak):
+    """Greedy on the headline workload (3 rotating sets > L2)."""
+    sets = [wl.chain_b64k7(dev, seed=5000 + i) for i in range(N_SETS)]
     nb = sv.spec_verify_workspace_bytes(sv.MODE_GREEDY, B, K_DRAFTS, V)
     ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
 
@@ -491,9 +517,12 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
                                      P(ws), nb, P(status), cur()), "spec_verify_greedy")
 
     ms = graph_time_ms(torch, [lambda i=i: greedy(i) for i in range(GRAPH_CALLS)], 20)
-    res["greedy_b64k7"] = _mode_entry(ms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2), peak, 2)
-    del sets
-    # Tree, both modes (3 x 117 MB).
+    return {"greedy_b64k7": _mode_entry(ms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2), peak, 2)}
+
+
+def _tree_modes(torch, sv, wl, dev, lib, P, cur, check, status, peak):
+    """Tree, both modes (3 x 117 MB)."""
+    res = {}
     trees = [wl.tree_b48(dev, seed=6000 + i) for i in range(N_SETS)]
     Bt, Nt, Vt = trees[0].shape
     tout = torch.empty((Bt, Nt), dtype=torch.int32, device=dev)
@@ -510,10 +539,14 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
 
         ms = graph_time_ms(torch, [lambda i=i: tree(i) for i in range(GRAPH_CALLS)], 20)
         res[name] = _mode_entry(ms, Bt * Nt, tree_bytes(Bt, Nt, Vt, 2), peak, 2)
-    del trees
-    # Block verification: one-hot on the headline workload, and with draft probabilities on the
-    # sweep's B=64, k=7 cell (logits 131 MB + q 230 MB per call, 3 sets).
-    sets = [wl.chain_b64k7(dev, seed=7000 + i) for i in range(N_SETS)]
+    return res
+
+
+def _block_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak, want):
+    """Block verification: one-hot on the headline workload, and with draft probabilities (with
+    the standard rule beside it) on the sweep's B=64, k=7 cell (logits 131 MB + q 230 MB per
+    call, 3 sets)."""
+    res = {}
     nb = sv.spec_verify_workspace_bytes(sv.MODE_BLOCK, B, K_DRAFTS, V)
     bws = torch.zeros(nb, dtype=torch.uint8, device=dev)
 
@@ -521,9 +554,13 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
         check(lib.spec_verify_block(P(x.logits), sv.BF16, P(x.drafts), P(q), B, K_DRAFTS, V, 1.0, x.seed, i,
                                     P(out), P(alen), P(bws), nb, P(status), cur()), "spec_verify_block")
 
-    ms = graph_time_ms(torch, [lambda i=i: block(i, sets[i % N_SETS], None) for i in range(GRAPH_CALLS)], 20)
-    res["block_b64k7_one_hot"] = _mode_entry(ms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2), peak, 2)
-    del sets
+    if "block" in want:
+        sets = [wl.chain_b64k7(dev, seed=7000 + i) for i in range(N_SETS)]
+        ms = graph_time_ms(torch, [lambda i=i: block(i, sets[i % N_SETS], None) for i in range(GRAPH_CALLS)], 20)
+        res["block_b64k7_one_hot"] = _mode_entry(ms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2), peak, 2)
+        del sets
+    if "with_q" not in want:
+        return res
     qsets = [wl.chain_sweep(dev, seed=7100 + i, B=B, k=K_DRAFTS, alpha=0.7) for i in range(N_SETS)]
     ms = graph_time_ms(torch, [lambda i=i: block(i, qsets[i % N_SETS], qsets[i % N_SETS].q) for i in range(12)], 10)
     nr = sv.spec_verify_workspace_bytes(sv.MODE_REJECTION, B, K_DRAFTS, V)
@@ -542,8 +579,11 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
         note="algorithmic bytes count the logits and q once; the block kernel reads the logits and q "
              "of the present rows a second time")
     del qsets
+    return res
 
-    # Standard rejection, B=1 k=3 (2.6 MB: L2 flushed before each call).
+
+def _b1k3_mode(torch, sv, wl, dev, lib, P, cur, check, status, peak):
+    """Standard rejection, B=1 k=3 (2.6 MB: L2 flushed before each call)."""
     inp = wl.chain_b1k3(dev)
     Bq, kq, Vq = inp.shape
     qout = torch.empty((Bq, kq + 1), dtype=torch.int32, device=dev)
@@ -558,11 +598,45 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
                                         P(status), cur()), "spec_verify_rejection")
 
     ms = graph_time_ms(torch, [standard], 100, flush=lambda: flush_buf.zero_())
-    res["standard_b1k3"] = _mode_entry(ms, Bq * (kq + 1), chain_bytes(Bq, kq, Vq, 2, with_q=True),
-                                       peak, 3, note="latency-bound; L2 flushed before each call; "
-                                       "algorithmic bytes count all of q")
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} in the other modes")
+    return {"standard_b1k3": _mode_entry(ms, Bq * (kq + 1), chain_bytes(Bq, kq, Vq, 2, with_q=True),
+                                         peak, 3, note="latency-bound; L2 flushed before each call; "
+                                         "algorithmic bytes count all of q")}
+
+
+def _kv_mode(torch, wl, dev, lib, P, cur, check, status, peak, max_pos):
+    """KV compaction after tree verification: a Llama-3-8B-sized cache (64 planes of 2048-byte
+    rows; 3.2 GB at 512 positions a request), B=48 requests of N=8 nodes; KV_SETS index sets over
+    the one pool, so the rows a call moves (about 9 MB) are not in L2 from the last call that
+    touched them."""
+    res = {}
+    kvs = [wl.kv_paged(dev, seed=8000, max_pos=max_pos)]
+    for i in range(1, KV_SETS):
+        kvs.append(wl.kv_paged(dev, seed=8000 + i, max_pos=max_pos, pool=kvs[0].pool))
+    pool = kvs[0].pool
+    planes, num_slots, row_el = pool.shape
+    row_bytes = row_el * pool.element_size()
+    Bk, Nk = kvs[0].accept_index.shape
+    c_out = torch.empty(Bk, dtype=torch.int32, device=dev)
+    moved = 0
+    for x in kvs:
+        ai, al = x.accept_index.cpu(), x.accept_len.cpu()
+        moved += sum(int((ai[b, 1:int(al[b]) + 1] != torch.arange(1, int(al[b]) + 1)).sum()) for b in range(Bk))
+
+    def kv(i):
+        x = kvs[i]
+        check(lib.spec_verify_kv_compact(P(pool), num_slots, row_bytes, planes, pool.stride(0) * pool.element_size(),
+                                         P(x.slot_table), x.slot_table.shape[1], P(x.committed), P(c_out),
+                                         P(x.accept_index), P(x.accept_len), Bk, Nk, P(status), cur()),
+              "spec_verify_kv_compact")
+
+    ms = graph_time_ms(torch, [lambda i=i: kv(i) for i in range(KV_SETS)], 20)
+    alg = (2 * moved * planes * row_bytes) / KV_SETS + Bk * (Nk * 4 + 12 + 2 * (Nk + 1) * 4)
+    e = _mode_entry(ms, Bk * Nk, alg, peak, 1,
+                    note="rows_moved_per_call counts accepted-path rows whose slot changes; algorithmic "
+                         "bytes = read + write of those rows in every plane, plus the index reads")
+    e["rows_moved_per_call"] = moved / KV_SETS
+    e["planes"], e["row_bytes"], e["max_pos"] = int(planes), int(row_bytes), int(max_pos)
+    res["kv_compact_b48_llama8b"] = e
     return res
 
 

@@ -71,6 +71,9 @@ extern "C" {
 #define SPEC_VERIFY_DEV_BAD_ROW 2     /* a logit row holding NaN or +inf, or no finite value */
 #define SPEC_VERIFY_DEV_BAD_TREE 3    /* parents[0] != -1, or parents[j] outside [0, j) */
 #define SPEC_VERIFY_DEV_DUP_SIBLING 4 /* two children of one node share a token (target-only) */
+#define SPEC_VERIFY_DEV_BAD_KV_POSITION 5 /* KV compaction: committed + N beyond the slot table,
+                                             accept_len >= N, or a path entry outside [0, N) */
+#define SPEC_VERIFY_DEV_BAD_KV_SLOT 6     /* KV compaction: a slot outside [0, num_slots) */
 
 /* Modes for spec_verify_workspace_bytes. */
 #define SPEC_VERIFY_MODE_GREEDY 0
@@ -160,6 +163,37 @@ int spec_verify_tree(const void *logits, int dtype, const int32_t *node_tokens,
                      uint64_t seed, uint64_t offset, int32_t *out_tokens, int32_t *accept_index,
                      int32_t *accept_len, void *workspace, size_t ws_bytes, int32_t *dev_status,
                      void *stream);
+
+/*
+ * After tree verification: move each request's accepted-path KV rows to contiguous positions
+ * after its committed prefix, and advance the committed length ("投机解码", section
+ * 与调度、KV 的交互, SGLang part: the committed length grows by the accepted count, and with
+ * topk > 1 the accepted path is moved to contiguous positions; "Draft sources: draft models,
+ * n-gram, suffix decoding", section "SGLang's suffix automaton, in tree", NGRAM walk-through:
+ * verification, then move_accept_tokens_to_target_kvcache).  The pages give the operation, not a
+ * layout; ours:
+ *   kv_pool       device memory, 16-byte aligned: `planes` planes (one per layer and K or V)
+ *                 plane_stride_bytes apart, each [num_slots][row_bytes] (any element type;
+ *                 row_bytes a multiple of 16; plane_stride_bytes a multiple of 16 and at least
+ *                 num_slots * row_bytes; ignored when planes = 1)
+ *   slot_table    [B][max_pos] int32: pool slot of each position of request b
+ *   committed_in  [B] int32: committed positions; the verify forward wrote tree node j's KV at
+ *                 position committed_in[b] + j (j < N)
+ *   committed_out [B] int32 (must not alias committed_in): committed_in + accept_len + 1, or
+ *                 committed_in unchanged for a request with accept_len = -1 or a fault
+ *   accept_index  [B][N], accept_len [B]: as spec_verify_tree writes them
+ * For i = 1..accept_len, in order, the row at position committed + accept_index[i] is copied to
+ * position committed + i in every plane (skipped where both are the same slot).  Requests must
+ * not share slots.  Device status codes 5 (committed + N beyond max_pos, accept_len >= N, or a
+ * path entry outside [0, N)) and 6 (a slot outside [0, num_slots)) mark requests that are left
+ * unchanged.  Host codes: SPEC_VERIFY_EINVAL for bad pointers or sizes (B > 65535, N > 64,
+ * max_pos < N), SPEC_VERIFY_ECUDA for a failed launch.  Asynchronous on `stream`.
+ */
+int spec_verify_kv_compact(void *kv_pool, int64_t num_slots, size_t row_bytes, int planes,
+                           size_t plane_stride_bytes, const int32_t *slot_table, int max_pos,
+                           const int32_t *committed_in, int32_t *committed_out,
+                           const int32_t *accept_index, const int32_t *accept_len, int B, int N,
+                           int32_t *dev_status, void *stream);
 
 /*
  * Workspace bytes needed by one call of the given mode (SPEC_VERIFY_MODE_*) with B requests,

@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     load_library,
     spec_verify_block,
     spec_verify_greedy,
+    spec_verify_kv_compact,
     spec_verify_philox,
     spec_verify_rejection,
     spec_verify_strerror,

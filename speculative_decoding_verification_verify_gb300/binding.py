@@ -21,6 +21,7 @@ MODE_GREEDY, MODE_REJECTION, MODE_TREE, MODE_BLOCK = 0, 1, 2, 3
 OK, EINVAL, EWORKSPACE, ECUDA, ETOOBIG = 0, -1, -2, -3, -4
 NOALLOC_SCRATCH_BYTES = 4 << 20
 DEV_OK, DEV_BAD_TOKEN, DEV_BAD_ROW, DEV_BAD_TREE, DEV_DUP_SIBLING = 0, 1, 2, 3, 4
+DEV_BAD_KV_POSITION, DEV_BAD_KV_SLOT = 5, 6
 
 _lib = None
 _lock = threading.Lock()
@@ -63,6 +64,9 @@ def load_library():
         lib.spec_verify_rejection_noalloc.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, u64,
                                                       u64, vp, vp, vp, vp, vp]
         lib.spec_verify_rejection_noalloc.restype = i32
+        lib.spec_verify_kv_compact.argtypes = [vp, ctypes.c_int64, sz, i32, sz, vp, i32, vp, vp,
+                                               vp, vp, i32, i32, vp, vp]
+        lib.spec_verify_kv_compact.restype = i32
         _lib = lib
         return lib
 
@@ -305,3 +309,54 @@ def spec_verify_rejection_noalloc(logits: torch.Tensor, draft_ids: torch.Tensor,
     if rc != OK:
         raise SpecVerifyError("spec_verify_rejection_noalloc", rc)
     return Result(out_tokens, accept_len, dev_status, None, out_probs)
+
+
+def spec_verify_kv_compact(kv_pool: torch.Tensor, slot_table: torch.Tensor,
+                           committed: torch.Tensor, accept_index: torch.Tensor,
+                           accept_len: torch.Tensor, *, stacked: bool = False, committed_out=None,
+                           dev_status=None, stream=None):
+    """Move each request's accepted-path KV rows (as spec_verify_tree reports them) to the
+    positions right after its committed prefix, in place in kv_pool, and return
+    (committed_out, dev_status).
+
+    kv_pool is [num_slots, ...] with contiguous slot rows, or with stacked=True
+    [planes, num_slots, ...] (one plane per layer and K or V) where each plane is contiguous and
+    planes may be any 16-byte multiple apart; a slot row's bytes must be a multiple of 16.
+    slot_table [B, max_pos], committed [B], accept_index [B, N] and accept_len [B] are int32
+    CUDA tensors."""
+    lib = load_library()
+    if not kv_pool.is_cuda:
+        raise ValueError("kv_pool must be a CUDA tensor")
+    for name, t in (("slot_table", slot_table), ("committed", committed),
+                    ("accept_index", accept_index), ("accept_len", accept_len)):
+        _check_dev(name, t, torch.int32)
+    B, N = accept_index.shape
+    if slot_table.dim() != 2 or slot_table.shape[0] != B or tuple(committed.shape) != (B,) \
+            or tuple(accept_len.shape) != (B,):
+        raise ValueError("slot_table must be [B, max_pos], committed and accept_len [B]")
+    if stacked:
+        if kv_pool.dim() < 3 or not kv_pool[0].is_contiguous():
+            raise ValueError("a stacked kv_pool is [planes, num_slots, ...] with contiguous planes")
+        planes, num_slots = kv_pool.shape[0], kv_pool.shape[1]
+        row_bytes = kv_pool[0, 0].numel() * kv_pool.element_size()
+        plane_stride = kv_pool.stride(0) * kv_pool.element_size()
+    else:
+        if kv_pool.dim() < 2 or not kv_pool.is_contiguous():
+            raise ValueError("kv_pool must be a contiguous [num_slots, ...] tensor")
+        planes, num_slots = 1, kv_pool.shape[0]
+        row_bytes = kv_pool[0].numel() * kv_pool.element_size()
+        plane_stride = 0
+    dev = kv_pool.device
+    stream = stream or torch.cuda.current_stream(dev)
+    if committed_out is None:
+        committed_out = torch.empty(B, dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    rc = lib.spec_verify_kv_compact(_ptr(kv_pool), int(num_slots), int(row_bytes), int(planes),
+                                    int(plane_stride), _ptr(slot_table), slot_table.shape[1],
+                                    _ptr(committed), _ptr(committed_out), _ptr(accept_index),
+                                    _ptr(accept_len), B, N, _ptr(dev_status),
+                                    ctypes.c_void_p(stream.cuda_stream))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_kv_compact", rc)
+    return committed_out, dev_status

@@ -1376,6 +1376,8 @@ const char *spec_verify_strerror(int code)
     case SPEC_VERIFY_DEV_BAD_ROW: return "device: a logit row holds NaN or +inf, or no finite value";
     case SPEC_VERIFY_DEV_BAD_TREE: return "device: malformed tree (parents[0] != -1 or parents[j] outside [0, j))";
     case SPEC_VERIFY_DEV_DUP_SIBLING: return "device: two children of one node share a token";
+    case SPEC_VERIFY_DEV_BAD_KV_POSITION: return "device: KV compaction positions outside the slot table";
+    case SPEC_VERIFY_DEV_BAD_KV_SLOT: return "device: KV compaction slot outside the pool";
     default: return "unknown status code";
     }
 }

@@ -22,6 +22,13 @@ verifier is specified on):
                 has it), else a uniform token distinct from its siblings.
   chain_sweep   B x k grid, V=128256 bf16 ~ N(0, 3^2); draft logits = target + N(0, sigma^2)
                 with sigma bisected so that the mean of sum(min(p, q)) is alpha; T = 1.
+  kv_paged      the KV cache that tree verification's accepted path is compacted in: planes =
+                layers x (K, V) = 64 and 2048-byte rows (8 KV heads x 128 dims, bf16) as in a
+                Llama-3-8B-sized target, B=48 requests of N=8 nodes, max_pos=512 positions each,
+                every position mapped to a distinct pool slot by a random permutation (a paged
+                allocator with one-token pages); committed uniform in [0, max_pos - N]; the
+                accepted path walks a tree_b48-shaped random tree from the root, taking a uniform
+                child and stopping with probability 0.3 before each step; pool bits uniform.
 """
 from __future__ import annotations
 
@@ -188,6 +195,49 @@ def chain_sweep(device="cpu", seed=1238, B=8, k=3, V=128256, alpha=0.7, T=1.0) -
               if k > 0 else torch.zeros((B, 0), dtype=torch.int32, device=device))
     return ChainInputs(f"chain_sweep_B{B}_k{k}_a{alpha}", logits.contiguous(), drafts.contiguous(),
                        q, T, seed + 17, meta=dict(alpha=alpha, sigma=sigma))
+
+
+@dataclass
+class KVInputs:
+    name: str
+    pool: torch.Tensor              # [planes, num_slots, row_bytes / 2] int16 (KV bit patterns)
+    slot_table: torch.Tensor        # [B, max_pos] int32
+    committed: torch.Tensor         # [B] int32
+    accept_index: torch.Tensor      # [B, N] int32 (root, then the path; -1 after it)
+    accept_len: torch.Tensor        # [B] int32
+
+
+def kv_paged(device="cpu", seed=1239, B=48, N=8, planes=64, row_bytes=2048, max_pos=512,
+             topk=4, steps=5, p_stop=0.3, extra_slots=0, pool=None) -> KVInputs:
+    """pool: reuse an existing [planes, num_slots, row_bytes / 2] int16 pool instead of drawing
+    one (other seeds then give other positions, slots and paths over the same cache)."""
+    rng = np.random.default_rng(seed)
+    num_slots = B * max_pos + extra_slots
+    slot_table = rng.permutation(num_slots)[: B * max_pos].astype(np.int32).reshape(B, max_pos)
+    committed = rng.integers(0, max_pos - N + 1, B).astype(np.int32)
+    accept_index = np.full((B, N), -1, np.int32)
+    accept_len = np.zeros(B, np.int32)
+    for b in range(B):
+        parents = _random_tree(rng, N, topk, steps)
+        path, cur = [0], 0
+        while True:
+            kids = np.flatnonzero(parents == cur)
+            kids = kids[kids > 0]
+            if kids.size == 0 or rng.random() < p_stop:
+                break
+            cur = int(rng.choice(kids))
+            path.append(cur)
+        accept_index[b, : len(path)] = path
+        accept_len[b] = len(path) - 1
+    if pool is None:
+        g = _gen(device, seed)
+        pool = torch.randint(-32768, 32768, (planes, num_slots, row_bytes // 2), generator=g,
+                             device=device, dtype=torch.int16)
+    elif tuple(pool.shape) != (planes, num_slots, row_bytes // 2) or pool.dtype != torch.int16:
+        raise ValueError("pool does not match the requested shape")
+    t = lambda a: torch.from_numpy(a).to(device)  # noqa: E731
+    return KVInputs(f"kv_paged_B{B}_N{N}_planes{planes}_row{row_bytes}", pool, t(slot_table),
+                    t(committed), t(accept_index), t(accept_len))
 
 
 # --------------------------------------------------------------------------------------------

@@ -53,7 +53,7 @@ def test_workspace_bytes(lib):
 
 
 def test_strerror(lib):
-    for code in (0, -1, -2, -3, -4, 1, 2, 3, 4, 12345):
+    for code in (0, -1, -2, -3, -4, 1, 2, 3, 4, 5, 6, 12345):
         s = binding.spec_verify_strerror(code)
         assert isinstance(s, str) and s
 
@@ -91,4 +91,18 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert lib.spec_verify_greedy(fake, 0, fake, 4, 3, 100, fake, fake, P(0x10008), n, None,
                                   None) == -2
     assert lib.spec_verify_philox(1, 0, 0, 4, fake, None) == -1
+    # KV compaction: (pool, num_slots, row_bytes, planes, plane_stride, slot_table, max_pos,
+    # committed_in, committed_out, accept_index, accept_len, B, N, dev_status, stream)
+    kv = lib.spec_verify_kv_compact
+    c_out = P(0x20000)
+    assert kv(fake, 100, 40, 1, 0, fake, 64, fake, c_out, fake, fake, 4, 8, None, None) == -1  # row % 16
+    assert kv(P(0x10008), 100, 48, 1, 0, fake, 64, fake, c_out, fake, fake, 4, 8, None, None) == -1
+    assert kv(fake, 100, 48, 1, 0, fake, 64, fake, fake, fake, fake, 4, 8, None, None) == -1  # alias
+    assert kv(fake, 100, 48, 1, 0, fake, 64, fake, c_out, fake, fake, 4, 65, None, None) == -1
+    assert kv(fake, 100, 48, 1, 0, fake, 6, fake, c_out, fake, fake, 4, 8, None, None) == -1  # max_pos < N
+    assert kv(fake, 100, 48, 1, 0, fake, 64, fake, c_out, fake, fake, 0, 8, None, None) == -1
+    assert kv(fake, 100, 48, 2, 48 * 99, fake, 64, fake, c_out, fake, fake, 4, 8, None, None) == -1
+    assert kv(fake, 100, 48, 2, 48 * 100 + 8, fake, 64, fake, c_out, fake, fake, 4, 8, None,
+              None) == -1
+    assert kv(None, 100, 48, 1, 0, fake, 64, fake, c_out, fake, fake, 4, 8, None, None) == -1
     del ws
