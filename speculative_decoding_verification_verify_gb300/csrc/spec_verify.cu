@@ -5,12 +5,14 @@
 // 接受规则为什么不改变分布; "The speculative decoding zoo", mlinterviewnotes 06-06, DFlash and
 // verification-method sections):
 //
-//   sv_stream_kernel   -- one pass over all B * rows * V logits.  The flat range is split evenly
-//                         over G persistent CTAs.  Each warp keeps a running (max, sum of
-//                         2^(l*cs - max*cs)) over its contiguous segment, skipping the tokens
-//                         that are drafts of the row (their logits are captured instead), or a
-//                         running argmax (greedy), and writes one record per SUB_VEC vectors of
-//                         its segment, carrying the columns it covers.
+//   sv_stream_kernel   -- one pass over all B * rows * V logits.  Each row is cut into chunks of
+//                         CHUNK_VEC 16-byte vectors; one CTA per SM takes an equal run of the
+//                         chunks, and its warps claim them one at a time from a shared counter,
+//                         so every warp of an SM keeps streaming until the SM's run is done.  A
+//                         warp folds its chunk into a (max, sum of 2^(l*cs - max*cs)) record,
+//                         skipping the tokens that are children of the row's node (their logits
+//                         are captured instead), or into an argmax record (greedy); a record
+//                         carries the columns it covers.
 //   sv_finalize_kernel -- one CTA per request, launched as a programmatic dependent of the
 //                         streaming kernel: it stages the request's inputs, waits for the records,
 //                         merges them per row, decides acceptance (warp-ballot first-reject scan
@@ -37,17 +39,9 @@
 
 namespace sv {
 
-#ifndef SV_MINB
-#define SV_MINB 3
-#endif
-constexpr int NT_FIN_MAX = 256;  // most threads of a finalising CTA: one warp per row, up to 8 rows
+constexpr int NT_FIN_MAX = 256;  // threads of a finalising CTA: one warp per row, up to 8 rows
+static_assert(NT_FIN_MAX == RESCAN_THREADS, "the stop row's rescan uses the whole finalising CTA");
 
-
-struct StreamSmem {
-    int ex_col[NW][MAX_RPR];   // per warp: sorted columns of its current row's child tokens
-    int ex_node[NW][MAX_RPR];  // the child node of each
-    int ex_cnt[NW];
-};
 
 // Per-request state of the finalising CTA.  Everything above the marked line depends only on the
 // call's inputs and is staged before the streaming kernel's records are read.
@@ -57,7 +51,6 @@ struct FinSmem {
     int ex_off[MAX_RPR], ex_n[MAX_RPR];           // each node's children, sorted by token column:
     int ex_col[MAX_RPR], ex_node[MAX_RPR];        //   ex_col/ex_node[ex_off[n] .. + ex_n[n])
     float qx[MAX_RPR], u[MAX_RPR], v[MAX_RPR];
-    long long g_lo[MAX_RPR];                      // first streaming CTA of each row
     long long row_base[MAX_RPR];                  // first record index of each row
     int row_L[MAX_RPR];                           // records of each row
     int need_draw[MAX_RPR];                       // the row's speculative draw may be emitted
@@ -93,89 +86,33 @@ struct ResidSmem {
 };
 
 // ---------------------------------------------------------------------------------------------
-// Children of node n with a usable token, sorted by token column (warp 0 builds it).
+// The streaming warp's view of a request's nodes: lane i holds nodes i and i + 32 (token and
+// parent; the chain is a path tree), and Kids marks the children of row n's node with a usable
+// token.
 // ---------------------------------------------------------------------------------------------
-__device__ void build_children(const Params &P, int b, int n, int *ex_col, int *ex_node,
-                               int *ex_cnt, int lane)
+struct NodeView {
+    int tok[2], par[2];
+};
+
+__device__ __forceinline__ void load_nodes(const Params &P, int b, int lane, NodeView &nv)
 {
-    int cnt = 0;
-    for (int base = n + 1; base < P.rpr; base += 32) {
-        const int ch = base + lane;
-        bool ok = false;
-        int tok = -1;
-        if (ch < P.rpr) {
-            const int pa = node_parent(P, b, ch);
-            tok = node_token(P, b, ch);
-            ok = (pa == n) && tok >= 0 && (int64_t)tok < P.V;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int m = lane + 32 * h;
+        nv.tok[h] = -1;
+        nv.par[h] = -1;
+        if (m >= 1 && m < P.rpr) {
+            nv.tok[h] = node_token(P, b, m);
+            nv.par[h] = node_parent(P, b, m);
         }
-        const unsigned m = __ballot_sync(0xffffffffu, ok);
-        if (ok) {
-            const int pos = cnt + __popc(m & ((1u << lane) - 1u));
-            ex_col[pos] = tok;
-            ex_node[pos] = ch;
-        }
-        cnt += __popc(m);
     }
-    __syncwarp();
-    if (lane == 0) {
-        for (int i = 1; i < cnt; ++i) {  // insertion sort by column (few entries)
-            const int c = ex_col[i], nd = ex_node[i];
-            int j = i - 1;
-            while (j >= 0 && ex_col[j] > c) {
-                ex_col[j + 1] = ex_col[j];
-                ex_node[j + 1] = ex_node[j];
-                --j;
-            }
-            ex_col[j + 1] = c;
-            ex_node[j + 1] = nd;
-        }
-        *ex_cnt = cnt;
-    }
-    __syncwarp();
 }
 
-// ---------------------------------------------------------------------------------------------
-// One warp streams its segment [c0, c1) of row r = (request b, node n): the unaligned head and
-// tail (fewer than VEC elements each) element by element, the 16-byte aligned body with vector
-// loads.  The body's first step and the head and tail elements are loaded before anything else,
-// so the child list is built while they are in flight.  Each lane visits its columns in
-// ascending order.
-// ---------------------------------------------------------------------------------------------
-template <typename T, bool SAMPLE>
-__device__ __forceinline__ void stream_segment(const Params &P, const T *row, const Seg &sg, int b, int n,
-                                               int lane, int *ex_col, int *ex_node, int *ex_cnt,
-                                               int64_t idx0)
+__device__ __forceinline__ void kids_of(const Params &P, const NodeView &nv, int n, Kids &kd)
 {
-    const float cs = P.cs;
-    const int c0 = (int)sg.c0, b0 = (int)sg.b0, b1 = (int)sg.b1, c1 = (int)sg.c1;
-    uint4 cur[VPL];
-    load_first_step<T>(cur, row, b0, b1, lane);
-    const bool has_head = c0 + lane < b0, has_tail = b1 + lane < c1;
-    const float xh = has_head ? Elt<T>::load(row, c0 + lane) : 0.f;
-    const float xt = has_tail ? Elt<T>::load(row, b1 + lane) : 0.f;
-    if (SAMPLE) build_children(P, b, n, ex_col, ex_node, ex_cnt, lane);
-    ExCursor ex;
-    ex.init(ex_col, ex_node, SAMPLE ? *ex_cnt : 0, P.caps + (int64_t)b * P.rpr);
-    SampleAcc sa;
-    GreedyAcc ga;
-    if (has_head) {
-        if (SAMPLE) sample_scalar(sa, xh, c0 + lane, cs, ex);
-        else greedy_scalar(ga, xh, c0 + lane);
-    }
-    stream_body<T, SAMPLE>(row, c0, b0, b1, lane, cs, ex, sa, ga, P.recs, idx0, cur);
-    if (has_tail) {
-        if (SAMPLE) sample_scalar(sa, xt, b1 + lane, cs, ex);
-        else greedy_scalar(ga, xt, b1 + lane);
-    }
-    const int nvec = (b1 - b0) / Elt<T>::VEC;
-    const int used = nvec > 0 ? (nvec + SUB_VEC - 1) / SUB_VEC : 1;
-    const int k = used - 1;
-    flush_record<SAMPLE>(P.recs, idx0 + k, lane, sa, ga, k == 0 ? c0 : b0 + k * SUB_VEC * Elt<T>::VEC, c1);
-    // Sub-slots this segment does not reach hold empty records.
-    if (lane == 0)
-        for (int k2 = used; k2 < P.nsub; ++k2)
-            P.recs[idx0 + k2] = SAMPLE ? make_float4(REF_NONE, 0.f, 0.f, 0.f)
-                                       : make_float4(NEG_INF, __int_as_float(INT_MAX), 0.f, 0.f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        kd.col[h] = (nv.par[h] == n && nv.tok[h] >= 0 && (int64_t)nv.tok[h] < P.V) ? nv.tok[h] : INT_MAX;
 }
 
 __device__ __forceinline__ void draw_init(DrawSmem &D, float cum)
@@ -250,11 +187,9 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
             F.u[n] = uv.x;
             F.v[n] = uv.y;
         }
-        const int64_t rr = rbase + n, rowf = rr * V;
-        const int64_t g_lo = rowf / P.E, g_hi = (rowf + V - 1) / P.E;
-        F.g_lo[n] = g_lo;
-        F.row_base[n] = (g_lo + rr) * NW * P.nsub;
-        F.row_L[n] = (int)((g_hi - g_lo + 1) * NW * P.nsub);
+        const int64_t rr = rbase + n;
+        F.row_base[n] = rr * P.nch;
+        F.row_L[n] = (int)P.nch;
     }
     if (tid == 0) F.status = 0;
     __syncthreads();
@@ -398,8 +333,11 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, 
             const int t = lane * q + i;
             rs.rr[i] = (i < q && t < L) ? __ldcg(P.recs + base + t) : make_float4(REF_NONE, 0.f, 0.f, 0.f);
         }
+        // The lane's records against their largest reference, rescaled independently.
 #pragma unroll
-        for (int i = 0; i < REC_PER_LANE; ++i) rec_merge(mc, s, rs.rr[i].x, rs.rr[i].y);
+        for (int i = 0; i < REC_PER_LANE; ++i) mc = fmaxf(mc, rs.rr[i].x);
+#pragma unroll
+        for (int i = 0; i < REC_PER_LANE; ++i) s += (rs.rr[i].y == 0.f) ? 0.f : rs.rr[i].y * ex2(rs.rr[i].x - mc);
     } else {
         for (int t = lane; t < L; t += 32) {
             const float4 rec = __ldcg(P.recs + base + t);
@@ -781,27 +719,45 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
 // The streaming kernel: every CTA folds its share of the flat logits range into per-warp records.
 // ---------------------------------------------------------------------------------------------
 template <typename T, bool SAMPLE>
-__global__ void __launch_bounds__(NT, SV_MINB) sv_stream_kernel(const Params P)
+__global__ void __launch_bounds__(NT_S, 1) sv_stream_kernel(const Params P)
 {
-    __shared__ StreamSmem st;
+    __shared__ unsigned next_chunk;
     constexpr int VEC = Elt<T>::VEC;
-    const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t V = P.V;
-    const int64_t F0 = (int64_t)g * P.E;
-    const int64_t F1 = min(F0 + P.E, P.total);
+    const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
     pdl_launch_dependents();
-    if (F0 >= F1) return;
-    const int64_t r_end = div_v(F1 - 1, V, P.v_inv);
-    for (int64_t r = div_v(F0, V, P.v_inv); r <= r_end; ++r) {
-        const int b = (int)r / P.rpr;  // rows < 2^31
-        const int n = (int)r - b * P.rpr;
-        // Each warp keeps its own child list, so no warp waits for another at a row change.
-        const Seg sg = seg_of<VEC>(P, g, r, warp);
-        const T *row = reinterpret_cast<const T *>(P.logits) + r * V;
-        stream_segment<T, SAMPLE>(P, row, sg, b, n, lane, st.ex_col[warp], st.ex_node[warp], &st.ex_cnt[warp],
-                                  ((g + r) * NW + warp) * P.nsub);
+    const int64_t q0 = (int64_t)g * P.cpc;
+    const int64_t nq = min(q0 + P.cpc, P.nchunks) - q0;
+    if (tid == 0) next_chunk = 0;
+    __syncthreads();
+    // Claims run one chunk ahead, so the shared-memory atomic is off the critical path.
+    unsigned c = 0;
+    if (lane == 0) c = atomicAdd(&next_chunk, 1u);
+    c = __shfl_sync(0xffffffffu, c, 0);
+    int cur_b = -1, cur_n = -1;
+    NodeView nv;
+    Kids kd;
+    kd.col[0] = kd.col[1] = INT_MAX;
+    while ((int64_t)c < nq) {
+        unsigned nxt = 0;
+        if (lane == 0) nxt = atomicAdd(&next_chunk, 1u);
+        const int64_t q = q0 + c;
+        const int64_t r = q / P.nch;
+        const int64_t j = q - r * P.nch;
+        const int b = (int)(r / P.rpr);  // rows < 2^31
+        const int n = (int)(r - (int64_t)b * P.rpr);
+        const Seg sg = chunk_of<VEC>(P, r, j);
+        const T *row = reinterpret_cast<const T *>(P.logits) + r * P.V;
+        // The row's child tokens are (re)derived while the chunk's first loads are in flight.
+        stream_chunk<T, SAMPLE>(row, sg, lane, P.cs, kd, P.caps + (int64_t)b * P.rpr, P.recs + q, [&]() {
+            if (SAMPLE && (b != cur_b || n != cur_n)) {
+                if (b != cur_b) load_nodes(P, b, lane, nv);
+                kids_of(P, nv, n, kd);
+                cur_b = b;
+                cur_n = n;
+            }
+        });
+        c = __shfl_sync(0xffffffffu, nxt, 0);
     }
-    (void)tid;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1179,35 +1135,20 @@ struct Layout {
     size_t cnt2, recs, caps, pend, recs2, bpend, recs3, total;
 };
 
-// Split the flat range: one CTA per resident slot of a GB300 (152 SMs x 3 streaming CTAs), but
-// never fewer than E_MIN elements each; E is a multiple of 64 elements so that CTA boundaries keep
-// 16-byte alignment.  The split depends only on the problem size, so the workspace size does too.
-#ifndef SV_WAVES
-#define SV_WAVES 1
-#endif
-constexpr int RESIDENT_CTAS = 152 * SV_MINB * SV_WAVES;
-
-static void plan_split(int64_t total, int64_t &E, int &G)
+// Streaming chunks per row for elements of `vec` per 16-byte vector (see chunk_of).
+static int64_t chunks_per_row(int64_t V, int vec)
 {
-    int64_t g = RESIDENT_CTAS;
-    const int64_t by_min = (total + E_MIN - 1) / E_MIN;
-    if (g > by_min) g = by_min;
-    if (g > G_MAX) g = G_MAX;
-    if (g < 1) g = 1;
-    E = (total + g - 1) / g;
-    E = (E + 63) / 64 * 64;
-    G = (int)((total + E - 1) / E);
+    const int64_t ce = (int64_t)CHUNK_VEC * vec;
+    return (V + vec - 1 + ce - 1) / ce;
 }
 
-// Sub-records per warp segment: a warp flushes a record every SUB_VEC vectors of its segment,
-// so the draw rescans at most SUB_VEC vectors.  A segment lies inside one piece (one row's part
-// of one CTA's range), so it holds at most min(E, V) elements.  vec = elements per 16-byte vector.
-static int nsub_of(int64_t E, int64_t V, int vec)
+// Streaming CTAs (one per SM at most) and the chunks each takes.
+static void plan_chunks(int64_t nchunks, int sms, int &G, int64_t &cpc)
 {
-    const int64_t piece = E < V ? E : V;
-    const int64_t per_warp = ((piece + vec - 1) / vec + 2 + NW - 1) / NW;
-    int64_t n = (per_warp + SUB_VEC - 1) / SUB_VEC;
-    return (int)(n < 1 ? 1 : n);
+    int64_t g = sms < 1 ? 1 : sms;
+    if (g > nchunks) g = nchunks;
+    cpc = (nchunks + g - 1) / g;
+    G = (int)((nchunks + cpc - 1) / cpc);
 }
 
 static Layout layout(int B, int rpr, int64_t V, bool block = false)
@@ -1217,16 +1158,13 @@ static Layout layout(int B, int rpr, int64_t V, bool block = false)
     // are: every call leaves that region zero, whatever the shape of the next call.
     const int64_t R = (int64_t)B * rpr;
     const int C2 = residual_chunks(B, V);
-    int64_t E;
-    int G;
-    plan_split(R * V, E, G);
-    const int nsub = nsub_of(E, V, 4);  // fp32 logits need the most sub-records
+    const int64_t nch = chunks_per_row(V, 4);  // fp32 logits need the most chunks
     Layout L;
     size_t off = 0;
     L.cnt2 = off;
     off += sizeof(unsigned) * (size_t)B_MAX;
     L.recs = off;
-    off += align256(sizeof(float4) * (size_t)(G + R) * NW * nsub);
+    off += align256(sizeof(float4) * (size_t)R * nch);
     L.caps = off;
     off += align256(sizeof(float) * (size_t)R);
     L.pend = off;
@@ -1286,8 +1224,9 @@ static int common_setup(Params &P, const void *logits, int dtype, int B, int rpr
     P.V = V;
     P.v_inv = 1.0 / (double)V;
     P.total = (int64_t)B * rpr * V;
-    plan_split(P.total, P.E, P.G);
-    P.nsub = nsub_of(P.E, V, esize == 2 ? 8 : 4);
+    P.nch = chunks_per_row(V, esize == 2 ? 8 : 4);
+    P.nchunks = (int64_t)B * rpr * P.nch;
+    plan_chunks(P.nchunks, d->sms, P.G, P.cpc);
     P.mis = (int)(((uintptr_t)logits % 16) / esize);
     P.cnt2 = reinterpret_cast<unsigned *>(ws + L.cnt2);
     P.recs = reinterpret_cast<float4 *>(ws + L.recs);
@@ -1317,8 +1256,7 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
     // start early, stage the request's inputs, and wait (griddepcontrol) for the records.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)P.B);
-    const int nwf = P.rpr < NT_FIN_MAX / 32 ? P.rpr : NT_FIN_MAX / 32;
-    cfg.blockDim = dim3(32u * (unsigned)nwf);
+    cfg.blockDim = dim3(NT_FIN_MAX);  // one warp per row (rows beyond 8 loop); the rescan wants all 8
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1327,12 +1265,12 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (dtype == SPEC_VERIFY_BF16) {
-        sv_stream_kernel<__nv_bfloat16, SAMPLE><<<P.G, NT, 0, s>>>(P);
+        sv_stream_kernel<__nv_bfloat16, SAMPLE><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
         if (cudaLaunchKernelEx(&cfg, sv_finalize_kernel<__nv_bfloat16, SAMPLE>, P) != cudaSuccess)
             return SPEC_VERIFY_ECUDA;
     } else {
-        sv_stream_kernel<float, SAMPLE><<<P.G, NT, 0, s>>>(P);
+        sv_stream_kernel<float, SAMPLE><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
         if (cudaLaunchKernelEx(&cfg, sv_finalize_kernel<float, SAMPLE>, P) != cudaSuccess)
             return SPEC_VERIFY_ECUDA;

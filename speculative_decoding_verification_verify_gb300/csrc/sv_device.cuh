@@ -9,17 +9,16 @@
 
 namespace sv {
 
-constexpr int NT = 256;       // threads per CTA
-constexpr int NW = NT / 32;   // warps per CTA; one (max, sum) record per warp per piece
+constexpr int NT = 256;       // threads per CTA of the finalising, residual and block kernels
+constexpr int NW = NT / 32;   // their warps
+constexpr int NT_S = 768;     // threads of a streaming CTA (one CTA per SM)
 constexpr int MAX_RPR = 64;   // rows per request: k + 1 <= 64 (chain) or N <= 64 (tree)
-constexpr int G_MAX = 4096;   // upper bound on CTAs of the streaming kernel
 constexpr int B_MAX = 65536;  // most requests per call (size of the fixed counter region)
 constexpr int C2_MAX = 1024;  // upper bound on column chunks of the residual kernel
-constexpr int64_t E_MIN = 8192;  // fewest elements a streaming CTA is given
-#ifndef SV_SUB_VEC
-#define SV_SUB_VEC 512
+#ifndef SV_CHUNK_VEC
+#define SV_CHUNK_VEC 512
 #endif
-constexpr int SUB_VEC = SV_SUB_VEC;  // 16-byte vectors per sub-record of a warp segment
+constexpr int CHUNK_VEC = SV_CHUNK_VEC;  // 16-byte vectors per streaming chunk (one record each)
 constexpr float NEG_INF = -__builtin_huge_valf();
 constexpr float POS_INF = __builtin_huge_valf();
 
@@ -39,7 +38,9 @@ struct Params {
     float cs;                    // log2(e) / T: p is proportional to 2^(logit * cs)
     uint32_t key0, key1, off0, off1;
     int64_t total;               // B * rpr * V
-    int64_t E;                   // elements per streaming CTA
+    int64_t nch;                 // streaming chunks per row
+    int64_t nchunks;             // B * rpr * nch
+    int64_t cpc;                 // chunks per streaming CTA
     int G;                       // streaming CTAs
     int mis;                     // logits base address mod 16, in elements
     int32_t *out_tokens;         // chain [B][k+1], tree [B][N]
@@ -49,14 +50,13 @@ struct Params {
     int32_t *dev_status;         // or null
     // workspace
     unsigned *cnt2;              // [B] arrivals at the residual kernel's counter
-    float4 *recs;                // [(G + R) * NW * nsub] per (piece, warp, sub) records
+    float4 *recs;                // [B * rpr * nch] one record per streaming chunk
     float *caps;                 // [B * rpr] logit of node j's token in its parent's row
     int4 *pend;                  // [B] residual draw pending: {row, mc bits, total bits, flag}
     float2 *recs2;               // [B * C2 * NW] residual-kernel records
     float4 *bpend;               // block with q: [B * rpr] per row {max ref, total, prefix weight, 1}
     float2 *recs3;               // block with q: [B * rpr * C2 * NW] per (row, chunk, warp) sums
     int C2;                      // residual-kernel column chunks per request
-    int nsub;                    // sub-records per warp segment
     int64_t Ec2;                 // columns per residual chunk
 };
 
@@ -231,14 +231,20 @@ __device__ __forceinline__ void rec_merge(float &mc, float &s, float omc, float 
     s = a + b;
 }
 
+// Merge the warp's records into one, in every lane: the largest reference first, then each
+// lane's sum rescaled to it once and a plain warp sum.  A record with s = 0 has the reference
+// REF_NONE (a lane that saw a finite logit has a term 2^0 = 1 in its sum), so it cannot raise the
+// reference; a NaN sum, or a +inf logit (reference +inf, rescale 2^NaN), makes the result NaN.
 __device__ __forceinline__ void warp_rec_merge(float &mc, float &s)
 {
+    float M = mc;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float omc = __shfl_xor_sync(0xffffffffu, mc, off);
-        const float os = __shfl_xor_sync(0xffffffffu, s, off);
-        rec_merge(mc, s, omc, os);
-    }
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float v = (s == 0.f) ? 0.f : s * ex2(mc - M);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    mc = M;
+    s = v;
 }
 
 // Argmax records: larger value wins, lower index on ties, NaN is sticky.
@@ -269,37 +275,38 @@ __device__ __forceinline__ void warp_arg_merge(float &v, int &i)
 }
 
 // ---------------------------------------------------------------------------------------------
-// Geometry of the flat split.  The [B * rpr * V] logits are cut into G ranges of E elements;
-// a "piece" is the part of one row inside one CTA's range, and each piece is cut into NW
-// contiguous warp segments.  Segment boundaries inside a piece fall on 16-byte boundaries;
-// warp 0 also takes the unaligned head, warp NW-1 the unaligned tail.  Record index of
-// (CTA g, row r, warp w) = (g + r) * NW + w, which is unique and makes the records of one row
-// contiguous in index order.
+// Geometry of the streaming chunks.  Row r is cut into nch chunks of CE = CHUNK_VEC * VEC
+// columns whose boundaries fall on the flat array's 16-byte grid: chunk j covers columns
+// [A + j * CE, A + (j + 1) * CE) of [0, V), A = -((r * V + mis) mod VEC) <= 0, so only a row's first
+// chunk has an unaligned head and only its last an unaligned tail; nch = ceil((V + VEC - 1) / CE)
+// covers every A, and a chunk past the row's end is empty.  The record of chunk (r, j) is
+// r * nch + j, so a row's records are contiguous.  The streaming CTAs take equal runs of the
+// B * rpr * nch chunks in that order.
 // ---------------------------------------------------------------------------------------------
 struct Seg {
-    int64_t c0, c1;  // segment columns [c0, c1)
+    int64_t c0, c1;  // chunk columns [c0, c1)
     int64_t b0, b1;  // its vector body [b0, b1), 16-byte aligned
 };
 
 template <int VEC>
-__device__ __forceinline__ Seg seg_of(const Params &P, int64_t g, int64_t r, int w)
+__device__ __forceinline__ Seg chunk_of(const Params &P, int64_t r, int64_t j)
 {
+    constexpr int64_t CE = (int64_t)CHUNK_VEC * VEC;
     const int64_t rowf = r * P.V;
-    const int64_t f0 = max(g * P.E, rowf);
-    const int64_t f1 = min(min((g + 1) * P.E, rowf + P.V), P.total);
-    const int64_t p0 = f0 - rowf, p1 = f1 - rowf;
-    int64_t a0 = p0 + (VEC - (f0 + P.mis) % VEC) % VEC;
+    const int64_t A = -((rowf + P.mis) % VEC);
+    int64_t p0 = A + j * CE, p1 = p0 + CE;
+    if (p0 < 0) p0 = 0;
+    if (p1 > P.V) p1 = P.V;
+    if (p0 > p1) p0 = p1;
+    int64_t a0 = p0 + (VEC - (rowf + p0 + P.mis) % VEC) % VEC;
     if (a0 > p1) a0 = p1;
-    int64_t a1 = p1 - (f1 + P.mis) % VEC;
+    int64_t a1 = p1 - (rowf + p1 + P.mis) % VEC;
     if (a1 < a0) a1 = a0;
-    const int64_t nv = (a1 - a0) / VEC;
-    const int64_t span = (nv + NW - 1) / NW;
-    const int64_t v0 = min((int64_t)w * span, nv), v1 = min((int64_t)(w + 1) * span, nv);
     Seg s;
-    s.b0 = a0 + v0 * VEC;
-    s.b1 = a0 + v1 * VEC;
-    s.c0 = (w == 0) ? p0 : s.b0;
-    s.c1 = (w == NW - 1) ? p1 : s.b1;
+    s.c0 = p0;
+    s.c1 = p1;
+    s.b0 = a0;
+    s.b1 = a1;
     return s;
 }
 

@@ -1,13 +1,11 @@
 // sv_rescan.cuh -- the finalising CTA draws a token from a short column range of a logit row.
 //
 // The finalising kernel knows which record of the streaming pass holds the crossing of the draw
-// threshold t, and the mass before that record.  The record covers a column range of at most
-// SUB_VEC 16-byte vectors (plus an unaligned head and tail), so the CTA copies that range into
-// shared memory with cp.async (every copy in flight at once, completion tracked by the
-// hardware), each thread weighs a contiguous run of a few vectors as the streaming pass did, a
-// block scan of the thread totals picks the thread that holds the crossing, and that thread walks
-// its run.  Loops stay short: this code runs once per request on an SM whose instruction cache
-// has not seen it.
+// threshold t, and the mass before that record.  The record covers one streaming chunk of at most
+// CHUNK_VEC 16-byte vectors (plus an unaligned head and tail), so the CTA copies that range into
+// shared memory with cp.async (every copy in flight at once, completion tracked by the hardware),
+// weighs it vector by vector, finds the vector where the running mass crosses t with a block-wide
+// scan, and the thread holding that vector walks its few elements.
 #pragma once
 
 #include <climits>
@@ -17,9 +15,9 @@
 
 namespace sv {
 
-// Shared-memory vectors the CTA stages: the range holds at most SUB_VEC aligned vectors plus a
+// Shared-memory vectors the CTA stages: the range holds at most CHUNK_VEC aligned vectors plus a
 // partial one at each end.
-constexpr int RESCAN_STAGE_VEC = SUB_VEC + 2;
+constexpr int RESCAN_STAGE_VEC = CHUNK_VEC + 2;
 
 // The 16-byte vector of a row starting at column col, with the elements outside [c0, c1) read
 // as -inf, element by element, so that no byte outside [c0, c1) is touched.
@@ -64,24 +62,15 @@ __device__ __forceinline__ void vec_weights_plain(const uint4 &w, int col, int c
     }
 }
 
-// The same with the excluded columns ex[e0..e1) (sorted) of this lane's run zeroed as well.
-template <typename T>
-__device__ __forceinline__ void vec_weights_ex(const uint4 &w, int col, int c0, int c1, float cs,
-                                               float mc, const int *ex, int e0, int e1,
-                                               float (&out)[Elt<T>::VEC])
-{
-    constexpr int VEC = Elt<T>::VEC;
-    vec_weights_plain<T>(w, col, c0, c1, cs, mc, out);
-    for (int e = e0; e < e1; ++e) {
-        const int d = ex[e] - col;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j)
-            if (j == d) out[j] = 0.f;
-    }
-}
+// Rounds of the rescan: thread t weighs vectors t, t + nt, t + 2 nt of the staged range.
+constexpr int RESCAN_ROUNDS = 3;
+constexpr int RESCAN_THREADS = 256;  // the finalising CTA's size, which the rounds assume
+static_assert(RESCAN_ROUNDS * RESCAN_THREADS >= RESCAN_STAGE_VEC, "three rounds cover the range");
 
 struct RescanSmem {
-    float wsum[32];  // per-warp totals
+    float wsum[RESCAN_ROUNDS * 8];  // per (round, warp) totals
+    int kmin;                       // first vector whose running mass crosses t
+    int klast;                      // last vector with positive mass
     int found;
 };
 
@@ -110,88 +99,103 @@ __device__ __forceinline__ void stage_range(const T *row, int64_t rowflat, int64
 
 // First column y of [c0, c1) at which cum0 + (running weight up to and including y) exceeds t;
 // when none does (t = +inf asks for that), the last column with positive weight; -1 if no weight
-// is positive.  Child tokens ex[0..ex_n) (sorted) weigh 0.  stage holds the range as stage_range
-// laid it out, visible to every thread.  Every thread of the CTA calls it and gets the result.
-// Threads take runs of at most RUN_MAX vectors; the warp whose prefix crosses t (or, with none,
-// the last warp with positive weight) finds the thread and the column, so two barriers suffice.
-constexpr int RUN_MAX = 3;  // vectors per thread: (SUB_VEC + 2) / NT_FIN rounded up to odd
-
+// is positive.  Child tokens ex[0..ex_n) weigh 0.  stage holds the range as stage_range laid it
+// out, visible to every thread; all RESCAN_THREADS threads of the CTA call it and get the result.
+// Thread t weighs whole vectors t + i * nt (conflict-free shared reads); per-round warp scans and
+// one table of (round, warp) totals give every vector its running mass; the first crossing vector
+// (or the last positive one) comes from shared-memory atomics, and its owner walks its VEC
+// elements.  Three barriers.
 template <typename T>
 __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs, float mc, float t,
                              float cum0, const int *ex, int ex_n, const uint4 *stage, RescanSmem &S)
 {
     constexpr int VEC = Elt<T>::VEC;
-    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int nt = RESCAN_THREADS, nw = RESCAN_THREADS / 32;
     const int a0 = c0 - (int)((rowflat + c0 + mis) % VEC);
     const int nvv = (c1 - a0 + VEC - 1) / VEC;
-    // Each thread weighs a contiguous run of odd length (conflict-free 16-byte shared reads).
-    const int per = ((nvv + nt - 1) / nt) | 1;
-    const int k0 = min(tid * per, nvv), k1 = min(k0 + per, nvv);
-    const int lc0 = a0 + k0 * VEC, lc1 = a0 + k1 * VEC;
-    int e0 = 0;
-    while (e0 < ex_n && ex[e0] < lc0) ++e0;
-    int e1 = e0;
-    while (e1 < ex_n && ex[e1] < lc1) ++e1;
-    float vs[RUN_MAX];
-    float own = 0.f;
-    if (per <= RUN_MAX) {
+    if (tid == 0) {
+        S.kmin = INT_MAX;
+        S.klast = -1;
+    }
+    float vs[RESCAN_ROUNDS], inc[RESCAN_ROUNDS];
 #pragma unroll
-        for (int i = 0; i < RUN_MAX; ++i) {
-            vs[i] = 0.f;
-            if (k0 + i < k1) {
-                float e[VEC];
-                vec_weights_ex<T>(stage[k0 + i], a0 + (k0 + i) * VEC, c0, c1, cs, mc, ex, e0, e1, e);
-                float p0 = (e[0] + e[1]) + (e[2] + e[3]);
-                if (VEC == 8) p0 += (e[VEC - 4] + e[VEC - 3]) + (e[VEC - 2] + e[VEC - 1]);
-                vs[i] = p0;
-            }
-            own += vs[i];
-        }
-    } else {
-        for (int k = k0; k < k1; ++k) {
+    for (int i = 0; i < RESCAN_ROUNDS; ++i) {
+        const int k = tid + i * nt;
+        vs[i] = 0.f;
+        if (k < nvv) {
+            const int col = a0 + k * VEC;
             float e[VEC];
-            vec_weights_ex<T>(stage[k], a0 + k * VEC, c0, c1, cs, mc, ex, e0, e1, e);
+            vec_weights_plain<T>(stage[k], col, c0, c1, cs, mc, e);
+            for (int x = 0; x < ex_n; ++x) {
+                const int d = ex[x] - col;
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) own += e[j];
+                for (int j = 0; j < VEC; ++j)
+                    if (j == d) e[j] = 0.f;
+            }
+            float p0 = (e[0] + e[1]) + (e[2] + e[3]);
+            if (VEC == 8) p0 += (e[VEC - 4] + e[VEC - 3]) + (e[VEC - 2] + e[VEC - 1]);
+            vs[i] = p0;
+        }
+        inc[i] = warp_incl_scan(vs[i], lane);
+        if (lane == 31) S.wsum[i * 8 + warp] = inc[i];
+    }
+    __syncthreads();
+    // Running mass before each (round, warp) block, in vector order.
+    float pre[RESCAN_ROUNDS];
+    float base = cum0;
+#pragma unroll
+    for (int i = 0; i < RESCAN_ROUNDS; ++i) {
+        pre[i] = 0.f;
+        for (int w = 0; w < nw; ++w) {
+            if (w == warp) pre[i] = base;
+            base += S.wsum[i * 8 + w];
         }
     }
-    // Warp totals, then every warp knows its prefix.
-    const float incl = warp_incl_scan(own, lane);
-    if (lane == 31) S.wsum[warp] = incl;
-    __syncthreads();
-    const float ws = lane < nw ? S.wsum[lane] : 0.f;
-    const float wi = warp_incl_scan(ws, lane);
-    const unsigned wcross = __ballot_sync(0xffffffffu, lane < nw && cum0 + wi > t);
-    const unsigned wpos = __ballot_sync(0xffffffffu, lane < nw && ws > 0.f);
-    const bool take_last = wcross == 0;
-    const int wsel = take_last ? (wpos ? 31 - __clz(wpos) : -1) : __ffs(wcross) - 1;
-    if (warp == wsel) {
-        const float cum = cum0 + __shfl_sync(0xffffffffu, wi - ws, warp);
-        const unsigned hit = __ballot_sync(0xffffffffu, !take_last && cum + incl > t);
-        const unsigned pos = __ballot_sync(0xffffffffu, own > 0.f);
-        // The crossing thread, or (take_last, or rounding) the warp's last positive thread.
-        const bool last_mode = hit == 0;
-        const int who = last_mode ? 31 - __clz(pos) : __ffs(hit) - 1;
-        if (lane == who) {
-            float c = cum + incl - own;
-            int found = -1, lp = -1;
-            for (int k = k0; k < k1 && found < 0; ++k) {
-                const int col = a0 + k * VEC;
-                float e[VEC];
-                vec_weights_ex<T>(stage[k], col, c0, c1, cs, mc, ex, e0, e1, e);
+    int kmin = INT_MAX, klast = -1;
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    if (found < 0 && e[j] > 0.f) {
-                        lp = col + j;
-                        c += e[j];
-                        if (!last_mode && c > t) found = lp;
-                    }
-                }
-            }
-            S.found = found >= 0 ? found : lp;
+    for (int i = 0; i < RESCAN_ROUNDS; ++i) {
+        const int k = tid + i * nt;
+        if (k < nvv && vs[i] > 0.f) {
+            const float before = pre[i] + inc[i] - vs[i];
+            if (kmin == INT_MAX && before + vs[i] > t) kmin = k;
+            klast = k;
         }
-    } else if (wsel < 0 && tid == 0) {
-        S.found = -1;
+    }
+    if (kmin != INT_MAX) atomicMin(&S.kmin, kmin);
+    if (klast >= 0) atomicMax(&S.klast, klast);
+    __syncthreads();
+    const bool last_mode = S.kmin == INT_MAX;
+    const int kv = last_mode ? S.klast : S.kmin;
+    if (kv < 0) {
+        if (tid == 0) S.found = -1;
+    } else if (kv % nt == tid) {
+        const int i = kv / nt;
+        float before = 0.f;
+#pragma unroll
+        for (int r = 0; r < RESCAN_ROUNDS; ++r)
+            if (r == i) before = pre[r] + inc[r] - vs[r];
+        const int col = a0 + kv * VEC;
+        float e[VEC];
+        vec_weights_plain<T>(stage[kv], col, c0, c1, cs, mc, e);
+        for (int x = 0; x < ex_n; ++x) {
+            const int d = ex[x] - col;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                if (j == d) e[j] = 0.f;
+        }
+        float c = before;
+        int found = -1, lp = -1;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            if (found < 0 && e[j] > 0.f) {
+                lp = col + j;
+                c += e[j];
+                if (!last_mode && c > t) found = lp;
+            }
+        }
+        // No element crossed (t = +inf, or rounding): the vector's last positive element.
+        S.found = found >= 0 ? found : lp;
     }
     __syncthreads();
     return S.found;

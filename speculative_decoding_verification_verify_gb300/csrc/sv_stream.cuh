@@ -1,6 +1,6 @@
-// sv_stream.cuh -- the streaming fold: each warp walks its contiguous segment of a logit row with
-// 16-byte non-allocating loads, eight per lane per step, and folds every element into a running
-// (max, sum of 2^(l*cs - mc)) or a running argmax, flushing a record every SUB_VEC vectors.
+// sv_stream.cuh -- the streaming fold: a warp takes one chunk of a logit row at a time, loads it
+// with 16-byte non-allocating loads (eight per lane per step), folds every element into a running
+// (max, sum of 2^(l*cs - mc)) or a running argmax, and writes the chunk's record.
 #pragma once
 
 #include <climits>
@@ -14,7 +14,7 @@ namespace sv {
 #endif
 constexpr int VPL = SV_VPL;            // 16-byte vectors per lane per step
 constexpr int STEP_VEC = 32 * VPL;     // vectors per warp step
-static_assert(SUB_VEC % STEP_VEC == 0, "a sub-record spans whole steps");
+static_assert(CHUNK_VEC % STEP_VEC == 0, "a chunk spans whole steps");
 
 // ---------------------------------------------------------------------------------------------
 // Packed fp32 pairs (sm_100+ f32x2 arithmetic): half the FMA-pipe instructions per element.
@@ -73,27 +73,11 @@ struct GreedyAcc {
     int idx = INT_MAX;
 };
 
-// The lane's next child-token column (tokens whose mass is kept out of the sums and whose
-// logits are captured instead).  A lane visits its columns in ascending order.
-struct ExCursor {
-    const int *col;
-    const int *node;
-    int cnt, ptr, next;
-    float *caps;
-    __device__ __forceinline__ void init(const int *c, const int *nd, int n, float *cp)
-    {
-        col = c;
-        node = nd;
-        cnt = n;
-        ptr = 0;
-        caps = cp;
-        next = n > 0 ? c[0] : INT_MAX;
-    }
-    __device__ __forceinline__ void advance()
-    {
-        ++ptr;
-        next = ptr < cnt ? col[ptr] : INT_MAX;
-    }
+// The child tokens of the row being streamed (tokens whose mass is kept out of the sums and
+// whose logits are captured instead): lane i stands for nodes i and i + 32 of the request, and
+// col[h] is that node's token column when the node is a child of the row's node, else INT_MAX.
+struct Kids {
+    int col[2];
 };
 
 __device__ __forceinline__ void sample_rescale(SampleAcc &a, float vmax, float cs)
@@ -139,37 +123,57 @@ __device__ __forceinline__ float take_element(uint4 &w, int j)
     return x;
 }
 
-// Rare: a child token lies in this lane's step (or the cursor still points before it).  Capture
-// each child's logit and mask it out of the vectors; filler vectors (step index >= nv) belong to
-// the next segment and are left alone.
+// Rare: child tokens lie in the step whose lane-0 vector starts at column lo (columns below hi
+// hold loaded data; the filler vectors past the chunk's body are left alone).  Each is captured
+// by the lane that holds it and masked out of its vector.
 template <typename T>
-__device__ __forceinline__ void exclude_children(uint4 (&w)[VPL], int nv, int col0, int lane, ExCursor &ex)
+__device__ __forceinline__ void exclude_step(uint4 (&w)[VPL], int lo, int hi, int lane, const Kids &kd,
+                                          float *caps)
 {
     constexpr int VEC = Elt<T>::VEC;
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-        if (lane + 32 * u < nv) {
-            const int col = col0 + u * 32 * VEC;
-            while (ex.next < col + VEC) {
-                if (ex.next >= col) ex.caps[ex.node[ex.ptr]] = take_element<T>(w[u], ex.next - col);
-                ex.advance();
+    for (int h = 0; h < 2; ++h) {
+        unsigned m = __ballot_sync(0xffffffffu, kd.col[h] >= lo && kd.col[h] < hi);
+        while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1;
+            const int c = __shfl_sync(0xffffffffu, kd.col[h], src);
+            const int v = (c - lo) / VEC;
+            if ((v & 31) == lane) {
+                const int u = v >> 5, j = c - lo - v * VEC;
+#pragma unroll
+                for (int uu = 0; uu < VPL; ++uu)
+                    if (uu == u) caps[src + 32 * h] = take_element<T>(w[uu], j);
             }
         }
     }
 }
 
-// One element outside the vector body (segment head or tail); a child token is captured instead.
-__device__ __forceinline__ void sample_scalar(SampleAcc &a, float x, int col, float cs, ExCursor &ex)
+// Whether column col (a head or tail element of this lane, when has) is a child token; if so its
+// logit x is captured.
+__device__ __forceinline__ bool scalar_is_child(int col, bool has, float x, int lo, int hi, int lane,
+                                                const Kids &kd, float *caps)
 {
     bool child = false;
-    while (ex.next <= col) {
-        if (ex.next == col) {
-            child = true;
-            ex.caps[ex.node[ex.ptr]] = x;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        unsigned m = __ballot_sync(0xffffffffu, kd.col[h] >= lo && kd.col[h] < hi);
+        while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1;
+            const int c = __shfl_sync(0xffffffffu, kd.col[h], src);
+            if (has && c == col) {
+                child = true;
+                caps[src + 32 * h] = x;
+            }
         }
-        ex.advance();
     }
-    if (child) return;
+    return child;
+}
+
+// One element outside the vector body (a row's unaligned head or tail).
+__device__ __forceinline__ void sample_scalar(SampleAcc &a, float x, float cs)
+{
     sample_rescale(a, x, cs);
     a.acc[0] = f2_add(a.acc[0], f2(ex2(fmaf(x, cs, -a.mc)), 0.f));
 }
@@ -253,22 +257,20 @@ __device__ __forceinline__ void sample_step_fast(SampleAcc &a, const uint4 (&w)[
     }
 }
 
-// Fold one step (VPL vectors per lane at columns col0 + u*32*VEC; those at step index >= nv are
-// fillers holding -inf, whose columns belong to the next warp's segment).
+// Fold one step (VPL vectors per lane at columns lo + (lane + 32 * u) * VEC; columns from hi on
+// are fillers holding -inf, which belong to the next chunk).
 template <typename T, bool SAMPLE>
-__device__ __forceinline__ void fold_step(uint4 (&w)[VPL], int nv, int col0, int lane, float cs,
-                                          uint64_t cs2, ExCursor &ex, SampleAcc &sa, GreedyAcc &ga)
+__device__ __forceinline__ void fold_step(uint4 (&w)[VPL], int lo, int hi, int lane, float cs, uint64_t cs2,
+                                          const Kids &kd, float *caps, SampleAcc &sa, GreedyAcc &ga)
 {
-    constexpr int VEC = Elt<T>::VEC;
     if (SAMPLE) {
-        // Last column this lane's step covers, fillers included.
-        const int last = col0 + ((VPL - 1) * 32 + 1) * VEC - 1;
-        if (ex.next <= last) exclude_children<T>(w, nv, col0, lane, ex);
+        const bool mine = (kd.col[0] >= lo && kd.col[0] < hi) || (kd.col[1] >= lo && kd.col[1] < hi);
+        if (__any_sync(0xffffffffu, mine)) exclude_step<T>(w, lo, hi, lane, kd, caps);
         sample_rescale(sa, step_max<T>(w), cs);
         const float nmc = -sa.mc;
         sample_step_fast<T>(sa, w, cs2, f2(nmc, nmc));
     } else {
-        greedy_step<T>(ga, w, col0, step_max<T>(w));
+        greedy_step<T>(ga, w, lo + lane * Elt<T>::VEC, step_max<T>(w));
     }
 }
 
@@ -276,25 +278,24 @@ __device__ __forceinline__ void fold_step(uint4 (&w)[VPL], int nv, int col0, int
 // lane keeps its reference mc, so later records stay in the same scaled domain per lane.  A
 // sampling record also carries the columns [c0, c1) it covers.
 template <bool SAMPLE>
-__device__ __forceinline__ void flush_record(float4 *recs, int64_t idx, int lane, SampleAcc &sa,
-                                             GreedyAcc &ga, int c0, int c1)
+__device__ __forceinline__ void flush_record(float4 *rec, int lane, SampleAcc &sa, GreedyAcc &ga, int c0, int c1)
 {
-    float4 rec;
+    float4 out;
     if (SAMPLE) {
         float mc = sa.mc, sum = sa.total();
         warp_rec_merge(mc, sum);
-        rec = make_float4(mc, sum, __int_as_float(c0), __int_as_float(c1));
+        out = make_float4(mc, sum, __int_as_float(c0), __int_as_float(c1));
 #pragma unroll
         for (int j = 0; j < 4; ++j) sa.acc[j] = 0;
     } else {
         float v = ga.best;
         int i = ga.idx;
         warp_arg_merge(v, i);
-        rec = make_float4(v, __int_as_float(i), 0.f, 0.f);
+        out = make_float4(v, __int_as_float(i), 0.f, 0.f);
         ga.best = NEG_INF;
         ga.idx = INT_MAX;
     }
-    if (lane == 0) recs[idx] = rec;
+    if (lane == 0) *rec = out;
 }
 
 // One lane's loads of a step: vectors p[32*u]; with CHECK, those at 32*u >= lim are -inf fillers.
@@ -305,49 +306,52 @@ __device__ __forceinline__ void load_step(uint4 (&d)[VPL], const uint4 *p, int l
     for (int u = 0; u < VPL; ++u) d[u] = (!CHECK || 32 * u < lim) ? ldg_stream(p + 32 * u) : neg_inf_vec<T>();
 }
 
-// Stream the 16-byte aligned body [b0, b1) of a warp segment that starts at column c0 (its
-// unaligned head, already folded, is [c0, b0)), VPL loads per lane per step; cur holds the first
-// step, loaded by the caller.  After every SUB_VEC vectors but the last sub-range, the
-// sub-range's record is flushed to recs[idx0 + k].
-template <typename T, bool SAMPLE>
-__device__ __forceinline__ void stream_body(const T *row, int c0, int b0, int b1, int lane, float cs,
-                                            ExCursor &ex, SampleAcc &sa, GreedyAcc &ga,
-                                            float4 *recs, int64_t idx0, uint4 (&cur)[VPL])
+// One warp streams chunk sg of a row: the body's first step and the head and tail elements are
+// loaded first (the caller may update kd meanwhile through `ready`), then the steps are folded
+// and the chunk's record is written to *rec.
+template <typename T, bool SAMPLE, typename Ready>
+__device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int lane, float cs, Kids &kd, float *caps,
+                                             float4 *rec, Ready ready)
 {
     constexpr int VEC = Elt<T>::VEC;
+    const int c0 = (int)sg.c0, b0 = (int)sg.b0, b1 = (int)sg.b1, c1 = (int)sg.c1;
     const int nvec = (b1 - b0) / VEC;
-    if (nvec <= 0) return;
     const uint4 *vp = reinterpret_cast<const uint4 *>(row + b0) + lane;
-    const int nst = (nvec + STEP_VEC - 1) / STEP_VEC;
-    const int nfull = nvec / STEP_VEC;  // steps whose vectors are all inside the segment
-    const uint64_t cs2 = f2(cs, cs);
-    for (int s = 0; s < nst; ++s) {
-        // All of a step's loads are issued together; the other warps of the SM cover their latency.
-        if (s > 0) {
-            if (s < nfull) load_step<T, false>(cur, vp + s * STEP_VEC, 0);
-            else load_step<T, true>(cur, vp + s * STEP_VEC, nvec - s * STEP_VEC - lane);
-        }
-        const int nv = min(STEP_VEC, nvec - s * STEP_VEC);
-        fold_step<T, SAMPLE>(cur, nv, b0 + (s * STEP_VEC + lane) * VEC, lane, cs, cs2, ex, sa, ga);
-        constexpr int STEPS_PER_SUB = SUB_VEC / STEP_VEC;
-        if ((s + 1) % STEPS_PER_SUB == 0 && s + 1 < nst) {
-            const int k = (s + 1) / STEPS_PER_SUB - 1;
-            flush_record<SAMPLE>(recs, idx0 + k, lane, sa, ga, k == 0 ? c0 : b0 + k * SUB_VEC * VEC,
-                                 b0 + (k + 1) * SUB_VEC * VEC);
+    uint4 cur[VPL];
+    if (nvec >= STEP_VEC) load_step<T, false>(cur, vp, 0);
+    else if (nvec > 0) load_step<T, true>(cur, vp, nvec - lane);
+    const bool has_head = c0 + lane < b0, has_tail = b1 + lane < c1;
+    const float xh = has_head ? Elt<T>::load(row, c0 + lane) : 0.f;
+    const float xt = has_tail ? Elt<T>::load(row, b1 + lane) : 0.f;
+    ready();
+    SampleAcc sa;
+    GreedyAcc ga;
+    if (b0 > c0) {  // warp-uniform
+        if (SAMPLE) {
+            if (!scalar_is_child(c0 + lane, has_head, xh, c0, b0, lane, kd, caps) && has_head) sample_scalar(sa, xh, cs);
+        } else if (has_head) {
+            greedy_scalar(ga, xh, c0 + lane);
         }
     }
-}
-
-// The first step of a segment body [b0, b1), issued before anything else of the segment.
-template <typename T>
-__device__ __forceinline__ void load_first_step(uint4 (&cur)[VPL], const T *row, int b0, int b1, int lane)
-{
-    constexpr int VEC = Elt<T>::VEC;
-    const int nvec = (b1 - b0) / VEC;
-    if (nvec <= 0) return;
-    const uint4 *vp = reinterpret_cast<const uint4 *>(row + b0) + lane;
-    if (nvec >= STEP_VEC) load_step<T, false>(cur, vp, 0);
-    else load_step<T, true>(cur, vp, nvec - lane);
+    const uint64_t cs2 = f2(cs, cs);
+    const int nst = (nvec + STEP_VEC - 1) / STEP_VEC;
+    for (int s = 0; s < nst; ++s) {
+        if (s > 0) {
+            if (nvec - s * STEP_VEC >= STEP_VEC) load_step<T, false>(cur, vp + s * STEP_VEC, 0);
+            else load_step<T, true>(cur, vp + s * STEP_VEC, nvec - s * STEP_VEC - lane);
+        }
+        const int lo = b0 + s * STEP_VEC * VEC;
+        const int hi = min(lo + STEP_VEC * VEC, b1);
+        fold_step<T, SAMPLE>(cur, lo, hi, lane, cs, cs2, kd, caps, sa, ga);
+    }
+    if (c1 > b1) {  // warp-uniform
+        if (SAMPLE) {
+            if (!scalar_is_child(b1 + lane, has_tail, xt, b1, c1, lane, kd, caps) && has_tail) sample_scalar(sa, xt, cs);
+        } else if (has_tail) {
+            greedy_scalar(ga, xt, b1 + lane);
+        }
+    }
+    flush_record<SAMPLE>(rec, lane, sa, ga, c0, c1);
 }
 
 }  // namespace sv
