@@ -83,6 +83,16 @@ def _load():
         lib.svo_grid_chain_first_token.restype = i32
         lib.svo_grid_tree_first_token.argtypes = [P, P, i32, i64, i32, P, F64P]
         lib.svo_grid_tree_first_token.restype = i32
+        lib.svo_grid_tree_first_token_t.argtypes = [P, P, i32, i64, i32, f64, f64, P, F64P]
+        lib.svo_grid_tree_first_token_t.restype = i32
+        lib.svo_chain_core_t.argtypes = [P, P, P, i32, i64, P, P, f64, f64, P, I32P, I32P, P, P]
+        lib.svo_chain_core_t.restype = i32
+        lib.svo_verify_ex.argtypes = [P, i32, P, P, i32, i32, i64, P, f64, f64, u64, u64, P, i32,
+                                      P, P, P, P, P]
+        lib.svo_verify_ex.restype = i32
+        lib.svo_verify_tree_ex.argtypes = [P, i32, P, P, i32, i32, i64, P, f64, f64, u64, u64, P,
+                                           i32, P, P, P, P, P]
+        lib.svo_verify_tree_ex.restype = i32
         _lib = lib
         return lib
 
@@ -239,16 +249,37 @@ def grid_chain_first_token(p0, q0, w, G: int):
     return dist, acc.value
 
 
-def grid_tree_first_token(p0, child_tokens, G: int):
+def grid_tree_first_token(p0, child_tokens, G: int, thr_single=1.0, thr_acc=1.0):
+    """Integrate one target-only tree level over a G x G (coin, v) grid; thresholds below 1
+    give the relaxed rule."""
     lib = _load()
     p0 = _c(p0, np.float64)
     V = p0.shape[0]
     ct = _c(child_tokens, np.int32)
     dist = np.zeros(V, np.float64)
     acc = ctypes.c_double()
-    _check(lib.svo_grid_tree_first_token(_ptr(p0), _ptr(ct), ct.shape[0], V, G, _ptr(dist),
-                                         ctypes.byref(acc)))
+    _check(lib.svo_grid_tree_first_token_t(_ptr(p0), _ptr(ct), ct.shape[0], V, G, float(thr_single),
+                                           float(thr_acc), _ptr(dist), ctypes.byref(acc)))
     return dist, acc.value
+
+
+def chain_core(p, q, drafts, u, v, thr_single=1.0, thr_acc=1.0):
+    """Chain verification of one request from probabilities: p [k+1, V], q [k, V] or None,
+    drafts [k], uniforms u, v [k+1].  Returns (tokens, accept_len, boundary)."""
+    lib = _load()
+    pp = _c(p, np.float64)
+    k1, V = pp.shape
+    k = k1 - 1
+    qq = None if q is None else _c(q, np.float64).reshape(k, V)
+    d = _c(drafts, np.int32).reshape(k)
+    uu, vv = _c(u, np.float64), _c(v, np.float64)
+    tok = np.zeros(k1, np.int32)
+    alen, bnd = ctypes.c_int32(), ctypes.c_int32(0)
+    work = np.zeros(V, np.float64)
+    _check(lib.svo_chain_core_t(_ptr(pp), _ptr(qq), _ptr(d), k, V, _ptr(uu), _ptr(vv),
+                                float(thr_single), float(thr_acc), _ptr(tok), ctypes.byref(alen),
+                                ctypes.byref(bnd), None, _ptr(work)))
+    return tok, alen.value, bnd.value
 
 
 # ---------------------------------------------------------------------------------------
@@ -290,6 +321,54 @@ def verify_rejection(logits, drafts, q, T: float, seed: int, offset: int, req_id
                                     offset, _ptr(ids), n, _ptr(out), _ptr(alen), _ptr(probs),
                                     _ptr(bnd), _ptr(status)))
     return dict(out_tokens=out, accept_len=alen, out_probs=probs, boundary=bnd, status=status)
+
+
+def verify_ex(logits, drafts, q, temps, seed: int, offset: int, thr_single=1.0, thr_acc=1.0,
+              req_ids=None):
+    """Chain verification with a temperature per request (temps [B]; 0 = greedy for that
+    request) and the relaxed thresholds of target-only decisions (q must be None unless both
+    are 1).  Same outputs as verify_rejection; a greedy request's out_probs are 0."""
+    lib = _load()
+    a, dt = _logits(logits)
+    B, k1, V = a.shape
+    k = k1 - 1
+    d = _c(drafts, np.int32).reshape(B, k)
+    qq = None if q is None else _c(q, np.float32).reshape(B, k, V)
+    tt = _c(temps, np.float64).reshape(B)
+    ids = _req_ids(req_ids, B)
+    n = ids.shape[0]
+    out = np.zeros((n, k + 1), np.int32)
+    alen = np.zeros(n, np.int32)
+    probs = np.zeros((n, k + 1, 3), np.float64)
+    bnd = np.zeros(n, np.int32)
+    status = np.zeros(n, np.int32)
+    _check(lib.svo_verify_ex(_ptr(a), dt, _ptr(d), _ptr(qq), B, k, V, _ptr(tt), float(thr_single),
+                             float(thr_acc), seed, offset, _ptr(ids), n, _ptr(out), _ptr(alen),
+                             _ptr(probs), _ptr(bnd), _ptr(status)))
+    return dict(out_tokens=out, accept_len=alen, out_probs=probs, boundary=bnd, status=status)
+
+
+def verify_tree_ex(logits, tokens, parents, temps, seed: int, offset: int, thr_single=1.0,
+                   thr_acc=1.0, req_ids=None):
+    """Tree verification with a temperature per request (0 = greedy walk for that request) and
+    the relaxed thresholds of the target-only walk."""
+    lib = _load()
+    a, dt = _logits(logits)
+    B, N, V = a.shape
+    t = _c(tokens, np.int32).reshape(B, N)
+    pa = _c(parents, np.int32).reshape(B, N)
+    tt = _c(temps, np.float64).reshape(B)
+    ids = _req_ids(req_ids, B)
+    n = ids.shape[0]
+    ot = np.zeros((n, N), np.int32)
+    ai = np.zeros((n, N), np.int32)
+    alen = np.zeros(n, np.int32)
+    bnd = np.zeros(n, np.int32)
+    status = np.zeros(n, np.int32)
+    _check(lib.svo_verify_tree_ex(_ptr(a), dt, _ptr(t), _ptr(pa), B, N, V, _ptr(tt),
+                                  float(thr_single), float(thr_acc), seed, offset, _ptr(ids), n,
+                                  _ptr(ot), _ptr(ai), _ptr(alen), _ptr(bnd), _ptr(status)))
+    return dict(out_tokens=ot, accept_index=ai, accept_len=alen, boundary=bnd, status=status)
 
 
 def block_core(p, q, drafts, u, v):

@@ -53,6 +53,18 @@
  *     accepted prefix is drawn from max(w_j p_j - q_j, 0) / Z (from p_j when j reaches the
  *     last draft or an absent draft), with v of slot j.  These follow Sun et al.'s algorithm.
  *
+ *   - Relaxed thresholds ("投机解码", section 接受规则为什么不改变分布, subsection SGLang 默认 and
+ *     its closing remark on the two thresholds): in target-only decisions a candidate c with
+ *     p(c) > 0 is accepted when coin < (running sum of the tried candidates' p) / threshold_acc,
+ *     or when p(c) >= threshold_single.  Both default to 1, which is the exact rule; smaller values
+ *     accept more and change the output distribution.  A chain without draft probabilities is
+ *     the one-candidate case (running sum = p(x)).  With draft probabilities the thresholds do
+ *     not apply (reading: the pages give them only for the target-only kernel).
+ *   - Per-request temperature in one batch ("The speculative decoding zoo", DSpark section:
+ *     accept_draft_tokens runs the greedy rule when the whole batch is greedy, the sampling rule
+ *     when none is, and both, merged, when the batch is mixed): request b uses T_b; T_b = 0
+ *     means greedy for that request (argmax rule), T_b > 0 the sampling rule with p at T_b.
+ *
  * Boundary draws: a decision whose operands lie within 1e-6 (relative) of the decision
  * boundary is flagged, because an fp32 implementation may legitimately decide it the other way.
  *
@@ -232,9 +244,10 @@ static int64_t svo_inverse_cdf(const double *r, int64_t V, double v, int32_t *bo
 /*   probs  : (k+1) x 3 or NULL: p_i(x_i), q_i(x_i), and Z at the stop slot                    */
 /*   work   : V doubles                                                                        */
 /* ------------------------------------------------------------------------------------------ */
-int svo_chain_core(const double *p, const double *q, const int32_t *drafts, int k, int64_t V,
-                   const double *u, const double *v, int32_t *tokens, int32_t *accept_len,
-                   int32_t *boundary, double *probs, double *work)
+int svo_chain_core_t(const double *p, const double *q, const int32_t *drafts, int k, int64_t V,
+                     const double *u, const double *v, double thr_single, double thr_acc,
+                     int32_t *tokens, int32_t *accept_len, int32_t *boundary, double *probs,
+                     double *work)
 {
     for (int i = 0; i <= k; ++i) tokens[i] = -1;
     if (probs) memset(probs, 0, sizeof(double) * 3 * (size_t)(k + 1));
@@ -260,10 +273,20 @@ int svo_chain_core(const double *p, const double *q, const int32_t *drafts, int 
             break;
         }
         double px = p[(int64_t)i * V + x];
-        double qx = q ? q[(int64_t)i * V + x] : 1.0;
-        double lhs = u[i] * qx;
-        if (fabs(lhs - px) < SVO_BOUNDARY_REL * fmax(qx, px)) *boundary = 1;
-        if (lhs < px) {
+        int accept;
+        if (q) {
+            double qx = q[(int64_t)i * V + x];
+            double lhs = u[i] * qx;
+            if (fabs(lhs - px) < SVO_BOUNDARY_REL * fmax(qx, px)) *boundary = 1;
+            accept = lhs < px;
+        } else {
+            /* One candidate: running sum = p(x); thresholds of 1 give the exact test u < p(x). */
+            double a = px / thr_acc;
+            if (fabs(u[i] - a) < SVO_BOUNDARY_REL * fmax(1.0, a)) *boundary = 1;
+            if (thr_single < 1.0 && fabs(px - thr_single) < SVO_BOUNDARY_REL) *boundary = 1;
+            accept = px > 0.0 && (u[i] < a || px >= thr_single);
+        }
+        if (accept) {
             tokens[i] = x;
             continue;
         }
@@ -294,6 +317,14 @@ int svo_chain_core(const double *p, const double *q, const int32_t *drafts, int 
     return SVO_OK;
 }
 
+int svo_chain_core(const double *p, const double *q, const int32_t *drafts, int k, int64_t V,
+                   const double *u, const double *v, int32_t *tokens, int32_t *accept_len,
+                   int32_t *boundary, double *probs, double *work)
+{
+    return svo_chain_core_t(p, q, drafts, k, V, u, v, 1.0, 1.0, tokens, accept_len, boundary, probs,
+                            work);
+}
+
 /* ------------------------------------------------------------------------------------------ */
 /* Tree verification of one request with explicit uniforms.                                    */
 /*   mode 0 (greedy): amax[n] is the argmax of node n's row; p is unused.                      */
@@ -319,10 +350,10 @@ int svo_tree_check(const int32_t *tokens, const int32_t *parents, int N, int64_t
     return st;
 }
 
-int svo_tree_core(const double *p, const int32_t *amax, const int32_t *tokens,
-                  const int32_t *parents, int N, int64_t V, int mode, const double *coin,
-                  const double *v, int32_t *out_tokens, int32_t *accept_index,
-                  int32_t *accept_len, int32_t *boundary, double *work)
+int svo_tree_core_t(const double *p, const int32_t *amax, const int32_t *tokens,
+                    const int32_t *parents, int N, int64_t V, int mode, const double *coin,
+                    const double *v, double thr_single, double thr_acc, int32_t *out_tokens,
+                    int32_t *accept_index, int32_t *accept_len, int32_t *boundary, double *work)
 {
     for (int i = 0; i < N; ++i) {
         out_tokens[i] = -1;
@@ -356,8 +387,10 @@ int svo_tree_core(const double *p, const int32_t *amax, const int32_t *tokens,
                 if (parents[ch] != cur || tokens[ch] < 0) continue;
                 double pt = pc[tokens[ch]];
                 acc += pt;
-                if (pt > 0.0 && fabs(c - acc) < SVO_BOUNDARY_REL) *boundary = 1;
-                if (pt > 0.0 && c < acc) {
+                double a = acc / thr_acc;
+                if (pt > 0.0 && fabs(c - a) < SVO_BOUNDARY_REL * fmax(1.0, a)) *boundary = 1;
+                if (pt > 0.0 && thr_single < 1.0 && fabs(pt - thr_single) < SVO_BOUNDARY_REL) *boundary = 1;
+                if (pt > 0.0 && (c < a || pt >= thr_single)) {
                     next = ch;
                     break;
                 }
@@ -385,6 +418,15 @@ int svo_tree_core(const double *p, const int32_t *amax, const int32_t *tokens,
     }
     *accept_len = L;
     return SVO_OK;
+}
+
+int svo_tree_core(const double *p, const int32_t *amax, const int32_t *tokens,
+                  const int32_t *parents, int N, int64_t V, int mode, const double *coin,
+                  const double *v, int32_t *out_tokens, int32_t *accept_index,
+                  int32_t *accept_len, int32_t *boundary, double *work)
+{
+    return svo_tree_core_t(p, amax, tokens, parents, N, V, mode, coin, v, 1.0, 1.0, out_tokens,
+                           accept_index, accept_len, boundary, work);
 }
 
 /* ------------------------------------------------------------------------------------------ */
@@ -712,8 +754,9 @@ int svo_grid_chain_first_token(const double *p0, const double *q0, const double 
 
 /* One level of a target-only tree: the root (row p0) has n_child children with the given     */
 /* tokens; integrate the first emitted token over (coin, v) on a G x G grid.                  */
-int svo_grid_tree_first_token(const double *p0, const int32_t *child_tokens, int n_child,
-                              int64_t V, int G, double *dist, double *accept_rate)
+int svo_grid_tree_first_token_t(const double *p0, const int32_t *child_tokens, int n_child,
+                                int64_t V, int G, double thr_single, double thr_acc, double *dist,
+                                double *accept_rate)
 {
     int N = n_child + 1;
     double *p = (double *)malloc(sizeof(double) * (size_t)N * (size_t)V);
@@ -746,8 +789,8 @@ int svo_grid_tree_first_token(const double *p0, const int32_t *child_tokens, int
                 v[d] = (c + 0.5) / G;
             }
             int32_t len, bnd = 0;
-            int st = svo_tree_core(p, NULL, tokens, parents, N, V, 1, coin, v, ot, ai, &len, &bnd,
-                                   work);
+            int st = svo_tree_core_t(p, NULL, tokens, parents, N, V, 1, coin, v, thr_single, thr_acc,
+                                     ot, ai, &len, &bnd, work);
             if (st != SVO_OK) {
                 rc = st;
                 goto done;
@@ -763,6 +806,158 @@ done:
     free(parents);
     free(ot);
     free(ai);
+    free(coin);
+    free(v);
+    return rc;
+}
+
+int svo_grid_tree_first_token(const double *p0, const int32_t *child_tokens, int n_child,
+                              int64_t V, int G, double *dist, double *accept_rate)
+{
+    return svo_grid_tree_first_token_t(p0, child_tokens, n_child, V, G, 1.0, 1.0, dist, accept_rate);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Batches with a temperature per request (T_b = 0: greedy for request b) and the relaxed      */
+/* thresholds of target-only decisions.  Chain: drafts [B][k], q [B][k][V] or NULL; outputs as */
+/* svo_verify_rejection (a greedy request's out_probs stay 0).  Tree: outputs as              */
+/* svo_verify_tree; a greedy request walks by argmax, the others by the target-only rule.     */
+/* ------------------------------------------------------------------------------------------ */
+static int svo_temp_ok(double T) { return T == 0.0 || (T > 0.0 && isfinite(T)); }
+static int svo_thr_ok(double t) { return t > 0.0 && t <= 1.0; }
+
+int svo_verify_ex(const void *logits, int dtype, const int32_t *drafts, const float *q, int B,
+                  int k, int64_t V, const double *temps, double thr_single, double thr_acc,
+                  uint64_t seed, uint64_t offset, const int32_t *req_ids, int n_req,
+                  int32_t *out_tokens, int32_t *accept_len, double *out_probs, int32_t *boundary,
+                  int32_t *status)
+{
+    if (B < 1 || k < 0 || V < 1 || n_req < 0 || !temps) return SVO_EINVAL;
+    if (!svo_thr_ok(thr_single) || !svo_thr_ok(thr_acc)) return SVO_EINVAL;
+    if (q && (thr_single != 1.0 || thr_acc != 1.0)) return SVO_EINVAL;
+    for (int b = 0; b < B; ++b)
+        if (!svo_temp_ok(temps[b])) return SVO_EINVAL;
+    double *p = (double *)malloc(sizeof(double) * (size_t)(k + 1) * (size_t)V);
+    double *qd = q ? (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1) * (size_t)V) : NULL;
+    double *work = (double *)malloc(sizeof(double) * (size_t)V);
+    double *u = (double *)malloc(sizeof(double) * (size_t)(k + 1));
+    double *v = (double *)malloc(sizeof(double) * (size_t)(k + 1));
+    int32_t *amax = (int32_t *)malloc(sizeof(int32_t) * (size_t)(k + 1));
+    int rc = SVO_OK;
+    if (!p || (q && !qd) || !work || !u || !v || !amax) {
+        rc = SVO_ENOMEM;
+        goto done;
+    }
+    for (int i = 0; i < n_req; ++i) {
+        int b = req_ids ? req_ids[i] : i;
+        int32_t *tok = out_tokens + (int64_t)i * (k + 1);
+        double *probs = out_probs ? out_probs + (int64_t)i * (k + 1) * 3 : NULL;
+        for (int r = 0; r <= k; ++r) tok[r] = -1;
+        if (probs) memset(probs, 0, sizeof(double) * 3 * (size_t)(k + 1));
+        accept_len[i] = -1;
+        boundary[i] = 0;
+        status[i] = SVO_OK;
+        if (b < 0 || b >= B) {
+            rc = SVO_EINVAL;
+            goto done;
+        }
+        const int32_t *d = drafts + (int64_t)b * k;
+        for (int r = 0; r < k; ++r)
+            if (d[r] < -1 || d[r] >= V) status[i] = SVO_BAD_TOKEN;
+        const double T = temps[b];
+        for (int r = 0; r <= k; ++r) {
+            int64_t row = (int64_t)b * (k + 1) + r;
+            int st = T == 0.0 ? svo_argmax_row(logits, dtype, row, V, &amax[r])
+                              : svo_softmax_row(logits, dtype, row, V, T, p + (int64_t)r * V);
+            if (st > status[i]) status[i] = st;
+        }
+        if (status[i] != SVO_OK) continue;
+        if (T == 0.0) {
+            /* Greedy request: accept while the draft is the row's argmax, then emit the argmax. */
+            int j = k;
+            for (int r = 0; r < k; ++r) {
+                if (d[r] < 0 || d[r] != amax[r]) {
+                    j = r;
+                    break;
+                }
+                tok[r] = d[r];
+            }
+            tok[j] = amax[j];
+            accept_len[i] = j;
+            continue;
+        }
+        if (q) {
+            const float *qb = q + (int64_t)b * k * V;
+            for (int64_t e = 0; e < (int64_t)k * V; ++e) qd[e] = (double)qb[e];
+        }
+        for (int r = 0; r <= k; ++r) svo_uniform_pair(seed, offset, (uint32_t)r, (uint32_t)b, &u[r], &v[r]);
+        status[i] = svo_chain_core_t(p, qd, d, k, V, u, v, thr_single, thr_acc, tok, &accept_len[i],
+                                     &boundary[i], probs, work);
+    }
+done:
+    free(p);
+    free(qd);
+    free(work);
+    free(u);
+    free(v);
+    free(amax);
+    return rc;
+}
+
+int svo_verify_tree_ex(const void *logits, int dtype, const int32_t *tokens, const int32_t *parents,
+                       int B, int N, int64_t V, const double *temps, double thr_single,
+                       double thr_acc, uint64_t seed, uint64_t offset, const int32_t *req_ids,
+                       int n_req, int32_t *out_tokens, int32_t *accept_index, int32_t *accept_len,
+                       int32_t *boundary, int32_t *status)
+{
+    if (B < 1 || N < 1 || V < 1 || n_req < 0 || !temps) return SVO_EINVAL;
+    if (!svo_thr_ok(thr_single) || !svo_thr_ok(thr_acc)) return SVO_EINVAL;
+    for (int b = 0; b < B; ++b)
+        if (!svo_temp_ok(temps[b])) return SVO_EINVAL;
+    double *p = (double *)malloc(sizeof(double) * (size_t)N * (size_t)V);
+    int32_t *amax = (int32_t *)malloc(sizeof(int32_t) * (size_t)N);
+    double *work = (double *)malloc(sizeof(double) * (size_t)V);
+    double *coin = (double *)malloc(sizeof(double) * (size_t)N);
+    double *v = (double *)malloc(sizeof(double) * (size_t)N);
+    int rc = SVO_OK;
+    if (!p || !amax || !work || !coin || !v) {
+        rc = SVO_ENOMEM;
+        goto done;
+    }
+    for (int i = 0; i < n_req; ++i) {
+        int b = req_ids ? req_ids[i] : i;
+        int32_t *ot = out_tokens + (int64_t)i * N;
+        int32_t *ai = accept_index + (int64_t)i * N;
+        for (int r = 0; r < N; ++r) ot[r] = ai[r] = -1;
+        accept_len[i] = -1;
+        boundary[i] = 0;
+        status[i] = SVO_OK;
+        if (b < 0 || b >= B) {
+            rc = SVO_EINVAL;
+            goto done;
+        }
+        const int mode = temps[b] == 0.0 ? 0 : 1;
+        const int32_t *tk = tokens + (int64_t)b * N;
+        const int32_t *pa = parents + (int64_t)b * N;
+        for (int r = 0; r < N; ++r) {
+            int64_t row = (int64_t)b * N + r;
+            int st = mode == 1 ? svo_softmax_row(logits, dtype, row, V, temps[b], p + (int64_t)r * V)
+                               : svo_argmax_row(logits, dtype, row, V, &amax[r]);
+            if (st > status[i]) status[i] = st;
+        }
+        if (status[i] != SVO_OK) {
+            int st = svo_tree_check(tk, pa, N, V, mode);
+            if (st > status[i]) status[i] = st;
+            continue;
+        }
+        for (int d = 0; d < N; ++d) svo_uniform_pair(seed, offset, (uint32_t)d, (uint32_t)b, &coin[d], &v[d]);
+        status[i] = svo_tree_core_t(p, amax, tk, pa, N, V, mode, coin, v, thr_single, thr_acc, ot, ai,
+                                    &accept_len[i], &boundary[i], work);
+    }
+done:
+    free(p);
+    free(amax);
+    free(work);
     free(coin);
     free(v);
     return rc;
