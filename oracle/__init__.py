@@ -187,8 +187,9 @@ def argmax_rows(logits):
 # ---------------------------------------------------------------------------------------
 # Cores with explicit uniforms (used by the self-tests)
 # ---------------------------------------------------------------------------------------
-def chain_core(p, q, drafts, u, v):
-    """One request: p [(k+1), V] fp64, q [k, V] fp64 or None, drafts [k], u/v [k+1]."""
+def chain_core(p, q, drafts, u, v, thr_single=1.0, thr_acc=1.0):
+    """One request: p [(k+1), V] fp64, q [k, V] fp64 or None, drafts [k], u/v [k+1]; thresholds
+    below 1 relax the target-only test (q None)."""
     lib = _load()
     p = _c(p, np.float64)
     k1, V = p.shape
@@ -201,8 +202,9 @@ def chain_core(p, q, drafts, u, v):
     probs = np.zeros((k + 1, 3), np.float64)
     work = np.zeros(V, np.float64)
     alen, bnd = ctypes.c_int32(), ctypes.c_int32(0)
-    st = lib.svo_chain_core(_ptr(p), _ptr(q), _ptr(d), k, V, _ptr(u), _ptr(v), _ptr(tokens),
-                            ctypes.byref(alen), ctypes.byref(bnd), _ptr(probs), _ptr(work))
+    st = lib.svo_chain_core_t(_ptr(p), _ptr(q), _ptr(d), k, V, _ptr(u), _ptr(v), float(thr_single),
+                              float(thr_acc), _ptr(tokens), ctypes.byref(alen), ctypes.byref(bnd),
+                              _ptr(probs), _ptr(work))
     return dict(status=st, tokens=tokens, accept_len=alen.value, boundary=bnd.value, probs=probs)
 
 
@@ -261,25 +263,6 @@ def grid_tree_first_token(p0, child_tokens, G: int, thr_single=1.0, thr_acc=1.0)
     _check(lib.svo_grid_tree_first_token_t(_ptr(p0), _ptr(ct), ct.shape[0], V, G, float(thr_single),
                                            float(thr_acc), _ptr(dist), ctypes.byref(acc)))
     return dist, acc.value
-
-
-def chain_core(p, q, drafts, u, v, thr_single=1.0, thr_acc=1.0):
-    """Chain verification of one request from probabilities: p [k+1, V], q [k, V] or None,
-    drafts [k], uniforms u, v [k+1].  Returns (tokens, accept_len, boundary)."""
-    lib = _load()
-    pp = _c(p, np.float64)
-    k1, V = pp.shape
-    k = k1 - 1
-    qq = None if q is None else _c(q, np.float64).reshape(k, V)
-    d = _c(drafts, np.int32).reshape(k)
-    uu, vv = _c(u, np.float64), _c(v, np.float64)
-    tok = np.zeros(k1, np.int32)
-    alen, bnd = ctypes.c_int32(), ctypes.c_int32(0)
-    work = np.zeros(V, np.float64)
-    _check(lib.svo_chain_core_t(_ptr(pp), _ptr(qq), _ptr(d), k, V, _ptr(uu), _ptr(vv),
-                                float(thr_single), float(thr_acc), _ptr(tok), ctypes.byref(alen),
-                                ctypes.byref(bnd), None, _ptr(work)))
-    return tok, alen.value, bnd.value
 
 
 # ---------------------------------------------------------------------------------------

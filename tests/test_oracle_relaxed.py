@@ -36,8 +36,12 @@ def test_thresholds_of_one_are_the_exact_rule(oracle):
             d[rng.integers(0, k)] = -1
         u, v = rng.random(k + 1), rng.random(k + 1)
         a = oracle.chain_core(p, None, d, u, v)
-        b = oracle.chain_core(p, None, d, u, v, 1.0, 1.0)
-        assert a[0].tolist() == b[0].tolist() and a[1] == b[1]
+        b = oracle.chain_core(p, None, d, u, v, 0.999999, 1.0)
+        c = oracle.chain_core(p, None, d, u, v, 1.0, 1.0)
+        assert a["tokens"].tolist() == c["tokens"].tolist() and a["accept_len"] == c["accept_len"]
+        # A threshold just below 1 changes nothing unless some p(x) reaches it.
+        if all(p[i, d[i]] < 0.999999 for i in range(k) if d[i] >= 0):
+            assert b["tokens"].tolist() == c["tokens"].tolist()
     P = rng.dirichlet(np.ones(7))
     dist, acc = oracle.grid_tree_first_token(P, [3, 1], G, 1.0, 1.0)
     np.testing.assert_allclose(dist, P, atol=2.0 / G)
@@ -58,13 +62,13 @@ def test_relaxed_single_candidate_closed_form(oracle, thr_single, thr_acc):
         us = (np.arange(256) + 0.5) / 256
         got = np.mean([oracle.chain_core(np.stack([p, p]), None, np.array([x], np.int32),
                                          np.array([u, 0.5]), np.array([0.5, 0.5]),
-                                         thr_single, thr_acc)[1] == 1 for u in us])
+                                         thr_single, thr_acc)["accept_len"] == 1 for u in us])
         assert got == pytest.approx(want, abs=1.0 / 256 + 1e-12)
         # A rejected candidate is never emitted at that slot.
-        tok, L, _ = oracle.chain_core(np.stack([p, p]), None, np.array([x], np.int32),
-                                      np.array([0.9999, 0.5]), np.array([0.3, 0.5]), thr_single, thr_acc)
-        if L == 0:
-            assert tok[0] != x
+        r = oracle.chain_core(np.stack([p, p]), None, np.array([x], np.int32),
+                              np.array([0.9999, 0.5]), np.array([0.3, 0.5]), thr_single, thr_acc)
+        if r["accept_len"] == 0:
+            assert r["tokens"][0] != x
 
 
 def _argmax_prefix(lg, d):
