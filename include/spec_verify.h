@@ -165,6 +165,54 @@ int spec_verify_tree(const void *logits, int dtype, const int32_t *node_tokens,
                      void *stream);
 
 /*
+ * Verify variants: a temperature per request and relaxed acceptance thresholds.
+ *   temperatures    [B] float, device, or NULL.  Request b samples at temperatures[b] > 0 or is
+ *                   greedy when temperatures[b] == 0: a batch may mix both ("The speculative
+ *                   decoding zoo", DSpark section: the greedy rule for greedy requests, the
+ *                   sampling rule for the others, merged).  NULL: every request uses
+ *                   `temperature` (0 = all greedy).
+ *   threshold_single, threshold_acc
+ *                   in (0, 1]; 1 is the exact rule.  Target-only decisions (chain without draft
+ *                   probabilities; tree) accept a candidate c with p(c) > 0 when the coin is below
+ *                   (running sum of the tried candidates' p) / threshold_acc, or when
+ *                   p(c) >= threshold_single ("投机解码", section 接受规则为什么不改变分布,
+ *                   SGLang 默认 subsection and its remark on the two thresholds): values below 1
+ *                   accept more and no longer preserve the target distribution.  With draft
+ *                   probabilities both must be 1 (SPEC_VERIFY_EINVAL otherwise).
+ */
+typedef struct spec_verify_options {
+    const float *temperatures;
+    float temperature;
+    float threshold_single;
+    float threshold_acc;
+} spec_verify_options;
+
+/*
+ * spec_verify_rejection with options: arguments, layouts, outputs and status codes as for
+ * spec_verify_rejection (temperature taken from opt); a greedy request's out_probs row is 0.
+ * Workspace: spec_verify_workspace_bytes(SPEC_VERIFY_MODE_REJECTION, B, k, V).
+ * SPEC_VERIFY_EINVAL also for a NULL opt, a temperature that is negative or not finite (the
+ * per-request temperatures are checked on the device: a negative or NaN entry is treated as
+ * sampling with that value and yields a bad-row status), or thresholds outside (0, 1].
+ */
+int spec_verify_rejection_ex(const void *logits, int dtype, const int32_t *draft_ids,
+                             const float *draft_probs, int B, int k, int V,
+                             const spec_verify_options *opt, uint64_t seed, uint64_t offset,
+                             int32_t *out_tokens, int32_t *accept_len, float *out_probs,
+                             void *workspace, size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * spec_verify_tree with options: a request with temperature 0 walks by argmax (mode 0), the
+ * others by the target-only rule at their temperature, with the relaxed thresholds.
+ * Workspace: spec_verify_workspace_bytes(SPEC_VERIFY_MODE_TREE, B, N, V).
+ */
+int spec_verify_tree_ex(const void *logits, int dtype, const int32_t *node_tokens,
+                        const int32_t *parents, int B, int N, int V, const spec_verify_options *opt,
+                        uint64_t seed, uint64_t offset, int32_t *out_tokens, int32_t *accept_index,
+                        int32_t *accept_len, void *workspace, size_t ws_bytes, int32_t *dev_status,
+                        void *stream);
+
+/*
  * After tree verification: move each request's accepted-path KV rows to contiguous positions
  * after its committed prefix, and advance the committed length ("投机解码", section
  * 与调度、KV 的交互, SGLang part: the committed length grows by the accepted count, and with

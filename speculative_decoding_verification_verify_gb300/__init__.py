@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     MODE_REJECTION,
     MODE_TREE,
     MODE_BLOCK,
+    Options,
     Result,
     SpecVerifyError,
     load_library,
@@ -18,7 +19,9 @@ from .binding import (  # noqa: F401
     spec_verify_kv_compact,
     spec_verify_philox,
     spec_verify_rejection,
+    spec_verify_rejection_ex,
     spec_verify_strerror,
     spec_verify_tree,
+    spec_verify_tree_ex,
     spec_verify_workspace_bytes,
 )

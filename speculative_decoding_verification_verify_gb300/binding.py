@@ -27,6 +27,13 @@ _lib = None
 _lock = threading.Lock()
 
 
+class Options(ctypes.Structure):
+    """spec_verify_options: a temperature per request (device float32 [B], 0 = greedy) or one
+    temperature for all, and the relaxed thresholds of target-only decisions (1 = exact)."""
+    _fields_ = [("temperatures", ctypes.c_void_p), ("temperature", ctypes.c_float),
+                ("threshold_single", ctypes.c_float), ("threshold_acc", ctypes.c_float)]
+
+
 def library_path() -> str:
     return _build.LIB_PATH
 
@@ -67,6 +74,13 @@ def load_library():
         lib.spec_verify_kv_compact.argtypes = [vp, ctypes.c_int64, sz, i32, sz, vp, i32, vp, vp,
                                                vp, vp, i32, i32, vp, vp]
         lib.spec_verify_kv_compact.restype = i32
+        OP = ctypes.POINTER(Options)
+        lib.spec_verify_rejection_ex.argtypes = [vp, i32, vp, vp, i32, i32, i32, OP, u64, u64, vp,
+                                                 vp, vp, vp, sz, vp, vp]
+        lib.spec_verify_rejection_ex.restype = i32
+        lib.spec_verify_tree_ex.argtypes = [vp, i32, vp, vp, i32, i32, i32, OP, u64, u64, vp, vp,
+                                            vp, vp, sz, vp, vp]
+        lib.spec_verify_tree_ex.restype = i32
         _lib = lib
         return lib
 
@@ -360,3 +374,75 @@ def spec_verify_kv_compact(kv_pool: torch.Tensor, slot_table: torch.Tensor,
     if rc != OK:
         raise SpecVerifyError("spec_verify_kv_compact", rc)
     return committed_out, dev_status
+
+
+def _options(temperatures, temperature, threshold_single, threshold_acc, B, device):
+    if temperatures is not None:
+        _check_dev("temperatures", temperatures, torch.float32)
+        if tuple(temperatures.shape) != (B,) or temperatures.device != device:
+            raise ValueError("temperatures must be a [B] float32 tensor on the logits' device")
+    return Options(None if temperatures is None else temperatures.data_ptr(), float(temperature),
+                   float(threshold_single), float(threshold_acc))
+
+
+def spec_verify_rejection_ex(logits: torch.Tensor, draft_ids: torch.Tensor,
+                             draft_probs: Optional[torch.Tensor] = None, *, temperatures=None,
+                             temperature: float = 1.0, threshold_single: float = 1.0,
+                             threshold_acc: float = 1.0, seed: int = 0, offset: int = 0,
+                             out_tokens=None, accept_len=None, out_probs=None, workspace=None,
+                             dev_status=None, stream=None) -> Result:
+    """spec_verify_rejection with a temperature per request (temperatures [B], 0 = greedy
+    request) and relaxed thresholds for target-only decisions."""
+    lib = load_library()
+    _check_dev("logits", logits)
+    B, k1, V = logits.shape
+    k = k1 - 1
+    _check_dev("draft_ids", draft_ids, torch.int32)
+    if draft_probs is not None:
+        _check_dev("draft_probs", draft_probs, torch.float32)
+    dev = logits.device
+    stream = stream or torch.cuda.current_stream(dev)
+    opt = _options(temperatures, temperature, threshold_single, threshold_acc, B, dev)
+    out_tokens = out_tokens if out_tokens is not None else torch.empty((B, k1), dtype=torch.int32, device=dev)
+    accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    nbytes = spec_verify_workspace_bytes(MODE_REJECTION, B, k, V)
+    workspace, dev_status = _ws_and_status(nbytes, dev, stream, workspace, dev_status)
+    rc = lib.spec_verify_rejection_ex(_ptr(logits), _logits_dtype(logits), _ptr(draft_ids),
+                                      _ptr(draft_probs), B, k, V, ctypes.byref(opt),
+                                      int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                      _ptr(out_tokens), _ptr(accept_len), _ptr(out_probs),
+                                      _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                      ctypes.c_void_p(stream.cuda_stream))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_rejection_ex", rc)
+    return Result(out_tokens, accept_len, dev_status, None, out_probs)
+
+
+def spec_verify_tree_ex(logits: torch.Tensor, node_tokens: torch.Tensor, parents: torch.Tensor, *,
+                        temperatures=None, temperature: float = 1.0, threshold_single: float = 1.0,
+                        threshold_acc: float = 1.0, seed: int = 0, offset: int = 0, out_tokens=None,
+                        accept_index=None, accept_len=None, workspace=None, dev_status=None,
+                        stream=None) -> Result:
+    """spec_verify_tree where a request with temperature 0 walks by argmax and the others by the
+    target-only rule at their temperature, with relaxed thresholds."""
+    lib = load_library()
+    _check_dev("logits", logits)
+    B, N, V = logits.shape
+    _check_dev("node_tokens", node_tokens, torch.int32)
+    _check_dev("parents", parents, torch.int32)
+    dev = logits.device
+    stream = stream or torch.cuda.current_stream(dev)
+    opt = _options(temperatures, temperature, threshold_single, threshold_acc, B, dev)
+    out_tokens = out_tokens if out_tokens is not None else torch.empty((B, N), dtype=torch.int32, device=dev)
+    accept_index = accept_index if accept_index is not None else torch.empty((B, N), dtype=torch.int32, device=dev)
+    accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    nbytes = spec_verify_workspace_bytes(MODE_TREE, B, N, V)
+    workspace, dev_status = _ws_and_status(nbytes, dev, stream, workspace, dev_status)
+    rc = lib.spec_verify_tree_ex(_ptr(logits), _logits_dtype(logits), _ptr(node_tokens),
+                                 _ptr(parents), B, N, V, ctypes.byref(opt), int(seed) & (2**64 - 1),
+                                 int(offset) & (2**64 - 1), _ptr(out_tokens), _ptr(accept_index),
+                                 _ptr(accept_len), _ptr(workspace), workspace.numel(),
+                                 _ptr(dev_status), ctypes.c_void_p(stream.cuda_stream))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_tree_ex", rc)
+    return Result(out_tokens, accept_len, dev_status, accept_index)

@@ -72,6 +72,7 @@ struct FinSmem {
     int L;        // accepted drafts
     int mode;     // 0 emit argmax, 1 emit the stop row's draw, 2 residual pending
     int last_tok;
+    float cs;     // the request's log2(e) / T
 };
 
 // State of the residual kernel's last CTA.
@@ -191,7 +192,10 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
         F.row_base[n] = rr * P.nch;
         F.row_L[n] = (int)P.nch;
     }
-    if (tid == 0) F.status = 0;
+    if (tid == 0) {
+        F.status = 0;
+        F.cs = P.temps ? cs_of(__ldg(P.temps + b)) : P.cs;
+    }
     __syncthreads();
     if (!P.is_tree) {
         // A chain is a path: node n's only child is n + 1 (when its draft is usable).
@@ -347,7 +351,7 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, 
     warp_rec_merge(mc, s);
     // The children: one reference M covers them and the rest, so a child far above every other
     // token cannot overflow.
-    const float cs = P.cs;
+    const float cs = F.cs;
     float M = mc;
 #pragma unroll
     for (int h = 0; h < 2; ++h) M = fmaxf(M, cap[h] * cs);
@@ -466,7 +470,7 @@ __device__ void row_draw_prep(const Params &P, int b, int n, FinSmem &F, int lan
         int lastc = -1, drawn = -1;
         for (int e = 0; e < rs.cnt && drawn < 0; ++e) {
             const float cp = __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[rs.off + e]);
-            const float w = ex2(fmaf(cp, P.cs, -rs.M));
+            const float w = ex2(fmaf(cp, F.cs, -rs.M));
             if (w > 0.f) {
                 lastc = F.ex_col[rs.off + e];
                 c += w;
@@ -539,8 +543,15 @@ __device__ void decide_request(const Params &P, FinSmem &F, int lane)
                     if (i < k) {
                         const int x = F.tok[i + 1];
                         if (x >= 0) {
-                            if (SAMPLE) acc = F.u[i] * F.qx[i + 1] < F.node_p[i + 1];
-                            else acc = (x == F.row_arg[i]);
+                            if (SAMPLE && P.q) {
+                                acc = F.u[i] * F.qx[i + 1] < F.node_p[i + 1];
+                            } else if (SAMPLE) {
+                                // Target-only: one candidate; thresholds of 1 give u < p(x).
+                                const float px = F.node_p[i + 1];
+                                acc = px > 0.f && (F.u[i] < px / P.thr_acc || px >= P.thr_single);
+                            } else {
+                                acc = (x == F.row_arg[i]);
+                            }
                         }
                     }
                     const unsigned m = __ballot_sync(0xffffffffu, i < k && !acc);
@@ -569,7 +580,7 @@ __device__ void decide_request(const Params &P, FinSmem &F, int lane)
                     for (int ch = F.first_child[cur]; ch >= 0; ch = F.next_sib[ch]) {
                         const float pc = F.node_p[ch];
                         accp += pc;
-                        if (pc > 0.f && coin < accp) {
+                        if (pc > 0.f && (coin < accp / P.thr_acc || pc >= P.thr_single)) {
                             next = ch;
                             break;
                         }
@@ -659,9 +670,9 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
             P.accept_len[b] = -1;
             raise_status(P.dev_status, F.status);
         }
-        if (SAMPLE && P.out_probs && !P.is_tree)
+        if (P.out_probs && !P.is_tree)
             for (int i = tid; i < (P.k + 1) * 3; i += blockDim.x) P.out_probs[(int64_t)b * (P.k + 1) * 3 + i] = 0.f;
-        if (SAMPLE && P.q && !P.is_tree && tid == 0) P.pend[b] = make_int4(-1, 0, 0, 0);
+        if (P.q && !P.is_tree && tid == 0) P.pend[b] = make_int4(-1, 0, 0, 0);
         return;
     }
     const int L = F.L, stop = F.stop, mode = F.mode;
@@ -677,7 +688,7 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
                            F.rs_c0[stop], F.rs_c1[stop], stage, tid, blockDim.x);
             cp_async_wait_all();
             __syncthreads();
-            drawn = rescan_staged<T>(r * P.V, P.mis, F.rs_c0[stop], F.rs_c1[stop], P.cs, F.row_mc[stop],
+            drawn = rescan_staged<T>(r * P.V, P.mis, F.rs_c0[stop], F.rs_c1[stop], F.cs, F.row_mc[stop],
                                      F.rs_t[stop], F.rs_cum[stop], F.ex_col + F.ex_off[stop], F.ex_n[stop],
                                      stage, F.RS);
         }
@@ -690,8 +701,11 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
         ot[i] = v;
         if (P.is_tree) P.accept_index[(int64_t)b * rpr + i] = (i == 0) ? 0 : (i <= L ? F.path[i - 1] : -1);
     }
+    if (!SAMPLE && P.out_probs && !P.is_tree)  // a greedy request of a mixed batch
+        for (int i = tid; i < (P.k + 1) * 3; i += blockDim.x) P.out_probs[(int64_t)b * (P.k + 1) * 3 + i] = 0.f;
     if (tid == 0) {
         P.accept_len[b] = L;
+        if (!SAMPLE && P.q && !P.is_tree) P.pend[b] = make_int4(-1, 0, 0, 0);
         if (SAMPLE && P.q && !P.is_tree) {
             if (mode == 2)
                 P.pend[b] = make_int4(stop, __float_as_int(F.row_M[stop]), __float_as_int(F.row_tot[stop]), 1);
@@ -718,9 +732,11 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
 // ---------------------------------------------------------------------------------------------
 // The streaming kernel: every CTA folds its share of the flat logits range into per-warp records.
 // ---------------------------------------------------------------------------------------------
-template <typename T, bool SAMPLE>
+// KIND: 0 greedy, 1 sampling, 2 a temperature per request (greedy or sampling per chunk).
+template <typename T, int KIND>
 __global__ void __launch_bounds__(NT_S, 1) sv_stream_kernel(const Params P)
 {
+    constexpr bool SAMPLE = KIND != 0;
     __shared__ unsigned next_chunk;
     constexpr int VEC = Elt<T>::VEC;
     const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
@@ -737,6 +753,8 @@ __global__ void __launch_bounds__(NT_S, 1) sv_stream_kernel(const Params P)
     NodeView nv;
     Kids kd;
     kd.col[0] = kd.col[1] = INT_MAX;
+    float cs = P.cs;
+    bool greedy_b = false;
     while ((int64_t)c < nq) {
         unsigned nxt = 0;
         if (lane == 0) nxt = atomicAdd(&next_chunk, 1u);
@@ -747,15 +765,34 @@ __global__ void __launch_bounds__(NT_S, 1) sv_stream_kernel(const Params P)
         const int n = (int)(r - (int64_t)b * P.rpr);
         const Seg sg = chunk_of<VEC>(P, r, j);
         const T *row = reinterpret_cast<const T *>(P.logits) + r * P.V;
-        // The row's child tokens are (re)derived while the chunk's first loads are in flight.
-        stream_chunk<T, SAMPLE>(row, sg, lane, P.cs, kd, P.caps + (int64_t)b * P.rpr, P.recs + q, [&]() {
-            if (SAMPLE && (b != cur_b || n != cur_n)) {
-                if (b != cur_b) load_nodes(P, b, lane, nv);
+        float *caps = P.caps + (int64_t)b * P.rpr;
+        if (KIND == 2) {
+            // The request's temperature decides the chunk's fold; nodes and children are
+            // refreshed first (a global load only when the request changes).
+            if (b != cur_b || n != cur_n) {
+                if (b != cur_b) {
+                    load_nodes(P, b, lane, nv);
+                    const float Tb = __ldg(P.temps + b);
+                    greedy_b = Tb == 0.f;
+                    cs = greedy_b ? 1.f : cs_of(Tb);
+                }
                 kids_of(P, nv, n, kd);
                 cur_b = b;
                 cur_n = n;
             }
-        });
+            if (greedy_b) stream_chunk<T, false>(row, sg, lane, cs, kd, caps, P.recs + q, []() {});
+            else stream_chunk<T, true>(row, sg, lane, cs, kd, caps, P.recs + q, []() {});
+        } else {
+            // The row's child tokens are (re)derived while the chunk's first loads are in flight.
+            stream_chunk<T, SAMPLE>(row, sg, lane, cs, kd, caps, P.recs + q, [&]() {
+                if (SAMPLE && (b != cur_b || n != cur_n)) {
+                    if (b != cur_b) load_nodes(P, b, lane, nv);
+                    kids_of(P, nv, n, kd);
+                    cur_b = b;
+                    cur_n = n;
+                }
+            });
+        }
         c = __shfl_sync(0xffffffffu, nxt, 0);
     }
 }
@@ -768,7 +805,10 @@ __global__ void __launch_bounds__(NT_FIN_MAX) sv_finalize_kernel(const Params P)
 {
     __shared__ FinSmem F;
     __shared__ uint4 stage[SAMPLE ? RESCAN_STAGE_VEC : 1];  // the stop row's rescan range
-    finalize_request<T, SAMPLE>(P, (int)blockIdx.x, F, stage);
+    const int b = (int)blockIdx.x;
+    // A batch with a temperature per request: a greedy request (T = 0) takes the argmax path.
+    if (SAMPLE && P.temps && __ldg(P.temps + b) == 0.f) finalize_request<T, false>(P, b, F, stage);
+    else finalize_request<T, SAMPLE>(P, b, F, stage);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -824,6 +864,7 @@ __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
     const int j = pd.x;
     const float mc = __int_as_float(pd.y), tot = __int_as_float(pd.z);
     const float inv = 1.f / tot;
+    const float cs = P.temps ? cs_of(__ldg(P.temps + b)) : P.cs;
     const int64_t V = P.V;
     const int64_t r = (int64_t)b * P.rpr + j;
     const void *row = reinterpret_cast<const T *>(P.logits) + r * V;
@@ -843,7 +884,7 @@ __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const float p = ex2(fmaf(l[u], P.cs, -mc)) * inv;
+            const float p = ex2(fmaf(l[u], cs, -mc)) * inv;
             zp += p;
             zr += fmaxf(0.f, p - q[u]);
         }
@@ -919,7 +960,7 @@ __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
         const int64_t a0 = (int64_t)rc * P.Ec2, a1 = min(a0 + P.Ec2, V);
         const int64_t sp = (a1 - a0 + NW - 1) / NW;
         const int64_t s0 = min(a0 + rw * sp, a1), s1 = min(s0 + sp, a1);
-        ResidSrc<T> src{row, qrow, s0, s1, P.cs, mc, inv, F.mode, 1.f};
+        ResidSrc<T> src{row, qrow, s0, s1, cs, mc, inv, F.mode, 1.f};
         draw_init(F.D, F.cum_before);
         draw_span<2>(src, (s1 - s0 + 7) / 8, F.take_last ? POS_INF : F.thresh, F.D);
         drawn = F.D.found >= 0 ? F.D.found : F.D.lastpos;
@@ -1219,6 +1260,8 @@ static int common_setup(Params &P, const void *logits, int dtype, int B, int rpr
     if (!d) return SPEC_VERIFY_ECUDA;
     char *ws = static_cast<char *>(workspace);
     P.logits = logits;
+    P.thr_single = 1.f;
+    P.thr_acc = 1.f;
     P.B = B;
     P.rpr = rpr;
     P.V = V;
@@ -1265,12 +1308,14 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (dtype == SPEC_VERIFY_BF16) {
-        sv_stream_kernel<__nv_bfloat16, SAMPLE><<<P.G, NT_S, 0, s>>>(P);
+        if (P.temps) sv_stream_kernel<__nv_bfloat16, 2><<<P.G, NT_S, 0, s>>>(P);
+        else sv_stream_kernel<__nv_bfloat16, SAMPLE ? 1 : 0><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
         if (cudaLaunchKernelEx(&cfg, sv_finalize_kernel<__nv_bfloat16, SAMPLE>, P) != cudaSuccess)
             return SPEC_VERIFY_ECUDA;
     } else {
-        sv_stream_kernel<float, SAMPLE><<<P.G, NT_S, 0, s>>>(P);
+        if (P.temps) sv_stream_kernel<float, 2><<<P.G, NT_S, 0, s>>>(P);
+        else sv_stream_kernel<float, SAMPLE ? 1 : 0><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
         if (cudaLaunchKernelEx(&cfg, sv_finalize_kernel<float, SAMPLE>, P) != cudaSuccess)
             return SPEC_VERIFY_ECUDA;
@@ -1434,6 +1479,95 @@ int spec_verify_tree(const void *logits, int dtype, const int32_t *node_tokens,
         return launch_stream<true>(P, dtype, s);
     }
     return launch_stream<false>(P, dtype, s);
+}
+
+static bool thresholds_ok(const spec_verify_options *opt)
+{
+    return opt->threshold_single > 0.f && opt->threshold_single <= 1.f && opt->threshold_acc > 0.f &&
+           opt->threshold_acc <= 1.f;
+}
+
+int spec_verify_rejection_ex(const void *logits, int dtype, const int32_t *draft_ids,
+                             const float *draft_probs, int B, int k, int V,
+                             const spec_verify_options *opt, uint64_t seed, uint64_t offset,
+                             int32_t *out_tokens, int32_t *accept_len, float *out_probs,
+                             void *workspace, size_t ws_bytes, int32_t *dev_status, void *stream)
+{
+    if (!opt || !thresholds_ok(opt)) return SPEC_VERIFY_EINVAL;
+    if (draft_probs && (opt->threshold_single != 1.f || opt->threshold_acc != 1.f)) return SPEC_VERIFY_EINVAL;
+    if ((uintptr_t)opt->temperatures % 4) return SPEC_VERIFY_EINVAL;
+    const float T = opt->temperature;
+    if (!opt->temperatures && !(T == 0.f || temperature_ok(T))) return SPEC_VERIFY_EINVAL;
+    if (!opt->temperatures && T == 0.f) {  // an all-greedy batch; out_probs, if given, are 0
+        int rc = spec_verify_greedy(logits, dtype, draft_ids, B, k, V, out_tokens, accept_len, workspace,
+                                    ws_bytes, dev_status, stream);
+        if (rc == SPEC_VERIFY_OK && out_probs &&
+            cudaMemsetAsync(out_probs, 0, sizeof(float) * 3 * (size_t)B * (size_t)(k + 1),
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            rc = SPEC_VERIFY_ECUDA;
+        return rc;
+    }
+    if (B < 1 || B > B_MAX || k < 0 || k + 1 > MAX_RPR || V < 1) return SPEC_VERIFY_EINVAL;
+    if ((k > 0 && !draft_ids) || !out_tokens || !accept_len) return SPEC_VERIFY_EINVAL;
+    if (draft_probs && ((uintptr_t)draft_probs % 4)) return SPEC_VERIFY_EINVAL;
+    Params P;
+    memset(&P, 0, sizeof P);
+    int rc = common_setup(P, logits, dtype, B, k + 1, V, workspace, ws_bytes);
+    if (rc) return rc;
+    P.drafts = draft_ids;
+    P.q = (k > 0) ? draft_probs : nullptr;
+    P.k = k;
+    P.is_tree = 0;
+    P.out_tokens = out_tokens;
+    P.accept_len = accept_len;
+    P.out_probs = out_probs;
+    P.dev_status = dev_status;
+    set_rng(P, opt->temperatures ? 1.f : T, seed, offset);
+    P.temps = opt->temperatures;
+    P.thr_single = opt->threshold_single;
+    P.thr_acc = opt->threshold_acc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = launch_stream<true>(P, dtype, s);
+    if (rc || !P.q) return rc;
+    const unsigned grid = (unsigned)P.C2 * (unsigned)B;
+    if (dtype == SPEC_VERIFY_BF16)
+        sv_residual_kernel<__nv_bfloat16><<<grid, NT, 0, s>>>(P);
+    else
+        sv_residual_kernel<float><<<grid, NT, 0, s>>>(P);
+    return cudaGetLastError() == cudaSuccess ? SPEC_VERIFY_OK : SPEC_VERIFY_ECUDA;
+}
+
+int spec_verify_tree_ex(const void *logits, int dtype, const int32_t *node_tokens,
+                        const int32_t *parents, int B, int N, int V, const spec_verify_options *opt,
+                        uint64_t seed, uint64_t offset, int32_t *out_tokens, int32_t *accept_index,
+                        int32_t *accept_len, void *workspace, size_t ws_bytes, int32_t *dev_status,
+                        void *stream)
+{
+    if (!opt || !thresholds_ok(opt)) return SPEC_VERIFY_EINVAL;
+    if ((uintptr_t)opt->temperatures % 4) return SPEC_VERIFY_EINVAL;
+    const float T = opt->temperature;
+    if (!opt->temperatures && !(T == 0.f || temperature_ok(T))) return SPEC_VERIFY_EINVAL;
+    if (B < 1 || B > B_MAX || N < 1 || N > MAX_RPR || V < 1) return SPEC_VERIFY_EINVAL;
+    if (!node_tokens || !parents || !out_tokens || !accept_index || !accept_len) return SPEC_VERIFY_EINVAL;
+    Params P;
+    memset(&P, 0, sizeof P);
+    int rc = common_setup(P, logits, dtype, B, N, V, workspace, ws_bytes);
+    if (rc) return rc;
+    P.node_tokens = node_tokens;
+    P.parents = parents;
+    P.k = N - 1;
+    P.is_tree = 1;
+    P.out_tokens = out_tokens;
+    P.accept_index = accept_index;
+    P.accept_len = accept_len;
+    P.dev_status = dev_status;
+    P.thr_single = opt->threshold_single;
+    P.thr_acc = opt->threshold_acc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!opt->temperatures && T == 0.f) return launch_stream<false>(P, dtype, s);
+    set_rng(P, opt->temperatures ? 1.f : T, seed, offset);
+    P.temps = opt->temperatures;
+    return launch_stream<true>(P, dtype, s);
 }
 
 int spec_verify_philox(uint64_t seed, uint64_t offset, int n_slot, int n_req, uint32_t *out,

@@ -36,6 +36,8 @@ struct Params {
     int64_t V;
     double v_inv;                // 1 / V, for quick exact division by V
     float cs;                    // log2(e) / T: p is proportional to 2^(logit * cs)
+    const float *temps;          // [B] per-request temperatures (0: greedy request), or null
+    float thr_single, thr_acc;   // relaxed thresholds of target-only decisions (1: exact)
     uint32_t key0, key1, off0, off1;
     int64_t total;               // B * rpr * V
     int64_t nch;                 // streaming chunks per row
@@ -206,6 +208,9 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
     }
     return make_uint4(c0, c1, c2, c3);
 }
+
+// log2(e) / T in double, rounded once: the scale of a request's logits (T > 0).
+__device__ __forceinline__ float cs_of(float T) { return (float)(1.4426950408889634 / (double)T); }
 
 __device__ __forceinline__ float u01(uint32_t x) { return (float)(x >> 8) * 5.9604644775390625e-08f; }
 

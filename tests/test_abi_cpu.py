@@ -91,6 +91,19 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert lib.spec_verify_greedy(fake, 0, fake, 4, 3, 100, fake, fake, P(0x10008), n, None,
                                   None) == -2
     assert lib.spec_verify_philox(1, 0, 0, 4, fake, None) == -1
+    # Options: thresholds outside (0, 1], thresholds with draft probabilities, bad temperature.
+    Opt = binding.Options
+    for bad in (Opt(None, 1.0, 0.0, 1.0), Opt(None, 1.0, 1.0, 1.5), Opt(None, -1.0, 1.0, 1.0),
+                Opt(None, float("nan"), 1.0, 1.0), Opt(0x10002, 1.0, 1.0, 1.0)):
+        assert lib.spec_verify_rejection_ex(fake, 0, fake, None, 4, 3, 100, ctypes.byref(bad), 1, 0,
+                                            fake, fake, None, fake, n, None, None) == -1
+        assert lib.spec_verify_tree_ex(fake, 0, fake, fake, 4, 8, 100, ctypes.byref(bad), 1, 0, fake,
+                                       fake, fake, fake, n, None, None) == -1
+    relaxed = Opt(None, 1.0, 0.5, 1.0)
+    assert lib.spec_verify_rejection_ex(fake, 0, fake, fake, 4, 3, 100, ctypes.byref(relaxed), 1, 0,
+                                        fake, fake, None, fake, n, None, None) == -1
+    assert lib.spec_verify_rejection_ex(fake, 0, fake, None, 4, 3, 100, None, 1, 0, fake, fake, None,
+                                        fake, n, None, None) == -1
     # KV compaction: (pool, num_slots, row_bytes, planes, plane_stride, slot_table, max_pos,
     # committed_in, committed_out, accept_index, accept_len, B, N, dev_status, stream)
     kv = lib.spec_verify_kv_compact
