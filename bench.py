@@ -61,7 +61,7 @@ def parse_args():
     ap.add_argument("--no-modes", action="store_true", help="skip the other verify modes")
     ap.add_argument("--modes", default="all",
                     help="comma list of other modes to time: greedy, tree, block, with_q, b1k3, "
-                         "kv_compact (default all)")
+                         "variants, kv_compact (default all)")
     ap.add_argument("--kv-max-pos", type=int, default=512,
                     help="positions per request of the KV-compaction cache (512: 3.2 GB)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -484,7 +484,7 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
             raise RuntimeError(f"{name} returned {rc}")
 
     res = {}
-    names = {"greedy", "tree", "block", "with_q", "b1k3", "kv_compact"}
+    names = {"greedy", "tree", "block", "with_q", "b1k3", "kv_compact", "variants"}
     want = names if args.modes == "all" else set(args.modes.split(","))
     if want - names:
         raise SystemExit(f"unknown modes {sorted(want - names)}; known: {sorted(names)}")
@@ -498,6 +498,8 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
         res.update(_block_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak, want))
     if "b1k3" in want:
         res.update(_b1k3_mode(torch, sv, wl, dev, lib, P, cur, check, status, peak))
+    if "variants" in want:
+        res.update(_variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak))
     if "kv_compact" in want:
         res.update(_kv_mode(torch, wl, dev, lib, P, cur, check, status, peak, args.kv_max_pos))
     if int(status.item()) != 0:
@@ -601,6 +603,31 @@ def _b1k3_mode(torch, sv, wl, dev, lib, P, cur, check, status, peak):
     return {"standard_b1k3": _mode_entry(ms, Bq * (kq + 1), chain_bytes(Bq, kq, Vq, 2, with_q=True),
                                          peak, 3, note="latency-bound; L2 flushed before each call; "
                                          "algorithmic bytes count all of q")}
+
+
+def _variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak):
+    """Verify variants on the headline workload: a temperature per request (every other request
+    greedy, the rest sampling at T in [0.6, 1.4]) and relaxed thresholds (0.5, 0.5)."""
+    import ctypes as ct
+
+    res = {}
+    sets = [wl.chain_b64k7(dev, seed=9000 + i) for i in range(N_SETS)]
+    nb = sv.spec_verify_workspace_bytes(sv.MODE_REJECTION, B, K_DRAFTS, V)
+    ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+    temps = torch.linspace(0.6, 1.4, B, device=dev)
+    temps[::2] = 0.0
+    opts = {"mixed_temperatures_b64k7": sv.Options(temps.data_ptr(), 1.0, 1.0, 1.0),
+            "relaxed_thresholds_b64k7": sv.Options(None, 1.0, 0.5, 0.5)}
+    for name, opt in opts.items():
+        def call(i, opt=opt):
+            x = sets[i % N_SETS]
+            check(lib.spec_verify_rejection_ex(P(x.logits), sv.BF16, P(x.drafts), None, B, K_DRAFTS, V,
+                                               ct.byref(opt), x.seed, i, P(out), P(alen), None, P(ws), nb,
+                                               P(status), cur()), "spec_verify_rejection_ex")
+
+        ms = graph_time_ms(torch, [lambda i=i: call(i) for i in range(GRAPH_CALLS)], 20)
+        res[name] = _mode_entry(ms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2), peak, 2)
+    return res
 
 
 def _kv_mode(torch, wl, dev, lib, P, cur, check, status, peak, max_pos):
