@@ -460,3 +460,49 @@ def kv_compact(pool, slot_table, committed, accept_index, accept_len):
                 planes[:, dst] = planes[:, src].copy()
         new[b] = c + L + 1
     return new.astype(np.int32), status
+
+
+# ---------------------------------------------------------------------------------------
+# Adaptive verification budget ("The speculative decoding zoo", section "The finer loop:
+# DSpark's confidence budget": every (request, position) slot scores the running product of the
+# request's confidences up to it, a global top-k admits the best slots, ties go to the earlier
+# position, and the budget maximises expected accepted tokens per unit of step cost;
+# "Inference Systems Frontier: new models and speculative decoding", section "Deciding how much
+# to verify by load": the same planner on a toy cost model).
+# Readings: confidences are clamped to [0, 1] with NaN read as 0; survival is the running
+# product in fp32 (the precision the GPU decides in); equal scores go to the earlier position,
+# then the lower request index; slots past a request's number of drafts never compete; the
+# gains are summed in fp64; cost[b] is the caller's cost of a step that admits b draft slots
+# (drafting plus verifying B + b tokens); the first maximal rate wins.
+# ---------------------------------------------------------------------------------------
+BUDGET_MAX_SLOTS = 16384
+
+
+def plan_budget(conf, cost, num_drafts=None):
+    """conf [B, K] confidences; cost [B*K + 1]; num_drafts [B] or None (all K).
+    Returns dict(budget, admitted [B], rate, boundary) where admitted[r] is the number of
+    request r's leading slots admitted and boundary flags a maximal rate that another budget
+    matches within 1e-12 (relative)."""
+    c = np.nan_to_num(np.asarray(conf, np.float32), nan=0.0)
+    c = np.clip(c, np.float32(0.0), np.float32(1.0))
+    B, K = c.shape
+    n_ok = np.full(B, K) if num_drafts is None else np.clip(np.asarray(num_drafts), 0, K)
+    surv = np.empty((B, K), np.float32)
+    run = np.ones(B, np.float32)
+    for i in range(K):
+        run = (run * c[:, i]).astype(np.float32)
+        surv[:, i] = run
+    slots = [(float(surv[r, i]), i, r) for r in range(B) for i in range(int(n_ok[r]))]
+    slots.sort(key=lambda t: (-t[0], t[1], t[2]))
+    gain = [0.0]
+    for s, _, _ in slots:
+        gain.append(gain[-1] + s)
+    cost = np.asarray(cost, np.float64)
+    rates = np.array([(B + gain[b]) / cost[b] for b in range(len(slots) + 1)])
+    best = int(np.argmax(rates))
+    others = np.delete(rates, best)
+    boundary = bool(others.size and np.any(np.abs(others - rates[best]) <= 1e-12 * abs(rates[best])))
+    admitted = np.zeros(B, np.int32)
+    for _, i, r in slots[:best]:
+        admitted[r] = max(admitted[r], i + 1)
+    return dict(budget=best, admitted=admitted, rate=float(rates[best]), boundary=boundary)
