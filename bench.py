@@ -61,7 +61,7 @@ def parse_args():
     ap.add_argument("--no-modes", action="store_true", help="skip the other verify modes")
     ap.add_argument("--modes", default="all",
                     help="comma list of other modes to time: greedy, tree, block, with_q, b1k3, "
-                         "variants, kv_compact (default all)")
+                         "variants, budget, kv_compact (default all)")
     ap.add_argument("--kv-max-pos", type=int, default=512,
                     help="positions per request of the KV-compaction cache (512: 3.2 GB)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -484,7 +484,7 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
             raise RuntimeError(f"{name} returned {rc}")
 
     res = {}
-    names = {"greedy", "tree", "block", "with_q", "b1k3", "kv_compact", "variants"}
+    names = {"greedy", "tree", "block", "with_q", "b1k3", "kv_compact", "variants", "budget"}
     want = names if args.modes == "all" else set(args.modes.split(","))
     if want - names:
         raise SystemExit(f"unknown modes {sorted(want - names)}; known: {sorted(names)}")
@@ -500,6 +500,8 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
         res.update(_b1k3_mode(torch, sv, wl, dev, lib, P, cur, check, status, peak))
     if "variants" in want:
         res.update(_variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak))
+    if "budget" in want:
+        res.update(_budget_modes(torch, sv, dev, lib, P, cur, check))
     if "kv_compact" in want:
         res.update(_kv_mode(torch, wl, dev, lib, P, cur, check, status, peak, args.kv_max_pos))
     if int(status.item()) != 0:
@@ -627,6 +629,32 @@ def _variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, pe
 
         ms = graph_time_ms(torch, [lambda i=i: call(i) for i in range(GRAPH_CALLS)], 20)
         res[name] = _mode_entry(ms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2), peak, 2)
+    return res
+
+
+def _budget_modes(torch, sv, dev, lib, P, cur, check):
+    """The adaptive verification budget (keys, rank, pick) on B x K slots of random confidences
+    with a roofline-shaped cost table; latency per plan."""
+    res = {}
+    g = torch.Generator(device=dev).manual_seed(5)
+    for B_, K_ in ((512, 7), (2048, 8)):
+        conf = torch.rand((B_, K_), generator=g, device=dev) * 0.5 + 0.5
+        b = torch.arange(B_ * K_ + 1, device=dev, dtype=torch.float64)
+        cost = 1.25e-3 + torch.clamp((B_ + b) * 3e-5 - 1e-3, min=0.0)
+        adm = torch.empty(B_, dtype=torch.int32, device=dev)
+        bud = torch.empty(1, dtype=torch.int32, device=dev)
+
+        nws = int(lib.spec_verify_plan_budget_workspace_bytes(B_, K_))
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+
+        def plan():
+            check(lib.spec_verify_plan_budget(P(conf), None, B_, K_, P(cost), P(adm), P(bud), None, P(ws), nws,
+                                              cur()), "spec_verify_plan_budget")
+
+        ms = graph_time_ms(torch, [plan] * 10, 20)
+        res[f"plan_budget_B{B_}_K{K_}"] = {"ms_per_call": ms, "slots": B_ * K_, "budget": int(bud.item()),
+                                          "launches_per_call": 4,
+                                          "note": "latency-bound: keys, a GPU-wide rank, scatter, one picking CTA"}
     return res
 
 

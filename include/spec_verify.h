@@ -213,6 +213,32 @@ int spec_verify_tree_ex(const void *logits, int dtype, const int32_t *node_token
                         void *stream);
 
 /*
+ * Adaptive verification budget: which draft slots of a batch to verify ("The speculative
+ * decoding zoo", section "The finer loop: DSpark's confidence budget"; "Inference Systems
+ * Frontier: new models and speculative decoding", section "Deciding how much to verify by load").
+ *   conf        [B][K] float, device: the drafter's confidence of each (request, position)
+ *               slot; clamped to [0, 1], NaN read as 0.  Survival of slot (r, i) = the fp32
+ *               running product conf[r][0..i].
+ *   num_drafts  [B] int32, device, or NULL (all K): slots at positions >= num_drafts[r] never
+ *               compete.
+ *   cost        [B*K + 1] double, device: cost of a step that admits b draft slots (drafting
+ *               plus verifying B + b tokens), any unit.
+ * Slots are ranked by survival (equal survivals: the earlier position, then the lower request);
+ * budget b scores (B + sum of the b best survivals) / cost[b], summed in fp64; the first maximal
+ * b is chosen.  Outputs (device): admitted [B] (request r verifies its first admitted[r] drafts;
+ * they sum to *budget), *budget, and *best_rate (or NULL).  cost must be positive.
+ * B * K <= 16384, K <= 64.  workspace: device memory, 8-byte aligned, of
+ * spec_verify_plan_budget_workspace_bytes(B, K) bytes (0 for unsupported sizes), caller-owned,
+ * no initialisation needed.  Three launches, asynchronous on `stream`.  SPEC_VERIFY_EINVAL for
+ * bad pointers, alignment or sizes; SPEC_VERIFY_EWORKSPACE for a short or misaligned workspace.
+ */
+#define SPEC_VERIFY_BUDGET_MAX_SLOTS 16384
+size_t spec_verify_plan_budget_workspace_bytes(int B, int K);
+int spec_verify_plan_budget(const float *conf, const int32_t *num_drafts, int B, int K,
+                            const double *cost, int32_t *admitted, int32_t *budget,
+                            double *best_rate, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * After tree verification: move each request's accepted-path KV rows to contiguous positions
  * after its committed prefix, and advance the committed length ("投机解码", section
  * 与调度、KV 的交互, SGLang part: the committed length grows by the accepted count, and with

@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     spec_verify_greedy,
     spec_verify_kv_compact,
     spec_verify_philox,
+    spec_verify_plan_budget,
     spec_verify_rejection,
     spec_verify_rejection_ex,
     spec_verify_strerror,

@@ -9,7 +9,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libspecverify.so")
-SOURCES = [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "sv_kv.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("spec_verify.cu", "sv_kv.cu", "sv_budget.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("sv_device.cuh", "sv_draw.cuh", "sv_stream.cuh", "sv_rescan.cuh")] + [
     os.path.join(INCLUDE, "spec_verify.h")]
 

@@ -81,6 +81,10 @@ def load_library():
         lib.spec_verify_tree_ex.argtypes = [vp, i32, vp, vp, i32, i32, i32, OP, u64, u64, vp, vp,
                                             vp, vp, sz, vp, vp]
         lib.spec_verify_tree_ex.restype = i32
+        lib.spec_verify_plan_budget.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+        lib.spec_verify_plan_budget.restype = i32
+        lib.spec_verify_plan_budget_workspace_bytes.argtypes = [i32, i32]
+        lib.spec_verify_plan_budget_workspace_bytes.restype = sz
         _lib = lib
         return lib
 
@@ -103,6 +107,7 @@ class SpecVerifyError(RuntimeError):
 # Marshalling helpers
 # --------------------------------------------------------------------------------------------
 _ws_cache: dict = {}
+_plan_ws_cache: dict = {}
 
 
 def workspace_for(nbytes: int, device: torch.device, stream: torch.cuda.Stream) -> torch.Tensor:
@@ -446,3 +451,39 @@ def spec_verify_tree_ex(logits: torch.Tensor, node_tokens: torch.Tensor, parents
     if rc != OK:
         raise SpecVerifyError("spec_verify_tree_ex", rc)
     return Result(out_tokens, accept_len, dev_status, accept_index)
+
+
+def spec_verify_plan_budget(conf: torch.Tensor, cost: torch.Tensor, num_drafts=None, *,
+                            admitted=None, budget=None, best_rate=None, stream=None):
+    """Adaptive verification budget: conf [B, K] float32, cost [B*K + 1] float64, num_drafts [B]
+    int32 or None (CUDA tensors).  Returns (admitted [B] int32, budget [1] int32, best_rate [1]
+    float64), all on the device."""
+    lib = load_library()
+    _check_dev("conf", conf, torch.float32)
+    _check_dev("cost", cost, torch.float64)
+    B, K = conf.shape
+    if cost.numel() != B * K + 1:
+        raise ValueError("cost must hold B*K + 1 entries")
+    if num_drafts is not None:
+        _check_dev("num_drafts", num_drafts, torch.int32)
+    dev = conf.device
+    stream = stream or torch.cuda.current_stream(dev)
+    admitted = admitted if admitted is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    budget = budget if budget is not None else torch.empty(1, dtype=torch.int32, device=dev)
+    best_rate = best_rate if best_rate is not None else torch.empty(1, dtype=torch.float64, device=dev)
+    nbytes = int(lib.spec_verify_plan_budget_workspace_bytes(B, K))
+    if nbytes == 0:
+        raise ValueError("the budget planner takes B * K <= 16384 slots and K <= 64")
+    # Not the verifiers' workspace: the planner overwrites its buffer, whose counter region the
+    # verifiers need to stay zero.
+    key = (dev.index, stream.cuda_stream)
+    ws = _plan_ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        _plan_ws_cache[key] = ws
+    rc = lib.spec_verify_plan_budget(_ptr(conf), _ptr(num_drafts), B, K, _ptr(cost), _ptr(admitted),
+                                     _ptr(budget), _ptr(best_rate), _ptr(ws), ws.numel(),
+                                     ctypes.c_void_p(stream.cuda_stream))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_plan_budget", rc)
+    return admitted, budget, best_rate

@@ -104,6 +104,16 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
                                         fake, fake, None, fake, n, None, None) == -1
     assert lib.spec_verify_rejection_ex(fake, 0, fake, None, 4, 3, 100, None, 1, 0, fake, fake, None,
                                         fake, n, None, None) == -1
+    # Budget planner: (conf, num_drafts, B, K, cost, admitted, budget, best_rate, stream)
+    pb = lib.spec_verify_plan_budget
+    assert pb(None, None, 4, 7, fake, fake, fake, None, fake, n, None) == -1
+    assert pb(fake, None, 4, 65, fake, fake, fake, None, fake, n, None) == -1
+    assert pb(fake, None, 2341, 7, fake, fake, fake, None, fake, n, None) == -1  # 16387 slots
+    assert pb(fake, None, 0, 7, fake, fake, fake, None, fake, n, None) == -1
+    assert pb(fake, None, 4, 7, P(0x10004), fake, fake, None, fake, n, None) == -1  # cost not 8-aligned
+    assert pb(fake, None, 4, 7, fake, fake, fake, None, fake, ctypes.c_size_t(8), None) == -2
+    assert lib.spec_verify_plan_budget_workspace_bytes(512, 7) == 20 * 512 * 7
+    assert lib.spec_verify_plan_budget_workspace_bytes(2341, 7) == 0
     # KV compaction: (pool, num_slots, row_bytes, planes, plane_stride, slot_table, max_pos,
     # committed_in, committed_out, accept_index, accept_len, B, N, dev_status, stream)
     kv = lib.spec_verify_kv_compact
