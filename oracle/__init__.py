@@ -87,11 +87,13 @@ def _load():
         lib.svo_grid_tree_first_token_t.restype = i32
         lib.svo_chain_core_t.argtypes = [P, P, P, i32, i64, P, P, f64, f64, P, I32P, I32P, P, P]
         lib.svo_chain_core_t.restype = i32
-        lib.svo_verify_ex.argtypes = [P, i32, P, P, i32, i32, i64, P, f64, f64, u64, u64, P, i32,
-                                      P, P, P, P, P]
+        lib.svo_verify_ex.argtypes = [P, i32, P, P, i32, i32, i64, P, f64, f64, P, P, u64, u64, P,
+                                      i32, P, P, P, P, P]
         lib.svo_verify_ex.restype = i32
-        lib.svo_verify_tree_ex.argtypes = [P, i32, P, P, i32, i32, i64, P, f64, f64, u64, u64, P,
-                                           i32, P, P, P, P, P]
+        lib.svo_verify_tree_ex.argtypes = [P, i32, P, P, i32, i32, i64, P, f64, f64, P, P, u64, u64,
+                                           P, i32, P, P, P, P, P]
+        lib.svo_filter_row.argtypes = [P, i32, i64, i64, i32, f64, P, I32P]
+        lib.svo_filter_row.restype = i32
         lib.svo_verify_tree_ex.restype = i32
         _lib = lib
         return lib
@@ -306,11 +308,30 @@ def verify_rejection(logits, drafts, q, T: float, seed: int, offset: int, req_id
     return dict(out_tokens=out, accept_len=alen, out_probs=probs, boundary=bnd, status=status)
 
 
+def _opt_arrays(B, top_k, top_p):
+    tk = None if top_k is None else _c(top_k, np.int32).reshape(B)
+    tp = None if top_p is None else _c(top_p, np.float64).reshape(B)
+    return tk, tp
+
+
+def filter_row(logits, row: int, T: float, top_k: int, top_p: float):
+    """Probabilities of one row of logits [rows, V] at temperature T after top-k and top-p."""
+    lib = _load()
+    a, dt = _logits(logits)
+    V = a.shape[-1]
+    p = np.zeros(V, np.float64)
+    _check(lib.svo_softmax_row(_ptr(a), dt, row, V, float(T), _ptr(p)))
+    bnd = ctypes.c_int32(0)
+    _check(lib.svo_filter_row(_ptr(a), dt, row, V, int(top_k), float(top_p), _ptr(p), ctypes.byref(bnd)))
+    return p, bnd.value
+
+
 def verify_ex(logits, drafts, q, temps, seed: int, offset: int, thr_single=1.0, thr_acc=1.0,
-              req_ids=None):
+              req_ids=None, top_k=None, top_p=None):
     """Chain verification with a temperature per request (temps [B]; 0 = greedy for that
-    request) and the relaxed thresholds of target-only decisions (q must be None unless both
-    are 1).  Same outputs as verify_rejection; a greedy request's out_probs are 0."""
+    request), the relaxed thresholds of target-only decisions (q must be None unless both are
+    1) and per-request top-k / top-p on p (top_k [B] int, 0 = off; top_p [B], 1 = off).  Same
+    outputs as verify_rejection; a greedy request's out_probs are 0."""
     lib = _load()
     a, dt = _logits(logits)
     B, k1, V = a.shape
@@ -318,6 +339,7 @@ def verify_ex(logits, drafts, q, temps, seed: int, offset: int, thr_single=1.0, 
     d = _c(drafts, np.int32).reshape(B, k)
     qq = None if q is None else _c(q, np.float32).reshape(B, k, V)
     tt = _c(temps, np.float64).reshape(B)
+    tk, tp = _opt_arrays(B, top_k, top_p)
     ids = _req_ids(req_ids, B)
     n = ids.shape[0]
     out = np.zeros((n, k + 1), np.int32)
@@ -326,13 +348,13 @@ def verify_ex(logits, drafts, q, temps, seed: int, offset: int, thr_single=1.0, 
     bnd = np.zeros(n, np.int32)
     status = np.zeros(n, np.int32)
     _check(lib.svo_verify_ex(_ptr(a), dt, _ptr(d), _ptr(qq), B, k, V, _ptr(tt), float(thr_single),
-                             float(thr_acc), seed, offset, _ptr(ids), n, _ptr(out), _ptr(alen),
-                             _ptr(probs), _ptr(bnd), _ptr(status)))
+                             float(thr_acc), _ptr(tk), _ptr(tp), seed, offset, _ptr(ids), n,
+                             _ptr(out), _ptr(alen), _ptr(probs), _ptr(bnd), _ptr(status)))
     return dict(out_tokens=out, accept_len=alen, out_probs=probs, boundary=bnd, status=status)
 
 
 def verify_tree_ex(logits, tokens, parents, temps, seed: int, offset: int, thr_single=1.0,
-                   thr_acc=1.0, req_ids=None):
+                   thr_acc=1.0, req_ids=None, top_k=None, top_p=None):
     """Tree verification with a temperature per request (0 = greedy walk for that request) and
     the relaxed thresholds of the target-only walk."""
     lib = _load()
@@ -341,6 +363,7 @@ def verify_tree_ex(logits, tokens, parents, temps, seed: int, offset: int, thr_s
     t = _c(tokens, np.int32).reshape(B, N)
     pa = _c(parents, np.int32).reshape(B, N)
     tt = _c(temps, np.float64).reshape(B)
+    tk, tp = _opt_arrays(B, top_k, top_p)
     ids = _req_ids(req_ids, B)
     n = ids.shape[0]
     ot = np.zeros((n, N), np.int32)
@@ -349,8 +372,8 @@ def verify_tree_ex(logits, tokens, parents, temps, seed: int, offset: int, thr_s
     bnd = np.zeros(n, np.int32)
     status = np.zeros(n, np.int32)
     _check(lib.svo_verify_tree_ex(_ptr(a), dt, _ptr(t), _ptr(pa), B, N, V, _ptr(tt),
-                                  float(thr_single), float(thr_acc), seed, offset, _ptr(ids), n,
-                                  _ptr(ot), _ptr(ai), _ptr(alen), _ptr(bnd), _ptr(status)))
+                                  float(thr_single), float(thr_acc), _ptr(tk), _ptr(tp), seed, offset,
+                                  _ptr(ids), n, _ptr(ot), _ptr(ai), _ptr(alen), _ptr(bnd), _ptr(status)))
     return dict(out_tokens=ot, accept_index=ai, accept_len=alen, boundary=bnd, status=status)
 
 

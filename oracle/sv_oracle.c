@@ -60,6 +60,13 @@
  *     accept more and change the output distribution.  A chain without draft probabilities is
  *     the one-candidate case (running sum = p(x)).  With draft probabilities the thresholds do
  *     not apply (reading: the pages give them only for the target-only kernel).
+ *   - Top-k / top-p: p is the target distribution after temperature and top-k / top-p ("投机解码",
+ *     section 接受规则为什么不改变分布: p already carries temperature, top-k and top-p).  The pages do
+ *     not define the filters; readings: top-k keeps every token whose logit reaches the k-th
+ *     largest logit (ties at the boundary all kept; k <= 0 or k >= V: off); top-p then keeps,
+ *     among those, the fewest whole value levels from the top whose probability (renormalised
+ *     over the top-k set) reaches top_p (top_p >= 1: off); p is renormalised over what is kept.
+ *     A top-p crossing within 1e-4 (relative) of its target is flagged as a boundary case.
  *   - Per-request temperature in one batch ("The speculative decoding zoo", DSpark section:
  *     accept_draft_tokens runs the greedy rule when the whole batch is greedy, the sampling rule
  *     when none is, and both, merged, when the batch is mixed): request b uses T_b; T_b = 0
@@ -183,6 +190,64 @@ int svo_softmax_row(const void *logits, int dtype, int64_t row, int64_t V, doubl
         sum += p[y];
     }
     for (int64_t y = 0; y < V; ++y) p[y] /= sum;
+    return SVO_OK;
+}
+
+/* Top-k then top-p on a row's probabilities p (from the logits of `row`), in place: zero what
+ * is not kept, renormalise.  Sets *boundary when a top-p decision is within 1e-4 of its target. */
+static int svo_cmp_desc(const void *a, const void *b)
+{
+    double x = *(const double *)a, y = *(const double *)b;
+    return x < y ? 1 : (x > y ? -1 : 0);
+}
+
+int svo_filter_row(const void *logits, int dtype, int64_t row, int64_t V, int top_k, double top_p,
+                   double *p, int32_t *boundary)
+{
+    int use_k = top_k >= 1 && top_k < V, use_p = top_p < 1.0;
+    if (!use_k && !use_p) return SVO_OK;
+    double *x = (double *)malloc(sizeof(double) * (size_t)V);
+    double *srt = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!x || !srt) {
+        free(x);
+        free(srt);
+        return SVO_ENOMEM;
+    }
+    for (int64_t y = 0; y < V; ++y) x[y] = srt[y] = svo_load(logits, dtype, row * V + y);
+    qsort(srt, (size_t)V, sizeof(double), svo_cmp_desc);
+    double tau = -INFINITY;
+    if (use_k) tau = srt[top_k - 1]; /* the k-th largest logit */
+    if (use_p) {
+        /* Mass of the top-k set, then whole value levels from the top until top_p of it. */
+        double zk = 0.0;
+        for (int64_t y = 0; y < V; ++y)
+            if (x[y] >= tau) zk += p[y];
+        double target = top_p * zk, cum = 0.0;
+        int64_t i = 0;
+        double taup = tau;
+        while (i < V && srt[i] >= tau) {
+            double level = srt[i], m = 0.0;
+            for (int64_t y = 0; y < V; ++y)
+                if (x[y] == level) m += p[y];
+            while (i < V && srt[i] == level) ++i;
+            double before = cum;
+            cum += m;
+            if (fabs(cum - target) < 1e-4 * zk || fabs(before - target) < 1e-4 * zk) *boundary = 1;
+            if (cum >= target) {
+                taup = level;
+                break;
+            }
+        }
+        if (taup > tau) tau = taup;
+    }
+    double z = 0.0;
+    for (int64_t y = 0; y < V; ++y) {
+        if (!(x[y] >= tau)) p[y] = 0.0;
+        z += p[y];
+    }
+    for (int64_t y = 0; y < V; ++y) p[y] /= z;
+    free(x);
+    free(srt);
     return SVO_OK;
 }
 
@@ -828,6 +893,7 @@ static int svo_thr_ok(double t) { return t > 0.0 && t <= 1.0; }
 
 int svo_verify_ex(const void *logits, int dtype, const int32_t *drafts, const float *q, int B,
                   int k, int64_t V, const double *temps, double thr_single, double thr_acc,
+                  const int32_t *top_k, const double *top_p,
                   uint64_t seed, uint64_t offset, const int32_t *req_ids, int n_req,
                   int32_t *out_tokens, int32_t *accept_len, double *out_probs, int32_t *boundary,
                   int32_t *status)
@@ -836,7 +902,7 @@ int svo_verify_ex(const void *logits, int dtype, const int32_t *drafts, const fl
     if (!svo_thr_ok(thr_single) || !svo_thr_ok(thr_acc)) return SVO_EINVAL;
     if (q && (thr_single != 1.0 || thr_acc != 1.0)) return SVO_EINVAL;
     for (int b = 0; b < B; ++b)
-        if (!svo_temp_ok(temps[b])) return SVO_EINVAL;
+        if (!svo_temp_ok(temps[b]) || (top_p && !(top_p[b] > 0.0))) return SVO_EINVAL;
     double *p = (double *)malloc(sizeof(double) * (size_t)(k + 1) * (size_t)V);
     double *qd = q ? (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1) * (size_t)V) : NULL;
     double *work = (double *)malloc(sizeof(double) * (size_t)V);
@@ -869,6 +935,9 @@ int svo_verify_ex(const void *logits, int dtype, const int32_t *drafts, const fl
             int64_t row = (int64_t)b * (k + 1) + r;
             int st = T == 0.0 ? svo_argmax_row(logits, dtype, row, V, &amax[r])
                               : svo_softmax_row(logits, dtype, row, V, T, p + (int64_t)r * V);
+            if (st == SVO_OK && T != 0.0)
+                st = svo_filter_row(logits, dtype, row, V, top_k ? top_k[b] : 0, top_p ? top_p[b] : 1.0,
+                                    p + (int64_t)r * V, &boundary[i]);
             if (st > status[i]) status[i] = st;
         }
         if (status[i] != SVO_OK) continue;
@@ -906,14 +975,15 @@ done:
 
 int svo_verify_tree_ex(const void *logits, int dtype, const int32_t *tokens, const int32_t *parents,
                        int B, int N, int64_t V, const double *temps, double thr_single,
-                       double thr_acc, uint64_t seed, uint64_t offset, const int32_t *req_ids,
+                       double thr_acc, const int32_t *top_k, const double *top_p, uint64_t seed,
+                       uint64_t offset, const int32_t *req_ids,
                        int n_req, int32_t *out_tokens, int32_t *accept_index, int32_t *accept_len,
                        int32_t *boundary, int32_t *status)
 {
     if (B < 1 || N < 1 || V < 1 || n_req < 0 || !temps) return SVO_EINVAL;
     if (!svo_thr_ok(thr_single) || !svo_thr_ok(thr_acc)) return SVO_EINVAL;
     for (int b = 0; b < B; ++b)
-        if (!svo_temp_ok(temps[b])) return SVO_EINVAL;
+        if (!svo_temp_ok(temps[b]) || (top_p && !(top_p[b] > 0.0))) return SVO_EINVAL;
     double *p = (double *)malloc(sizeof(double) * (size_t)N * (size_t)V);
     int32_t *amax = (int32_t *)malloc(sizeof(int32_t) * (size_t)N);
     double *work = (double *)malloc(sizeof(double) * (size_t)V);
@@ -943,6 +1013,9 @@ int svo_verify_tree_ex(const void *logits, int dtype, const int32_t *tokens, con
             int64_t row = (int64_t)b * N + r;
             int st = mode == 1 ? svo_softmax_row(logits, dtype, row, V, temps[b], p + (int64_t)r * V)
                                : svo_argmax_row(logits, dtype, row, V, &amax[r]);
+            if (st == SVO_OK && mode == 1)
+                st = svo_filter_row(logits, dtype, row, V, top_k ? top_k[b] : 0, top_p ? top_p[b] : 1.0,
+                                    p + (int64_t)r * V, &boundary[i]);
             if (st > status[i]) status[i] = st;
         }
         if (status[i] != SVO_OK) {
