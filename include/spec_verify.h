@@ -179,12 +179,22 @@ int spec_verify_tree(const void *logits, int dtype, const int32_t *node_tokens,
  *                   SGLang 默认 subsection and its remark on the two thresholds): values below 1
  *                   accept more and no longer preserve the target distribution.  With draft
  *                   probabilities both must be 1 (SPEC_VERIFY_EINVAL otherwise).
+ *   top_k, top_p    [B] int32 / float, device, or NULL: p is the target distribution after
+ *                   temperature, top-k and top-p ("投机解码", section 接受规则为什么不改变分布).
+ *                   Top-k keeps every token whose logit reaches the k-th largest logit (ties kept
+ *                   whole; k <= 0 or k >= V: off); top-p then keeps the fewest whole value levels
+ *                   from the top whose probability, renormalised over the top-k set, reaches top_p
+ *                   (>= 1: off; <= 0 keeps the top level).  p is renormalised over what is kept;
+ *                   greedy requests are unaffected.  An extra kernel finds each row's logit
+ *                   threshold first (a few passes over the row).
  */
 typedef struct spec_verify_options {
     const float *temperatures;
     float temperature;
     float threshold_single;
     float threshold_acc;
+    const int32_t *top_k;
+    const float *top_p;
 } spec_verify_options;
 
 /*

@@ -31,7 +31,8 @@ class Options(ctypes.Structure):
     """spec_verify_options: a temperature per request (device float32 [B], 0 = greedy) or one
     temperature for all, and the relaxed thresholds of target-only decisions (1 = exact)."""
     _fields_ = [("temperatures", ctypes.c_void_p), ("temperature", ctypes.c_float),
-                ("threshold_single", ctypes.c_float), ("threshold_acc", ctypes.c_float)]
+                ("threshold_single", ctypes.c_float), ("threshold_acc", ctypes.c_float),
+                ("top_k", ctypes.c_void_p), ("top_p", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -381,23 +382,29 @@ def spec_verify_kv_compact(kv_pool: torch.Tensor, slot_table: torch.Tensor,
     return committed_out, dev_status
 
 
-def _options(temperatures, temperature, threshold_single, threshold_acc, B, device):
-    if temperatures is not None:
-        _check_dev("temperatures", temperatures, torch.float32)
-        if tuple(temperatures.shape) != (B,) or temperatures.device != device:
-            raise ValueError("temperatures must be a [B] float32 tensor on the logits' device")
-    return Options(None if temperatures is None else temperatures.data_ptr(), float(temperature),
-                   float(threshold_single), float(threshold_acc))
+def _options(temperatures, temperature, threshold_single, threshold_acc, B, device, top_k=None,
+             top_p=None):
+    for name, t, dt in (("temperatures", temperatures, torch.float32), ("top_k", top_k, torch.int32),
+                        ("top_p", top_p, torch.float32)):
+        if t is not None:
+            _check_dev(name, t, dt)
+            if tuple(t.shape) != (B,) or t.device != device:
+                raise ValueError(f"{name} must be a [B] {dt} tensor on the logits' device")
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    return Options(ptr(temperatures), float(temperature), float(threshold_single), float(threshold_acc),
+                   ptr(top_k), ptr(top_p))
 
 
 def spec_verify_rejection_ex(logits: torch.Tensor, draft_ids: torch.Tensor,
                              draft_probs: Optional[torch.Tensor] = None, *, temperatures=None,
                              temperature: float = 1.0, threshold_single: float = 1.0,
-                             threshold_acc: float = 1.0, seed: int = 0, offset: int = 0,
+                             threshold_acc: float = 1.0, top_k=None, top_p=None, seed: int = 0,
+                             offset: int = 0,
                              out_tokens=None, accept_len=None, out_probs=None, workspace=None,
                              dev_status=None, stream=None) -> Result:
     """spec_verify_rejection with a temperature per request (temperatures [B], 0 = greedy
-    request) and relaxed thresholds for target-only decisions."""
+    request), relaxed thresholds for target-only decisions, and per-request top-k / top-p
+    (top_k [B] int32, top_p [B] float32) on the target distribution."""
     lib = load_library()
     _check_dev("logits", logits)
     B, k1, V = logits.shape
@@ -407,7 +414,7 @@ def spec_verify_rejection_ex(logits: torch.Tensor, draft_ids: torch.Tensor,
         _check_dev("draft_probs", draft_probs, torch.float32)
     dev = logits.device
     stream = stream or torch.cuda.current_stream(dev)
-    opt = _options(temperatures, temperature, threshold_single, threshold_acc, B, dev)
+    opt = _options(temperatures, temperature, threshold_single, threshold_acc, B, dev, top_k, top_p)
     out_tokens = out_tokens if out_tokens is not None else torch.empty((B, k1), dtype=torch.int32, device=dev)
     accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)
     nbytes = spec_verify_workspace_bytes(MODE_REJECTION, B, k, V)
@@ -425,7 +432,8 @@ def spec_verify_rejection_ex(logits: torch.Tensor, draft_ids: torch.Tensor,
 
 def spec_verify_tree_ex(logits: torch.Tensor, node_tokens: torch.Tensor, parents: torch.Tensor, *,
                         temperatures=None, temperature: float = 1.0, threshold_single: float = 1.0,
-                        threshold_acc: float = 1.0, seed: int = 0, offset: int = 0, out_tokens=None,
+                        threshold_acc: float = 1.0, top_k=None, top_p=None, seed: int = 0,
+                        offset: int = 0, out_tokens=None,
                         accept_index=None, accept_len=None, workspace=None, dev_status=None,
                         stream=None) -> Result:
     """spec_verify_tree where a request with temperature 0 walks by argmax and the others by the
@@ -437,7 +445,7 @@ def spec_verify_tree_ex(logits: torch.Tensor, node_tokens: torch.Tensor, parents
     _check_dev("parents", parents, torch.int32)
     dev = logits.device
     stream = stream or torch.cuda.current_stream(dev)
-    opt = _options(temperatures, temperature, threshold_single, threshold_acc, B, dev)
+    opt = _options(temperatures, temperature, threshold_single, threshold_acc, B, dev, top_k, top_p)
     out_tokens = out_tokens if out_tokens is not None else torch.empty((B, N), dtype=torch.int32, device=dev)
     accept_index = accept_index if accept_index is not None else torch.empty((B, N), dtype=torch.int32, device=dev)
     accept_len = accept_len if accept_len is not None else torch.empty(B, dtype=torch.int32, device=dev)

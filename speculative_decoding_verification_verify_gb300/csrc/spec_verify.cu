@@ -36,6 +36,7 @@
 #include "sv_draw.cuh"
 #include "sv_stream.cuh"
 #include "sv_rescan.cuh"
+#include "sv_topkp.cuh"
 
 namespace sv {
 
@@ -73,6 +74,7 @@ struct FinSmem {
     int mode;     // 0 emit argmax, 1 emit the stop row's draw, 2 residual pending
     int last_tok;
     float cs;     // the request's log2(e) / T
+    float thr[MAX_RPR];  // each row's top-k / top-p logit threshold (-inf: not filtered)
 };
 
 // State of the residual kernel's last CTA.
@@ -183,6 +185,7 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
             if (x >= 0 && (int64_t)x < V) qv = __ldg(P.q + ((int64_t)b * P.k + (n - 1)) * V + x);
         }
         F.qx[n] = qv;
+        F.thr[n] = P.thr && (P.top_k || P.top_p) ? __ldcg(P.thr + rbase + n) : NEG_INF;
         if (SAMPLE) {
             const float2 uv = uniforms(P, (uint32_t)n, (uint32_t)b);
             F.u[n] = uv.x;
@@ -326,6 +329,7 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, 
     for (int h = 0; h < 2; ++h) {
         const int e = lane + 32 * h;
         cap[h] = e < cnt ? __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[off + e]) : NEG_INF;
+        if (!(cap[h] >= F.thr[n])) cap[h] = NEG_INF;  // below the row's top-k / top-p threshold
     }
     const int q = (L + 31) >> 5;
     rs.q = q;
@@ -470,7 +474,7 @@ __device__ void row_draw_prep(const Params &P, int b, int n, FinSmem &F, int lan
         int lastc = -1, drawn = -1;
         for (int e = 0; e < rs.cnt && drawn < 0; ++e) {
             const float cp = __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[rs.off + e]);
-            const float w = ex2(fmaf(cp, F.cs, -rs.M));
+            const float w = cp >= F.thr[n] ? ex2(fmaf(cp, F.cs, -rs.M)) : 0.f;
             if (w > 0.f) {
                 lastc = F.ex_col[rs.off + e];
                 c += w;
@@ -689,7 +693,7 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
             cp_async_wait_all();
             __syncthreads();
             drawn = rescan_staged<T>(r * P.V, P.mis, F.rs_c0[stop], F.rs_c1[stop], F.cs, F.row_mc[stop],
-                                     F.rs_t[stop], F.rs_cum[stop], F.ex_col + F.ex_off[stop], F.ex_n[stop],
+                                     F.thr[stop], F.rs_t[stop], F.rs_cum[stop], F.ex_col + F.ex_off[stop], F.ex_n[stop],
                                      stage, F.RS);
         }
         last = drawn >= 0 ? drawn : 0;  // < 0 only through rounding
@@ -732,7 +736,8 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
 // ---------------------------------------------------------------------------------------------
 // The streaming kernel: every CTA folds its share of the flat logits range into per-warp records.
 // ---------------------------------------------------------------------------------------------
-// KIND: 0 greedy, 1 sampling, 2 a temperature per request (greedy or sampling per chunk).
+// KIND: 0 greedy, 1 sampling, 2 a temperature per request (greedy or sampling per chunk),
+// 3 as 2 with each row's top-k / top-p threshold applied in the sampling fold.
 template <typename T, int KIND>
 __global__ void __launch_bounds__(NT_S, 1) sv_stream_kernel(const Params P)
 {
@@ -754,6 +759,7 @@ __global__ void __launch_bounds__(NT_S, 1) sv_stream_kernel(const Params P)
     Kids kd;
     kd.col[0] = kd.col[1] = INT_MAX;
     float cs = P.cs;
+    float thr = NEG_INF;
     bool greedy_b = false;
     while ((int64_t)c < nq) {
         unsigned nxt = 0;
@@ -766,32 +772,33 @@ __global__ void __launch_bounds__(NT_S, 1) sv_stream_kernel(const Params P)
         const Seg sg = chunk_of<VEC>(P, r, j);
         const T *row = reinterpret_cast<const T *>(P.logits) + r * P.V;
         float *caps = P.caps + (int64_t)b * P.rpr;
-        if (KIND == 2) {
-            // The request's temperature decides the chunk's fold; nodes and children are
-            // refreshed first (a global load only when the request changes).
+        if (KIND >= 2) {
+            // The request's temperature decides the chunk's fold; nodes, children and the row's
+            // threshold are refreshed first (global loads only when the request or row changes).
             if (b != cur_b || n != cur_n) {
                 if (b != cur_b) {
                     load_nodes(P, b, lane, nv);
-                    const float Tb = __ldg(P.temps + b);
+                    const float Tb = P.temps ? __ldg(P.temps + b) : 1.f;
                     greedy_b = Tb == 0.f;
-                    cs = greedy_b ? 1.f : cs_of(Tb);
+                    cs = greedy_b ? 1.f : (P.temps ? cs_of(Tb) : P.cs);
                 }
                 kids_of(P, nv, n, kd);
+                if (KIND == 3) thr = __ldcg(P.thr + r);
                 cur_b = b;
                 cur_n = n;
             }
-            if (greedy_b) stream_chunk<T, false>(row, sg, lane, cs, kd, caps, P.recs + q, []() {});
-            else stream_chunk<T, true>(row, sg, lane, cs, kd, caps, P.recs + q, []() {});
+            if (greedy_b) stream_chunk<T, false, false>(row, sg, lane, cs, kd, caps, P.recs + q, []() {}, thr);
+            else stream_chunk<T, true, KIND == 3>(row, sg, lane, cs, kd, caps, P.recs + q, []() {}, thr);
         } else {
             // The row's child tokens are (re)derived while the chunk's first loads are in flight.
-            stream_chunk<T, SAMPLE>(row, sg, lane, cs, kd, caps, P.recs + q, [&]() {
+            stream_chunk<T, SAMPLE, false>(row, sg, lane, cs, kd, caps, P.recs + q, [&]() {
                 if (SAMPLE && (b != cur_b || n != cur_n)) {
                     if (b != cur_b) load_nodes(P, b, lane, nv);
                     kids_of(P, nv, n, kd);
                     cur_b = b;
                     cur_n = n;
                 }
-            });
+            }, NEG_INF);
         }
         c = __shfl_sync(0xffffffffu, nxt, 0);
     }
@@ -829,6 +836,7 @@ struct ResidSrc {
     float cs, mc, inv;
     int use_p;           // draw from p instead (residual mass underflowed, or no draft here)
     float w;             // prefix weight of block verification (1 for the standard residual)
+    float thr;           // the row's top-k / top-p threshold: logits below it have p = 0
     __device__ Raw prefetch(int64_t gi) const
     {
         Raw r;
@@ -845,7 +853,7 @@ struct ResidSrc {
     {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float p = ex2(fmaf(r.l[j], cs, -mc)) * inv;
+            const float p = r.l[j] >= thr ? ex2(fmaf(r.l[j], cs, -mc)) * inv : 0.f;
             w[j] = use_p ? p : fmaxf(0.f, this->w * p - r.q[j]);
         }
         return (int)(col0 + gi * 8);
@@ -867,6 +875,7 @@ __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
     const float cs = P.temps ? cs_of(__ldg(P.temps + b)) : P.cs;
     const int64_t V = P.V;
     const int64_t r = (int64_t)b * P.rpr + j;
+    const float thr = P.thr && (P.top_k || P.top_p) ? __ldcg(P.thr + r) : NEG_INF;
     const void *row = reinterpret_cast<const T *>(P.logits) + r * V;
     const float *qrow = P.q + ((int64_t)b * P.k + j) * V;
     const int64_t cc0 = (int64_t)c * P.Ec2, cc1 = min(cc0 + P.Ec2, V);
@@ -884,7 +893,7 @@ __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const float p = ex2(fmaf(l[u], cs, -mc)) * inv;
+            const float p = l[u] >= thr ? ex2(fmaf(l[u], cs, -mc)) * inv : 0.f;
             zp += p;
             zr += fmaxf(0.f, p - q[u]);
         }
@@ -960,7 +969,7 @@ __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
         const int64_t a0 = (int64_t)rc * P.Ec2, a1 = min(a0 + P.Ec2, V);
         const int64_t sp = (a1 - a0 + NW - 1) / NW;
         const int64_t s0 = min(a0 + rw * sp, a1), s1 = min(s0 + sp, a1);
-        ResidSrc<T> src{row, qrow, s0, s1, cs, mc, inv, F.mode, 1.f};
+        ResidSrc<T> src{row, qrow, s0, s1, cs, mc, inv, F.mode, 1.f, thr};
         draw_init(F.D, F.cum_before);
         draw_span<2>(src, (s1 - s0 + 7) / 8, F.take_last ? POS_INF : F.thresh, F.D);
         drawn = F.D.found >= 0 ? F.D.found : F.D.lastpos;
@@ -1129,7 +1138,7 @@ __global__ void __launch_bounds__(NT) sv_block_kernel(const Params P)
         const int64_t r = (int64_t)b * rpr + j;
         const void *row = reinterpret_cast<const T *>(P.logits) + r * V;
         const float *qrow = (j < P.k && !S.use_p) ? P.q + ((int64_t)b * P.k + j) * V : nullptr;
-        ResidSrc<T> src{row, qrow, s0, s1, P.cs, bp.x, 1.f / bp.y, S.use_p, bp.z};
+        ResidSrc<T> src{row, qrow, s0, s1, P.cs, bp.x, 1.f / bp.y, S.use_p, bp.z, NEG_INF};
         draw_init(F.D, F.cum_before);
         draw_span<2>(src, (s1 - s0 + 7) / 8, F.take_last ? POS_INF : S.t, F.D);
         drawn = F.D.found >= 0 ? F.D.found : F.D.lastpos;
@@ -1173,7 +1182,7 @@ static int residual_chunks(int B, int64_t V)
 }
 
 struct Layout {
-    size_t cnt2, recs, caps, pend, recs2, bpend, recs3, total;
+    size_t cnt2, recs, caps, thr, pend, recs2, bpend, recs3, total;
 };
 
 // Streaming chunks per row for elements of `vec` per 16-byte vector (see chunk_of).
@@ -1207,6 +1216,8 @@ static Layout layout(int B, int rpr, int64_t V, bool block = false)
     L.recs = off;
     off += align256(sizeof(float4) * (size_t)R * nch);
     L.caps = off;
+    off += align256(sizeof(float) * (size_t)R);
+    L.thr = off;
     off += align256(sizeof(float) * (size_t)R);
     L.pend = off;
     off += align256(sizeof(int4) * (size_t)B);
@@ -1274,6 +1285,7 @@ static int common_setup(Params &P, const void *logits, int dtype, int B, int rpr
     P.cnt2 = reinterpret_cast<unsigned *>(ws + L.cnt2);
     P.recs = reinterpret_cast<float4 *>(ws + L.recs);
     P.caps = reinterpret_cast<float *>(ws + L.caps);
+    P.thr = reinterpret_cast<float *>(ws + L.thr);
     P.pend = reinterpret_cast<int4 *>(ws + L.pend);
     P.recs2 = reinterpret_cast<float2 *>(ws + L.recs2);
     P.bpend = reinterpret_cast<float4 *>(ws + L.bpend);
@@ -1307,14 +1319,23 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    const bool filt = SAMPLE && (P.top_k || P.top_p);
+    if (filt) {  // each row's top-k / top-p threshold, before the rows are streamed
+        const unsigned rows = (unsigned)((int64_t)P.B * P.rpr);
+        if (dtype == SPEC_VERIFY_BF16) sv_topkp_kernel<__nv_bfloat16><<<rows, NT_TK, 0, s>>>(P);
+        else sv_topkp_kernel<float><<<rows, NT_TK, 0, s>>>(P);
+        if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
+    }
     if (dtype == SPEC_VERIFY_BF16) {
-        if (P.temps) sv_stream_kernel<__nv_bfloat16, 2><<<P.G, NT_S, 0, s>>>(P);
+        if (filt) sv_stream_kernel<__nv_bfloat16, 3><<<P.G, NT_S, 0, s>>>(P);
+        else if (P.temps) sv_stream_kernel<__nv_bfloat16, 2><<<P.G, NT_S, 0, s>>>(P);
         else sv_stream_kernel<__nv_bfloat16, SAMPLE ? 1 : 0><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
         if (cudaLaunchKernelEx(&cfg, sv_finalize_kernel<__nv_bfloat16, SAMPLE>, P) != cudaSuccess)
             return SPEC_VERIFY_ECUDA;
     } else {
-        if (P.temps) sv_stream_kernel<float, 2><<<P.G, NT_S, 0, s>>>(P);
+        if (filt) sv_stream_kernel<float, 3><<<P.G, NT_S, 0, s>>>(P);
+        else if (P.temps) sv_stream_kernel<float, 2><<<P.G, NT_S, 0, s>>>(P);
         else sv_stream_kernel<float, SAMPLE ? 1 : 0><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
         if (cudaLaunchKernelEx(&cfg, sv_finalize_kernel<float, SAMPLE>, P) != cudaSuccess)
@@ -1495,7 +1516,8 @@ int spec_verify_rejection_ex(const void *logits, int dtype, const int32_t *draft
 {
     if (!opt || !thresholds_ok(opt)) return SPEC_VERIFY_EINVAL;
     if (draft_probs && (opt->threshold_single != 1.f || opt->threshold_acc != 1.f)) return SPEC_VERIFY_EINVAL;
-    if ((uintptr_t)opt->temperatures % 4) return SPEC_VERIFY_EINVAL;
+    if ((uintptr_t)opt->temperatures % 4 || (uintptr_t)opt->top_k % 4 || (uintptr_t)opt->top_p % 4)
+        return SPEC_VERIFY_EINVAL;
     const float T = opt->temperature;
     if (!opt->temperatures && !(T == 0.f || temperature_ok(T))) return SPEC_VERIFY_EINVAL;
     if (!opt->temperatures && T == 0.f) {  // an all-greedy batch; out_probs, if given, are 0
@@ -1526,6 +1548,8 @@ int spec_verify_rejection_ex(const void *logits, int dtype, const int32_t *draft
     P.temps = opt->temperatures;
     P.thr_single = opt->threshold_single;
     P.thr_acc = opt->threshold_acc;
+    P.top_k = opt->top_k;
+    P.top_p = opt->top_p;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = launch_stream<true>(P, dtype, s);
     if (rc || !P.q) return rc;
@@ -1544,7 +1568,8 @@ int spec_verify_tree_ex(const void *logits, int dtype, const int32_t *node_token
                         void *stream)
 {
     if (!opt || !thresholds_ok(opt)) return SPEC_VERIFY_EINVAL;
-    if ((uintptr_t)opt->temperatures % 4) return SPEC_VERIFY_EINVAL;
+    if ((uintptr_t)opt->temperatures % 4 || (uintptr_t)opt->top_k % 4 || (uintptr_t)opt->top_p % 4)
+        return SPEC_VERIFY_EINVAL;
     const float T = opt->temperature;
     if (!opt->temperatures && !(T == 0.f || temperature_ok(T))) return SPEC_VERIFY_EINVAL;
     if (B < 1 || B > B_MAX || N < 1 || N > MAX_RPR || V < 1) return SPEC_VERIFY_EINVAL;
@@ -1567,6 +1592,8 @@ int spec_verify_tree_ex(const void *logits, int dtype, const int32_t *node_token
     if (!opt->temperatures && T == 0.f) return launch_stream<false>(P, dtype, s);
     set_rng(P, opt->temperatures ? 1.f : T, seed, offset);
     P.temps = opt->temperatures;
+    P.top_k = opt->top_k;
+    P.top_p = opt->top_p;
     return launch_stream<true>(P, dtype, s);
 }
 

@@ -37,6 +37,9 @@ struct Params {
     double v_inv;                // 1 / V, for quick exact division by V
     float cs;                    // log2(e) / T: p is proportional to 2^(logit * cs)
     const float *temps;          // [B] per-request temperatures (0: greedy request), or null
+    const int32_t *top_k;        // [B] per-request top-k (<= 0 or >= V: off), or null
+    const float *top_p;          // [B] per-request top-p (>= 1: off), or null
+    float *thr;                  // [B * rpr] logit threshold of each row (-inf: not filtered)
     float thr_single, thr_acc;   // relaxed thresholds of target-only decisions (1: exact)
     uint32_t key0, key1, off0, off1;
     int64_t total;               // B * rpr * V

@@ -44,17 +44,17 @@ __device__ __noinline__ uint4 load_partial(const T *row, int64_t col, int64_t c0
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Weights of one vector at column col with no excluded column in it; elements outside [c0, c1)
-// weigh 0 (only the range's first and last vectors have such elements).
+// Weights of one vector at column col with no excluded column in it; elements outside [c0, c1),
+// or below the row's top-k / top-p threshold thr, weigh 0.
 template <typename T>
 __device__ __forceinline__ void vec_weights_plain(const uint4 &w, int col, int c0, int c1, float cs,
-                                                  float mc, float (&out)[Elt<T>::VEC])
+                                                  float mc, float thr, float (&out)[Elt<T>::VEC])
 {
     constexpr int VEC = Elt<T>::VEC;
     float x[VEC];
     Elt<T>::unpack(w, x);
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) out[j] = ex2(fmaf(x[j], cs, -mc));
+    for (int j = 0; j < VEC; ++j) out[j] = x[j] >= thr ? ex2(fmaf(x[j], cs, -mc)) : 0.f;
     if (col < c0 || col + VEC > c1) {
 #pragma unroll
         for (int j = 0; j < VEC; ++j)
@@ -106,7 +106,7 @@ __device__ __forceinline__ void stage_range(const T *row, int64_t rowflat, int64
 // (or the last positive one) comes from shared-memory atomics, and its owner walks its VEC
 // elements.  Three barriers.
 template <typename T>
-__device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs, float mc, float t,
+__device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs, float mc, float thr, float t,
                              float cum0, const int *ex, int ex_n, const uint4 *stage, RescanSmem &S)
 {
     constexpr int VEC = Elt<T>::VEC;
@@ -126,7 +126,7 @@ __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs,
         if (k < nvv) {
             const int col = a0 + k * VEC;
             float e[VEC];
-            vec_weights_plain<T>(stage[k], col, c0, c1, cs, mc, e);
+            vec_weights_plain<T>(stage[k], col, c0, c1, cs, mc, thr, e);
             for (int x = 0; x < ex_n; ++x) {
                 const int d = ex[x] - col;
 #pragma unroll
@@ -177,7 +177,7 @@ __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs,
             if (r == i) before = pre[r] + inc[r] - vs[r];
         const int col = a0 + kv * VEC;
         float e[VEC];
-        vec_weights_plain<T>(stage[kv], col, c0, c1, cs, mc, e);
+        vec_weights_plain<T>(stage[kv], col, c0, c1, cs, mc, thr, e);
         for (int x = 0; x < ex_n; ++x) {
             const int d = ex[x] - col;
 #pragma unroll

@@ -171,11 +171,12 @@ __device__ __forceinline__ bool scalar_is_child(int col, bool has, float x, int 
     return child;
 }
 
-// One element outside the vector body (a row's unaligned head or tail).
-__device__ __forceinline__ void sample_scalar(SampleAcc &a, float x, float cs)
+// One element outside the vector body (a row's unaligned head or tail); with a top-k / top-p
+// threshold, logits below it weigh 0 (the row's maximum is always kept, so the reference stays).
+__device__ __forceinline__ void sample_scalar(SampleAcc &a, float x, float cs, float thr)
 {
     sample_rescale(a, x, cs);
-    a.acc[0] = f2_add(a.acc[0], f2(ex2(fmaf(x, cs, -a.mc)), 0.f));
+    if (x >= thr) a.acc[0] = f2_add(a.acc[0], f2(ex2(fmaf(x, cs, -a.mc)), 0.f));
 }
 
 __device__ __forceinline__ void greedy_scalar(GreedyAcc &a, float x, int col)
@@ -237,9 +238,9 @@ __device__ __forceinline__ void greedy_step(GreedyAcc &a, const uint4 (&w)[VPL],
 
 // Fold a lane's step (child tokens already masked to -inf): no per-vector checks; filler and
 // masked elements add 2^-inf = 0 to the sums.
-template <typename T>
+template <typename T, bool FILT>
 __device__ __forceinline__ void sample_step_fast(SampleAcc &a, const uint4 (&w)[VPL], uint64_t cs2,
-                                                 uint64_t nmc2)
+                                                 uint64_t nmc2, float thr)
 {
     constexpr int NP = Elt<T>::VEC / 2;
 #pragma unroll
@@ -247,10 +248,14 @@ __device__ __forceinline__ void sample_step_fast(SampleAcc &a, const uint4 (&w)[
         const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
-            uint64_t x2;
-            if (NP == 4) x2 = f2(bf_lo(ww[p]), bf_hi(ww[p]));
-            else x2 = f2(__uint_as_float(ww[2 * p]), __uint_as_float(ww[2 * p + 1]));
-            const float2 z = f2_split(f2_fma(x2, cs2, nmc2));
+            const float xlo = NP == 4 ? bf_lo(ww[p]) : __uint_as_float(ww[2 * p]);
+            const float xhi = NP == 4 ? bf_hi(ww[p]) : __uint_as_float(ww[2 * p + 1]);
+            const uint64_t x2 = f2(xlo, xhi);
+            float2 z = f2_split(f2_fma(x2, cs2, nmc2));
+            if (FILT) {  // below the row's top-k / top-p threshold: weight 0
+                z.x = xlo >= thr ? z.x : NEG_INF;
+                z.y = xhi >= thr ? z.y : NEG_INF;
+            }
             const int j = (u * NP + p) & 3;
             a.acc[j] = f2_add(a.acc[j], f2(ex2(z.x), ex2(z.y)));
         }
@@ -259,16 +264,16 @@ __device__ __forceinline__ void sample_step_fast(SampleAcc &a, const uint4 (&w)[
 
 // Fold one step (VPL vectors per lane at columns lo + (lane + 32 * u) * VEC; columns from hi on
 // are fillers holding -inf, which belong to the next chunk).
-template <typename T, bool SAMPLE>
+template <typename T, bool SAMPLE, bool FILT>
 __device__ __forceinline__ void fold_step(uint4 (&w)[VPL], int lo, int hi, int lane, float cs, uint64_t cs2,
-                                          const Kids &kd, float *caps, SampleAcc &sa, GreedyAcc &ga)
+                                          const Kids &kd, float *caps, SampleAcc &sa, GreedyAcc &ga, float thr)
 {
     if (SAMPLE) {
         const bool mine = (kd.col[0] >= lo && kd.col[0] < hi) || (kd.col[1] >= lo && kd.col[1] < hi);
         if (__any_sync(0xffffffffu, mine)) exclude_step<T>(w, lo, hi, lane, kd, caps);
         sample_rescale(sa, step_max<T>(w), cs);
         const float nmc = -sa.mc;
-        sample_step_fast<T>(sa, w, cs2, f2(nmc, nmc));
+        sample_step_fast<T, FILT>(sa, w, cs2, f2(nmc, nmc), thr);
     } else {
         greedy_step<T>(ga, w, lo + lane * Elt<T>::VEC, step_max<T>(w));
     }
@@ -309,9 +314,9 @@ __device__ __forceinline__ void load_step(uint4 (&d)[VPL], const uint4 *p, int l
 // One warp streams chunk sg of a row: the body's first step and the head and tail elements are
 // loaded first (the caller may update kd meanwhile through `ready`), then the steps are folded
 // and the chunk's record is written to *rec.
-template <typename T, bool SAMPLE, typename Ready>
+template <typename T, bool SAMPLE, bool FILT, typename Ready>
 __device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int lane, float cs, Kids &kd, float *caps,
-                                             float4 *rec, Ready ready)
+                                             float4 *rec, Ready ready, float thr)
 {
     constexpr int VEC = Elt<T>::VEC;
     const int c0 = (int)sg.c0, b0 = (int)sg.b0, b1 = (int)sg.b1, c1 = (int)sg.c1;
@@ -328,7 +333,8 @@ __device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int la
     GreedyAcc ga;
     if (b0 > c0) {  // warp-uniform
         if (SAMPLE) {
-            if (!scalar_is_child(c0 + lane, has_head, xh, c0, b0, lane, kd, caps) && has_head) sample_scalar(sa, xh, cs);
+            if (!scalar_is_child(c0 + lane, has_head, xh, c0, b0, lane, kd, caps) && has_head)
+                sample_scalar(sa, xh, cs, FILT ? thr : NEG_INF);
         } else if (has_head) {
             greedy_scalar(ga, xh, c0 + lane);
         }
@@ -342,11 +348,12 @@ __device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int la
         }
         const int lo = b0 + s * STEP_VEC * VEC;
         const int hi = min(lo + STEP_VEC * VEC, b1);
-        fold_step<T, SAMPLE>(cur, lo, hi, lane, cs, cs2, kd, caps, sa, ga);
+        fold_step<T, SAMPLE, FILT>(cur, lo, hi, lane, cs, cs2, kd, caps, sa, ga, thr);
     }
     if (c1 > b1) {  // warp-uniform
         if (SAMPLE) {
-            if (!scalar_is_child(b1 + lane, has_tail, xt, b1, c1, lane, kd, caps) && has_tail) sample_scalar(sa, xt, cs);
+            if (!scalar_is_child(b1 + lane, has_tail, xt, b1, c1, lane, kd, caps) && has_tail)
+                sample_scalar(sa, xt, cs, FILT ? thr : NEG_INF);
         } else if (has_tail) {
             greedy_scalar(ga, xt, b1 + lane);
         }

@@ -94,7 +94,8 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     # Options: thresholds outside (0, 1], thresholds with draft probabilities, bad temperature.
     Opt = binding.Options
     for bad in (Opt(None, 1.0, 0.0, 1.0), Opt(None, 1.0, 1.0, 1.5), Opt(None, -1.0, 1.0, 1.0),
-                Opt(None, float("nan"), 1.0, 1.0), Opt(0x10002, 1.0, 1.0, 1.0)):
+                Opt(None, float("nan"), 1.0, 1.0), Opt(0x10002, 1.0, 1.0, 1.0),
+                Opt(None, 1.0, 1.0, 1.0, 0x10002, None), Opt(None, 1.0, 1.0, 1.0, None, 0x10001)):
         assert lib.spec_verify_rejection_ex(fake, 0, fake, None, 4, 3, 100, ctypes.byref(bad), 1, 0,
                                             fake, fake, None, fake, n, None, None) == -1
         assert lib.spec_verify_tree_ex(fake, 0, fake, fake, 4, 8, 100, ctypes.byref(bad), 1, 0, fake,
