@@ -169,7 +169,9 @@ __device__ __forceinline__ float rec_mass(const float4 &r, float mc)
 }
 
 // Stage the request's structure, uniforms and record ranges (inputs only).
-template <bool SAMPLE>
+// VAR: the call has per-request temperatures or top-k / top-p thresholds (read from the staged
+// F.cs / F.thr); without it the scale is the call's and nothing is filtered.
+template <bool SAMPLE, bool VAR>
 __device__ void stage_request(const Params &P, int b, FinSmem &F)
 {
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -185,7 +187,7 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
             if (x >= 0 && (int64_t)x < V) qv = __ldg(P.q + ((int64_t)b * P.k + (n - 1)) * V + x);
         }
         F.qx[n] = qv;
-        F.thr[n] = P.thr && (P.top_k || P.top_p) ? __ldcg(P.thr + rbase + n) : NEG_INF;
+        if (VAR) F.thr[n] = P.top_k || P.top_p ? __ldcg(P.thr + rbase + n) : NEG_INF;
         if (SAMPLE) {
             const float2 uv = uniforms(P, (uint32_t)n, (uint32_t)b);
             F.u[n] = uv.x;
@@ -197,7 +199,7 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
     }
     if (tid == 0) {
         F.status = 0;
-        F.cs = P.temps ? cs_of(__ldg(P.temps + b)) : P.cs;
+        if (VAR) F.cs = P.temps ? cs_of(__ldg(P.temps + b)) : P.cs;
     }
     __syncthreads();
     if (!P.is_tree) {
@@ -295,7 +297,7 @@ struct RowState {
 
 // Row n of request b, by one warp, once the records are visible: merge the records, weigh the
 // row's children.
-template <typename T, bool SAMPLE>
+template <typename T, bool SAMPLE, bool VAR>
 __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, RowState &rs)
 {
     rs.base = F.row_base[n];
@@ -329,7 +331,7 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, 
     for (int h = 0; h < 2; ++h) {
         const int e = lane + 32 * h;
         cap[h] = e < cnt ? __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[off + e]) : NEG_INF;
-        if (!(cap[h] >= F.thr[n])) cap[h] = NEG_INF;  // below the row's top-k / top-p threshold
+        if (VAR && !(cap[h] >= F.thr[n])) cap[h] = NEG_INF;  // below the row's top-k / top-p threshold
     }
     const int q = (L + 31) >> 5;
     rs.q = q;
@@ -355,7 +357,7 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, 
     warp_rec_merge(mc, s);
     // The children: one reference M covers them and the rest, so a child far above every other
     // token cannot overflow.
-    const float cs = F.cs;
+    const float cs = VAR ? F.cs : P.cs;
     float M = mc;
 #pragma unroll
     for (int h = 0; h < 2; ++h) M = fmaxf(M, cap[h] * cs);
@@ -394,6 +396,7 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, 
 // The row's draw, children excluded, threshold v * Z with Z the non-child mass: locate the
 // record holding the crossing (F.rs_*) for the rescan, or, when every non-child token is -inf,
 // draw among the children directly (F.cand).
+template <bool VAR>
 __device__ void row_draw_prep(const Params &P, int b, int n, FinSmem &F, int lane, const RowState &rs)
 {
     const float vdraw = F.v[P.is_tree ? F.dep[n] : n];
@@ -474,7 +477,7 @@ __device__ void row_draw_prep(const Params &P, int b, int n, FinSmem &F, int lan
         int lastc = -1, drawn = -1;
         for (int e = 0; e < rs.cnt && drawn < 0; ++e) {
             const float cp = __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[rs.off + e]);
-            const float w = cp >= F.thr[n] ? ex2(fmaf(cp, F.cs, -rs.M)) : 0.f;
+            const float w = (!VAR || cp >= F.thr[n]) ? ex2(fmaf(cp, VAR ? F.cs : P.cs, -rs.M)) : 0.f;
             if (w > 0.f) {
                 lastc = F.ex_col[rs.off + e];
                 c += w;
@@ -486,7 +489,8 @@ __device__ void row_draw_prep(const Params &P, int b, int n, FinSmem &F, int lan
 }
 
 // Decide the accepted path and the stop node (warp 0 calls it; the tree walk runs in lane 0).
-template <bool SAMPLE>
+// VAR: the relaxed thresholds may differ from 1.
+template <bool SAMPLE, bool VAR>
 __device__ void decide_request(const Params &P, FinSmem &F, int lane)
 {
     if (F.status == 0) {
@@ -547,12 +551,12 @@ __device__ void decide_request(const Params &P, FinSmem &F, int lane)
                     if (i < k) {
                         const int x = F.tok[i + 1];
                         if (x >= 0) {
-                            if (SAMPLE && P.q) {
+                            if (SAMPLE && (P.q || !VAR)) {
                                 acc = F.u[i] * F.qx[i + 1] < F.node_p[i + 1];
                             } else if (SAMPLE) {
                                 // Target-only: one candidate; thresholds of 1 give u < p(x).
                                 const float px = F.node_p[i + 1];
-                                acc = px > 0.f && (F.u[i] < px / P.thr_acc || px >= P.thr_single);
+                                acc = px > 0.f && (F.u[i] * P.thr_acc < px || px >= P.thr_single);
                             } else {
                                 acc = (x == F.row_arg[i]);
                             }
@@ -584,7 +588,7 @@ __device__ void decide_request(const Params &P, FinSmem &F, int lane)
                     for (int ch = F.first_child[cur]; ch >= 0; ch = F.next_sib[ch]) {
                         const float pc = F.node_p[ch];
                         accp += pc;
-                        if (pc > 0.f && (coin < accp / P.thr_acc || pc >= P.thr_single)) {
+                        if (pc > 0.f && (VAR ? (coin * P.thr_acc < accp || pc >= P.thr_single) : coin < accp)) {
                             next = ch;
                             break;
                         }
@@ -610,22 +614,22 @@ __device__ void decide_request(const Params &P, FinSmem &F, int lane)
     }
 }
 
-template <typename T, bool SAMPLE>
+template <typename T, bool SAMPLE, bool VAR>
 __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stage)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwf = blockDim.x >> 5;
     const int rpr = P.rpr;
 
-    stage_request<SAMPLE>(P, b, F);
+    stage_request<SAMPLE, VAR>(P, b, F);
     // From here on the streaming kernel's records and captures are read.
     pdl_wait();
     for (int n = warp; n < rpr; n += nwf) {
         RowState rs;
-        finish_row<T, SAMPLE>(P, b, n, F, lane, rs);
-        if (SAMPLE && !rs.bad && F.need_draw[n]) row_draw_prep(P, b, n, F, lane, rs);
+        finish_row<T, SAMPLE, VAR>(P, b, n, F, lane, rs);
+        if (SAMPLE && !rs.bad && F.need_draw[n]) row_draw_prep<VAR>(P, b, n, F, lane, rs);
     }
     __syncthreads();
-    if (warp == 0 && !(P.block && P.q)) decide_request<SAMPLE>(P, F, lane);
+    if (warp == 0 && !(P.block && P.q)) decide_request<SAMPLE, VAR>(P, F, lane);
     __syncthreads();
     const bool faulted = F.status != 0;
 
@@ -692,8 +696,8 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
                            F.rs_c0[stop], F.rs_c1[stop], stage, tid, blockDim.x);
             cp_async_wait_all();
             __syncthreads();
-            drawn = rescan_staged<T>(r * P.V, P.mis, F.rs_c0[stop], F.rs_c1[stop], F.cs, F.row_mc[stop],
-                                     F.thr[stop], F.rs_t[stop], F.rs_cum[stop], F.ex_col + F.ex_off[stop], F.ex_n[stop],
+            drawn = rescan_staged<T, VAR>(r * P.V, P.mis, F.rs_c0[stop], F.rs_c1[stop], VAR ? F.cs : P.cs,
+                                          F.row_mc[stop], VAR ? F.thr[stop] : NEG_INF, F.rs_t[stop], F.rs_cum[stop], F.ex_col + F.ex_off[stop], F.ex_n[stop],
                                      stage, F.RS);
         }
         last = drawn >= 0 ? drawn : 0;  // < 0 only through rounding
@@ -807,15 +811,16 @@ __global__ void __launch_bounds__(NT_S, 1) sv_stream_kernel(const Params P)
 // ---------------------------------------------------------------------------------------------
 // The finalising kernel: one CTA per request merges its records, decides and draws.
 // ---------------------------------------------------------------------------------------------
-template <typename T, bool SAMPLE>
+// VAR: per-request temperatures (a greedy request, T = 0, takes the argmax path) or top-k /
+// top-p thresholds; a separate instantiation, so the plain kernels carry only their own code.
+template <typename T, bool SAMPLE, bool VAR>
 __global__ void __launch_bounds__(NT_FIN_MAX) sv_finalize_kernel(const Params P)
 {
     __shared__ FinSmem F;
     __shared__ uint4 stage[SAMPLE ? RESCAN_STAGE_VEC : 1];  // the stop row's rescan range
     const int b = (int)blockIdx.x;
-    // A batch with a temperature per request: a greedy request (T = 0) takes the argmax path.
-    if (SAMPLE && P.temps && __ldg(P.temps + b) == 0.f) finalize_request<T, false>(P, b, F, stage);
-    else finalize_request<T, SAMPLE>(P, b, F, stage);
+    if (VAR && P.temps && __ldg(P.temps + b) == 0.f) finalize_request<T, false, false>(P, b, F, stage);
+    else finalize_request<T, SAMPLE, VAR>(P, b, F, stage);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1320,6 +1325,7 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const bool filt = SAMPLE && (P.top_k || P.top_p);
+    const bool var = filt || P.temps || P.thr_single != 1.f || P.thr_acc != 1.f;
     if (filt) {  // each row's top-k / top-p threshold, before the rows are streamed
         const unsigned rows = (unsigned)((int64_t)P.B * P.rpr);
         if (dtype == SPEC_VERIFY_BF16) sv_topkp_kernel<__nv_bfloat16><<<rows, NT_TK, 0, s>>>(P);
@@ -1331,14 +1337,18 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
         else if (P.temps) sv_stream_kernel<__nv_bfloat16, 2><<<P.G, NT_S, 0, s>>>(P);
         else sv_stream_kernel<__nv_bfloat16, SAMPLE ? 1 : 0><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
-        if (cudaLaunchKernelEx(&cfg, sv_finalize_kernel<__nv_bfloat16, SAMPLE>, P) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, SAMPLE && var ? sv_finalize_kernel<__nv_bfloat16, SAMPLE, true>
+                                                   : sv_finalize_kernel<__nv_bfloat16, SAMPLE, false>,
+                               P) != cudaSuccess)
             return SPEC_VERIFY_ECUDA;
     } else {
         if (filt) sv_stream_kernel<float, 3><<<P.G, NT_S, 0, s>>>(P);
         else if (P.temps) sv_stream_kernel<float, 2><<<P.G, NT_S, 0, s>>>(P);
         else sv_stream_kernel<float, SAMPLE ? 1 : 0><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
-        if (cudaLaunchKernelEx(&cfg, sv_finalize_kernel<float, SAMPLE>, P) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, SAMPLE && var ? sv_finalize_kernel<float, SAMPLE, true>
+                                               : sv_finalize_kernel<float, SAMPLE, false>,
+                               P) != cudaSuccess)
             return SPEC_VERIFY_ECUDA;
     }
     return cudaGetLastError() == cudaSuccess ? SPEC_VERIFY_OK : SPEC_VERIFY_ECUDA;

@@ -46,7 +46,7 @@ __device__ __noinline__ uint4 load_partial(const T *row, int64_t col, int64_t c0
 
 // Weights of one vector at column col with no excluded column in it; elements outside [c0, c1),
 // or below the row's top-k / top-p threshold thr, weigh 0.
-template <typename T>
+template <typename T, bool FILT>
 __device__ __forceinline__ void vec_weights_plain(const uint4 &w, int col, int c0, int c1, float cs,
                                                   float mc, float thr, float (&out)[Elt<T>::VEC])
 {
@@ -54,7 +54,7 @@ __device__ __forceinline__ void vec_weights_plain(const uint4 &w, int col, int c
     float x[VEC];
     Elt<T>::unpack(w, x);
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) out[j] = x[j] >= thr ? ex2(fmaf(x[j], cs, -mc)) : 0.f;
+    for (int j = 0; j < VEC; ++j) out[j] = (!FILT || x[j] >= thr) ? ex2(fmaf(x[j], cs, -mc)) : 0.f;
     if (col < c0 || col + VEC > c1) {
 #pragma unroll
         for (int j = 0; j < VEC; ++j)
@@ -105,7 +105,7 @@ __device__ __forceinline__ void stage_range(const T *row, int64_t rowflat, int64
 // one table of (round, warp) totals give every vector its running mass; the first crossing vector
 // (or the last positive one) comes from shared-memory atomics, and its owner walks its VEC
 // elements.  Three barriers.
-template <typename T>
+template <typename T, bool FILT>
 __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs, float mc, float thr, float t,
                              float cum0, const int *ex, int ex_n, const uint4 *stage, RescanSmem &S)
 {
@@ -126,7 +126,7 @@ __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs,
         if (k < nvv) {
             const int col = a0 + k * VEC;
             float e[VEC];
-            vec_weights_plain<T>(stage[k], col, c0, c1, cs, mc, thr, e);
+            vec_weights_plain<T, FILT>(stage[k], col, c0, c1, cs, mc, thr, e);
             for (int x = 0; x < ex_n; ++x) {
                 const int d = ex[x] - col;
 #pragma unroll
@@ -177,7 +177,7 @@ __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs,
             if (r == i) before = pre[r] + inc[r] - vs[r];
         const int col = a0 + kv * VEC;
         float e[VEC];
-        vec_weights_plain<T>(stage[kv], col, c0, c1, cs, mc, thr, e);
+        vec_weights_plain<T, FILT>(stage[kv], col, c0, c1, cs, mc, thr, e);
         for (int x = 0; x < ex_n; ++x) {
             const int d = ex[x] - col;
 #pragma unroll

@@ -173,10 +173,11 @@ __device__ __forceinline__ bool scalar_is_child(int col, bool has, float x, int 
 
 // One element outside the vector body (a row's unaligned head or tail); with a top-k / top-p
 // threshold, logits below it weigh 0 (the row's maximum is always kept, so the reference stays).
+template <bool FILT>
 __device__ __forceinline__ void sample_scalar(SampleAcc &a, float x, float cs, float thr)
 {
     sample_rescale(a, x, cs);
-    if (x >= thr) a.acc[0] = f2_add(a.acc[0], f2(ex2(fmaf(x, cs, -a.mc)), 0.f));
+    if (!FILT || x >= thr) a.acc[0] = f2_add(a.acc[0], f2(ex2(fmaf(x, cs, -a.mc)), 0.f));
 }
 
 __device__ __forceinline__ void greedy_scalar(GreedyAcc &a, float x, int col)
@@ -334,7 +335,7 @@ __device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int la
     if (b0 > c0) {  // warp-uniform
         if (SAMPLE) {
             if (!scalar_is_child(c0 + lane, has_head, xh, c0, b0, lane, kd, caps) && has_head)
-                sample_scalar(sa, xh, cs, FILT ? thr : NEG_INF);
+                sample_scalar<FILT>(sa, xh, cs, thr);
         } else if (has_head) {
             greedy_scalar(ga, xh, c0 + lane);
         }
@@ -353,7 +354,7 @@ __device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int la
     if (c1 > b1) {  // warp-uniform
         if (SAMPLE) {
             if (!scalar_is_child(b1 + lane, has_tail, xt, b1, c1, lane, kd, caps) && has_tail)
-                sample_scalar(sa, xt, cs, FILT ? thr : NEG_INF);
+                sample_scalar<FILT>(sa, xt, cs, thr);
         } else if (has_tail) {
             greedy_scalar(ga, xt, b1 + lane);
         }

@@ -7,10 +7,11 @@
 // {logit >= tau}, so one logit threshold per row describes the filter: the streaming fold, the
 // finaliser, the rescan and the residual kernel treat logits below it as -inf.
 //
-// One CTA per row finds tau by radix descent over order-preserving keys of the logits (2 digit
-// levels of 8 bits for bf16, 3 levels of 11, 11 and 10 bits for fp32): at each level a pass over
-// the row histograms the next digit of the keys that match the chosen prefix (counts for top-k,
-// masses 2^((l - max) * cs) for top-p) in shared memory, and one warp walks the bins from the top.
+// One CTA per row finds tau by radix descent over order-preserving keys of the logits (8-bit
+// digits: 2 levels for bf16, 4 for fp32): at each level a pass over the row (16-byte loads)
+// histograms the next digit of the keys that match the chosen prefix (counts for top-k, masses
+// 2^((l - max) * cs) for top-p) in per-warp shared-memory copies, and one warp walks the bins
+// from the top.
 #pragma once
 
 #include "sv_device.cuh"
@@ -18,7 +19,8 @@
 namespace sv {
 
 constexpr int NT_TK = 512;
-constexpr int TK_BINS = 2048;
+constexpr int TK_BINS = 256;        // 8-bit digits
+constexpr int TK_WARPS = NT_TK / 32;
 
 template <typename T>
 struct KeyOf;
@@ -26,12 +28,25 @@ struct KeyOf;
 template <>
 struct KeyOf<__nv_bfloat16> {
     static constexpr int LEVELS = 2;
-    static __device__ __forceinline__ int shift(int lvl) { return lvl == 0 ? 8 : 0; }
-    static __device__ __forceinline__ int bits(int) { return 8; }
+    static constexpr int VEC = 8;
+    static __device__ __forceinline__ int shift(int lvl) { return 8 * (LEVELS - 1 - lvl); }
+    static __device__ __forceinline__ uint32_t key_of_bits(uint32_t u)
+    {
+        return (u & 0x8000u) ? (~u & 0xffffu) : (u | 0x8000u);
+    }
     static __device__ __forceinline__ uint32_t key(const void *row, int64_t c)
     {
-        const uint32_t u = __ldg((const unsigned short *)row + c);
-        return (u & 0x8000u) ? (~u & 0xffffu) : (u | 0x8000u);
+        return key_of_bits(__ldg((const unsigned short *)row + c));
+    }
+    // The VEC keys of a 16-byte vector.
+    static __device__ __forceinline__ void keys(const uint4 &w, uint32_t (&k)[VEC])
+    {
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            k[2 * i] = key_of_bits(ww[i] & 0xffffu);
+            k[2 * i + 1] = key_of_bits(ww[i] >> 16);
+        }
     }
     static __device__ __forceinline__ float value(uint32_t k)
     {
@@ -42,13 +57,23 @@ struct KeyOf<__nv_bfloat16> {
 
 template <>
 struct KeyOf<float> {
-    static constexpr int LEVELS = 3;
-    static __device__ __forceinline__ int shift(int lvl) { return lvl == 0 ? 21 : lvl == 1 ? 10 : 0; }
-    static __device__ __forceinline__ int bits(int lvl) { return lvl == 2 ? 10 : 11; }
+    static constexpr int LEVELS = 4;
+    static constexpr int VEC = 4;
+    static __device__ __forceinline__ int shift(int lvl) { return 8 * (LEVELS - 1 - lvl); }
+    static __device__ __forceinline__ uint32_t key_of_bits(uint32_t u)
+    {
+        return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
     static __device__ __forceinline__ uint32_t key(const void *row, int64_t c)
     {
-        const uint32_t u = __float_as_uint(__ldg((const float *)row + c));
-        return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+        return key_of_bits(__float_as_uint(__ldg((const float *)row + c)));
+    }
+    static __device__ __forceinline__ void keys(const uint4 &w, uint32_t (&k)[VEC])
+    {
+        k[0] = key_of_bits(w.x);
+        k[1] = key_of_bits(w.y);
+        k[2] = key_of_bits(w.z);
+        k[3] = key_of_bits(w.w);
     }
     static __device__ __forceinline__ float value(uint32_t k)
     {
@@ -60,6 +85,8 @@ struct KeyOf<float> {
 struct TopkpSmem {
     int cnt[TK_BINS];
     float mass[TK_BINS];
+    int wcnt[TK_WARPS][TK_BINS];     // per-warp histograms, merged into cnt / mass
+    float wmass[TK_WARPS][TK_BINS];
     float wmax[NT_TK / 32];
     int sel;          // chosen digit
     int above_cnt;    // count in bins above it
@@ -71,7 +98,7 @@ struct TopkpSmem {
 // totals above it; when nothing reaches (rounding), the lowest non-empty bin.
 __device__ __forceinline__ void walk_bins(TopkpSmem &S, int nb, bool by_mass, int rank, float target, int lane)
 {
-    const int per = nb / 32;  // nb is 256, 1024 or 2048
+    const int per = nb / 32;  // nb is 256
     // Lane l takes bins [nb - (l + 1) * per, nb - l * per), the top bins first.
     const int hi = nb - lane * per;
     float m = 0.f;
@@ -122,62 +149,90 @@ __device__ __forceinline__ void walk_bins(TopkpSmem &S, int nb, bool by_mass, in
     }
 }
 
-// Histogram of the next digit of the keys that match `prefix` on the bits above this level's
-// digit and are >= floor_key: counts (MASS false) or masses 2^((l - mx) * cs) (MASS true).  The
-// lanes of a warp that share a digit add their share once, through their lowest lane.
-template <typename T, bool MASS>
-__device__ void key_histogram(const void *row, int64_t V, uint32_t prefix, int lvl, uint32_t floor_key, float mx,
-                              float cs, TopkpSmem &S)
+// Visit every key of a row (row = column 0, rowflat its flat index, mis the logits base's
+// misalignment in elements): the 16-byte aligned body with vector loads, the head and tail
+// element by element.  f(key) is called once per element.
+template <typename T, typename F>
+__device__ __forceinline__ void for_each_key(const void *row, int64_t rowflat, int64_t V, int mis, F f)
 {
-    const int sh = KeyOf<T>::shift(lvl), nb = 1 << KeyOf<T>::bits(lvl);
-    const int top = sh + KeyOf<T>::bits(lvl);
-    const int lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < nb; i += NT_TK) {
-        S.cnt[i] = 0;
-        S.mass[i] = 0.f;
+    constexpr int VEC = KeyOf<T>::VEC;
+    const int64_t a0 = min((int64_t)((VEC - (rowflat + mis) % VEC) % VEC), V);
+    const int64_t nv = (V - a0) / VEC;
+    const int64_t a1 = a0 + nv * VEC;
+    for (int64_t c = threadIdx.x; c < a0; c += NT_TK) f(KeyOf<T>::key(row, c));
+    for (int64_t c = a1 + threadIdx.x; c < V; c += NT_TK) f(KeyOf<T>::key(row, c));
+    const uint4 *vp = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(row) + a0);
+    for (int64_t i = threadIdx.x; i < nv; i += NT_TK) {
+        uint32_t k[VEC];
+        KeyOf<T>::keys(ldg_stream(vp + i), k);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f(k[e]);
     }
-    __syncthreads();
-    for (int64_t base = 0; base < V; base += NT_TK) {
-        const int64_t c = base + threadIdx.x;
-        const uint32_t k = c < V ? KeyOf<T>::key(row, c) : 0u;
-        const bool match = c < V && (top >= 32 || (k >> top) == (prefix >> top)) && k >= floor_key;
-        const unsigned active = __ballot_sync(0xffffffffu, match);
-        if (match) {
-            const int d = (int)((k >> sh) & (uint32_t)(nb - 1));
-            const unsigned grp = __match_any_sync(active, d);
-            const int leader = __ffs(grp) - 1;
-            if (MASS) {
-                const float x = ex2((KeyOf<T>::value(k) - mx) * cs);
-                float sum = 0.f;
-                for (unsigned g = grp; g; g &= g - 1) sum += __shfl_sync(grp, x, __ffs(g) - 1);
-                if (lane == leader) atomicAdd(&S.mass[d], sum);
-            } else if (lane == leader) {
-                atomicAdd(&S.cnt[d], __popc(grp));
-            }
-        }
-    }
-    __syncthreads();
 }
 
-// Sum over the row of the masses of keys >= floor_key.
-template <typename T>
-__device__ float mass_at_or_above(const void *row, int64_t V, uint32_t floor_key, float mx, float cs, TopkpSmem &S)
+// Histogram of the next digit of the keys that match `prefix` on the bits above this level's
+// digit and are >= floor_key: counts (MASS false) or masses 2^((l - mx) * cs) (MASS true).  Each
+// warp fills its own copy; a thread adds a run of equal digits at once (logits cluster in a few
+// high digits), and the copies are merged at the end.
+template <typename T, bool MASS, bool MAX = false>
+__device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int mis, uint32_t prefix, int lvl,
+                              uint32_t floor_key, float mx, float cs, TopkpSmem &S, uint32_t *kmax_out = nullptr,
+                              bool *nan_out = nullptr)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float z = 0.f;
-    for (int64_t c = threadIdx.x; c < V; c += NT_TK) {
-        const uint32_t k = KeyOf<T>::key(row, c);
-        if (k >= floor_key) z += ex2((KeyOf<T>::value(k) - mx) * cs);
+    const int sh = KeyOf<T>::shift(lvl);
+    const int top = sh + 8;
+    const int warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < TK_WARPS * TK_BINS; i += NT_TK) {
+        (&S.wcnt[0][0])[i] = 0;
+        (&S.wmass[0][0])[i] = 0.f;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
     __syncthreads();
-    if (lane == 0) S.wmax[warp] = z;
+    int run_d = -1, run_c = 0;
+    float run_m = 0.f;
+    // Start from the key of -inf: a thread with no element must not report key 0, which is the
+    // key of a NaN bit pattern.
+    uint32_t kmax = KeyOf<T>::key_of_bits(sizeof(T) == 2 ? 0xff80u : 0xff800000u);
+    bool nan = false;
+    for_each_key<T>(row, rowflat, V, mis, [&](uint32_t k) {
+        if (MAX) {
+            kmax = k > kmax ? k : kmax;
+            nan |= KeyOf<T>::value(k) != KeyOf<T>::value(k);
+        }
+        if ((top >= 32 || (k >> top) == (prefix >> top)) && k >= floor_key) {
+            const int d = (int)((k >> sh) & 0xffu);
+            if (d != run_d) {
+                if (run_d >= 0) {
+                    if (MASS) atomicAdd(&S.wmass[warp][run_d], run_m);
+                    else atomicAdd(&S.wcnt[warp][run_d], run_c);
+                }
+                run_d = d;
+                run_c = 0;
+                run_m = 0.f;
+            }
+            if (MASS) run_m += ex2((KeyOf<T>::value(k) - mx) * cs);
+            else ++run_c;
+        }
+    });
+    if (run_d >= 0) {
+        if (MASS) atomicAdd(&S.wmass[warp][run_d], run_m);
+        else atomicAdd(&S.wcnt[warp][run_d], run_c);
+    }
+    if (MAX) {
+        *kmax_out = kmax;
+        *nan_out = nan;
+    }
     __syncthreads();
-    float t = 0.f;
-    for (int w = 0; w < NT_TK / 32; ++w) t += S.wmax[w];
+    for (int i = threadIdx.x; i < TK_BINS; i += NT_TK) {
+        int c = 0;
+        float m = 0.f;
+        for (int w = 0; w < TK_WARPS; ++w) {
+            c += S.wcnt[w][i];
+            m += S.wmass[w][i];
+        }
+        S.cnt[i] = c;
+        S.mass[i] = m;
+    }
     __syncthreads();
-    return t;
 }
 
 // Grid: one CTA per row.  thr[r] = the row's logit threshold, or -inf when the row is not
@@ -200,9 +255,14 @@ __global__ void __launch_bounds__(NT_TK) sv_topkp_kernel(const Params P)
     }
     const float cs = P.temps ? cs_of(Tb) : P.cs;
     const void *row = reinterpret_cast<const T *>(P.logits) + r * V;
-    // The row's largest logit, the masses' reference.
-    float mx = NEG_INF;
-    for (int64_t c = tid; c < V; c += NT_TK) mx = fmax_nan(mx, KeyOf<T>::value(KeyOf<T>::key(row, c)));
+    const int64_t rowflat = r * V;
+    constexpr int LV = KeyOf<T>::LEVELS;
+    // First pass: the row's largest logit (the masses' reference; NaN if the row holds one) and
+    // the top digit's counts, which top-k needs first.
+    uint32_t kmax;
+    bool nan;
+    key_histogram<T, false, true>(row, rowflat, V, P.mis, 0u, 0, 0u, 0.f, cs, S, &kmax, &nan);
+    float mx = nan ? __int_as_float(0x7fc00000) : KeyOf<T>::value(kmax);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) S.wmax[warp] = mx;
@@ -214,15 +274,14 @@ __global__ void __launch_bounds__(NT_TK) sv_topkp_kernel(const Params P)
         if (tid == 0) P.thr[r] = NEG_INF;
         return;
     }
-    constexpr int LV = KeyOf<T>::LEVELS;
-    // Top-k: the key of the k-th largest logit (counts only).
+    // Top-k: the key of the k-th largest logit (counts only; the top digit's are in S already).
     uint32_t kkey = 0u;
     if (use_k) {
         int rank = kk;
         uint32_t prefix = 0u;
         for (int lvl = 0; lvl < LV; ++lvl) {
-            key_histogram<T, false>(row, V, prefix, lvl, 0u, mx, cs, S);
-            if (warp == 0) walk_bins(S, 1 << KeyOf<T>::bits(lvl), false, rank, 0.f, lane);
+            if (lvl > 0) key_histogram<T, false>(row, rowflat, V, P.mis, prefix, lvl, 0u, mx, cs, S);
+            if (warp == 0) walk_bins(S, TK_BINS, false, rank, 0.f, lane);
             __syncthreads();
             prefix |= (uint32_t)S.sel << KeyOf<T>::shift(lvl);
             rank -= S.above_cnt;
@@ -232,12 +291,25 @@ __global__ void __launch_bounds__(NT_TK) sv_topkp_kernel(const Params P)
     }
     uint32_t pkey = kkey;
     if (use_p) {
-        // Top-p within the top-k set: the fewest value levels from the top holding top_p of its mass.
-        float target = pp * mass_at_or_above<T>(row, V, kkey, mx, cs, S);
+        // Top-p within the top-k set: the fewest value levels from the top holding top_p of its
+        // mass; the top digit's mass histogram over the set also gives the set's total.
+        float target = 0.f;
         uint32_t prefix = 0u;
         for (int lvl = 0; lvl < LV; ++lvl) {
-            key_histogram<T, true>(row, V, prefix, lvl, kkey, mx, cs, S);
-            if (warp == 0) walk_bins(S, 1 << KeyOf<T>::bits(lvl), true, 0, target, lane);
+            key_histogram<T, true>(row, rowflat, V, P.mis, prefix, lvl, kkey, mx, cs, S);
+            if (lvl == 0) {
+                if (warp == 0) {
+                    float z = 0.f;
+                    for (int i = lane; i < TK_BINS; i += 32) z += S.mass[i];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+                    if (lane == 0) S.above_mass = z;
+                }
+                __syncthreads();
+                target = pp * S.above_mass;
+                __syncthreads();
+            }
+            if (warp == 0) walk_bins(S, TK_BINS, true, 0, target, lane);
             __syncthreads();
             prefix |= (uint32_t)S.sel << KeyOf<T>::shift(lvl);
             target -= S.above_mass;
