@@ -1327,9 +1327,13 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
     const bool filt = SAMPLE && (P.top_k || P.top_p);
     const bool var = filt || P.temps || P.thr_single != 1.f || P.thr_acc != 1.f;
     if (filt) {  // each row's top-k / top-p threshold, before the rows are streamed
-        const unsigned rows = (unsigned)((int64_t)P.B * P.rpr);
-        if (dtype == SPEC_VERIFY_BF16) sv_topkp_kernel<__nv_bfloat16><<<rows, NT_TK, 0, s>>>(P);
-        else sv_topkp_kernel<float><<<rows, NT_TK, 0, s>>>(P);
+        // Rows in flight: two CTAs per SM hold about 2 * 152 rows (78 MB of bf16 rows of 128256).
+        const int64_t rows = (int64_t)P.B * P.rpr;
+        const DevInfo *d = device_info();
+        const int64_t cap = 2 * (int64_t)(d ? d->sms : 152);
+        const unsigned grid = (unsigned)(rows < cap ? rows : cap);
+        if (dtype == SPEC_VERIFY_BF16) sv_topkp_kernel<__nv_bfloat16><<<grid, NT_TK, 0, s>>>(P);
+        else sv_topkp_kernel<float><<<grid, NT_TK, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
     }
     if (dtype == SPEC_VERIFY_BF16) {

@@ -235,13 +235,11 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
     __syncthreads();
 }
 
-// Grid: one CTA per row.  thr[r] = the row's logit threshold, or -inf when the row is not
+// The threshold of row r: thr[r] = the row's logit threshold, or -inf when the row is not
 // filtered (top-k off and top-p off, or a greedy request).
 template <typename T>
-__global__ void __launch_bounds__(NT_TK) sv_topkp_kernel(const Params P)
+__device__ void topkp_row(const Params &P, int64_t r, TopkpSmem &S)
 {
-    __shared__ TopkpSmem S;
-    const int64_t r = blockIdx.x;
     const int b = (int)(r / P.rpr);
     const int64_t V = P.V;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -318,6 +316,17 @@ __global__ void __launch_bounds__(NT_TK) sv_topkp_kernel(const Params P)
         pkey = prefix > kkey ? prefix : kkey;
     }
     if (tid == 0) P.thr[r] = KeyOf<T>::value(pkey);
+    __syncthreads();
+}
+
+// A few CTAs per SM, each taking rows in turn, so that the rows being filtered at any time fit in
+// L2 and a row's later passes are served from it.
+template <typename T>
+__global__ void __launch_bounds__(NT_TK) sv_topkp_kernel(const Params P)
+{
+    __shared__ TopkpSmem S;
+    const int64_t R = (int64_t)P.B * P.rpr;
+    for (int64_t r = blockIdx.x; r < R; r += gridDim.x) topkp_row<T>(P, r, S);
 }
 
 }  // namespace sv
