@@ -41,6 +41,10 @@
 namespace sv {
 
 constexpr int NT_FIN_MAX = 256;  // threads of a finalising CTA: one warp per row, up to 8 rows
+// Rows whose crossing range is copied to shared memory as soon as it is located, before the
+// decide names the stop row (one 8 KB slot per warp's first row).
+constexpr int PF_ROWS = NT_FIN_MAX / 32;
+constexpr int PF_SMEM_BYTES = PF_ROWS * RESCAN_STAGE_VEC * (int)sizeof(uint4);
 static_assert(NT_FIN_MAX == RESCAN_THREADS, "the stop row's rescan uses the whole finalising CTA");
 
 
@@ -615,7 +619,7 @@ __device__ void decide_request(const Params &P, FinSmem &F, int lane)
 }
 
 template <typename T, bool SAMPLE, bool VAR>
-__device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stage)
+__device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stage, uint4 *pstage)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwf = blockDim.x >> 5;
     const int rpr = P.rpr;
@@ -627,6 +631,16 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
         RowState rs;
         finish_row<T, SAMPLE, VAR>(P, b, n, F, lane, rs);
         if (SAMPLE && !rs.bad && F.need_draw[n]) row_draw_prep<VAR>(P, b, n, F, lane, rs);
+        if (SAMPLE && n < PF_ROWS) {
+            // Copy the row's crossing range now, in case the decide stops here: the copy
+            // overlaps the decide instead of following it.
+            __syncwarp();  // rs_ok / rs_c0 / rs_c1 were written by one lane
+            if (F.rs_ok[n]) {
+                const int64_t r = (int64_t)b * rpr + n;
+                stage_range<T>(reinterpret_cast<const T *>(P.logits) + r * P.V, r * P.V, P.total, P.mis,
+                               F.rs_c0[n], F.rs_c1[n], pstage + n * RESCAN_STAGE_VEC, lane, 32);
+            }
+        }
     }
     __syncthreads();
     if (warp == 0 && !(P.block && P.q)) decide_request<SAMPLE, VAR>(P, F, lane);
@@ -690,10 +704,12 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
     } else if (mode == 1) {
         int drawn = F.cand[stop];
         if (F.rs_ok[stop]) {
-            // The stop row's crossing record range: copy it to shared memory, then rescan it.
+            // The stop row's crossing record range, in shared memory (copied after its locate for
+            // the first PF_ROWS rows, else now), then rescanned.
             const int64_t r = (int64_t)b * rpr + stop;
-            stage_range<T>(reinterpret_cast<const T *>(P.logits) + r * P.V, r * P.V, P.total, P.mis,
-                           F.rs_c0[stop], F.rs_c1[stop], stage, tid, blockDim.x);
+            if (stop < PF_ROWS) stage = pstage + stop * RESCAN_STAGE_VEC;
+            else stage_range<T>(reinterpret_cast<const T *>(P.logits) + r * P.V, r * P.V, P.total, P.mis,
+                                F.rs_c0[stop], F.rs_c1[stop], stage, tid, blockDim.x);
             cp_async_wait_all();
             __syncthreads();
             drawn = rescan_staged<T, VAR>(r * P.V, P.mis, F.rs_c0[stop], F.rs_c1[stop], VAR ? F.cs : P.cs,
@@ -817,10 +833,12 @@ template <typename T, bool SAMPLE, bool VAR>
 __global__ void __launch_bounds__(NT_FIN_MAX) sv_finalize_kernel(const Params P)
 {
     __shared__ FinSmem F;
-    __shared__ uint4 stage[SAMPLE ? RESCAN_STAGE_VEC : 1];  // the stop row's rescan range
+    __shared__ uint4 stage[SAMPLE ? RESCAN_STAGE_VEC : 1];  // the stop row's rescan range (rows >= PF_ROWS)
+    extern __shared__ uint4 pstage[];  // sampling: PF_ROWS slots of RESCAN_STAGE_VEC vectors
     const int b = (int)blockIdx.x;
-    if (VAR && P.temps && __ldg(P.temps + b) == 0.f) finalize_request<T, false, false>(P, b, F, stage);
-    else finalize_request<T, SAMPLE, VAR>(P, b, F, stage);
+    if (VAR && P.temps && __ldg(P.temps + b) == 0.f) finalize_request<T, false, false>(P, b, F, stage, pstage);
+    else finalize_request<T, SAMPLE, VAR>(P, b, F, stage, pstage);
+    cp_async_wait_all();  // copies of rows that did not stop the round land before the CTA exits
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1241,6 +1259,7 @@ static Layout layout(int B, int rpr, int64_t V, bool block = false)
 
 struct DevInfo {
     int sms = 0;
+    bool fin_smem = false;  // the sampling finalisers may take PF_SMEM_BYTES of dynamic shared memory
 };
 
 static std::mutex g_dev_mu;
@@ -1257,6 +1276,23 @@ static const DevInfo *device_info()
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
         cudaGetLastError();
         d.sms = sms;
+    }
+    if (!d.fin_smem) {
+        // Above the 48 KB default, so each sampling finaliser is allowed it once per device.
+        const bool ok =
+            cudaFuncSetAttribute(sv_finalize_kernel<__nv_bfloat16, true, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES) == cudaSuccess &&
+            cudaFuncSetAttribute(sv_finalize_kernel<__nv_bfloat16, true, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES) == cudaSuccess &&
+            cudaFuncSetAttribute(sv_finalize_kernel<float, true, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES) == cudaSuccess &&
+            cudaFuncSetAttribute(sv_finalize_kernel<float, true, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES) == cudaSuccess;
+        if (!ok) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        d.fin_smem = true;
     }
     return &d;
 }
@@ -1317,7 +1353,7 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)P.B);
     cfg.blockDim = dim3(NT_FIN_MAX);  // one warp per row (rows beyond 8 loop); the rescan wants all 8
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = SAMPLE ? PF_SMEM_BYTES : 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -138,7 +138,9 @@ __device__ void draw_span(const Src &src, int64_t ngroups, float t, DrawSmem &D)
         __syncthreads();
         const float incl = cum + (D.wpre[warp] + incl_w);
         const float excl = cum + (D.wpre[warp] + excl_w);
-        if (incl > t) atomicMin(&D.first_thread, tid);
+        // The warp's first crossing lane, then one shared-memory atomic per warp.
+        const unsigned cross = __ballot_sync(0xffffffffu, incl > t);
+        if (lane == 0 && cross) atomicMin(&D.first_thread, warp * 32 + __ffs(cross) - 1);
         __syncthreads();
         if (tid == D.first_thread) {
             const int64_t gi = gbase + (int64_t)kstar * NT + tid;

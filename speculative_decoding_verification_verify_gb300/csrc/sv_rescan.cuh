@@ -104,7 +104,7 @@ __device__ __forceinline__ void stage_range(const T *row, int64_t rowflat, int64
 // Thread t weighs whole vectors t + i * nt (conflict-free shared reads); per-round warp scans and
 // one table of (round, warp) totals give every vector its running mass; the first crossing vector
 // (or the last positive one) comes from shared-memory atomics, and its owner walks its VEC
-// elements.  Three barriers.
+// elements.  Three barriers, and one shared-memory atomic per warp.
 template <typename T, bool FILT>
 __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs, float mc, float thr, float t,
                              float cum0, const int *ex, int ex_n, const uint4 *stage, RescanSmem &S)
@@ -162,8 +162,12 @@ __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs,
             klast = k;
         }
     }
-    if (kmin != INT_MAX) atomicMin(&S.kmin, kmin);
-    if (klast >= 0) atomicMax(&S.klast, klast);
+    // Reduce within the warp first: one shared-memory atomic per warp, not one per thread (every
+    // thread past the crossing holds a candidate, and the same-address atomics serialise).
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    klast = __reduce_max_sync(0xffffffffu, klast);
+    if (lane == 0 && kmin != INT_MAX) atomicMin(&S.kmin, kmin);
+    if (lane == 0 && klast >= 0) atomicMax(&S.klast, klast);
     __syncthreads();
     const bool last_mode = S.kmin == INT_MAX;
     const int kv = last_mode ? S.klast : S.kmin;
