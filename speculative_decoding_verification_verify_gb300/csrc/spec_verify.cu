@@ -841,6 +841,77 @@ __global__ void __launch_bounds__(NT_FIN_MAX) sv_finalize_kernel(const Params P)
     cp_async_wait_all();  // copies of rows that did not stop the round land before the CTA exits
 }
 
+// 8 consecutive logits (one 16-byte vector of bf16, two of fp32) or q values, as floats; the
+// address must be 16-byte aligned.
+template <typename T>
+__device__ __forceinline__ void load8(const T *p, float (&x)[8])
+{
+    if (sizeof(T) == 2) {
+        float y[8];
+        Elt<__nv_bfloat16>::unpack(ldg_stream(p), y);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = y[j];
+    } else {
+        const uint4 a = ldg_stream(p), c = ldg_stream(p + 4);
+        x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+        x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+        x[4] = __uint_as_float(c.x); x[5] = __uint_as_float(c.y);
+        x[6] = __uint_as_float(c.z); x[7] = __uint_as_float(c.w);
+    }
+}
+
+// One warp's residual sums over the columns [w0, w1) of a logit row: zr += max(0, w p - q) and
+// zp += p, with p = 2^(l cs - mc) * inv (0 for logits below thr when FILT) and q = 0 without a
+// q row.  lflat / qflat are the row's first element in the flat logits / q arrays, whose bases
+// are lmis / qmis elements past a 16-byte boundary.  Groups of 8 columns whose logits and q both
+// start on a 16-byte boundary are read with 16-byte loads, two groups per lane in flight; the
+// columns before the first group and after the last (fewer than 8 each), or the whole span
+// when the logits and the q row cannot be aligned at the same column, are read one by one.
+template <typename T, bool FILT>
+__device__ __forceinline__ void resid_sums(const T *row, const float *qrow, int64_t lflat, int64_t qflat,
+                                           int lmis, int qmis, int64_t w0, int64_t w1, float cs, float mc,
+                                           float inv, float w, float thr, int lane, float &zr, float &zp)
+{
+    constexpr int VEC = Elt<T>::VEC;
+    auto add = [&](float l, float q) {
+        const float p = (!FILT || l >= thr) ? ex2(fmaf(l, cs, -mc)) * inv : 0.f;
+        zp += p;
+        zr += fmaxf(0.f, w * p - q);
+    };
+    // Logits start a vector at the columns congruent to h (mod VEC); q (4 floats to a vector) at
+    // those congruent to h mod 4 either everywhere or nowhere, as VEC is 4 or 8.
+    int64_t h = w0 + (VEC - (int)((lmis + lflat + w0) % VEC)) % VEC;
+    const bool vec_ok = qmis >= 0 && (!qrow || (qmis + qflat + h) % 4 == 0);
+    if (!vec_ok || h > w1) h = w1;
+    const int64_t ng = (w1 - h) / 8, t0 = h + ng * 8;
+    for (int64_t c = w0 + lane; c < h; c += 32) add(Elt<T>::load(row, c), qrow ? __ldg(qrow + c) : 0.f);
+    for (int64_t g = lane; g < ng; g += 64) {
+        const bool two = g + 32 < ng;
+        float l0[8], q0[8], l1[8], q1[8];
+        const int64_t c0 = h + g * 8, c1 = c0 + 32 * 8;
+        load8<T>(row + c0, l0);
+        if (qrow) load8<float>(qrow + c0, q0);
+        if (two) {
+            load8<T>(row + c1, l1);
+            if (qrow) load8<float>(qrow + c1, q1);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) add(l0[j], qrow ? q0[j] : 0.f);
+        if (two) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) add(l1[j], qrow ? q1[j] : 0.f);
+        }
+    }
+    for (int64_t c = t0 + lane; c < w1; c += 32) add(Elt<T>::load(row, c), qrow ? __ldg(qrow + c) : 0.f);
+}
+
+// Elements the q array's base lies past a 16-byte boundary, or -1 when it is not 4-byte aligned.
+__device__ __forceinline__ int q_mis(const float *q)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(q);
+    return (a & 3) ? -1 : (int)((a & 15) >> 2);
+}
+
 // ---------------------------------------------------------------------------------------------
 // Residual kernel (standard rejection): draw from max(0, p - q) at the rejected row.
 // Grid (C2, B).  Each warp sums the residual r = max(0, p - q) and p over its part of the
@@ -905,22 +976,8 @@ __global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
     const int64_t span = (cc1 - cc0 + NW - 1) / NW;
     const int64_t w0 = min(cc0 + warp * span, cc1), w1 = min(w0 + span, cc1);
     float zr = 0.f, zp = 0.f;
-    for (int64_t base = w0; base < w1; base += 32 * 8) {
-        float l[8], q[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int64_t col = base + lane + 32 * u;
-            const bool in = col < w1;
-            l[u] = in ? Elt<T>::load(row, col) : NEG_INF;
-            q[u] = in ? __ldg(qrow + col) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const float p = l[u] >= thr ? ex2(fmaf(l[u], cs, -mc)) * inv : 0.f;
-            zp += p;
-            zr += fmaxf(0.f, p - q[u]);
-        }
-    }
+    resid_sums<T, true>(reinterpret_cast<const T *>(row), qrow, r * V, ((int64_t)b * P.k + j) * V, P.mis,
+                        q_mis(P.q), w0, w1, cs, mc, inv, 1.f, thr, lane, zr, zp);
     zr = warp_sum(zr);
     zp = warp_sum(zp);
     if (lane == 0) P.recs2[((int64_t)b * P.C2 + c) * NW + warp] = make_float2(zr, zp);
@@ -1046,22 +1103,8 @@ __global__ void __launch_bounds__(NT) sv_block_kernel(const Params P)
         const int64_t span = (cc1 - cc0 + NW - 1) / NW;
         const int64_t w0 = min(cc0 + warp * span, cc1), w1 = min(w0 + span, cc1);
         float zr = 0.f, zp = 0.f;
-        for (int64_t base = w0; base < w1; base += 32 * 8) {
-            float l[8], q[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int64_t col = base + lane + 32 * u;
-                const bool in = col < w1;
-                l[u] = in ? Elt<T>::load(row, col) : NEG_INF;
-                q[u] = (in && qrow) ? __ldg(qrow + col) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float p = ex2(fmaf(l[u], P.cs, -mc)) * inv;
-                zp += p;
-                zr += fmaxf(0.f, w * p - q[u]);
-            }
-        }
+        resid_sums<T, false>(reinterpret_cast<const T *>(row), qrow, r * V, ((int64_t)b * P.k + L) * V, P.mis,
+                             q_mis(P.q), w0, w1, P.cs, mc, inv, w, NEG_INF, lane, zr, zp);
         zr = warp_sum(zr);
         zp = warp_sum(zp);
         if (lane == 0) P.recs3[(r * P.C2 + c) * NW + warp] = make_float2(zr, zp);
