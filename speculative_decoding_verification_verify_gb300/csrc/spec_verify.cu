@@ -955,7 +955,7 @@ struct ResidSrc {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(NT) sv_residual_kernel(const Params P)
+__global__ void __launch_bounds__(NT, 4) sv_residual_kernel(const Params P)
 {
     __shared__ ResidSmem F;
     __shared__ int is_last;
@@ -1079,7 +1079,7 @@ struct BlockSmem {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(NT) sv_block_kernel(const Params P)
+__global__ void __launch_bounds__(NT, 4) sv_block_kernel(const Params P)
 {
     __shared__ BlockSmem S;
     __shared__ int is_last;
@@ -1406,10 +1406,11 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
     const bool filt = SAMPLE && (P.top_k || P.top_p);
     const bool var = filt || P.temps || P.thr_single != 1.f || P.thr_acc != 1.f;
     if (filt) {  // each row's top-k / top-p threshold, before the rows are streamed
-        // Rows in flight: two CTAs per SM hold about 2 * 152 rows (78 MB of bf16 rows of 128256).
+        // Rows in flight: TK_CTAS CTAs per SM, one row each (two per SM hold 304 rows, 78 MB of
+        // bf16 rows of 128256, which L2 keeps for the row's later passes).
         const int64_t rows = (int64_t)P.B * P.rpr;
         const DevInfo *d = device_info();
-        const int64_t cap = 2 * (int64_t)(d ? d->sms : 152);
+        const int64_t cap = TK_CTAS * (int64_t)(d ? d->sms : 152);
         const unsigned grid = (unsigned)(rows < cap ? rows : cap);
         if (dtype == SPEC_VERIFY_BF16) sv_topkp_kernel<__nv_bfloat16><<<grid, NT_TK, 0, s>>>(P);
         else sv_topkp_kernel<float><<<grid, NT_TK, 0, s>>>(P);

@@ -21,6 +21,14 @@ namespace sv {
 constexpr int NT_TK = 512;
 constexpr int TK_BINS = 256;        // 8-bit digits
 constexpr int TK_WARPS = NT_TK / 32;
+#ifndef SV_TK_UNROLL
+#define SV_TK_UNROLL 2
+#endif
+#ifndef SV_TK_CTAS
+#define SV_TK_CTAS 2
+#endif
+constexpr int TK_UNROLL = SV_TK_UNROLL;  // 16-byte loads a thread keeps in flight in a pass
+constexpr int TK_CTAS = SV_TK_CTAS;      // threshold CTAs per SM (each holds one row at a time)
 
 template <typename T>
 struct KeyOf;
@@ -149,35 +157,61 @@ __device__ __forceinline__ void walk_bins(TopkpSmem &S, int nb, bool by_mass, in
     }
 }
 
-// Visit every key of a row (row = column 0, rowflat its flat index, mis the logits base's
+// Visit the keys of a row (row = column 0, rowflat its flat index, mis the logits base's
 // misalignment in elements): the 16-byte aligned body with vector loads, the head and tail
-// element by element.  f(key) is called once per element.
-template <typename T, typename F>
-__device__ __forceinline__ void for_each_key(const void *row, int64_t rowflat, int64_t V, int mis, F f)
+// element by element.  f(key) is called once per visited element.  With MAX, vmx takes the
+// largest logit of every element (NaN if one is NaN).  With SKIP, a vector whose largest logit is
+// below fl (a value, not NaN) is not visited: none of its keys can reach the key of fl.
+template <typename T, bool MAX, bool SKIP, typename F>
+__device__ __forceinline__ void for_each_key(const void *row, int64_t rowflat, int64_t V, int mis, float fl,
+                                             float &vmx, F f)
 {
     constexpr int VEC = KeyOf<T>::VEC;
     const int64_t a0 = min((int64_t)((VEC - (rowflat + mis) % VEC) % VEC), V);
     const int64_t nv = (V - a0) / VEC;
     const int64_t a1 = a0 + nv * VEC;
-    for (int64_t c = threadIdx.x; c < a0; c += NT_TK) f(KeyOf<T>::key(row, c));
-    for (int64_t c = a1 + threadIdx.x; c < V; c += NT_TK) f(KeyOf<T>::key(row, c));
+    auto one = [&](int64_t c) {
+        const uint32_t k = KeyOf<T>::key(row, c);
+        if (MAX) vmx = fmax_nan(vmx, KeyOf<T>::value(k));
+        f(k);
+    };
+    for (int64_t c = threadIdx.x; c < a0; c += NT_TK) one(c);
+    for (int64_t c = a1 + threadIdx.x; c < V; c += NT_TK) one(c);
+    // TK_UNROLL vectors per thread in flight: a pass is bound by the loads' latency otherwise.
     const uint4 *vp = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(row) + a0);
-    for (int64_t i = threadIdx.x; i < nv; i += NT_TK) {
-        uint32_t k[VEC];
-        KeyOf<T>::keys(ldg_stream(vp + i), k);
+    for (int64_t i0 = threadIdx.x; i0 < nv; i0 += (int64_t)TK_UNROLL * NT_TK) {
+        uint4 w[TK_UNROLL];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) f(k[e]);
+        for (int u = 0; u < TK_UNROLL; ++u) {
+            const int64_t i = i0 + (int64_t)u * NT_TK;
+            if (i < nv) w[u] = ldg_stream(vp + i);
+        }
+#pragma unroll
+        for (int u = 0; u < TK_UNROLL; ++u) {
+            if (i0 + (int64_t)u * NT_TK >= nv) break;
+            if (MAX || SKIP) {
+                const float m = Elt<T>::vmax(w[u]);
+                if (MAX) vmx = fmax_nan(vmx, m);
+                if (SKIP && !(m >= fl)) continue;
+            }
+            uint32_t k[VEC];
+            KeyOf<T>::keys(w[u], k);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) f(k[e]);
+        }
     }
 }
 
 // Histogram of the next digit of the keys that match `prefix` on the bits above this level's
 // digit and are >= floor_key: counts (MASS false) or masses 2^((l - mx) * cs) (MASS true).  Each
 // warp fills its own copy; a thread adds a run of equal digits at once (logits cluster in a few
-// high digits), and the copies are merged at the end.
+// high digits), and the copies are merged at the end.  Every counted key is at least
+// max(prefix, floor_key) (prefix has zeros below this level's digit), so vectors whose largest
+// logit lies below that key's value are skipped whole.  MAX (first level only): *mx_out = the
+// row's largest logit as seen by this thread, NaN if it saw a NaN.
 template <typename T, bool MASS, bool MAX = false>
 __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int mis, uint32_t prefix, int lvl,
-                              uint32_t floor_key, float mx, float cs, TopkpSmem &S, uint32_t *kmax_out = nullptr,
-                              bool *nan_out = nullptr)
+                              uint32_t floor_key, float mx, float cs, TopkpSmem &S, float *mx_out = nullptr)
 {
     const int sh = KeyOf<T>::shift(lvl);
     const int top = sh + 8;
@@ -189,15 +223,13 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
     __syncthreads();
     int run_d = -1, run_c = 0;
     float run_m = 0.f;
-    // Start from the key of -inf: a thread with no element must not report key 0, which is the
-    // key of a NaN bit pattern.
-    uint32_t kmax = KeyOf<T>::key_of_bits(sizeof(T) == 2 ? 0xff80u : 0xff800000u);
-    bool nan = false;
-    for_each_key<T>(row, rowflat, V, mis, [&](uint32_t k) {
-        if (MAX) {
-            kmax = k > kmax ? k : kmax;
-            nan |= KeyOf<T>::value(k) != KeyOf<T>::value(k);
-        }
+    // The skip bound: the value of the smallest key that can be counted, when it lies above the
+    // key of -inf (a NaN-free row's keys lie between those of -inf and +inf).
+    const uint32_t fk = prefix > floor_key ? prefix : floor_key;
+    const float fl = KeyOf<T>::value(fk);
+    const bool skip = fk > KeyOf<T>::key_of_bits(sizeof(T) == 2 ? 0xff80u : 0xff800000u) && fl == fl;
+    float vmx = NEG_INF;
+    auto visit = [&](uint32_t k) {
         if ((top >= 32 || (k >> top) == (prefix >> top)) && k >= floor_key) {
             const int d = (int)((k >> sh) & 0xffu);
             if (d != run_d) {
@@ -212,15 +244,14 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
             if (MASS) run_m += ex2((KeyOf<T>::value(k) - mx) * cs);
             else ++run_c;
         }
-    });
+    };
+    if (!MAX && skip) for_each_key<T, false, true>(row, rowflat, V, mis, fl, vmx, visit);
+    else for_each_key<T, MAX, false>(row, rowflat, V, mis, fl, vmx, visit);
     if (run_d >= 0) {
         if (MASS) atomicAdd(&S.wmass[warp][run_d], run_m);
         else atomicAdd(&S.wcnt[warp][run_d], run_c);
     }
-    if (MAX) {
-        *kmax_out = kmax;
-        *nan_out = nan;
-    }
+    if (MAX) *mx_out = vmx;
     __syncthreads();
     for (int i = threadIdx.x; i < TK_BINS; i += NT_TK) {
         int c = 0;
@@ -257,10 +288,8 @@ __device__ void topkp_row(const Params &P, int64_t r, TopkpSmem &S)
     constexpr int LV = KeyOf<T>::LEVELS;
     // First pass: the row's largest logit (the masses' reference; NaN if the row holds one) and
     // the top digit's counts, which top-k needs first.
-    uint32_t kmax;
-    bool nan;
-    key_histogram<T, false, true>(row, rowflat, V, P.mis, 0u, 0, 0u, 0.f, cs, S, &kmax, &nan);
-    float mx = nan ? __int_as_float(0x7fc00000) : KeyOf<T>::value(kmax);
+    float mx;
+    key_histogram<T, false, true>(row, rowflat, V, P.mis, 0u, 0, 0u, 0.f, cs, S, &mx);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) S.wmax[warp] = mx;
@@ -322,7 +351,7 @@ __device__ void topkp_row(const Params &P, int64_t r, TopkpSmem &S)
 // A few CTAs per SM, each taking rows in turn, so that the rows being filtered at any time fit in
 // L2 and a row's later passes are served from it.
 template <typename T>
-__global__ void __launch_bounds__(NT_TK) sv_topkp_kernel(const Params P)
+__global__ void __launch_bounds__(NT_TK, TK_CTAS) sv_topkp_kernel(const Params P)
 {
     __shared__ TopkpSmem S;
     const int64_t R = (int64_t)P.B * P.rpr;
