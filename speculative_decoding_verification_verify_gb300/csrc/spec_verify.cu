@@ -759,7 +759,7 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
 // KIND: 0 greedy, 1 sampling, 2 a temperature per request (greedy or sampling per chunk),
 // 3 as 2 with each row's top-k / top-p threshold applied in the sampling fold.
 template <typename T, int KIND>
-__global__ void __launch_bounds__(NT_S, 1) sv_stream_kernel(const Params P)
+__global__ void __launch_bounds__(stream_threads(KIND), 1) sv_stream_kernel(const Params P)
 {
     constexpr bool SAMPLE = KIND != 0;
     __shared__ unsigned next_chunk;
@@ -1417,8 +1417,8 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
     }
     if (dtype == SPEC_VERIFY_BF16) {
-        if (filt) sv_stream_kernel<__nv_bfloat16, 3><<<P.G, NT_S, 0, s>>>(P);
-        else if (P.temps) sv_stream_kernel<__nv_bfloat16, 2><<<P.G, NT_S, 0, s>>>(P);
+        if (filt) sv_stream_kernel<__nv_bfloat16, 3><<<P.G, stream_threads(3), 0, s>>>(P);
+        else if (P.temps) sv_stream_kernel<__nv_bfloat16, 2><<<P.G, stream_threads(2), 0, s>>>(P);
         else sv_stream_kernel<__nv_bfloat16, SAMPLE ? 1 : 0><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
         if (cudaLaunchKernelEx(&cfg, SAMPLE && var ? sv_finalize_kernel<__nv_bfloat16, SAMPLE, true>
@@ -1426,8 +1426,8 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
                                P) != cudaSuccess)
             return SPEC_VERIFY_ECUDA;
     } else {
-        if (filt) sv_stream_kernel<float, 3><<<P.G, NT_S, 0, s>>>(P);
-        else if (P.temps) sv_stream_kernel<float, 2><<<P.G, NT_S, 0, s>>>(P);
+        if (filt) sv_stream_kernel<float, 3><<<P.G, stream_threads(3), 0, s>>>(P);
+        else if (P.temps) sv_stream_kernel<float, 2><<<P.G, stream_threads(2), 0, s>>>(P);
         else sv_stream_kernel<float, SAMPLE ? 1 : 0><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
         if (cudaLaunchKernelEx(&cfg, SAMPLE && var ? sv_finalize_kernel<float, SAMPLE, true>

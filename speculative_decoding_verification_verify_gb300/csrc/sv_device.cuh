@@ -12,6 +12,13 @@ namespace sv {
 constexpr int NT = 256;       // threads per CTA of the finalising, residual and block kernels
 constexpr int NW = NT / 32;   // their warps
 constexpr int NT_S = 768;     // threads of a streaming CTA (one CTA per SM)
+#ifndef SV_NT_SV
+#define SV_NT_SV 512
+#endif
+// The variant streaming kernels (a temperature per request, top-k / top-p) hold both folds'
+// state: fewer warps per CTA leave each thread the registers to do so without spilling.
+constexpr int NT_SV = SV_NT_SV;
+__host__ __device__ constexpr int stream_threads(int kind) { return kind >= 2 ? NT_SV : NT_S; }
 constexpr int MAX_RPR = 64;   // rows per request: k + 1 <= 64 (chain) or N <= 64 (tree)
 constexpr int B_MAX = 65536;  // most requests per call (size of the fixed counter region)
 constexpr int C2_MAX = 1024;  // upper bound on column chunks of the residual kernel
