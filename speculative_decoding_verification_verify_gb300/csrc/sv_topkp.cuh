@@ -18,7 +18,10 @@
 
 namespace sv {
 
-constexpr int NT_TK = 512;
+#ifndef SV_NT_TK
+#define SV_NT_TK 512
+#endif
+constexpr int NT_TK = SV_NT_TK;
 constexpr int TK_BINS = 256;        // 8-bit digits
 constexpr int TK_WARPS = NT_TK / 32;
 #ifndef SV_TK_UNROLL
@@ -93,8 +96,10 @@ struct KeyOf<float> {
 struct TopkpSmem {
     int cnt[TK_BINS];
     float mass[TK_BINS];
-    int wcnt[TK_WARPS][TK_BINS];     // per-warp histograms, merged into cnt / mass
-    float wmass[TK_WARPS][TK_BINS];
+    union {                          // per-warp histograms of one pass, merged into cnt / mass
+        int wcnt[TK_WARPS][TK_BINS];
+        float wmass[TK_WARPS][TK_BINS];
+    };
     float wmax[NT_TK / 32];
     int sel;          // chosen digit
     int above_cnt;    // count in bins above it
@@ -204,8 +209,9 @@ __device__ __forceinline__ void for_each_key(const void *row, int64_t rowflat, i
 
 // Histogram of the next digit of the keys that match `prefix` on the bits above this level's
 // digit and are >= floor_key: counts (MASS false) or masses 2^((l - mx) * cs) (MASS true).  Each
-// warp fills its own copy; a thread adds a run of equal digits at once (logits cluster in a few
-// high digits), and the copies are merged at the end.  Every counted key is at least
+// warp adds every counted key to its own copy with a shared-memory atomic, and the copies are
+// merged at the end.  (Adding a thread's runs of equal digits at once was slower: consecutive
+// logits rarely share a digit, and the run test makes the warp diverge.)  Every counted key is at least
 // max(prefix, floor_key) (prefix has zeros below this level's digit), so vectors whose largest
 // logit lies below that key's value are skipped whole.  MAX (first level only): *mx_out = the
 // row's largest logit as seen by this thread, NaN if it saw a NaN.
@@ -216,13 +222,8 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
     const int sh = KeyOf<T>::shift(lvl);
     const int top = sh + 8;
     const int warp = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < TK_WARPS * TK_BINS; i += NT_TK) {
-        (&S.wcnt[0][0])[i] = 0;
-        (&S.wmass[0][0])[i] = 0.f;
-    }
+    for (int i = threadIdx.x; i < TK_WARPS * TK_BINS; i += NT_TK) (&S.wcnt[0][0])[i] = 0;
     __syncthreads();
-    int run_d = -1, run_c = 0;
-    float run_m = 0.f;
     // The skip bound: the value of the smallest key that can be counted, when it lies above the
     // key of -inf (a NaN-free row's keys lie between those of -inf and +inf).
     const uint32_t fk = prefix > floor_key ? prefix : floor_key;
@@ -232,34 +233,21 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
     auto visit = [&](uint32_t k) {
         if ((top >= 32 || (k >> top) == (prefix >> top)) && k >= floor_key) {
             const int d = (int)((k >> sh) & 0xffu);
-            if (d != run_d) {
-                if (run_d >= 0) {
-                    if (MASS) atomicAdd(&S.wmass[warp][run_d], run_m);
-                    else atomicAdd(&S.wcnt[warp][run_d], run_c);
-                }
-                run_d = d;
-                run_c = 0;
-                run_m = 0.f;
-            }
-            if (MASS) run_m += ex2((KeyOf<T>::value(k) - mx) * cs);
-            else ++run_c;
+            if (MASS) atomicAdd(&S.wmass[warp][d], ex2((KeyOf<T>::value(k) - mx) * cs));
+            else atomicAdd(&S.wcnt[warp][d], 1);
         }
     };
     if (!MAX && skip) for_each_key<T, false, true>(row, rowflat, V, mis, fl, vmx, visit);
     else for_each_key<T, MAX, false>(row, rowflat, V, mis, fl, vmx, visit);
-    if (run_d >= 0) {
-        if (MASS) atomicAdd(&S.wmass[warp][run_d], run_m);
-        else atomicAdd(&S.wcnt[warp][run_d], run_c);
-    }
     if (MAX) *mx_out = vmx;
     __syncthreads();
     for (int i = threadIdx.x; i < TK_BINS; i += NT_TK) {
         int c = 0;
         float m = 0.f;
-        for (int w = 0; w < TK_WARPS; ++w) {
-            c += S.wcnt[w][i];
-            m += S.wmass[w][i];
-        }
+        if (MASS)
+            for (int w = 0; w < TK_WARPS; ++w) m += S.wmass[w][i];
+        else
+            for (int w = 0; w < TK_WARPS; ++w) c += S.wcnt[w][i];
         S.cnt[i] = c;
         S.mass[i] = m;
     }
