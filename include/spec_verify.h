@@ -19,6 +19,9 @@
  *     (16-byte aligned rows take the vectorised path everywhere).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue
  *     work on it; none synchronises the host, and none allocates memory.
+ *   - The first call on a device (of any entry point, with that device current) reads its SM
+ *     count and allows the sampling finalisers their 66 KB of dynamic shared memory
+ *     (cudaFuncSetAttribute); make it before any stream capture on that device.
  *   - The return value is a host status, known when the call returns:
  *       SPEC_VERIFY_OK, SPEC_VERIFY_EINVAL (bad argument), SPEC_VERIFY_EWORKSPACE
  *       (workspace too small or misaligned), SPEC_VERIFY_ECUDA (a launch failed).
