@@ -40,7 +40,8 @@ GRAPH_CALLS = 30  # verify calls captured in one CUDA graph for the timed region
 KV_SETS = 8       # KV-compaction index sets rotated over one pool
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_verify_gb300", "csrc", f)
-                  for f in ("spec_verify.cu", "sv_device.cuh", "sv_draw.cuh", "sv_stream.cuh", "sv_rescan.cuh")]
+                  for f in ("spec_verify.cu", "sv_device.cuh", "sv_draw.cuh", "sv_stream.cuh", "sv_rescan.cuh",
+                          "sv_decide.cuh")]
 
 
 def kernel_source_hash() -> str:

@@ -20,8 +20,10 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue
  *     work on it; none synchronises the host, and none allocates memory.
  *   - The first call on a device (of any entry point, with that device current) reads its SM
- *     count and allows the sampling finalisers their 66 KB of dynamic shared memory
- *     (cudaFuncSetAttribute); make it before any stream capture on that device.
+ *     count and raises the dynamic shared-memory limits of the kernels that need more than the
+ *     default (cudaFuncSetAttribute: 193 KB for the verify kernel, 66 KB for the variants'
+ *     finaliser); make it before any stream capture on that device.  The library keeps this per
+ *     device for the life of the process, so it must not be used again after cudaDeviceReset.
  *   - The return value is a host status, known when the call returns:
  *       SPEC_VERIFY_OK, SPEC_VERIFY_EINVAL (bad argument), SPEC_VERIFY_EWORKSPACE
  *       (workspace too small or misaligned), SPEC_VERIFY_ECUDA (a launch failed).
@@ -45,7 +47,8 @@
  *   - Draws use the inverse CDF in ascending token order: the smallest y whose running sum
  *     of the (unnormalised) weights exceeds v * Z.
  *   - Limits: 1 <= B <= 65536, 0 <= k <= 63 (chain), 1 <= N <= 64 (tree), 1 <= V < 2^31,
- *     and |logit| / T must stay below 2^127 (the scaled logit is formed in fp32).
+ *     B * rows * ceil((V + 7) / 4096) < 2^31 (bf16; fp32: 2048 in place of 4096), and
+ *     |logit| / T must stay below 2^127 (the scaled logit is formed in fp32).
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -242,7 +245,8 @@ int spec_verify_tree_ex(const void *logits, int dtype, const int32_t *node_token
  * they sum to *budget), *budget, and *best_rate (or NULL).  cost must be positive.
  * B * K <= 16384, K <= 64.  workspace: device memory, 8-byte aligned, of
  * spec_verify_plan_budget_workspace_bytes(B, K) bytes (0 for unsupported sizes), caller-owned,
- * no initialisation needed.  Three launches, asynchronous on `stream`.  SPEC_VERIFY_EINVAL for
+ * no initialisation needed.  Four launches, asynchronous on `stream`: the survival keys, their
+ * ranks, the scatter into rank order, and the picking CTA.  SPEC_VERIFY_EINVAL for
  * bad pointers, alignment or sizes; SPEC_VERIFY_EWORKSPACE for a short or misaligned workspace.
  */
 #define SPEC_VERIFY_BUDGET_MAX_SLOTS 16384

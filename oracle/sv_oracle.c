@@ -33,7 +33,7 @@
  *     h_L = r_L / (r_L + 1 - w_L) (h = 1 when that denominator is 0), h_k = w_k for the last
  *     draft; the accepted length is the largest L with a passing test.
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent:
  *   - Uniforms: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
  *     1, 2, 3", SC'11), counter = (slot, request, offset_lo, offset_hi), key = (seed_lo,
  *     seed_hi). Word 0 -> u (accept test / tree coin), word 1 -> v (the draw at the stop slot).

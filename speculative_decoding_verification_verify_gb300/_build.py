@@ -10,7 +10,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libspecverify.so")
 SOURCES = [os.path.join(CSRC, f) for f in ("spec_verify.cu", "sv_kv.cu", "sv_budget.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("sv_device.cuh", "sv_draw.cuh", "sv_stream.cuh", "sv_rescan.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("sv_device.cuh", "sv_draw.cuh", "sv_stream.cuh", "sv_rescan.cuh", "sv_decide.cuh", "sv_topkp.cuh")] + [
     os.path.join(INCLUDE, "spec_verify.h")]
 
 NVCC_FLAGS = [

@@ -34,6 +34,7 @@
 #include "spec_verify.h"
 #include "sv_device.cuh"
 #include "sv_draw.cuh"
+#include "sv_decide.cuh"
 #include "sv_stream.cuh"
 #include "sv_rescan.cuh"
 #include "sv_topkp.cuh"
@@ -41,10 +42,6 @@
 namespace sv {
 
 constexpr int NT_FIN_MAX = 256;  // threads of a finalising CTA: one warp per row, up to 8 rows
-// Rows whose crossing range is copied to shared memory as soon as it is located, before the
-// decide names the stop row (one 8 KB slot per warp's first row).
-constexpr int PF_ROWS = NT_FIN_MAX / 32;
-constexpr int PF_SMEM_BYTES = PF_ROWS * RESCAN_STAGE_VEC * (int)sizeof(uint4);
 static_assert(NT_FIN_MAX == RESCAN_THREADS, "the stop row's rescan uses the whole finalising CTA");
 
 
@@ -58,7 +55,6 @@ struct FinSmem {
     float qx[MAX_RPR], u[MAX_RPR], v[MAX_RPR];
     long long row_base[MAX_RPR];                  // first record index of each row
     int row_L[MAX_RPR];                           // records of each row
-    int need_draw[MAX_RPR];                       // the row's speculative draw may be emitted
     // ---- from the records
     float row_mc[MAX_RPR], row_S[MAX_RPR];        // non-child mass S * 2^row_mc
     float row_M[MAX_RPR], row_tot[MAX_RPR];       // reference covering the children too; total in it
@@ -92,36 +88,6 @@ struct ResidSmem {
     DrawSmem D;
 };
 
-// ---------------------------------------------------------------------------------------------
-// The streaming warp's view of a request's nodes: lane i holds nodes i and i + 32 (token and
-// parent; the chain is a path tree), and Kids marks the children of row n's node with a usable
-// token.
-// ---------------------------------------------------------------------------------------------
-struct NodeView {
-    int tok[2], par[2];
-};
-
-__device__ __forceinline__ void load_nodes(const Params &P, int b, int lane, NodeView &nv)
-{
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int m = lane + 32 * h;
-        nv.tok[h] = -1;
-        nv.par[h] = -1;
-        if (m >= 1 && m < P.rpr) {
-            nv.tok[h] = node_token(P, b, m);
-            nv.par[h] = node_parent(P, b, m);
-        }
-    }
-}
-
-__device__ __forceinline__ void kids_of(const Params &P, const NodeView &nv, int n, Kids &kd)
-{
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-        kd.col[h] = (nv.par[h] == n && nv.tok[h] >= 0 && (int64_t)nv.tok[h] < P.V) ? nv.tok[h] : INT_MAX;
-}
-
 __device__ __forceinline__ void draw_init(DrawSmem &D, float cum)
 {
     if (threadIdx.x == 0) {
@@ -137,40 +103,6 @@ __device__ __forceinline__ void draw_init(DrawSmem &D, float cum)
 // children and draws the row's candidate token; then one warp decides.
 // ---------------------------------------------------------------------------------------------
 constexpr int REC_PER_LANE = 4;  // records a lane keeps in registers for the draw's locate step
-
-// Locate step over one chunk of 32 records with masses m (in the row's reference): finds the
-// first record where the running mass exceeds t, and tracks the last record with positive mass.
-struct Locate {
-    float cum = 0.f, before = 0.f, lp_before = 0.f;
-    int found = -1, lastpos = -1;
-};
-
-__device__ __forceinline__ bool locate_chunk(Locate &Lc, float m, int c0, float t, int lane)
-{
-    const float incl = warp_incl_scan(m, lane);
-    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0.f;
-    const unsigned hit = __ballot_sync(0xffffffffu, Lc.cum + incl > t);
-    const unsigned pos = __ballot_sync(0xffffffffu, m > 0.f);
-    if (pos) {
-        const int lp = 31 - __clz(pos);
-        Lc.lastpos = c0 + lp;
-        Lc.lp_before = Lc.cum + __shfl_sync(0xffffffffu, excl, lp);
-    }
-    if (hit) {
-        const int fl = __ffs(hit) - 1;
-        Lc.found = c0 + fl;
-        Lc.before = Lc.cum + __shfl_sync(0xffffffffu, excl, fl);
-        return true;
-    }
-    Lc.cum += __shfl_sync(0xffffffffu, incl, 31);
-    return false;
-}
-
-__device__ __forceinline__ float rec_mass(const float4 &r, float mc)
-{
-    return (r.y == 0.f) ? 0.f : r.y * ex2(r.x - mc);
-}
 
 // Stage the request's structure, uniforms and record ranges (inputs only).
 // VAR: the call has per-request temperatures or top-k / top-p thresholds (read from the staged
@@ -223,9 +155,6 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
                 F.ex_node[off] = n + 1;
             }
             F.dep[n] = n;
-            // With draft probabilities a rejected draft's row is left to the residual kernel, and
-            // block verification with draft probabilities draws in the block kernel.
-            F.need_draw[n] = SAMPLE && !(P.q && has) && !(P.block && P.q);
         }
         __syncthreads();
         return;
@@ -265,7 +194,6 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
             ++d;
         }
         F.dep[n] = d;
-        F.need_draw[n] = SAMPLE;
     }
     __syncthreads();
     for (int n = tid; n < rpr; n += nt) {
@@ -293,6 +221,8 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
 // What a warp keeps between merging a row's records and locating the draw's crossing in them.
 struct RowState {
     float4 rr[REC_PER_LANE];  // a lane's contiguous run of q records (when inreg)
+    float m[REC_PER_LANE];    // their masses in the reference mc (when inreg)
+    float own, incl;          // the lane's run mass, and the running mass through it (when inreg)
     int64_t base;             // first record index of the row
     int L, q, off, cnt;       // records, records per lane, the row's children (ex_off, ex_n)
     bool inreg, bad;
@@ -340,41 +270,73 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, 
     const int q = (L + 31) >> 5;
     rs.q = q;
     rs.inreg = q <= REC_PER_LANE;
-    float mc = REF_NONE, s = 0.f;
+    const float cs = VAR ? F.cs : P.cs;
+    float mc = REF_NONE, s = 0.f, M, esum;
+    float ec[2];
     if (rs.inreg) {
 #pragma unroll
         for (int i = 0; i < REC_PER_LANE; ++i) {
             const int t = lane * q + i;
             rs.rr[i] = (i < q && t < L) ? __ldcg(P.recs + base + t) : make_float4(REF_NONE, 0.f, 0.f, 0.f);
         }
-        // The lane's records against their largest reference, rescaled independently.
+        // The non-child reference mc (largest record reference) and the children's largest scaled
+        // logit, reduced side by side; M covers both, so a child far above every other token
+        // cannot overflow.
+        float cm = fmaxf(cap[0] * cs, cap[1] * cs);
 #pragma unroll
         for (int i = 0; i < REC_PER_LANE; ++i) mc = fmaxf(mc, rs.rr[i].x);
 #pragma unroll
-        for (int i = 0; i < REC_PER_LANE; ++i) s += (rs.rr[i].y == 0.f) ? 0.f : rs.rr[i].y * ex2(rs.rr[i].x - mc);
+        for (int o = 16; o > 0; o >>= 1) {
+            mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+        }
+        M = fmaxf(mc, cm);
+        // Each record's mass in the reference mc (kept for the draw's locate step), the children's
+        // weights in M; the two sums and the running sum over the lanes' runs, side by side.
+        float own = 0.f;
+#pragma unroll
+        for (int i = 0; i < REC_PER_LANE; ++i) {
+            rs.m[i] = (rs.rr[i].y == 0.f) ? 0.f : rs.rr[i].y * ex2(rs.rr[i].x - mc);
+            own += rs.m[i];
+        }
+        float le = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            ec[h] = (lane + 32 * h < cnt) ? ex2(fmaf(cap[h], cs, -M)) : 0.f;
+            le += ec[h];
+        }
+        float incl = own;
+        s = own;
+        esum = le;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+            esum += __shfl_xor_sync(0xffffffffu, esum, o);
+            if (lane >= o) incl += y;
+        }
+        rs.own = own;
+        rs.incl = incl;
     } else {
         for (int t = lane; t < L; t += 32) {
             const float4 rec = __ldcg(P.recs + base + t);
             rec_merge(mc, s, rec.x, rec.y);
         }
+        warp_rec_merge(mc, s);
+        M = mc;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) M = fmaxf(M, cap[h] * cs);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        esum = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            ec[h] = (lane + 32 * h < cnt) ? ex2(fmaf(cap[h], cs, -M)) : 0.f;
+            esum += ec[h];
+        }
+        esum = warp_sum(esum);
     }
-    warp_rec_merge(mc, s);
-    // The children: one reference M covers them and the rest, so a child far above every other
-    // token cannot overflow.
-    const float cs = VAR ? F.cs : P.cs;
-    float M = mc;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) M = fmaxf(M, cap[h] * cs);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float s_ref = (s == 0.f) ? 0.f : s * ex2(mc - M);
-    float ec[2], esum = 0.f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        ec[h] = (lane + 32 * h < cnt) ? ex2(fmaf(cap[h], cs, -M)) : 0.f;
-        esum += ec[h];
-    }
-    esum = warp_sum(esum);
     const float tot = s_ref + esum;
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -413,13 +375,8 @@ __device__ void row_draw_prep(const Params &P, int b, int n, FinSmem &F, int lan
         bool take_last = false;
         float4 frec = make_float4(0.f, 0.f, 0.f, 0.f);
         if (rs.inreg) {
-            float m[REC_PER_LANE], own = 0.f;
-#pragma unroll
-            for (int i = 0; i < REC_PER_LANE; ++i) {
-                m[i] = rec_mass(rs.rr[i], mc);
-                own += m[i];
-            }
-            const float incl = warp_incl_scan(own, lane);
+            const float own = rs.own, incl = rs.incl;
+            const float(&m)[REC_PER_LANE] = rs.m;
             float excl = __shfl_up_sync(0xffffffffu, incl, 1);
             if (lane == 0) excl = 0.f;
             const unsigned hit = __ballot_sync(0xffffffffu, excl + own > t);
@@ -492,134 +449,8 @@ __device__ void row_draw_prep(const Params &P, int b, int n, FinSmem &F, int lan
     }
 }
 
-// Decide the accepted path and the stop node (warp 0 calls it; the tree walk runs in lane 0).
-// VAR: the relaxed thresholds may differ from 1.
-template <bool SAMPLE, bool VAR>
-__device__ void decide_request(const Params &P, FinSmem &F, int lane)
-{
-    if (F.status == 0) {
-        if (SAMPLE && !P.is_tree && P.block && !P.q) {
-            // Block verification with one-hot drafts (Sun et al.; "The speculative decoding zoo",
-            // block branch of the rejection sampler): the prefix of L drafts has joint weight
-            // w_L = prod_{i<L} p_i(x_{i+1}); candidate length L passes iff u_{L-1} < h_L, where
-            // h_L = r_L / (r_L + 1 - w_L) with r_L = w_L * (the non-child share of row L) below
-            // the last present draft, and h = w there.  The largest passing L is accepted.
-            const int k = P.k;
-            int ke = k;  // drafts present: an absent draft ends the block
-            for (int c0 = 0; c0 < k; c0 += 32) {
-                const unsigned m = __ballot_sync(0xffffffffu, c0 + lane < k && F.tok[c0 + lane + 1] < 0);
-                if (m) {
-                    ke = c0 + __ffs(m) - 1;
-                    break;
-                }
-            }
-            float wcarry = 1.f;
-            int j = 0;
-            for (int c0 = 0; c0 < ke; c0 += 32) {
-                const int i = c0 + lane, L = i + 1;
-                float w = i < ke ? F.node_p[i + 1] : 1.f;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, w, off);
-                    if (lane >= off) w *= y;
-                }
-                w *= wcarry;  // w_L
-                bool pass = false;
-                if (i < ke) {
-                    float h = w;
-                    if (L < ke) {
-                        const float r = w * F.row_z[L];
-                        const float denom = r + 1.f - w;
-                        h = denom > 0.f ? r / denom : 1.f;
-                    }
-                    pass = F.u[i] < h;
-                }
-                const unsigned m = __ballot_sync(0xffffffffu, pass);
-                if (m) j = c0 + 32 - __clz(m);
-                wcarry = __shfl_sync(0xffffffffu, w, 31);
-            }
-            for (int i = lane; i < j; i += 32) F.path[i] = i + 1;
-            if (lane == 0) {
-                F.L = j;
-                F.stop = j;
-                F.mode = 1;  // the token after the prefix: p with the next draft zeroed, or p
-            }
-        } else if (!P.is_tree) {
-            // Chain: the first draft slot that is not accepted stops the round (warp ballots).
-            {
-                const int k = P.k;
-                int j = k;
-                for (int c0 = 0; c0 < k; c0 += 32) {
-                    const int i = c0 + lane;
-                    bool acc = false;
-                    if (i < k) {
-                        const int x = F.tok[i + 1];
-                        if (x >= 0) {
-                            if (SAMPLE && (P.q || !VAR)) {
-                                acc = F.u[i] * F.qx[i + 1] < F.node_p[i + 1];
-                            } else if (SAMPLE) {
-                                // Target-only: one candidate; thresholds of 1 give u < p(x).
-                                const float px = F.node_p[i + 1];
-                                acc = px > 0.f && (F.u[i] * P.thr_acc < px || px >= P.thr_single);
-                            } else {
-                                acc = (x == F.row_arg[i]);
-                            }
-                        }
-                    }
-                    const unsigned m = __ballot_sync(0xffffffffu, i < k && !acc);
-                    if (m) {
-                        j = c0 + __ffs(m) - 1;
-                        break;
-                    }
-                }
-                for (int i = lane; i < j; i += 32) F.path[i] = i + 1;
-                if (lane == 0) {
-                    F.L = j;
-                    F.stop = j;
-                    if (!SAMPLE) F.mode = 0;
-                    else if (j < k && F.tok[j + 1] >= 0 && P.q) F.mode = 2;
-                    else F.mode = 1;
-                }
-            }
-        } else if (lane == 0) {
-            // Tree walk: one coin per depth, children in ascending node index.
-            int cur = 0, depth = 0, L = 0;
-            for (;;) {
-                int next = -1;
-                if (SAMPLE) {
-                    const float coin = F.u[depth];
-                    float accp = 0.f;
-                    for (int ch = F.first_child[cur]; ch >= 0; ch = F.next_sib[ch]) {
-                        const float pc = F.node_p[ch];
-                        accp += pc;
-                        if (pc > 0.f && (VAR ? (coin * P.thr_acc < accp || pc >= P.thr_single) : coin < accp)) {
-                            next = ch;
-                            break;
-                        }
-                    }
-                } else {
-                    const int am = F.row_arg[cur];
-                    for (int ch = F.first_child[cur]; ch >= 0; ch = F.next_sib[ch]) {
-                        if (F.tok[ch] == am) {
-                            next = ch;
-                            break;
-                        }
-                    }
-                }
-                if (next < 0) break;
-                F.path[L++] = next;
-                cur = next;
-                ++depth;
-            }
-            F.L = L;
-            F.stop = cur;
-            F.mode = SAMPLE ? 1 : 0;
-        }
-    }
-}
-
 template <typename T, bool SAMPLE, bool VAR>
-__device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stage, uint4 *pstage)
+__device__ void finalize_request(const Params &P, int b, FinSmem &F)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwf = blockDim.x >> 5;
     const int rpr = P.rpr;
@@ -627,24 +458,30 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
     stage_request<SAMPLE, VAR>(P, b, F);
     // From here on the streaming kernel's records and captures are read.
     pdl_wait();
+    // Each warp merges its rows and, when sampling, locates each row's crossing record at once:
+    // whichever row the decision stops at, its draw needs only the rescan of that record.
+    RowState rs;
     for (int n = warp; n < rpr; n += nwf) {
-        RowState rs;
         finish_row<T, SAMPLE, VAR>(P, b, n, F, lane, rs);
-        if (SAMPLE && !rs.bad && F.need_draw[n]) row_draw_prep<VAR>(P, b, n, F, lane, rs);
-        if (SAMPLE && n < PF_ROWS) {
-            // Copy the row's crossing range now, in case the decide stops here: the copy
-            // overlaps the decide instead of following it.
-            __syncwarp();  // rs_ok / rs_c0 / rs_c1 were written by one lane
-            if (F.rs_ok[n]) {
-                const int64_t r = (int64_t)b * rpr + n;
-                stage_range<T>(reinterpret_cast<const T *>(P.logits) + r * P.V, r * P.V, P.total, P.mis,
-                               F.rs_c0[n], F.rs_c1[n], pstage + n * RESCAN_STAGE_VEC, lane, 32);
-            }
-        }
+        if (SAMPLE && !rs.bad) row_draw_prep<VAR>(P, b, n, F, lane, rs);
     }
     __syncthreads();
-    if (warp == 0 && !(P.block && P.q)) decide_request<SAMPLE, VAR>(P, F, lane);
-    __syncthreads();
+    // A plain chain's decision is a few shared-memory reads and a ballot: every warp takes it
+    // itself.  Block verification and trees decide in warp 0.
+    const bool chain = !P.is_tree && !P.block;
+    int L = 0, stop = 0, mode = 0;
+    if (chain) {
+        if (F.status == 0) {
+            L = stop = chain_stop<SAMPLE, VAR>(P, F, lane);
+            mode = chain_mode<SAMPLE>(P, F, stop);
+        }
+    } else {
+        if (warp == 0 && !(P.block && P.q)) decide_request<SAMPLE, VAR>(P, F, lane);
+        __syncthreads();
+        L = F.L;
+        stop = F.stop;
+        mode = F.mode;
+    }
     const bool faulted = F.status != 0;
 
     if (SAMPLE && P.block && P.q) {
@@ -697,30 +534,26 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F, uint4 *stag
         if (P.q && !P.is_tree && tid == 0) P.pend[b] = make_int4(-1, 0, 0, 0);
         return;
     }
-    const int L = F.L, stop = F.stop, mode = F.mode;
     int last = -1;
     if (mode == 0) {
         last = F.row_arg[stop];
-    } else if (mode == 1) {
+    } else if (SAMPLE && mode == 1) {
+        // The draw at the stop row: the whole CTA rescans the columns of its crossing record.
         int drawn = F.cand[stop];
         if (F.rs_ok[stop]) {
-            // The stop row's crossing record range, in shared memory (copied after its locate for
-            // the first PF_ROWS rows, else now), then rescanned.
             const int64_t r = (int64_t)b * rpr + stop;
-            if (stop < PF_ROWS) stage = pstage + stop * RESCAN_STAGE_VEC;
-            else stage_range<T>(reinterpret_cast<const T *>(P.logits) + r * P.V, r * P.V, P.total, P.mis,
-                                F.rs_c0[stop], F.rs_c1[stop], stage, tid, blockDim.x);
-            cp_async_wait_all();
-            __syncthreads();
-            drawn = rescan_staged<T, VAR>(r * P.V, P.mis, F.rs_c0[stop], F.rs_c1[stop], VAR ? F.cs : P.cs,
-                                          F.row_mc[stop], VAR ? F.thr[stop] : NEG_INF, F.rs_t[stop], F.rs_cum[stop], F.ex_col + F.ex_off[stop], F.ex_n[stop],
-                                     stage, F.RS);
+            const T *row = reinterpret_cast<const T *>(P.logits) + r * P.V;
+            uint4 w[RESCAN_ROUNDS];
+            load_range<T>(row, r * P.V, P.total, P.mis, F.rs_c0[stop], F.rs_c1[stop], w);
+            drawn = rescan_range<T, VAR>(r * P.V, P.mis, F.rs_c0[stop], F.rs_c1[stop], VAR ? F.cs : P.cs,
+                                         F.row_mc[stop], VAR ? F.thr[stop] : NEG_INF, F.rs_t[stop], F.rs_cum[stop],
+                                         F.ex_col + F.ex_off[stop], F.ex_n[stop], w, F.RS);
         }
         last = drawn >= 0 ? drawn : 0;  // < 0 only through rounding
     }
     for (int i = tid; i < out_w; i += blockDim.x) {
         int v = -1;
-        if (i < L) v = F.tok[F.path[i]];
+        if (i < L) v = F.tok[P.is_tree ? F.path[i] : i + 1];
         else if (i == L) v = last;
         ot[i] = v;
         if (P.is_tree) P.accept_index[(int64_t)b * rpr + i] = (i == 0) ? 0 : (i <= L ? F.path[i - 1] : -1);
@@ -833,12 +666,9 @@ template <typename T, bool SAMPLE, bool VAR>
 __global__ void __launch_bounds__(NT_FIN_MAX) sv_finalize_kernel(const Params P)
 {
     __shared__ FinSmem F;
-    __shared__ uint4 stage[SAMPLE ? RESCAN_STAGE_VEC : 1];  // the stop row's rescan range (rows >= PF_ROWS)
-    extern __shared__ uint4 pstage[];  // sampling: PF_ROWS slots of RESCAN_STAGE_VEC vectors
     const int b = (int)blockIdx.x;
-    if (VAR && P.temps && __ldg(P.temps + b) == 0.f) finalize_request<T, false, false>(P, b, F, stage, pstage);
-    else finalize_request<T, SAMPLE, VAR>(P, b, F, stage, pstage);
-    cp_async_wait_all();  // copies of rows that did not stop the round land before the CTA exits
+    if (VAR && P.temps && __ldg(P.temps + b) == 0.f) finalize_request<T, false, false>(P, b, F);
+    else finalize_request<T, SAMPLE, VAR>(P, b, F);
 }
 
 // 8 consecutive logits (one 16-byte vector of bf16, two of fp32) or q values, as floats; the
@@ -1251,6 +1081,7 @@ struct Layout {
     size_t cnt2, recs, caps, thr, pend, recs2, bpend, recs3, total;
 };
 
+
 // Streaming chunks per row for elements of `vec` per 16-byte vector (see chunk_of).
 static int64_t chunks_per_row(int64_t V, int vec)
 {
@@ -1302,7 +1133,8 @@ static Layout layout(int B, int rpr, int64_t V, bool block = false)
 
 struct DevInfo {
     int sms = 0;
-    bool fin_smem = false;  // the sampling finalisers may take PF_SMEM_BYTES of dynamic shared memory
+    int smem_sm = 0;        // shared memory per SM
+    int fin_smem_max = 0;   // dynamic shared memory the finalising kernels may request
 };
 
 static std::mutex g_dev_mu;
@@ -1320,22 +1152,30 @@ static const DevInfo *device_info()
         cudaGetLastError();
         d.sms = sms;
     }
-    if (!d.fin_smem) {
-        // Above the 48 KB default, so each sampling finaliser is allowed it once per device.
-        const bool ok =
-            cudaFuncSetAttribute(sv_finalize_kernel<__nv_bfloat16, true, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES) == cudaSuccess &&
-            cudaFuncSetAttribute(sv_finalize_kernel<__nv_bfloat16, true, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES) == cudaSuccess &&
-            cudaFuncSetAttribute(sv_finalize_kernel<float, true, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES) == cudaSuccess &&
-            cudaFuncSetAttribute(sv_finalize_kernel<float, true, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES) == cudaSuccess;
+    if (d.fin_smem_max == 0) {
+        // The finalising kernels take dynamic shared memory only to limit how many of their CTAs
+        // share an SM (see fin_dyn_smem); they are allowed up to the per-CTA maximum once per
+        // device.
+        int smem_sm = 0, optin = 0;
+        if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        const int mx = optin - (int)sizeof(FinSmem);
+        const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+        const bool ok = cudaFuncSetAttribute(sv_finalize_kernel<__nv_bfloat16, false, false>, attr, mx) == cudaSuccess &&
+                        cudaFuncSetAttribute(sv_finalize_kernel<__nv_bfloat16, true, false>, attr, mx) == cudaSuccess &&
+                        cudaFuncSetAttribute(sv_finalize_kernel<__nv_bfloat16, true, true>, attr, mx) == cudaSuccess &&
+                        cudaFuncSetAttribute(sv_finalize_kernel<float, false, false>, attr, mx) == cudaSuccess &&
+                        cudaFuncSetAttribute(sv_finalize_kernel<float, true, false>, attr, mx) == cudaSuccess &&
+                        cudaFuncSetAttribute(sv_finalize_kernel<float, true, true>, attr, mx) == cudaSuccess;
         if (!ok) {
             cudaGetLastError();
             return nullptr;
         }
-        d.fin_smem = true;
+        d.smem_sm = smem_sm;
+        d.fin_smem_max = mx;
     }
     return &d;
 }
@@ -1388,15 +1228,32 @@ static void set_rng(Params &P, float temperature, uint64_t seed, uint64_t offset
     P.off1 = (uint32_t)(offset >> 32);
 }
 
+// Dynamic shared memory for the finalising kernel's launch.  Its CTAs are placed as the streaming
+// CTAs leave their SMs, and without a limit the first SMs to empty take as many as fit (eight),
+// which then share one SM's issue slots and special-function units while most SMs idle.  Asking
+// for a share of the SM's shared memory caps them at ceil(B / SMs) per SM: one per SM whenever
+// the batch has no more requests than the GPU has SMs.
+static size_t fin_dyn_smem(const DevInfo &d, int B)
+{
+    int per_sm = (B + d.sms - 1) / d.sms;
+    if (per_sm > 2048 / NT_FIN_MAX) return 0;  // as many as the SM's threads allow anyway
+    const int reserve = 1024;                  // shared memory the system keeps per CTA
+    int dyn = d.smem_sm / per_sm - (int)sizeof(FinSmem) - reserve;
+    if (dyn > d.fin_smem_max) dyn = d.fin_smem_max;
+    return dyn > 0 ? (size_t)dyn : 0;
+}
+
 template <bool SAMPLE>
 static int launch_stream(const Params &P, int dtype, cudaStream_t s)
 {
+    const DevInfo *dinfo = device_info();
+    if (!dinfo) return SPEC_VERIFY_ECUDA;
     // The finaliser is launched as a programmatic dependent of the streaming kernel: its CTAs may
     // start early, stage the request's inputs, and wait (griddepcontrol) for the records.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)P.B);
     cfg.blockDim = dim3(NT_FIN_MAX);  // one warp per row (rows beyond 8 loop); the rescan wants all 8
-    cfg.dynamicSmemBytes = SAMPLE ? PF_SMEM_BYTES : 0;
+    cfg.dynamicSmemBytes = fin_dyn_smem(*dinfo, P.B);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1409,8 +1266,7 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
         // Rows in flight: TK_CTAS CTAs per SM, one row each (two per SM hold 304 rows, 78 MB of
         // bf16 rows of 128256, which L2 keeps for the row's later passes).
         const int64_t rows = (int64_t)P.B * P.rpr;
-        const DevInfo *d = device_info();
-        const int64_t cap = TK_CTAS * (int64_t)(d ? d->sms : 152);
+        const int64_t cap = TK_CTAS * (int64_t)dinfo->sms;
         const unsigned grid = (unsigned)(rows < cap ? rows : cap);
         if (dtype == SPEC_VERIFY_BF16) sv_topkp_kernel<__nv_bfloat16><<<grid, NT_TK, 0, s>>>(P);
         else sv_topkp_kernel<float><<<grid, NT_TK, 0, s>>>(P);
@@ -1439,6 +1295,21 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
 }
 
 static bool temperature_ok(float t) { return t > 0.f && std::isfinite(t); }
+
+// The argument checks of spec_verify_rejection that need no workspace.
+static bool rejection_args_ok(const void *logits, int dtype, const int32_t *draft_ids, const float *draft_probs,
+                              int B, int k, int V, float temperature, const int32_t *out_tokens,
+                              const int32_t *accept_len)
+{
+    if (B < 1 || B > B_MAX || k < 0 || k + 1 > MAX_RPR || V < 1) return false;
+    if ((k > 0 && !draft_ids) || !out_tokens || !accept_len) return false;
+    if (!temperature_ok(temperature)) return false;
+    if (draft_probs && ((uintptr_t)draft_probs % 4)) return false;
+    if (!logits || (dtype != SPEC_VERIFY_BF16 && dtype != SPEC_VERIFY_FP32)) return false;
+    if ((uintptr_t)logits % (dtype == SPEC_VERIFY_BF16 ? 2 : 4)) return false;
+    const int64_t nch = chunks_per_row(V, dtype == SPEC_VERIFY_BF16 ? 8 : 4);
+    return (int64_t)B * (k + 1) * nch < ((int64_t)1 << 31);
+}
 
 }  // namespace sv
 
@@ -1505,10 +1376,8 @@ int spec_verify_rejection(const void *logits, int dtype, const int32_t *draft_id
                           int32_t *accept_len, float *out_probs, void *workspace,
                           size_t ws_bytes, int32_t *dev_status, void *stream)
 {
-    if (B < 1 || B > B_MAX || k < 0 || k + 1 > MAX_RPR || V < 1) return SPEC_VERIFY_EINVAL;
-    if ((k > 0 && !draft_ids) || !out_tokens || !accept_len) return SPEC_VERIFY_EINVAL;
-    if (!temperature_ok(temperature)) return SPEC_VERIFY_EINVAL;
-    if (draft_probs && ((uintptr_t)draft_probs % 4)) return SPEC_VERIFY_EINVAL;
+    if (!rejection_args_ok(logits, dtype, draft_ids, draft_probs, B, k, V, temperature, out_tokens, accept_len))
+        return SPEC_VERIFY_EINVAL;
     Params P;
     memset(&P, 0, sizeof P);
     int rc = common_setup(P, logits, dtype, B, k + 1, V, workspace, ws_bytes);
@@ -1752,14 +1621,18 @@ extern "C" int spec_verify_rejection_noalloc(const void *logits, int dtype,
                                              int32_t *accept_len, float *out_probs,
                                              int32_t *dev_status, void *stream)
 {
-    if (B < 1 || B > B_MAX || k < 0 || k + 1 > MAX_RPR || V < 1) return SPEC_VERIFY_EINVAL;
+    // Every argument check comes first, so that a rejected call enqueues nothing.
+    if (!rejection_args_ok(logits, dtype, draft_ids, draft_probs, B, k, V, temperature, out_tokens, accept_len))
+        return SPEC_VERIFY_EINVAL;
     const size_t need = spec_verify_workspace_bytes(SPEC_VERIFY_MODE_REJECTION, B, k, V);
     if (need == 0) return SPEC_VERIFY_EINVAL;
     if (need > SPEC_VERIFY_NOALLOC_SCRATCH_BYTES) return SPEC_VERIFY_ETOOBIG;
+    if (!device_info()) return SPEC_VERIFY_ECUDA;
     void *scratch = noalloc_scratch_address();
     if (!scratch) return SPEC_VERIFY_ECUDA;
     // The scratch keeps whatever the previous call left; the arrival counters of the requests
-    // this call uses must start at zero, so clear them (a memset, no allocation).
+    // this call uses must start at zero (every completed call leaves them zero, but a call cut
+    // short may not), so clear them (a memset, no allocation).
     const Layout L = layout(B, k + 1, V);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *base = static_cast<char *>(scratch);

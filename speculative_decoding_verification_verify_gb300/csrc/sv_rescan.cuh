@@ -2,10 +2,10 @@
 //
 // The finalising kernel knows which record of the streaming pass holds the crossing of the draw
 // threshold t, and the mass before that record.  The record covers one streaming chunk of at most
-// CHUNK_VEC 16-byte vectors (plus an unaligned head and tail), so the CTA copies that range into
-// shared memory with cp.async (every copy in flight at once, completion tracked by the hardware),
-// weighs it vector by vector, finds the vector where the running mass crosses t with a block-wide
-// scan, and the thread holding that vector walks its few elements.
+// CHUNK_VEC 16-byte vectors (plus an unaligned head and tail), so every thread of the CTA loads
+// its few vectors of that range straight into registers (one round trip, mostly L2 hits: the
+// chunk was streamed a few microseconds earlier), weighs them, finds the vector where the running
+// mass crosses t with a block-wide scan, and the thread holding that vector walks its elements.
 #pragma once
 
 #include <climits>
@@ -15,9 +15,8 @@
 
 namespace sv {
 
-// Shared-memory vectors the CTA stages: the range holds at most CHUNK_VEC aligned vectors plus a
-// partial one at each end.
-constexpr int RESCAN_STAGE_VEC = CHUNK_VEC + 2;
+// Vectors of a crossing range: at most CHUNK_VEC aligned vectors plus a partial one at each end.
+constexpr int RESCAN_RANGE_VEC = CHUNK_VEC + 2;
 
 // The 16-byte vector of a row starting at column col, with the elements outside [c0, c1) read
 // as -inf, element by element, so that no byte outside [c0, c1) is touched.
@@ -62,10 +61,10 @@ __device__ __forceinline__ void vec_weights_plain(const uint4 &w, int col, int c
     }
 }
 
-// Rounds of the rescan: thread t weighs vectors t, t + nt, t + 2 nt of the staged range.
+// Rounds of the rescan: thread t weighs vectors t, t + nt, t + 2 nt of the range.
 constexpr int RESCAN_ROUNDS = 3;
 constexpr int RESCAN_THREADS = 256;  // the finalising CTA's size, which the rounds assume
-static_assert(RESCAN_ROUNDS * RESCAN_THREADS >= RESCAN_STAGE_VEC, "three rounds cover the range");
+static_assert(RESCAN_ROUNDS * RESCAN_THREADS >= RESCAN_RANGE_VEC, "three rounds cover the range");
 
 struct RescanSmem {
     float wsum[RESCAN_ROUNDS * 8];  // per (round, warp) totals
@@ -74,40 +73,41 @@ struct RescanSmem {
     int found;
 };
 
-// Copy the vectors covering columns [c0, c1) of a row into stage: vector i starts at column
-// a0 + i*VEC, a0 being c0 rounded down to a 16-byte boundary (row points at column 0; rowflat is
-// the row's first element in the flat logits array of `total` elements, whose base is mis
-// elements past a 16-byte boundary).  Whole aligned vectors are copied even where they stick out
-// of [c0, c1) (the weights mask those elements); only a vector that would reach outside the
-// logits array is read element by element.  Threads t = 0..nt-1 share the copies; each thread
-// commits its cp.async group and must wait for it before the stage is read.
+// The vectors covering columns [c0, c1) of a row, vector i starting at column a0 + i * VEC, a0
+// being c0 rounded down to a 16-byte boundary (row points at column 0; rowflat is the row's first
+// element in the flat logits array of `total` elements, whose base is mis elements past a 16-byte
+// boundary): thread t loads vectors t + i * RESCAN_THREADS.  Whole aligned vectors are read even
+// where they stick out of [c0, c1) (the weights mask those elements); only a vector that would
+// reach outside the logits array is read element by element.
 template <typename T>
-__device__ __forceinline__ void stage_range(const T *row, int64_t rowflat, int64_t total, int mis, int c0,
-                                            int c1, uint4 *stage, int t, int nt)
+__device__ __forceinline__ void load_range(const T *row, int64_t rowflat, int64_t total, int mis, int c0, int c1,
+                                           uint4 (&w)[RESCAN_ROUNDS])
 {
     constexpr int VEC = Elt<T>::VEC;
     const int a0 = c0 - (int)((rowflat + c0 + mis) % VEC);
     const int nvv = (c1 - a0 + VEC - 1) / VEC;
-    for (int i = t; i < nvv; i += nt) {
-        const int col = a0 + i * VEC;
-        const int64_t f = rowflat + col;
-        if (f >= 0 && f + VEC <= total) cp_async16(stage + i, row + col);
-        else stage[i] = load_partial<T>(row, col, c0, c1);
+#pragma unroll
+    for (int i = 0; i < RESCAN_ROUNDS; ++i) {
+        const int k = threadIdx.x + i * RESCAN_THREADS;
+        w[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (k < nvv) {
+            const int col = a0 + k * VEC;
+            const int64_t f = rowflat + col;
+            w[i] = (f >= 0 && f + VEC <= total) ? ldg_stream(row + col) : load_partial<T>(row, col, c0, c1);
+        }
     }
-    cp_async_commit();
 }
 
 // First column y of [c0, c1) at which cum0 + (running weight up to and including y) exceeds t;
 // when none does (t = +inf asks for that), the last column with positive weight; -1 if no weight
-// is positive.  Child tokens ex[0..ex_n) weigh 0.  stage holds the range as stage_range laid it
-// out, visible to every thread; all RESCAN_THREADS threads of the CTA call it and get the result.
-// Thread t weighs whole vectors t + i * nt (conflict-free shared reads); per-round warp scans and
-// one table of (round, warp) totals give every vector its running mass; the first crossing vector
+// is positive.  Child tokens ex[0..ex_n) weigh 0.  w holds the range as load_range loads it; all
+// RESCAN_THREADS threads of the CTA call it and get the result.  Per-round warp scans and one
+// table of (round, warp) totals give every vector its running mass; the first crossing vector
 // (or the last positive one) comes from shared-memory atomics, and its owner walks its VEC
 // elements.  Three barriers, and one shared-memory atomic per warp.
 template <typename T, bool FILT>
-__device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs, float mc, float thr, float t,
-                             float cum0, const int *ex, int ex_n, const uint4 *stage, RescanSmem &S)
+__device__ int rescan_range(int64_t rowflat, int mis, int c0, int c1, float cs, float mc, float thr, float t,
+                            float cum0, const int *ex, int ex_n, const uint4 (&w)[RESCAN_ROUNDS], RescanSmem &S)
 {
     constexpr int VEC = Elt<T>::VEC;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -126,7 +126,7 @@ __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs,
         if (k < nvv) {
             const int col = a0 + k * VEC;
             float e[VEC];
-            vec_weights_plain<T, FILT>(stage[k], col, c0, c1, cs, mc, thr, e);
+            vec_weights_plain<T, FILT>(w[i], col, c0, c1, cs, mc, thr, e);
             for (int x = 0; x < ex_n; ++x) {
                 const int d = ex[x] - col;
 #pragma unroll
@@ -147,9 +147,9 @@ __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs,
 #pragma unroll
     for (int i = 0; i < RESCAN_ROUNDS; ++i) {
         pre[i] = 0.f;
-        for (int w = 0; w < nw; ++w) {
-            if (w == warp) pre[i] = base;
-            base += S.wsum[i * 8 + w];
+        for (int q = 0; q < nw; ++q) {
+            if (q == warp) pre[i] = base;
+            base += S.wsum[i * 8 + q];
         }
     }
     int kmin = INT_MAX, klast = -1;
@@ -180,8 +180,12 @@ __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs,
         for (int r = 0; r < RESCAN_ROUNDS; ++r)
             if (r == i) before = pre[r] + inc[r] - vs[r];
         const int col = a0 + kv * VEC;
+        uint4 wv = w[0];
+#pragma unroll
+        for (int r = 1; r < RESCAN_ROUNDS; ++r)
+            if (r == i) wv = w[r];
         float e[VEC];
-        vec_weights_plain<T, FILT>(stage[kv], col, c0, c1, cs, mc, thr, e);
+        vec_weights_plain<T, FILT>(wv, col, c0, c1, cs, mc, thr, e);
         for (int x = 0; x < ex_n; ++x) {
             const int d = ex[x] - col;
 #pragma unroll
@@ -203,6 +207,40 @@ __device__ int rescan_staged(int64_t rowflat, int mis, int c0, int c1, float cs,
     }
     __syncthreads();
     return S.found;
+}
+
+// Locate step over one chunk of 32 records with masses m (in the row's reference): finds the
+// first record where the running mass exceeds t, and tracks the last record with positive mass.
+struct Locate {
+    float cum = 0.f, before = 0.f, lp_before = 0.f;
+    int found = -1, lastpos = -1;
+};
+
+__device__ __forceinline__ bool locate_chunk(Locate &Lc, float m, int c0, float t, int lane)
+{
+    const float incl = warp_incl_scan(m, lane);
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.f;
+    const unsigned hit = __ballot_sync(0xffffffffu, Lc.cum + incl > t);
+    const unsigned pos = __ballot_sync(0xffffffffu, m > 0.f);
+    if (pos) {
+        const int lp = 31 - __clz(pos);
+        Lc.lastpos = c0 + lp;
+        Lc.lp_before = Lc.cum + __shfl_sync(0xffffffffu, excl, lp);
+    }
+    if (hit) {
+        const int fl = __ffs(hit) - 1;
+        Lc.found = c0 + fl;
+        Lc.before = Lc.cum + __shfl_sync(0xffffffffu, excl, fl);
+        return true;
+    }
+    Lc.cum += __shfl_sync(0xffffffffu, incl, 31);
+    return false;
+}
+
+__device__ __forceinline__ float rec_mass(const float4 &r, float mc)
+{
+    return (r.y == 0.f) ? 0.f : r.y * ex2(r.x - mc);
 }
 
 }  // namespace sv

@@ -362,4 +362,34 @@ __device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int la
     flush_record<SAMPLE>(rec, lane, sa, ga, c0, c1);
 }
 
+// ---------------------------------------------------------------------------------------------
+// The streaming warp's view of a request's nodes: lane i holds nodes i and i + 32 (token and
+// parent; the chain is a path tree), and Kids marks the children of row n's node with a usable
+// token.
+// ---------------------------------------------------------------------------------------------
+struct NodeView {
+    int tok[2], par[2];
+};
+
+__device__ __forceinline__ void load_nodes(const Params &P, int b, int lane, NodeView &nv)
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int m = lane + 32 * h;
+        nv.tok[h] = -1;
+        nv.par[h] = -1;
+        if (m >= 1 && m < P.rpr) {
+            nv.tok[h] = node_token(P, b, m);
+            nv.par[h] = node_parent(P, b, m);
+        }
+    }
+}
+
+__device__ __forceinline__ void kids_of(const Params &P, const NodeView &nv, int n, Kids &kd)
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        kd.col[h] = (nv.par[h] == n && nv.tok[h] >= 0 && (int64_t)nv.tok[h] < P.V) ? nv.tok[h] : INT_MAX;
+}
+
 }  // namespace sv
