@@ -36,7 +36,9 @@ B, K_DRAFTS, V = 64, 7, 128256
 N_SETS = 3  # rotating input sets: 3 x 131 MB > L2 (129 MB)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_call_b64k7_traffic.json")
 LAUNCHES_PER_CALL = 2  # sv_stream_kernel, then sv_finalize_kernel (programmatic dependent launch)
-GRAPH_CALLS = 30  # verify calls captured in one CUDA graph for the timed region
+GRAPH_CALLS = 30  # verify calls captured in one CUDA graph when timing the other modes
+MAX_GRAPH_CALLS = 100  # largest graph of headline calls; more steps replay it several times
+SPREAD_REPLAYS = 10   # replays, after the timed region, that give the per-call spread
 KV_SETS = 8       # KV-compaction index sets rotated over one pool
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 KERNEL_SOURCES = [os.path.join(ROOT, "speculative_decoding_verification_verify_gb300", "csrc", f)
@@ -117,6 +119,20 @@ def chain_bytes(B, k, V, esize, with_q=False):
     logits = B * (k + 1) * V * esize
     q = B * k * V * 4 if with_q else 0
     return logits + q + B * k * 4 + B * (k + 1) * 4 + B * 4
+
+
+def required_bytes(B, k, V, esize, rejected_rows):
+    """Bytes standard rejection must read: every logit once, q at each draft (a gather), one q row
+    per request whose round stops at a rejected draft (the residual max(0, p - q) needs that whole
+    row), the drafts, and the outputs."""
+    return B * (k + 1) * V * esize + B * k * 4 + rejected_rows * V * 4 + B * k * 4 + B * (k + 1) * 4 + B * 4
+
+
+def rejected_rows(alen, k, drafts):
+    """Requests whose round stopped at a present draft (a rejection, not a bonus or a gap)."""
+    a = alen.cpu().numpy()
+    d = drafts.cpu().numpy()
+    return int(sum(1 for b in range(a.shape[0]) if 0 <= a[b] < k and d[b, a[b]] >= 0))
 
 
 def tree_bytes(B, N, V, esize):
@@ -201,47 +217,72 @@ def gpu_selector(torch, dev) -> str:
         return str(dev.index or 0)
 
 
-def capture_calls(torch, calls):
-    """One CUDA graph holding the given launches back to back (each call enqueues on the current
-    stream, which is the capture stream inside the block)."""
-    graph = torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        calls[0]()  # warm-up outside capture on the side stream (first-use setup, if any)
-    torch.cuda.current_stream().wait_stream(side)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(graph):
-        for c in calls:
-            c()
-    return graph
+def _event(torch):
+    """A timing event that can be recorded inside a CUDA graph (an event-record node)."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:  # a torch without external events: record around the replay instead
+        return None
+
+
+class TimedGraph:
+    """One CUDA graph holding the given calls back to back (each enqueues on the current stream,
+    the capture stream inside the block), bracketed by two timing events recorded inside the graph
+    where torch supports it, so a replay's interval is the device time of exactly these calls."""
+
+    def __init__(self, torch, calls):
+        self.torch = torch
+        self.n = len(calls)
+        self.graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            calls[0]()  # first-use setup, if any, outside capture
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.e0, self.e1 = _event(torch), _event(torch)
+        self.inside = self.e0 is not None and self.e1 is not None
+        if not self.inside:
+            self.e0 = torch.cuda.Event(enable_timing=True)
+            self.e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.graph(self.graph):
+            if self.inside:
+                self.e0.record()
+            for c in calls:
+                c()
+            if self.inside:
+                self.e1.record()
+
+    def replay(self):
+        if not self.inside:
+            self.e0.record()
+        self.graph.replay()
+        if not self.inside:
+            self.e1.record()
+
+    def last_ms(self):
+        """Device time of the last replay (call after synchronising)."""
+        return self.e0.elapsed_time(self.e1)
 
 
 def graph_time_ms(torch, calls, reps, flush=None):
-    """Per-call device time (ms) of calls replayed back to back from one CUDA graph."""
-    graph = capture_calls(torch, calls)
+    """Per-call device time (ms): median over `reps` replays of a graph of the calls.  With
+    `flush` the graph holds one call and the flush runs before each replay, outside the timed
+    interval."""
+    tg = TimedGraph(torch, calls)
     for _ in range(3):
-        graph.replay()
+        if flush is not None:
+            flush()
+        tg.replay()
     torch.cuda.synchronize()
-    if flush is None:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            graph.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / (reps * len(calls))
-    # Flushed: one call per graph, L2 cleared between replays, each replay timed on its own.
     times = []
     for _ in range(reps):
-        flush()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        graph.replay()
-        e1.record()
+        if flush is not None:
+            flush()
+        tg.replay()
         torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1))
-    return statistics.median(times) / len(calls)
+        times.append(tg.last_ms() / tg.n)
+    return statistics.median(times)
 
 
 # --------------------------------------------------------------------------------------------
@@ -289,33 +330,50 @@ def run_ours(args, D: Dist):
         call(w, off0 + w)
     torch.cuda.synchronize()
 
-    # The timed region replays a CUDA graph of GRAPH_CALLS back-to-back calls (the input sets
-    # rotate, each call has its own Philox offset), so host launch overhead does not pace the GPU.
-    graph = capture_calls(torch, [lambda i=i: call(i, off0 + args.warmup + i) for i in range(GRAPH_CALLS)])
-    reps = max(1, args.steps // GRAPH_CALLS)
-    K = reps * GRAPH_CALLS
+    # The timed region is exactly K calls (the input sets rotate, each call has its own Philox
+    # offset), replayed from CUDA graphs so that host launches do not pace the GPU: one graph of
+    # all K calls when K <= MAX_GRAPH_CALLS (its timing events recorded inside the graph), else
+    # graphs of MAX_GRAPH_CALLS calls and one of the remainder, replayed back to back.
+    K = args.steps
+    base = off0 + args.warmup
+    GC = min(K, MAX_GRAPH_CALLS)
+    nfull, rem = divmod(K, GC)
+    main = TimedGraph(torch, [lambda i=i: call(i, base + i) for i in range(GC)])
+    tail = (TimedGraph(torch, [lambda i=i: call(nfull * GC + i, base + nfull * GC + i) for i in range(rem)])
+            if rem else None)
     for _ in range(3):
-        graph.replay()
+        main.replay()
     torch.cuda.synchronize()
     clocks = ClockSampler(gpu_selector(torch, dev))
     time.sleep(0.1)
     D.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    # One event pair per replay (30 calls each) gives the spread; their span gives the total.
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-    ev[0].record()
-    for i in range(reps):
-        graph.replay()
-        ev[i + 1].record()
-    torch.cuda.synchronize()
+    if nfull == 1 and tail is None:
+        main.replay()
+        torch.cuda.synchronize()
+        total_ms = main.last_ms()
+    else:
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(nfull):
+            main.replay()
+        if tail is not None:
+            tail.replay()
+        s1.record()
+        torch.cuda.synchronize()
+        total_ms = s0.elapsed_time(s1)
     t1 = time.time()
     D.barrier()
     clocks.stop()
-    total_ms = ev[0].elapsed_time(ev[-1])
-    per_call = [ev[i].elapsed_time(ev[i + 1]) / GRAPH_CALLS for i in range(reps)]
     launch_ms = total_ms / K
     max_total_ms = D.max(total_ms, dev)
+    # The spread, outside the timed region: per-call time over further replays of the graph.
+    per_call = []
+    for _ in range(SPREAD_REPLAYS):
+        main.replay()
+        torch.cuda.synchronize()
+        per_call.append(main.last_ms() / main.n)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the benchmark")
 
@@ -357,7 +415,9 @@ def run_ours(args, D: Dist):
                                                   float(np.percentile(per_call, 10)),
                                                   float(np.percentile(per_call, 90))],
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                     "timing": f"CUDA events around each of {reps} replays of a graph of {GRAPH_CALLS} calls"},
+                     "timing": (f"{K} calls from CUDA graphs of {GC} calls"
+                                + (", timing events recorded inside the graph" if main.inside else "")
+                                + f"; spread over {SPREAD_REPLAYS} further replays of {GC} calls")},
         "gpu_launches": LAUNCHES_PER_CALL * K,
         "clocks": clocks.summary(t0, t1),
     }
@@ -367,6 +427,8 @@ def run_ours(args, D: Dist):
     if not args.no_e2e:
         line["e2e"] = run_e2e(args, D, torch, sv, lib, sets, ws, ws_bytes, status, stream, sh, off0)
 
+    if D.rank == 0:
+        line["acceptance"] = acceptance_stats(lib, sv, torch, sets[0], ws, ws_bytes, off0 + 12345)
     if D.rank == 0 and D.world == 1 and args.cpu_seconds > 0:
         line["cpu_baseline"] = cpu_baseline(sets[0][0], args.cpu_seconds)
     if not args.no_modes:
@@ -376,12 +438,94 @@ def run_ours(args, D: Dist):
         print(json.dumps(line), flush=True)
 
 
+def gpu_numa_node(torch, dev):
+    """The NUMA node the GPU's PCI function reports (sysfs), or None."""
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        bus = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        node = int(open(f"/sys/bus/pci/devices/{bus}/numa_node").read().strip())
+        return node if node >= 0 else None
+    except (AttributeError, OSError, ValueError):
+        return None
+
+
+def node_cpus(node):
+    """CPUs of a NUMA node (sysfs cpulist), or an empty set."""
+    try:
+        txt = open(f"/sys/devices/system/node/node{node}/cpulist").read().strip()
+    except OSError:
+        return set()
+    cpus = set()
+    for part in txt.split(","):
+        if "-" in part:
+            lo, hi = part.split("-")
+            cpus.update(range(int(lo), int(hi) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus
+
+
+class NodeBinding:
+    """Bind this thread's CPU affinity and memory policy to one NUMA node while pinned host
+    buffers are allocated and the end-to-end leg runs (process settings only; no GPU setting is
+    touched).  Restores both on exit."""
+    MPOL_DEFAULT, MPOL_BIND = 0, 2
+    NR_SET_MEMPOLICY = {"aarch64": 237, "x86_64": 238}
+
+    def __init__(self, node):
+        self.node, self.ok, self.mem_ok = node, False, False
+        self.old_aff = None
+
+    def _set_mempolicy(self, mode, mask):
+        import platform
+
+        nr = self.NR_SET_MEMPOLICY.get(platform.machine())
+        if nr is None:
+            return False
+        libc = ctypes.CDLL(None, use_errno=True)
+        m = ctypes.c_ulong(mask)
+        return libc.syscall(nr, mode, ctypes.byref(m) if mask else None, 64 if mask else 0) == 0
+
+    def __enter__(self):
+        cpus = node_cpus(self.node) if self.node is not None else set()
+        if cpus:
+            self.old_aff = os.sched_getaffinity(0)
+            os.sched_setaffinity(0, cpus)
+            self.ok = True
+            self.mem_ok = self._set_mempolicy(self.MPOL_BIND, 1 << self.node)
+        return self
+
+    def __exit__(self, *exc):
+        if self.mem_ok:
+            self._set_mempolicy(self.MPOL_DEFAULT, 0)
+        if self.old_aff is not None:
+            os.sched_setaffinity(0, self.old_aff)
+
+
 def run_e2e(args, D, torch, sv, lib, sets, ws, ws_bytes, status, stream, sh, off0):
     """End to end through the C ABI from pinned host buffers: every step copies its logits and
     drafts host -> device, verifies, and copies the outputs back.  The device inputs are double
-    buffered: step s + 1's copy (on a copy stream) overlaps step s's verification, which is
-    what a serving loop does; the host -> device link (about 210 GB/s on this machine) bounds
-    the rate."""
+    buffered: step s + 1's copy (on a copy stream) overlaps step s's verification, which is what a
+    serving loop does; the host -> device link bounds the rate.  Measured with the process as it
+    starts, and again with its CPU affinity and memory policy bound to the GPU's NUMA node (the
+    pinned buffers allocated under that policy); the line reports the bound run when the node is
+    known."""
+    node = gpu_numa_node(torch, stream.device)
+    plain = _e2e_once(args, D, torch, sv, lib, sets, ws, ws_bytes, status, stream, sh, off0)
+    plain["numa"] = {"gpu_node": node, "bound": False}
+    if node is None:
+        return plain
+    with NodeBinding(node) as nb:
+        if not nb.ok:
+            return plain
+        bound = _e2e_once(args, D, torch, sv, lib, sets, ws, ws_bytes, status, stream, sh, off0)
+    bound["numa"] = {"gpu_node": node, "bound": True, "memory_policy_bound": nb.mem_ok,
+                     "cpus": len(node_cpus(node))}
+    bound["unbound"] = {k: plain[k] for k in ("value", "ms_per_step", "h2d_gbs")}
+    return bound
+
+
+def _e2e_once(args, D, torch, sv, lib, sets, ws, ws_bytes, status, stream, sh, off0):
     steps = min(args.steps, 200)
     host = []
     for inp, out, alen in sets[:2]:
@@ -444,12 +588,55 @@ def run_e2e(args, D, torch, sv, lib, sets, ws, ws_bytes, status, stream, sh, off
     torch.cuda.synchronize()
     D.barrier()
     ms = D.max(e0.elapsed_time(e1), torch.device("cuda", D.local_rank))
+    del host, hl, hd, ho, ha
+    # Pinned blocks go back to torch's host cache; empty it so the next leg allocates afresh
+    # (under its own memory policy).
+    if hasattr(torch._C, "_host_emptyCache"):
+        torch._C._host_emptyCache()
     return {"value": D.world * B * (K_DRAFTS + 1) * steps / (ms * 1e-3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": ms / steps, "gpu_launches": LAUNCHES_PER_CALL * steps,
             "h2d_gbs": h2d * steps / (ms * 1e-3) / 1e9,
             "path": "pinned host -> device copy (double-buffered, copy stream), spec_verify_rejection, "
                     "device -> pinned host"}
+
+
+def acceptance_stats(lib, sv, torch, one_set, ws, ws_bytes, offset):
+    """What the round emitted on the timed batch (input set 0, one Philox offset), outside the
+    timed region: the oracle's accepted lengths, the accepted-per-position counts (requests whose
+    draft at position i was accepted), the emitted tokens per request, and the draws the oracle
+    flags as lying within 1e-6 of a decision boundary; the GPU's outputs of the same call are
+    compared with the oracle's request by request."""
+    import numpy as np
+
+    import oracle
+    from speculative_decoding_verification_verify_gb300 import workloads as wl
+
+    inp, out, alen = one_set
+    st = torch.zeros(1, dtype=torch.int32, device=out.device)
+    rc = lib.spec_verify_rejection(
+        ctypes.c_void_p(inp.logits.data_ptr()), sv.BF16, ctypes.c_void_p(inp.drafts.data_ptr()), None, B,
+        K_DRAFTS, V, 1.0, inp.seed, offset, ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(alen.data_ptr()),
+        None, ctypes.c_void_p(ws.data_ptr()), ws_bytes, ctypes.c_void_p(st.data_ptr()),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if rc != 0:
+        raise RuntimeError(f"spec_verify_rejection returned {rc}")
+    torch.cuda.synchronize()
+    g_tok, g_len = out.cpu().numpy(), alen.cpu().numpy()
+    oracle.build()
+    ref = oracle.verify_rejection(wl.to_numpy_logits(inp.logits), inp.drafts.cpu().numpy(), None, 1.0, inp.seed,
+                                  offset)
+    flagged = ref["boundary"].astype(bool)
+    same = (g_len == ref["accept_len"]) & np.all(g_tok == ref["out_tokens"], axis=1)
+    L = ref["accept_len"]
+    return {"requests": int(B), "boundary_draws": int(flagged.sum()),
+            "differing_requests_outside_boundary": int((~same & ~flagged).sum()),
+            "device_status": int(st.item()),
+            "mean_accept_len": float(L.mean()), "mean_emitted_tokens": float((L + 1).mean()),
+            "accept_len_histogram": np.bincount(L, minlength=K_DRAFTS + 1).tolist(),
+            "accepted_per_position": [int((L > i).sum()) for i in range(K_DRAFTS)],
+            "source": f"CPU oracle on input set 0 of the timed batch at Philox offset {offset}; the GPU's "
+                      "outputs of the same call compared request by request"}
 
 
 def _oracle_rate(lg, d, seed, seconds, threads):
@@ -512,7 +699,7 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
             raise RuntimeError(f"{name} returned {rc}")
 
     res = {}
-    names = {"greedy", "tree", "block", "with_q", "b1k3", "kv_compact", "variants", "budget"}
+    names = {"greedy", "tree", "block", "with_q", "b1k3", "tiny", "sweep", "kv_compact", "variants", "budget"}
     want = names if args.modes == "all" else set(args.modes.split(","))
     if want - names:
         raise SystemExit(f"unknown modes {sorted(want - names)}; known: {sorted(names)}")
@@ -526,6 +713,10 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
         res.update(_block_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak, want))
     if "b1k3" in want:
         res.update(_b1k3_mode(torch, sv, wl, dev, lib, P, cur, check, status, peak))
+    if "tiny" in want:
+        res.update(_tiny_mode(torch, sv, wl, dev, lib, P, cur, check, status))
+    if "sweep" in want:
+        res.update(_sweep_modes(torch, sv, wl, dev, lib, P, cur, check, status, peak))
     if "variants" in want:
         res.update(_variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak))
     if "budget" in want:
@@ -595,21 +786,15 @@ def _block_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak
         return res
     qsets = [wl.chain_sweep(dev, seed=7100 + i, B=B, k=K_DRAFTS, alpha=0.7) for i in range(N_SETS)]
     ms = graph_time_ms(torch, [lambda i=i: block(i, qsets[i % N_SETS], qsets[i % N_SETS].q) for i in range(12)], 10)
-    nr = sv.spec_verify_workspace_bytes(sv.MODE_REJECTION, B, K_DRAFTS, V)
-    rws = torch.zeros(nr, dtype=torch.uint8, device=dev)
-
-    def standard_q(i, x):
-        check(lib.spec_verify_rejection(P(x.logits), sv.BF16, P(x.drafts), P(x.q), B, K_DRAFTS, V, 1.0, x.seed, i,
-                                        P(out), P(alen), None, P(rws), nr, P(status), cur()), "spec_verify_rejection")
-
-    sms = graph_time_ms(torch, [lambda i=i: standard_q(i, qsets[i % N_SETS]) for i in range(12)], 10)
-    res["standard_sweep_b64k7_with_q"] = _mode_entry(
-        sms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2, with_q=True), peak, 3,
-        note="algorithmic bytes count all of q; the residual kernel reads q only at rejected rows")
-    res["block_sweep_b64k7_with_q"] = _mode_entry(
-        ms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2, with_q=True), peak, 3,
-        note="algorithmic bytes count the logits and q once; the block kernel reads the logits and q "
-             "of the present rows a second time")
+    # The block rule needs every present row's q (its residual masses r_L sum max(0, w_L p - q) over
+    # the whole row), so its bytes are the logits and all of q once; the kernel reads both a second
+    # time in its residual pass.
+    both = chain_bytes(B, K_DRAFTS, V, 2, with_q=True)
+    e = _mode_entry(ms, B * (K_DRAFTS + 1), both, peak, 3,
+                    note="bytes the block rule must read: the logits and every present q row once; the "
+                         "design reads both twice (the streaming pass, then the block kernel's residual pass)")
+    e["gbs_counting_both_passes"] = 2 * both / (ms * 1e-3) / 1e9
+    res["block_sweep_b64k7_with_q"] = e
     del qsets
     return res
 
@@ -630,9 +815,96 @@ def _b1k3_mode(torch, sv, wl, dev, lib, P, cur, check, status, peak):
                                         P(status), cur()), "spec_verify_rejection")
 
     ms = graph_time_ms(torch, [standard], 100, flush=lambda: flush_buf.zero_())
-    return {"standard_b1k3": _mode_entry(ms, Bq * (kq + 1), chain_bytes(Bq, kq, Vq, 2, with_q=True),
-                                         peak, 3, note="latency-bound; L2 flushed before each call; "
-                                         "algorithmic bytes count all of q")}
+    standard()
+    nrej = rejected_rows(qal, kq, inp.drafts)
+    e = _mode_entry(ms, Bq * (kq + 1), required_bytes(Bq, kq, Vq, 2, nrej), peak, 3,
+                    note="latency-bound; L2 flushed before each call; bytes = what the rule must read")
+    e["bytes_all_of_q"] = chain_bytes(Bq, kq, Vq, 2, with_q=True)
+    return {"standard_b1k3": e}
+
+
+def _tiny_mode(torch, sv, wl, dev, lib, P, cur, check, status):
+    """The tiny configuration (B=4, k=3, V=1024, fp32): latency of standard rejection and greedy,
+    L2 flushed before each call, device time of the call alone."""
+    inp = wl.chain_tiny(dev)
+    Bt, kt, Vt = inp.shape
+    o = torch.empty((Bt, kt + 1), dtype=torch.int32, device=dev)
+    al = torch.empty(Bt, dtype=torch.int32, device=dev)
+    nb = sv.spec_verify_workspace_bytes(sv.MODE_REJECTION, Bt, kt, Vt)
+    ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def standard():
+        check(lib.spec_verify_rejection(P(inp.logits), sv.FP32, P(inp.drafts), P(inp.q), Bt, kt, Vt,
+                                        inp.temperature, inp.seed, 3, P(o), P(al), None, P(ws), nb, P(status),
+                                        cur()), "spec_verify_rejection")
+
+    def greedy():
+        check(lib.spec_verify_greedy(P(inp.logits), sv.FP32, P(inp.drafts), Bt, kt, Vt, P(o), P(al), P(ws), nb,
+                                     P(status), cur()), "spec_verify_greedy")
+
+    res = {}
+    for name, fn, launches in (("tiny_standard", standard, 3), ("tiny_greedy", greedy, 2)):
+        ms = graph_time_ms(torch, [fn], 50, flush=lambda: flush_buf.zero_())
+        res[name] = {"ms_per_call": ms, "us_per_call": ms * 1e3, "positions_per_s": Bt * (kt + 1) / (ms * 1e-3),
+                     "launches_per_call": launches,
+                     "note": "B=4, k=3, V=1024 fp32: latency-bound, reported as latency; L2 flushed before each call"}
+    return res
+
+
+SWEEP_B = (1, 8, 32, 64, 512)
+SWEEP_K = (0, 1, 3, 7)
+SWEEP_ALPHA = (0.35, 0.7)
+
+
+def _sweep_modes(torch, sv, wl, dev, lib, P, cur, check, status, peak):
+    """The adaptive-schedule grid: B x k x alpha, standard rejection with draft distributions,
+    V=128256 bf16, T=1.  Cells whose logits and q together are under 2/3 of L2 are timed one call
+    at a time with L2 flushed before each; larger cells rotate three input sets.  Each cell reports
+    positions/s, GB/s against the bytes the rule must read (the logits, q at the drafts, and the q
+    row of each request whose round stops at a rejection), and beside it the count with all of q."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    res = {}
+    for Bs in SWEEP_B:
+        for ks in SWEEP_K:
+            for a in SWEEP_ALPHA:
+                all_q = chain_bytes(Bs, ks, V, 2, with_q=True)
+                rotate = all_q * 3 >= 2 * l2
+                nsets = N_SETS if rotate else 1
+                sets = [wl.chain_sweep(dev, seed=11000 + 97 * i, B=Bs, k=ks, alpha=a) for i in range(nsets)]
+                o = torch.empty((Bs, ks + 1), dtype=torch.int32, device=dev)
+                al = torch.empty(Bs, dtype=torch.int32, device=dev)
+                nb = sv.spec_verify_workspace_bytes(sv.MODE_REJECTION, Bs, ks, V)
+                ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+
+                def call(i, Bs=Bs, ks=ks, sets=sets, o=o, al=al, ws=ws, nb=nb):
+                    x = sets[i % len(sets)]
+                    check(lib.spec_verify_rejection(P(x.logits), sv.BF16, P(x.drafts), P(x.q) if ks > 0 else None,
+                                                    Bs, ks, V, 1.0, x.seed, i, P(o), P(al), None, P(ws), nb,
+                                                    P(status), cur()), "spec_verify_rejection")
+
+                if rotate:
+                    ms = graph_time_ms(torch, [lambda i=i: call(i) for i in range(12)], 10)
+                else:
+                    ms = graph_time_ms(torch, [lambda: call(0)], 20, flush=lambda: flush_buf.zero_())
+                nrej = 0
+                for i, x in enumerate(sets):
+                    call(i)
+                    torch.cuda.synchronize()
+                    nrej += rejected_rows(al, ks, x.drafts) if ks > 0 else 0
+                nrej = nrej / len(sets)
+                need = required_bytes(Bs, ks, V, 2, nrej)
+                gbs = need / (ms * 1e-3) / 1e9
+                res[f"sweep_B{Bs}_k{ks}_a{a}"] = {
+                    "B": Bs, "k": ks, "alpha": a, "ms_per_call": ms, "positions_per_s": Bs * (ks + 1) / (ms * 1e-3),
+                    "bytes_required": need, "gbs": gbs, "frac_of_peak": gbs / peak,
+                    "rejected_rows_per_call": nrej, "bytes_all_of_q": all_q,
+                    "gbs_all_of_q": all_q / (ms * 1e-3) / 1e9,
+                    "l2": "3 rotating input sets" if rotate else "L2 flushed before each call",
+                    "launches_per_call": 3 if ks > 0 else 2}
+                del sets, ws
+    return res
 
 
 def _variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak):
@@ -752,20 +1024,24 @@ def run_reference(args, D: Dist):
     from speculative_decoding_verification_verify_gb300 import workloads as wl
 
     oracle.build()
-    inp = wl.chain_b64k7("cpu", seed=1236)
+    # The same inputs as our arm's first input set (drawn on the GPU when there is one, since the
+    # generator's stream differs per device).
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = wl.chain_b64k7(gen_dev, seed=1236 + 7919 * D.rank)
     lg = wl.to_numpy_logits(inp.logits)
-    d = inp.drafts.numpy()
+    d = inp.drafts.cpu().numpy()
 
     import concurrent.futures as cf
 
     threads = os.cpu_count() or 1
     pool = cf.ThreadPoolExecutor(max_workers=threads)
+    groups = [np.arange(B, dtype=np.int32)[g::threads] for g in range(threads)]
+    groups = [g for g in groups if g.size]
 
     def step(s):
-        # One step verifies `threads` requests of the workload, one per host thread.
-        ids = [(s * threads + i) % B for i in range(threads)]
-        list(pool.map(lambda b: oracle.verify_rejection(lg, d, None, 1.0, inp.seed, s,
-                                                        req_ids=np.array([b], np.int32)), ids))
+        # One step verifies the whole batch (B requests), the requests split over the host threads
+        # (the oracle's C code runs without the GIL).
+        list(pool.map(lambda ids: oracle.verify_rejection(lg, d, None, 1.0, inp.seed, s, req_ids=ids), groups))
 
     for w in range(args.warmup):
         step(w)
@@ -774,17 +1050,18 @@ def run_reference(args, D: Dist):
         step(args.warmup + s)
     el = time.perf_counter() - t0
     pool.shutdown()
-    value = (K_DRAFTS + 1) * threads * args.steps / el
+    value = B * (K_DRAFTS + 1) * args.steps / el
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": D.world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B, "k": K_DRAFTS, "V": V, "logits": "bf16",
-                   "mode": "target-only (one-hot q)",
-                   "step": f"{threads} requests (8 positions each) of the workload per step, one per host thread"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{args.steps} steps of {threads} requests of the b64k7 workload"},
+                   "mode": "target-only (one-hot q)", "positions_per_step": B * (K_DRAFTS + 1),
+                   "step": f"the whole batch of {B} requests per step, split over {len(groups)} host threads"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(groups), "kind": "oracle",
+                         "sample": f"{args.steps} steps, each the whole b64k7 batch ({B} requests, "
+                                   f"{B * (K_DRAFTS + 1)} positions)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
