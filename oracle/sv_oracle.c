@@ -66,7 +66,7 @@
  *     largest logit (ties at the boundary all kept; k <= 0 or k >= V: off); top-p then keeps,
  *     among those, the fewest whole value levels from the top whose probability (renormalised
  *     over the top-k set) reaches top_p (top_p >= 1: off); p is renormalised over what is kept.
- *     A top-p crossing within 1e-4 (relative) of its target is flagged as a boundary case.
+ *     A top-p crossing within 1e-6 (relative) of its target is flagged as a boundary case.
  *   - Per-request temperature in one batch ("The speculative decoding zoo", DSpark section:
  *     accept_draft_tokens runs the greedy rule when the whole batch is greedy, the sampling rule
  *     when none is, and both, merged, when the batch is mixed): request b uses T_b; T_b = 0
@@ -194,7 +194,7 @@ int svo_softmax_row(const void *logits, int dtype, int64_t row, int64_t V, doubl
 }
 
 /* Top-k then top-p on a row's probabilities p (from the logits of `row`), in place: zero what
- * is not kept, renormalise.  Sets *boundary when a top-p decision is within 1e-4 of its target. */
+ * is not kept, renormalise.  Sets *boundary when a top-p decision is within 1e-6 of its target. */
 static int svo_cmp_desc(const void *a, const void *b)
 {
     double x = *(const double *)a, y = *(const double *)b;
@@ -232,7 +232,7 @@ int svo_filter_row(const void *logits, int dtype, int64_t row, int64_t V, int to
             while (i < V && srt[i] == level) ++i;
             double before = cum;
             cum += m;
-            if (fabs(cum - target) < 1e-4 * zk || fabs(before - target) < 1e-4 * zk) *boundary = 1;
+            if (fabs(cum - target) < 1e-6 * zk || fabs(before - target) < 1e-6 * zk) *boundary = 1;
             if (cum >= target) {
                 taup = level;
                 break;

@@ -61,10 +61,10 @@ __device__ __forceinline__ void vec_weights_plain(const uint4 &w, int col, int c
     }
 }
 
-// Rounds of the rescan: thread t weighs vectors t, t + nt, t + 2 nt of the range.
-constexpr int RESCAN_ROUNDS = 3;
+// Rounds of the rescan: thread t weighs vectors t, t + nt, ... of the range.
+constexpr int RESCAN_ROUNDS = (RESCAN_RANGE_VEC + 255) / 256;
 constexpr int RESCAN_THREADS = 256;  // the finalising CTA's size, which the rounds assume
-static_assert(RESCAN_ROUNDS * RESCAN_THREADS >= RESCAN_RANGE_VEC, "three rounds cover the range");
+static_assert(RESCAN_ROUNDS * RESCAN_THREADS >= RESCAN_RANGE_VEC, "the rounds cover the range");
 
 struct RescanSmem {
     float wsum[RESCAN_ROUNDS * 8];  // per (round, warp) totals

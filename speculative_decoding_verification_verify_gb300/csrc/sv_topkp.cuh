@@ -11,7 +11,8 @@
 // digits: 2 levels for bf16, 4 for fp32): at each level a pass over the row (16-byte loads)
 // histograms the next digit of the keys that match the chosen prefix (counts for top-k, masses
 // 2^((l - max) * cs) for top-p) in per-warp shared-memory copies, and one warp walks the bins
-// from the top.
+// from the top.  The masses are fp32 terms summed in fp64, so a row's top-p crossing is placed
+// within about 2e-7 of its mass (the terms' own error) whatever the row's length.
 #pragma once
 
 #include "sv_device.cuh"
@@ -95,37 +96,37 @@ struct KeyOf<float> {
 
 struct TopkpSmem {
     int cnt[TK_BINS];
-    float mass[TK_BINS];
+    double mass[TK_BINS];
     union {                          // per-warp histograms of one pass, merged into cnt / mass
         int wcnt[TK_WARPS][TK_BINS];
-        float wmass[TK_WARPS][TK_BINS];
+        double wmass[TK_WARPS][TK_BINS];
     };
     float wmax[NT_TK / 32];
-    int sel;          // chosen digit
-    int above_cnt;    // count in bins above it
-    float above_mass; // mass in bins above it
+    int sel;           // chosen digit
+    int above_cnt;     // count in bins above it
+    double above_mass; // mass in bins above it
 };
 
 // One warp: the bins [0, nb) from the top; the first bin where the running count reaches `rank`
 // (by_mass false) or the running mass reaches `target` (by_mass true).  Sets S.sel and the
 // totals above it; when nothing reaches (rounding), the lowest non-empty bin.
-__device__ __forceinline__ void walk_bins(TopkpSmem &S, int nb, bool by_mass, int rank, float target, int lane)
+__device__ __forceinline__ void walk_bins(TopkpSmem &S, int nb, bool by_mass, int rank, double target, int lane)
 {
     const int per = nb / 32;  // nb is 256
     // Lane l takes bins [nb - (l + 1) * per, nb - l * per), the top bins first.
     const int hi = nb - lane * per;
-    float m = 0.f;
+    double m = 0.0;
     int c = 0;
     for (int i = hi - 1; i >= hi - per; --i) {
         m += S.mass[i];
         c += S.cnt[i];
     }
-    const bool ne = by_mass ? m > 0.f : c > 0;
-    float mi = m;
+    const bool ne = by_mass ? m > 0.0 : c > 0;
+    double mi = m;
     int ci = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const float ym = __shfl_up_sync(0xffffffffu, mi, o);
+        const double ym = __shfl_up_sync(0xffffffffu, mi, o);
         const int yc = __shfl_up_sync(0xffffffffu, ci, o);
         if (lane >= o) {
             mi += ym;
@@ -137,13 +138,13 @@ __device__ __forceinline__ void walk_bins(TopkpSmem &S, int nb, bool by_mass, in
     const unsigned nonempty = __ballot_sync(0xffffffffu, ne);
     const int who = hit ? __ffs(hit) - 1 : (nonempty ? 31 - __clz(nonempty) : 31);
     if (lane == who) {
-        float am = mi - m;
+        double am = mi - m;
         int ac = ci - c;
         int sel = -1, lastne = hi - per;
-        float lm = am;
+        double lm = am;
         int lc = ac;
         for (int i = hi - 1; i >= hi - per; --i) {
-            const bool bne = by_mass ? S.mass[i] > 0.f : S.cnt[i] > 0;
+            const bool bne = by_mass ? S.mass[i] > 0.0 : S.cnt[i] > 0;
             if (bne) {
                 if (hit && (by_mass ? am + S.mass[i] >= target : ac + S.cnt[i] >= rank)) {
                     sel = i;
@@ -222,7 +223,10 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
     const int sh = KeyOf<T>::shift(lvl);
     const int top = sh + 8;
     const int warp = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < TK_WARPS * TK_BINS; i += NT_TK) (&S.wcnt[0][0])[i] = 0;
+    if (MASS)
+        for (int i = threadIdx.x; i < TK_WARPS * TK_BINS; i += NT_TK) (&S.wmass[0][0])[i] = 0.0;
+    else
+        for (int i = threadIdx.x; i < TK_WARPS * TK_BINS; i += NT_TK) (&S.wcnt[0][0])[i] = 0;
     __syncthreads();
     // The skip bound: the value of the smallest key that can be counted, when it lies above the
     // key of -inf (a NaN-free row's keys lie between those of -inf and +inf).
@@ -233,7 +237,7 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
     auto visit = [&](uint32_t k) {
         if ((top >= 32 || (k >> top) == (prefix >> top)) && k >= floor_key) {
             const int d = (int)((k >> sh) & 0xffu);
-            if (MASS) atomicAdd(&S.wmass[warp][d], ex2((KeyOf<T>::value(k) - mx) * cs));
+            if (MASS) atomicAdd(&S.wmass[warp][d], (double)ex2((KeyOf<T>::value(k) - mx) * cs));
             else atomicAdd(&S.wcnt[warp][d], 1);
         }
     };
@@ -243,7 +247,7 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
     __syncthreads();
     for (int i = threadIdx.x; i < TK_BINS; i += NT_TK) {
         int c = 0;
-        float m = 0.f;
+        double m = 0.0;
         if (MASS)
             for (int w = 0; w < TK_WARPS; ++w) m += S.wmass[w][i];
         else
@@ -296,7 +300,7 @@ __device__ void topkp_row(const Params &P, int64_t r, TopkpSmem &S)
         uint32_t prefix = 0u;
         for (int lvl = 0; lvl < LV; ++lvl) {
             if (lvl > 0) key_histogram<T, false>(row, rowflat, V, P.mis, prefix, lvl, 0u, mx, cs, S);
-            if (warp == 0) walk_bins(S, TK_BINS, false, rank, 0.f, lane);
+            if (warp == 0) walk_bins(S, TK_BINS, false, rank, 0.0, lane);
             __syncthreads();
             prefix |= (uint32_t)S.sel << KeyOf<T>::shift(lvl);
             rank -= S.above_cnt;
@@ -308,20 +312,20 @@ __device__ void topkp_row(const Params &P, int64_t r, TopkpSmem &S)
     if (use_p) {
         // Top-p within the top-k set: the fewest value levels from the top holding top_p of its
         // mass; the top digit's mass histogram over the set also gives the set's total.
-        float target = 0.f;
+        double target = 0.0;
         uint32_t prefix = 0u;
         for (int lvl = 0; lvl < LV; ++lvl) {
             key_histogram<T, true>(row, rowflat, V, P.mis, prefix, lvl, kkey, mx, cs, S);
             if (lvl == 0) {
                 if (warp == 0) {
-                    float z = 0.f;
+                    double z = 0.0;
                     for (int i = lane; i < TK_BINS; i += 32) z += S.mass[i];
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
                     if (lane == 0) S.above_mass = z;
                 }
                 __syncthreads();
-                target = pp * S.above_mass;
+                target = (double)pp * S.above_mass;
                 __syncthreads();
             }
             if (warp == 0) walk_bins(S, TK_BINS, true, 0, target, lane);

@@ -42,14 +42,19 @@ def _req_sample(B, n, seed=0):
 
 
 def _compare(gpu_tokens, gpu_len, ref, ids, extra=None):
+    """Exact agreement outside the oracle's boundary draws.  A draw is flagged when its uniform lies
+    within 1e-6 of a decision boundary (for a draw, 1e-6 * Z of its token's interval); at
+    V = 128256 that is a tenth of an average token's mass, so about one draw in twenty is flagged.
+    The GPU decides in fp32, about 1e-7 * Z from the exact boundary, so flagged draws must still
+    agree almost always."""
     gt, gl = _np(gpu_tokens)[ids], _np(gpu_len)[ids]
     flagged = ref.get("boundary", np.zeros(len(ids), np.int32)).astype(bool)
-    ok = ~flagged
-    np.testing.assert_array_equal(gl[ok], ref["accept_len"][ok])
-    np.testing.assert_array_equal(gt[ok], ref["out_tokens"][ok])
+    differ = (gl != ref["accept_len"]) | (gt != ref["out_tokens"]).any(1)
     if extra is not None:
-        np.testing.assert_array_equal(_np(extra[0])[ids][ok], ref[extra[1]][ok])
-    assert flagged.sum() <= max(2, len(ids) // 100), f"{flagged.sum()} boundary draws"
+        differ |= (_np(extra[0])[ids] != ref[extra[1]]).any(1)
+    assert not (differ & ~flagged).any(), f"requests {np.flatnonzero(differ & ~flagged)} differ outside the boundary"
+    assert (differ & flagged).sum() <= max(1, len(ids) // 50), f"{(differ & flagged).sum()} flagged requests differ"
+    assert flagged.sum() <= max(2, len(ids) // 6), f"{flagged.sum()} of {len(ids)} requests flagged"
     return int(flagged.sum())
 
 
@@ -209,14 +214,13 @@ def test_greedy_ties_lowest_index():
 
 
 # --------------------------------------------------------------------------------------------
-# Full-size configurations (sampled requests for the oracle)
+# Full-size configurations, every request compared with the oracle
 # --------------------------------------------------------------------------------------------
 def test_full_b64k7_onehot():
     inp = wl.chain_b64k7(DEV)
-    ids = _req_sample(64, 10)
     for off in (0, 1):
-        run_chain(inp, "onehot", offset=off, ids=ids)
-    run_chain(inp, "greedy", ids=ids)
+        run_chain(inp, "onehot", offset=off)
+    run_chain(inp, "greedy")
 
 
 def test_full_b1k3_standard():
@@ -228,9 +232,8 @@ def test_full_b1k3_standard():
 @pytest.mark.parametrize("mode", [0, 1])
 def test_full_tree(mode):
     inp = wl.tree_b48(DEV)
-    ids = _req_sample(48, 10)
     for off in (0, 1):
-        run_tree(inp, mode, offset=off, ids=ids)
+        run_tree(inp, mode, offset=off)
 
 
 def test_sweep_cells_sampled():
@@ -239,10 +242,90 @@ def test_sweep_cells_sampled():
         run_chain(inp, "standard", ids=_req_sample(B, 4))
 
 
-def test_sweep_largest_cell_sampled():
-    # The sweep's largest cell (B=512, k=7, 1.05 GB of logits and 1.84 GB of q), sampled.
+def test_sweep_largest_cell():
+    # The sweep's largest cell (B=512, k=7, 1.05 GB of logits and 1.84 GB of q), every request.
     inp = wl.chain_sweep(DEV, B=512, k=7, alpha=0.35)
-    run_chain(inp, "standard", ids=_req_sample(512, 6, seed=3))
+    run_chain(inp, "standard")
+
+
+def _stops_at(B, k, V, stops, seed, T=1.0, dtype=torch.bfloat16):
+    """A chain whose round stops at row stops[b] of request b (almost surely): logits ~N(0, 3^2);
+    on each row before the stop the draft sits on a token raised 40 above the row's maximum
+    (accepted with p(x) ~ 1), at the stop row the draft is a uniform token of an untouched row
+    (rejected with probability ~1, and the draw there lands anywhere in the row); stops[b] = k
+    gives the bonus row.  Drafts after the stop are uniform."""
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    x = torch.randn((B, k + 1, V), generator=g, device=DEV) * 3.0
+    drafts = torch.randint(0, V, (B, k), generator=g, device=DEV)
+    top = x.max(dim=-1).values
+    for b in range(B):
+        for i in range(min(int(stops[b]), k)):
+            x[b, i, drafts[b, i]] = top[b, i] + 40.0
+    return wl.ChainInputs("stops_at", x.to(dtype).contiguous(), drafts.int().contiguous(), None, T, seed)
+
+
+def test_onehot_stops_at_every_row_large_vocab():
+    # V = 128256, k = 7: requests stopping at each row 0..6 and at the bonus row 7, so the stop
+    # row's draw (locate + rescan of a 32-record row) runs at every row of the finaliser.
+    k, V = 7, 128256
+    stops = np.array([0, 1, 2, 3, 4, 5, 6, 7, 3, 7, 0, 5], np.int64)
+    inp = _stops_at(len(stops), k, V, stops, 501)
+    for off in (0, 1):
+        r, ref = run_chain(inp, "onehot", offset=off)
+        np.testing.assert_array_equal(ref["accept_len"], stops)
+
+
+@pytest.mark.parametrize("k", [12, 40])
+def test_long_chains_large_vocab(k):
+    # Stop rows at and beyond the finaliser's eighth warp (rows loop) on 32-record rows, in every
+    # chain mode: one-hot, greedy, block (one-hot and with draft probabilities), standard.
+    V = 128256
+    stops = np.array([0, 8, 9, k - 1, k, 11 if k > 11 else 3], np.int64)
+    inp = _stops_at(len(stops), k, V, stops, 600 + k)
+    r, ref = run_chain(inp, "onehot")
+    np.testing.assert_array_equal(ref["accept_len"], stops)
+    run_chain(inp, "greedy")
+    lg, d = wl.to_numpy_logits(inp.logits), _np(inp.drafts)
+    b = sv.spec_verify_block(inp.logits, inp.drafts, None, temperature=1.0, seed=inp.seed, offset=0)
+    _compare(b.out_tokens, b.accept_len, oracle.verify_block(lg, d, None, 1.0, inp.seed, 0),
+             np.arange(len(stops), dtype=np.int32))
+    q_inp = wl.chain_sweep(DEV, B=3, k=k, V=V, alpha=0.9)
+    run_chain(q_inp, "standard")
+    qlg, qd, qq = wl.to_numpy_logits(q_inp.logits), _np(q_inp.drafts), _np(q_inp.q)
+    b = sv.spec_verify_block(q_inp.logits, q_inp.drafts, q_inp.q, temperature=1.0, seed=q_inp.seed, offset=0)
+    _compare(b.out_tokens, b.accept_len, oracle.verify_block(qlg, qd, qq, 1.0, q_inp.seed, 0),
+             np.arange(3, dtype=np.int32))
+
+
+def _deep_path_tree(B, N, V, topk, steps, seed):
+    """A tree_b48-shaped random tree per request whose deepest root-to-leaf path is made
+    dominant: on that path each node's token is raised 40 above its parent row's maximum, so the
+    target-only and greedy walks follow it to its leaf (the last node on it ends the walk)."""
+    t = wl.tree_b48(DEV, B=B, N=N, V=V, topk=topk, steps=steps, seed=seed)
+    x = t.logits.float()
+    pa = _np(t.parents)
+    tok = _np(t.node_tokens)
+    top = x.max(dim=-1).values
+    for b in range(B):
+        depth = np.zeros(N, np.int64)
+        for j in range(1, N):
+            depth[j] = depth[pa[b, j]] + 1
+        leaf = int(np.argmax(depth))
+        node = leaf
+        while node > 0:
+            x[b, pa[b, node], int(tok[b, node])] = top[b, pa[b, node]] + 40.0
+            node = int(pa[b, node])
+    return wl.TreeInputs("deep_path", x.to(torch.bfloat16).contiguous(), t.node_tokens, t.parents, 1.0, seed + 17)
+
+
+@pytest.mark.parametrize("N,topk,steps", [(16, 4, 15), (64, 3, 40)])
+def test_trees_large_vocab_deep_stops(N, topk, steps):
+    # Rows 8 and up are each warp's second row in the finaliser: the walks stop at such nodes.
+    inp = _deep_path_tree(4, N, 151936, topk, steps, 700 + N)
+    for mode in (0, 1):
+        r, ref = run_tree(inp, mode)
+        last = ref["accept_index"][np.arange(4), ref["accept_len"]]
+        assert int(last.max()) >= 8, (ref["accept_len"], last)
 
 
 def _dominant_chain(B, k, V, T, seed, hit):

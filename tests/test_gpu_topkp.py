@@ -12,6 +12,7 @@ from speculative_decoding_verification_verify_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
+PROB_RTOL = 1e-5
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -47,22 +48,25 @@ def run_chain(inp, tk, tp, with_q=False, temps=None, T=1.0, offset=0):
     torch.cuda.synchronize()
     _compare(_np(r.out_tokens), _np(r.accept_len), ref)
     assert int(_np(r.dev_status)[0]) == int(ref["status"].max())
-    got = _np(op)
+    got = _np(op).astype(np.float64)
     for b in np.flatnonzero(~ref["boundary"].astype(bool)):
-        np.testing.assert_allclose(got[b], ref["out_probs"][b], rtol=1e-4, atol=1e-6)
+        r = ref["out_probs"][b]
+        big = np.abs(r) > 1e-30
+        rel = np.abs(got[b][big] - r[big]) / np.abs(r[big])
+        assert rel.size == 0 or rel.max() < PROB_RTOL, (b, rel.max())
+        assert np.all(np.abs(got[b][~big]) < 1e-29)
     return ref
 
 
 def _compare(tokens, alen, ref, extra=()):
-    """Every request must match, except flagged ones (a top-p crossing within 1e-4 of a value
-    level, or a uniform within 1e-6 of a decision); a one-level difference in a top-p threshold
-    moves only a sliver of mass, so even flagged requests must rarely differ."""
+    """Every request must match, except flagged ones (a top-p crossing within 1e-6 of its mass from
+    a value level's edge, or a uniform within 1e-6 of a decision), which must stay rare."""
     flagged = ref["boundary"].astype(bool)
     differ = (tokens != ref["out_tokens"]).any(1) | (alen != ref["accept_len"])
     for g, key in extra:
         differ |= (g != ref[key]).any(1)
     assert not (differ & ~flagged).any(), f"unflagged mismatches at {np.flatnonzero(differ & ~flagged)}"
-    assert differ.sum() <= max(1, len(alen) // 20), f"{differ.sum()} of {len(alen)} requests differ"
+    assert flagged.sum() <= max(2, len(alen) // 100), f"{flagged.sum()} of {len(alen)} requests flagged"
 
 
 @pytest.mark.parametrize("V", [1031, 9001, 128256])
