@@ -306,6 +306,20 @@ int spec_verify_philox(uint64_t seed, uint64_t offset, int n_slot, int n_req, ui
                        void *stream);
 
 /*
+ * Range checks of a debug build.  Compiled with -DSV_DEBUG, every kernel checks the index of each
+ * global-memory access against the extent of the array it falls in (the inputs as sized by the
+ * call's arguments, the outputs, the workspace); an index out of range is skipped, not followed,
+ * and the first one is recorded.  This reads and clears that record: *fault = 0 when every access
+ * was in range, else bit 63 set, the check's site number in bits 48..62 and the low 48 bits of the
+ * offending index.  A release build makes no checks and always reports 0.  Synchronous: it
+ * copies the record from the device (after the work already enqueued on the legacy default
+ * stream; synchronise other streams first).  Returns SPEC_VERIFY_OK, SPEC_VERIFY_EINVAL for a
+ * NULL fault, or SPEC_VERIFY_ECUDA.  Not a part of the pages' method: a test aid that stands in
+ * for a memory checker.
+ */
+int spec_verify_debug_fault(uint64_t *fault);
+
+/*
  * Allocation-free variant of spec_verify_rejection.  The pages have no counterpart: this entry
  * point exists for callers that cannot allocate device memory when they verify (a step running
  * under an allocator that forbids new allocations, an engine whose device memory is owned by

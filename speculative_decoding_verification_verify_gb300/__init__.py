@@ -13,8 +13,10 @@ from .binding import (  # noqa: F401
     Options,
     Result,
     SpecVerifyError,
+    load_debug_library,
     load_library,
     spec_verify_block,
+    spec_verify_debug_fault,
     spec_verify_greedy,
     spec_verify_kv_compact,
     spec_verify_philox,
@@ -25,4 +27,5 @@ from .binding import (  # noqa: F401
     spec_verify_tree,
     spec_verify_tree_ex,
     spec_verify_workspace_bytes,
+    using_library,
 )

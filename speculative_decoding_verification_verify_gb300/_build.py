@@ -9,8 +9,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libspecverify.so")
+DEBUG_LIB_PATH = os.path.join(PKG, "libspecverify_debug.so")  # range-checked build (-DSV_DEBUG)
 SOURCES = [os.path.join(CSRC, f) for f in ("spec_verify.cu", "sv_kv.cu", "sv_budget.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("sv_device.cuh", "sv_draw.cuh", "sv_stream.cuh", "sv_rescan.cuh", "sv_decide.cuh", "sv_topkp.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("sv_device.cuh", "sv_draw.cuh", "sv_stream.cuh", "sv_rescan.cuh",
+                                                  "sv_decide.cuh", "sv_topkp.cuh", "sv_check.cuh")] + [
     os.path.join(INCLUDE, "spec_verify.h")]
 
 NVCC_FLAGS = [
@@ -20,37 +22,47 @@ NVCC_FLAGS = [
 ]
 
 
-def nvcc_command(out: str = LIB_PATH) -> list[str]:
+def nvcc_command(out: str = LIB_PATH, debug: bool = False) -> list[str]:
     nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
     if not os.path.exists(nvcc):
         nvcc = "nvcc"
-    return [nvcc, *NVCC_FLAGS, "-I", INCLUDE, *SOURCES, "-o", out]
+    return [nvcc, *NVCC_FLAGS, *(["-DSV_DEBUG"] if debug else []), "-I", INCLUDE, *SOURCES, "-o", out]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(d) <= t for d in DEPS)
 
 
-def start_build(force: bool = False):
-    """Start nvcc in the background; returns the Popen (or None when already built)."""
-    if not force and up_to_date():
+def start_build(force: bool = False, debug: bool = False):
+    """Start nvcc in the background; returns the Popen (or None when already built).  debug: the
+    range-checked library (libspecverify_debug.so) instead of the release one."""
+    path = DEBUG_LIB_PATH if debug else LIB_PATH
+    if not force and up_to_date(path):
         return None
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    proc = subprocess.Popen(nvcc_command(tmp))
-    proc._sv_tmp = tmp  # type: ignore[attr-defined]
+    tmp = path + f".tmp{os.getpid()}"
+    proc = subprocess.Popen(nvcc_command(tmp, debug))
+    proc._sv_tmp, proc._sv_path = tmp, path  # type: ignore[attr-defined]
     return proc
 
 
 def finish_build(proc) -> str:
-    if proc is not None:
-        if proc.wait() != 0:
-            raise RuntimeError("nvcc failed building libspecverify.so")
-        os.replace(proc._sv_tmp, LIB_PATH)  # type: ignore[attr-defined]
-    return LIB_PATH
+    if proc is None:
+        return LIB_PATH
+    if proc.wait() != 0:
+        raise RuntimeError(f"nvcc failed building {os.path.basename(proc._sv_path)}")  # type: ignore[attr-defined]
+    os.replace(proc._sv_tmp, proc._sv_path)  # type: ignore[attr-defined]
+    return proc._sv_path  # type: ignore[attr-defined]
 
 
 def build(force: bool = False) -> str:
-    return finish_build(start_build(force))
+    finish_build(start_build(force))
+    return LIB_PATH
+
+
+def build_debug(force: bool = False) -> str:
+    """The range-checked library: every global-memory access of every kernel checked (-DSV_DEBUG)."""
+    finish_build(start_build(force, debug=True))
+    return DEBUG_LIB_PATH

@@ -7,6 +7,7 @@ fallback: if the library is not built or no GPU is present, these functions rais
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -39,6 +40,49 @@ def library_path() -> str:
     return _build.LIB_PATH
 
 
+def _declare(lib):
+    """Argument and result types of every entry point of include/spec_verify.h."""
+    vp, i32, u64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_float,
+                             ctypes.c_size_t)
+    lib.spec_verify_greedy.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp, vp, sz, vp, vp]
+    lib.spec_verify_greedy.restype = i32
+    lib.spec_verify_rejection.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, u64, u64, vp,
+                                          vp, vp, vp, sz, vp, vp]
+    lib.spec_verify_rejection.restype = i32
+    lib.spec_verify_block.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp,
+                                      vp, sz, vp, vp]
+    lib.spec_verify_block.restype = i32
+    lib.spec_verify_tree.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, f32, u64, u64, vp,
+                                     vp, vp, vp, sz, vp, vp]
+    lib.spec_verify_tree.restype = i32
+    lib.spec_verify_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.spec_verify_workspace_bytes.restype = sz
+    lib.spec_verify_strerror.argtypes = [i32]
+    lib.spec_verify_strerror.restype = ctypes.c_char_p
+    lib.spec_verify_philox.argtypes = [u64, u64, i32, i32, vp, vp]
+    lib.spec_verify_philox.restype = i32
+    lib.spec_verify_rejection_noalloc.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, u64,
+                                                  u64, vp, vp, vp, vp, vp]
+    lib.spec_verify_rejection_noalloc.restype = i32
+    lib.spec_verify_kv_compact.argtypes = [vp, ctypes.c_int64, sz, i32, sz, vp, i32, vp, vp,
+                                           vp, vp, i32, i32, vp, vp]
+    lib.spec_verify_kv_compact.restype = i32
+    OP = ctypes.POINTER(Options)
+    lib.spec_verify_rejection_ex.argtypes = [vp, i32, vp, vp, i32, i32, i32, OP, u64, u64, vp,
+                                             vp, vp, vp, sz, vp, vp]
+    lib.spec_verify_rejection_ex.restype = i32
+    lib.spec_verify_tree_ex.argtypes = [vp, i32, vp, vp, i32, i32, i32, OP, u64, u64, vp, vp,
+                                        vp, vp, sz, vp, vp]
+    lib.spec_verify_tree_ex.restype = i32
+    lib.spec_verify_plan_budget.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.spec_verify_plan_budget.restype = i32
+    lib.spec_verify_plan_budget_workspace_bytes.argtypes = [i32, i32]
+    lib.spec_verify_plan_budget_workspace_bytes.restype = sz
+    lib.spec_verify_debug_fault.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+    lib.spec_verify_debug_fault.restype = i32
+    return lib
+
+
 def load_library():
     """Load libspecverify.so (in-tree).  Raises when it has not been built."""
     global _lib
@@ -49,45 +93,38 @@ def load_library():
         if not os.path.exists(path):
             raise RuntimeError(
                 f"{path} is missing: build it with __graft_entry__.build() (nvcc, sm_103a)")
-        lib = ctypes.CDLL(path)
-        vp, i32, u64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_float,
-                                 ctypes.c_size_t)
-        lib.spec_verify_greedy.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp, vp, sz, vp, vp]
-        lib.spec_verify_greedy.restype = i32
-        lib.spec_verify_rejection.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, u64, u64, vp,
-                                              vp, vp, vp, sz, vp, vp]
-        lib.spec_verify_rejection.restype = i32
-        lib.spec_verify_block.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp,
-                                          vp, sz, vp, vp]
-        lib.spec_verify_block.restype = i32
-        lib.spec_verify_tree.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, f32, u64, u64, vp,
-                                         vp, vp, vp, sz, vp, vp]
-        lib.spec_verify_tree.restype = i32
-        lib.spec_verify_workspace_bytes.argtypes = [i32, i32, i32, i32]
-        lib.spec_verify_workspace_bytes.restype = sz
-        lib.spec_verify_strerror.argtypes = [i32]
-        lib.spec_verify_strerror.restype = ctypes.c_char_p
-        lib.spec_verify_philox.argtypes = [u64, u64, i32, i32, vp, vp]
-        lib.spec_verify_philox.restype = i32
-        lib.spec_verify_rejection_noalloc.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, u64,
-                                                      u64, vp, vp, vp, vp, vp]
-        lib.spec_verify_rejection_noalloc.restype = i32
-        lib.spec_verify_kv_compact.argtypes = [vp, ctypes.c_int64, sz, i32, sz, vp, i32, vp, vp,
-                                               vp, vp, i32, i32, vp, vp]
-        lib.spec_verify_kv_compact.restype = i32
-        OP = ctypes.POINTER(Options)
-        lib.spec_verify_rejection_ex.argtypes = [vp, i32, vp, vp, i32, i32, i32, OP, u64, u64, vp,
-                                                 vp, vp, vp, sz, vp, vp]
-        lib.spec_verify_rejection_ex.restype = i32
-        lib.spec_verify_tree_ex.argtypes = [vp, i32, vp, vp, i32, i32, i32, OP, u64, u64, vp, vp,
-                                            vp, vp, sz, vp, vp]
-        lib.spec_verify_tree_ex.restype = i32
-        lib.spec_verify_plan_budget.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, sz, vp]
-        lib.spec_verify_plan_budget.restype = i32
-        lib.spec_verify_plan_budget_workspace_bytes.argtypes = [i32, i32]
-        lib.spec_verify_plan_budget_workspace_bytes.restype = sz
-        _lib = lib
-        return lib
+        _lib = _declare(ctypes.CDLL(path))
+        return _lib
+
+
+def load_debug_library():
+    """The range-checked build (libspecverify_debug.so, compiled on first use): the same entry
+    points, every kernel's global-memory indices checked (spec_verify_debug_fault reports)."""
+    return _declare(ctypes.CDLL(_build.build_debug()))
+
+
+@contextlib.contextmanager
+def using_library(lib):
+    """Route this module's wrappers through another build of the library (e.g. the debug one)."""
+    global _lib
+    load_library()
+    with _lock:
+        prev, _lib = _lib, lib
+    try:
+        yield lib
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def spec_verify_debug_fault(lib=None) -> int:
+    """The first out-of-range index recorded by a debug build since the last read (0: none)."""
+    lib = lib or load_library()
+    w = ctypes.c_uint64(0)
+    rc = lib.spec_verify_debug_fault(ctypes.byref(w))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_debug_fault", rc)
+    return int(w.value)
 
 
 def spec_verify_strerror(code: int) -> str:

@@ -115,15 +115,19 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
     const int64_t V = P.V;
     const int64_t rbase = (int64_t)b * rpr;
     for (int n = tid; n < rpr; n += nt) {
-        F.par[n] = n == 0 ? (P.is_tree ? __ldg(P.parents + rbase) : -1) : node_parent(P, b, n);
+        F.par[n] = n == 0 ? (P.is_tree && SV_INB(rbase, (int64_t)P.B * rpr, 301) ? __ldg(P.parents + rbase) : -1)
+                          : node_parent(P, b, n);
         F.tok[n] = n == 0 ? -1 : node_token(P, b, n);
         float qv = 1.f;
         if (SAMPLE && P.q && n >= 1 && n <= P.k) {
             const int x = F.tok[n];
-            if (x >= 0 && (int64_t)x < V) qv = __ldg(P.q + ((int64_t)b * P.k + (n - 1)) * V + x);
+            const int64_t qi = ((int64_t)b * P.k + (n - 1)) * V + x;
+            if (x >= 0 && (int64_t)x < V && SV_INB(qi, (int64_t)P.B * P.k * V, 302)) qv = __ldg(P.q + qi);
         }
         F.qx[n] = qv;
-        if (VAR) F.thr[n] = P.top_k || P.top_p ? __ldcg(P.thr + rbase + n) : NEG_INF;
+        if (VAR)
+            F.thr[n] = (P.top_k || P.top_p) && SV_INB(rbase + n, (int64_t)P.B * rpr, 303) ? __ldcg(P.thr + rbase + n)
+                                                                                          : NEG_INF;
         if (SAMPLE) {
             const float2 uv = uniforms(P, (uint32_t)n, (uint32_t)b);
             F.u[n] = uv.x;
@@ -135,7 +139,7 @@ __device__ void stage_request(const Params &P, int b, FinSmem &F)
     }
     if (tid == 0) {
         F.status = 0;
-        if (VAR) F.cs = P.temps ? cs_of(__ldg(P.temps + b)) : P.cs;
+        if (VAR) F.cs = P.temps && SV_INB(b, P.B, 304) ? cs_of(__ldg(P.temps + b)) : P.cs;
     }
     __syncthreads();
     if (!P.is_tree) {
@@ -243,6 +247,7 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, 
         float best = NEG_INF;
         int idx = INT_MAX;
         for (int t = lane; t < L; t += 32) {
+            if (!SV_INB(base + t, P.nchunks, 305)) continue;
             const float4 rec = __ldcg(P.recs + base + t);
             arg_merge(best, idx, rec.x, __float_as_int(rec.y));
         }
@@ -264,7 +269,8 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, 
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int e = lane + 32 * h;
-        cap[h] = e < cnt ? __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[off + e]) : NEG_INF;
+        const int64_t ci = (int64_t)b * P.rpr + (e < cnt ? F.ex_node[off + e] : 0);
+        cap[h] = e < cnt && SV_INB(ci, (int64_t)P.B * P.rpr, 306) ? __ldcg(P.caps + ci) : NEG_INF;
         if (VAR && !(cap[h] >= F.thr[n])) cap[h] = NEG_INF;  // below the row's top-k / top-p threshold
     }
     const int q = (L + 31) >> 5;
@@ -277,7 +283,8 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, 
 #pragma unroll
         for (int i = 0; i < REC_PER_LANE; ++i) {
             const int t = lane * q + i;
-            rs.rr[i] = (i < q && t < L) ? __ldcg(P.recs + base + t) : make_float4(REF_NONE, 0.f, 0.f, 0.f);
+            rs.rr[i] = (i < q && t < L && SV_INB(base + t, P.nchunks, 307)) ? __ldcg(P.recs + base + t)
+                                                                             : make_float4(REF_NONE, 0.f, 0.f, 0.f);
         }
         // The non-child reference mc (largest record reference) and the children's largest scaled
         // logit, reduced side by side; M covers both, so a child far above every other token
@@ -319,6 +326,7 @@ __device__ void finish_row(const Params &P, int b, int n, FinSmem &F, int lane, 
         rs.incl = incl;
     } else {
         for (int t = lane; t < L; t += 32) {
+            if (!SV_INB(base + t, P.nchunks, 308)) continue;
             const float4 rec = __ldcg(P.recs + base + t);
             rec_merge(mc, s, rec.x, rec.y);
         }
@@ -413,15 +421,16 @@ __device__ void row_draw_prep(const Params &P, int b, int n, FinSmem &F, int lan
         } else {
             Locate Lc;
             for (int c0 = 0; c0 < L; c0 += 32) {
-                const float4 rec = c0 + lane < L ? __ldcg(P.recs + rs.base + c0 + lane)
-                                                 : make_float4(REF_NONE, 0.f, 0.f, 0.f);
+                const float4 rec = c0 + lane < L && SV_INB(rs.base + c0 + lane, P.nchunks, 309)
+                                       ? __ldcg(P.recs + rs.base + c0 + lane)
+                                       : make_float4(REF_NONE, 0.f, 0.f, 0.f);
                 if (locate_chunk(Lc, rec_mass(rec, mc), c0, t, lane)) break;
             }
             if (lane == 0) {
                 fi = Lc.found >= 0 ? Lc.found : Lc.lastpos;
                 before = Lc.found >= 0 ? Lc.before : Lc.lp_before;
                 take_last = Lc.found < 0;
-                if (fi >= 0) frec = __ldcg(P.recs + rs.base + fi);
+                if (fi >= 0 && SV_INB(rs.base + fi, P.nchunks, 310)) frec = __ldcg(P.recs + rs.base + fi);
             }
         }
         if (fi >= 0) {  // exactly one lane holds it
@@ -437,7 +446,8 @@ __device__ void row_draw_prep(const Params &P, int b, int n, FinSmem &F, int lan
         float c = 0.f;
         int lastc = -1, drawn = -1;
         for (int e = 0; e < rs.cnt && drawn < 0; ++e) {
-            const float cp = __ldcg(P.caps + (int64_t)b * P.rpr + F.ex_node[rs.off + e]);
+            const int64_t ci = (int64_t)b * P.rpr + F.ex_node[rs.off + e];
+            const float cp = SV_INB(ci, (int64_t)P.B * P.rpr, 311) ? __ldcg(P.caps + ci) : NEG_INF;
             const float w = (!VAR || cp >= F.thr[n]) ? ex2(fmaf(cp, VAR ? F.cs : P.cs, -rs.M)) : 0.f;
             if (w > 0.f) {
                 lastc = F.ex_col[rs.off + e];
@@ -489,8 +499,10 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F)
         // statistics, so the block kernel decides and draws.  Hand it each present row's
         // reference, total and prefix weight w_L = min(1, w_{L-1} p(x)/q(x)).
         if (faulted) {
-            for (int i = tid; i <= P.k; i += blockDim.x) P.out_tokens[(int64_t)b * (P.k + 1) + i] = -1;
-            if (tid == 0) {
+            for (int i = tid; i <= P.k; i += blockDim.x)
+                if (SV_INB((int64_t)b * (P.k + 1) + i, (int64_t)P.B * (P.k + 1), 320))
+                    P.out_tokens[(int64_t)b * (P.k + 1) + i] = -1;
+            if (tid == 0 && SV_INB(b, P.B, 321)) {
                 P.accept_len[b] = -1;
                 raise_status(P.dev_status, F.status);
                 P.pend[b] = make_int4(-1, 0, 0, 0);
@@ -506,13 +518,14 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F)
                 }
             float w = 1.f;
             for (int L = 0; L <= ke; ++L) {
-                P.bpend[(int64_t)b * rpr + L] = make_float4(F.row_M[L], F.row_tot[L], w, 1.f);
+                if (SV_INB((int64_t)b * rpr + L, (int64_t)P.B * rpr, 322))
+                    P.bpend[(int64_t)b * rpr + L] = make_float4(F.row_M[L], F.row_tot[L], w, 1.f);
                 if (L < ke) {
                     const float px = F.node_p[L + 1], qx = F.qx[L + 1];
                     w = (w * px <= 0.f) ? 0.f : (qx <= 0.f ? 1.f : fminf(1.f, w * px / qx));
                 }
             }
-            P.pend[b] = make_int4(ke, 0, 0, 1);
+            if (SV_INB(b, P.B, 323)) P.pend[b] = make_int4(ke, 0, 0, 1);
         }
         return;
     }
@@ -520,18 +533,21 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F)
     // Outputs.
     const int out_w = P.is_tree ? rpr : P.k + 1;
     int32_t *ot = P.out_tokens + (int64_t)b * out_w;
+    [[maybe_unused]] const int64_t ot_n = (int64_t)P.B * out_w;  // extents for debug builds' range checks
+    [[maybe_unused]] const int64_t op_n = (int64_t)P.B * (P.k + 1) * 3;
     if (faulted) {
         for (int i = tid; i < out_w; i += blockDim.x) {
-            ot[i] = -1;
-            if (P.is_tree) P.accept_index[(int64_t)b * rpr + i] = -1;
+            if (SV_INB((int64_t)b * out_w + i, ot_n, 324)) ot[i] = -1;
+            if (P.is_tree && SV_INB((int64_t)b * rpr + i, ot_n, 325)) P.accept_index[(int64_t)b * rpr + i] = -1;
         }
-        if (tid == 0) {
+        if (tid == 0 && SV_INB(b, P.B, 326)) {
             P.accept_len[b] = -1;
             raise_status(P.dev_status, F.status);
         }
         if (P.out_probs && !P.is_tree)
-            for (int i = tid; i < (P.k + 1) * 3; i += blockDim.x) P.out_probs[(int64_t)b * (P.k + 1) * 3 + i] = 0.f;
-        if (P.q && !P.is_tree && tid == 0) P.pend[b] = make_int4(-1, 0, 0, 0);
+            for (int i = tid; i < (P.k + 1) * 3; i += blockDim.x)
+                if (SV_INB((int64_t)b * (P.k + 1) * 3 + i, op_n, 327)) P.out_probs[(int64_t)b * (P.k + 1) * 3 + i] = 0.f;
+        if (P.q && !P.is_tree && tid == 0 && SV_INB(b, P.B, 328)) P.pend[b] = make_int4(-1, 0, 0, 0);
         return;
     }
     int last = -1;
@@ -544,6 +560,7 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F)
             const int64_t r = (int64_t)b * rpr + stop;
             const T *row = reinterpret_cast<const T *>(P.logits) + r * P.V;
             uint4 w[RESCAN_ROUNDS];
+            if (!(SV_INB(F.rs_c0[stop], P.V + 1, 341) && SV_INB(F.rs_c1[stop], P.V + 1, 342))) F.rs_c1[stop] = F.rs_c0[stop];
             load_range<T>(row, r * P.V, P.total, P.mis, F.rs_c0[stop], F.rs_c1[stop], w);
             drawn = rescan_range<T, VAR>(r * P.V, P.mis, F.rs_c0[stop], F.rs_c1[stop], VAR ? F.cs : P.cs,
                                          F.row_mc[stop], VAR ? F.thr[stop] : NEG_INF, F.rs_t[stop], F.rs_cum[stop],
@@ -555,12 +572,14 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F)
         int v = -1;
         if (i < L) v = F.tok[P.is_tree ? F.path[i] : i + 1];
         else if (i == L) v = last;
-        ot[i] = v;
-        if (P.is_tree) P.accept_index[(int64_t)b * rpr + i] = (i == 0) ? 0 : (i <= L ? F.path[i - 1] : -1);
+        if (SV_INB((int64_t)b * out_w + i, ot_n, 329)) ot[i] = v;
+        if (P.is_tree && SV_INB((int64_t)b * rpr + i, ot_n, 330))
+            P.accept_index[(int64_t)b * rpr + i] = (i == 0) ? 0 : (i <= L ? F.path[i - 1] : -1);
     }
     if (!SAMPLE && P.out_probs && !P.is_tree)  // a greedy request of a mixed batch
-        for (int i = tid; i < (P.k + 1) * 3; i += blockDim.x) P.out_probs[(int64_t)b * (P.k + 1) * 3 + i] = 0.f;
-    if (tid == 0) {
+        for (int i = tid; i < (P.k + 1) * 3; i += blockDim.x)
+            if (SV_INB((int64_t)b * (P.k + 1) * 3 + i, op_n, 331)) P.out_probs[(int64_t)b * (P.k + 1) * 3 + i] = 0.f;
+    if (tid == 0 && SV_INB(b, P.B, 332)) {
         P.accept_len[b] = L;
         if (!SAMPLE && P.q && !P.is_tree) P.pend[b] = make_int4(-1, 0, 0, 0);
         if (SAMPLE && P.q && !P.is_tree) {
@@ -579,6 +598,7 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F)
                 q0 = F.qx[i + 1];
             }
             if (i == stop && mode == 1) z = F.row_z[i];
+            if (!SV_INB((int64_t)b * (P.k + 1) * 3 + 3 * i + 2, op_n, 333)) continue;
             op[3 * i + 0] = p0;
             op[3 * i + 1] = q0;
             op[3 * i + 2] = z;
@@ -625,23 +645,28 @@ __global__ void __launch_bounds__(stream_threads(KIND), 1) sv_stream_kernel(cons
         const Seg sg = chunk_of<VEC>(P, r, j);
         const T *row = reinterpret_cast<const T *>(P.logits) + r * P.V;
         float *caps = P.caps + (int64_t)b * P.rpr;
+        const bool rec_ok = SV_INB(q, P.nchunks, 205);
         if (KIND >= 2) {
             // The request's temperature decides the chunk's fold; nodes, children and the row's
             // threshold are refreshed first (global loads only when the request or row changes).
             if (b != cur_b || n != cur_n) {
                 if (b != cur_b) {
                     load_nodes(P, b, lane, nv);
-                    const float Tb = P.temps ? __ldg(P.temps + b) : 1.f;
+                    const float Tb = P.temps && SV_INB(b, P.B, 206) ? __ldg(P.temps + b) : 1.f;
                     greedy_b = Tb == 0.f;
                     cs = greedy_b ? 1.f : (P.temps ? cs_of(Tb) : P.cs);
                 }
                 kids_of(P, nv, n, kd);
-                if (KIND == 3) thr = __ldcg(P.thr + r);
+                if (KIND == 3) thr = SV_INB(r, (int64_t)P.B * P.rpr, 207) ? __ldcg(P.thr + r) : NEG_INF;
                 cur_b = b;
                 cur_n = n;
             }
-            if (greedy_b) stream_chunk<T, false, false>(row, sg, lane, cs, kd, caps, P.recs + q, []() {}, thr);
-            else stream_chunk<T, true, KIND == 3>(row, sg, lane, cs, kd, caps, P.recs + q, []() {}, thr);
+            if (greedy_b)
+                stream_chunk<T, false, false>(row, sg, lane, cs, kd, caps, P.recs + q, []() {}, thr, r * P.V, P.total,
+                                              P.rpr, rec_ok);
+            else
+                stream_chunk<T, true, KIND == 3>(row, sg, lane, cs, kd, caps, P.recs + q, []() {}, thr, r * P.V,
+                                                 P.total, P.rpr, rec_ok);
         } else {
             // The row's child tokens are (re)derived while the chunk's first loads are in flight.
             stream_chunk<T, SAMPLE, false>(row, sg, lane, cs, kd, caps, P.recs + q, [&]() {
@@ -651,7 +676,7 @@ __global__ void __launch_bounds__(stream_threads(KIND), 1) sv_stream_kernel(cons
                     cur_b = b;
                     cur_n = n;
                 }
-            }, NEG_INF);
+            }, NEG_INF, r * P.V, P.total, P.rpr, rec_ok);
         }
         c = __shfl_sync(0xffffffffu, nxt, 0);
     }
@@ -667,7 +692,7 @@ __global__ void __launch_bounds__(NT_FIN_MAX) sv_finalize_kernel(const Params P)
 {
     __shared__ FinSmem F;
     const int b = (int)blockIdx.x;
-    if (VAR && P.temps && __ldg(P.temps + b) == 0.f) finalize_request<T, false, false>(P, b, F);
+    if (VAR && P.temps && SV_INB(b, P.B, 340) && __ldg(P.temps + b) == 0.f) finalize_request<T, false, false>(P, b, F);
     else finalize_request<T, SAMPLE, VAR>(P, b, F);
 }
 
@@ -791,6 +816,7 @@ __global__ void __launch_bounds__(NT, 4) sv_residual_kernel(const Params P)
     __shared__ int is_last;
     const int c = (int)(blockIdx.x % (unsigned)P.C2), b = (int)(blockIdx.x / (unsigned)P.C2);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (!SV_INB(b, P.B, 501)) return;
     const int4 pd = P.pend[b];
     if (pd.w != 1) return;
     const int j = pd.x;
@@ -799,6 +825,7 @@ __global__ void __launch_bounds__(NT, 4) sv_residual_kernel(const Params P)
     const float cs = P.temps ? cs_of(__ldg(P.temps + b)) : P.cs;
     const int64_t V = P.V;
     const int64_t r = (int64_t)b * P.rpr + j;
+    if (!SV_INB(j, P.k, 502)) return;  // a pending residual draw sits at a draft slot
     const float thr = P.thr && (P.top_k || P.top_p) ? __ldcg(P.thr + r) : NEG_INF;
     const void *row = reinterpret_cast<const T *>(P.logits) + r * V;
     const float *qrow = P.q + ((int64_t)b * P.k + j) * V;
@@ -806,11 +833,15 @@ __global__ void __launch_bounds__(NT, 4) sv_residual_kernel(const Params P)
     const int64_t span = (cc1 - cc0 + NW - 1) / NW;
     const int64_t w0 = min(cc0 + warp * span, cc1), w1 = min(w0 + span, cc1);
     float zr = 0.f, zp = 0.f;
-    resid_sums<T, true>(reinterpret_cast<const T *>(row), qrow, r * V, ((int64_t)b * P.k + j) * V, P.mis,
-                        q_mis(P.q), w0, w1, cs, mc, inv, 1.f, thr, lane, zr, zp);
+    // The warp's columns [w0, w1) of the row and of its q row: both ends in range.
+    if (w1 <= w0 || (SV_INB(r * V + w1 - 1, P.total, 503) && SV_INB(((int64_t)b * P.k + j) * V + w1 - 1,
+                                                                     (int64_t)P.B * P.k * V, 504)))
+        resid_sums<T, true>(reinterpret_cast<const T *>(row), qrow, r * V, ((int64_t)b * P.k + j) * V, P.mis,
+                            q_mis(P.q), w0, w1, cs, mc, inv, 1.f, thr, lane, zr, zp);
     zr = warp_sum(zr);
     zp = warp_sum(zp);
-    if (lane == 0) P.recs2[((int64_t)b * P.C2 + c) * NW + warp] = make_float2(zr, zp);
+    const int64_t ri = ((int64_t)b * P.C2 + c) * NW + warp;
+    if (lane == 0 && SV_INB(ri, (int64_t)P.B * P.C2 * NW, 505)) P.recs2[ri] = make_float2(zr, zp);
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -824,6 +855,7 @@ __global__ void __launch_bounds__(NT, 4) sv_residual_kernel(const Params P)
     // Last CTA: total residual mass, then the crossing record (warp 0), then the rescan.
     const float2 *rb = P.recs2 + (int64_t)b * P.C2 * NW;
     const int L = P.C2 * NW;
+    if (!SV_INB((int64_t)b * P.C2 * NW + L - 1, (int64_t)P.B * P.C2 * NW, 506)) return;
     if (warp == 0) {
         float zr_t = 0.f, zp_t = 0.f;
         for (int t = lane; t < L; t += 32) {
@@ -878,15 +910,17 @@ __global__ void __launch_bounds__(NT, 4) sv_residual_kernel(const Params P)
         const int rc = F.rec / NW, rw = F.rec % NW;
         const int64_t a0 = (int64_t)rc * P.Ec2, a1 = min(a0 + P.Ec2, V);
         const int64_t sp = (a1 - a0 + NW - 1) / NW;
-        const int64_t s0 = min(a0 + rw * sp, a1), s1 = min(s0 + sp, a1);
+        const int64_t s0 = min(a0 + rw * sp, a1), s1 = SV_INB(min(s0 + sp, a1) - 1, V, 507) ? min(s0 + sp, a1) : s0;
         ResidSrc<T> src{row, qrow, s0, s1, cs, mc, inv, F.mode, 1.f, thr};
         draw_init(F.D, F.cum_before);
         draw_span<2>(src, (s1 - s0 + 7) / 8, F.take_last ? POS_INF : F.thresh, F.D);
         drawn = F.D.found >= 0 ? F.D.found : F.D.lastpos;
     }
     if (tid == 0) {
-        P.out_tokens[(int64_t)b * (P.k + 1) + j] = drawn >= 0 ? drawn : 0;
-        if (P.out_probs) P.out_probs[((int64_t)b * (P.k + 1) + j) * 3 + 2] = F.z;
+        if (SV_INB((int64_t)b * (P.k + 1) + j, (int64_t)P.B * (P.k + 1), 508))
+            P.out_tokens[(int64_t)b * (P.k + 1) + j] = drawn >= 0 ? drawn : 0;
+        if (P.out_probs && SV_INB(((int64_t)b * (P.k + 1) + j) * 3 + 2, (int64_t)P.B * (P.k + 1) * 3, 509))
+            P.out_probs[((int64_t)b * (P.k + 1) + j) * 3 + 2] = F.z;
         P.cnt2[b] = 0u;
     }
 }
@@ -918,10 +952,11 @@ __global__ void __launch_bounds__(NT, 4) sv_block_kernel(const Params P)
     const int rest = (int)(blockIdx.x / (unsigned)P.C2);
     const int L = rest % rpr, b = rest / rpr;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (!SV_INB(b, P.B, 601)) return;
     const int4 pd = P.pend[b];
     if (pd.w != 1) return;
     const int ke = pd.x;
-    if (L > ke) return;
+    if (L > ke || !SV_INB(ke, rpr, 602)) return;
     const int64_t V = P.V;
     {
         const float4 bp = P.bpend[(int64_t)b * rpr + L];
@@ -933,11 +968,14 @@ __global__ void __launch_bounds__(NT, 4) sv_block_kernel(const Params P)
         const int64_t span = (cc1 - cc0 + NW - 1) / NW;
         const int64_t w0 = min(cc0 + warp * span, cc1), w1 = min(w0 + span, cc1);
         float zr = 0.f, zp = 0.f;
-        resid_sums<T, false>(reinterpret_cast<const T *>(row), qrow, r * V, ((int64_t)b * P.k + L) * V, P.mis,
-                             q_mis(P.q), w0, w1, P.cs, mc, inv, w, NEG_INF, lane, zr, zp);
+        if (w1 <= w0 || (SV_INB(r * V + w1 - 1, P.total, 603) &&
+                         (!qrow || SV_INB(((int64_t)b * P.k + L) * V + w1 - 1, (int64_t)P.B * P.k * V, 604))))
+            resid_sums<T, false>(reinterpret_cast<const T *>(row), qrow, r * V, ((int64_t)b * P.k + L) * V, P.mis,
+                                 q_mis(P.q), w0, w1, P.cs, mc, inv, w, NEG_INF, lane, zr, zp);
         zr = warp_sum(zr);
         zp = warp_sum(zp);
-        if (lane == 0) P.recs3[(r * P.C2 + c) * NW + warp] = make_float2(zr, zp);
+        if (lane == 0 && SV_INB((r * P.C2 + c) * NW + warp, (int64_t)P.B * rpr * P.C2 * NW, 605))
+            P.recs3[(r * P.C2 + c) * NW + warp] = make_float2(zr, zp);
     }
     __threadfence();
     __syncthreads();
@@ -951,6 +989,7 @@ __global__ void __launch_bounds__(NT, 4) sv_block_kernel(const Params P)
 
     // Last CTA of request b: row masses, the decision, then the draw.
     const int per_row = P.C2 * NW;
+    if (!SV_INB(((int64_t)b * rpr + ke) * per_row + per_row - 1, (int64_t)P.B * rpr * per_row, 606)) return;
     for (int Lr = warp; Lr <= ke; Lr += NW) {
         const float2 *rb = P.recs3 + ((int64_t)b * rpr + Lr) * per_row;
         float a = 0.f, z = 0.f;
@@ -1029,7 +1068,7 @@ __global__ void __launch_bounds__(NT, 4) sv_block_kernel(const Params P)
         const int rc = F.rec / NW, rw = F.rec % NW;
         const int64_t a0 = (int64_t)rc * P.Ec2, a1 = min(a0 + P.Ec2, V);
         const int64_t sp = (a1 - a0 + NW - 1) / NW;
-        const int64_t s0 = min(a0 + rw * sp, a1), s1 = min(s0 + sp, a1);
+        const int64_t s0 = min(a0 + rw * sp, a1), s1 = SV_INB(min(s0 + sp, a1) - 1, V, 607) ? min(s0 + sp, a1) : s0;
         const float4 bp = P.bpend[(int64_t)b * rpr + j];
         const int64_t r = (int64_t)b * rpr + j;
         const void *row = reinterpret_cast<const T *>(P.logits) + r * V;
@@ -1042,9 +1081,9 @@ __global__ void __launch_bounds__(NT, 4) sv_block_kernel(const Params P)
     int32_t *ot = P.out_tokens + (int64_t)b * (P.k + 1);
     for (int i = tid; i <= P.k; i += NT) {
         int v = -1;
-        if (i < j) v = __ldg(P.drafts + (int64_t)b * P.k + i);
+        if (i < j && SV_INB((int64_t)b * P.k + i, (int64_t)P.B * P.k, 608)) v = __ldg(P.drafts + (int64_t)b * P.k + i);
         else if (i == j) v = drawn >= 0 ? drawn : 0;
-        ot[i] = v;
+        if (SV_INB((int64_t)b * (P.k + 1) + i, (int64_t)P.B * (P.k + 1), 609)) ot[i] = v;
     }
     if (tid == 0) {
         P.accept_len[b] = j;
@@ -1575,6 +1614,29 @@ int spec_verify_philox(uint64_t seed, uint64_t offset, int n_slot, int n_req, ui
 }
 
 }  // extern "C"
+
+namespace sv {
+unsigned long long kv_debug_fault();
+unsigned long long budget_debug_fault();
+}  // namespace sv
+
+// The first out-of-range index the kernels met (debug builds), read and cleared across the
+// library's three modules; synchronous (symbol copies).
+extern "C" int spec_verify_debug_fault(uint64_t *fault)
+{
+    if (!fault) return SPEC_VERIFY_EINVAL;
+    unsigned long long w = 0;
+#ifdef SV_DEBUG
+    unsigned long long z = 0;
+    if (cudaMemcpyFromSymbol(&w, sv::g_sv_debug_fault, sizeof w) != cudaSuccess ||
+        cudaMemcpyToSymbol(sv::g_sv_debug_fault, &z, sizeof z) != cudaSuccess)
+        return SPEC_VERIFY_ECUDA;
+#endif
+    const unsigned long long kv = sv::kv_debug_fault(), bu = sv::budget_debug_fault();
+    if (kv == ~0ull || bu == ~0ull) return SPEC_VERIFY_ECUDA;
+    *fault = w ? w : (kv ? kv : bu);
+    return SPEC_VERIFY_OK;
+}
 
 // ---------------------------------------------------------------------------------------------
 // Allocation-free entry point.

@@ -20,6 +20,7 @@
 #include <stdint.h>
 
 #include "spec_verify.h"
+#include "sv_check.cuh"
 
 namespace svb {
 
@@ -40,6 +41,7 @@ __global__ void keys_kernel(const float *conf, const int32_t *num_drafts, int B,
 {
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= B) return;
+    if (!SV_INB((int64_t)r * K + K - 1, (int64_t)B * K, 901)) return;
     for (int i = 0; i < K; ++i) rank[(int64_t)r * K + i] = 0;
     const int nd = num_drafts ? min(max(num_drafts[r], 0), K) : K;
     float run = 1.f;
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(NT_RANK) rank_kernel(const uint64_t *keys, int
 __global__ void scatter_kernel(const uint64_t *keys, const int32_t *rank, int n, uint64_t *sorted)
 {
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
-    if (j < n) sorted[rank[j]] = keys[j];
+    if (j < n && SV_INB(rank[j], n, 902)) sorted[rank[j]] = keys[j];
 }
 
 __device__ __forceinline__ double warp_excl_scan(double x, int lane, double &total)
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(NT_PICK) pick_kernel(const uint64_t *sorted, i
     }
     for (int j = j0; j < j1; ++j) {
         gain += (double)score_of(sorted[j]);
-        const double num = (double)B + gain, c = cost[j + 1];
+        const double num = (double)B + gain, c = SV_INB(j + 1, n + 1, 903) ? cost[j + 1] : 1.0;
         if (bb < 0 || rate_above(num, c, bn, bc)) {
             bn = num;
             bc = c;
@@ -183,11 +185,27 @@ __global__ void __launch_bounds__(NT_PICK) pick_kernel(const uint64_t *sorted, i
     const int budget = wb[0];
     for (int j = tid; j < budget; j += NT_PICK) {
         const uint32_t lo = (uint32_t)sorted[j];
-        atomicMax(admitted + (lo & 0x3fffu), (int)((lo >> 14) & 0x3fu) + 1);
+        if (SV_INB(lo & 0x3fffu, B, 904)) atomicMax(admitted + (lo & 0x3fffu), (int)((lo >> 14) & 0x3fu) + 1);
     }
 }
 
 }  // namespace svb
+
+namespace sv {
+// This module's first range violation (debug builds; 0 otherwise), cleared when read.
+unsigned long long budget_debug_fault()
+{
+#ifdef SV_DEBUG
+    unsigned long long w = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&w, g_sv_debug_fault, sizeof w) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_sv_debug_fault, &z, sizeof z) != cudaSuccess)
+        return ~0ull;
+    return w;
+#else
+    return 0;
+#endif
+}
+}  // namespace sv
 
 extern "C" size_t spec_verify_plan_budget_workspace_bytes(int B, int K)
 {

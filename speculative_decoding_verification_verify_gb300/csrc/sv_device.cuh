@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "sv_check.cuh"
+
 namespace sv {
 
 constexpr int NT = 256;       // threads per CTA of the finalising, residual and block kernels
@@ -330,13 +332,18 @@ __device__ __forceinline__ Seg chunk_of(const Params &P, int64_t r, int64_t j)
 __device__ __forceinline__ int node_parent(const Params &P, int b, int n)
 {
     if (!P.is_tree) return n - 1;
-    return __ldg(P.parents + (int64_t)b * P.rpr + n);
+    const int64_t i = (int64_t)b * P.rpr + n;
+    return SV_INB(i, (int64_t)P.B * P.rpr, 101) ? __ldg(P.parents + i) : -1;
 }
 
 __device__ __forceinline__ int node_token(const Params &P, int b, int n)
 {
-    if (!P.is_tree) return __ldg(P.drafts + (int64_t)b * P.k + (n - 1));
-    return __ldg(P.node_tokens + (int64_t)b * P.rpr + n);
+    if (!P.is_tree) {
+        const int64_t i = (int64_t)b * P.k + (n - 1);
+        return SV_INB(i, (int64_t)P.B * P.k, 102) ? __ldg(P.drafts + i) : -1;
+    }
+    const int64_t i = (int64_t)b * P.rpr + n;
+    return SV_INB(i, (int64_t)P.B * P.rpr, 103) ? __ldg(P.node_tokens + i) : -1;
 }
 
 }  // namespace sv

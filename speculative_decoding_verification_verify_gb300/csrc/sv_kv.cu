@@ -22,6 +22,7 @@
 #include <stdint.h>
 
 #include "spec_verify.h"
+#include "sv_check.cuh"
 
 namespace svkv {
 
@@ -31,8 +32,9 @@ constexpr int SB = 4;           // path steps whose rows a thread holds at once
 constexpr int CHUNK = NT * K;   // vectors per CTA
 constexpr int MAX_NODES = 64;
 
+// pool_vec: the pool's extent in 16-byte vectors (for the range checks of debug builds).
 __global__ void __launch_bounds__(NT) kv_compact_kernel(uint4 *pool, int64_t num_slots, int64_t row_vec,
-                                                        int64_t plane_vec, int64_t work,
+                                                        int64_t plane_vec, int64_t work, int64_t pool_vec,
                                                         const int32_t *slot_table, int max_pos,
                                                         const int32_t *committed_in, int32_t *committed_out,
                                                         const int32_t *accept_index, const int32_t *accept_len,
@@ -46,14 +48,16 @@ __global__ void __launch_bounds__(NT) kv_compact_kernel(uint4 *pool, int64_t num
     // The three index reads are independent: one round trip.
     const int L = accept_len[b];
     const int c = committed_in[b];
-    const int a = tid < N ? accept_index[(int64_t)b * N + tid] : 0;
+    const int a = tid < N && SV_INB((int64_t)b * N + tid, (int64_t)gridDim.y * N, 801) ? accept_index[(int64_t)b * N + tid]
+                                                                                  : 0;
     const bool first = blockIdx.x == 0 && tid == 0;
     if (L < 0) {  // a request the verifier faulted: nothing moves, nothing is committed
         if (first) committed_out[b] = c;
         return;
     }
     const bool pos_ok = c >= 0 && (int64_t)c + N <= max_pos && L < N;
-    if (pos_ok && tid < N) slot_s[tid] = slot_table[(int64_t)b * max_pos + c + tid];
+    if (pos_ok && tid < N && SV_INB((int64_t)b * max_pos + c + tid, (int64_t)gridDim.y * max_pos, 802))
+        slot_s[tid] = slot_table[(int64_t)b * max_pos + c + tid];
     if (tid == 0) flags = pos_ok ? 0 : 1;
     __syncthreads();
     if (pos_ok && tid <= L) {
@@ -104,7 +108,7 @@ __global__ void __launch_bounds__(NT) kv_compact_kernel(uint4 *pool, int64_t num
                 if (i <= L && src_s[i] != dst_s[i]) {
 #pragma unroll
                     for (int k = 0; k < K; ++k)
-                        if (has[k]) v[u][k] = pool[src_s[i] + off[k]];
+                        if (has[k] && SV_INB(src_s[i] + off[k], pool_vec, 803)) v[u][k] = pool[src_s[i] + off[k]];
                 }
             }
 #pragma unroll
@@ -113,7 +117,7 @@ __global__ void __launch_bounds__(NT) kv_compact_kernel(uint4 *pool, int64_t num
                 if (i <= L && src_s[i] != dst_s[i]) {
 #pragma unroll
                     for (int k = 0; k < K; ++k)
-                        if (has[k]) pool[dst_s[i] + off[k]] = v[u][k];
+                        if (has[k] && SV_INB(dst_s[i] + off[k], pool_vec, 804)) pool[dst_s[i] + off[k]] = v[u][k];
                 }
             }
         }
@@ -123,16 +127,32 @@ __global__ void __launch_bounds__(NT) kv_compact_kernel(uint4 *pool, int64_t num
             uint4 v[K];
 #pragma unroll
             for (int k = 0; k < K; ++k)
-                if (has[k]) v[k] = pool[src_s[i] + off[k]];
+                if (has[k] && SV_INB(src_s[i] + off[k], pool_vec, 805)) v[k] = pool[src_s[i] + off[k]];
 #pragma unroll
             for (int k = 0; k < K; ++k)
-                if (has[k]) pool[dst_s[i] + off[k]] = v[k];
+                if (has[k] && SV_INB(dst_s[i] + off[k], pool_vec, 806)) pool[dst_s[i] + off[k]] = v[k];
         }
     }
     if (first) committed_out[b] = c + L + 1;
 }
 
 }  // namespace svkv
+
+namespace sv {
+// This module's first range violation (debug builds; 0 otherwise), cleared when read.
+unsigned long long kv_debug_fault()
+{
+#ifdef SV_DEBUG
+    unsigned long long w = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&w, g_sv_debug_fault, sizeof w) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_sv_debug_fault, &z, sizeof z) != cudaSuccess)
+        return ~0ull;
+    return w;
+#else
+    return 0;
+#endif
+}
+}  // namespace sv
 
 extern "C" int spec_verify_kv_compact(void *kv_pool, int64_t num_slots, size_t row_bytes, int planes,
                                       size_t plane_stride_bytes, const int32_t *slot_table, int max_pos,
@@ -154,8 +174,9 @@ extern "C" int spec_verify_kv_compact(void *kv_pool, int64_t num_slots, size_t r
     const int64_t chunks = (work + svkv::CHUNK - 1) / svkv::CHUNK;
     if (chunks > 0x7fffffff) return SPEC_VERIFY_EINVAL;
     dim3 grid((unsigned)chunks, (unsigned)B);
+    const int64_t pool_vec = (int64_t)(planes - 1) * plane_vec + num_slots * row_vec;
     svkv::kv_compact_kernel<<<grid, svkv::NT, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint4 *>(kv_pool), num_slots, row_vec, plane_vec, work, slot_table, max_pos, committed_in,
-        committed_out, accept_index, accept_len, N, dev_status);
+        static_cast<uint4 *>(kv_pool), num_slots, row_vec, plane_vec, work, pool_vec, slot_table, max_pos,
+        committed_in, committed_out, accept_index, accept_len, N, dev_status);
     return cudaGetLastError() == cudaSuccess ? SPEC_VERIFY_OK : SPEC_VERIFY_ECUDA;
 }

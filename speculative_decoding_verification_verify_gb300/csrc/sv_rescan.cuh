@@ -93,7 +93,8 @@ __device__ __forceinline__ void load_range(const T *row, int64_t rowflat, int64_
         if (k < nvv) {
             const int col = a0 + k * VEC;
             const int64_t f = rowflat + col;
-            w[i] = (f >= 0 && f + VEC <= total) ? ldg_stream(row + col) : load_partial<T>(row, col, c0, c1);
+            w[i] = (f >= 0 && f + VEC <= total && SV_INB(f + VEC - 1, total, 401)) ? ldg_stream(row + col)
+                                                                               : load_partial<T>(row, col, c0, c1);
         }
     }
 }

@@ -128,7 +128,7 @@ __device__ __forceinline__ float take_element(uint4 &w, int j)
 // by the lane that holds it and masked out of its vector.
 template <typename T>
 __device__ __forceinline__ void exclude_step(uint4 (&w)[VPL], int lo, int hi, int lane, const Kids &kd,
-                                          float *caps)
+                                          float *caps, int rpr)
 {
     constexpr int VEC = Elt<T>::VEC;
 #pragma unroll
@@ -143,7 +143,10 @@ __device__ __forceinline__ void exclude_step(uint4 (&w)[VPL], int lo, int hi, in
                 const int u = v >> 5, j = c - lo - v * VEC;
 #pragma unroll
                 for (int uu = 0; uu < VPL; ++uu)
-                    if (uu == u) caps[src + 32 * h] = take_element<T>(w[uu], j);
+                    if (uu == u) {
+                        const float x = take_element<T>(w[uu], j);
+                        if (SV_INB(src + 32 * h, rpr, 203)) caps[src + 32 * h] = x;
+                    }
             }
         }
     }
@@ -152,7 +155,7 @@ __device__ __forceinline__ void exclude_step(uint4 (&w)[VPL], int lo, int hi, in
 // Whether column col (a head or tail element of this lane, when has) is a child token; if so its
 // logit x is captured.
 __device__ __forceinline__ bool scalar_is_child(int col, bool has, float x, int lo, int hi, int lane,
-                                                const Kids &kd, float *caps)
+                                                const Kids &kd, float *caps, int rpr)
 {
     bool child = false;
 #pragma unroll
@@ -164,7 +167,7 @@ __device__ __forceinline__ bool scalar_is_child(int col, bool has, float x, int 
             const int c = __shfl_sync(0xffffffffu, kd.col[h], src);
             if (has && c == col) {
                 child = true;
-                caps[src + 32 * h] = x;
+                if (SV_INB(src + 32 * h, rpr, 204)) caps[src + 32 * h] = x;
             }
         }
     }
@@ -267,11 +270,12 @@ __device__ __forceinline__ void sample_step_fast(SampleAcc &a, const uint4 (&w)[
 // are fillers holding -inf, which belong to the next chunk).
 template <typename T, bool SAMPLE, bool FILT>
 __device__ __forceinline__ void fold_step(uint4 (&w)[VPL], int lo, int hi, int lane, float cs, uint64_t cs2,
-                                          const Kids &kd, float *caps, SampleAcc &sa, GreedyAcc &ga, float thr)
+                                          const Kids &kd, float *caps, int rpr, SampleAcc &sa, GreedyAcc &ga,
+                                          float thr)
 {
     if (SAMPLE) {
         const bool mine = (kd.col[0] >= lo && kd.col[0] < hi) || (kd.col[1] >= lo && kd.col[1] < hi);
-        if (__any_sync(0xffffffffu, mine)) exclude_step<T>(w, lo, hi, lane, kd, caps);
+        if (__any_sync(0xffffffffu, mine)) exclude_step<T>(w, lo, hi, lane, kd, caps, rpr);
         sample_rescale(sa, step_max<T>(w), cs);
         const float nmc = -sa.mc;
         sample_step_fast<T, FILT>(sa, w, cs2, f2(nmc, nmc), thr);
@@ -284,7 +288,8 @@ __device__ __forceinline__ void fold_step(uint4 (&w)[VPL], int lo, int hi, int l
 // lane keeps its reference mc, so later records stay in the same scaled domain per lane.  A
 // sampling record also carries the columns [c0, c1) it covers.
 template <bool SAMPLE>
-__device__ __forceinline__ void flush_record(float4 *rec, int lane, SampleAcc &sa, GreedyAcc &ga, int c0, int c1)
+__device__ __forceinline__ void flush_record(float4 *rec, bool rec_ok, int lane, SampleAcc &sa, GreedyAcc &ga, int c0,
+                                             int c1)
 {
     float4 out;
     if (SAMPLE) {
@@ -301,32 +306,42 @@ __device__ __forceinline__ void flush_record(float4 *rec, int lane, SampleAcc &s
         ga.best = NEG_INF;
         ga.idx = INT_MAX;
     }
-    if (lane == 0) *rec = out;
+    if (lane == 0 && rec_ok) *rec = out;
 }
 
 // One lane's loads of a step: vectors p[32*u]; with CHECK, those at 32*u >= lim are -inf fillers.
+// el is p's first element in the flat logits array of `total` elements (checked in debug builds).
 template <typename T, bool CHECK>
-__device__ __forceinline__ void load_step(uint4 (&d)[VPL], const uint4 *p, int lim)
+__device__ __forceinline__ void load_step(uint4 (&d)[VPL], const uint4 *p, int lim, int64_t el, int64_t total)
 {
+    [[maybe_unused]] constexpr int VEC = Elt<T>::VEC;
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) d[u] = (!CHECK || 32 * u < lim) ? ldg_stream(p + 32 * u) : neg_inf_vec<T>();
+    for (int u = 0; u < VPL; ++u)
+        d[u] = ((!CHECK || 32 * u < lim) && SV_INB(el + (int64_t)(32 * u + 1) * VEC - 1, total, 201))
+                   ? ldg_stream(p + 32 * u)
+                   : neg_inf_vec<T>();
 }
 
 // One warp streams chunk sg of a row: the body's first step and the head and tail elements are
 // loaded first (the caller may update kd meanwhile through `ready`), then the steps are folded
-// and the chunk's record is written to *rec.
+// and the chunk's record is written to *rec (when rec_ok).  rowflat is the row's first element in
+// the flat logits array of `total` elements, rpr the request's rows (both for the range checks of
+// debug builds).
 template <typename T, bool SAMPLE, bool FILT, typename Ready>
 __device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int lane, float cs, Kids &kd, float *caps,
-                                             float4 *rec, Ready ready, float thr)
+                                             float4 *rec, Ready ready, float thr, int64_t rowflat, int64_t total,
+                                             int rpr, bool rec_ok)
 {
     constexpr int VEC = Elt<T>::VEC;
     const int c0 = (int)sg.c0, b0 = (int)sg.b0, b1 = (int)sg.b1, c1 = (int)sg.c1;
     const int nvec = (b1 - b0) / VEC;
     const uint4 *vp = reinterpret_cast<const uint4 *>(row + b0) + lane;
+    const int64_t el = rowflat + b0 + (int64_t)lane * VEC;
     uint4 cur[VPL];
-    if (nvec >= STEP_VEC) load_step<T, false>(cur, vp, 0);
-    else if (nvec > 0) load_step<T, true>(cur, vp, nvec - lane);
-    const bool has_head = c0 + lane < b0, has_tail = b1 + lane < c1;
+    if (nvec >= STEP_VEC) load_step<T, false>(cur, vp, 0, el, total);
+    else if (nvec > 0) load_step<T, true>(cur, vp, nvec - lane, el, total);
+    const bool has_head = c0 + lane < b0 && SV_INB(rowflat + c0 + lane, total, 202);
+    const bool has_tail = b1 + lane < c1 && SV_INB(rowflat + b1 + lane, total, 202);
     const float xh = has_head ? Elt<T>::load(row, c0 + lane) : 0.f;
     const float xt = has_tail ? Elt<T>::load(row, b1 + lane) : 0.f;
     ready();
@@ -334,7 +349,7 @@ __device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int la
     GreedyAcc ga;
     if (b0 > c0) {  // warp-uniform
         if (SAMPLE) {
-            if (!scalar_is_child(c0 + lane, has_head, xh, c0, b0, lane, kd, caps) && has_head)
+            if (!scalar_is_child(c0 + lane, has_head, xh, c0, b0, lane, kd, caps, rpr) && has_head)
                 sample_scalar<FILT>(sa, xh, cs, thr);
         } else if (has_head) {
             greedy_scalar(ga, xh, c0 + lane);
@@ -344,22 +359,23 @@ __device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int la
     const int nst = (nvec + STEP_VEC - 1) / STEP_VEC;
     for (int s = 0; s < nst; ++s) {
         if (s > 0) {
-            if (nvec - s * STEP_VEC >= STEP_VEC) load_step<T, false>(cur, vp + s * STEP_VEC, 0);
-            else load_step<T, true>(cur, vp + s * STEP_VEC, nvec - s * STEP_VEC - lane);
+            const int64_t es = el + (int64_t)s * STEP_VEC * VEC;
+            if (nvec - s * STEP_VEC >= STEP_VEC) load_step<T, false>(cur, vp + s * STEP_VEC, 0, es, total);
+            else load_step<T, true>(cur, vp + s * STEP_VEC, nvec - s * STEP_VEC - lane, es, total);
         }
         const int lo = b0 + s * STEP_VEC * VEC;
         const int hi = min(lo + STEP_VEC * VEC, b1);
-        fold_step<T, SAMPLE, FILT>(cur, lo, hi, lane, cs, cs2, kd, caps, sa, ga, thr);
+        fold_step<T, SAMPLE, FILT>(cur, lo, hi, lane, cs, cs2, kd, caps, rpr, sa, ga, thr);
     }
     if (c1 > b1) {  // warp-uniform
         if (SAMPLE) {
-            if (!scalar_is_child(b1 + lane, has_tail, xt, b1, c1, lane, kd, caps) && has_tail)
+            if (!scalar_is_child(b1 + lane, has_tail, xt, b1, c1, lane, kd, caps, rpr) && has_tail)
                 sample_scalar<FILT>(sa, xt, cs, thr);
         } else if (has_tail) {
             greedy_scalar(ga, xt, b1 + lane);
         }
     }
-    flush_record<SAMPLE>(rec, lane, sa, ga, c0, c1);
+    flush_record<SAMPLE>(rec, rec_ok, lane, sa, ga, c0, c1);
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -266,6 +266,8 @@ __device__ void topkp_row(const Params &P, int64_t r, TopkpSmem &S)
     const int b = (int)(r / P.rpr);
     const int64_t V = P.V;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // The row, its request's options and its threshold slot (range-checked in debug builds).
+    if (!(SV_INB(b, P.B, 701) && SV_INB(r, (int64_t)P.B * P.rpr, 702) && SV_INB(r * V + V - 1, P.total, 703))) return;
     const float Tb = P.temps ? __ldg(P.temps + b) : 1.f;
     const int kk = P.top_k ? __ldg(P.top_k + b) : 0;
     const float pp = P.top_p ? __ldg(P.top_p + b) : 1.f;
