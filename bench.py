@@ -932,7 +932,7 @@ def _variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, pe
                                                P(status), cur()), "spec_verify_rejection_ex")
 
         ms = graph_time_ms(torch, [lambda i=i: call(i) for i in range(GRAPH_CALLS)], 20)
-        launches = 3 if name.startswith("top_k") else 2
+        launches = 4 if name.startswith("top_k") else 2
         res[name] = _mode_entry(ms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2), peak, launches,
                                 note="the threshold kernel reads each row several times" if launches == 3 else None)
     return res

@@ -1305,10 +1305,15 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
         // Rows in flight: TK_CTAS CTAs per SM, one row each (two per SM hold 304 rows, 78 MB of
         // bf16 rows of 128256, which L2 keeps for the row's later passes).
         const int64_t rows = (int64_t)P.B * P.rpr;
-        const int64_t cap = TK_CTAS * (int64_t)dinfo->sms;
+        const int64_t cap = TK_CTAS * (int64_t)dinfo->sms, cap_fast = TK_FAST_CTAS * (int64_t)dinfo->sms;
         const unsigned grid = (unsigned)(rows < cap ? rows : cap);
-        if (dtype == SPEC_VERIFY_BF16) sv_topkp_kernel<__nv_bfloat16><<<grid, NT_TK, 0, s>>>(P);
-        else sv_topkp_kernel<float><<<grid, NT_TK, 0, s>>>(P);
+        if (dtype == SPEC_VERIFY_BF16) {
+            // The fast kernel first (two lean passes); the general one takes the rows it leaves.
+            sv_topkp_fast_kernel<__nv_bfloat16><<<(unsigned)(rows < cap_fast ? rows : cap_fast), NT_TK, 0, s>>>(P);
+            sv_topkp_kernel<__nv_bfloat16><<<grid, NT_TK, 0, s>>>(P, 1);
+        } else {
+            sv_topkp_kernel<float><<<grid, NT_TK, 0, s>>>(P, 0);
+        }
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
     }
     if (dtype == SPEC_VERIFY_BF16) {
