@@ -20,10 +20,12 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue
  *     work on it; none synchronises the host, and none allocates memory.
  *   - The first call on a device (of any entry point, with that device current) reads its SM
- *     count and raises the dynamic shared-memory limits of the kernels that need more than the
- *     default (cudaFuncSetAttribute: 193 KB for the verify kernel, 66 KB for the variants'
- *     finaliser); make it before any stream capture on that device.  The library keeps this per
- *     device for the life of the process, so it must not be used again after cudaDeviceReset.
+ *     count and shared memory per SM and raises the dynamic shared-memory limits of the kernels
+ *     that take more than the default (cudaFuncSetAttribute: the finalising kernels, which size
+ *     their request so that at most ceil(B / SMs) of their CTAs share an SM, and the top-k / top-p
+ *     ring kernel's 218 KiB); make it before any stream capture on that device.  The library keeps
+ *     this per device for the life of the process, so it must not be used again after
+ *     cudaDeviceReset.
  *   - The return value is a host status, known when the call returns:
  *       SPEC_VERIFY_OK, SPEC_VERIFY_EINVAL (bad argument), SPEC_VERIFY_EWORKSPACE
  *       (workspace too small or misaligned), SPEC_VERIFY_ECUDA (a launch failed).
@@ -318,6 +320,17 @@ int spec_verify_philox(uint64_t seed, uint64_t offset, int n_slot, int n_req, ui
  * for a memory checker.
  */
 int spec_verify_debug_fault(uint64_t *fault);
+
+/*
+ * Waits that ran out of time in the top-k / top-p threshold kernel, read and cleared.  That
+ * kernel streams rows through shared memory with asynchronous bulk copies and waits on each
+ * copy's completion for at most 0.2 s; a wait that runs out (a copy should land in microseconds)
+ * hands that CTA's remaining rows to the general threshold kernel, so the outputs are unaffected,
+ * and adds one to this count.  *count = the waits that ran out since the last read (0 in normal
+ * operation).  Synchronous (symbol copies after the work already enqueued on the legacy default
+ * stream).  Returns SPEC_VERIFY_OK, SPEC_VERIFY_EINVAL for a NULL count, or SPEC_VERIFY_ECUDA.
+ */
+int spec_verify_wait_timeouts(uint64_t *count);
 
 /*
  * Allocation-free variant of spec_verify_rejection.  The pages have no counterpart: this entry

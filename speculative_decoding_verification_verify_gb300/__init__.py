@@ -26,6 +26,7 @@ from .binding import (  # noqa: F401
     spec_verify_strerror,
     spec_verify_tree,
     spec_verify_tree_ex,
+    spec_verify_wait_timeouts,
     spec_verify_workspace_bytes,
     using_library,
 )

@@ -12,7 +12,8 @@ LIB_PATH = os.path.join(PKG, "libspecverify.so")
 DEBUG_LIB_PATH = os.path.join(PKG, "libspecverify_debug.so")  # range-checked build (-DSV_DEBUG)
 SOURCES = [os.path.join(CSRC, f) for f in ("spec_verify.cu", "sv_kv.cu", "sv_budget.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("sv_device.cuh", "sv_draw.cuh", "sv_stream.cuh", "sv_rescan.cuh",
-                                                  "sv_decide.cuh", "sv_topkp.cuh", "sv_check.cuh")] + [
+                                                  "sv_decide.cuh", "sv_topkp.cuh", "sv_topkp_ring.cuh",
+                                                  "sv_check.cuh")] + [
     os.path.join(INCLUDE, "spec_verify.h")]
 
 NVCC_FLAGS = [

@@ -80,6 +80,8 @@ def _declare(lib):
     lib.spec_verify_plan_budget_workspace_bytes.restype = sz
     lib.spec_verify_debug_fault.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
     lib.spec_verify_debug_fault.restype = i32
+    lib.spec_verify_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+    lib.spec_verify_wait_timeouts.restype = i32
     return lib
 
 
@@ -125,6 +127,17 @@ def spec_verify_debug_fault(lib=None) -> int:
     if rc != OK:
         raise SpecVerifyError("spec_verify_debug_fault", rc)
     return int(w.value)
+
+
+def spec_verify_wait_timeouts(lib=None) -> int:
+    """Waits of the top-k / top-p ring kernel that ran out of time since the last read (0 in
+    normal operation; their rows were finished by the general threshold kernel)."""
+    lib = lib or load_library()
+    n = ctypes.c_uint64(0)
+    rc = lib.spec_verify_wait_timeouts(ctypes.byref(n))
+    if rc != OK:
+        raise SpecVerifyError("spec_verify_wait_timeouts", rc)
+    return int(n.value)
 
 
 def spec_verify_strerror(code: int) -> str:

@@ -38,6 +38,11 @@
 #include "sv_stream.cuh"
 #include "sv_rescan.cuh"
 #include "sv_topkp.cuh"
+#include "sv_topkp_ring.cuh"
+
+#ifndef SV_PDL_TOPKP
+#define SV_PDL_TOPKP 1
+#endif
 
 namespace sv {
 
@@ -610,7 +615,8 @@ __device__ void finalize_request(const Params &P, int b, FinSmem &F)
 // The streaming kernel: every CTA folds its share of the flat logits range into per-warp records.
 // ---------------------------------------------------------------------------------------------
 // KIND: 0 greedy, 1 sampling, 2 a temperature per request (greedy or sampling per chunk),
-// 3 as 2 with each row's top-k / top-p threshold applied in the sampling fold.
+// 3 as 2 with each row's top-k / top-p threshold applied in the sampling fold, 4 sampling at one
+// temperature with each row's threshold (the sampling fold alone: 24 warps, as kinds 0 and 1).
 template <typename T, int KIND>
 __global__ void __launch_bounds__(stream_threads(KIND), 1) sv_stream_kernel(const Params P)
 {
@@ -646,7 +652,7 @@ __global__ void __launch_bounds__(stream_threads(KIND), 1) sv_stream_kernel(cons
         const T *row = reinterpret_cast<const T *>(P.logits) + r * P.V;
         float *caps = P.caps + (int64_t)b * P.rpr;
         const bool rec_ok = SV_INB(q, P.nchunks, 205);
-        if (KIND >= 2) {
+        if (KIND == 2 || KIND == 3) {
             // The request's temperature decides the chunk's fold; nodes, children and the row's
             // threshold are refreshed first (global loads only when the request or row changes).
             if (b != cur_b || n != cur_n) {
@@ -667,6 +673,17 @@ __global__ void __launch_bounds__(stream_threads(KIND), 1) sv_stream_kernel(cons
             else
                 stream_chunk<T, true, KIND == 3>(row, sg, lane, cs, kd, caps, P.recs + q, []() {}, thr, r * P.V,
                                                  P.total, P.rpr, rec_ok);
+        } else if (KIND == 4) {
+            // The row's children and threshold are refreshed when the row changes.
+            if (b != cur_b || n != cur_n) {
+                if (b != cur_b) load_nodes(P, b, lane, nv);
+                kids_of(P, nv, n, kd);
+                thr = SV_INB(r, (int64_t)P.B * P.rpr, 207) ? __ldcg(P.thr + r) : NEG_INF;
+                cur_b = b;
+                cur_n = n;
+            }
+            stream_chunk<T, true, true>(row, sg, lane, cs, kd, caps, P.recs + q, []() {}, thr, r * P.V, P.total,
+                                        P.rpr, rec_ok);
         } else {
             // The row's child tokens are (re)derived while the chunk's first loads are in flight.
             stream_chunk<T, SAMPLE, false>(row, sg, lane, cs, kd, caps, P.recs + q, [&]() {
@@ -1174,6 +1191,7 @@ struct DevInfo {
     int sms = 0;
     int smem_sm = 0;        // shared memory per SM
     int fin_smem_max = 0;   // dynamic shared memory the finalising kernels may request
+    int fin_static = 0;     // their static shared memory as the runtime counts it
 };
 
 static std::mutex g_dev_mu;
@@ -1194,26 +1212,40 @@ static const DevInfo *device_info()
     if (d.fin_smem_max == 0) {
         // The finalising kernels take dynamic shared memory only to limit how many of their CTAs
         // share an SM (see fin_dyn_smem); they are allowed up to the per-CTA maximum once per
-        // device.
+        // device.  That maximum is the opt-in limit less the kernel's static shared memory as the
+        // runtime counts it (FinSmem, padded to the alignment of the module's dynamic part).
         int smem_sm = 0, optin = 0;
         if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
             cudaGetLastError();
             return nullptr;
         }
-        const int mx = optin - (int)sizeof(FinSmem);
+        const void *fins[] = {(const void *)sv_finalize_kernel<__nv_bfloat16, false, false>,
+                              (const void *)sv_finalize_kernel<__nv_bfloat16, true, false>,
+                              (const void *)sv_finalize_kernel<__nv_bfloat16, true, true>,
+                              (const void *)sv_finalize_kernel<float, false, false>,
+                              (const void *)sv_finalize_kernel<float, true, false>,
+                              (const void *)sv_finalize_kernel<float, true, true>};
+        size_t st = 0;
+        for (const void *f : fins) {
+            cudaFuncAttributes fa;
+            if (cudaFuncGetAttributes(&fa, f) != cudaSuccess) {
+                cudaGetLastError();
+                return nullptr;
+            }
+            if (fa.sharedSizeBytes > st) st = fa.sharedSizeBytes;
+        }
+        const int mx = optin - (int)st;
         const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-        const bool ok = cudaFuncSetAttribute(sv_finalize_kernel<__nv_bfloat16, false, false>, attr, mx) == cudaSuccess &&
-                        cudaFuncSetAttribute(sv_finalize_kernel<__nv_bfloat16, true, false>, attr, mx) == cudaSuccess &&
-                        cudaFuncSetAttribute(sv_finalize_kernel<__nv_bfloat16, true, true>, attr, mx) == cudaSuccess &&
-                        cudaFuncSetAttribute(sv_finalize_kernel<float, false, false>, attr, mx) == cudaSuccess &&
-                        cudaFuncSetAttribute(sv_finalize_kernel<float, true, false>, attr, mx) == cudaSuccess &&
-                        cudaFuncSetAttribute(sv_finalize_kernel<float, true, true>, attr, mx) == cudaSuccess;
+        bool ok = mx > 0 && cudaFuncSetAttribute((const void *)sv_topkp_ring_kernel<__nv_bfloat16>, attr,
+                                                 (int)sizeof(RingSmem)) == cudaSuccess;
+        for (const void *f : fins) ok = ok && cudaFuncSetAttribute(f, attr, mx) == cudaSuccess;
         if (!ok) {
             cudaGetLastError();
             return nullptr;
         }
         d.smem_sm = smem_sm;
+        d.fin_static = (int)st;
         d.fin_smem_max = mx;
     }
     return &d;
@@ -1277,7 +1309,7 @@ static size_t fin_dyn_smem(const DevInfo &d, int B)
     int per_sm = (B + d.sms - 1) / d.sms;
     if (per_sm > 2048 / NT_FIN_MAX) return 0;  // as many as the SM's threads allow anyway
     const int reserve = 1024;                  // shared memory the system keeps per CTA
-    int dyn = d.smem_sm / per_sm - (int)sizeof(FinSmem) - reserve;
+    int dyn = d.smem_sm / per_sm - d.fin_static - reserve;
     if (dyn > d.fin_smem_max) dyn = d.fin_smem_max;
     return dyn > 0 ? (size_t)dyn : 0;
 }
@@ -1305,19 +1337,35 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
         // Rows in flight: TK_CTAS CTAs per SM, one row each (two per SM hold 304 rows, 78 MB of
         // bf16 rows of 128256, which L2 keeps for the row's later passes).
         const int64_t rows = (int64_t)P.B * P.rpr;
-        const int64_t cap = TK_CTAS * (int64_t)dinfo->sms, cap_fast = TK_FAST_CTAS * (int64_t)dinfo->sms;
+        const int64_t cap = TK_CTAS * (int64_t)dinfo->sms;
         const unsigned grid = (unsigned)(rows < cap ? rows : cap);
         if (dtype == SPEC_VERIFY_BF16) {
-            // The fast kernel first (two lean passes); the general one takes the rows it leaves.
-            sv_topkp_fast_kernel<__nv_bfloat16><<<(unsigned)(rows < cap_fast ? rows : cap_fast), NT_TK, 0, s>>>(P);
+            // The ring kernel first (RING_CTAS CTAs per SM, one read of each row); the general one
+            // takes the rows it leaves, launched as a programmatic dependent so that its launch
+            // overlaps the ring kernel's last rows (it waits for the ring grid before reading).
+            const int64_t ring_cap = (int64_t)RING_CTAS * dinfo->sms;
+            const unsigned ring_grid = (unsigned)(rows < ring_cap ? rows : ring_cap);
+            sv_topkp_ring_kernel<__nv_bfloat16><<<ring_grid, NT_RING + 32, sizeof(RingSmem), s>>>(P);
+#if SV_PDL_TOPKP
+            cudaLaunchConfig_t gcfg = {};
+            gcfg.gridDim = dim3(grid);
+            gcfg.blockDim = dim3(NT_TK);
+            gcfg.stream = s;
+            gcfg.attrs = attr;
+            gcfg.numAttrs = 1;
+            if (cudaLaunchKernelEx(&gcfg, sv_topkp_kernel<__nv_bfloat16>, P, 1) != cudaSuccess)
+                return SPEC_VERIFY_ECUDA;
+#else
             sv_topkp_kernel<__nv_bfloat16><<<grid, NT_TK, 0, s>>>(P, 1);
+#endif
         } else {
             sv_topkp_kernel<float><<<grid, NT_TK, 0, s>>>(P, 0);
         }
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
     }
     if (dtype == SPEC_VERIFY_BF16) {
-        if (filt) sv_stream_kernel<__nv_bfloat16, 3><<<P.G, stream_threads(3), 0, s>>>(P);
+        if (filt && !P.temps) sv_stream_kernel<__nv_bfloat16, 4><<<P.G, stream_threads(4), 0, s>>>(P);
+        else if (filt) sv_stream_kernel<__nv_bfloat16, 3><<<P.G, stream_threads(3), 0, s>>>(P);
         else if (P.temps) sv_stream_kernel<__nv_bfloat16, 2><<<P.G, stream_threads(2), 0, s>>>(P);
         else sv_stream_kernel<__nv_bfloat16, SAMPLE ? 1 : 0><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
@@ -1326,7 +1374,8 @@ static int launch_stream(const Params &P, int dtype, cudaStream_t s)
                                P) != cudaSuccess)
             return SPEC_VERIFY_ECUDA;
     } else {
-        if (filt) sv_stream_kernel<float, 3><<<P.G, stream_threads(3), 0, s>>>(P);
+        if (filt && !P.temps) sv_stream_kernel<float, 4><<<P.G, stream_threads(4), 0, s>>>(P);
+        else if (filt) sv_stream_kernel<float, 3><<<P.G, stream_threads(3), 0, s>>>(P);
         else if (P.temps) sv_stream_kernel<float, 2><<<P.G, stream_threads(2), 0, s>>>(P);
         else sv_stream_kernel<float, SAMPLE ? 1 : 0><<<P.G, NT_S, 0, s>>>(P);
         if (cudaGetLastError() != cudaSuccess) return SPEC_VERIFY_ECUDA;
@@ -1640,6 +1689,18 @@ extern "C" int spec_verify_debug_fault(uint64_t *fault)
     const unsigned long long kv = sv::kv_debug_fault(), bu = sv::budget_debug_fault();
     if (kv == ~0ull || bu == ~0ull) return SPEC_VERIFY_ECUDA;
     *fault = w ? w : (kv ? kv : bu);
+    return SPEC_VERIFY_OK;
+}
+
+// Stage waits of the threshold ring kernel that ran out of time, read and cleared; synchronous.
+extern "C" int spec_verify_wait_timeouts(uint64_t *count)
+{
+    if (!count) return SPEC_VERIFY_EINVAL;
+    unsigned long long n = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&n, sv::g_ring_timeouts, sizeof n) != cudaSuccess ||
+        cudaMemcpyToSymbol(sv::g_ring_timeouts, &z, sizeof z) != cudaSuccess)
+        return SPEC_VERIFY_ECUDA;
+    *count = n;
     return SPEC_VERIFY_OK;
 }
 

@@ -20,7 +20,14 @@ constexpr int NT_S = 768;     // threads of a streaming CTA (one CTA per SM)
 // The variant streaming kernels (a temperature per request, top-k / top-p) hold both folds'
 // state: fewer warps per CTA leave each thread the registers to do so without spilling.
 constexpr int NT_SV = SV_NT_SV;
-__host__ __device__ constexpr int stream_threads(int kind) { return kind >= 2 ? NT_SV : NT_S; }
+#ifndef SV_NT_S4
+#define SV_NT_S4 640
+#endif
+constexpr int NT_S4 = SV_NT_S4;  // the filtered one-temperature kind: 20 warps keep its fold in registers
+__host__ __device__ constexpr int stream_threads(int kind)
+{
+    return kind == 2 || kind == 3 ? NT_SV : (kind == 4 ? NT_S4 : NT_S);
+}
 constexpr int MAX_RPR = 64;   // rows per request: k + 1 <= 64 (chain) or N <= 64 (tree)
 constexpr int B_MAX = 65536;  // most requests per call (size of the fixed counter region)
 constexpr int C2_MAX = 1024;  // upper bound on column chunks of the residual kernel
@@ -84,6 +91,19 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p)
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
         : "l"(p));
+    return r;
+}
+
+// The same with L2 priority evict-first: a line this load brings into L2 is among the first to
+// go, so that the lines a previous pass left there at normal priority stay.
+__device__ __forceinline__ uint4 ldg_stream_ef(const void *p)
+{
+    uint4 r;
+    unsigned long long pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p), "l"(pol));
     return r;
 }
 

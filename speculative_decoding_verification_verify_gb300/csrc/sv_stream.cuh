@@ -311,14 +311,19 @@ __device__ __forceinline__ void flush_record(float4 *rec, bool rec_ok, int lane,
 
 // One lane's loads of a step: vectors p[32*u]; with CHECK, those at 32*u >= lim are -inf fillers.
 // el is p's first element in the flat logits array of `total` elements (checked in debug builds).
-template <typename T, bool CHECK>
+#ifndef SV_STREAM_EF
+#define SV_STREAM_EF 1
+#endif
+// EF: evict-first loads (with SV_STREAM_EF; the filtered pass, whose rows the threshold pass read
+// just before).
+template <typename T, bool CHECK, bool EF = false>
 __device__ __forceinline__ void load_step(uint4 (&d)[VPL], const uint4 *p, int lim, int64_t el, int64_t total)
 {
     [[maybe_unused]] constexpr int VEC = Elt<T>::VEC;
 #pragma unroll
     for (int u = 0; u < VPL; ++u)
         d[u] = ((!CHECK || 32 * u < lim) && SV_INB(el + (int64_t)(32 * u + 1) * VEC - 1, total, 201))
-                   ? ldg_stream(p + 32 * u)
+                   ? ((EF && SV_STREAM_EF) ? ldg_stream_ef(p + 32 * u) : ldg_stream(p + 32 * u))
                    : neg_inf_vec<T>();
 }
 
@@ -338,8 +343,8 @@ __device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int la
     const uint4 *vp = reinterpret_cast<const uint4 *>(row + b0) + lane;
     const int64_t el = rowflat + b0 + (int64_t)lane * VEC;
     uint4 cur[VPL];
-    if (nvec >= STEP_VEC) load_step<T, false>(cur, vp, 0, el, total);
-    else if (nvec > 0) load_step<T, true>(cur, vp, nvec - lane, el, total);
+    if (nvec >= STEP_VEC) load_step<T, false, FILT>(cur, vp, 0, el, total);
+    else if (nvec > 0) load_step<T, true, FILT>(cur, vp, nvec - lane, el, total);
     const bool has_head = c0 + lane < b0 && SV_INB(rowflat + c0 + lane, total, 202);
     const bool has_tail = b1 + lane < c1 && SV_INB(rowflat + b1 + lane, total, 202);
     const float xh = has_head ? Elt<T>::load(row, c0 + lane) : 0.f;
@@ -360,8 +365,8 @@ __device__ __forceinline__ void stream_chunk(const T *row, const Seg &sg, int la
     for (int s = 0; s < nst; ++s) {
         if (s > 0) {
             const int64_t es = el + (int64_t)s * STEP_VEC * VEC;
-            if (nvec - s * STEP_VEC >= STEP_VEC) load_step<T, false>(cur, vp + s * STEP_VEC, 0, es, total);
-            else load_step<T, true>(cur, vp + s * STEP_VEC, nvec - s * STEP_VEC - lane, es, total);
+            if (nvec - s * STEP_VEC >= STEP_VEC) load_step<T, false, FILT>(cur, vp + s * STEP_VEC, 0, es, total);
+            else load_step<T, true, FILT>(cur, vp + s * STEP_VEC, nvec - s * STEP_VEC - lane, es, total);
         }
         const int lo = b0 + s * STEP_VEC * VEC;
         const int hi = min(lo + STEP_VEC * VEC, b1);

@@ -34,15 +34,8 @@ constexpr int TK_WARPS = NT_TK / 32;
 #define SV_TK_CTAS 2
 #endif
 constexpr int TK_UNROLL = SV_TK_UNROLL;  // 16-byte loads a thread keeps in flight in a pass
-#ifndef SV_TK_FAST_UNROLL
-#define SV_TK_FAST_UNROLL 4
-#endif
-constexpr int TK_FAST_UNROLL = SV_TK_FAST_UNROLL;  // the same for the fast path's two passes
-#ifndef SV_TK_FAST_CTAS
-#define SV_TK_FAST_CTAS 2
-#endif
-constexpr int TK_FAST_CTAS = SV_TK_FAST_CTAS;  // fast-path CTAs per SM
-// A threshold slot the fast kernel leaves to the general one (a NaN no row's threshold can be).
+// A threshold slot the ring kernel (sv_topkp_ring.cuh) leaves to the general one (a NaN no row's
+// threshold can be).
 constexpr uint32_t TK_PENDING = 0x7fc0beefu;
 constexpr int TK_CTAS = SV_TK_CTAS;      // threshold CTAs per SM (each holds one row at a time)
 
@@ -106,28 +99,19 @@ struct KeyOf<float> {
     }
 };
 
-constexpr int TK_SPAN = 2048;  // keys the fast path's exact histogram covers below the row maximum
+constexpr int TK_SPAN = 2048;  // keys the ring kernel's exact histogram covers below the row maximum
 
 struct TopkpSmem {
     int cnt[TK_BINS];
     double mass[TK_BINS];
-    union {
-        int wcnt[TK_WARPS][TK_BINS];      // per-warp histograms of one pass, merged into cnt / mass
+    union {                          // per-warp histograms of one pass, merged into cnt / mass
+        int wcnt[TK_WARPS][TK_BINS];
         double wmass[TK_WARPS][TK_BINS];
-        struct {                          // the fast path: one bin per key below the row maximum
-            int cnt[TK_SPAN];
-            double mass[TK_SPAN];
-        } exact;
     };
-    uint32_t tkey[NT_TK];  // the fast path: the key of each thread's largest logit
     float wmax[NT_TK / 32];
-    int wcnt_tot[NT_TK / 32];
-    double wmass_tot[NT_TK / 32];
     int sel;           // chosen digit
     int above_cnt;     // count in bins above it
     double above_mass; // mass in bins above it
-    int dk, dp;        // the fast path's crossings (key distances below the maximum)
-    double zk;         // the fast path: mass of the top-k set
 };
 
 // One warp: the bins [0, nb) from the top; the first bin where the running count reaches `rank`
@@ -191,7 +175,7 @@ __device__ __forceinline__ void walk_bins(TopkpSmem &S, int nb, bool by_mass, in
 // element by element.  f(key) is called once per visited element.  With MAX, vmx takes the
 // largest logit of every element (NaN if one is NaN).  With SKIP, a vector whose largest logit is
 // below fl (a value, not NaN) is not visited: none of its keys can reach the key of fl.
-template <typename T, bool MAX, bool SKIP, typename F, int UN = TK_UNROLL>
+template <typename T, bool MAX, bool SKIP, typename F>
 __device__ __forceinline__ void for_each_key(const void *row, int64_t rowflat, int64_t V, int mis, float fl,
                                              float &vmx, F f)
 {
@@ -206,17 +190,17 @@ __device__ __forceinline__ void for_each_key(const void *row, int64_t rowflat, i
     };
     for (int64_t c = threadIdx.x; c < a0; c += NT_TK) one(c);
     for (int64_t c = a1 + threadIdx.x; c < V; c += NT_TK) one(c);
-    // UN vectors per thread in flight: a pass is bound by the loads' latency otherwise.
+    // TK_UNROLL vectors per thread in flight: a pass is bound by the loads' latency otherwise.
     const uint4 *vp = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(row) + a0);
-    for (int64_t i0 = threadIdx.x; i0 < nv; i0 += (int64_t)UN * NT_TK) {
-        uint4 w[UN];
+    for (int64_t i0 = threadIdx.x; i0 < nv; i0 += (int64_t)TK_UNROLL * NT_TK) {
+        uint4 w[TK_UNROLL];
 #pragma unroll
-        for (int u = 0; u < UN; ++u) {
+        for (int u = 0; u < TK_UNROLL; ++u) {
             const int64_t i = i0 + (int64_t)u * NT_TK;
             if (i < nv) w[u] = ldg_stream(vp + i);
         }
 #pragma unroll
-        for (int u = 0; u < UN; ++u) {
+        for (int u = 0; u < TK_UNROLL; ++u) {
             if (i0 + (int64_t)u * NT_TK >= nv) break;
             if (MAX || SKIP) {
                 const float m = Elt<T>::vmax(w[u]);
@@ -279,153 +263,6 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
         S.mass[i] = m;
     }
     __syncthreads();
-}
-
-// Fast path of a row's threshold (bf16 logits, top-k on with k <= NT_TK): two passes, no radix
-// levels.  The first pass (the row's only read from DRAM) keeps each thread's largest logit.  The
-// k-th largest of the NT_TK thread maxima, L, is at most the row's k-th largest logit (the k
-// largest thread maxima are k distinct logits of the row), so every logit of the top-k set lies in
-// [L, max].  When that range holds at most TK_SPAN keys, the second pass (mostly from L2, vectors
-// whose largest logit is below L skipped whole) bins each logit >= L by its key's distance below
-// the maximum's key: exact counts, and for top-p exact masses (fp32 terms summed in fp64), one bin
-// per value level.  One scan from the top then gives the k-th largest key and the fewest whole
-// levels holding top_p of the top-k set's mass.  Returns false (nothing written) when the range is
-// wider; the general path then runs.
-template <typename T>
-__device__ bool topkp_fast(const Params &P, int64_t r, TopkpSmem &S, const void *row, int64_t rowflat, float cs,
-                           int kk, float pp, bool use_p)
-{
-    const int64_t V = P.V;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    float vmx = NEG_INF;
-    for_each_key<T, true, false, void (*)(uint32_t), TK_FAST_UNROLL>(row, rowflat, V, P.mis, 0.f, vmx,
-                                                                     [](uint32_t) {});
-    S.tkey[tid] = KeyOf<T>::key_of_bits(__float_as_uint(vmx) >> 16);
-    float mx = vmx;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) S.wmax[warp] = mx;
-    // The k-th largest thread maximum, by a radix select over their keys (two 8-bit levels).
-    for (int i = tid; i < TK_BINS; i += NT_TK) {
-        S.cnt[i] = 0;
-        S.mass[i] = 0.0;
-    }
-    __syncthreads();
-    mx = S.wmax[0];
-    for (int w = 1; w < NT_TK / 32; ++w) mx = fmax_nan(mx, S.wmax[w]);
-    if (!(mx > NEG_INF) || mx != mx || mx == POS_INF) {  // the streaming pass flags such rows
-        if (tid == 0) P.thr[r] = NEG_INF;
-        __syncthreads();  // every warp has read wmax before the next row writes it
-        return true;
-    }
-    const uint32_t mine = S.tkey[tid];
-    atomicAdd(&S.cnt[mine >> 8], 1);
-    __syncthreads();
-    if (warp == 0) walk_bins(S, TK_BINS, false, kk, 0.0, lane);
-    __syncthreads();
-    const uint32_t hi8 = (uint32_t)S.sel;
-    const int rank = kk - S.above_cnt;
-    __syncthreads();
-    for (int i = tid; i < TK_BINS; i += NT_TK) S.cnt[i] = 0;
-    __syncthreads();
-    if ((mine >> 8) == hi8) atomicAdd(&S.cnt[mine & 0xffu], 1);
-    __syncthreads();
-    if (warp == 0) walk_bins(S, TK_BINS, false, rank, 0.0, lane);
-    __syncthreads();
-    const uint32_t lkey = (hi8 << 8) | (uint32_t)S.sel;
-    const uint32_t mkey = KeyOf<T>::key_of_bits(__float_as_uint(mx) >> 16);
-    const int span = (int)(mkey - lkey) + 1;
-    __syncthreads();
-    if (span > TK_SPAN) return false;
-    for (int i = tid; i < span; i += NT_TK) {
-        S.exact.cnt[i] = 0;
-        S.exact.mass[i] = 0.0;
-    }
-    __syncthreads();
-    // Second pass: every logit >= L, binned by its key's distance below the maximum.
-    float unused = NEG_INF;
-    auto bin = [&](uint32_t k) {
-        if (k >= lkey) {
-            const int d = (int)(mkey - k);
-            atomicAdd(&S.exact.cnt[d], 1);
-            if (use_p) atomicAdd(&S.exact.mass[d], (double)ex2((KeyOf<T>::value(k) - mx) * cs));
-        }
-    };
-    for_each_key<T, false, true, decltype(bin), TK_FAST_UNROLL>(row, rowflat, V, P.mis, KeyOf<T>::value(lkey), unused,
-                                                               bin);
-    __syncthreads();
-    // Scan the bins from the top (d = 0): thread t owns a contiguous block of bins.
-    const int per = (span + NT_TK - 1) / NT_TK;
-    const int d0 = min(tid * per, span), d1 = min(d0 + per, span);
-    int c_own = 0;
-    double m_own = 0.0;
-    for (int d = d0; d < d1; ++d) {
-        c_own += S.exact.cnt[d];
-        m_own += S.exact.mass[d];
-    }
-    int c_inc = c_own;
-    double m_inc = m_own;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int yc = __shfl_up_sync(0xffffffffu, c_inc, o);
-        const double ym = __shfl_up_sync(0xffffffffu, m_inc, o);
-        if (lane >= o) {
-            c_inc += yc;
-            m_inc += ym;
-        }
-    }
-    if (lane == 31) {
-        S.wcnt_tot[warp] = c_inc;
-        S.wmass_tot[warp] = m_inc;
-    }
-    if (tid == 0) {
-        S.dk = INT_MAX;
-        S.dp = INT_MAX;
-    }
-    __syncthreads();
-    int c_before = c_inc - c_own;
-    double m_before = m_inc - m_own;
-    for (int w = 0; w < warp; ++w) {
-        c_before += S.wcnt_tot[w];
-        m_before += S.wmass_tot[w];
-    }
-    // The k-th largest key: the first bin where the running count reaches k.
-    {
-        int c = c_before;
-        for (int d = d0; d < d1; ++d) {
-            c += S.exact.cnt[d];
-            if (c >= kk) {
-                atomicMin(&S.dk, d);
-                break;
-            }
-        }
-    }
-    __syncthreads();
-    const int dk = S.dk;
-    int dsel = dk;
-    if (use_p) {
-        // The top-k set's mass, then the first level whose running mass reaches top_p of it.
-        if (dk >= d0 && dk < d1) {
-            double m = m_before;
-            for (int d = d0; d <= dk; ++d) m += S.exact.mass[d];
-            S.zk = m;
-        }
-        __syncthreads();
-        const double target = (double)pp * S.zk;
-        double m = m_before;
-        for (int d = d0; d < d1 && d <= dk; ++d) {
-            m += S.exact.mass[d];
-            if (S.exact.cnt[d] > 0 && m >= target) {
-                atomicMin(&S.dp, d);
-                break;
-            }
-        }
-        __syncthreads();
-        dsel = min(S.dp, dk);
-    }
-    if (tid == 0) P.thr[r] = KeyOf<T>::value(mkey - (uint32_t)dsel);
-    __syncthreads();
-    return true;
 }
 
 // The threshold of row r: thr[r] = the row's logit threshold, or -inf when the row is not
@@ -512,50 +349,20 @@ __device__ void topkp_row(const Params &P, int64_t r, TopkpSmem &S)
     __syncthreads();
 }
 
-// The fast kernel's share of row r: the threshold when the row is unfiltered (-inf) or the fast
-// path finds it, else TK_PENDING for the general kernel.
-template <typename T>
-__device__ void topkp_fast_row(const Params &P, int64_t r, TopkpSmem &S)
-{
-    const int b = (int)(r / P.rpr);
-    const int64_t V = P.V;
-    if (!(SV_INB(b, P.B, 711) && SV_INB(r, (int64_t)P.B * P.rpr, 712) && SV_INB(r * V + V - 1, P.total, 713))) return;
-    const float Tb = P.temps ? __ldg(P.temps + b) : 1.f;
-    const int kk = P.top_k ? __ldg(P.top_k + b) : 0;
-    const float pp = P.top_p ? __ldg(P.top_p + b) : 1.f;
-    const bool use_k = kk >= 1 && (int64_t)kk < V, use_p = pp < 1.f;
-    if (Tb == 0.f || (!use_k && !use_p)) {
-        if (threadIdx.x == 0) P.thr[r] = NEG_INF;
-        return;
-    }
-    const float cs = P.temps ? cs_of(Tb) : P.cs;
-    const void *row = reinterpret_cast<const T *>(P.logits) + r * V;
-    if (use_k && kk <= NT_TK && topkp_fast<T>(P, r, S, row, r * V, cs, kk, pp, use_p)) return;
-    if (threadIdx.x == 0) P.thr[r] = __uint_as_float(TK_PENDING);
-    __syncthreads();
-}
-
 // A few CTAs per SM, each taking rows in turn, so that the rows being filtered at any time fit in
 // L2 and a row's later passes are served from it.
-// after_fast: the fast kernel ran first; only the rows it left TK_PENDING are taken.
+// after_ring: the ring kernel ran first; only the rows it left TK_PENDING are taken.
 template <typename T>
-__global__ void __launch_bounds__(NT_TK, TK_CTAS) sv_topkp_kernel(const Params P, int after_fast)
+__global__ void __launch_bounds__(NT_TK, TK_CTAS) sv_topkp_kernel(const Params P, int after_ring)
 {
     __shared__ TopkpSmem S;
     const int64_t R = (int64_t)P.B * P.rpr;
+    pdl_launch_dependents();
+    if (after_ring) pdl_wait();  // the ring grid's thresholds (a no-op unless launched as a dependent)
     for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
-        if (after_fast && __float_as_uint(__ldcg(P.thr + r)) != TK_PENDING) continue;
+        if (after_ring && __float_as_uint(__ldcg(P.thr + r)) != TK_PENDING) continue;
         topkp_row<T>(P, r, S);
     }
-}
-
-// The fast path's kernel (bf16 logits): the rows whose top-k set it can bound (see topkp_fast).
-template <typename T>
-__global__ void __launch_bounds__(NT_TK, TK_FAST_CTAS) sv_topkp_fast_kernel(const Params P)
-{
-    __shared__ TopkpSmem S;
-    const int64_t R = (int64_t)P.B * P.rpr;
-    for (int64_t r = blockIdx.x; r < R; r += gridDim.x) topkp_fast_row<T>(P, r, S);
 }
 
 }  // namespace sv

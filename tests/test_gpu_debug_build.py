@@ -49,6 +49,10 @@ def _cases():
     view.copy_(base.logits)
     out.append(("unaligned", lambda: sv.spec_verify_rejection(view, base.drafts, None, temperature=1.0, seed=1,
                                                               offset=0)))
+    tk3 = torch.tensor([1, 60, 512], dtype=torch.int32, device=DEV)
+    tp3 = torch.tensor([0.9, 1.0, 0.5], device=DEV)
+    out.append(("unaligned top-k top-p", lambda: sv.spec_verify_rejection_ex(view, base.drafts, None, top_k=tk3,
+                                                                             top_p=tp3, seed=1, offset=0)))
     tr = wl.tree_b48(DEV, B=5, N=8, V=5003, seed=6)
     for mode in (0, 1):
         out.append((f"tree mode {mode}", lambda mode=mode: sv.spec_verify_tree(

@@ -129,3 +129,77 @@ def test_filters_off_match_the_plain_path():
     b = sv.spec_verify_rejection(inp.logits, inp.drafts, None, temperature=1.0, seed=2, offset=1)
     torch.cuda.synchronize()
     assert torch.equal(a.out_tokens, b.out_tokens) and torch.equal(a.accept_len, b.accept_len)
+
+
+# Edges of the one-read threshold kernel (bf16 rows with top-k <= 256 and at most 32768 vectors):
+# every case is compared with the oracle, and no stage wait may run out.
+
+@pytest.mark.parametrize("shift", [1, 3, 6])
+def test_topkp_unaligned_rows(shift):
+    """A logits base off the 16-byte grid: every row has a head and a tail outside its aligned
+    body, read element by element and folded into the first group."""
+    base = wl.chain_sweep(DEV, B=6, k=3, V=10007, alpha=0.7)
+    B, k, V = base.logits.shape[0], 3, 10007
+    buf = torch.empty(B * (k + 1) * V + 8, dtype=torch.bfloat16, device=DEV)
+    view = buf[shift:shift + B * (k + 1) * V].view(B, k + 1, V)
+    view.copy_(base.logits)
+    tk = np.array([1, 7, 50, 200, 512, 3], np.int32)
+    tp = np.array([1.0, 0.9, 0.5, 0.95, 1.0, 0.2], np.float32)
+    one_hot = wl.ChainInputs("unaligned", view, base.drafts, None, 1.0, base.seed)
+    run_chain(one_hot, tk, tp, offset=shift)
+    run_chain(one_hot, tk, None, offset=shift)
+
+
+def test_topkp_k_at_the_ring_limit():
+    """top-k 256 (the one-read kernel's largest) and 257, 512 (the general kernel) on the same rows."""
+    inp = wl.chain_sweep(DEV, B=4, k=3, V=32000, alpha=0.7)
+    one_hot = wl.ChainInputs("one-hot", inp.logits, inp.drafts, None, 1.0, inp.seed)
+    for kk in (256, 257, 512):
+        tk = np.full(4, kk, np.int32)
+        run_chain(one_hot, tk, np.array([1.0, 0.9, 0.99, 0.6], np.float32))
+
+
+@pytest.mark.parametrize("V", [262144, 262160])
+def test_topkp_longest_rows(V):
+    """Rows of exactly 32768 vectors (the one-read kernel's limit) and just above it (general)."""
+    inp = wl.chain_sweep(DEV, B=2, k=1, V=V, alpha=0.7)
+    one_hot = wl.ChainInputs("one-hot", inp.logits, inp.drafts, None, 1.0, inp.seed)
+    run_chain(one_hot, np.array([50, 300], np.int32), np.array([0.9, 1.0], np.float32))
+
+
+@pytest.mark.parametrize("V", [5, 9, 17, 40])
+def test_topkp_tiny_rows(V):
+    """Rows with no or few aligned vectors: the head and tail elements carry the row."""
+    inp = wl.chain_sweep(DEV, B=6, k=2, V=V, alpha=0.7)
+    one_hot = wl.ChainInputs("one-hot", inp.logits, inp.drafts, None, 1.0, inp.seed)
+    tk = np.array([1, 2, 3, V - 1, 4, 2], np.int32)
+    run_chain(one_hot, tk, np.array([1.0, 0.5, 0.9, 0.99, 1.0, 0.3], np.float32))
+
+
+def test_topkp_heavy_ties_and_signed_zeros():
+    """Logits on a coarse grid (few value levels, long ties at every boundary) with zeros of both
+    signs, including rows whose maximum is zero."""
+    B, k, V = 8, 3, 20011
+    g = torch.Generator(device=DEV).manual_seed(21)
+    lv = torch.randint(-6, 3, (B, k + 1, V), generator=g, device=DEV).float() * 0.5
+    lv[:, :, ::3] = torch.where(lv[:, :, ::3] == 0, -0.0, lv[:, :, ::3])
+    lv[:4] = torch.minimum(lv[:4], torch.zeros_like(lv[:4]))  # rows topped by +0 / -0
+    lv[:4, :, ::5] = -0.0
+    logits = lv.to(torch.bfloat16).contiguous()
+    drafts = torch.randint(0, V, (B, k), generator=g, device=DEV, dtype=torch.int32)
+    inp = wl.ChainInputs("ties", logits, drafts, None, 1.0, 77)
+    tk = np.array([1, 5, 100, 512, 30, 2, 256, 9], np.int32)
+    tp = np.array([0.9, 0.5, 1.0, 0.8, 0.3, 1.0, 0.99, 0.6], np.float32)
+    run_chain(inp, tk, tp)
+    run_chain(inp, tk, None, offset=4)
+
+
+def test_no_wait_ran_out():
+    inp = wl.chain_b64k7(DEV, B=16, k=7, V=128256, seed=4)
+    tk = torch.full((16,), 50, dtype=torch.int32, device=DEV)
+    tp = torch.full((16,), 0.9, dtype=torch.float32, device=DEV)
+    sv.spec_verify_wait_timeouts()
+    for i in range(3):
+        sv.spec_verify_rejection_ex(inp.logits, inp.drafts, None, top_k=tk, top_p=tp, seed=1, offset=i)
+    torch.cuda.synchronize()
+    assert sv.spec_verify_wait_timeouts() == 0
