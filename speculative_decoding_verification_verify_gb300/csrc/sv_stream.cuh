@@ -276,7 +276,12 @@ __device__ __forceinline__ void fold_step(uint4 (&w)[VPL], int lo, int hi, int l
     if (SAMPLE) {
         const bool mine = (kd.col[0] >= lo && kd.col[0] < hi) || (kd.col[1] >= lo && kd.col[1] < hi);
         if (__any_sync(0xffffffffu, mine)) exclude_step<T>(w, lo, hi, lane, kd, caps, rpr);
-        sample_rescale(sa, step_max<T>(w), cs);
+        const float smax = step_max<T>(w);
+        sample_rescale(sa, smax, cs);
+        // Filtered: a step in which no lane holds a logit at or above the row's threshold adds
+        // only zeros (most steps of a row, whose top-k set is small), so its exponentials are
+        // skipped; the sums are the same.
+        if (FILT && !__any_sync(0xffffffffu, smax >= thr)) return;
         const float nmc = -sa.mc;
         sample_step_fast<T, FILT>(sa, w, cs2, f2(nmc, nmc), thr);
     } else {
