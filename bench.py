@@ -959,8 +959,8 @@ def _budget_modes(torch, sv, dev, lib, P, cur, check):
 
         ms = graph_time_ms(torch, [plan] * 10, 20)
         res[f"plan_budget_B{B_}_K{K_}"] = {"ms_per_call": ms, "slots": B_ * K_, "budget": int(bud.item()),
-                                          "launches_per_call": 4,
-                                          "note": "latency-bound: keys, a GPU-wide rank, scatter, one picking CTA"}
+                                          "launches_per_call": 1,
+                                          "note": "latency-bound: one cluster of 8 CTAs sorts, scans, picks and admits in distributed shared memory"}
     return res
 
 

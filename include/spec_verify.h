@@ -246,10 +246,16 @@ int spec_verify_tree_ex(const void *logits, int dtype, const int32_t *node_token
  * b is chosen.  Outputs (device): admitted [B] (request r verifies its first admitted[r] drafts;
  * they sum to *budget), *budget, and *best_rate (or NULL).  cost must be positive.
  * B * K <= 16384, K <= 64.  workspace: device memory, 8-byte aligned, of
- * spec_verify_plan_budget_workspace_bytes(B, K) bytes (0 for unsupported sizes), caller-owned,
- * no initialisation needed.  Four launches, asynchronous on `stream`: the survival keys, their
- * ranks, the scatter into rank order, and the picking CTA.  SPEC_VERIFY_EINVAL for
- * bad pointers, alignment or sizes; SPEC_VERIFY_EWORKSPACE for a short or misaligned workspace.
+ * spec_verify_plan_budget_workspace_bytes(B, K) bytes (0 for unsupported sizes; 256, reserved:
+ * the planner keeps its work in shared memory), caller-owned, no initialisation needed.  One
+ * launch, asynchronous on `stream`: a cluster of 8 CTAs sorts the slots' survival scores (a
+ * bitonic sort per CTA, then each key's rank across the cluster through distributed shared
+ * memory), sums them in 64-bit fixed point, picks the budget (fp32 rates, the near-best ones
+ * compared again in fp64) and writes the admitted prefixes.  The first call on a device raises
+ * the kernel's dynamic shared-memory limit (cudaFuncSetAttribute); make it before any stream
+ * capture on that device.  SPEC_VERIFY_EINVAL for bad pointers, alignment or
+ * sizes; SPEC_VERIFY_EWORKSPACE for a short or misaligned workspace; SPEC_VERIFY_ECUDA for a
+ * failed launch.
  */
 #define SPEC_VERIFY_BUDGET_MAX_SLOTS 16384
 size_t spec_verify_plan_budget_workspace_bytes(int B, int K);

@@ -5,188 +5,526 @@
 // expected accepted tokens per unit of step cost; "Inference Systems Frontier: new models and
 // speculative decoding", section "Deciding how much to verify by load").
 //
-// Four kernels.  keys_kernel: the slots' survival products (fp32, the precision the decision is
-// taken in) and unique 64-bit keys whose ascending order is descending survival, then position,
-// then request, with out-of-range slots last.  rank_kernel: every slot counts the keys below its
-// own; the grid splits both the slots and the keys they are compared with (tiles in shared
-// memory read by broadcast, four slots per thread), so the whole GPU counts, and the partial
-// counts add up atomically.  scatter_kernel puts every slot at its rank, so the slots end up
-// sorted without a sorting network.  pick_kernel
-// (one CTA): an fp64 scan of the sorted scores, the rate (B + gain[b]) / cost[b] of every budget
-// (compared by cross-multiplication, divided once at the end), the first maximum, and each
-// request's admitted count (its admitted slots are leading ones: the largest admitted position
-// + 1).
+// One kernel: a cluster of CL = 8 CTAs of 1024 threads that share their shared memory
+// (distributed shared memory), n = B * K <= 16384 slots, CTA c owning slots [c 2048, c 2048 + 2048):
+//   1. Survival products (fp32, the precision the decision is taken in) and sort keys ~bits(score),
+//      whose ascending order is descending score; slots past a request's draft count, and past n,
+//      take the key of a zero score.  Each CTA sorts its 2048 keys (a bitonic network in shared
+//      memory).
+//   2. Every key's rank in the whole batch: its local index plus, for each other CTA, the count of
+//      its keys that come first (binary searches in local copies of the other CTAs' sorted keys,
+//      laid out as breadth-first search trees, and short walks on for the next key; equal keys
+//      are ordered by CTA).  Each key is stored at its rank in the owning CTA's slice,
+//      so CTA c ends with positions [c 2048, c 2048 + 2048) of the sorted order.  Equal scores come
+//      out in some order: the gains depend only on the values, and admission orders ties as the
+//      rule does.
+//   3. gain[b] = the sum of the b best scores, a scan in 64-bit fixed point (units of 2^-49: exact
+//      for scores >= 2^-26, the rest truncated by less than 2^-49 each, so B + gain is within
+//      64 * 2^-49 ~ 1e-13 of exact relative to B, as n <= 64 B); the rate (B + gain[b]) / cost[b]
+//      of every budget in fp32, the cluster's maximum M, and the budgets within 2^-16 of M compared
+//      exactly in fp64 (cross-multiplication, first maximum).  GB300 has few fp64 units; the
+//      prefilter keeps them to a handful of budgets.
+//   4. The admitted prefix of each request: its slots scoring above the chosen budget's last score
+//      s*, then its slots scoring s* in the rule's tie order (position, then request) while the
+//      budget lasts.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "spec_verify.h"
 #include "sv_check.cuh"
 
 namespace svb {
 
+namespace cg = cooperative_groups;
+
 constexpr int MAX_SLOTS = SPEC_VERIFY_BUDGET_MAX_SLOTS;
 constexpr int MAX_K = 64;
-constexpr int NT_RANK = 128;     // threads of a ranking CTA
-constexpr int RPT = 4;           // slots a ranking thread compares with each key
-constexpr int SLOTS_PER_CTA = NT_RANK * RPT;
-constexpr int NT_PICK = 1024;
-constexpr uint64_t OUT_OF_RANGE = 1ull << 20;  // above every (position, request) field
+constexpr int CL = 8;                 // CTAs of the cluster
+constexpr int NT = 1024;
+constexpr int NW = NT / 32;
+constexpr int PER = MAX_SLOTS / CL;   // slots of a CTA
+constexpr int KPT = PER / NT;         // slots of a thread
+constexpr uint32_t ZERO_KEY = 0xffffffffu;  // ~bits(+0): the last key; also the padding
+constexpr int FIX_SHIFT = 49;
+constexpr int TREE_H = 11;            // the other CTAs' sorted keys as trees of 2^11 - 1 keys plus the last
+static_assert(PER == 1 << TREE_H, "a CTA's keys: a perfect tree and one more");
 
-__device__ __forceinline__ float score_of(uint64_t key) { return __uint_as_float(~(uint32_t)(key >> 32)); }
-
-// Ascending key order: descending survival (the sign bit dropped, so -0 ranks as 0), then
-// ascending position, then ascending request; out-of-range slots after every valid one.
-__global__ void keys_kernel(const float *conf, const int32_t *num_drafts, int B, int K, uint64_t *keys,
-                            int32_t *rank)
+// Breadth-first index (1-based) of the key at in-order position i (1-based) of a perfect binary
+// search tree of height TREE_H: a binary search then reads consecutive words at each level, so a
+// warp's probes fall in distinct banks (on a sorted array they would all fall in one).
+__device__ __forceinline__ int bfs_of(int i)
 {
-    const int r = blockIdx.x * blockDim.x + threadIdx.x;
-    if (r >= B) return;
-    if (!SV_INB((int64_t)r * K + K - 1, (int64_t)B * K, 901)) return;
-    for (int i = 0; i < K; ++i) rank[(int64_t)r * K + i] = 0;
-    const int nd = num_drafts ? min(max(num_drafts[r], 0), K) : K;
-    float run = 1.f;
-    for (int i = 0; i < K; ++i) {
-        const float c = fminf(fmaxf(conf[(int64_t)r * K + i], 0.f), 1.f);  // NaN reads as 0
-        run = run * c;
-        const uint64_t low = ((uint64_t)i << 14) | (uint64_t)r;
-        keys[(int64_t)r * K + i] = i < nd ? ((uint64_t)(~(__float_as_uint(run) & 0x7fffffffu)) << 32) | low
-                                          : (0xffffffffull << 32) | OUT_OF_RANGE | low;
-    }
+    const int z = __ffs(i) - 1;  // the node's height above the leaves
+    return (i >> (z + 1)) | (1 << (TREE_H - 1 - z));
 }
 
-// CTA (x, y): slots [x * SLOTS_PER_CTA, + SLOTS_PER_CTA) against keys [y * span, + span).
-__global__ void __launch_bounds__(NT_RANK) rank_kernel(const uint64_t *keys, int n, int span, int32_t *rank)
+struct PlanSmem {
+    uint32_t loc[PER];          // this CTA's keys, sorted locally
+    uint32_t orig[PER];         // the same keys in slot order (request-major)
+    uint32_t fin[PER];          // this CTA's slice of the batch's sorted order
+    uint32_t all[CL][PER];      // staged confidences, then every other CTA's keys: a search tree
+                                //  at [1, PER) in breadth-first order, the largest key at [0]
+    uint32_t srt[CL][PER];      // every other CTA's keys in sorted order
+    unsigned long long wsum[NW];
+    unsigned long long cg_[PER + 1];  // candidates' gains
+    int cand[PER + 1];                // candidate budgets (at most this CTA's budgets)
+    int wcnt[NW], wcnt2[NW];
+    float wmax[NW];
+    // Published to the cluster:
+    unsigned long long total;   // fixed-point sum of this CTA's slice (valid positions)
+    double bn, bc;              // this CTA's best candidate (rate numerator, cost) ...
+    int bb;                     // ... and its budget (-1: none)
+    float maxrate;
+    int nvalid, ncand, above, ties;
+    uint32_t skey;              // the key of the budget's last slot
+};
+
+__device__ __forceinline__ float score_of_key(uint32_t k) { return __uint_as_float(~k); }
+
+// A score in [0, 1] in units of 2^-49, rounded down: the mantissa shifted by the exponent.
+__device__ __forceinline__ unsigned long long fixed49(float v)
 {
-    __shared__ uint64_t tile[NT_RANK];
-    const int j0 = blockIdx.x * SLOTS_PER_CTA + threadIdx.x;
-    uint64_t mine[RPT];
-    int below[RPT];
-#pragma unroll
-    for (int u = 0; u < RPT; ++u) {
-        const int j = j0 + u * NT_RANK;
-        mine[u] = j < n ? keys[j] : 0ull;
-        below[u] = 0;
-    }
-    const int k0 = blockIdx.y * span, k1 = min(k0 + span, n);
-    for (int t0 = k0; t0 < k1; t0 += NT_RANK) {
-        __syncthreads();
-        if (t0 + (int)threadIdx.x < k1) tile[threadIdx.x] = keys[t0 + threadIdx.x];
-        __syncthreads();
-        const int m = min(NT_RANK, k1 - t0);
-        for (int i = 0; i < m; ++i) {
-            const uint64_t t = tile[i];
-#pragma unroll
-            for (int u = 0; u < RPT; ++u) below[u] += t < mine[u];
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < RPT; ++u) {
-        const int j = j0 + u * NT_RANK;
-        if (j < n && below[u]) atomicAdd(rank + j, below[u]);
-    }
+    const uint32_t u = __float_as_uint(v);
+    const int ex = (int)(u >> 23) - 127;
+    if (!(v > 0.f) || ex < -49) return 0ull;
+    const unsigned long long m = (u & 0x7fffffu) | 0x800000u;
+    const int sh = ex + FIX_SHIFT - 23;
+    return sh >= 0 ? m << sh : m >> (-sh);
 }
 
-// Keys are unique, so the ranks are a permutation.
-__global__ void scatter_kernel(const uint64_t *keys, const int32_t *rank, int n, uint64_t *sorted)
+// An fp32 approximation (relative error below 2^-23) of a positive double, by its bits; `odd` is
+// set for a value the approximation cannot carry (outside 2^-100 .. 2^100, or not positive).
+__device__ __forceinline__ float approx_f32(double d, bool &odd)
 {
-    const int j = blockIdx.x * blockDim.x + threadIdx.x;
-    if (j < n && SV_INB(rank[j], n, 902)) sorted[rank[j]] = keys[j];
-}
-
-__device__ __forceinline__ double warp_excl_scan(double x, int lane, double &total)
-{
-    double incl = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+    const unsigned long long u = (unsigned long long)__double_as_longlong(d);
+    const int ex = (int)((u >> 52) & 0x7ff) - 1023;
+    if ((u >> 63) || ex < -100 || ex > 100) {
+        odd = true;
+        return 1.f;
     }
-    total = __shfl_sync(0xffffffffu, incl, 31);
-    return incl - x;
+    return __uint_as_float(((uint32_t)(ex + 127) << 23) | (uint32_t)((u >> 29) & 0x7fffffu));
 }
 
 // Is rate a = na / ca above rate b = nb / cb?  Costs are positive.
 __device__ __forceinline__ bool rate_above(double na, double ca, double nb, double cb) { return na * cb > nb * ca; }
 
-__global__ void __launch_bounds__(NT_PICK) pick_kernel(const uint64_t *sorted, int n, int B, const double *cost,
-                                                       int32_t *admitted, int32_t *budget_out, double *rate_out)
+// The first maximum: does (na, ca, a) beat (nb, cb, b)?  b < 0: nothing yet.
+__device__ __forceinline__ bool beats(double na, double ca, int a, double nb, double cb, int b)
 {
-    constexpr int NW = NT_PICK / 32;
-    __shared__ double wtot[NW];
-    __shared__ double wnum[NW], wcost[NW];
-    __shared__ int wb[NW];
-    __shared__ int n_valid;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int r = tid; r < B; r += NT_PICK) admitted[r] = 0;
-    // The valid slots are a prefix of the sorted order; find its length.
-    if (tid == 0) n_valid = n;
+    return a >= 0 && (b < 0 || rate_above(na, ca, nb, cb) || (!rate_above(nb, cb, na, ca) && a < b));
+}
+
+__device__ __forceinline__ float clip01(float c) { return fminf(fmaxf(c, 0.f), 1.f); }  // NaN reads as 0
+__device__ __forceinline__ uint32_t key_of(float run) { return ~(__float_as_uint(run) & 0x7fffffffu); }
+
+// Block-wide sum of one int per thread (every thread of the CTA calls it).
+__device__ __forceinline__ int block_sum(int x, int lane, int warp, int *ws)
+{
+    x = __reduce_add_sync(0xffffffffu, x);
     __syncthreads();
-    for (int j = tid; j < n; j += NT_PICK)
-        if ((sorted[j] & OUT_OF_RANGE) && (j == 0 || !(sorted[j - 1] & OUT_OF_RANGE))) n_valid = j;
+    if (lane == 0) ws[warp] = x;
     __syncthreads();
-    const int nv = n_valid;
-    const int per = (nv + NT_PICK - 1) / NT_PICK;
-    const int j0 = min(tid * per, nv), j1 = min(j0 + per, nv);
-    double own = 0.0;
-    for (int j = j0; j < j1; ++j) own += (double)score_of(sorted[j]);
-    double wt;
-    const double wex = warp_excl_scan(own, lane, wt);
-    if (lane == 0) wtot[warp] = wt;
-    __syncthreads();
-    double gain = wex;
-    for (int w = 0; w < warp; ++w) gain += wtot[w];
-    // Budgets this thread owns: b = j + 1 for its slots, and b = 0 for thread 0; first maximum.
-    double bn = 0.0, bc = 1.0;
-    int bb = -1;
-    if (tid == 0) {
-        bn = (double)B;
-        bc = cost[0];
-        bb = 0;
+    int t = 0;
+    for (int w = 0; w < NW; ++w) t += ws[w];
+    return t;
+}
+
+// Block-wide exclusive scan of one int per thread; *total = the sum.
+__device__ __forceinline__ int block_excl_scan(int x, int lane, int warp, int *ws, int &total)
+{
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
     }
-    for (int j = j0; j < j1; ++j) {
-        gain += (double)score_of(sorted[j]);
-        const double num = (double)B + gain, c = SV_INB(j + 1, n + 1, 903) ? cost[j + 1] : 1.0;
-        if (bb < 0 || rate_above(num, c, bn, bc)) {
-            bn = num;
-            bc = c;
-            bb = j + 1;
+    __syncthreads();
+    if (lane == 31) ws[warp] = incl;
+    __syncthreads();
+    int before = incl - x;
+    total = 0;
+    for (int w = 0; w < NW; ++w) {
+        if (w < warp) before += ws[w];
+        total += ws[w];
+    }
+    return before;
+}
+
+// Count of keys of a tree copy t below k (upper: at or below k): one probe per level, the leaf
+// position reached is the count among the tree's keys, and t[0] (the largest key) adds one.
+__device__ __forceinline__ int count_below(const uint32_t *t, uint32_t k, bool upper)
+{
+    int j = 1;
+#pragma unroll
+    for (int l = 0; l < TREE_H; ++l) {
+        const uint32_t x = t[j];
+        j = 2 * j + ((upper ? x <= k : x < k) ? 1 : 0);
+    }
+    const uint32_t x = t[0];
+    return (j - PER) + ((upper ? x <= k : x < k) ? 1 : 0);
+}
+
+// The same count on a plain sorted array a[0, PER).
+__device__ __forceinline__ int count_sorted(const uint32_t *a, uint32_t k, bool upper)
+{
+    int pos = 0;
+#pragma unroll
+    for (int step = PER / 2; step > 0; step >>= 1) {
+        const uint32_t x = a[pos + step - 1];
+        pos += (upper ? x <= k : x < k) ? step : 0;
+    }
+    const uint32_t x = a[pos];
+    return pos + ((upper ? x <= k : x < k) ? 1 : 0);
+}
+
+// One compare-exchange of a bitonic stage: elements e (this lane's x) and e ^ j (the partner's y),
+// ascending where (e & k) == 0.
+__device__ __forceinline__ uint32_t cx(uint32_t x, uint32_t y, int e, int j, int k)
+{
+    const bool low = (e & j) == 0, asc = (e & k) == 0;
+    return (low == asc) ? min(x, y) : max(x, y);
+}
+
+// Bitonic sort of loc[0, PER) (ascending) by NT threads: thread t holds elements 2t and 2t + 1 for
+// the stages with j < 64 (within the thread, then across the warp by shuffles), and the stages
+// with j >= 64 go through shared memory, one pair per thread.
+__device__ __forceinline__ void bitonic_sort(uint32_t *loc, int tid, int lane)
+{
+    static_assert(PER == 2 * NT, "two elements per thread");
+    for (int k = 2; k <= PER; k <<= 1) {
+        int j = k >> 1;
+        for (; j >= 64; j >>= 1) {
+            __syncthreads();
+            const int i = ((tid & ~(j - 1)) << 1) | (tid & (j - 1)), q = i + j;
+            const uint32_t a = loc[i], b = loc[q];
+            const bool asc = (i & k) == 0;
+            loc[i] = asc ? min(a, b) : max(a, b);
+            loc[q] = asc ? max(a, b) : min(a, b);
+        }
+        __syncthreads();
+        uint32_t v0 = loc[2 * tid], v1 = loc[2 * tid + 1];
+        for (; j >= 2; j >>= 1) {
+            const int m = j >> 1;  // partner lane: lane ^ m (elements 2t + h and (2t + h) ^ j)
+            const uint32_t y0 = __shfl_xor_sync(0xffffffffu, v0, m), y1 = __shfl_xor_sync(0xffffffffu, v1, m);
+            v0 = cx(v0, y0, 2 * tid, j, k);
+            v1 = cx(v1, y1, 2 * tid + 1, j, k);
+        }
+        {  // j == 1: within the thread
+            const bool asc = ((2 * tid) & k) == 0;
+            const uint32_t lo = min(v0, v1), hi = max(v0, v1);
+            v0 = asc ? lo : hi;
+            v1 = asc ? hi : lo;
+        }
+        loc[2 * tid] = v0;
+        loc[2 * tid + 1] = v1;
+    }
+    __syncthreads();
+}
+
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
+    plan_kernel(const float *conf, const int32_t *num_drafts, int B, int K, const double *cost, int32_t *admitted,
+                int32_t *budget_out, double *rate_out)
+{
+    extern __shared__ __align__(16) unsigned char plan_raw[];
+    PlanSmem &S = *reinterpret_cast<PlanSmem *>(plan_raw);
+    cg::cluster_group cluster = cg::this_cluster();
+    const int c = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = B * K;
+    auto drafts_of = [&](int r) { return num_drafts ? min(max(num_drafts[r], 0), K) : K; };
+    auto peer = [&](auto *p, int rank) { return cluster.map_shared_rank(p, rank); };
+    // 1. Keys of slots [s0, s1): the confidences of the requests touching them staged first.
+    const int s0 = c * PER, s1 = min(s0 + PER, n);
+    float *cf = reinterpret_cast<float *>(&S.all[0][0]);
+    const int r0 = s0 < n ? s0 / K : 0, r1 = s1 > s0 ? (s1 - 1) / K + 1 : 0;  // requests [r0, r1)
+    const int c0 = r0 * K, nc = r1 > r0 ? min(r1 * K, n) - c0 : 0;
+    for (int j = tid; j < nc; j += NT) cf[j] = SV_INB(c0 + j, n, 901) ? conf[c0 + j] : 0.f;
+    for (int x = tid; x < PER; x += NT) S.loc[x] = ZERO_KEY;
+    if (tid == 0) S.ncand = 0;
+    __syncthreads();
+    int my_valid = 0;
+    for (int r = r0 + tid; r < r1; r += NT) {
+        const int nd = drafts_of(r);
+        float run = 1.f;
+        for (int i = 0; i < nd; ++i) {
+            run = run * clip01(cf[(r - r0) * K + i]);
+            const int j = r * K + i;
+            if (j >= s0 && j < s1) {
+                S.loc[j - s0] = key_of(run);
+                ++my_valid;
+            }
         }
     }
-    for (int round = 0; round < 2; ++round) {
-        if (round == 1) {
-            __syncthreads();
-            if (warp != 0) break;
-            bn = wnum[lane];
-            bc = wcost[lane];
-            bb = wb[lane];
+    const int part_valid = block_sum(my_valid, lane, warp, S.wcnt);
+    for (int x = tid; x < PER; x += NT) S.orig[x] = S.loc[x];
+    if (tid == 0) S.nvalid = part_valid;
+    // Local bitonic sort of loc (ascending keys).
+    bitonic_sort(S.loc, tid, lane);
+    cluster.sync();  // #1: every CTA's sorted keys and valid count are visible
+    int nvq[CL];
+#pragma unroll
+    for (int q = 0; q < CL; ++q) nvq[q] = *peer(&S.nvalid, q);  // loads in flight together
+    int nv = 0;
+#pragma unroll
+    for (int q = 0; q < CL; ++q) nv += nvq[q];
+    // 2. Copies of the other CTAs' sorted keys, then every local key's rank in the batch.
+    for (int q = 0; q < CL; ++q) {
+        if (q == c) continue;
+        const uint4 *src = reinterpret_cast<const uint4 *>(peer(&S.loc[0], q));
+        uint32_t *dst = &S.all[q][0];
+        for (int x = tid; x < PER / 4; x += NT) {
+            const uint4 v = src[x];
+            reinterpret_cast<uint4 *>(&S.srt[q][0])[x] = v;
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 4 * x + e;  // in-order position i + 1; the last key goes to word 0
+                dst[i + 1 < PER ? bfs_of(i + 1) : 0] = w[e];
+            }
+        }
+    }
+    __syncthreads();
+    {
+        // Thread t ranks keys 2t and 2t + 1: the first by a tree search in each other CTA's keys,
+        // the second by a short walk on from there in the sorted copy (a search when it is long).
+        const uint32_t k0 = S.loc[2 * tid], k1 = S.loc[2 * tid + 1];
+        int r0 = 2 * tid, r1 = 2 * tid + 1;
+        for (int q = 0; q < CL; ++q) {
+            if (q == c) continue;
+            const bool up = q < c;
+            const int n0 = count_below(S.all[q], k0, up);
+            int n1 = n0;
+            const uint32_t *sq = S.srt[q];
+            int steps = 0;
+            while (n1 < PER && (up ? sq[n1] <= k1 : sq[n1] < k1) && steps < 8) {
+                ++n1;
+                ++steps;
+            }
+            if (steps == 8) n1 = count_below(S.all[q], k1, up);
+            r0 += n0;
+            r1 += n1;
+        }
+        if (SV_INB(r0, CL * PER, 905)) *peer(&S.fin[r0 % PER], r0 / PER) = k0;
+        if (SV_INB(r1, CL * PER, 905)) *peer(&S.fin[r1 % PER], r1 / PER) = k1;
+    }
+    cluster.sync();  // #2: every CTA holds its slice of the sorted order
+    // 3. Gains of this CTA's positions g = s0 + x (budget b = g + 1), then rates.
+    const int xb = tid * KPT;  // this thread's positions [xb, xb + KPT), blocked for the scan
+    unsigned long long own = 0ull;
+    for (int u = 0; u < KPT; ++u)
+        if (s0 + xb + u < nv) own += fixed49(score_of_key(S.fin[xb + u]));
+    unsigned long long incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) S.wsum[warp] = incl;
+    __syncthreads();
+    unsigned long long before = incl - own;
+    unsigned long long ctot = 0ull;
+    for (int w = 0; w < NW; ++w) {
+        if (w < warp) before += S.wsum[w];
+        ctot += S.wsum[w];
+    }
+    if (tid == 0) S.total = ctot;
+    cluster.sync();  // #3: slice totals
+    {
+        unsigned long long tq[CL];
+#pragma unroll
+        for (int q = 0; q < CL; ++q) tq[q] = q < c ? *peer(&S.total, q) : 0ull;
+#pragma unroll
+        for (int q = 0; q < CL; ++q) before += tq[q];
+    }
+    const float Bf = (float)B, unit = 1.0f / (float)(1ull << FIX_SHIFT);
+    bool odd = false;  // a cost the fp32 prefilter cannot carry: every budget is compared exactly
+    float r32[KPT + 1];
+    unsigned long long gsum[KPT + 1];
+    int bud[KPT + 1];
+    float best32 = 0.f;
+    {
+        unsigned long long g = before;
+        for (int u = 0; u <= KPT; ++u) {
+            // u < KPT: budget s0 + xb + u + 1; u == KPT: budget 0 (CTA 0, thread 0 only)
+            const int b = u < KPT ? s0 + xb + u + 1 : 0;
+            bud[u] = -1;
+            if (u < KPT) {
+                if (b > nv) continue;
+                g += fixed49(score_of_key(S.fin[xb + u]));
+            } else if (c != 0 || tid != 0) {
+                continue;
+            }
+            const unsigned long long gb = u < KPT ? g : 0ull;
+            const float inv = __fdividef(1.f, approx_f32(SV_INB(b, n + 1, 903) ? cost[b] : 1.0, odd));
+            r32[u] = (Bf + (float)gb * unit) * inv;
+            gsum[u] = gb;
+            bud[u] = b;
+            best32 = fmaxf(best32, r32[u]);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best32 = fmaxf(best32, __shfl_xor_sync(0xffffffffu, best32, o));
+    if (lane == 0) S.wmax[warp] = best32;
+    const bool any_odd = __syncthreads_or(odd);
+    if (tid == 0) {
+        float m = S.wmax[0];
+        for (int w = 1; w < NW; ++w) m = fmaxf(m, S.wmax[w]);
+        S.maxrate = any_odd ? __int_as_float(0x7f800000) : m;  // +inf: every budget is a candidate
+    }
+    cluster.sync();  // #4: the CTAs' maxima
+    float mq[CL];
+#pragma unroll
+    for (int q = 0; q < CL; ++q) mq[q] = *peer(&S.maxrate, q);
+    float M = 0.f;
+#pragma unroll
+    for (int q = 0; q < CL; ++q) M = fmaxf(M, mq[q]);
+    // Candidates: fp32 rates within 2^-16 of M (they err by less than 2^-20); all budgets when a
+    // cost fell outside the prefilter's range (M = +inf).
+    const float floor32 = M == __int_as_float(0x7f800000) ? -1.f : M * (1.f - 1.f / 65536.f);
+    for (int u = 0; u <= KPT; ++u)
+        if (bud[u] >= 0 && (floor32 < 0.f || r32[u] >= floor32)) {
+            const int q = atomicAdd(&S.ncand, 1);
+            if (SV_INB(q, PER + 1, 906)) {
+                S.cand[q] = bud[u];
+                S.cg_[q] = gsum[u];
+            }
+        }
+    __syncthreads();
+    if (warp == 0) {
+        // This CTA's candidates compared exactly (fp64, cross-multiplied); the first maximum.
+        const int ncd = min(S.ncand, PER + 1);
+        double bn = 0.0, bc = 1.0;
+        int bb = -1;
+        for (int q = lane; q < ncd; q += 32) {
+            const int b = S.cand[q];
+            const double num = (double)B + (double)S.cg_[q] * (1.0 / (double)(1ull << FIX_SHIFT));
+            const double cb = SV_INB(b, n + 1, 903) ? cost[b] : 1.0;
+            if (beats(num, cb, b, bn, bc, bb)) {
+                bn = num;
+                bc = cb;
+                bb = b;
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const double on = __shfl_xor_sync(0xffffffffu, bn, o), oc = __shfl_xor_sync(0xffffffffu, bc, o);
             const int ob = __shfl_xor_sync(0xffffffffu, bb, o);
-            if (ob >= 0 && (bb < 0 || rate_above(on, oc, bn, bc) || (!rate_above(bn, bc, on, oc) && ob < bb))) {
+            if (beats(on, oc, ob, bn, bc, bb)) {
                 bn = on;
                 bc = oc;
                 bb = ob;
             }
         }
-        if (round == 0 && lane == 0) {
-            wnum[warp] = bn;
-            wcost[warp] = bc;
-            wb[warp] = bb;
+        if (lane == 0) {
+            S.bn = bn;
+            S.bc = bc;
+            S.bb = bb;
         }
     }
-    if (tid == 0) {
-        wb[0] = bb;
-        *budget_out = bb;
+    cluster.sync();  // #5: the CTAs' best candidates
+    // Every CTA reduces the eight bests the same way (first maximum), so all agree on the budget.
+    double bnq[CL], bcq[CL];
+    int bbq[CL];
+#pragma unroll
+    for (int q = 0; q < CL; ++q) {
+        bnq[q] = *peer(&S.bn, q);
+        bcq[q] = *peer(&S.bc, q);
+        bbq[q] = *peer(&S.bb, q);
+    }
+    double bn = 0.0, bc = 1.0;
+    int budget = -1;
+    for (int q = 0; q < CL; ++q)
+        if (beats(bnq[q], bcq[q], bbq[q], bn, bc, budget)) {
+            bn = bnq[q];
+            bc = bcq[q];
+            budget = bbq[q];
+        }
+    if (c == 0 && tid == 0) {
+        *budget_out = budget;
         if (rate_out) *rate_out = bn / bc;
     }
-    __syncthreads();
-    const int budget = wb[0];
-    for (int j = tid; j < budget; j += NT_PICK) {
-        const uint32_t lo = (uint32_t)sorted[j];
-        if (SV_INB(lo & 0x3fffu, B, 904)) atomicMax(admitted + (lo & 0x3fffu), (int)((lo >> 14) & 0x3fu) + 1);
+    // s*: the key at sorted position budget - 1 (in its owner's slice); the valid slots scoring
+    // above it and at it, counted in the batch's sorted keys (this CTA's and the other CTAs' trees).
+    if (tid == 0) {
+        uint32_t skey = 0u;
+        int above = 0, ties = 0;
+        if (budget > 0 && SV_INB(budget - 1, CL * PER, 904)) {
+            skey = *peer(&S.fin[(budget - 1) % PER], (budget - 1) / PER);
+            int lo = 0, hi = 0;
+            for (int q = 0; q < CL; ++q) {
+                if (q == c) {  // this CTA's sorted keys: binary searches on the array
+                    lo += count_sorted(S.loc, skey, false);
+                    hi += count_sorted(S.loc, skey, true);
+                } else {
+                    lo += count_below(S.all[q], skey, false);
+                    hi += count_below(S.all[q], skey, true);
+                }
+            }
+            above = lo;
+            ties = skey == ZERO_KEY ? nv - lo : hi - lo;  // the padding shares the zero key
+        }
+        S.skey = skey;
+        S.above = above;
+        S.ties = ties;
     }
+    __syncthreads();
+    const uint32_t skey = S.skey;
+    const int above = S.above, ties = S.ties;
+    // 4. Admission.  Request r is handled by the CTA owning its first slot; its keys are read from
+    // the slot-order copies (the next CTA's for slots past this CTA's range).
+    auto key_at = [&](int j) { return j < s1 ? S.orig[j - s0] : *peer(&S.orig[(j - s0) - PER], c + 1); };
+    const int ra = (s0 + K - 1) / K, rb = s1 > s0 ? (s1 - 1) / K + 1 : ra;  // requests starting here
+    const int need = budget - above;  // tie slots admitted (1 <= need <= ties when budget > 0)
+    if (budget <= 0 || need >= ties) {
+        for (int r = ra + tid; r < rb; r += NT) {
+            int a = 0;
+            if (budget > 0) {
+                const int nd = drafts_of(r);
+                for (int i = 0; i < nd; ++i) a += key_at(r * K + i) <= skey;
+            }
+            admitted[r] = a;
+        }
+    } else if (c == 0) {
+        // Part of the tie group: position by position, requests in order (a block scan per chunk
+        // of NT requests), the tie slots ranked below `need` admitted.  CTA 0 alone.
+        auto key_any = [&](int j) { return *peer(&S.orig[j % PER], j / PER); };
+        auto gt_eq = [&](int r, int &gt, int &eq) {
+            gt = 0;
+            eq = 0;
+            const int nd = drafts_of(r);
+            for (int i = 0; i < nd; ++i) {
+                const uint32_t x = key_any(r * K + i);
+                gt += x < skey;
+                eq += x == skey;
+            }
+        };
+        const int chunks = (B + NT - 1) / NT;
+        for (int m = 0; m < chunks; ++m) {
+            const int r = m * NT + tid;
+            if (r < B) {
+                int gt, eq;
+                gt_eq(r, gt, eq);
+                admitted[r] = gt;
+            }
+        }
+        int tie_base = 0;
+        for (int i = 0; i < K; ++i) {
+            for (int m = 0; m < chunks; ++m) {
+                const int r = m * NT + tid;
+                int gt = 0, eq = 0;
+                if (r < B) gt_eq(r, gt, eq);
+                const int is_tie = r < B && i >= gt && i < gt + eq;
+                int total;
+                const int rank = tie_base + block_excl_scan(is_tie, lane, warp, S.wcnt, total);
+                if (is_tie && rank < need) admitted[r] = i + 1;
+                tie_base += total;
+            }
+        }
+    }
+    cluster.sync();  // #6: no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace svb
@@ -210,8 +548,11 @@ unsigned long long budget_debug_fault()
 extern "C" size_t spec_verify_plan_budget_workspace_bytes(int B, int K)
 {
     if (B < 1 || K < 1 || K > svb::MAX_K || (int64_t)B * K > svb::MAX_SLOTS) return 0;
-    return (2 * sizeof(uint64_t) + sizeof(int32_t)) * (size_t)B * (size_t)K;
+    return 256;  // reserved: the planner keeps its work in shared memory
 }
+
+static std::mutex g_plan_mu;
+static bool g_plan_attr[64];
 
 extern "C" int spec_verify_plan_budget(const float *conf, const int32_t *num_drafts, int B, int K,
                                        const double *cost, int32_t *admitted, int32_t *budget,
@@ -222,23 +563,23 @@ extern "C" int spec_verify_plan_budget(const float *conf, const int32_t *num_dra
     if ((uintptr_t)conf % 4 || (uintptr_t)cost % 8 || (uintptr_t)admitted % 4 || (uintptr_t)budget % 4 ||
         (uintptr_t)num_drafts % 4 || (uintptr_t)best_rate % 8)
         return SPEC_VERIFY_EINVAL;
-    const int n = B * K;
     if ((uintptr_t)workspace % 8 || ws_bytes < spec_verify_plan_budget_workspace_bytes(B, K))
         return SPEC_VERIFY_EWORKSPACE;
-    uint64_t *keys = static_cast<uint64_t *>(workspace);
-    uint64_t *sorted = keys + n;
-    int32_t *rank = reinterpret_cast<int32_t *>(sorted + n);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPEC_VERIFY_ECUDA;
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        if (!g_plan_attr[dev]) {
+            if (cudaFuncSetAttribute(svb::plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)sizeof(svb::PlanSmem)) != cudaSuccess) {
+                cudaGetLastError();
+                return SPEC_VERIFY_ECUDA;
+            }
+            g_plan_attr[dev] = true;
+        }
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    svb::keys_kernel<<<(B + 255) / 256, 256, 0, s>>>(conf, num_drafts, B, K, keys, rank);
-    // Split the keys each slot is compared with until about 1024 CTAs count at once.
-    const int gx = (n + svb::SLOTS_PER_CTA - 1) / svb::SLOTS_PER_CTA;
-    int gy = (1024 + gx - 1) / gx;
-    const int max_gy = (n + svb::NT_RANK - 1) / svb::NT_RANK;
-    if (gy > max_gy) gy = max_gy;
-    const int span = ((n + gy - 1) / gy + svb::NT_RANK - 1) / svb::NT_RANK * svb::NT_RANK;
-    gy = (n + span - 1) / span;
-    svb::rank_kernel<<<dim3(gx, gy), svb::NT_RANK, 0, s>>>(keys, n, span, rank);
-    svb::scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(keys, rank, n, sorted);
-    svb::pick_kernel<<<1, svb::NT_PICK, 0, s>>>(sorted, n, B, cost, admitted, budget, best_rate);
+    svb::plan_kernel<<<svb::CL, svb::NT, sizeof(svb::PlanSmem), s>>>(conf, num_drafts, B, K, cost, admitted,
+                                                                     budget, best_rate);
     return cudaGetLastError() == cudaSuccess ? SPEC_VERIFY_OK : SPEC_VERIFY_ECUDA;
 }

@@ -113,7 +113,7 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert pb(fake, None, 0, 7, fake, fake, fake, None, fake, n, None) == -1
     assert pb(fake, None, 4, 7, P(0x10004), fake, fake, None, fake, n, None) == -1  # cost not 8-aligned
     assert pb(fake, None, 4, 7, fake, fake, fake, None, fake, ctypes.c_size_t(8), None) == -2
-    assert lib.spec_verify_plan_budget_workspace_bytes(512, 7) == 20 * 512 * 7
+    assert lib.spec_verify_plan_budget_workspace_bytes(512, 7) == 256
     assert lib.spec_verify_plan_budget_workspace_bytes(2341, 7) == 0
     # KV compaction: (pool, num_slots, row_bytes, planes, plane_stride, slot_table, max_pos,
     # committed_in, committed_out, accept_index, accept_len, B, N, dev_status, stream)
