@@ -640,14 +640,29 @@ __global__ void __launch_bounds__(stream_threads(KIND), 1) sv_stream_kernel(cons
     float cs = P.cs;
     float thr = NEG_INF;
     bool greedy_b = false;
+    // A warp's claims only grow, by about a round of claims at a time, so its chunk's row (and the
+    // row's request and node) are advanced from the last claim's instead of divided out afresh.
+    int64_t r = -1, rq = 0;  // the row, and its first chunk's index
+    int b = 0, n = -1;       // its request and node (rows < 2^31)
     while ((int64_t)c < nq) {
         unsigned nxt = 0;
         if (lane == 0) nxt = atomicAdd(&next_chunk, 1u);
         const int64_t q = q0 + c;
-        const int64_t r = q / P.nch;
-        const int64_t j = q - r * P.nch;
-        const int b = (int)(r / P.rpr);  // rows < 2^31
-        const int n = (int)(r - (int64_t)b * P.rpr);
+        if (r < 0 || q - rq >= 4 * P.nch) {
+            r = q / P.nch;
+            rq = r * P.nch;
+            b = (int)(r / P.rpr);
+            n = (int)(r - (int64_t)b * P.rpr);
+        }
+        while (q - rq >= P.nch) {
+            ++r;
+            rq += P.nch;
+            if (++n == P.rpr) {
+                n = 0;
+                ++b;
+            }
+        }
+        const int64_t j = q - rq;
         const Seg sg = chunk_of<VEC>(P, r, j);
         const T *row = reinterpret_cast<const T *>(P.logits) + r * P.V;
         float *caps = P.caps + (int64_t)b * P.rpr;
