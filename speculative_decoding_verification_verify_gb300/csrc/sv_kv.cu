@@ -26,14 +26,29 @@
 
 namespace svkv {
 
-constexpr int NT = 128;         // threads per CTA
-constexpr int K = 4;            // 16-byte vectors (columns) per thread
-constexpr int SB = 4;           // path steps whose rows a thread holds at once
+#ifndef SV_KV_NT
+#define SV_KV_NT 128
+#endif
+#ifndef SV_KV_K
+#define SV_KV_K 4
+#endif
+#ifndef SV_KV_SB
+#define SV_KV_SB 2
+#endif
+#ifndef SV_KV_MINB
+#define SV_KV_MINB 8
+#endif
+constexpr int NT = SV_KV_NT;    // threads per CTA
+constexpr int K = SV_KV_K;      // 16-byte vectors (columns) per thread
+constexpr int SB = SV_KV_SB;    // path steps whose rows a thread holds at once
+// CTAs resident per SM the registers are budgeted for: most of a call's time is each CTA's chain
+// of dependent round trips (indices, slots, data), so more CTAs in flight per SM hide more of it
+// (two steps held and eight CTAs of 128 threads, 64 registers, beat four steps and five CTAs).
 constexpr int CHUNK = NT * K;   // vectors per CTA
 constexpr int MAX_NODES = 64;
 
 // pool_vec: the pool's extent in 16-byte vectors (for the range checks of debug builds).
-__global__ void __launch_bounds__(NT) kv_compact_kernel(uint4 *pool, int64_t num_slots, int64_t row_vec,
+__global__ void __launch_bounds__(NT, SV_KV_MINB) kv_compact_kernel(uint4 *pool, int64_t num_slots, int64_t row_vec,
                                                         int64_t plane_vec, int64_t work, int64_t pool_vec,
                                                         const int32_t *slot_table, int max_pos,
                                                         const int32_t *committed_in, int32_t *committed_out,
