@@ -11,8 +11,11 @@
 // digits: 2 levels for bf16, 4 for fp32): at each level a pass over the row (16-byte loads)
 // histograms the next digit of the keys that match the chosen prefix (counts for top-k, masses
 // 2^((l - max) * cs) for top-p) in per-warp shared-memory copies, and one warp walks the bins
-// from the top.  The masses are fp32 terms summed in fp64, so a row's top-p crossing is placed
-// within about 2e-7 of its mass (the terms' own error) whatever the row's length.
+// from the top.  The masses are fp32 terms summed in 64-bit fixed point (units of 2^-shift of the
+// row maximum's term, shift = 62 - bits(V), so no row's sum overflows; integer atomics and exact
+// sums, GB300 having few fp64 units), so a row's top-p crossing is placed within about 2e-7 of
+// its mass: the terms' own error, the truncation adding less than V^2 2^-62 of the maximum's term
+// (4e-9 at V = 128256, below 1e-6 up to V = 2^21).
 #pragma once
 
 #include <climits>
@@ -106,7 +109,7 @@ struct TopkpSmem {
     double mass[TK_BINS];
     union {                          // per-warp histograms of one pass, merged into cnt / mass
         int wcnt[TK_WARPS][TK_BINS];
-        double wmass[TK_WARPS][TK_BINS];
+        unsigned long long wmass[TK_WARPS][TK_BINS];  // fixed point (see fixed_term)
     };
     float wmax[NT_TK / 32];
     int sel;           // chosen digit
@@ -215,6 +218,24 @@ __device__ __forceinline__ void for_each_key(const void *row, int64_t rowflat, i
     }
 }
 
+// A term t in [0, 1] as an integer in units of 2^-shift, rounded down (an error below 2^-shift):
+// the bit pattern's mantissa shifted by its exponent, integer operations only.
+__device__ __forceinline__ unsigned long long fixed_term(float t, int shift)
+{
+    const uint32_t u = __float_as_uint(t);
+    const int ex = (int)(u >> 23) - 127;  // t = 1.m * 2^ex, ex <= 0
+    if (!(t > 0.f) || ex + shift < 0) return 0ull;
+    const unsigned long long m = (u & 0x7fffffu) | 0x800000u;
+    const int s = ex + shift - 23;
+    return s >= 0 ? m << s : m >> (-s);
+}
+
+// The fixed-point unit of a row of V terms in [0, 1]: V * 2^shift stays below 2^62.
+__device__ __forceinline__ int mass_shift(int64_t V)
+{
+    return 62 - (64 - __clzll((long long)V));
+}
+
 // Histogram of the next digit of the keys that match `prefix` on the bits above this level's
 // digit and are >= floor_key: counts (MASS false) or masses 2^((l - mx) * cs) (MASS true).  Each
 // warp adds every counted key to its own copy with a shared-memory atomic, and the copies are
@@ -231,7 +252,7 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
     const int top = sh + 8;
     const int warp = threadIdx.x >> 5;
     if (MASS)
-        for (int i = threadIdx.x; i < TK_WARPS * TK_BINS; i += NT_TK) (&S.wmass[0][0])[i] = 0.0;
+        for (int i = threadIdx.x; i < TK_WARPS * TK_BINS; i += NT_TK) (&S.wmass[0][0])[i] = 0ull;
     else
         for (int i = threadIdx.x; i < TK_WARPS * TK_BINS; i += NT_TK) (&S.wcnt[0][0])[i] = 0;
     __syncthreads();
@@ -241,10 +262,11 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
     const float fl = KeyOf<T>::value(fk);
     const bool skip = fk > KeyOf<T>::key_of_bits(sizeof(T) == 2 ? 0xff80u : 0xff800000u) && fl == fl;
     float vmx = NEG_INF;
+    const int fsh = mass_shift(V);
     auto visit = [&](uint32_t k) {
         if ((top >= 32 || (k >> top) == (prefix >> top)) && k >= floor_key) {
             const int d = (int)((k >> sh) & 0xffu);
-            if (MASS) atomicAdd(&S.wmass[warp][d], (double)ex2((KeyOf<T>::value(k) - mx) * cs));
+            if (MASS) atomicAdd(&S.wmass[warp][d], fixed_term(ex2((KeyOf<T>::value(k) - mx) * cs), fsh));
             else atomicAdd(&S.wcnt[warp][d], 1);
         }
     };
@@ -254,13 +276,13 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
     __syncthreads();
     for (int i = threadIdx.x; i < TK_BINS; i += NT_TK) {
         int c = 0;
-        double m = 0.0;
+        unsigned long long m = 0ull;
         if (MASS)
             for (int w = 0; w < TK_WARPS; ++w) m += S.wmass[w][i];
         else
             for (int w = 0; w < TK_WARPS; ++w) c += S.wcnt[w][i];
         S.cnt[i] = c;
-        S.mass[i] = m;
+        S.mass[i] = MASS ? ldexp((double)m, -fsh) : 0.0;  // 256 conversions a pass, not one per logit
     }
     __syncthreads();
 }

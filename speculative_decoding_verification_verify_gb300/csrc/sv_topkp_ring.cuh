@@ -164,19 +164,10 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t pari
     return true;
 }
 
-// A term t in [0, 1] as an integer in units of 2^-44, rounded down (an error below 2^-44): the
-// bit pattern's mantissa shifted by its exponent, integer operations only.  A row's masses,
-// count times term summed over levels, then stay below 2^63 for rows of up to 2^19 logits, and
-// the sums are exact; the top-p crossing is placed within about 1e-8 of the row maximum's term.
-__device__ __forceinline__ unsigned long long fixed44(float t)
-{
-    const uint32_t u = __float_as_uint(t);
-    const int ex = (int)(u >> 23) - 127;  // t = 1.m * 2^ex, ex <= 0
-    if (!(t > 0.f) || ex < -64) return 0ull;
-    const unsigned long long m = (u & 0x7fffffu) | 0x800000u;
-    const int sh = ex + 44 - 23;
-    return sh >= 0 ? m << sh : m >> (-sh);
-}
+// A term in units of 2^-44 of the row maximum's term (see fixed_term): a row's masses, count times
+// term summed over levels, stay below 2^63 for rows of up to 2^19 logits, and the sums are exact;
+// the top-p crossing is placed within about 1e-8 of the row maximum's term.
+__device__ __forceinline__ unsigned long long fixed44(float t) { return fixed_term(t, 44); }
 
 // What becomes of row r: kind 0 not filtered (threshold -inf), 1 this kernel, 2 the general one.
 struct RingRow {
