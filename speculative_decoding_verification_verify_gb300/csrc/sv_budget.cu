@@ -13,8 +13,8 @@
 //      memory).
 //   2. Every key's rank in the whole batch: its local index plus, for each other CTA, the count of
 //      its keys that come first (binary searches in local copies of the other CTAs' sorted keys,
-//      laid out as breadth-first search trees, and short walks on for the next key; equal keys
-//      are ordered by CTA).  Each key is stored at its rank in the owning CTA's slice,
+//      laid out as breadth-first search trees and stepped together; equal keys are ordered by
+//      CTA).  Each key is stored at its rank in the owning CTA's slice,
 //      so CTA c ends with positions [c 2048, c 2048 + 2048) of the sorted order.  Equal scores come
 //      out in some order: the gains depend only on the values, and admission orders ties as the
 //      rule does.
@@ -67,7 +67,6 @@ struct PlanSmem {
     uint32_t fin[PER];          // this CTA's slice of the batch's sorted order
     uint32_t all[CL][PER];      // staged confidences, then every other CTA's keys: a search tree
                                 //  at [1, PER) in breadth-first order, the largest key at [0]
-    uint32_t srt[CL][PER];      // every other CTA's keys in sorted order
     unsigned long long wsum[NW];
     unsigned long long cg_[PER + 1];  // candidates' gains
     int cand[PER + 1];                // candidate budgets (at most this CTA's budgets)
@@ -277,7 +276,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         uint32_t *dst = &S.all[q][0];
         for (int x = tid; x < PER / 4; x += NT) {
             const uint4 v = src[x];
-            reinterpret_cast<uint4 *>(&S.srt[q][0])[x] = v;
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -288,24 +286,32 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     }
     __syncthreads();
     {
-        // Thread t ranks keys 2t and 2t + 1: the first by a tree search in each other CTA's keys,
-        // the second by a short walk on from there in the sorted copy (a search when it is long).
+        // Thread t ranks keys 2t and 2t + 1: for each of them a tree search in every other CTA's
+        // keys, the fourteen searches stepped together level by level so that their loads are in
+        // flight at once.
         const uint32_t k0 = S.loc[2 * tid], k1 = S.loc[2 * tid + 1];
+        int j0[CL], j1[CL];
+#pragma unroll
+        for (int q = 0; q < CL; ++q) j0[q] = j1[q] = 1;
+#pragma unroll
+        for (int l = 0; l < TREE_H; ++l) {
+#pragma unroll
+            for (int q = 0; q < CL; ++q) {
+                if (q == c) continue;
+                const bool up = q < c;
+                const uint32_t x0 = S.all[q][j0[q]], x1 = S.all[q][j1[q]];
+                j0[q] = 2 * j0[q] + ((up ? x0 <= k0 : x0 < k0) ? 1 : 0);
+                j1[q] = 2 * j1[q] + ((up ? x1 <= k1 : x1 < k1) ? 1 : 0);
+            }
+        }
         int r0 = 2 * tid, r1 = 2 * tid + 1;
+#pragma unroll
         for (int q = 0; q < CL; ++q) {
             if (q == c) continue;
             const bool up = q < c;
-            const int n0 = count_below(S.all[q], k0, up);
-            int n1 = n0;
-            const uint32_t *sq = S.srt[q];
-            int steps = 0;
-            while (n1 < PER && (up ? sq[n1] <= k1 : sq[n1] < k1) && steps < 8) {
-                ++n1;
-                ++steps;
-            }
-            if (steps == 8) n1 = count_below(S.all[q], k1, up);
-            r0 += n0;
-            r1 += n1;
+            const uint32_t last = S.all[q][0];  // the largest key, outside the tree
+            r0 += (j0[q] - PER) + ((up ? last <= k0 : last < k0) ? 1 : 0);
+            r1 += (j1[q] - PER) + ((up ? last <= k1 : last < k1) ? 1 : 0);
         }
         if (SV_INB(r0, CL * PER, 905)) *peer(&S.fin[r0 % PER], r0 / PER) = k0;
         if (SV_INB(r1, CL * PER, 905)) *peer(&S.fin[r1 % PER], r1 / PER) = k1;
