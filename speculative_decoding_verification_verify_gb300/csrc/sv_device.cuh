@@ -28,6 +28,10 @@ __host__ __device__ constexpr int stream_threads(int kind)
 {
     return kind == 2 || kind == 3 ? NT_SV : (kind == 4 ? NT_S4 : NT_S);
 }
+#ifndef SV_RESID_GROUPS
+#define SV_RESID_GROUPS 2
+#endif
+constexpr int RESID_GROUPS = SV_RESID_GROUPS;  // 8-column groups a lane of the residual sums loads at once
 constexpr int MAX_RPR = 64;   // rows per request: k + 1 <= 64 (chain) or N <= 64 (tree)
 constexpr int B_MAX = 65536;  // most requests per call (size of the fixed counter region)
 constexpr int C2_MAX = 1024;  // upper bound on column chunks of the residual kernel
