@@ -23,7 +23,7 @@
  *     count and shared memory per SM and raises the dynamic shared-memory limits of the kernels
  *     that take more than the default (cudaFuncSetAttribute: the finalising kernels, which size
  *     their request so that at most ceil(B / SMs) of their CTAs share an SM, and the top-k / top-p
- *     ring kernel's 218 KiB); make it before any stream capture on that device.  The library keeps
+ *     ring kernel's 109 KiB); make it before any stream capture on that device.  The library keeps
  *     this per device for the life of the process, so it must not be used again after
  *     cudaDeviceReset.
  *   - The return value is a host status, known when the call returns:

@@ -203,3 +203,25 @@ def test_no_wait_ran_out():
         sv.spec_verify_rejection_ex(inp.logits, inp.drafts, None, top_k=tk, top_p=tp, seed=1, offset=i)
     torch.cuda.synchronize()
     assert sv.spec_verify_wait_timeouts() == 0
+
+
+def test_topkp_ring_hands_rows_to_the_general_kernel():
+    """One call whose rows take every route: ordinary rows (the one-read kernel), fully tied rows
+    (more groups reach L than the kernel lists, so the general kernel takes them), rows with one
+    logit far above the rest (the key range [L, max] is too wide), and top-p alone (general)."""
+    B, k, V = 6, 3, 128256
+    g = torch.Generator(device=DEV).manual_seed(31)
+    lv = torch.randn((B, k + 1, V), generator=g, device=DEV) * 2.0
+    lv[1] = 0.75                      # every logit equal
+    lv[2] = torch.randn((k + 1, V), generator=g, device=DEV) * 0.5
+    lv[2, :, 777] = 90.0              # one spike far above a flat row
+    lv[3, :, ::2] = 1.5               # half the row tied at one level
+    logits = lv.to(torch.bfloat16).contiguous()
+    drafts = torch.randint(0, V, (B, k), generator=g, device=DEV, dtype=torch.int32)
+    drafts[2, 0] = 777
+    inp = wl.ChainInputs("routes", logits, drafts, None, 1.0, 91)
+    tk = np.array([50, 20, 100, 200, 0, 256], np.int32)
+    tp = np.array([0.9, 1.0, 0.95, 0.5, 0.8, 1.0], np.float32)
+    run_chain(inp, tk, tp)
+    run_chain(inp, tk, None, offset=2)
+    assert sv.spec_verify_wait_timeouts() == 0
