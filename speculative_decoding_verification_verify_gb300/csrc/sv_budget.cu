@@ -11,13 +11,14 @@
 //      whose ascending order is descending score; slots past a request's draft count, and past n,
 //      take the key of a zero score.  Each CTA sorts its 2048 keys (a bitonic network in shared
 //      memory).
-//   2. Every key's rank in the whole batch: its local index plus, for each other CTA, the count of
-//      its keys that come first (binary searches in local copies of the other CTAs' sorted keys,
-//      laid out as breadth-first search trees and stepped together; equal keys are ordered by
-//      CTA).  Each key is stored at its rank in the owning CTA's slice,
-//      so CTA c ends with positions [c 2048, c 2048 + 2048) of the sorted order.  Equal scores come
-//      out in some order: the gains depend only on the values, and admission orders ties as the
-//      rule does.
+//   2. The batch's sorted order, by three rounds of merging: round L merges, in every group of 2^L
+//      CTAs, the sorted sequences of its two halves, each CTA writing its own 2048 positions of the
+//      group's merge.  The merge path gives the two ends of that slice (a 32-way search by one warp
+//      in the other CTAs' keys), the two pieces between them are copied in, and each thread merges
+//      two positions (one merge-path search in the local copies).  Equal keys: the lower half's
+//      first.  CTA c ends with positions [c 2048, c 2048 + 2048) of the sorted order.  Equal
+//      scores come out in some order: the gains depend only on the values, and admission orders
+//      ties as the rule does.
 //   3. gain[b] = the sum of the b best scores, a scan in 64-bit fixed point (units of 2^-49: exact
 //      for scores >= 2^-26, the rest truncated by less than 2^-49 each, so B + gain is within
 //      64 * 2^-49 ~ 1e-13 of exact relative to B, as n <= 64 B); the rate (B + gain[b]) / cost[b]
@@ -49,35 +50,34 @@ constexpr int PER = MAX_SLOTS / CL;   // slots of a CTA
 constexpr int KPT = PER / NT;         // slots of a thread
 constexpr uint32_t ZERO_KEY = 0xffffffffu;  // ~bits(+0): the last key; also the padding
 constexpr int FIX_SHIFT = 49;
-constexpr int TREE_H = 11;            // the other CTAs' sorted keys as trees of 2^11 - 1 keys plus the last
-static_assert(PER == 1 << TREE_H, "a CTA's keys: a perfect tree and one more");
-
-// Breadth-first index (1-based) of the key at in-order position i (1-based) of a perfect binary
-// search tree of height TREE_H: a binary search then reads consecutive words at each level, so a
-// warp's probes fall in distinct banks (on a sorted array they would all fall in one).
-__device__ __forceinline__ int bfs_of(int i)
-{
-    const int z = __ffs(i) - 1;  // the node's height above the leaves
-    return (i >> (z + 1)) | (1 << (TREE_H - 1 - z));
-}
+constexpr int LOG_PER = 11;
+static_assert(PER == 1 << LOG_PER, "a CTA's slots: a power of two");
 
 struct PlanSmem {
-    uint32_t loc[PER];          // this CTA's keys, sorted locally
+    uint32_t loc[PER];          // this CTA's keys sorted locally; later the second merge round's output
     uint32_t orig[PER];         // the same keys in slot order (request-major)
-    uint32_t fin[PER];          // this CTA's slice of the batch's sorted order
-    uint32_t all[CL][PER];      // staged confidences, then every other CTA's keys: a search tree
-                                //  at [1, PER) in breadth-first order, the largest key at [0]
+    uint32_t fin[PER];          // the first and third merge rounds' output: at the end, this CTA's
+                                //  slice of the batch's sorted order
+    union {
+        float cf[PER + 2 * MAX_K];  // the confidences of the requests touching this CTA's slots
+        uint32_t tmp[PER];          // a merge round's two pieces
+    };
+    double cst[PER];            // cost[s0 + x + 1]: the costs of this CTA's budgets
+    double cost0;               // cost[0] (CTA 0)
+    int nd[PER + 2];            // num_drafts of the requests touching this CTA's slots, as given
     unsigned long long wsum[NW];
     unsigned long long cg_[PER + 1];  // candidates' gains
     int cand[PER + 1];                // candidate budgets (at most this CTA's budgets)
-    int wcnt[NW], wcnt2[NW];
+    int wcnt[NW];
     float wmax[NW];
+    int split[2];               // a merge round's split at this slice's two ends
+    int lohi[2];                // valid keys below s*'s key, at or below it
     // Published to the cluster:
     unsigned long long total;   // fixed-point sum of this CTA's slice (valid positions)
     double bn, bc;              // this CTA's best candidate (rate numerator, cost) ...
     int bb;                     // ... and its budget (-1: none)
     float maxrate;
-    int nvalid, ncand, above, ties;
+    int nvalid, ncand;
     uint32_t skey;              // the key of the budget's last slot
 };
 
@@ -152,31 +152,35 @@ __device__ __forceinline__ int block_excl_scan(int x, int lane, int warp, int *w
     return before;
 }
 
-// Count of keys of a tree copy t below k (upper: at or below k): one probe per level, the leaf
-// position reached is the count among the tree's keys, and t[0] (the largest key) adds one.
-__device__ __forceinline__ int count_below(const uint32_t *t, uint32_t k, bool upper)
+// Global-to-shared copies that do not pass through registers, so that all of a thread's loads are
+// in flight at once; cp_async_wait() waits for this thread's.
+__device__ __forceinline__ void cp_async4(void *dst, const void *src)
 {
-    int j = 1;
-#pragma unroll
-    for (int l = 0; l < TREE_H; ++l) {
-        const uint32_t x = t[j];
-        j = 2 * j + ((upper ? x <= k : x < k) ? 1 : 0);
-    }
-    const uint32_t x = t[0];
-    return (j - PER) + ((upper ? x <= k : x < k) ? 1 : 0);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
 }
-
-// The same count on a plain sorted array a[0, PER).
-__device__ __forceinline__ int count_sorted(const uint32_t *a, uint32_t k, bool upper)
+__device__ __forceinline__ void cp_async8(void *dst, const void *src)
 {
-    int pos = 0;
-#pragma unroll
-    for (int step = PER / 2; step > 0; step >>= 1) {
-        const uint32_t x = a[pos + step - 1];
-        pos += (upper ? x <= k : x < k) ? step : 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The first index in [lo, hi] at which the predicate f (true on a prefix, then false) is false,
+// f(hi) taken as false: one warp, each round probing 32 evenly spaced points (f is evaluated only
+// below hi) and keeping the interval between the last true and the first false probe.  A range of
+// 16385 takes three rounds.
+template <class F>
+__device__ __forceinline__ int warp_first_false(int lo, int hi, int lane, F f)
+{
+    while (hi > lo) {
+        const int step = (hi - lo + 31) >> 5;
+        const int p = lo + (lane + 1) * step - 1;
+        const int t = __popc(__ballot_sync(0xffffffffu, p < hi && f(p)));
+        lo += t * step;
+        hi = min(hi, lo + step - 1);
     }
-    const uint32_t x = a[pos];
-    return pos + ((upper ? x <= k : x < k) ? 1 : 0);
+    return lo;
 }
 
 // One compare-exchange of a bitonic stage: elements e (this lane's x) and e ^ j (the partner's y),
@@ -235,21 +239,33 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     const int n = B * K;
     auto drafts_of = [&](int r) { return num_drafts ? min(max(num_drafts[r], 0), K) : K; };
     auto peer = [&](auto *p, int rank) { return cluster.map_shared_rank(p, rank); };
-    // 1. Keys of slots [s0, s1): the confidences of the requests touching them staged first.
+    // 1. Keys of slots [s0, s1).  Staged first, all in flight together: the confidences of the
+    // requests touching them, their draft counts, and the costs of this CTA's budgets.
     const int s0 = c * PER, s1 = min(s0 + PER, n);
-    float *cf = reinterpret_cast<float *>(&S.all[0][0]);
     const int r0 = s0 < n ? s0 / K : 0, r1 = s1 > s0 ? (s1 - 1) / K + 1 : 0;  // requests [r0, r1)
     const int c0 = r0 * K, nc = r1 > r0 ? min(r1 * K, n) - c0 : 0;
-    for (int j = tid; j < nc; j += NT) cf[j] = SV_INB(c0 + j, n, 901) ? conf[c0 + j] : 0.f;
-    for (int x = tid; x < PER; x += NT) S.loc[x] = ZERO_KEY;
+    for (int j = tid; j < nc; j += NT) {
+        if (SV_INB(c0 + j, n, 901)) cp_async4(&S.cf[j], conf + c0 + j);
+        else S.cf[j] = 0.f;
+    }
+    if (num_drafts)
+        for (int r = r0 + tid; r < r1; r += NT) cp_async4(&S.nd[r - r0], num_drafts + r);
+    for (int x = tid; x < PER; x += NT) {
+        if (s0 + x + 1 <= n) cp_async8(&S.cst[x], cost + s0 + x + 1);
+        else S.cst[x] = 1.0;
+        S.loc[x] = ZERO_KEY;
+    }
+    if (c == 0 && tid == 0) cp_async8(&S.cost0, cost);
     if (tid == 0) S.ncand = 0;
+    cp_async_wait();
     __syncthreads();
+    auto nd_of = [&](int r) { return num_drafts ? min(max(S.nd[r - r0], 0), K) : K; };  // r in [r0, r1)
     int my_valid = 0;
     for (int r = r0 + tid; r < r1; r += NT) {
-        const int nd = drafts_of(r);
+        const int nd = nd_of(r);
         float run = 1.f;
         for (int i = 0; i < nd; ++i) {
-            run = run * clip01(cf[(r - r0) * K + i]);
+            run = run * clip01(S.cf[(r - r0) * K + i]);
             const int j = r * K + i;
             if (j >= s0 && j < s1) {
                 S.loc[j - s0] = key_of(run);
@@ -269,54 +285,51 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     int nv = 0;
 #pragma unroll
     for (int q = 0; q < CL; ++q) nv += nvq[q];
-    // 2. Copies of the other CTAs' sorted keys, then every local key's rank in the batch.
-    for (int q = 0; q < CL; ++q) {
-        if (q == c) continue;
-        const uint4 *src = reinterpret_cast<const uint4 *>(peer(&S.loc[0], q));
-        uint32_t *dst = &S.all[q][0];
-        for (int x = tid; x < PER / 4; x += NT) {
-            const uint4 v = src[x];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    // 2. Merge rounds L = 1, 2, 3: in each group of 2^L CTAs (from g0), the halves' sorted
+    // sequences A (CTAs g0 ..) and B (the rest), half PER keys each, merged into dst; this CTA
+    // writes positions [d0, d0 + PER) of the group's merge, d0 = (c - g0) PER.  The merge path at
+    // diagonal d: the count a of A's keys among the merge's first d, the first a at which
+    // A[a] <= B[d - a - 1] fails (A's keys first on ties).
+    for (int L = 1; L <= 3; ++L) {
+        const uint32_t *src = L == 2 ? S.fin : S.loc;
+        uint32_t *dst = L == 2 ? S.loc : S.fin;
+        const int half = 1 << (L - 1), g0 = c & ~(2 * half - 1), na = half * PER;
+        auto key_a = [&](int i) { return *peer(&src[i & (PER - 1)], g0 + (i >> LOG_PER)); };
+        auto key_b = [&](int i) { return *peer(&src[i & (PER - 1)], g0 + half + (i >> LOG_PER)); };
+        const int d0 = (c - g0) * PER;
+        if (warp < 2) {  // warp 0: the split at d0; warp 1: at d0 + PER
+            const int d = d0 + warp * PER;
+            const int a = warp_first_false(max(0, d - na), min(d, na), lane,
+                                           [&](int p) { return key_a(p) <= key_b(d - p - 1); });
+            if (lane == 0) S.split[warp] = a;
+        }
+        __syncthreads();
+        const int a0 = S.split[0], la = S.split[1] - a0, lb = PER - la, b0 = d0 - a0;
+        for (int e = tid; e < PER; e += NT) {
+            const bool in_a = e < la;
+            const int i = in_a ? a0 + e : b0 + (e - la);
+            S.tmp[e] = SV_INB(i, na, 907) ? (in_a ? key_a(i) : key_b(i)) : ZERO_KEY;
+        }
+        __syncthreads();
+        {
+            // Positions 2 tid and 2 tid + 1 of the slice: the merge path of the two local pieces.
+            const uint32_t *ta = S.tmp, *tb = S.tmp + la;
+            const int d = 2 * tid;
+            int lo = max(0, d - lb), hi = min(d, la);
+            while (lo < hi) {
+                const int m = (lo + hi) >> 1;
+                if (ta[m] <= tb[d - m - 1]) lo = m + 1;
+                else hi = m;
+            }
+            int ia = lo, ib = d - lo;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = 4 * x + e;  // in-order position i + 1; the last key goes to word 0
-                dst[i + 1 < PER ? bfs_of(i + 1) : 0] = w[e];
+            for (int e = 0; e < 2; ++e) {
+                const bool take_a = ia < la && (ib >= lb || ta[ia] <= tb[ib]);
+                dst[d + e] = take_a ? ta[ia++] : tb[ib++];
             }
         }
+        cluster.sync();  // the round's slices are complete, and its sources no longer read
     }
-    __syncthreads();
-    {
-        // Thread t ranks keys 2t and 2t + 1: for each of them a tree search in every other CTA's
-        // keys, the fourteen searches stepped together level by level so that their loads are in
-        // flight at once.
-        const uint32_t k0 = S.loc[2 * tid], k1 = S.loc[2 * tid + 1];
-        int j0[CL], j1[CL];
-#pragma unroll
-        for (int q = 0; q < CL; ++q) j0[q] = j1[q] = 1;
-#pragma unroll
-        for (int l = 0; l < TREE_H; ++l) {
-#pragma unroll
-            for (int q = 0; q < CL; ++q) {
-                if (q == c) continue;
-                const bool up = q < c;
-                const uint32_t x0 = S.all[q][j0[q]], x1 = S.all[q][j1[q]];
-                j0[q] = 2 * j0[q] + ((up ? x0 <= k0 : x0 < k0) ? 1 : 0);
-                j1[q] = 2 * j1[q] + ((up ? x1 <= k1 : x1 < k1) ? 1 : 0);
-            }
-        }
-        int r0 = 2 * tid, r1 = 2 * tid + 1;
-#pragma unroll
-        for (int q = 0; q < CL; ++q) {
-            if (q == c) continue;
-            const bool up = q < c;
-            const uint32_t last = S.all[q][0];  // the largest key, outside the tree
-            r0 += (j0[q] - PER) + ((up ? last <= k0 : last < k0) ? 1 : 0);
-            r1 += (j1[q] - PER) + ((up ? last <= k1 : last < k1) ? 1 : 0);
-        }
-        if (SV_INB(r0, CL * PER, 905)) *peer(&S.fin[r0 % PER], r0 / PER) = k0;
-        if (SV_INB(r1, CL * PER, 905)) *peer(&S.fin[r1 % PER], r1 / PER) = k1;
-    }
-    cluster.sync();  // #2: every CTA holds its slice of the sorted order
     // 3. Gains of this CTA's positions g = s0 + x (budget b = g + 1), then rates.
     const int xb = tid * KPT;  // this thread's positions [xb, xb + KPT), blocked for the scan
     unsigned long long own = 0ull;
@@ -346,6 +359,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         for (int q = 0; q < CL; ++q) before += tq[q];
     }
     const float Bf = (float)B, unit = 1.0f / (float)(1ull << FIX_SHIFT);
+    // The cost of budget b, for b = 0 (CTA 0) and this CTA's budgets [s0 + 1, s0 + PER].
+    auto cost_of = [&](int b) { return b == 0 ? S.cost0 : SV_INB(b - s0 - 1, PER, 903) ? S.cst[b - s0 - 1] : 1.0; };
     bool odd = false;  // a cost the fp32 prefilter cannot carry: every budget is compared exactly
     float r32[KPT + 1];
     unsigned long long gsum[KPT + 1];
@@ -364,7 +379,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
                 continue;
             }
             const unsigned long long gb = u < KPT ? g : 0ull;
-            const float inv = __fdividef(1.f, approx_f32(SV_INB(b, n + 1, 903) ? cost[b] : 1.0, odd));
+            const float inv = __fdividef(1.f, approx_f32(cost_of(b), odd));
             r32[u] = (Bf + (float)gb * unit) * inv;
             gsum[u] = gb;
             bud[u] = b;
@@ -407,7 +422,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         for (int q = lane; q < ncd; q += 32) {
             const int b = S.cand[q];
             const double num = (double)B + (double)S.cg_[q] * (1.0 / (double)(1ull << FIX_SHIFT));
-            const double cb = SV_INB(b, n + 1, 903) ? cost[b] : 1.0;
+            const double cb = cost_of(b);
             if (beats(num, cb, b, bn, bc, bb)) {
                 bn = num;
                 bc = cb;
@@ -453,32 +468,30 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         if (rate_out) *rate_out = bn / bc;
     }
     // s*: the key at sorted position budget - 1 (in its owner's slice); the valid slots scoring
-    // above it and at it, counted in the batch's sorted keys (this CTA's and the other CTAs' trees).
-    if (tid == 0) {
-        uint32_t skey = 0u;
-        int above = 0, ties = 0;
+    // above it and at it, by searches in the batch's sorted keys (warp 0: keys below s*'s key;
+    // warp 1: at or below it).
+    if (warp < 2) {
+        uint32_t sk = 0u;
+        int cnt = 0;
         if (budget > 0 && SV_INB(budget - 1, CL * PER, 904)) {
-            skey = *peer(&S.fin[(budget - 1) % PER], (budget - 1) / PER);
-            int lo = 0, hi = 0;
-            for (int q = 0; q < CL; ++q) {
-                if (q == c) {  // this CTA's sorted keys: binary searches on the array
-                    lo += count_sorted(S.loc, skey, false);
-                    hi += count_sorted(S.loc, skey, true);
-                } else {
-                    lo += count_below(S.all[q], skey, false);
-                    hi += count_below(S.all[q], skey, true);
-                }
-            }
-            above = lo;
-            ties = skey == ZERO_KEY ? nv - lo : hi - lo;  // the padding shares the zero key
+            auto key_g = [&](int i) { return *peer(&S.fin[i & (PER - 1)], i >> LOG_PER); };
+            sk = key_g(budget - 1);
+            const bool upper = warp == 1;
+            cnt = warp_first_false(0, CL * PER, lane, [&](int i) {
+                const uint32_t x = key_g(i);
+                return upper ? x <= sk : x < sk;
+            });
         }
-        S.skey = skey;
-        S.above = above;
-        S.ties = ties;
+        if (lane == 0) {
+            S.lohi[warp] = cnt;
+            if (warp == 0) S.skey = sk;
+        }
     }
     __syncthreads();
     const uint32_t skey = S.skey;
-    const int above = S.above, ties = S.ties;
+    const int above = S.lohi[0];
+    // The padding shares the zero key: ties of a zero s* are the valid zero scores.
+    const int ties = budget <= 0 ? 0 : skey == ZERO_KEY ? nv - above : S.lohi[1] - above;
     // 4. Admission.  Request r is handled by the CTA owning its first slot; its keys are read from
     // the slot-order copies (the next CTA's for slots past this CTA's range).
     auto key_at = [&](int j) { return j < s1 ? S.orig[j - s0] : *peer(&S.orig[(j - s0) - PER], c + 1); };
@@ -488,7 +501,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         for (int r = ra + tid; r < rb; r += NT) {
             int a = 0;
             if (budget > 0) {
-                const int nd = drafts_of(r);
+                const int nd = nd_of(r);
                 for (int i = 0; i < nd; ++i) a += key_at(r * K + i) <= skey;
             }
             admitted[r] = a;
