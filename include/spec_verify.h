@@ -242,16 +242,17 @@ int spec_verify_tree_ex(const void *logits, int dtype, const int32_t *node_token
  *   cost        [B*K + 1] double, device: cost of a step that admits b draft slots (drafting
  *               plus verifying B + b tokens), any unit.
  * Slots are ranked by survival (equal survivals: the earlier position, then the lower request);
- * budget b scores (B + sum of the b best survivals) / cost[b], summed in fp64; the first maximal
- * b is chosen.  Outputs (device): admitted [B] (request r verifies its first admitted[r] drafts;
+ * budget b scores (B + sum of the b best survivals) / cost[b] (the sum in 64-bit fixed point,
+ * units of 2^-49; the rate to a relative 2^-45, so budgets whose rates agree to about 2^-44 may
+ * be taken in either order); the first maximal b is chosen.  Outputs (device): admitted [B] (request r verifies its first admitted[r] drafts;
  * they sum to *budget), *budget, and *best_rate (or NULL).  cost must be positive.
  * B * K <= 16384, K <= 64.  workspace: device memory, 8-byte aligned, of
  * spec_verify_plan_budget_workspace_bytes(B, K) bytes (0 for unsupported sizes; 256, reserved:
  * the planner keeps its work in shared memory), caller-owned, no initialisation needed.  One
  * launch, asynchronous on `stream`: a cluster of 8 CTAs sorts the slots' survival scores (a
- * bitonic sort per CTA, then each key's rank across the cluster through distributed shared
- * memory), sums them in 64-bit fixed point, picks the budget (fp32 rates, the near-best ones
- * compared again in fp64) and writes the admitted prefixes.  The first call on a device raises
+ * sort per CTA, then three merge rounds across the cluster through distributed shared memory),
+ * sums them in 64-bit fixed point, picks the budget (rate keys in fp32 double-float arithmetic,
+ * an integer maximum) and writes the admitted prefixes.  The first call on a device raises
  * the kernel's dynamic shared-memory limit (cudaFuncSetAttribute); make it before any stream
  * capture on that device.  SPEC_VERIFY_EINVAL for bad pointers, alignment or
  * sizes; SPEC_VERIFY_EWORKSPACE for a short or misaligned workspace; SPEC_VERIFY_ECUDA for a

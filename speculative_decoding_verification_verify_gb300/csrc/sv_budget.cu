@@ -9,8 +9,8 @@
 // (distributed shared memory), n = B * K <= 16384 slots, CTA c owning slots [c 2048, c 2048 + 2048):
 //   1. Survival products (fp32, the precision the decision is taken in) and sort keys ~bits(score),
 //      whose ascending order is descending score; slots past a request's draft count, and past n,
-//      take the key of a zero score.  Each CTA sorts its 2048 keys (a bitonic network in shared
-//      memory).
+//      take the key of a zero score.  Each CTA sorts its 2048 keys: blocks of 64 by a bitonic
+//      network in registers, then five merge-path rounds in shared memory.
 //   2. The batch's sorted order, by three rounds of merging: round L merges, in every group of 2^L
 //      CTAs, the sorted sequences of its two halves, each CTA writing its own 2048 positions of the
 //      group's merge.  The merge path gives the two ends of that slice (a 32-way search by one warp
@@ -22,9 +22,11 @@
 //   3. gain[b] = the sum of the b best scores, a scan in 64-bit fixed point (units of 2^-49: exact
 //      for scores >= 2^-26, the rest truncated by less than 2^-49 each, so B + gain is within
 //      64 * 2^-49 ~ 1e-13 of exact relative to B, as n <= 64 B); the rate (B + gain[b]) / cost[b]
-//      of every budget in fp32, the cluster's maximum M, and the budgets within 2^-16 of M compared
-//      exactly in fp64 (cross-multiplication, first maximum).  GB300 has few fp64 units; the
-//      prefilter keeps them to a handful of budgets.
+//      of every budget as a 64-bit key (exponent, then 47 mantissa bits; relative error below
+//      2^-45) computed in fp32 double-float arithmetic, and the first maximum of the keys: in each
+//      CTA, then over the eight CTAs.  Rates within about 2^-44 of each other may come out in
+//      either order.  No fp64 arithmetic: GB300 has few fp64 units, and a chain of fp64
+//      comparisons run by every thread cost microseconds.
 //   4. The admitted prefix of each request: its slots scoring above the chosen budget's last score
 //      s*, then its slots scoring s* in the rule's tie order (position, then request) while the
 //      budget lasts.
@@ -66,18 +68,16 @@ struct PlanSmem {
     double cost0;               // cost[0] (CTA 0)
     int nd[PER + 2];            // num_drafts of the requests touching this CTA's slots, as given
     unsigned long long wsum[NW];
-    unsigned long long cg_[PER + 1];  // candidates' gains
-    int cand[PER + 1];                // candidate budgets (at most this CTA's budgets)
+    unsigned long long wkey[NW];  // the warps' best rate keys ...
+    int wbud[NW];                 // ... and budgets
     int wcnt[NW];
-    float wmax[NW];
     int split[2];               // a merge round's split at this slice's two ends
     int lohi[2];                // valid keys below s*'s key, at or below it
     // Published to the cluster:
     unsigned long long total;   // fixed-point sum of this CTA's slice (valid positions)
-    double bn, bc;              // this CTA's best candidate (rate numerator, cost) ...
-    int bb;                     // ... and its budget (-1: none)
-    float maxrate;
-    int nvalid, ncand;
+    unsigned long long bkey;    // this CTA's best rate key ...
+    int bb;                     // ... and its budget
+    int nvalid;
     uint32_t skey;              // the key of the budget's last slot
 };
 
@@ -94,26 +94,64 @@ __device__ __forceinline__ unsigned long long fixed49(float v)
     return sh >= 0 ? m << sh : m >> (-sh);
 }
 
-// An fp32 approximation (relative error below 2^-23) of a positive double, by its bits; `odd` is
-// set for a value the approximation cannot carry (outside 2^-100 .. 2^100, or not positive).
-__device__ __forceinline__ float approx_f32(double d, bool &odd)
+constexpr int KEY_BIAS = 2048;  // rate keys: the binary exponent E + KEY_BIAS above 47 mantissa bits
+
+// An fp32 value of the 24 bits of m below its top bit (which sits at bit `top`), scaled into
+// [0, 2^-23) -- the low word of a double-float whose high word holds the top 24 bits.
+__device__ __forceinline__ float low24(unsigned long long m, int top)
 {
-    const unsigned long long u = (unsigned long long)__double_as_longlong(d);
-    const int ex = (int)((u >> 52) & 0x7ff) - 1023;
-    if ((u >> 63) || ex < -100 || ex > 100) {
-        odd = true;
-        return 1.f;
-    }
-    return __uint_as_float(((uint32_t)(ex + 127) << 23) | (uint32_t)((u >> 29) & 0x7fffffu));
+    return (float)(uint32_t)((m >> (top - 47)) & 0xffffffu) * 0x1p-47f;
 }
 
-// Is rate a = na / ca above rate b = nb / cb?  Costs are positive.
-__device__ __forceinline__ bool rate_above(double na, double ca, double nb, double cb) { return na * cb > nb * ca; }
-
-// The first maximum: does (na, ca, a) beat (nb, cb, b)?  b < 0: nothing yet.
-__device__ __forceinline__ bool beats(double na, double ca, int a, double nb, double cb, int b)
+// A sortable key of the rate N / c, N = nfix 2^-48 (0 < nfix < 2^63), c a double: the rate is
+// M 2^(E - 47) with M in [2^47, 2^48), and the key ((E + KEY_BIAS) << 47) | (M - 2^47) orders as
+// the rates do wherever they differ by more than about 2^-44 (relative error below 2^-45).  N and
+// c's mantissa are cut to 48 bits as fp32 pairs hi + lo (double-float numbers), divided by one
+// correctly rounded fp32 division, whose remainder nh - qh ch is exact under an fma, and one
+// correction step.  A cost that is not positive and finite gives key 0.  No fp64 arithmetic:
+// GB300 has few fp64 units.
+__device__ __forceinline__ unsigned long long rate_key(unsigned long long nfix, double c)
 {
-    return a >= 0 && (b < 0 || rate_above(na, ca, nb, cb) || (!rate_above(nb, cb, na, ca) && a < b));
+    const unsigned long long cb = (unsigned long long)__double_as_longlong(c);
+    int ec = (int)((cb >> 52) & 0x7ff);
+    unsigned long long mc = cb & ((1ull << 52) - 1);
+    if ((cb >> 63) || ec == 0x7ff || (ec == 0 && mc == 0)) return 0ull;
+    if (ec == 0) {  // subnormal: bring the top bit to bit 52
+        const int sh = __clzll((long long)mc) - 11;
+        mc = (mc << sh) & ((1ull << 52) - 1);
+        ec = 1 - sh;
+    }
+    mc |= 1ull << 52;
+    const float ch = __uint_as_float(0x3f800000u | (uint32_t)((mc >> 29) & 0x7fffffu)), cl = low24(mc, 52);
+    const int lz = __clzll((long long)nfix);
+    const unsigned long long m = nfix << lz;  // top bit at 63: N = (m 2^-63) 2^(15 - lz)
+    const float nh = __uint_as_float(0x3f800000u | (uint32_t)((m >> 40) & 0x7fffffu)), nl = low24(m, 63);
+    const float qh = __fdiv_rn(nh, ch);
+    const float r = fmaf(-qh, ch, nh) + fmaf(-qh, cl, nl);
+    const float ql = __fdividef(r, ch);
+    long long M = (long long)(qh * 0x1p47f) + __float2ll_rn(ql * 0x1p47f);  // quotient in (2^46, 2^48)
+    int E = (15 - lz) - (ec - 1023);
+    const int s = __clzll(M) - 16;  // normalise M into [2^47, 2^48)
+    M = s >= 0 ? M << s : M >> -s;
+    E -= s;
+    E = min(max(E + KEY_BIAS, 1), 4095);
+    return ((unsigned long long)E << 47) | ((unsigned long long)M & ((1ull << 47) - 1));
+}
+
+// The double nearest the rate a key stands for (to 48 bits), by its bits.
+__device__ __forceinline__ double rate_of_key(unsigned long long key)
+{
+    if (key == 0ull) return 0.0;
+    const int be = (int)(key >> 47) - KEY_BIAS + 1023;  // the double's biased exponent
+    if (be <= 0) return 0.0;
+    if (be >= 2047) return __longlong_as_double(0x7ff0000000000000ll);
+    return __longlong_as_double((long long)(((unsigned long long)be << 52) | ((key & ((1ull << 47) - 1)) << 5)));
+}
+
+// The first maximum: does budget a with key ka come before budget b with key kb?
+__device__ __forceinline__ bool beats(unsigned long long ka, int a, unsigned long long kb, int b)
+{
+    return ka > kb || (ka == kb && a < b);
 }
 
 __device__ __forceinline__ float clip01(float c) { return fminf(fmaxf(c, 0.f), 1.f); }  // NaN reads as 0
@@ -191,38 +229,60 @@ __device__ __forceinline__ uint32_t cx(uint32_t x, uint32_t y, int e, int j, int
     return (low == asc) ? min(x, y) : max(x, y);
 }
 
-// Bitonic sort of loc[0, PER) (ascending) by NT threads: thread t holds elements 2t and 2t + 1 for
-// the stages with j < 64 (within the thread, then across the warp by shuffles), and the stages
-// with j >= 64 go through shared memory, one pair per thread.
-__device__ __forceinline__ void bitonic_sort(uint32_t *loc, int tid, int lane)
+// Merge-path output of positions d and d + 1 of the merge of sorted ta[0, la) and tb[0, lb)
+// (d + 1 < la + lb; ta's keys first on ties) into out[d], out[d + 1]: the count of ta's keys among
+// the first d is the first a at which ta[a] <= tb[d - a - 1] fails.
+__device__ __forceinline__ void merge_two(const uint32_t *ta, int la, const uint32_t *tb, int lb, int d,
+                                          uint32_t *out)
+{
+    int lo = max(0, d - lb), hi = min(d, la);
+    while (lo < hi) {
+        const int m = (lo + hi) >> 1;
+        if (ta[m] <= tb[d - m - 1]) lo = m + 1;
+        else hi = m;
+    }
+    int ia = lo, ib = d - lo;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const bool take_a = ia < la && (ib >= lb || ta[ia] <= tb[ib]);
+        out[d + e] = take_a ? ta[ia++] : tb[ib++];
+    }
+}
+
+// Ascending sort of loc[0, PER) by NT threads, through tmp: blocks of 64 by a bitonic network in
+// registers (thread t holds elements 2t and 2t + 1, the stages across a warp by shuffles; the last
+// phase sorts every block ascending), then five merge-path rounds double the sorted blocks up to
+// PER, two positions per thread.
+__device__ __forceinline__ void local_sort(uint32_t *loc, uint32_t *tmp, int tid)
 {
     static_assert(PER == 2 * NT, "two elements per thread");
-    for (int k = 2; k <= PER; k <<= 1) {
-        int j = k >> 1;
-        for (; j >= 64; j >>= 1) {
-            __syncthreads();
-            const int i = ((tid & ~(j - 1)) << 1) | (tid & (j - 1)), q = i + j;
-            const uint32_t a = loc[i], b = loc[q];
-            const bool asc = (i & k) == 0;
-            loc[i] = asc ? min(a, b) : max(a, b);
-            loc[q] = asc ? max(a, b) : min(a, b);
-        }
-        __syncthreads();
-        uint32_t v0 = loc[2 * tid], v1 = loc[2 * tid + 1];
-        for (; j >= 2; j >>= 1) {
+    uint32_t v0 = loc[2 * tid], v1 = loc[2 * tid + 1];
+#pragma unroll
+    for (int k = 2; k <= 64; k <<= 1) {
+        const int kd = k == 64 ? PER : k;  // the direction bit of element e is e & kd
+#pragma unroll
+        for (int j = k >> 1; j >= 2; j >>= 1) {
             const int m = j >> 1;  // partner lane: lane ^ m (elements 2t + h and (2t + h) ^ j)
             const uint32_t y0 = __shfl_xor_sync(0xffffffffu, v0, m), y1 = __shfl_xor_sync(0xffffffffu, v1, m);
-            v0 = cx(v0, y0, 2 * tid, j, k);
-            v1 = cx(v1, y1, 2 * tid + 1, j, k);
+            v0 = cx(v0, y0, 2 * tid, j, kd);
+            v1 = cx(v1, y1, 2 * tid + 1, j, kd);
         }
-        {  // j == 1: within the thread
-            const bool asc = ((2 * tid) & k) == 0;
-            const uint32_t lo = min(v0, v1), hi = max(v0, v1);
-            v0 = asc ? lo : hi;
-            v1 = asc ? hi : lo;
-        }
-        loc[2 * tid] = v0;
-        loc[2 * tid + 1] = v1;
+        const bool asc = ((2 * tid) & kd) == 0;  // j == 1: within the thread
+        const uint32_t lo = min(v0, v1), hi = max(v0, v1);
+        v0 = asc ? lo : hi;
+        v1 = asc ? hi : lo;
+    }
+    tmp[2 * tid] = v0;
+    tmp[2 * tid + 1] = v1;
+    const uint32_t *src = tmp;
+    uint32_t *dst = loc;
+    for (int w = 64; w < PER; w <<= 1) {  // five rounds: tmp -> loc -> tmp -> loc -> tmp -> loc
+        __syncthreads();
+        const int base = (2 * tid) & ~(2 * w - 1);
+        merge_two(src + base, w, src + base + w, w, 2 * tid - base, dst + base);
+        const uint32_t *t = src;
+        src = dst;
+        dst = const_cast<uint32_t *>(t);
     }
     __syncthreads();
 }
@@ -256,7 +316,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         S.loc[x] = ZERO_KEY;
     }
     if (c == 0 && tid == 0) cp_async8(&S.cost0, cost);
-    if (tid == 0) S.ncand = 0;
     cp_async_wait();
     __syncthreads();
     auto nd_of = [&](int r) { return num_drafts ? min(max(S.nd[r - r0], 0), K) : K; };  // r in [r0, r1)
@@ -276,8 +335,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     const int part_valid = block_sum(my_valid, lane, warp, S.wcnt);
     for (int x = tid; x < PER; x += NT) S.orig[x] = S.loc[x];
     if (tid == 0) S.nvalid = part_valid;
-    // Local bitonic sort of loc (ascending keys).
-    bitonic_sort(S.loc, tid, lane);
+    local_sort(S.loc, S.tmp, tid);  // the confidences' staging area is free again
     cluster.sync();  // #1: every CTA's sorted keys and valid count are visible
     int nvq[CL];
 #pragma unroll
@@ -289,7 +347,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     // sequences A (CTAs g0 ..) and B (the rest), half PER keys each, merged into dst; this CTA
     // writes positions [d0, d0 + PER) of the group's merge, d0 = (c - g0) PER.  The merge path at
     // diagonal d: the count a of A's keys among the merge's first d, the first a at which
-    // A[a] <= B[d - a - 1] fails (A's keys first on ties).
+    // A[a] <= B[d - a - 1] fails (A's keys first on ties).  The last round also sums this CTA's
+    // slice (3., below), so that the round's cluster barrier publishes the total.
+    const int xb = tid * KPT;  // this thread's positions [xb, xb + KPT): those it merges in
+    unsigned long long before = 0ull;  // fixed-point sum of the valid positions before xb
     for (int L = 1; L <= 3; ++L) {
         const uint32_t *src = L == 2 ? S.fin : S.loc;
         uint32_t *dst = L == 2 ? S.loc : S.fin;
@@ -304,53 +365,42 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
             if (lane == 0) S.split[warp] = a;
         }
         __syncthreads();
-        const int a0 = S.split[0], la = S.split[1] - a0, lb = PER - la, b0 = d0 - a0;
+        const int a0 = S.split[0], la = S.split[1] - a0, b0 = d0 - a0;
         for (int e = tid; e < PER; e += NT) {
             const bool in_a = e < la;
             const int i = in_a ? a0 + e : b0 + (e - la);
             S.tmp[e] = SV_INB(i, na, 907) ? (in_a ? key_a(i) : key_b(i)) : ZERO_KEY;
         }
         __syncthreads();
-        {
-            // Positions 2 tid and 2 tid + 1 of the slice: the merge path of the two local pieces.
-            const uint32_t *ta = S.tmp, *tb = S.tmp + la;
-            const int d = 2 * tid;
-            int lo = max(0, d - lb), hi = min(d, la);
-            while (lo < hi) {
-                const int m = (lo + hi) >> 1;
-                if (ta[m] <= tb[d - m - 1]) lo = m + 1;
-                else hi = m;
-            }
-            int ia = lo, ib = d - lo;
+        merge_two(S.tmp, la, S.tmp + la, PER - la, xb, dst);
+        if (L == 3) {
+            // 3. The fixed-point sum of this CTA's slice, and of the valid positions before xb.
+            unsigned long long own = 0ull;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const bool take_a = ia < la && (ib >= lb || ta[ia] <= tb[ib]);
-                dst[d + e] = take_a ? ta[ia++] : tb[ib++];
+            for (int u = 0; u < KPT; ++u)
+                if (s0 + xb + u < nv) own += fixed49(score_of_key(dst[xb + u]));
+            unsigned long long incl = own;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
             }
+            if (lane == 31) S.wsum[warp] = incl;
+            __syncthreads();
+            static_assert(NW == 32, "one warp sum per lane");
+            const unsigned long long ws = S.wsum[lane];
+            unsigned long long wincl = ws;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, wincl, o);
+                if (lane >= o) wincl += y;
+            }
+            before = incl - own + __shfl_sync(0xffffffffu, wincl - ws, warp);
+            const unsigned long long ctot = __shfl_sync(0xffffffffu, wincl, 31);
+            if (tid == 0) S.total = ctot;
         }
-        cluster.sync();  // the round's slices are complete, and its sources no longer read
+        cluster.sync();  // the round's slices (and the totals) are complete, its sources no longer read
     }
-    // 3. Gains of this CTA's positions g = s0 + x (budget b = g + 1), then rates.
-    const int xb = tid * KPT;  // this thread's positions [xb, xb + KPT), blocked for the scan
-    unsigned long long own = 0ull;
-    for (int u = 0; u < KPT; ++u)
-        if (s0 + xb + u < nv) own += fixed49(score_of_key(S.fin[xb + u]));
-    unsigned long long incl = own;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) S.wsum[warp] = incl;
-    __syncthreads();
-    unsigned long long before = incl - own;
-    unsigned long long ctot = 0ull;
-    for (int w = 0; w < NW; ++w) {
-        if (w < warp) before += S.wsum[w];
-        ctot += S.wsum[w];
-    }
-    if (tid == 0) S.total = ctot;
-    cluster.sync();  // #3: slice totals
     {
         unsigned long long tq[CL];
 #pragma unroll
@@ -358,114 +408,88 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
 #pragma unroll
         for (int q = 0; q < CL; ++q) before += tq[q];
     }
-    const float Bf = (float)B, unit = 1.0f / (float)(1ull << FIX_SHIFT);
+    // Gains of this CTA's positions g = s0 + x (budget b = g + 1), their rates' keys, and the first
+    // maximum: of this thread's budgets, of the CTA's (shuffles, then one warp over the warps'),
+    // and of the cluster's (every CTA reduces the eight CTAs' bests the same way, so all agree).
     // The cost of budget b, for b = 0 (CTA 0) and this CTA's budgets [s0 + 1, s0 + PER].
     auto cost_of = [&](int b) { return b == 0 ? S.cost0 : SV_INB(b - s0 - 1, PER, 903) ? S.cst[b - s0 - 1] : 1.0; };
-    bool odd = false;  // a cost the fp32 prefilter cannot carry: every budget is compared exactly
-    float r32[KPT + 1];
-    unsigned long long gsum[KPT + 1];
-    int bud[KPT + 1];
-    float best32 = 0.f;
+    const unsigned long long bfix = (unsigned long long)B << (FIX_SHIFT - 1);  // B in units of 2^-48
+    unsigned long long bkey = 0ull;
+    int bbud = 0x7fffffff;
     {
         unsigned long long g = before;
-        for (int u = 0; u <= KPT; ++u) {
-            // u < KPT: budget s0 + xb + u + 1; u == KPT: budget 0 (CTA 0, thread 0 only)
-            const int b = u < KPT ? s0 + xb + u + 1 : 0;
-            bud[u] = -1;
-            if (u < KPT) {
-                if (b > nv) continue;
-                g += fixed49(score_of_key(S.fin[xb + u]));
-            } else if (c != 0 || tid != 0) {
-                continue;
+#pragma unroll
+        for (int u = 0; u < KPT; ++u) {
+            const int b = s0 + xb + u + 1;
+            if (b > nv) break;
+            g += fixed49(score_of_key(S.fin[xb + u]));
+            const unsigned long long k = rate_key(bfix + (g >> 1), cost_of(b));
+            if (beats(k, b, bkey, bbud)) {
+                bkey = k;
+                bbud = b;
             }
-            const unsigned long long gb = u < KPT ? g : 0ull;
-            const float inv = __fdividef(1.f, approx_f32(cost_of(b), odd));
-            r32[u] = (Bf + (float)gb * unit) * inv;
-            gsum[u] = gb;
-            bud[u] = b;
-            best32 = fmaxf(best32, r32[u]);
+        }
+        if (c == 0 && tid == 0) {  // budget 0
+            const unsigned long long k = rate_key(bfix, cost_of(0));
+            if (beats(k, 0, bkey, bbud)) {
+                bkey = k;
+                bbud = 0;
+            }
         }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) best32 = fmaxf(best32, __shfl_xor_sync(0xffffffffu, best32, o));
-    if (lane == 0) S.wmax[warp] = best32;
-    const bool any_odd = __syncthreads_or(odd);
-    if (tid == 0) {
-        float m = S.wmax[0];
-        for (int w = 1; w < NW; ++w) m = fmaxf(m, S.wmax[w]);
-        S.maxrate = any_odd ? __int_as_float(0x7f800000) : m;  // +inf: every budget is a candidate
-    }
-    cluster.sync();  // #4: the CTAs' maxima
-    float mq[CL];
-#pragma unroll
-    for (int q = 0; q < CL; ++q) mq[q] = *peer(&S.maxrate, q);
-    float M = 0.f;
-#pragma unroll
-    for (int q = 0; q < CL; ++q) M = fmaxf(M, mq[q]);
-    // Candidates: fp32 rates within 2^-16 of M (they err by less than 2^-20); all budgets when a
-    // cost fell outside the prefilter's range (M = +inf).
-    const float floor32 = M == __int_as_float(0x7f800000) ? -1.f : M * (1.f - 1.f / 65536.f);
-    for (int u = 0; u <= KPT; ++u)
-        if (bud[u] >= 0 && (floor32 < 0.f || r32[u] >= floor32)) {
-            const int q = atomicAdd(&S.ncand, 1);
-            if (SV_INB(q, PER + 1, 906)) {
-                S.cand[q] = bud[u];
-                S.cg_[q] = gsum[u];
-            }
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long ok = __shfl_xor_sync(0xffffffffu, bkey, o);
+        const int ob = __shfl_xor_sync(0xffffffffu, bbud, o);
+        if (beats(ok, ob, bkey, bbud)) {
+            bkey = ok;
+            bbud = ob;
         }
+    }
+    if (lane == 0) {
+        S.wkey[warp] = bkey;
+        S.wbud[warp] = bbud;
+    }
     __syncthreads();
     if (warp == 0) {
-        // This CTA's candidates compared exactly (fp64, cross-multiplied); the first maximum.
-        const int ncd = min(S.ncand, PER + 1);
-        double bn = 0.0, bc = 1.0;
-        int bb = -1;
-        for (int q = lane; q < ncd; q += 32) {
-            const int b = S.cand[q];
-            const double num = (double)B + (double)S.cg_[q] * (1.0 / (double)(1ull << FIX_SHIFT));
-            const double cb = cost_of(b);
-            if (beats(num, cb, b, bn, bc, bb)) {
-                bn = num;
-                bc = cb;
-                bb = b;
-            }
-        }
+        bkey = S.wkey[lane];
+        bbud = S.wbud[lane];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            const double on = __shfl_xor_sync(0xffffffffu, bn, o), oc = __shfl_xor_sync(0xffffffffu, bc, o);
-            const int ob = __shfl_xor_sync(0xffffffffu, bb, o);
-            if (beats(on, oc, ob, bn, bc, bb)) {
-                bn = on;
-                bc = oc;
-                bb = ob;
+            const unsigned long long ok = __shfl_xor_sync(0xffffffffu, bkey, o);
+            const int ob = __shfl_xor_sync(0xffffffffu, bbud, o);
+            if (beats(ok, ob, bkey, bbud)) {
+                bkey = ok;
+                bbud = ob;
             }
         }
         if (lane == 0) {
-            S.bn = bn;
-            S.bc = bc;
-            S.bb = bb;
+            S.bkey = bkey;
+            S.bb = bbud;
         }
     }
-    cluster.sync();  // #5: the CTAs' best candidates
-    // Every CTA reduces the eight bests the same way (first maximum), so all agree on the budget.
-    double bnq[CL], bcq[CL];
-    int bbq[CL];
+    cluster.sync();  // #2: the CTAs' bests
+    int budget;
+    {
+        unsigned long long kq[CL];
+        int bq[CL];
 #pragma unroll
-    for (int q = 0; q < CL; ++q) {
-        bnq[q] = *peer(&S.bn, q);
-        bcq[q] = *peer(&S.bc, q);
-        bbq[q] = *peer(&S.bb, q);
-    }
-    double bn = 0.0, bc = 1.0;
-    int budget = -1;
-    for (int q = 0; q < CL; ++q)
-        if (beats(bnq[q], bcq[q], bbq[q], bn, bc, budget)) {
-            bn = bnq[q];
-            bc = bcq[q];
-            budget = bbq[q];
+        for (int q = 0; q < CL; ++q) {
+            kq[q] = *peer(&S.bkey, q);
+            bq[q] = *peer(&S.bb, q);
         }
+        bkey = kq[0];
+        budget = bq[0];
+#pragma unroll
+        for (int q = 1; q < CL; ++q)
+            if (beats(kq[q], bq[q], bkey, budget)) {
+                bkey = kq[q];
+                budget = bq[q];
+            }
+    }
     if (c == 0 && tid == 0) {
         *budget_out = budget;
-        if (rate_out) *rate_out = bn / bc;
+        if (rate_out) *rate_out = rate_of_key(bkey);
     }
     // s*: the key at sorted position budget - 1 (in its owner's slice); the valid slots scoring
     // above it and at it, by searches in the batch's sorted keys (warp 0: keys below s*'s key;
@@ -543,7 +567,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
             }
         }
     }
-    cluster.sync();  // #6: no CTA leaves while another may still read its shared memory
+    cluster.sync();  // #3: no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace svb
