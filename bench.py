@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work spent timing the oracle baseline")
     ap.add_argument("--no-modes", action="store_true", help="skip the other verify modes")
+    ap.add_argument("--budget-shapes", default="512x7,2048x8",
+                    help="B x K shapes of the budget mode, comma-separated (default 512x7,2048x8)")
     ap.add_argument("--modes", default="all",
                     help="comma list of other modes to time: greedy, tree, block, with_q, b1k3, "
                          "variants, budget, kv_compact (default all)")
@@ -724,7 +726,8 @@ def other_modes(args, D, torch, sv, wl, dev, stream, peak):
     if "variants" in want:
         res.update(_variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak))
     if "budget" in want:
-        res.update(_budget_modes(torch, sv, dev, lib, P, cur, check))
+        shapes = [tuple(int(x) for x in t.split("x")) for t in args.budget_shapes.split(",") if t]
+        res.update(_budget_modes(torch, sv, dev, lib, P, cur, check, shapes))
     if "kv_compact" in want:
         res.update(_kv_mode(torch, wl, dev, lib, P, cur, check, status, peak, args.kv_max_pos))
     if int(status.item()) != 0:
@@ -942,12 +945,12 @@ def _variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, pe
     return res
 
 
-def _budget_modes(torch, sv, dev, lib, P, cur, check):
+def _budget_modes(torch, sv, dev, lib, P, cur, check, shapes=((512, 7), (2048, 8))):
     """The adaptive verification budget (keys, rank, pick) on B x K slots of random confidences
     with a roofline-shaped cost table; latency per plan."""
     res = {}
     g = torch.Generator(device=dev).manual_seed(5)
-    for B_, K_ in ((512, 7), (2048, 8)):
+    for B_, K_ in shapes:
         conf = torch.rand((B_, K_), generator=g, device=dev) * 0.5 + 0.5
         b = torch.arange(B_ * K_ + 1, device=dev, dtype=torch.float64)
         cost = 1.25e-3 + torch.clamp((B_ + b) * 3e-5 - 1e-3, min=0.0)

@@ -1296,7 +1296,6 @@ static int common_setup(Params &P, const void *logits, int dtype, int B, int rpr
     P.B = B;
     P.rpr = rpr;
     P.V = V;
-    P.v_inv = 1.0 / (double)V;
     P.total = (int64_t)B * rpr * V;
     P.nch = chunks_per_row(V, esize == 2 ? 8 : 4);
     P.nchunks = (int64_t)B * rpr * P.nch;

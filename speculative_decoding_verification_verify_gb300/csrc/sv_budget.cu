@@ -73,12 +73,14 @@ struct PlanSmem {
     int wcnt[NW];
     int split[2];               // a merge round's split at this slice's two ends
     int lohi[2];                // valid keys below s*'s key, at or below it
+    // Written by every CTA q of the cluster into slot q (stored ahead of a cluster barrier, so that
+    // after it each CTA reads its own copy):
+    unsigned long long tot_in[CL];  // fixed-point sums of the CTAs' slices (valid positions)
+    unsigned long long key_in[CL];  // the CTAs' best rate keys ...
+    int bud_in[CL];                 // ... budgets ...
+    uint32_t skey_in[CL];           // ... and the keys at those budgets' last positions
     // Published to the cluster:
-    unsigned long long total;   // fixed-point sum of this CTA's slice (valid positions)
-    unsigned long long bkey;    // this CTA's best rate key ...
-    int bb;                     // ... and its budget
     int nvalid;
-    uint32_t skey;              // the key of the budget's last slot
 };
 
 __device__ __forceinline__ float score_of_key(uint32_t k) { return __uint_as_float(~k); }
@@ -129,7 +131,7 @@ __device__ __forceinline__ unsigned long long rate_key(unsigned long long nfix, 
     const float qh = __fdiv_rn(nh, ch);
     const float r = fmaf(-qh, ch, nh) + fmaf(-qh, cl, nl);
     const float ql = __fdividef(r, ch);
-    long long M = (long long)(qh * 0x1p47f) + __float2ll_rn(ql * 0x1p47f);  // quotient in (2^46, 2^48)
+    long long M = (long long)(qh * 0x1p47f) + __float2ll_rn(ql * 0x1p47f);  // the quotient 2^47, in (2^46, 2^48)
     int E = (15 - lz) - (ec - 1023);
     const int s = __clzll(M) - 16;  // normalise M into [2^47, 2^48)
     M = s >= 0 ? M << s : M >> -s;
@@ -397,17 +399,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
             }
             before = incl - own + __shfl_sync(0xffffffffu, wincl - ws, warp);
             const unsigned long long ctot = __shfl_sync(0xffffffffu, wincl, 31);
-            if (tid == 0) S.total = ctot;
+            if (tid < CL) *peer(&S.tot_in[c], tid) = ctot;
         }
         cluster.sync();  // the round's slices (and the totals) are complete, its sources no longer read
     }
-    {
-        unsigned long long tq[CL];
-#pragma unroll
-        for (int q = 0; q < CL; ++q) tq[q] = q < c ? *peer(&S.total, q) : 0ull;
-#pragma unroll
-        for (int q = 0; q < CL; ++q) before += tq[q];
-    }
+    for (int q = 0; q < c; ++q) before += S.tot_in[q];
     // Gains of this CTA's positions g = s0 + x (budget b = g + 1), their rates' keys, and the first
     // maximum: of this thread's budgets, of the CTA's (shuffles, then one warp over the warps'),
     // and of the cluster's (every CTA reduces the eight CTAs' bests the same way, so all agree).
@@ -463,56 +459,50 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
                 bbud = ob;
             }
         }
-        if (lane == 0) {
-            S.bkey = bkey;
-            S.bb = bbud;
+        // The best budget's last position, b - 1, is this CTA's when b is in [s0 + 1, s0 + PER]
+        // (b is 0, or past the range when this CTA has no valid budget).
+        const uint32_t sk = bbud > s0 && bbud <= s0 + PER ? S.fin[bbud - 1 - s0] : 0u;
+        if (lane < CL) {
+            *peer(&S.key_in[c], lane) = bkey;
+            *peer(&S.bud_in[c], lane) = bbud;
+            *peer(&S.skey_in[c], lane) = sk;
         }
     }
     cluster.sync();  // #2: the CTAs' bests
-    int budget;
-    {
-        unsigned long long kq[CL];
-        int bq[CL];
-#pragma unroll
-        for (int q = 0; q < CL; ++q) {
-            kq[q] = *peer(&S.bkey, q);
-            bq[q] = *peer(&S.bb, q);
+    int budget = S.bud_in[0], win = 0;
+    bkey = S.key_in[0];
+    for (int q = 1; q < CL; ++q)
+        if (beats(S.key_in[q], S.bud_in[q], bkey, budget)) {
+            bkey = S.key_in[q];
+            budget = S.bud_in[q];
+            win = q;
         }
-        bkey = kq[0];
-        budget = bq[0];
-#pragma unroll
-        for (int q = 1; q < CL; ++q)
-            if (beats(kq[q], bq[q], bkey, budget)) {
-                bkey = kq[q];
-                budget = bq[q];
-            }
-    }
     if (c == 0 && tid == 0) {
         *budget_out = budget;
         if (rate_out) *rate_out = rate_of_key(bkey);
     }
-    // s*: the key at sorted position budget - 1 (in its owner's slice); the valid slots scoring
-    // above it and at it, by searches in the batch's sorted keys (warp 0: keys below s*'s key;
-    // warp 1: at or below it).
+    // s*: the key at sorted position budget - 1 (sent by its owner with its best); the valid slots
+    // scoring above it and at it, counted in the batch's sorted keys G: warp 0 the keys below s*'s
+    // key (budget - 1 unless G[budget - 2] ties it), warp 1 those at or below it (budget unless
+    // G[budget] ties it); a tie is resolved by a search over the positions past the neighbour.
+    const uint32_t skey = budget > 0 ? S.skey_in[win] : 0u;
     if (warp < 2) {
-        uint32_t sk = 0u;
         int cnt = 0;
-        if (budget > 0 && SV_INB(budget - 1, CL * PER, 904)) {
+        if (budget > 0) {
             auto key_g = [&](int i) { return *peer(&S.fin[i & (PER - 1)], i >> LOG_PER); };
-            sk = key_g(budget - 1);
-            const bool upper = warp == 1;
-            cnt = warp_first_false(0, CL * PER, lane, [&](int i) {
-                const uint32_t x = key_g(i);
-                return upper ? x <= sk : x < sk;
-            });
+            if (warp == 0) {
+                cnt = budget - 1;
+                if (cnt > 0 && !(key_g(cnt - 1) < skey))
+                    cnt = warp_first_false(0, cnt - 1, lane, [&](int i) { return key_g(i) < skey; });
+            } else {
+                cnt = budget;
+                if (cnt < CL * PER && key_g(cnt) <= skey)
+                    cnt = warp_first_false(cnt + 1, CL * PER, lane, [&](int i) { return key_g(i) <= skey; });
+            }
         }
-        if (lane == 0) {
-            S.lohi[warp] = cnt;
-            if (warp == 0) S.skey = sk;
-        }
+        if (lane == 0) S.lohi[warp] = cnt;
     }
     __syncthreads();
-    const uint32_t skey = S.skey;
     const int above = S.lohi[0];
     // The padding shares the zero key: ties of a zero s* are the valid zero scores.
     const int ties = budget <= 0 ? 0 : skey == ZERO_KEY ? nv - above : S.lohi[1] - above;

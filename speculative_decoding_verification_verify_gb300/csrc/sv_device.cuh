@@ -54,7 +54,6 @@ struct Params {
     int B, k, rpr, is_tree;
     int block;                   // chains: block verification instead of token-by-token
     int64_t V;
-    double v_inv;                // 1 / V, for quick exact division by V
     float cs;                    // log2(e) / T: p is proportional to 2^(logit * cs)
     const float *temps;          // [B] per-request temperatures (0: greedy request), or null
     const int32_t *top_k;        // [B] per-request top-k (<= 0 or >= V: off), or null
@@ -144,15 +143,6 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// floor(x / P.V) for 0 <= x < 2^52: a double-precision estimate, then an exact correction.
-__device__ __forceinline__ int64_t div_v(int64_t x, int64_t V, double v_inv)
-{
-    int64_t q = (int64_t)((double)x * v_inv);
-    if (q * V > x) --q;
-    else if ((q + 1) * V <= x) ++q;
-    return q;
 }
 
 // 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned), in the thread's
