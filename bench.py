@@ -14,6 +14,7 @@ communication.  --impl reference times the CPU oracle on the same workload (rank
 from __future__ import annotations
 
 import argparse
+import contextlib
 import ctypes
 import hashlib
 import json
@@ -51,6 +52,22 @@ def kernel_source_hash() -> str:
     for p in KERNEL_SOURCES:
         h.update(open(p, "rb").read())
     return h.hexdigest()[:16]
+
+
+@contextlib.contextmanager
+def nvtx_range(torch, name):
+    """A named NVTX range around a phase of the bench (seen by Nsight tools; a no-op without one)."""
+    pushed = False
+    try:
+        torch.cuda.nvtx.range_push(name)
+        pushed = True
+    except Exception:
+        pass
+    try:
+        yield
+    finally:
+        if pushed:
+            torch.cuda.nvtx.range_pop()
 
 
 def parse_args():
@@ -328,9 +345,10 @@ def run_ours(args, D: Dist):
         if rc != 0:
             raise RuntimeError(f"spec_verify_rejection returned {rc}")
 
-    for w in range(args.warmup):
-        call(w, off0 + w)
-    torch.cuda.synchronize()
+    with nvtx_range(torch, "warmup"):
+        for w in range(args.warmup):
+            call(w, off0 + w)
+        torch.cuda.synchronize()
 
     # The timed region is exactly K calls (the input sets rotate, each call has its own Philox
     # offset), replayed from CUDA graphs so that host launches do not pace the GPU: one graph of
@@ -355,20 +373,21 @@ def run_ours(args, D: Dist):
     D.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    if nfull == 1 and tail is None:
-        main.replay()
-        torch.cuda.synchronize()
-        total_ms = main.last_ms()
-    else:
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record()
-        for _ in range(nfull):
+    with nvtx_range(torch, "timed region"):
+        if nfull == 1 and tail is None:
             main.replay()
-        if tail is not None:
-            tail.replay()
-        s1.record()
-        torch.cuda.synchronize()
-        total_ms = s0.elapsed_time(s1)
+            torch.cuda.synchronize()
+            total_ms = main.last_ms()
+        else:
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            for _ in range(nfull):
+                main.replay()
+            if tail is not None:
+                tail.replay()
+            s1.record()
+            torch.cuda.synchronize()
+            total_ms = s0.elapsed_time(s1)
     t1 = time.time()
     D.barrier()
     clocks.stop()
@@ -376,10 +395,11 @@ def run_ours(args, D: Dist):
     max_total_ms = D.max(total_ms, dev)
     # The spread, outside the timed region: per-call time over further replays of the graph.
     per_call = []
-    for _ in range(SPREAD_REPLAYS):
-        main.replay()
-        torch.cuda.synchronize()
-        per_call.append(main.last_ms() / main.n)
+    with nvtx_range(torch, "spread replays"):
+        for _ in range(SPREAD_REPLAYS):
+            main.replay()
+            torch.cuda.synchronize()
+            per_call.append(main.last_ms() / main.n)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the benchmark")
 
@@ -431,14 +451,17 @@ def run_ours(args, D: Dist):
     # End to end through the same C ABI with host buffers: H2D of the step's inputs from pinned
     # memory, the call, D2H of its outputs, every step.
     if not args.no_e2e:
-        line["e2e"] = run_e2e(args, D, torch, sv, lib, sets, ws, ws_bytes, status, stream, sh, off0)
+        with nvtx_range(torch, "end to end"):
+            line["e2e"] = run_e2e(args, D, torch, sv, lib, sets, ws, ws_bytes, status, stream, sh, off0)
 
     if D.rank == 0:
-        line["acceptance"] = acceptance_stats(lib, sv, torch, sets[0], ws, ws_bytes, off0 + 12345)
+        with nvtx_range(torch, "acceptance"):
+            line["acceptance"] = acceptance_stats(lib, sv, torch, sets[0], ws, ws_bytes, off0 + 12345)
     if D.rank == 0 and D.world == 1 and args.cpu_seconds > 0:
         line["cpu_baseline"] = cpu_baseline(sets[0][0], args.cpu_seconds)
     if not args.no_modes:
-        line["modes"] = other_modes(args, D, torch, sv, wl, dev, stream, peak)
+        with nvtx_range(torch, "other modes"):
+            line["modes"] = other_modes(args, D, torch, sv, wl, dev, stream, peak)
     D.close()
     if D.rank == 0:
         print(json.dumps(line), flush=True)
