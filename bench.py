@@ -939,8 +939,8 @@ def _sweep_modes(torch, sv, wl, dev, lib, P, cur, check, status, peak):
 
 def _variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, peak):
     """Verify variants on the headline workload: a temperature per request (every other request
-    greedy, the rest sampling at T in [0.6, 1.4]), relaxed thresholds (0.5, 0.5), and top-k 50 with
-    top-p 0.9 on every request."""
+    greedy, the rest sampling at T in [0.6, 1.4]), relaxed thresholds (0.5, 0.5), top-k 50 with
+    top-p 0.9 on every request, and top-p 0.9 alone."""
     import ctypes as ct
 
     res = {}
@@ -953,7 +953,8 @@ def _variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, pe
     top_p = torch.full((B,), 0.9, dtype=torch.float32, device=dev)
     opts = {"mixed_temperatures_b64k7": sv.Options(temps.data_ptr(), 1.0, 1.0, 1.0, None, None),
             "relaxed_thresholds_b64k7": sv.Options(None, 1.0, 0.5, 0.5, None, None),
-            "top_k50_top_p0.9_b64k7": sv.Options(None, 1.0, 1.0, 1.0, top_k.data_ptr(), top_p.data_ptr())}
+            "top_k50_top_p0.9_b64k7": sv.Options(None, 1.0, 1.0, 1.0, top_k.data_ptr(), top_p.data_ptr()),
+            "top_p0.9_b64k7": sv.Options(None, 1.0, 1.0, 1.0, None, top_p.data_ptr())}
     for name, opt in opts.items():
         def call(i, opt=opt):
             x = sets[i % N_SETS]
@@ -962,9 +963,10 @@ def _variant_modes(torch, sv, wl, dev, lib, P, cur, check, status, out, alen, pe
                                                P(status), cur()), "spec_verify_rejection_ex")
 
         ms = graph_time_ms(torch, [lambda i=i: call(i) for i in range(GRAPH_CALLS)], 20)
-        launches = 4 if name.startswith("top_k") else 2
+        launches = 4 if name.startswith("top_") else 2
         res[name] = _mode_entry(ms, B * (K_DRAFTS + 1), chain_bytes(B, K_DRAFTS, V, 2), peak, launches,
-                                note="the threshold kernel reads each row several times" if launches == 3 else None)
+                                note=("thresholds first: the one-read ring kernel, then the general kernel for the "
+                                      "rows it leaves (top-p alone: all of them)") if launches == 4 else None)
     return res
 
 

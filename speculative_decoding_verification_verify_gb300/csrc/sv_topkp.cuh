@@ -112,7 +112,8 @@ struct TopkpSmem {
         unsigned long long wmass[TK_WARPS][TK_BINS];  // fixed point (see fixed_term)
     };
     float wmax[NT_TK / 32];
-    int sel;           // chosen digit
+    unsigned long long wz[TK_WARPS];  // per-warp sums of the fine top-p pass
+    int sel;           // chosen digit (the fine top-p pass: the chosen key's distance from the maximum's)
     int above_cnt;     // count in bins above it
     double above_mass; // mass in bins above it
 };
@@ -174,13 +175,14 @@ __device__ __forceinline__ void walk_bins(TopkpSmem &S, int nb, bool by_mass, in
 }
 
 // Visit the keys of a row (row = column 0, rowflat its flat index, mis the logits base's
-// misalignment in elements): the 16-byte aligned body with vector loads, the head and tail
-// element by element.  f(key) is called once per visited element.  With MAX, vmx takes the
-// largest logit of every element (NaN if one is NaN).  With SKIP, a vector whose largest logit is
-// below fl (a value, not NaN) is not visited: none of its keys can reach the key of fl.
-template <typename T, bool MAX, bool SKIP, typename F>
-__device__ __forceinline__ void for_each_key(const void *row, int64_t rowflat, int64_t V, int mis, float fl,
-                                             float &vmx, F f)
+// misalignment in elements): the 16-byte aligned body with vector loads, UNR of them in flight a
+// thread, the head and tail element by element.  f(key) is called for each element of the head
+// and tail, g(keys) once for each visited vector of the body.  With MAX, vmx takes the largest
+// logit of every element (NaN if one is NaN).  With SKIP, a vector whose largest logit is below
+// fl (a value, not NaN) is not visited: none of its keys can reach the key of fl.
+template <typename T, bool MAX, bool SKIP, int UNR, typename F, typename G>
+__device__ __forceinline__ void for_each_vec(const void *row, int64_t rowflat, int64_t V, int mis, float fl,
+                                             float &vmx, F f, G g)
 {
     constexpr int VEC = KeyOf<T>::VEC;
     const int64_t a0 = min((int64_t)((VEC - (rowflat + mis) % VEC) % VEC), V);
@@ -193,17 +195,17 @@ __device__ __forceinline__ void for_each_key(const void *row, int64_t rowflat, i
     };
     for (int64_t c = threadIdx.x; c < a0; c += NT_TK) one(c);
     for (int64_t c = a1 + threadIdx.x; c < V; c += NT_TK) one(c);
-    // TK_UNROLL vectors per thread in flight: a pass is bound by the loads' latency otherwise.
+    // UNR vectors per thread in flight: a pass is bound by the loads' latency otherwise.
     const uint4 *vp = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(row) + a0);
-    for (int64_t i0 = threadIdx.x; i0 < nv; i0 += (int64_t)TK_UNROLL * NT_TK) {
-        uint4 w[TK_UNROLL];
+    for (int64_t i0 = threadIdx.x; i0 < nv; i0 += (int64_t)UNR * NT_TK) {
+        uint4 w[UNR];
 #pragma unroll
-        for (int u = 0; u < TK_UNROLL; ++u) {
+        for (int u = 0; u < UNR; ++u) {
             const int64_t i = i0 + (int64_t)u * NT_TK;
             if (i < nv) w[u] = ldg_stream(vp + i);
         }
 #pragma unroll
-        for (int u = 0; u < TK_UNROLL; ++u) {
+        for (int u = 0; u < UNR; ++u) {
             if (i0 + (int64_t)u * NT_TK >= nv) break;
             if (MAX || SKIP) {
                 const float m = Elt<T>::vmax(w[u]);
@@ -212,18 +214,29 @@ __device__ __forceinline__ void for_each_key(const void *row, int64_t rowflat, i
             }
             uint32_t k[VEC];
             KeyOf<T>::keys(w[u], k);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) f(k[e]);
+            g(k);
         }
     }
 }
 
-// A term t in [0, 1] as an integer in units of 2^-shift, rounded down (an error below 2^-shift):
-// the bit pattern's mantissa shifted by its exponent, integer operations only.
+// The same visit with f called for every element, TK_UNROLL vectors in flight.
+template <typename T, bool MAX, bool SKIP, typename F>
+__device__ __forceinline__ void for_each_key(const void *row, int64_t rowflat, int64_t V, int mis, float fl,
+                                             float &vmx, F f)
+{
+    constexpr int VEC = KeyOf<T>::VEC;
+    for_each_vec<T, MAX, SKIP, TK_UNROLL>(row, rowflat, V, mis, fl, vmx, f, [&](const uint32_t (&k)[VEC]) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f(k[e]);
+    });
+}
+
+// A term t >= 0 as an integer in units of 2^-shift, rounded down (an error below 2^-shift), for
+// t 2^shift < 2^62: the bit pattern's mantissa shifted by its exponent, integer operations only.
 __device__ __forceinline__ unsigned long long fixed_term(float t, int shift)
 {
     const uint32_t u = __float_as_uint(t);
-    const int ex = (int)(u >> 23) - 127;  // t = 1.m * 2^ex, ex <= 0
+    const int ex = (int)(u >> 23) - 127;  // t = 1.m * 2^ex
     if (!(t > 0.f) || ex + shift < 0) return 0ull;
     const unsigned long long m = (u & 0x7fffffu) | 0x800000u;
     const int s = ex + shift - 23;
@@ -287,6 +300,126 @@ __device__ void key_histogram(const void *row, int64_t rowflat, int64_t V, int m
     __syncthreads();
 }
 
+// Keys of a 16-bit row the fine top-p pass can cover: one 64-bit mass bin each, in the space of
+// the per-warp histograms.
+constexpr int TK_FINE = TK_WARPS * TK_BINS;
+
+// Top-p over the keys >= kkey of a row of 16-bit logits, in one histogram at full key resolution.
+// Z = the set's mass in fixed point: zin when the caller's first pass summed it (top-p alone),
+// else summed here.  Every key below
+// x0 = mx + log2(Z (1 - p) / (2 V)) / cs weighs at most 2^((x0 - mx) cs), so all of them together
+// hold at most half of the (1 - p) Z that lies outside the top-p set: the threshold is at least
+// x0, and the walk from the top over the keys in [x0, mx] reaches p Z exactly where the walk over
+// the whole row would.  One count per key there (32-bit shared-memory atomics spread over up to
+// TK_FINE keys, where the top digit's 256 bins put a flat row's logits in a handful; a key's mass
+// is its count times its term); false, with the shared state free for the digit passes, when
+// that span is wider than TK_FINE.  pkey: the key of the threshold.
+template <typename T>
+__device__ __noinline__ bool topp_fine(const void *row, int64_t rowflat, int64_t V, int mis, uint32_t kkey, float mx, float cs,
+                          float pp, unsigned long long zin, TopkpSmem &S, uint32_t &pkey)
+{
+    static_assert(sizeof(T) == 2, "16-bit keys");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int fsh = mass_shift(V);
+    const uint32_t ninf_key = KeyOf<T>::key_of_bits(0xff80u);
+    float vmx = NEG_INF;
+    constexpr int VEC = KeyOf<T>::VEC;
+    constexpr int UNR = 4;  // vectors in flight a thread: these passes carry little state
+    auto term = [&](uint32_t k) { return ex2((KeyOf<T>::value(k) - mx) * cs); };
+    // Z over the set (keys >= kkey; vectors below kkey's value skipped when kkey lies above -inf):
+    // a vector's terms summed in fp32, then added in fixed point (an error below 2^-45 a vector).
+    unsigned long long z = 0ull;
+    auto z1 = [&](uint32_t k) {
+        if (k >= kkey) z += fixed_term(term(k), fsh);
+    };
+    auto zv = [&](const uint32_t (&k)[VEC]) {
+        float t = 0.f;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) t += k[e] >= kkey ? term(k[e]) : 0.f;
+        z += fixed_term(t, fsh);
+    };
+    unsigned long long Z = zin;
+    if (Z == 0ull) {  // not summed by the caller's first pass
+        if (kkey > ninf_key) for_each_vec<T, false, true, UNR>(row, rowflat, V, mis, KeyOf<T>::value(kkey), vmx, z1, zv);
+        else for_each_vec<T, false, false, UNR>(row, rowflat, V, mis, 0.f, vmx, z1, zv);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        if (lane == 0) S.wz[warp] = z;
+        __syncthreads();
+        for (int w = 0; w < TK_WARPS; ++w) Z += S.wz[w];
+    }
+    // The floor: x0's key rounded down, within [kkey, the maximum's key].
+    const uint32_t mxkey = KeyOf<T>::key_of_bits(__float_as_uint(mx) >> 16);
+    const float lg = log2f((float)Z) - (float)fsh + log2f(0.5f * (1.f - pp)) - log2f((float)V);
+    const float x0 = mx + lg / cs;
+    uint32_t fk = ninf_key;
+    if (x0 > NEG_INF) {
+        fk = KeyOf<T>::key_of_bits(__float_as_uint(x0) >> 16);  // the low bits cut: toward zero
+        if (KeyOf<T>::value(fk) > x0) --fk;
+    }
+    fk = min(max(fk, kkey), mxkey);
+    const int span = (int)(mxkey - fk) + 1;
+    if (span > TK_FINE) {
+        __syncthreads();  // S.wz read by every thread before the digit passes reuse S
+        return false;
+    }
+    // One count per key of [fk, mxkey], bin 0 the maximum's; a key's mass is its count times its
+    // term, formed once a bin in the walk.
+    int *cnt = &S.wcnt[0][0];
+    for (int i = tid; i < span; i += NT_TK) cnt[i] = 0;
+    if (tid == 0) S.sel = 0x7fffffff;
+    __syncthreads();
+    auto h1 = [&](uint32_t k) {
+        if (k >= fk && k <= mxkey) atomicAdd(&cnt[mxkey - k], 1);
+    };
+    auto hv = [&](const uint32_t (&k)[VEC]) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) h1(k[e]);
+    };
+    if (fk > ninf_key) for_each_vec<T, false, true, UNR>(row, rowflat, V, mis, KeyOf<T>::value(fk), vmx, h1, hv);
+    else for_each_vec<T, false, false, UNR>(row, rowflat, V, mis, 0.f, vmx, h1, hv);
+    __syncthreads();
+    // The walk: the first key from the top whose bin is not empty and whose running mass reaches
+    // ceil(p Z).  Thread t holds bins [8t, 8t + 8); an exclusive block scan of their sums.
+    constexpr int PT = TK_FINE / NT_TK;
+    const double tgt = (double)pp * (double)Z;  // one fp64 product a row
+    const unsigned long long target = tgt <= 0.0 ? 0ull : (unsigned long long)ceil(tgt);
+    unsigned long long bm[PT];
+    unsigned long long own = 0ull;
+#pragma unroll
+    for (int e = 0; e < PT; ++e) {
+        const int i = PT * tid + e;
+        const int c = i < span ? cnt[i] : 0;
+        bm[e] = c > 0 ? (unsigned long long)c * fixed_term(term(mxkey - (uint32_t)i), fsh) : 0ull;
+        own += bm[e];
+    }
+    unsigned long long incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    __syncthreads();  // every thread has read S.wz above
+    if (lane == 31) S.wz[warp] = incl;
+    __syncthreads();
+    unsigned long long run = incl - own;
+    for (int w = 0; w < warp; ++w) run += S.wz[w];
+#pragma unroll
+    for (int e = 0; e < PT; ++e) {
+        run += bm[e];
+        if (bm[e] > 0ull && run >= target) {
+            atomicMin(&S.sel, PT * tid + e);
+            break;
+        }
+    }
+    __syncthreads();
+    const int sel = S.sel;
+    __syncthreads();  // S.sel read before the caller's next use of S
+    if (sel == 0x7fffffff) return false;  // not reached (cannot happen by the bound; the digit passes decide)
+    pkey = mxkey - (uint32_t)sel;
+    return true;
+}
+
 // The threshold of row r: thr[r] = the row's logit threshold, or -inf when the row is not
 // filtered (top-k off and top-p off, or a greedy request).
 template <typename T>
@@ -311,8 +444,50 @@ __device__ void topkp_row(const Params &P, int64_t r, TopkpSmem &S)
     constexpr int LV = KeyOf<T>::LEVELS;
     // First pass: the row's largest logit (the masses' reference; NaN if the row holds one) and
     // the top digit's counts, which top-k needs first.
-    float mx;
-    key_histogram<T, false, true>(row, rowflat, V, P.mis, 0u, 0, 0u, 0.f, cs, S, &mx);
+    float mx = NEG_INF;
+    // Top-p alone: the maximum, and for 16-bit logits the row's mass in the same read, summed
+    // against this thread's running maximum mrun (rescaled when it grows; each vector's terms
+    // summed in fp32, the vector sums added with compensation), so the fine pass needs no pass of
+    // its own for Z (relative error about 1e-7, far inside the 1e-6 at which top-p boundaries are
+    // told apart).
+    constexpr bool FUSE = sizeof(T) == 2;
+    float zrun = 0.f, zc = 0.f, mrun = NEG_INF;
+    auto zadd = [&](float t) {
+        const float y = t - zc, u = zrun + y;
+        zc = (u - zrun) - y;
+        zrun = u;
+    };
+    auto rebase = [&]() {  // mx: this thread's maximum so far, this vector's included
+        if (mx > mrun) {
+            const float f = mrun > NEG_INF ? ex2((mrun - mx) * cs) : 0.f;
+            zrun *= f;
+            zc *= f;
+            mrun = mx;
+        }
+    };
+    if (use_k) {
+        key_histogram<T, false, true>(row, rowflat, V, P.mis, 0u, 0, 0u, 0.f, cs, S, &mx);
+    } else if (FUSE && use_p) {
+        for_each_vec<T, true, false, 4>(
+            row, rowflat, V, P.mis, 0.f, mx,
+            [&](uint32_t k) {
+                rebase();
+                if (mrun > NEG_INF) zadd(ex2((KeyOf<T>::value(k) - mrun) * cs));
+            },
+            [&](const uint32_t (&k)[KeyOf<T>::VEC]) {
+                rebase();
+                if (mrun > NEG_INF) {
+                    float t = 0.f;
+#pragma unroll
+                    for (int e = 0; e < KeyOf<T>::VEC; ++e) t += ex2((KeyOf<T>::value(k[e]) - mrun) * cs);
+                    zadd(t);
+                }
+            });
+    } else {
+        for_each_vec<T, true, false, 4>(row, rowflat, V, P.mis, 0.f, mx, [](uint32_t) {},  // the maximum only
+                                        [](const uint32_t (&)[KeyOf<T>::VEC]) {});
+    }
+    const float mine = mx;  // this thread's maximum (mrun, when the mass was summed)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) S.wmax[warp] = mx;
@@ -323,6 +498,18 @@ __device__ void topkp_row(const Params &P, int64_t r, TopkpSmem &S)
     if (!(mx > NEG_INF) || mx != mx || mx == POS_INF) {  // the streaming pass flags such rows
         if (tid == 0) P.thr[r] = NEG_INF;
         return;
+    }
+    // The fused pass's Z in fixed point: each thread's sum moved to the row maximum.
+    unsigned long long zpre = 0ull;
+    if (FUSE && !use_k && use_p) {
+        const float zt = mine > NEG_INF ? (zrun - zc) * ex2((mine - mx) * cs) : 0.f;
+        unsigned long long z = fixed_term(zt, mass_shift(V));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        if (lane == 0) S.wz[warp] = z;
+        __syncthreads();
+        for (int w = 0; w < TK_WARPS; ++w) zpre += S.wz[w];
+        __syncthreads();
     }
     // Top-k: the key of the k-th largest logit (counts only; the top digit's are in S already).
     uint32_t kkey = 0u;
@@ -340,7 +527,11 @@ __device__ void topkp_row(const Params &P, int64_t r, TopkpSmem &S)
         kkey = prefix;
     }
     uint32_t pkey = kkey;
-    if (use_p) {
+    bool fine = false;
+    if constexpr (sizeof(T) == 2) {
+        if (use_p) fine = topp_fine<T>(row, rowflat, V, P.mis, kkey, mx, cs, pp, zpre, S, pkey);
+    }
+    if (use_p && !fine) {
         // Top-p within the top-k set: the fewest value levels from the top holding top_p of its
         // mass; the top digit's mass histogram over the set also gives the set's total.
         double target = 0.0;
