@@ -87,3 +87,40 @@ def test_printed_toy_on_the_gpu():
         cost = cm["draft_seconds"] + np.array(step)
         ref = run(conf, cost)
         assert ref["budget"] == g["printed"][str(batch)]["budget"]
+
+
+@pytest.mark.parametrize("B,K", [(2049, 1), (683, 6), (1, 64), (2, 64), (4095, 4)])
+def test_budget_slot_counts_across_cta_slices(B, K):
+    """Slot counts just past the planner's 2048-slot CTA slices, and the longest drafts."""
+    rng = np.random.default_rng(B * 7 + K)
+    conf = rng.beta(3, 1, (B, K)).astype(np.float32)
+    for kind in ("roofline", "random"):
+        run(conf, _cost(B, K, rng, kind))
+        run(conf, _cost(B, K, rng, kind), rng.integers(0, K + 1, B))
+
+
+def test_budget_costs_over_a_wide_exponent_range():
+    """Costs from 1e-200 to 1e200: the rates' binary exponents span most of fp64's range."""
+    rng = np.random.default_rng(11)
+    for B, K in ((64, 7), (700, 5)):
+        conf = rng.beta(3, 1, (B, K)).astype(np.float32)
+        run(conf, 10.0 ** rng.uniform(-200, 200, B * K + 1))
+        run(conf, 10.0 ** rng.uniform(-5, 5, B * K + 1) * 1e-150)
+
+
+def test_budget_exact_rate_ties_take_the_first_budget():
+    """Every budget at exactly the same rate, a power of two, which the planner's rate keys carry
+    exactly: the first maximum, budget 0, admitting nothing.  (The oracle flags such calls as
+    boundary cases; the rule itself fixes the answer.  Tied rates whose quotient is not exact in
+    the keys' arithmetic may come out in either order, as for any two rates within 2^-44.)"""
+    for B, K in ((5, 3), (512, 7), (2048, 8)):
+        conf = np.ones((B, K), np.float32)  # survivals 1: gain[b] = b exactly
+        for scale in (1.0, 4.0, 0.125):
+            cost = scale * (B + np.arange(B * K + 1, dtype=np.float64))
+            c = torch.from_numpy(conf).to(DEV)
+            k = torch.from_numpy(cost).to(DEV)
+            adm, bud, rate = sv.spec_verify_plan_budget(c, k, None)
+            torch.cuda.synchronize()
+            assert int(bud.item()) == 0
+            assert not adm.cpu().numpy().any()
+            assert float(rate.item()) == pytest.approx(1.0 / scale, rel=1e-12)
