@@ -193,8 +193,10 @@ int spec_verify_tree(const void *logits, int dtype, const int32_t *node_tokens,
  *                   whole; k <= 0 or k >= V: off); top-p then keeps the fewest whole value levels
  *                   from the top whose probability, renormalised over the top-k set, reaches top_p
  *                   (>= 1: off; <= 0 keeps the top level).  p is renormalised over what is kept;
- *                   greedy requests are unaffected.  An extra kernel finds each row's logit
- *                   threshold first (a few passes over the row).
+ *                   greedy requests are unaffected.  Two extra kernels find each row's logit
+ *                   threshold first: one that reads each bf16 row once (top-k <= 256), then a
+ *                   general one for the rows it leaves (top-p alone, larger k, fp32 logits; two
+ *                   to five passes over a row).
  */
 typedef struct spec_verify_options {
     const float *temperatures;
