@@ -276,15 +276,14 @@ __device__ __forceinline__ void local_sort(uint32_t *loc, uint32_t *tmp, int tid
     }
     tmp[2 * tid] = v0;
     tmp[2 * tid + 1] = v1;
-    const uint32_t *src = tmp;
-    uint32_t *dst = loc;
+    uint32_t *src = tmp, *dst = loc;
     for (int w = 64; w < PER; w <<= 1) {  // five rounds: tmp -> loc -> tmp -> loc -> tmp -> loc
         __syncthreads();
         const int base = (2 * tid) & ~(2 * w - 1);
         merge_two(src + base, w, src + base + w, w, 2 * tid - base, dst + base);
-        const uint32_t *t = src;
+        uint32_t *t = src;
         src = dst;
-        dst = const_cast<uint32_t *>(t);
+        dst = t;
     }
     __syncthreads();
 }
