@@ -1,6 +1,11 @@
 """Pins of the oracle's adaptive verification budget: the worked example the pages print (budgets
 112 / 57 / 7 and their throughputs), brute force over every prefix-closed admission on tiny
-inputs, and the tie and range rules."""
+inputs, and the tie and range rules.
+
+Planting each of these mistakes in a copy of the oracle fails at least one pin: later positions
+first on equal survivals, the higher request first on equal survivals, the last maximum for the
+first, the rate without B, cost[b - 1] for cost[b], confidences not multiplied along the drafts,
+num_drafts ignored, confidences not clamped to [0, 1], the slots taken worst first."""
 import itertools
 import json
 import os
@@ -79,6 +84,13 @@ def test_ties_prefer_earlier_positions_and_ragged_requests(oracle):
     assert r["admitted"].tolist() == [0]
     r = oracle.plan_budget(np.array([[2.0, 0.5]], np.float32), np.array([1.0, 1.0, 1.0]))
     assert r["admitted"].tolist() == [2]
+    # The clamp decides: read as 1, the survivals [1, .5] make budget 1 best (2 / 1 against
+    # 2.5 / 1.3); unclamped, [2, 1] would make it budget 2 (4 / 1.3 against 3 / 1).
+    r = oracle.plan_budget(np.array([[2.0, 0.5]], np.float32), np.array([1.0, 1.0, 1.3]))
+    assert r["budget"] == 1 and r["admitted"].tolist() == [1] and r["rate"] == pytest.approx(2.0)
+    # Equal survivals at the same position of two requests: the lower request is admitted first.
+    r = oracle.plan_budget(np.array([[0.5], [0.5]], np.float32), np.array([1.0, 0.5, 10.0]))
+    assert r["budget"] == 1 and r["admitted"].tolist() == [1, 0]
 
 
 def test_zero_gain_keeps_the_smaller_budget(oracle):

@@ -1,7 +1,14 @@
 """Pins of the oracle's top-k / top-p filter on p (the target distribution after temperature,
 top-k and top-p): the off settings leave softmax unchanged; top-k and top-p keep what their
 definitions keep, checked by brute force over prefixes of the sorted vocabulary; ties at a
-boundary are kept whole; and a verification with filtered p emits the filtered distribution."""
+boundary are kept whole; and a verification with filtered p emits the filtered distribution.
+
+Planting each of these mistakes in a copy of the oracle's filter fails at least one pin: the
+(k+1)-th largest logit for the k-th, the top-p mass taken over the whole row instead of the top-k
+set, one level kept past the crossing, the level before the crossing as the last one kept, the
+boundary level dropped, p not renormalised.  A strict crossing (cum > target for cum >= target)
+is not caught: it differs only where a level's running mass equals the target exactly, and the
+oracle flags every request within 1e-6 of that as a boundary case."""
 import numpy as np
 import pytest
 from scipy.special import softmax
