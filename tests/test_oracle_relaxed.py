@@ -2,8 +2,16 @@
 
 The relaxed rule is pinned by the worked example the pages print for it (acceptance 1.0, total
 variation 0.35 on the six-token toy) and by closed forms for one candidate; thresholds of 1 must
-reduce to the exact rule.  The per-request temperature dispatch is pinned by the argmax-prefix
-rule computed here from numpy argmax, and by the single-temperature oracle on each request."""
+reduce to the exact rule; a tree level with several candidates (one at or above
+threshold_single, one of probability 0) matches its closed form.  The per-request temperature
+dispatch is pinned by the argmax-prefix rule computed here from numpy argmax, and by the
+single-temperature oracle on each request.
+
+Planting each of these mistakes in a copy of the oracle fails at least one pin: p(x) times
+threshold_acc for p(x) / threshold_acc, threshold_single ignored (chain and tree), a candidate's
+own p for the running sum, threshold_acc ignored in trees, a running sum carried into a level.
+Dropping the p > 0 guard of an acceptance is not caught and cannot be: with thresholds in (0, 1]
+a candidate of probability 0 meets neither condition on a coin that an earlier one left."""
 import json
 import os
 
@@ -69,6 +77,48 @@ def test_relaxed_single_candidate_closed_form(oracle, thr_single, thr_acc):
                               np.array([0.9999, 0.5]), np.array([0.3, 0.5]), thr_single, thr_acc)
         if r["accept_len"] == 0:
             assert r["tokens"][0] != x
+
+
+def _relaxed_level(p, children, ts, ta):
+    """One tree level under the relaxed rule, in closed form: children are tried in order, child
+    j (p_j > 0) accepting a coin below S_j / ta (S_j the running sum of the tried children's p)
+    or any coin when p_j >= ts; the first acceptance wins.  Returns the first token's law."""
+    dist = np.zeros_like(p)
+    prev, S = 0.0, 0.0
+    for t in children:
+        S += p[t]
+        if p[t] <= 0.0:
+            continue
+        hi = 1.0 if p[t] >= ts else min(1.0, S / ta)
+        dist[t] += max(0.0, hi - prev)
+        prev = max(prev, hi)
+    rest = np.ones_like(p, dtype=bool)
+    rest[list(children)] = False
+    if rest.any() and p[rest].sum() > 0:
+        dist[rest] = (1.0 - prev) * p[rest] / p[rest].sum()
+    return dist, prev
+
+
+@pytest.mark.parametrize("ts,ta", [(0.25, 1.0), (0.4, 0.8), (1.0, 0.6), (0.2, 0.3)])
+def test_relaxed_tree_level_closed_form(oracle, ts, ta):
+    """Several candidates, one of them at or above threshold_single, one of probability 0: the
+    grid-integrated first token matches the closed form above."""
+    rng = np.random.default_rng(3)
+    for _ in range(5):
+        V = 7
+        p = rng.dirichlet(np.ones(V))
+        p[4] = 0.0
+        if ts < 1.0:  # child 2 at threshold_single + 0.05, the rest scaled around it
+            others = np.arange(V) != 2
+            p[others] *= (1.0 - (ts + 0.05)) / p[others].sum()
+            p[2] = ts + 0.05
+        p /= p.sum()
+        assert ts >= 1.0 or p[2] >= ts
+        children = [0, 4, 2, 5]
+        dist, acc = oracle.grid_tree_first_token(p, children, G, ts, ta)
+        want, wacc = _relaxed_level(p, children, ts, ta)
+        assert acc == pytest.approx(wacc, abs=2.0 / G)
+        np.testing.assert_allclose(dist, want, atol=3.0 / G)
 
 
 def _argmax_prefix(lg, d):
