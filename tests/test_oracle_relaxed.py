@@ -9,7 +9,9 @@ single-temperature oracle on each request.
 
 Planting each of these mistakes in a copy of the oracle fails at least one pin: p(x) times
 threshold_acc for p(x) / threshold_acc, threshold_single ignored (chain and tree), a candidate's
-own p for the running sum, threshold_acc ignored in trees, a running sum carried into a level.
+own p for the running sum, threshold_acc ignored in trees, a running sum carried into a level,
+the first request's temperature used for every request, the draft emitted at a greedy stop, a
+greedy request accepting past its first mismatch.
 Dropping the p > 0 guard of an acceptance is not caught and cannot be: with thresholds in (0, 1]
 a candidate of probability 0 meets neither condition on a coin that an earlier one left."""
 import json
